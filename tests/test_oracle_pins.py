@@ -1,0 +1,424 @@
+"""Pins for the CPU oracle: values the pages print, closed forms, invariants
+and brute force — never the oracle's own formula retyped.
+
+Each fixture under tests/golden/ carries its citation in its "source" field.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def frac(s):
+    """Parse "a/b" or a number from a fixture."""
+    if isinstance(s, str) and "/" in s:
+        a, b = s.split("/")
+        return Fraction(int(a), int(b))
+    return Fraction(s)
+
+
+def qdq_rows(mat, bits):
+    """Per-row groups (Value per-token axis) via the unit-level V quantizer."""
+    m = np.asarray(mat, np.float32)
+    T, D = m.shape
+    codes, vmin, vscale = orc.quantize_v_unit(orc.f32_to_bf16_exact(m), D, bits)
+    return orc.dequant_v_unit(codes, vmin, vscale, D, bits)
+
+
+def qdq_cols(mat, bits):
+    """Per-column groups (Key per-channel axis) via the unit-level K quantizer."""
+    m = np.asarray(mat, np.float32)
+    T, D = m.shape
+    codes, kmin, kscale = orc.quantize_k_unit(orc.f32_to_bf16_exact(m), T, bits)
+    return orc.dequant_k_unit(codes, kmin, kscale, T, bits)
+
+
+# ------------------------------------------------------------ KIVI §3 Key
+def test_key_example_per_token_row0():
+    g = golden("kivi_key_4x4.json")
+    row0 = g["key"][0]
+    codes, m, s = orc.quantize_group(row0, g["bits"])
+    assert list(codes) == [3, 0, 0, 0]
+    assert m == -1.0
+    # step is the fp32 rounding of 101/3 (fp32 step reading)
+    assert s == np.float32(101.0) / np.float32(3.0)
+    assert abs(Fraction(float(s)) - frac(g["per_token_row0_step"])) < Fraction(1, 2**19)
+    rec = qdq_rows(g["key"], g["bits"])[0]
+    np.testing.assert_allclose(rec, g["per_token_row0_reconstruction"], rtol=0, atol=1e-5)
+
+
+def test_key_example_per_channel_reconstructs_exactly():
+    g = golden("kivi_key_4x4.json")
+    rec = qdq_cols(g["key"], g["bits"])
+    assert np.array_equal(rec, np.asarray(g["key"], np.float64))
+    for col, grid in zip(range(2), g["per_channel_column_grids"]):
+        codes, m, s = orc.quantize_group([r[col] for r in g["key"]], 2)
+        assert sorted(orc.dequantize_group(np.arange(4), m, s)) == grid
+
+
+def _probs(keys, q):
+    D = len(q)
+    n = len(keys)
+    _, p = orc.attention(q, np.asarray(keys, np.float64), np.zeros((n, D)), p_out=True)
+    return p
+
+
+def test_key_example_attention_decision():
+    g = golden("kivi_key_4x4.json")
+    q = g["query"]
+    p_orig = _probs(g["key"], q)
+    p_tok = _probs(qdq_rows(g["key"], 2), q)
+    p_chan = _probs(qdq_cols(g["key"], 2), q)
+    assert np.array_equal(p_chan, p_orig)
+    assert int(np.argmax(p_orig)) == g["argmax_original"]
+    assert int(np.argmax(p_tok)) == g["argmax_per_token"]
+    assert np.max(np.abs(p_orig - p_tok)) > g["min_prob_change_per_token"]
+
+
+# ---------------------------------------------------------- KIVI §3 Value
+def test_value_example_axes():
+    g = golden("kivi_value_4x4.json")
+    p = np.asarray(g["p"])
+    out_tok = p @ qdq_rows(g["value"], g["bits"])
+    out_col = p @ qdq_cols(g["value"], g["bits"])
+    # codes of the selected row are exact; with an fp32 step the top grid
+    # point m + 3*fl32(1/3) differs from 1 by the step's rounding only
+    codes, m, s = orc.quantize_group(g["value"][1], g["bits"])
+    assert list(codes) == [3, 0, 3, 0] and m == 0.0
+    np.testing.assert_allclose(out_tok, g["per_token_output"], rtol=0, atol=3 * 2.0**-24)
+    target = float(frac(g["per_column_output_each"]))
+    # fp32 step 200/3 carries a relative error below 2^-24
+    np.testing.assert_allclose(out_col, [target] * 4, rtol=1e-6)
+    codes, m, s = orc.quantize_group([r[1] for r in g["value"]], 2)
+    assert abs(Fraction(float(s)) - frac(g["per_column_step"])) < Fraction(1, 2**16)
+
+
+# --------------------------------------------------------------- KIVI §2
+def test_two_bit_grid_has_no_zero():
+    g = golden("kivi_grid_2bit.json")
+    lo, hi = g["range"]
+    codes, m, s = orc.quantize_group([lo, hi], g["bits"])
+    grid = orc.dequantize_group(np.arange(4), m, s)
+    for got, want in zip(grid, g["grid"]):
+        assert abs(got - float(frac(want))) < 1e-7
+    assert not np.any(grid == 0.0)
+
+
+def test_constant_groups_exact():
+    g = golden("kivi_constant_groups.json")
+    for grp in g["groups"]:
+        codes, m, s = orc.quantize_group(grp, g["bits"])
+        assert list(orc.dequantize_group(codes, m, s)) == grp
+        assert list(codes) == [0] * len(grp) and s == 0.0
+
+
+def test_pack2_layout():
+    g = golden("kivi_pack2.json")
+    codes, _, _ = orc.quantize_group([100.0, 101.0, 102.0, 103.0], 2)
+    assert list(codes) == g["codes_first_column"]
+    packed = orc.pack_lsb(codes, 2)
+    assert packed.hex() == g["packed_first_column_hex"]
+    assert list(orc.unpack_lsb(packed, 4, 2)) == g["codes_first_column"]
+    short = orc.pack_lsb(g["short_codes"], 2)
+    assert len(short) == 1
+    assert list(orc.unpack_lsb(short, g["short_length"], 2)) == g["short_codes"]
+    with pytest.raises(ValueError):
+        orc.unpack_lsb(short, 5, 2)
+
+
+def test_four_bit_packing_low_nibble_first():
+    # 4-bit analogue of the LSB-first rule: two codes per byte, first code low.
+    assert orc.pack_lsb([0x3, 0xA, 0xF], 4).hex() == "a30f"
+
+
+def test_round_half_to_even():
+    # step 1 exactly: (x - m)/step lands on the ties 0.5 and 2.5
+    codes, m, s = orc.quantize_group([0.0, 0.5, 2.5, 3.0], 2)
+    assert s == 1.0
+    assert list(codes) == [0, 0, 2, 3]     # half-away-from-zero gives [0,1,3,3]
+
+
+def test_rejects_nonfinite_and_unrepresentable_step():
+    with pytest.raises(orc.OracleError) as e:
+        orc.quantize_group([0.0, float("nan"), 1.0], 2)
+    assert e.value.status == orc.ORC_ERR_NONFINITE
+    with pytest.raises(orc.OracleError) as e:
+        orc.quantize_group([0.0, float("inf")], 2)
+    assert e.value.status == orc.ORC_ERR_NONFINITE
+    big = float(np.finfo(np.float32).max)
+    with pytest.raises(orc.OracleError) as e:
+        orc.quantize_group([-big, big], 2)
+    assert e.value.status == orc.ORC_ERR_RANGE
+
+
+# ---------------------------------------- MixKVQ appendix: error bound, brute force
+@pytest.mark.parametrize("bits", [2, 4])
+def test_error_bound_half_step(bits):
+    g = golden("mixkvq_error_bound.json")
+    rng = np.random.default_rng(7 + bits)
+    for n in (4, 32, 128):
+        for trial in range(50):
+            x = (rng.standard_normal(n) * rng.choice([1e-3, 1.0, 30.0])).astype(np.float32)
+            if trial % 7 == 0:
+                x[rng.integers(n)] *= 40.0                       # an outlier
+            codes, m, s = orc.quantize_group(x, bits)
+            rec = orc.dequantize_group(codes, m, s)
+            # fp32 (x - m) and division each round once: <= (2^b-1)*2^-23 steps
+            slack = (2**bits - 1) * 2.0**-22
+            assert np.all(np.abs(x.astype(np.float64) - rec) <= float(s) * (g["bound_fraction_of_step"] + slack))
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_codes_brute_force_nearest(bits):
+    """Every code is a nearest grid point of the exact (x - m)/step; exact
+    ties (representable without rounding) go to the even code."""
+    rng = np.random.default_rng(100 + bits)
+    top = 2**bits - 1
+    for trial in range(300):
+        n = int(rng.integers(2, 9))
+        x = (rng.integers(-40, 40, n) / rng.choice([1, 2, 4, 8])).astype(np.float32)
+        if trial % 3 == 0:
+            x = rng.standard_normal(n).astype(np.float32)
+        if x.max() == x.min():
+            continue
+        codes, m, s = orc.quantize_group(x, bits)
+        for xi, c in zip(x, codes):
+            y = (Fraction(float(xi)) - Fraction(float(m))) / Fraction(float(s))
+            dists = [abs(y - k) for k in range(top + 1)]
+            best = min(dists)
+            assert dists[int(c)] <= best + Fraction(1, 2**20)
+            if best == Fraction(1, 2) and dists[int(c)] == best and y.denominator == 2:
+                assert int(c) % 2 == 0
+
+
+# ---------------------------------------------------------- attention pins
+def test_global_softmax_example():
+    g = golden("kivi_global_softmax.json")
+    q = [math.sqrt(2.0), 0.0]
+    K = np.array([[0.0, 0.0]] * g["key_quant_rows"] + [[math.log(9.0), 0.0]])
+    V = np.array([[float(t), -float(t)] for t in g["value_rows_first_dim"]])
+    o, p = orc.attention(q, K, V, p_out=True)
+    for got, want in zip(p, g["probabilities"]):
+        assert abs(got - float(frac(want))) < 1e-12
+    assert abs(o[0] - float(frac(g["output_first_dim"]))) < 1e-12
+    assert abs(o[0] - g["output_first_dim_decimal"]) < 1e-6
+    vb = g["value_boundary"]
+    mixed = p[:vb] @ V[:vb] + p[vb:] @ V[vb:]
+    assert np.allclose(mixed, o, atol=1e-12, rtol=0)
+    kb = g["key_boundary"]
+    # normalising the two Key segments separately is the page's wrong answer
+    wrong = orc.attention(q, K[:kb], V[:kb])[0] + orc.attention(q, K[kb:], V[kb:])[0]
+    assert abs(wrong - g["separate_softmax_output_first_dim"]) < 1e-12
+    assert abs(wrong - o[0]) > 1.0
+
+
+def test_attention_brute_force_high_precision():
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 40
+    rng = np.random.default_rng(3)
+    for trial in range(40):
+        n = int(rng.integers(1, 9))
+        D = int(rng.choice([1, 2, 3, 4, 8]))
+        q = rng.standard_normal(D) * 2
+        K = rng.standard_normal((n, D)) * 3
+        V = rng.standard_normal((n, D))
+        o = orc.attention(q, K, V)
+        # softmax without a max shift, 40 significant digits
+        e = [mpmath.e ** (mpmath.fsum(mpmath.mpf(q[d]) * mpmath.mpf(K[t, d]) for d in range(D))
+                          / mpmath.sqrt(D)) for t in range(n)]
+        tot = mpmath.fsum(e)
+        for d in range(D):
+            ref = mpmath.fsum(e[t] * mpmath.mpf(V[t, d]) for t in range(n)) / tot
+            assert abs(o[d] - float(ref)) <= 1e-13 * (1 + abs(float(ref)))
+
+
+def test_output_error_decomposition_identity():
+    """KIVI §1: o^ - o = (p^ - p) V + p^ E_V, with K^ = K + E_K, V^ = V + E_V."""
+    rng = np.random.default_rng(11)
+    n, D = 37, 16
+    q = rng.standard_normal(D)
+    K = rng.standard_normal((n, D))
+    V = rng.standard_normal((n, D))
+    EK = rng.standard_normal((n, D)) * 0.05
+    EV = rng.standard_normal((n, D)) * 0.05
+    o, p = orc.attention(q, K, V, p_out=True)
+    oh, ph = orc.attention(q, K + EK, V + EV, p_out=True)
+    assert np.allclose(oh - o, (ph - p) @ V + ph @ EV, atol=1e-12, rtol=0)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(5)
+    D = 8
+    v = rng.standard_normal((1, D))
+    assert np.allclose(orc.attention(rng.standard_normal(D), rng.standard_normal((1, D)), v), v[0])
+    V = rng.standard_normal((6, D))
+    assert np.allclose(orc.attention(np.zeros(D), rng.standard_normal((6, D)), V), V.mean(0))
+    # shift invariance: adding a constant logit to every row changes nothing
+    q = np.zeros(D); q[0] = 1.0
+    K = rng.standard_normal((6, D))
+    K2 = K.copy(); K2[:, 0] += 5.0
+    assert np.allclose(orc.attention(q, K, V), orc.attention(q, K2, V), atol=1e-12)
+
+
+# ------------------------------------------------------------ state machine
+def test_residual_trace_block_flush():
+    g = golden("kivi_residual_trace.json")
+    R, G, D = g["R"], g["G"], 4
+    cache = orc.OracleCache(1, 1, D, Gk=G, Gv=D, R=R)
+    rng = np.random.default_rng(0)
+    lengths = []
+    for step in range(g["steps"]):
+        kv = orc.f32_to_bf16_exact(rng.integers(-8, 8, (2, 1, 1, D)).astype(np.float32))
+        cache.append(kv[0], kv[1])
+        if cache.r == R:
+            cache.flush()
+        lengths.append(cache.r)
+    assert lengths == g["persisted_key_residual_lengths"]
+    assert [cache.T_q, cache.r] == g["step9_key_split"]
+    with pytest.raises(ValueError):
+        cache.flush()                          # residual not full
+
+
+def test_state_machine_errors_and_prefill_split():
+    D = 8
+    cache = orc.OracleCache(1, 1, D, Gk=4, Gv=8, R=4)
+    rng = np.random.default_rng(1)
+    KV = orc.f32_to_bf16_exact(rng.integers(-8, 8, (2, 1, 1, 10, D)).astype(np.float32))
+    with pytest.raises(ValueError):
+        cache.attention(KV[0][:, :, 0])        # empty cache
+    cache.prefill(KV[0], KV[1])
+    assert (cache.T_q, cache.r) == (8, 2)      # r = 10 mod 4
+    with pytest.raises(ValueError):
+        cache.prefill(KV[0], KV[1])            # not empty
+    for _ in range(2):
+        cache.append(KV[0][:, :, 0], KV[1][:, :, 0])
+    with pytest.raises(ValueError):
+        cache.append(KV[0][:, :, 0], KV[1][:, :, 0])   # full: flush first
+
+
+def test_cache_attention_reduces_to_textbook_without_history():
+    """T_q = 0: attention over the bf16 residual alone is textbook softmax."""
+    rng = np.random.default_rng(2)
+    D, r, Hq = 16, 5, 2
+    cache = orc.OracleCache(1, 1, D, Gk=8, Gv=8, R=8)
+    K = orc.f32_to_bf16_exact(rng.integers(-6, 6, (1, 1, r, D)).astype(np.float32))
+    V = orc.f32_to_bf16_exact(rng.integers(-6, 6, (1, 1, r, D)).astype(np.float32))
+    cache.prefill(K, V)
+    q = orc.f32_to_bf16_exact(rng.integers(-3, 3, (1, Hq, D)).astype(np.float32))
+    out = cache.attention(q)
+    kf = orc.bf16_to_f32(K[0, 0]).astype(np.float64)
+    vf = orc.bf16_to_f32(V[0, 0]).astype(np.float64)
+    for h in range(Hq):
+        s = kf @ orc.bf16_to_f32(q[0, h]).astype(np.float64) / np.sqrt(D)
+        w = np.exp(s - s.max()); w /= w.sum()
+        assert np.allclose(out[0, h], w @ vf, atol=1e-12)
+
+
+def test_canonical_k_layout_channel_codes_along_tokens():
+    """K codes: group g, channel d holds that channel's G codes packed LSB
+    first along tokens (PN-Mix App. G; KIVI §3 packer)."""
+    T, D, G = 8, 3, 4
+    k = np.zeros((T, D), np.float32)
+    k[:, 1] = [0, 1, 2, 3, 3, 2, 1, 0]           # channel 1: codes are the values
+    k[:, 0] = 7.0                                # constant channel
+    k[:, 2] = [0, 3, 0, 3, 1, 1, 1, 4]
+    codes, kmin, kscale = orc.quantize_k_unit(orc.f32_to_bf16_exact(k), G, 2)
+    assert codes.shape == (2, 3, 1)
+    assert codes[0, 1, 0] == 0b11100100 and codes[1, 1, 0] == 0b00011011
+    assert codes[0, 0, 0] == 0 and kscale[0, 0] == 0.0 and orc.bf16_to_f32(kmin[0, 0]) == 7.0
+    assert list(orc.unpack_lsb(bytes(codes[0, 2]), 4, 2)) == [0, 3, 0, 3]
+
+
+# ---------------------------------------------------------------- saliency
+def test_saliency_hand_computed():
+    """MixKVQ: I_d = mean |Q_{i,d}| over the GQA group's heads and the window,
+    S_d = (max - min)/(2^B - 1), A_d = I_d * S_d — on integer inputs whose
+    results are exact."""
+    n_rep, Lq, D = 2, 2, 4
+    Q = np.zeros((n_rep, Lq, D), np.float32)
+    Q[:, :, 0] = [[1, -2], [3, -4]]      # sum |.| 10 -> I 2.5
+    Q[:, :, 1] = [[0, 0], [0, 8]]        # 8 -> 2
+    Q[:, :, 2] = [[-1, -1], [-1, -1]]    # 4 -> 1
+    Q[:, :, 3] = [[2, 2], [2, 2]]        # 8 -> 2
+    I = orc.importance(orc.f32_to_bf16_exact(Q))
+    assert list(I) == [2.5, 2.0, 1.0, 2.0]
+    K = np.zeros((4, D), np.float32)
+    K[:, 0] = [0, 3, 1, 2]               # range 3 -> S 1
+    K[:, 1] = [-6, 0, 0, 0]              # range 6 -> S 2
+    K[:, 2] = [5, 5, 5, 5]               # range 0 -> S 0
+    K[:, 3] = [1, 2, 3, 4]               # range 3 -> S 1
+    S = orc.sensitivity(orc.f32_to_bf16_exact(K), 2)
+    assert list(S) == [1.0, 2.0, 0.0, 1.0]
+    A = orc.salience(I, S)
+    assert list(A) == [2.5, 4.0, 0.0, 2.0]
+    # rank form: one BF16, one UINT4, the rest UINT2
+    assert list(orc.tiers_rank(A, 1, 1)) == [orc.TIER_UINT4, orc.TIER_BF16,
+                                             orc.TIER_UINT2, orc.TIER_UINT2]
+    # threshold form: strict ">" at both thresholds
+    assert list(orc.tiers_threshold(A, 2.5, 2.0)) == [orc.TIER_UINT4, orc.TIER_BF16,
+                                                     orc.TIER_UINT2, orc.TIER_UINT2]
+    assert list(orc.tiers_threshold(A, 2.4, 1.9)) == [orc.TIER_BF16, orc.TIER_BF16,
+                                                     orc.TIER_UINT2, orc.TIER_UINT4]
+
+
+def test_tier_rank_ties_lower_channel_first():
+    A = np.array([1.0, 3.0, 3.0, 1.0, 3.0], np.float32)
+    assert list(orc.tiers_rank(A, 2, 2)) == [orc.TIER_UINT4, orc.TIER_BF16, orc.TIER_BF16,
+                                             orc.TIER_UINT2, orc.TIER_UINT4]
+
+
+def test_mixed_group_storage_and_reconstruction():
+    G, D = 8, 6
+    rng = np.random.default_rng(9)
+    k = np.zeros((G, D), np.float32)
+    k[:, 0] = rng.integers(0, 16, G)          # on a 4-bit grid incl. 0 and 15
+    k[0, 0], k[1, 0] = 0, 15
+    k[:, 1] = rng.standard_normal(G)
+    k[:, 2] = [0, 1, 2, 3, 0, 1, 2, 3]        # on the 2-bit grid
+    k[:, 3] = rng.standard_normal(G) * 9
+    k[:, 4] = rng.standard_normal(G)
+    k[:, 5] = -2.0                            # constant
+    kb = orc.f32_to_bf16_exact(orc.bf16_to_f32(
+        (k.view(np.uint32) >> 16).astype(np.uint16)))      # truncate to bf16 values
+    tiers = np.array([orc.TIER_UINT4, orc.TIER_UINT2, orc.TIER_UINT2,
+                      orc.TIER_BF16, orc.TIER_UINT4, orc.TIER_UINT2], np.uint8)
+    grp = orc.quantize_k_mixed_group(kb, tiers)
+    assert list(grp.perm) == [3, 0, 4, 1, 2, 5]
+    assert np.array_equal(grp.raw[0], kb[:, 3])
+    rec = orc.dequant_k_mixed_group(grp, G)
+    kf = orc.bf16_to_f32(kb).astype(np.float64)
+    assert np.array_equal(rec[:, 3], kf[:, 3])            # BF16 tier verbatim
+    assert np.array_equal(rec[:, 0], kf[:, 0])            # exact 4-bit grid
+    assert np.array_equal(rec[:, 2], kf[:, 2])            # exact 2-bit grid
+    assert np.array_equal(rec[:, 5], kf[:, 5])            # constant channel
+    assert grp.s4[1] == np.float32(np.float32(kf[:, 4].max() - kf[:, 4].min()) / np.float32(15))
+    assert np.all(np.abs(rec[:, 4] - kf[:, 4]) <= grp.s4[1] * (0.5 + 2**-18))
+    assert np.all(np.abs(rec[:, 1] - kf[:, 1]) <= grp.s2[0] * (0.5 + 2**-18))
+
+
+# ---------------------------------------------------------- byte accounting
+def test_byte_formula_example():
+    g = golden("kivi_byte_formula.json")
+    args = dict(T=g["T"], D=g["D"], k_bits=g["b"], v_bits=g["b"], Gk=g["G"], Gv=g["G"],
+                origin_bytes=g["e"], step_bytes=g["e"])
+    total = orc.cache_bytes(rK=g["rK"], rV=g["rV"], float_bytes=g["f"], **args)
+    quant = orc.cache_bytes(rK=g["rK"], rV=g["rV"], float_bytes=0, **args)
+    assert total == g["total_kib"] * 1024
+    assert round(quant / 1024) == g["quantized_kib"]
+    assert total - quant == g["residual_kib"] * 1024
+    assert 2 * g["T"] * g["D"] * g["f"] == g["unquantized_mib"] * 2**20
+    one = orc.cache_bytes(T=g["G"], rK=0, rV=0, D=1, k_bits=g["b"], v_bits=g["b"], Gk=g["G"],
+                          Gv=g["G"], origin_bytes=g["e"], step_bytes=g["e"], float_bytes=g["f"])
+    assert one * 8 / (2 * g["G"]) == g["bits_per_element"]
