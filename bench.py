@@ -1,0 +1,479 @@
+#!/usr/bin/env python3
+"""Quantized-KV decode benchmark (one JSON line on rank 0).
+
+Workload (default): Llama-3.1-8B-shaped GQA decode layer, 32 query / 8 KV
+heads, D = 128, batch 16, 32768 quantized tokens + 100 residual tokens, K and
+V at 2 bits (K per channel over 128-token groups, V per token over 32
+channels), synthetic seeded bf16 inputs with 4 outlier key channels per KV
+head.
+
+A step is one MixKVQ Algorithm 1 decode step through the C ABI: append the
+new token's key/value to the residual, flush (quantize 128 tokens) when the
+residual is full, then the fused split-K decode attention (partial +
+combine).  The quantized history starts below the workload's length by half
+the groups the timed steps will flush, so the mean context over the timed
+region is the workload's.
+
+metric/value: effective HBM GB/s = algorithmic bytes of the steps (packed
+cache 94 B/token/KV head at 2 bits, residual 512 B/token, q and o, append and
+flush traffic) / device time.  The roofline object covers the decode
+attention launch pair (partial + combine) measured with CUDA events on the
+launching stream.  e2e repeats the steps through the same API with q, k_new
+and v_new copied from pinned host memory and the output copied back every
+step.  cpu_baseline times the CPU oracle on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized-KV decode attention: effective HBM GB/s (% of peak), µs/step"
+FALLBACK_HBM_GBS = 6800.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum per decode-attention launch
+# pair from the ncu capture summarized in profiles/, keyed by the sha256 of
+# the decode kernel source it was taken on (a stale entry reports null).
+NCU_TRAFFIC = {}
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1024)
+    p.add_argument("--warmup", type=int, default=8)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="llama8b_gqa_32k_b16")
+    p.add_argument("--batch", type=int, default=0, help="override the batch (profiling)")
+    p.add_argument("--context", type=int, default=0, help="override quantized tokens")
+    p.add_argument("--bits", type=int, default=0, help="override k/v bits")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-bf16", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler(threading.Thread):
+    """Samples SM clock and clock-event reasons through NVML while running."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, period_s=0.002):
+        super().__init__(daemon=True)
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self.ok = False
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            import torch
+            idx = torch.cuda.current_device()
+            ids = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+            if idx < len(ids) and ids[idx].isdigit():
+                idx = int(ids[idx])             # NVML counts physical devices
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def run(self):
+        if not self.ok:
+            return
+        mhz = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        getr = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(mhz.value)
+            if getr(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(self.period)
+
+    def stop(self):
+        self._stop.set()
+        self.join(timeout=1.0)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "samples": len(self.samples),
+                "reasons": [n for b, n in self.REASONS.items() if self.reasons & b]}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("decode.cu", "kvq_internal.h"):
+        with open(os.path.join(ROOT, "bit_kv_cache_kvq_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------ algorithmic bytes
+def bytes_per_token(bits):  # packed K + V, per quantized token per KV head
+    D = 128
+    return (D * bits // 8 + D * 6 // 128) + (D * bits // 8 + (D // 32) * 6)
+
+
+def attention_bytes(w, T_q, r):
+    """Packed cache + bf16 residual + q (bf16) + o (fp32) of one decode
+    attention call."""
+    U = w.B * w.Hkv
+    per_tok = bytes_per_token(w.k_bits) if w.k_bits == w.v_bits else \
+        (128 * w.k_bits // 8 + 6) + (128 * w.v_bits // 8 + 24)
+    return U * (T_q * per_tok + r * 512) + w.B * w.Hq * (256 + 512)
+
+
+def append_bytes(w):
+    return w.B * w.Hkv * 2 * 2 * 256  # read k_new, v_new; write residual slots
+
+
+def flush_bytes(w):
+    U = w.B * w.Hkv
+    per_tok = bytes_per_token(w.k_bits) if w.k_bits == w.v_bits else \
+        (128 * w.k_bits // 8 + 6) + (128 * w.v_bits // 8 + 24)
+    return U * (128 * 512 + 128 * per_tok)
+
+
+# ---------------------------------------------------------------- arms
+def workload_from(args):
+    from bit_kv_cache_kvq_gb300.workloads import WORKLOADS, scaled
+    w = WORKLOADS[args.workload]
+    ch = {}
+    if args.batch:
+        ch["B"] = args.batch
+    if args.context:
+        ch["T_q"] = args.context
+    if args.bits:
+        ch["k_bits"] = ch["v_bits"] = args.bits
+    return scaled(w, **ch) if ch else w
+
+
+def config_of(w, extra=None):
+    c = {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": 128,
+         "quantized_tokens": w.T_q, "residual_tokens": w.r, "k_bits": w.k_bits,
+         "v_bits": w.v_bits, "k_group_tokens": 128, "v_group_channels": 32}
+    if extra:
+        c.update(extra)
+    return c
+
+
+class OracleSample:
+    """A few (batch row, KV head) units of the workload, quantized by the CPU
+    oracle (untimed); time_step() times the oracle's decode attention
+    (dequantize + fp64 attention of the unit's n_rep query heads) on one."""
+
+    def __init__(self, w, n_units):
+        import oracle as orc
+        from bit_kv_cache_kvq_gb300.workloads import bf16_bits, make_kv, make_q, scaled
+        oracle_mod = orc
+        self.one = scaled(w, B=1, Hkv=1, Hq=w.n_rep, k_outliers=min(w.k_outliers, 4))
+        self.units = []
+        for j in range(n_units):
+            u = scaled(self.one, seed=self.one.seed + 17 * j)
+            K, V = make_kv(u)
+            c = oracle_mod.OracleCache(1, 1, 128, u.k_bits, u.v_bits)
+            c.prefill(bf16_bits(K), bf16_bits(V))
+            self.units.append((u, c, [bf16_bits(make_q(u, step=s)) for s in range(4)]))
+        self.calls = 0
+
+    def time_step(self):
+        import numpy as np
+        u, c, qs = self.units[self.calls % len(self.units)]
+        q = qs[(self.calls // len(self.units)) % len(qs)]
+        self.calls += 1
+        t0 = time.perf_counter()
+        out = c.attention(q)
+        sec = time.perf_counter() - t0
+        assert np.all(np.isfinite(out))
+        return attention_bytes(u, c.T_q, c.r), sec
+
+
+def oracle_sample(w, seconds):
+    """(bytes, seconds, calls) of the oracle over about `seconds` of work."""
+    smp = OracleSample(w, 2)
+    nbytes, spent = 0, 0.0
+    while smp.calls == 0 or spent < seconds:
+        nb, sec = smp.time_step()
+        nbytes += nb
+        spent += sec
+    return nbytes, spent, smp.calls
+
+
+def run_reference(args, rank, world):
+    w = workload_from(args)
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    smp = OracleSample(w, 2)
+    nbytes_tot, secs_tot = 0, 0.0
+    for i in range(args.warmup + args.steps):
+        nb, sec = smp.time_step()
+        if i >= args.warmup:
+            nbytes_tot += nb
+            secs_tot += sec
+    gbs = nbytes_tot / secs_tot / 1e9
+    sample = (f"per step: one (batch row, KV head) unit, its {w.n_rep} query heads over "
+              f"{w.T_q} quantized + {w.r} residual tokens (dequantize + fp64 attention)")
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs_tot / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w),
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    return line
+
+
+def run_ours(args, rank, world):
+    import torch
+    import bit_kv_cache_kvq_gb300 as kvq
+    from bit_kv_cache_kvq_gb300 import _build
+    from bit_kv_cache_kvq_gb300.workloads import make_kv, make_q, make_token, scaled
+
+    _build.build()
+    kvq.lib()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w0 = workload_from(args)
+    w = scaled(w0, seed=w0.seed + 100 * rank)     # weak scaling: each rank its own batch
+    K, W = args.steps, args.warmup
+    if W > w.r:
+        raise SystemExit("--warmup must not exceed the residual tokens of the workload")
+    n_flush = (w.r + K) // 128                     # flushes inside the timed steps
+    T0 = max(0, w.T_q - 128 * (n_flush // 2))     # mean context over the timed steps ~ workload's
+    r0 = w.r - W
+    cap = T0 + 128 * (n_flush + 2)
+
+    Kall, Vall = make_kv(w, L=w.T_q + w.r, device=dev)
+    toks = [make_token(w, i, device=dev) for i in range(W + K)]
+    n_q = min(W + K, 64)
+    qs = [make_q(w, step=i, device=dev) for i in range(n_q)]
+    cache = kvq.KVCache(w.B, w.Hkv, cap, w.k_bits, w.v_bits, device=dev)
+    out = torch.empty(w.B, w.Hq, 128, dtype=torch.float32, device=dev)
+    ws = cache.workspace(w.Hq)
+    stream = torch.cuda.current_stream()
+
+    def prefill():
+        cache.reset()
+        cache.prefill(Kall[:, :, :T0 + r0].contiguous(), Vall[:, :, :T0 + r0].contiguous())
+
+    def step(i, ev=None):
+        """One decode step; returns (launches, algorithmic bytes)."""
+        kn, vn = toks[i]
+        cache.append(kn, vn)
+        launches, nb = 1, append_bytes(w)
+        if cache.lengths()[1] == 128:
+            cache.flush()
+            launches += 1
+            nb += flush_bytes(w)
+        tq, r = cache.lengths()
+        if ev is not None:
+            ev[0].record(stream)
+        cache.attention(qs[i % n_q], out=out, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+        return launches + 2, nb + attention_bytes(w, tq, r), attention_bytes(w, tq, r)
+
+    prefill()
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler()
+    clk.start()
+    time.sleep(0.02)
+    t_start.record(stream)
+    launches = 0
+    total_bytes = 0
+    attn_bytes = []
+    for i in range(K):
+        n, nb, ab = step(W + i, evs[i])
+        launches += n
+        total_bytes += nb
+        attn_bytes.append(ab)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        torch.distributed.barrier()
+    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    attn_avg_ms = sum(attn_ms) / K
+    attn_avg_bytes = sum(attn_bytes) / K
+    ms_per_step = elapsed_ms / K
+    value = total_bytes * world / (elapsed_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = attn_avg_bytes / (attn_avg_ms * 1e-3) / 1e9
+    src_hash = kernel_source_hash()
+    traffic = NCU_TRAFFIC.get(src_hash, {}).get((w.name, w.B, w.T_q, w.k_bits))
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(w0, {
+            "l2": "inputs larger than L2 (packed cache %.0f MB vs 129 MB L2)"
+                  % (attention_bytes(w, w.T_q, w.r) / 1e6),
+            "first_timed_context": T0 + w.r, "timed_flushes": n_flush,
+            "per_rank_seed_offset": 100}),
+        "us_per_step": 1e3 * ms_per_step,
+        "decode_attention_us": 1e3 * attn_avg_ms,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "decode attention (split-K partial + combine)",
+                     "algorithmic_bytes_per_launch": attn_avg_bytes, "traffic": traffic,
+                     "kernel_source": src_hash},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+
+    # bf16 unquantized comparator at the same batch and context
+    if not args.no_bf16:
+        q0 = qs[0]
+        for _ in range(3):
+            kvq.decode_bf16(Kall, Vall, q0, out=out)
+        nb16 = w.B * w.Hkv * (w.T_q + w.r) * 512 + w.B * w.Hq * (256 + 512)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        a.record(stream)
+        for _ in range(reps):
+            kvq.decode_bf16(Kall, Vall, q0, out=out)
+        b.record(stream)
+        torch.cuda.synchronize()
+        us16 = 1e3 * a.elapsed_time(b) / reps
+        line["comparators"] = {"bf16_decode_us": us16,
+                               "bf16_decode_gbs": nb16 / (us16 * 1e-6) / 1e9,
+                               "bf16_bytes_per_step": nb16,
+                               "speedup_vs_bf16": us16 / (1e3 * attn_avg_ms)}
+
+    # e2e: host buffers, copies inside the timed region
+    if not args.no_e2e:
+        prefill()
+        KE = min(K, 256)
+        h_tok = [(kn.cpu().pin_memory(), vn.cpu().pin_memory()) for kn, vn in toks[:W + KE]]
+        h_q = [q.cpu().pin_memory() for q in qs]
+        d_k = torch.empty_like(toks[0][0])
+        d_v = torch.empty_like(toks[0][1])
+        d_q = torch.empty_like(qs[0])
+        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        e2e_bytes = 0
+
+        def e2e_step(i):
+            d_k.copy_(h_tok[i][0], non_blocking=True)
+            d_v.copy_(h_tok[i][1], non_blocking=True)
+            d_q.copy_(h_q[i % n_q], non_blocking=True)
+            cache.append(d_k, d_v)
+            nb = append_bytes(w)
+            if cache.lengths()[1] == 128:
+                cache.flush()
+                nb += flush_bytes(w)
+            tq, r = cache.lengths()
+            cache.attention(d_q, out=out, workspace=ws)
+            h_out.copy_(out, non_blocking=True)
+            stream.synchronize()
+            return nb + attention_bytes(w, tq, r)
+
+        for i in range(W):
+            e2e_step(i)
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for i in range(KE):
+            e2e_bytes += e2e_step(W + i)
+        t1 = time.perf_counter()
+        e2e_s = t1 - t0
+        if world > 1:
+            t = torch.tensor([e2e_s], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        h2d = d_k.numel() * 2 + d_v.numel() * 2 + d_q.numel() * 2
+        line["e2e"] = {"value": e2e_bytes * world / e2e_s / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * 4,
+                       "steps": KE, "us_per_step": 1e6 * e2e_s / KE}
+
+    # CPU oracle on a bounded sample (rank 0, N = 1 only)
+    if not args.no_cpu and rank == 0 and world == 1:
+        nb, sec, units = oracle_sample(w0, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": nb / sec / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{units} decode-attention calls, each one (batch row, KV head) unit "
+                      f"of this workload with its {w0.n_rep} query heads over {w0.T_q} + "
+                      f"{w0.r} tokens (dequantize + fp64 attention), {sec:.1f} s "
+                      f"single-threaded",
+            "cpu_model": _cpu_model(), "host_cores": os.cpu_count()}
+    return line
+
+
+def _cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "ours":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,314 @@
+"""GB300 low-bit KV-cache quantization and fused decode attention.
+
+Thin ctypes binding over ``libkvq.so`` (declared in ``include/kvq.h``).  Every
+computation runs in the library's CUDA kernels; this module only checks
+tensor dtypes/shapes/devices, passes raw pointers and the current CUDA stream,
+and turns return codes into exceptions.  PyTorch provides device memory and
+streams.  There is no CPU fallback: if the library is missing the first call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "KVCache", "decode_bf16", "channel_saliency", "KVQError", "lib",
+    "KVQ_K_UNIFORM", "KVQ_K_MIXED", "TIER_BF16", "TIER_UINT4", "TIER_UINT2",
+    "FLAG_NONFINITE", "FLAG_RANGE", "HEAD_DIM", "K_GROUP", "V_GROUP", "RESIDUAL",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvq.so")
+
+HEAD_DIM, K_GROUP, V_GROUP, RESIDUAL = 128, 128, 32, 128
+KVQ_K_UNIFORM, KVQ_K_MIXED = 0, 1
+TIER_BF16, TIER_UINT4, TIER_UINT2 = 0, 1, 2
+TIERS_RANK, TIERS_THRESHOLD = 0, 1
+FLAG_NONFINITE, FLAG_RANGE = 1, 2
+
+_CODES = {0: "OK", 1: "ARG", 2: "SHAPE", 3: "CAPACITY", 4: "RESIDUAL_FULL",
+          5: "RESIDUAL_NOT_FULL", 6: "EMPTY", 7: "NOT_EMPTY", 8: "CUDA", 9: "WORKSPACE",
+          10: "MODE"}
+
+
+class KVQError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: KVQ_ERR_{_CODES.get(code, code)}")
+        self.code = code
+        self.name = _CODES.get(code, str(code))
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "batch", "kv_heads", "head_dim", "max_tokens", "k_bits", "v_bits", "k_mode",
+        "n_bf16", "n_uint4")]
+
+
+class _TierSpec(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("n_bf16", ctypes.c_int), ("n_uint4", ctypes.c_int),
+                ("tau_bf16", ctypes.c_float), ("tau_uint4", ctypes.c_float)]
+
+
+_lib = None
+
+# name -> (restype, argtypes); P = pointer, I = int, Z = size_t
+_P, _I, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_SIGS = {
+    "kvq_cache_bytes": (_Z, [_P]),
+    "kvq_cache_alloc": (_I, [_P, _P, _Z, _P, _P]),
+    "kvq_cache_free": (_I, [_P, _P]),
+    "kvq_cache_lengths": (_I, [_P, _P, _P]),
+    "kvq_cache_reset": (_I, [_P, _P]),
+    "kvq_append_residual": (_I, [_P, _P, _P, _P]),
+    "kvq_flush_group": (_I, [_P, _P, _P]),
+    "kvq_quantize_prefill": (_I, [_P, _P, _P, _I, _P, _P]),
+    "kvq_decode_workspace_bytes": (_Z, [_P, _I]),
+    "kvq_decode_attention": (_I, [_P, _P, _I, _P, _P, _Z, _P]),
+    "kvq_decode_bf16_workspace_bytes": (_Z, [_I, _I, _I, _I]),
+    "kvq_decode_bf16": (_I, [_P, _P, _I, _I, _I, _P, _I, _P, _P, _Z, _P]),
+    "kvq_channel_saliency": (_I, [_P, _I, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "kvq_cache_status": (_I, [_P, _P, _P]),
+    "kvq_export_k": (_I, [_P, _P, _P, _P, _P]),
+    "kvq_export_v": (_I, [_P, _P, _P, _P, _P]),
+    "kvq_export_residual": (_I, [_P, _P, _P, _P]),
+    "kvq_export_k_mixed": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "kvq_status_string": (ctypes.c_char_p, [_I]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkvq.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libkvq.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise KVQError(code, what)
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, shape=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+class KVCache:
+    """One layer's packed KV cache on the current GPU (MixKVQ Algorithm 1
+    state: packed history + bf16 residual of up to 128 tokens).
+
+    mode "uniform": keys at k_bits per channel over 128-token groups;
+    mode "mixed": keys tiered per group into n_bf16 BF16, n_uint4 UINT4 and
+    the rest UINT2 channels.  Values always v_bits per token over 32 channels.
+    The device buffer is a torch uint8 tensor owned by this object.
+    """
+
+    def __init__(self, batch: int, kv_heads: int, max_tokens: int, k_bits: int = 2,
+                 v_bits: int = 2, mode: str = "uniform", n_bf16: int = 0, n_uint4: int = 0,
+                 head_dim: int = HEAD_DIM, device=None, stream=None):
+        self.cfg = _Config(batch, kv_heads, head_dim, max_tokens, k_bits, v_bits,
+                           KVQ_K_MIXED if mode == "mixed" else KVQ_K_UNIFORM, n_bf16, n_uint4)
+        self.mode = mode
+        nbytes = lib().kvq_cache_bytes(ctypes.byref(self.cfg))
+        if nbytes == 0:
+            raise KVQError(1, "kvq_cache_bytes (invalid config)")
+        self.nbytes = nbytes
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        h = ctypes.c_void_p()
+        with torch.cuda.device(dev):
+            _check(lib().kvq_cache_alloc(ctypes.byref(self.cfg), self.buffer.data_ptr(), nbytes,
+                                         _stream(stream), ctypes.byref(h)), "kvq_cache_alloc")
+        self._h = h
+        self.batch, self.kv_heads, self.max_tokens = batch, kv_heads, max_tokens
+        self.k_bits, self.v_bits, self.n_bf16, self.n_uint4 = k_bits, v_bits, n_bf16, n_uint4
+        self.device = dev
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.kvq_cache_free(h, None)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    # -- state
+    def lengths(self) -> tuple[int, int]:
+        tq, r = ctypes.c_int(), ctypes.c_int()
+        _check(lib().kvq_cache_lengths(self._h, ctypes.byref(tq), ctypes.byref(r)), "lengths")
+        return tq.value, r.value
+
+    def status(self, stream=None) -> int:
+        st = ctypes.c_int()
+        _check(lib().kvq_cache_status(self._h, _stream(stream), ctypes.byref(st)), "status")
+        return st.value
+
+    def reset(self, stream=None):
+        _check(lib().kvq_cache_reset(self._h, _stream(stream)), "reset")
+
+    # -- Algorithm 1
+    def prefill(self, k: torch.Tensor, v: torch.Tensor, importance: torch.Tensor | None = None,
+                stream=None):
+        B, H, L, D = k.shape
+        shp = (self.batch, self.kv_heads, L, HEAD_DIM)
+        _check(lib().kvq_quantize_prefill(
+            self._h, _ptr(k, torch.bfloat16, shp, "k"), _ptr(v, torch.bfloat16, shp, "v"), L,
+            _ptr(importance, torch.float32, (self.batch, self.kv_heads, HEAD_DIM), "importance"),
+            _stream(stream)), "kvq_quantize_prefill")
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        shp = (self.batch, self.kv_heads, HEAD_DIM)
+        _check(lib().kvq_append_residual(self._h, _ptr(k_new, torch.bfloat16, shp, "k_new"),
+                                         _ptr(v_new, torch.bfloat16, shp, "v_new"),
+                                         _stream(stream)), "kvq_append_residual")
+
+    def flush(self, importance: torch.Tensor | None = None, stream=None):
+        _check(lib().kvq_flush_group(
+            self._h, _ptr(importance, torch.float32, (self.batch, self.kv_heads, HEAD_DIM),
+                          "importance"), _stream(stream)), "kvq_flush_group")
+
+    def workspace_bytes(self, Hq: int) -> int:
+        return lib().kvq_decode_workspace_bytes(self._h, Hq)
+
+    def workspace(self, Hq: int) -> torch.Tensor:
+        return torch.empty(self.workspace_bytes(Hq), dtype=torch.uint8, device=self.device)
+
+    def attention(self, q: torch.Tensor, out: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        B, Hq, D = q.shape
+        if out is None:
+            out = torch.empty(B, Hq, HEAD_DIM, dtype=torch.float32, device=q.device)
+        if workspace is None:
+            workspace = self.workspace(Hq)
+        _check(lib().kvq_decode_attention(
+            self._h, _ptr(q, torch.bfloat16, (self.batch, Hq, HEAD_DIM), "q"), Hq,
+            _ptr(out, torch.float32, (self.batch, Hq, HEAD_DIM), "out"),
+            _ptr(workspace, torch.uint8, None, "workspace"), workspace.numel(),
+            _stream(stream)), "kvq_decode_attention")
+        return out
+
+    # -- canonical export (device tensors)
+    def export_k(self, stream=None):
+        tq, _ = self.lengths()
+        n = tq // K_GROUP
+        B, H, dev = self.batch, self.kv_heads, self.device
+        codes = torch.empty(B, H, n, HEAD_DIM, K_GROUP * self.k_bits // 8, dtype=torch.uint8, device=dev)
+        kmin = torch.empty(B, H, n, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        kscale = torch.empty(B, H, n, HEAD_DIM, dtype=torch.float32, device=dev)
+        _check(lib().kvq_export_k(self._h, codes.data_ptr(), kmin.data_ptr(), kscale.data_ptr(),
+                                  _stream(stream)), "kvq_export_k")
+        return codes, kmin, kscale
+
+    def export_v(self, stream=None):
+        tq, _ = self.lengths()
+        B, H, dev = self.batch, self.kv_heads, self.device
+        codes = torch.empty(B, H, tq, HEAD_DIM * self.v_bits // 8, dtype=torch.uint8, device=dev)
+        vmin = torch.empty(B, H, tq, HEAD_DIM // V_GROUP, dtype=torch.bfloat16, device=dev)
+        vscale = torch.empty(B, H, tq, HEAD_DIM // V_GROUP, dtype=torch.float32, device=dev)
+        _check(lib().kvq_export_v(self._h, codes.data_ptr(), vmin.data_ptr(), vscale.data_ptr(),
+                                  _stream(stream)), "kvq_export_v")
+        return codes, vmin, vscale
+
+    def export_residual(self, stream=None):
+        _, r = self.lengths()
+        B, H, dev = self.batch, self.kv_heads, self.device
+        kr = torch.empty(B, H, r, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        vr = torch.empty(B, H, r, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        _check(lib().kvq_export_residual(self._h, kr.data_ptr(), vr.data_ptr(), _stream(stream)),
+               "kvq_export_residual")
+        return kr, vr
+
+    def export_k_mixed(self, stream=None):
+        tq, _ = self.lengths()
+        n = tq // K_GROUP
+        B, H, dev = self.batch, self.kv_heads, self.device
+        nb, n4 = self.n_bf16, self.n_uint4
+        n2 = HEAD_DIM - nb - n4
+        t = dict(
+            perm=torch.empty(B, H, n, HEAD_DIM, dtype=torch.uint8, device=dev),
+            raw=torch.empty(B, H, n, nb, K_GROUP, dtype=torch.bfloat16, device=dev),
+            c4=torch.empty(B, H, n, n4, K_GROUP // 2, dtype=torch.uint8, device=dev),
+            m4=torch.empty(B, H, n, n4, dtype=torch.bfloat16, device=dev),
+            s4=torch.empty(B, H, n, n4, dtype=torch.float32, device=dev),
+            c2=torch.empty(B, H, n, n2, K_GROUP // 4, dtype=torch.uint8, device=dev),
+            m2=torch.empty(B, H, n, n2, dtype=torch.bfloat16, device=dev),
+            s2=torch.empty(B, H, n, n2, dtype=torch.float32, device=dev))
+        _check(lib().kvq_export_k_mixed(self._h, *[x.data_ptr() for x in t.values()],
+                                        _stream(stream)), "kvq_export_k_mixed")
+        return t
+
+
+def decode_bf16(k: torch.Tensor, v: torch.Tensor, q: torch.Tensor,
+                out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """Unquantized comparator over bf16 k, v [B, Hkv, T, D]; q [B, Hq, D]."""
+    B, Hkv, T, D = k.shape
+    Hq = q.shape[1]
+    if out is None:
+        out = torch.empty(B, Hq, HEAD_DIM, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(lib().kvq_decode_bf16_workspace_bytes(B, Hkv, T, Hq),
+                                dtype=torch.uint8, device=q.device)
+    _check(lib().kvq_decode_bf16(
+        _ptr(k, torch.bfloat16, (B, Hkv, T, HEAD_DIM), "k"),
+        _ptr(v, torch.bfloat16, (B, Hkv, T, HEAD_DIM), "v"), B, Hkv, T,
+        _ptr(q, torch.bfloat16, (B, Hq, HEAD_DIM), "q"), Hq,
+        _ptr(out, torch.float32, (B, Hq, HEAD_DIM), "out"),
+        _ptr(workspace, torch.uint8, None, "workspace"), workspace.numel(), _stream(stream)),
+        "kvq_decode_bf16")
+    return out
+
+
+def channel_saliency(q_win: torch.Tensor, k_grp: torch.Tensor, sal_bits: int = 2,
+                     n_bf16: int | None = None, n_uint4: int | None = None,
+                     tau_bf16: float | None = None, tau_uint4: float | None = None,
+                     stream=None):
+    """MixKVQ I_d, A_d = I_d * S_d and tiers per (b, kv head, d).
+
+    q_win bf16 [B, Hq, Lq, D]; k_grp bf16 [B, Hkv, G, D].  Rank tiers when
+    n_bf16/n_uint4 are given, threshold tiers when tau_bf16/tau_uint4 are.
+    Returns (I, A, tiers) as device tensors.
+    """
+    B, Hq, Lq, D = q_win.shape
+    _, Hkv, G, _ = k_grp.shape
+    if n_bf16 is not None:
+        spec = _TierSpec(TIERS_RANK, n_bf16, n_uint4 or 0, 0.0, 0.0)
+    else:
+        spec = _TierSpec(TIERS_THRESHOLD, 0, 0, float(tau_bf16), float(tau_uint4))
+    dev = q_win.device
+    I = torch.empty(B, Hkv, HEAD_DIM, dtype=torch.float32, device=dev)
+    A = torch.empty_like(I)
+    tiers = torch.empty(B, Hkv, HEAD_DIM, dtype=torch.uint8, device=dev)
+    _check(lib().kvq_channel_saliency(
+        _ptr(q_win, torch.bfloat16, (B, Hq, Lq, HEAD_DIM), "q_win"), Hq, Lq,
+        _ptr(k_grp, torch.bfloat16, (B, Hkv, G, HEAD_DIM), "k_grp"), B, Hkv, G, sal_bits,
+        ctypes.byref(spec), I.data_ptr(), A.data_ptr(), tiers.data_ptr(), _stream(stream)),
+        "kvq_channel_saliency")
+    return I, A, tiers

@@ -1,0 +1,315 @@
+// extern "C" entry points of libkvq.so (declared and documented in kvq.h).
+// Host side only: argument checks, the cache handle and its lengths, and the
+// kernel launches.  Every check runs before anything is enqueued, so a call
+// that returns an error leaves the cache unchanged.
+#include <cuda_runtime.h>
+
+#include <new>
+
+#include "kvq_internal.h"
+
+using namespace kvq;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool valid_config(const kvq_config* c) {
+  if (!c) return false;
+  if (c->batch < 1 || c->kv_heads < 1 || c->max_tokens < 0) return false;
+  if (c->head_dim != kD) return false;
+  if (c->max_tokens % kKG) return false;
+  if (c->v_bits != 2 && c->v_bits != 4) return false;
+  if (c->k_mode == KVQ_K_UNIFORM) {
+    if (c->k_bits != 2 && c->k_bits != 4) return false;
+  } else if (c->k_mode == KVQ_K_MIXED) {
+    if (c->n_bf16 < 0 || c->n_uint4 < 0 || c->n_bf16 + c->n_uint4 > kD) return false;
+  } else {
+    return false;
+  }
+  return true;
+}
+
+RecLayout layout_of(const kvq_config* c) {
+  return make_layout(c->k_mode == KVQ_K_MIXED, c->k_mode == KVQ_K_MIXED ? 2 : c->k_bits,
+                     c->v_bits, c->n_bf16, c->n_uint4);
+}
+
+struct Sizes {
+  size_t records, residual, status, total;
+};
+
+Sizes sizes_of(const kvq_config* c) {
+  const RecLayout L = layout_of(c);
+  const size_t units = static_cast<size_t>(c->batch) * c->kv_heads;
+  Sizes s;
+  s.records = round_up(units * (c->max_tokens / kKG) * static_cast<size_t>(L.bytes));
+  s.residual = round_up(units * kR * kD * sizeof(kvq_bf16));
+  s.status = kAlign;
+  s.total = s.records + 2 * s.residual + s.status;
+  return s;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+size_t kvq_cache_bytes(const kvq_config* cfg) {
+  if (!valid_config(cfg)) return 0;
+  return sizes_of(cfg).total;
+}
+
+int kvq_cache_alloc(const kvq_config* cfg, void* dev_buf, size_t buf_bytes,
+                    cudaStream_t s, kvq_cache** out) {
+  if (!out || !cfg) return KVQ_ERR_ARG;
+  *out = nullptr;
+  if (cfg->head_dim != kD) return KVQ_ERR_SHAPE;
+  if (!valid_config(cfg)) return KVQ_ERR_ARG;
+  const Sizes sz = sizes_of(cfg);
+  if (dev_buf) {
+    if (buf_bytes < sz.total) return KVQ_ERR_CAPACITY;
+    if (reinterpret_cast<uintptr_t>(dev_buf) % kAlign) return KVQ_ERR_ARG;
+  }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  kvq_cache* c = new (std::nothrow) kvq_cache{};
+  if (!c) return KVQ_ERR_CUDA;
+  c->cfg = *cfg;
+  if (cfg->k_mode == KVQ_K_MIXED) c->cfg.k_bits = 2;
+  c->lay = layout_of(cfg);
+  c->device = dev;
+  c->num_sms = sms;
+  c->bytes = sz.total;
+  c->owned = dev_buf == nullptr;
+  if (c->owned) {
+    void* p = nullptr;
+    if (cudaMallocAsync(&p, sz.total, s) != cudaSuccess) {
+      delete c;
+      return KVQ_ERR_CUDA;
+    }
+    c->base = static_cast<uint8_t*>(p);
+  } else {
+    c->base = static_cast<uint8_t*>(dev_buf);
+  }
+  c->records = c->base;
+  c->max_groups = cfg->max_tokens / kKG;
+  c->res_k = reinterpret_cast<kvq_bf16*>(c->base + sz.records);
+  c->res_v = reinterpret_cast<kvq_bf16*>(c->base + sz.records + sz.residual);
+  c->status = reinterpret_cast<unsigned*>(c->base + sz.records + 2 * sz.residual);
+  c->t_q = 0;
+  c->r = 0;
+  if (cudaMemsetAsync(c->status, 0, sizeof(unsigned), s) != cudaSuccess) {
+    if (c->owned) cudaFreeAsync(c->base, s);
+    delete c;
+    return KVQ_ERR_CUDA;
+  }
+  *out = c;
+  return KVQ_OK;
+}
+
+int kvq_cache_free(kvq_cache* c, cudaStream_t s) {
+  if (!c) return KVQ_ERR_ARG;
+  cudaError_t e = cudaSuccess;
+  if (c->owned) e = cudaFreeAsync(c->base, s);
+  delete c;
+  return cuda_status(e);
+}
+
+int kvq_cache_lengths(const kvq_cache* c, int* quantized_tokens, int* residual_tokens) {
+  if (!c) return KVQ_ERR_ARG;
+  if (quantized_tokens) *quantized_tokens = c->t_q;
+  if (residual_tokens) *residual_tokens = c->r;
+  return KVQ_OK;
+}
+
+int kvq_cache_reset(kvq_cache* c, cudaStream_t s) {
+  if (!c) return KVQ_ERR_ARG;
+  if (cudaMemsetAsync(c->status, 0, sizeof(unsigned), s) != cudaSuccess) return KVQ_ERR_CUDA;
+  c->t_q = 0;
+  c->r = 0;
+  return KVQ_OK;
+}
+
+int kvq_append_residual(kvq_cache* c, const kvq_bf16* k_new, const kvq_bf16* v_new,
+                        cudaStream_t s) {
+  if (!c || !k_new || !v_new) return KVQ_ERR_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
+  if (c->r >= kR) return KVQ_ERR_RESIDUAL_FULL;
+  const cudaError_t e = launch_append(c, k_new, v_new, s);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  c->r += 1;
+  return KVQ_OK;
+}
+
+static int check_importance(const kvq_cache* c, const float* importance) {
+  if (c->cfg.k_mode == KVQ_K_MIXED) return importance ? KVQ_OK : KVQ_ERR_MODE;
+  return importance ? KVQ_ERR_MODE : KVQ_OK;
+}
+
+int kvq_flush_group(kvq_cache* c, const float* importance, cudaStream_t s) {
+  if (!c) return KVQ_ERR_ARG;
+  const int m = check_importance(c, importance);
+  if (m != KVQ_OK) return m;
+  if (c->r != kR) return KVQ_ERR_RESIDUAL_NOT_FULL;
+  if (c->t_q + kKG > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
+  QuantSrc src{c->res_k, c->res_v, static_cast<long long>(kR) * kD, 0};
+  const cudaError_t e = launch_quantize(c, src, 1, c->t_q / kKG, importance, s);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  c->t_q += kKG;
+  c->r = 0;
+  return KVQ_OK;
+}
+
+int kvq_quantize_prefill(kvq_cache* c, const kvq_bf16* k, const kvq_bf16* v, int L,
+                         const float* importance, cudaStream_t s) {
+  if (!c || L < 0) return KVQ_ERR_ARG;
+  if (L > 0 && (!k || !v)) return KVQ_ERR_ARG;
+  if (L > 0 && (!aligned16(k) || !aligned16(v))) return KVQ_ERR_ARG;
+  const int m = check_importance(c, importance);
+  if (m != KVQ_OK) return m;
+  if (c->t_q != 0 || c->r != 0) return KVQ_ERR_NOT_EMPTY;
+  const int n_q = L / kKG;
+  const int r = L % kKG;
+  if (n_q * kKG > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
+  if (L == 0) return KVQ_OK;
+  QuantSrc src{k, v, static_cast<long long>(L) * kD, static_cast<long long>(kKG) * kD};
+  cudaError_t e = launch_quantize(c, src, n_q, 0, importance, s);
+  if (e == cudaSuccess) e = launch_residual_tail(c, k, v, L, n_q * kKG, r, s);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  c->t_q = n_q * kKG;
+  c->r = r;
+  return KVQ_OK;
+}
+
+size_t kvq_decode_workspace_bytes(const kvq_cache* c, int Hq) {
+  if (!c || Hq < 1 || Hq % c->cfg.kv_heads) return 0;
+  return decode_ws_bytes(static_cast<long long>(c->cfg.batch) * Hq, kMaxSplits);
+}
+
+static bool valid_rep(int Hq, int Hkv) {
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv) return false;
+  const int n = Hq / Hkv;
+  return n == 1 || n == 2 || n == 4 || n == 8;
+}
+
+int kvq_decode_attention(const kvq_cache* c, const kvq_bf16* q, int Hq, float* out,
+                         void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (!c || !q || !out) return KVQ_ERR_ARG;
+  if (!valid_rep(Hq, c->cfg.kv_heads)) return KVQ_ERR_SHAPE;
+  if (c->cfg.k_mode != KVQ_K_UNIFORM) return KVQ_ERR_MODE;
+  if (c->t_q + c->r == 0) return KVQ_ERR_EMPTY;
+  if (!ws || ws_bytes < kvq_decode_workspace_bytes(c, Hq) || !aligned16(ws))
+    return KVQ_ERR_WORKSPACE;
+  const int units = c->cfg.batch * c->cfg.kv_heads;
+  const int n_split = choose_splits(c->num_sms, units, c->t_q / kKG);
+  return cuda_status(launch_decode(c, q, Hq, out, static_cast<float*>(ws), n_split, s));
+}
+
+size_t kvq_decode_bf16_workspace_bytes(int B, int Hkv, int T, int Hq) {
+  if (B < 1 || Hkv < 1 || T < 1 || !valid_rep(Hq, Hkv)) return 0;
+  return decode_ws_bytes(static_cast<long long>(B) * Hq, kMaxSplits);
+}
+
+int kvq_decode_bf16(const kvq_bf16* k, const kvq_bf16* v, int B, int Hkv, int T,
+                    const kvq_bf16* q, int Hq, float* out, void* ws, size_t ws_bytes,
+                    cudaStream_t s) {
+  if (!k || !v || !q || !out || B < 1 || Hkv < 1 || T < 1) return KVQ_ERR_ARG;
+  if (!aligned16(k) || !aligned16(v)) return KVQ_ERR_ARG;
+  if (!valid_rep(Hq, Hkv)) return KVQ_ERR_SHAPE;
+  if (!ws || ws_bytes < kvq_decode_bf16_workspace_bytes(B, Hkv, T, Hq) || !aligned16(ws))
+    return KVQ_ERR_WORKSPACE;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  const int n_split = choose_splits(sms, B * Hkv, (T + kKG - 1) / kKG);
+  return cuda_status(launch_decode_bf16(k, v, B, Hkv, T, q, Hq, out,
+                                        static_cast<float*>(ws), n_split, sms, s));
+}
+
+int kvq_channel_saliency(const kvq_bf16* q_win, int Hq, int Lq, const kvq_bf16* k_grp,
+                         int B, int Hkv, int G, int sal_bits, const kvq_tier_spec* spec,
+                         float* I_out, float* A_out, uint8_t* tiers_out, cudaStream_t s) {
+  if (!q_win || !k_grp || !spec || B < 1 || Hkv < 1 || Lq < 1 || G < 1) return KVQ_ERR_ARG;
+  if (Hq < Hkv || Hq % Hkv) return KVQ_ERR_SHAPE;
+  if (sal_bits < 1 || sal_bits > 8) return KVQ_ERR_ARG;
+  if (spec->mode == KVQ_TIERS_RANK) {
+    if (spec->n_bf16 < 0 || spec->n_uint4 < 0 || spec->n_bf16 + spec->n_uint4 > kD)
+      return KVQ_ERR_ARG;
+  } else if (spec->mode != KVQ_TIERS_THRESHOLD) {
+    return KVQ_ERR_ARG;
+  }
+  return cuda_status(launch_saliency(q_win, Hq, Lq, k_grp, B, Hkv, G, sal_bits, spec,
+                                     I_out, A_out, tiers_out, s));
+}
+
+int kvq_cache_status(kvq_cache* c, cudaStream_t s, int* status) {
+  if (!c || !status) return KVQ_ERR_ARG;
+  unsigned host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, c->status, sizeof host, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  *status = static_cast<int>(host);
+  return KVQ_OK;
+}
+
+int kvq_export_k(const kvq_cache* c, uint8_t* codes, kvq_bf16* kmin, float* kscale,
+                 cudaStream_t s) {
+  if (!c || !codes || !kmin || !kscale) return KVQ_ERR_ARG;
+  if (c->cfg.k_mode != KVQ_K_UNIFORM) return KVQ_ERR_MODE;
+  return cuda_status(launch_export_k_uniform(c, codes, kmin, kscale, s));
+}
+
+int kvq_export_v(const kvq_cache* c, uint8_t* codes, kvq_bf16* vmin, float* vscale,
+                 cudaStream_t s) {
+  if (!c || !codes || !vmin || !vscale) return KVQ_ERR_ARG;
+  return cuda_status(launch_export_v(c, codes, vmin, vscale, s));
+}
+
+int kvq_export_residual(const kvq_cache* c, kvq_bf16* k_r, kvq_bf16* v_r, cudaStream_t s) {
+  if (!c || !k_r || !v_r) return KVQ_ERR_ARG;
+  if (c->r == 0) return KVQ_OK;
+  const int units = c->cfg.batch * c->cfg.kv_heads;
+  const size_t row = kD * sizeof(kvq_bf16);
+  cudaError_t e = cudaMemcpy2DAsync(k_r, c->r * row, c->res_k, kR * row, c->r * row, units,
+                                    cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpy2DAsync(v_r, c->r * row, c->res_v, kR * row, c->r * row, units,
+                          cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+int kvq_export_k_mixed(const kvq_cache* c, uint8_t* perm, kvq_bf16* raw, uint8_t* c4,
+                       kvq_bf16* m4, float* s4, uint8_t* c2, kvq_bf16* m2, float* s2,
+                       cudaStream_t s) {
+  if (!c || !perm || !raw || !c4 || !m4 || !s4 || !c2 || !m2 || !s2) return KVQ_ERR_ARG;
+  if (c->cfg.k_mode != KVQ_K_MIXED) return KVQ_ERR_MODE;
+  return cuda_status(launch_export_k_mixed(c, perm, raw, c4, m4, s4, c2, m2, s2, s));
+}
+
+const char* kvq_status_string(int code) {
+  switch (code) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_ARG: return "KVQ_ERR_ARG";
+    case KVQ_ERR_SHAPE: return "KVQ_ERR_SHAPE";
+    case KVQ_ERR_CAPACITY: return "KVQ_ERR_CAPACITY";
+    case KVQ_ERR_RESIDUAL_FULL: return "KVQ_ERR_RESIDUAL_FULL";
+    case KVQ_ERR_RESIDUAL_NOT_FULL: return "KVQ_ERR_RESIDUAL_NOT_FULL";
+    case KVQ_ERR_EMPTY: return "KVQ_ERR_EMPTY";
+    case KVQ_ERR_NOT_EMPTY: return "KVQ_ERR_NOT_EMPTY";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA";
+    case KVQ_ERR_WORKSPACE: return "KVQ_ERR_WORKSPACE";
+    case KVQ_ERR_MODE: return "KVQ_ERR_MODE";
+    default: return "KVQ_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

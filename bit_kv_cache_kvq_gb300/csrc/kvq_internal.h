@@ -1,0 +1,168 @@
+// Internal definitions of libkvq: HBM layout of the packed cache, the cache
+// handle and the kernel launchers shared between translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kD = KVQ_HEAD_DIM;   // head_dim
+constexpr int kKG = KVQ_K_GROUP;   // tokens per key group
+constexpr int kVG = KVQ_V_GROUP;   // channels per value group
+constexpr int kR = KVQ_RESIDUAL;   // residual capacity
+constexpr int kVGroups = kD / kVG; // value groups per token (4)
+constexpr int kMaxSplits = 64;     // split-K partitions per (batch, KV head)
+constexpr int kMaxRep = 8;         // query heads per KV head
+
+// ---------------------------------------------------------------------------
+// One "group record" holds everything the decode kernel reads for 128
+// consecutive tokens of one (batch row, KV head): the Key codes and per-
+// channel (step, origin), then the Value codes and per-token (step, origin).
+// Records of one (b, kv head) are contiguous, so a split of the token axis
+// is one contiguous byte range (streamed with plain 16-byte loads).
+//
+// Uniform key (k_bits = kb):
+//   [0]            K codes  uint8 [D][128*kb/8]   channel d's 128 codes,
+//                                                 LSB first along tokens
+//   [kc]           kscale   fp32  [D]
+//   [kc+4D]        kmin     bf16  [D]
+// Mixed key (n_bf16 = nb, n_uint4 = n4, n_uint2 = n2):
+//   [0]            perm     uint8 [D]   BF16, UINT4, UINT2 channels, ascending
+//   [D]            raw      bf16  [nb][128]
+//   [..]           c4       uint8 [n4][64]
+//   [..]           c2       uint8 [n2][32]
+//   [..]           s4, s2   fp32  [n4], [n2]
+//   [..]           m4, m2   bf16  [n4], [n2]      (padded to 16 bytes)
+// Value (v_bits = vb), after the key part at offset kpart:
+//   [kpart]        V codes  uint8 [128][D*vb/8]   token t's D codes, LSB
+//                                                 first along channels
+//   [+vc]          vscale   fp32  [128][D/32]
+//   [+vc+2048]     vmin     bf16  [128][D/32]
+// Every section starts on a 16-byte boundary.
+// ---------------------------------------------------------------------------
+struct RecLayout {
+  int mixed;
+  int kb, vb;
+  int nb, n4, n2;
+  // key (uniform)
+  int k_codes, k_scale, k_min;
+  // key (mixed)
+  int perm, raw, c4, c2, s4, s2, m4, m2;
+  int kpart;  // bytes of the key part
+  // value
+  int v_codes, v_scale, v_min;
+  int bytes;  // total record bytes (multiple of 16)
+};
+
+__host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
+
+__host__ __device__ inline RecLayout make_layout(int mixed, int kb, int vb,
+                                                 int nb, int n4) {
+  RecLayout L{};
+  L.mixed = mixed;
+  L.kb = kb;
+  L.vb = vb;
+  if (!mixed) {
+    L.k_codes = 0;
+    L.k_scale = kD * kKG * kb / 8;
+    L.k_min = L.k_scale + 4 * kD;
+    L.kpart = align16(L.k_min + 2 * kD);
+  } else {
+    L.nb = nb;
+    L.n4 = n4;
+    L.n2 = kD - nb - n4;
+    L.perm = 0;
+    L.raw = kD;
+    L.c4 = L.raw + nb * kKG * 2;
+    L.c2 = L.c4 + L.n4 * (kKG / 2);
+    L.s4 = L.c2 + L.n2 * (kKG / 4);
+    L.s2 = L.s4 + 4 * L.n4;
+    L.m4 = L.s2 + 4 * L.n2;
+    L.m2 = L.m4 + 2 * L.n4;
+    L.kpart = align16(L.m2 + 2 * L.n2);
+  }
+  L.v_codes = L.kpart;
+  L.v_scale = L.v_codes + kKG * kD * vb / 8;
+  L.v_min = L.v_scale + 4 * kKG * kVGroups;
+  L.bytes = align16(L.v_min + 2 * kKG * kVGroups);
+  return L;
+}
+
+}  // namespace kvq
+
+// The opaque handle.
+struct kvq_cache {
+  kvq_config cfg;
+  kvq::RecLayout lay;
+  int device;
+  int num_sms;
+  uint8_t* base;       // whole device allocation
+  bool owned;          // allocated by the library
+  size_t bytes;
+  uint8_t* records;    // [B*Hkv][max_groups][lay.bytes]
+  int max_groups;
+  kvq_bf16* res_k;     // [B*Hkv][128][D]
+  kvq_bf16* res_v;
+  unsigned* status;    // sticky KVQ_FLAG_* word
+  int t_q;             // quantized tokens (multiple of 128)
+  int r;               // residual tokens (0..128)
+};
+
+namespace kvq {
+
+// Where the quantize kernel reads its 128-token tiles from.
+struct QuantSrc {
+  const kvq_bf16* k;
+  const kvq_bf16* v;
+  long long unit_stride;   // elements between consecutive (b, kv head)
+  long long group_stride;  // elements between consecutive 128-token tiles
+};
+
+cudaError_t launch_append(const kvq_cache* c, const kvq_bf16* k_new,
+                          const kvq_bf16* v_new, cudaStream_t s);
+cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
+                            int first_group, const float* importance,
+                            cudaStream_t s);
+cudaError_t launch_residual_tail(const kvq_cache* c, const kvq_bf16* k,
+                                 const kvq_bf16* v, int L, int first,
+                                 int count, cudaStream_t s);
+
+int choose_splits(int num_sms, int units, int n_chunks);
+
+cudaError_t launch_decode(const kvq_cache* c, const kvq_bf16* q, int Hq,
+                          float* out, float* ws, int n_split, cudaStream_t s);
+cudaError_t launch_decode_bf16(const kvq_bf16* k, const kvq_bf16* v, int B,
+                               int Hkv, int T, const kvq_bf16* q, int Hq,
+                               float* out, float* ws, int n_split, int num_sms,
+                               cudaStream_t s);
+cudaError_t launch_combine(const float* ws, int rows, int n_split, float* out,
+                           cudaStream_t s);
+
+cudaError_t launch_saliency(const kvq_bf16* q_win, int Hq, int Lq,
+                            const kvq_bf16* k_grp, int B, int Hkv, int G,
+                            int sal_bits, const kvq_tier_spec* spec,
+                            float* I_out, float* A_out, uint8_t* tiers_out,
+                            cudaStream_t s);
+
+cudaError_t launch_export_k_uniform(const kvq_cache* c, uint8_t* codes,
+                                    kvq_bf16* kmin, float* kscale,
+                                    cudaStream_t s);
+cudaError_t launch_export_v(const kvq_cache* c, uint8_t* codes, kvq_bf16* vmin,
+                            float* vscale, cudaStream_t s);
+cudaError_t launch_export_k_mixed(const kvq_cache* c, uint8_t* perm,
+                                  kvq_bf16* raw, uint8_t* c4, kvq_bf16* m4,
+                                  float* s4, uint8_t* c2, kvq_bf16* m2,
+                                  float* s2, cudaStream_t s);
+
+// Workspace layout of the split-K decode: o partials [rows][n_split][D]
+// followed by (m, l) pairs [rows][n_split][2], fp32.
+inline size_t decode_ws_bytes(long long rows, int n_split) {
+  return (size_t)rows * (size_t)n_split * (size_t)(kD + 2) * sizeof(float);
+}
+
+}  // namespace kvq

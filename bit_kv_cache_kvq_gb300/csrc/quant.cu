@@ -1,0 +1,418 @@
+// Residual append, group quantization (flush and prefill, uniform and mixed
+// keys) and canonical export of the packed cache.
+//
+// Quantizer ("KIVI: KV cache axes" §2; MixKVQ "KV cache quantization
+// principle"; PN-Mix Eq. 2): per group m = min, M = max,
+//   step = fl32(fl32(M - m) / (2^b - 1)),  c = clip(RNE(fl32(fl32(x - m) / step)))
+// with IEEE fp32 subtraction and division (__fsub_rn / __fdiv_rn), codes
+// rounded half-to-even, and a constant group (M == m) stored as step 0,
+// codes 0, origin m.  Groups: Key per channel over the 128 tokens of a tile,
+// Value per token over 32 consecutive channels (KIVI §3).
+#include <cuda_runtime.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ float bf2f(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Order-preserving key of a finite float; -0.0 sorts below +0.0.
+__device__ __forceinline__ uint32_t fkey(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unkey(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+struct Params {
+  float m;
+  float step;
+  unsigned flags;
+};
+
+__device__ __forceinline__ Params group_params(float lo, float hi, int top,
+                                               bool nonfinite) {
+  Params p{lo, 0.0f, nonfinite ? (unsigned)KVQ_FLAG_NONFINITE : 0u};
+  if (nonfinite || hi == lo) return p;
+  const float range = __fsub_rn(hi, lo);
+  const float step = __fdiv_rn(range, static_cast<float>(top));
+  if (!(step > 0.0f) || !isfinite(step)) p.flags |= KVQ_FLAG_RANGE;
+  p.step = step;
+  return p;
+}
+
+__device__ __forceinline__ uint32_t code_of(float x, const Params& p, int top) {
+  if (p.step == 0.0f) return 0u;
+  const float y = __fdiv_rn(__fsub_rn(x, p.m), p.step);
+  float r = rintf(y);  // round half to even
+  r = fminf(fmaxf(r, 0.0f), static_cast<float>(top));
+  return static_cast<uint32_t>(r);
+}
+
+__device__ __forceinline__ uint16_t f2bf_bits(float exact_bf16_value) {
+  return static_cast<uint16_t>(__float_as_uint(exact_bf16_value) >> 16);
+}
+
+struct QuantArgs {
+  QuantSrc src;
+  uint8_t* records;
+  long long rec_bytes;
+  int max_groups;
+  int first_group;
+  RecLayout lay;
+  const float* importance;  // mixed: [units][D]
+  unsigned* status;
+};
+
+// Stage one 128-token tile of K and V (bf16 [128][128] each) in shared memory.
+__device__ __forceinline__ void load_tiles(const QuantArgs& a, uint16_t* sK,
+                                           uint16_t* sV) {
+  const long long off = static_cast<long long>(blockIdx.y) * a.src.unit_stride +
+                        static_cast<long long>(blockIdx.x) * a.src.group_stride;
+  const uint4* gk = reinterpret_cast<const uint4*>(a.src.k + off);
+  const uint4* gv = reinterpret_cast<const uint4*>(a.src.v + off);
+  uint4* tk = reinterpret_cast<uint4*>(sK);
+  uint4* tv = reinterpret_cast<uint4*>(sV);
+  for (int i = threadIdx.x; i < kKG * kD * 2 / 16; i += blockDim.x) {
+    tk[i] = __ldg(gk + i);
+    tv[i] = __ldg(gv + i);
+  }
+}
+
+// One Key channel over the tile's 128 tokens: min/max and finiteness.
+__device__ __forceinline__ void channel_range(const uint16_t* sK, int d,
+                                              float& lo, float& hi, bool& bad) {
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  bad = false;
+  for (int t = 0; t < kKG; ++t) {
+    const float x = bf2f(sK[t * kD + d]);
+    bad |= !isfinite(x);
+    const uint32_t k = fkey(x);
+    kmin = min(kmin, k);
+    kmax = max(kmax, k);
+  }
+  lo = unkey(kmin);
+  hi = unkey(kmax);
+}
+
+// Codes of one Key channel, packed LSB first along tokens into dst (16-byte
+// aligned, 128*bits/8 bytes).
+__device__ __forceinline__ void pack_channel(const uint16_t* sK, int d,
+                                             const Params& p, int bits,
+                                             uint8_t* dst) {
+  const int top = (1 << bits) - 1;
+  const int per = 32 / bits;
+  uint32_t* w = reinterpret_cast<uint32_t*>(dst);
+  for (int wi = 0; wi < kKG / per; ++wi) {
+    uint32_t acc = 0;
+    for (int i = 0; i < per; ++i) {
+      const int t = wi * per + i;
+      acc |= code_of(bf2f(sK[t * kD + d]), p, top) << (bits * i);
+    }
+    w[wi] = acc;
+  }
+}
+
+// Value groups: one warp per (token, 32-channel group); lane = channel.
+template <int VB>
+__device__ __forceinline__ unsigned value_groups(const QuantArgs& a,
+                                                 const uint16_t* sV,
+                                                 uint8_t* rec, int warp0,
+                                                 int nwarps) {
+  constexpr int top = (1 << VB) - 1;
+  constexpr int per = 32 / VB;  // lanes per 32-bit code word
+  const int lane = threadIdx.x & 31;
+  const int warp = (threadIdx.x >> 5) - warp0;
+  uint8_t* vcodes = rec + a.lay.v_codes;
+  float* vscale = reinterpret_cast<float*>(rec + a.lay.v_scale);
+  uint16_t* vmin = reinterpret_cast<uint16_t*>(rec + a.lay.v_min);
+  unsigned flags = 0;
+  for (int task = warp; task < kKG * kVGroups; task += nwarps) {
+    const int t = task / kVGroups;
+    const int j = task % kVGroups;
+    const float x = bf2f(sV[t * kD + j * kVG + lane]);
+    const bool bad = __any_sync(kFull, !isfinite(x));
+    const uint32_t k = fkey(x);
+    const float lo = unkey(__reduce_min_sync(kFull, k));
+    const float hi = unkey(__reduce_max_sync(kFull, k));
+    const Params p = group_params(lo, hi, top, bad);
+    const uint32_t c = code_of(x, p, top) << (VB * (lane % per));
+    uint32_t* dst = reinterpret_cast<uint32_t*>(vcodes + t * (kD * VB / 8) + j * (kVG * VB / 8));
+#pragma unroll
+    for (int wi = 0; wi < 32 / per; ++wi) {
+      const uint32_t word = __reduce_or_sync(kFull, (lane / per == wi) ? c : 0u);
+      if (lane == 0) dst[wi] = word;
+    }
+    if (lane == 0) {
+      vscale[t * kVGroups + j] = p.step;
+      vmin[t * kVGroups + j] = f2bf_bits(p.m);
+    }
+    flags |= p.flags;
+  }
+  return flags;
+}
+
+template <int KB, int VB>
+__global__ void __launch_bounds__(256) quantize_uniform_kernel(QuantArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* sK = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* sV = sK + kKG * kD;
+  load_tiles(a, sK, sV);
+  __syncthreads();
+
+  const int u = blockIdx.y;
+  uint8_t* rec = a.records + (static_cast<long long>(u) * a.max_groups +
+                              a.first_group + blockIdx.x) * a.rec_bytes;
+  unsigned flags = 0;
+  if (threadIdx.x < kD) {
+    // warps 0-3: one Key channel per thread
+    const int d = threadIdx.x;
+    float lo, hi;
+    bool bad;
+    channel_range(sK, d, lo, hi, bad);
+    const Params p = group_params(lo, hi, (1 << KB) - 1, bad);
+    pack_channel(sK, d, p, KB, rec + a.lay.k_codes + d * (kKG * KB / 8));
+    reinterpret_cast<float*>(rec + a.lay.k_scale)[d] = p.step;
+    reinterpret_cast<uint16_t*>(rec + a.lay.k_min)[d] = f2bf_bits(p.m);
+    flags = p.flags;
+  } else {
+    // warps 4-7: the Value groups
+    flags = value_groups<VB>(a, sV, rec, 4, 4);
+  }
+  if (flags) atomicOr(a.status, flags);
+}
+
+// Mixed keys (MixKVQ KeyQuant): per channel S_d = fl32(fl32(M - m)/3) over
+// the tile, A_d = fl32(I_d * S_d); tiers by rank (A descending, channel
+// ascending on ties): n_bf16 BF16, n_uint4 UINT4, rest UINT2.  Storage
+// order BF16, UINT4, UINT2 channels, each ascending.
+template <int VB>
+__global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* sK = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* sV = sK + kKG * kD;
+  __shared__ uint32_t sKey[kD];
+  __shared__ uint8_t sTier[kD];
+  load_tiles(a, sK, sV);
+  __syncthreads();
+
+  const int u = blockIdx.y;
+  uint8_t* rec = a.records + (static_cast<long long>(u) * a.max_groups +
+                              a.first_group + blockIdx.x) * a.rec_bytes;
+  const RecLayout& L = a.lay;
+  unsigned flags = 0;
+  if (threadIdx.x < kD) {
+    const int d = threadIdx.x;
+    float lo, hi;
+    bool bad;
+    channel_range(sK, d, lo, hi, bad);
+    float S = 0.0f;
+    if (!bad) S = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
+    const float I = a.importance[static_cast<long long>(u) * kD + d];
+    if (!isfinite(I)) flags |= KVQ_FLAG_NONFINITE;
+    if (bad) flags |= KVQ_FLAG_NONFINITE;
+    else if (!isfinite(S)) flags |= KVQ_FLAG_RANGE;
+    const float A = __fmul_rn(I, S);
+    // Rank by a total-order key (NaN, only possible on a flagged group,
+    // sorts last) so ranks are always a permutation and every slot stays
+    // inside its tier's region.
+    const uint32_t key = isnan(A) ? 0u : fkey(A);
+    sKey[d] = key;
+    asm volatile("bar.sync 1, 128;");
+    int rank = 0;
+    for (int e = 0; e < kD; ++e) {
+      const uint32_t ke = sKey[e];
+      rank += (ke > key || (ke == key && e < d)) ? 1 : 0;
+    }
+    const int tier = rank < L.nb ? KVQ_TIER_BF16
+                     : rank < L.nb + L.n4 ? KVQ_TIER_UINT4
+                                          : KVQ_TIER_UINT2;
+    sTier[d] = static_cast<uint8_t>(tier);
+    asm volatile("bar.sync 1, 128;");
+    int slot = tier == KVQ_TIER_BF16 ? 0 : tier == KVQ_TIER_UINT4 ? L.nb : L.nb + L.n4;
+    for (int e = 0; e < d; ++e) slot += (sTier[e] == tier) ? 1 : 0;
+    rec[L.perm + slot] = static_cast<uint8_t>(d);
+    if (tier == KVQ_TIER_BF16) {
+      uint16_t* raw = reinterpret_cast<uint16_t*>(rec + L.raw) + slot * kKG;
+      for (int t = 0; t < kKG; ++t) raw[t] = sK[t * kD + d];
+    } else {
+      const int bits = tier == KVQ_TIER_UINT4 ? 4 : 2;
+      const Params p = group_params(lo, hi, (1 << bits) - 1, bad);
+      flags |= p.flags;
+      if (bits == 4) {
+        const int j = slot - L.nb;
+        pack_channel(sK, d, p, 4, rec + L.c4 + j * (kKG / 2));
+        reinterpret_cast<float*>(rec + L.s4)[j] = p.step;
+        reinterpret_cast<uint16_t*>(rec + L.m4)[j] = f2bf_bits(p.m);
+      } else {
+        const int j = slot - L.nb - L.n4;
+        pack_channel(sK, d, p, 2, rec + L.c2 + j * (kKG / 4));
+        reinterpret_cast<float*>(rec + L.s2)[j] = p.step;
+        reinterpret_cast<uint16_t*>(rec + L.m2)[j] = f2bf_bits(p.m);
+      }
+    }
+  } else {
+    flags = value_groups<VB>(a, sV, rec, 4, 4);
+  }
+  if (flags) atomicOr(a.status, flags);
+}
+
+__global__ void append_kernel(const uint4* __restrict__ k_new,
+                              const uint4* __restrict__ v_new, uint4* res_k,
+                              uint4* res_v, int r) {
+  // one (b, kv head) per block; 16 x 16 bytes per row of D bf16
+  constexpr int kRow = kD * 2 / 16;
+  const int u = blockIdx.x;
+  const int i = threadIdx.x;
+  const long long dst = (static_cast<long long>(u) * kR + r) * kRow;
+  if (i < kRow)
+    res_k[dst + i] = __ldg(k_new + static_cast<long long>(u) * kRow + i);
+  else if (i < 2 * kRow)
+    res_v[dst + i - kRow] = __ldg(v_new + static_cast<long long>(u) * kRow + i - kRow);
+}
+
+// Copy one section (bytes at offset off of every group record) of records
+// [u][g0 .. g0+n) into dst [u][n][bytes].
+__global__ void gather_section_kernel(const uint8_t* __restrict__ records,
+                                      long long rec_bytes, int max_groups,
+                                      int off, int bytes, uint8_t* dst, int n) {
+  const int g = blockIdx.x;
+  const int u = blockIdx.y;
+  const uint8_t* src = records + (static_cast<long long>(u) * max_groups + g) * rec_bytes + off;
+  uint8_t* out = dst + (static_cast<long long>(u) * n + g) * bytes;
+  const bool vec = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(out) |
+                     static_cast<uintptr_t>(bytes)) & 15) == 0;
+  if (vec) {
+    for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x)
+      reinterpret_cast<uint4*>(out)[i] = reinterpret_cast<const uint4*>(src)[i];
+  } else {
+    for (int i = threadIdx.x; i < bytes; i += blockDim.x) out[i] = src[i];
+  }
+}
+
+cudaError_t gather(const kvq_cache* c, int off, int bytes, void* dst,
+                   cudaStream_t s) {
+  const int n = c->t_q / kKG;
+  const int units = c->cfg.batch * c->cfg.kv_heads;
+  if (n == 0 || bytes == 0) return cudaSuccess;
+  gather_section_kernel<<<dim3(n, units), 128, 0, s>>>(
+      c->records, c->lay.bytes, c->max_groups, off, bytes,
+      static_cast<uint8_t*>(dst), n);
+  return cudaGetLastError();
+}
+
+constexpr int kQuantSmem = 2 * kKG * kD * 2;  // K and V tiles, 64 KB
+
+template <typename K>
+cudaError_t set_smem(K kernel) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kQuantSmem);
+}
+
+}  // namespace
+
+cudaError_t launch_append(const kvq_cache* c, const kvq_bf16* k_new,
+                          const kvq_bf16* v_new, cudaStream_t s) {
+  const int units = c->cfg.batch * c->cfg.kv_heads;
+  append_kernel<<<units, 32, 0, s>>>(reinterpret_cast<const uint4*>(k_new),
+                                     reinterpret_cast<const uint4*>(v_new),
+                                     reinterpret_cast<uint4*>(c->res_k),
+                                     reinterpret_cast<uint4*>(c->res_v), c->r);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
+                            int first_group, const float* importance,
+                            cudaStream_t s) {
+  if (n_groups == 0) return cudaSuccess;
+  QuantArgs a;
+  a.src = src;
+  a.records = c->records;
+  a.rec_bytes = c->lay.bytes;
+  a.max_groups = c->max_groups;
+  a.first_group = first_group;
+  a.lay = c->lay;
+  a.importance = importance;
+  a.status = c->status;
+  const dim3 grid(n_groups, c->cfg.batch * c->cfg.kv_heads);
+  const int kb = c->cfg.k_bits, vb = c->cfg.v_bits;
+  cudaError_t e = cudaSuccess;
+#define KVQ_LAUNCH(KERNEL)                                   \
+  do {                                                       \
+    e = set_smem(KERNEL);                                    \
+    if (e != cudaSuccess) return e;                          \
+    KERNEL<<<grid, 256, kQuantSmem, s>>>(a);                 \
+  } while (0)
+  if (c->cfg.k_mode == KVQ_K_MIXED) {
+    if (vb == 2) KVQ_LAUNCH(quantize_mixed_kernel<2>);
+    else KVQ_LAUNCH(quantize_mixed_kernel<4>);
+  } else if (kb == 2 && vb == 2) {
+    KVQ_LAUNCH((quantize_uniform_kernel<2, 2>));
+  } else if (kb == 2 && vb == 4) {
+    KVQ_LAUNCH((quantize_uniform_kernel<2, 4>));
+  } else if (kb == 4 && vb == 2) {
+    KVQ_LAUNCH((quantize_uniform_kernel<4, 2>));
+  } else {
+    KVQ_LAUNCH((quantize_uniform_kernel<4, 4>));
+  }
+#undef KVQ_LAUNCH
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual_tail(const kvq_cache* c, const kvq_bf16* k,
+                                 const kvq_bf16* v, int L, int first,
+                                 int count, cudaStream_t s) {
+  if (count == 0) return cudaSuccess;
+  const int units = c->cfg.batch * c->cfg.kv_heads;
+  const size_t row = static_cast<size_t>(kD) * sizeof(kvq_bf16);
+  cudaError_t e = cudaMemcpy2DAsync(c->res_k, kR * row, k + static_cast<size_t>(first) * kD,
+                                    static_cast<size_t>(L) * row, count * row, units,
+                                    cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return e;
+  return cudaMemcpy2DAsync(c->res_v, kR * row, v + static_cast<size_t>(first) * kD,
+                           static_cast<size_t>(L) * row, count * row, units,
+                           cudaMemcpyDeviceToDevice, s);
+}
+
+cudaError_t launch_export_k_uniform(const kvq_cache* c, uint8_t* codes,
+                                    kvq_bf16* kmin, float* kscale,
+                                    cudaStream_t s) {
+  const RecLayout& L = c->lay;
+  cudaError_t e = gather(c, L.k_codes, kD * kKG * L.kb / 8, codes, s);
+  if (e == cudaSuccess) e = gather(c, L.k_min, kD * 2, kmin, s);
+  if (e == cudaSuccess) e = gather(c, L.k_scale, kD * 4, kscale, s);
+  return e;
+}
+
+cudaError_t launch_export_v(const kvq_cache* c, uint8_t* codes, kvq_bf16* vmin,
+                            float* vscale, cudaStream_t s) {
+  const RecLayout& L = c->lay;
+  cudaError_t e = gather(c, L.v_codes, kKG * kD * L.vb / 8, codes, s);
+  if (e == cudaSuccess) e = gather(c, L.v_min, kKG * kVGroups * 2, vmin, s);
+  if (e == cudaSuccess) e = gather(c, L.v_scale, kKG * kVGroups * 4, vscale, s);
+  return e;
+}
+
+cudaError_t launch_export_k_mixed(const kvq_cache* c, uint8_t* perm,
+                                  kvq_bf16* raw, uint8_t* c4, kvq_bf16* m4,
+                                  float* s4, uint8_t* c2, kvq_bf16* m2,
+                                  float* s2, cudaStream_t s) {
+  const RecLayout& L = c->lay;
+  cudaError_t e = gather(c, L.perm, kD, perm, s);
+  if (e == cudaSuccess) e = gather(c, L.raw, L.nb * kKG * 2, raw, s);
+  if (e == cudaSuccess) e = gather(c, L.c4, L.n4 * kKG / 2, c4, s);
+  if (e == cudaSuccess) e = gather(c, L.m4, L.n4 * 2, m4, s);
+  if (e == cudaSuccess) e = gather(c, L.s4, L.n4 * 4, s4, s);
+  if (e == cudaSuccess) e = gather(c, L.c2, L.n2 * kKG / 4, c2, s);
+  if (e == cudaSuccess) e = gather(c, L.m2, L.n2 * 2, m2, s);
+  if (e == cudaSuccess) e = gather(c, L.s2, L.n2 * 4, s2, s);
+  return e;
+}
+
+}  // namespace kvq

@@ -1,0 +1,257 @@
+/*
+ * kvq.h — C ABI of libkvq.so: low-bit KV-cache quantization (KIVI-style
+ * asymmetric min–max codes, MixKVQ query-aware mixed-precision keys) and
+ * fused decode attention over the packed cache, for one GB300 GPU (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *  - "KIVI: KV cache axes" article: §1 decode attention s = qK^T/sqrt(D),
+ *    p = softmax(s), o = pV; §2 group contract m = min, step =
+ *    (max - m)/(2^b - 1), c = RNE((x - m)/step), x^ = m + step*c; §3 Key
+ *    groups per channel over consecutive tokens, Value groups per token over
+ *    consecutive channels; §4 residual buffer sealed in whole groups; §6 one
+ *    global softmax over quantized history and residual; §7 byte accounting.
+ *  - "MixKVQ: Query-Aware Mixed-Precision KV Cache Quantization for
+ *    Long-Context Reasoning": salience A_d = I_d * S_d, three tiers
+ *    BF16/UINT4/UINT2, residual R = 128 with lazy update, Algorithm 1
+ *    (Prefill / Decoding / KeyQuant), GQA aggregation.
+ *  - "PN-Mix" reproduction notes: Eq. 2 (clipped codes, constant-group
+ *    branch), App. G (Key codes packed along tokens), the cache API shape
+ *    (from_prefill / append / attention / storage; [batch, heads, tokens,
+ *    head_dim]; query heads ordered by GQA group).
+ *
+ * Conventions for every call:
+ *  - Device pointers are caller-owned, contiguous, on the current device and
+ *    must stay valid until the stream work that uses them has finished.
+ *  - Every call that takes a stream only enqueues work on it (asynchronous);
+ *    none synchronizes except kvq_cache_status.
+ *  - bf16 tensors are passed as kvq_bf16 (raw bf16 bit patterns).
+ *  - Query head h reads KV head h / (Hq / Hkv) (heads ordered by GQA group).
+ *  - Return value: KVQ_OK or one KVQ_ERR_* code; on error nothing was
+ *    enqueued and the cache state is unchanged.  Data-dependent problems
+ *    (non-finite input, an unrepresentable step) cannot be seen on the host
+ *    without a sync; kernels record them as sticky flags in a device status
+ *    word read by kvq_cache_status.
+ *  - There is no CPU fallback: every computation runs in this library's
+ *    CUDA kernels.
+ *  - A kvq_cache handle is not thread-safe.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kvq_bf16; /* raw bf16 bit pattern */
+
+/* Fixed geometry of this implementation. */
+#define KVQ_HEAD_DIM 128     /* D */
+#define KVQ_K_GROUP 128      /* Key group: tokens per channel group        */
+#define KVQ_V_GROUP 32       /* Value group: channels per token group      */
+#define KVQ_RESIDUAL 128     /* R: residual capacity = flush granularity   */
+
+/* Return codes. */
+enum {
+  KVQ_OK = 0,
+  KVQ_ERR_ARG = 1,            /* NULL pointer, bad enum, negative size      */
+  KVQ_ERR_SHAPE = 2,          /* unsupported geometry (D, bits, heads)      */
+  KVQ_ERR_CAPACITY = 3,       /* quantized history would exceed max_tokens  */
+  KVQ_ERR_RESIDUAL_FULL = 4,  /* append with 128 residual tokens: flush     */
+  KVQ_ERR_RESIDUAL_NOT_FULL = 5, /* flush with fewer than 128 tokens        */
+  KVQ_ERR_EMPTY = 6,          /* attention over a cache with no tokens      */
+  KVQ_ERR_NOT_EMPTY = 7,      /* prefill into a cache that holds tokens     */
+  KVQ_ERR_CUDA = 8,           /* a CUDA call or launch failed               */
+  KVQ_ERR_WORKSPACE = 9,      /* workspace NULL or smaller than required    */
+  KVQ_ERR_MODE = 10           /* call does not match the cache's key mode   */
+};
+
+/* Sticky device status flags (OR-ed), read by kvq_cache_status. */
+enum {
+  KVQ_FLAG_NONFINITE = 1,     /* a group held a NaN or infinity             */
+  KVQ_FLAG_RANGE = 2          /* (max - min)/(2^b - 1) not positive finite  */
+};
+
+/* Key storage mode. */
+enum { KVQ_K_UNIFORM = 0, KVQ_K_MIXED = 1 };
+
+/* Channel tier ids (MixKVQ three-tier strategy). */
+enum { KVQ_TIER_BF16 = 0, KVQ_TIER_UINT4 = 1, KVQ_TIER_UINT2 = 2 };
+
+/* Tier selection rule for kvq_channel_saliency. */
+enum { KVQ_TIERS_RANK = 0, KVQ_TIERS_THRESHOLD = 1 };
+
+typedef struct kvq_config {
+  int batch;       /* B >= 1                                                */
+  int kv_heads;    /* Hkv >= 1                                              */
+  int head_dim;    /* D; must be KVQ_HEAD_DIM                               */
+  int max_tokens;  /* capacity of the quantized history; multiple of 128    */
+  int k_bits;      /* 2 or 4 (KVQ_K_UNIFORM); ignored for KVQ_K_MIXED       */
+  int v_bits;      /* 2 or 4                                                */
+  int k_mode;      /* KVQ_K_UNIFORM or KVQ_K_MIXED                          */
+  int n_bf16;      /* KVQ_K_MIXED: BF16-tier channels per key group         */
+  int n_uint4;     /* KVQ_K_MIXED: UINT4-tier channels per key group; the
+                      remaining D - n_bf16 - n_uint4 channels are UINT2     */
+} kvq_config;
+
+typedef struct kvq_tier_spec {
+  int mode;         /* KVQ_TIERS_RANK or KVQ_TIERS_THRESHOLD                */
+  int n_bf16;       /* RANK: channels with the largest A_d kept BF16        */
+  int n_uint4;      /* RANK: the next channels stored UINT4                 */
+  float tau_bf16;   /* THRESHOLD: A_d > tau_bf16 -> BF16                    */
+  float tau_uint4;  /* THRESHOLD: tau_uint4 < A_d <= tau_bf16 -> UINT4      */
+} kvq_tier_spec;
+
+typedef struct kvq_cache kvq_cache; /* opaque */
+
+/*
+ * Device bytes one cache needs: the packed history (per (batch row, KV
+ * head), max_tokens/128 group records of codes plus per-group origins
+ * (bf16) and steps (fp32)), the bf16 residual windows [B][Hkv][128][D] for
+ * K and V, and the status word.  KIVI article §7 gives the accounting.
+ * Returns 0 for an invalid config.
+ */
+size_t kvq_cache_bytes(const kvq_config* cfg);
+
+/*
+ * Create a cache.  dev_buf: NULL -> the library allocates kvq_cache_bytes
+ * with cudaMallocAsync on s and frees it in kvq_cache_free; else a caller
+ * buffer of buf_bytes >= kvq_cache_bytes (256-byte aligned), which the
+ * caller keeps alive and frees after kvq_cache_free.  The cache starts
+ * empty (no quantized tokens, empty residual, status 0).
+ * Errors: ARG, SHAPE, CAPACITY (buf too small), CUDA.
+ */
+int kvq_cache_alloc(const kvq_config* cfg, void* dev_buf, size_t buf_bytes,
+                    cudaStream_t s, kvq_cache** out);
+int kvq_cache_free(kvq_cache* cache, cudaStream_t s);
+
+/* Host-side lengths: quantized history tokens and residual tokens. */
+int kvq_cache_lengths(const kvq_cache* cache, int* quantized_tokens,
+                      int* residual_tokens);
+
+/* Empty the cache (lengths to 0, status word cleared on s). */
+int kvq_cache_reset(kvq_cache* cache, cudaStream_t s);
+
+/*
+ * MixKVQ Algorithm 1, Decoding, first step: append one token's key and
+ * value (k_new, v_new: bf16 [B][Hkv][D]) to residual slot r; r += 1.
+ * Errors: ARG, RESIDUAL_FULL (r == 128: call kvq_flush_group first), CUDA.
+ */
+int kvq_append_residual(kvq_cache* cache, const kvq_bf16* k_new,
+                        const kvq_bf16* v_new, cudaStream_t s);
+
+/*
+ * MixKVQ Algorithm 1, Decoding, "if len(X_K_r) == R": quantize the full
+ * residual window as one Key group per (batch row, KV head, channel) over
+ * its 128 tokens and one Value group per (token, 32 channels), append it to
+ * the packed history and empty the residual.  KIVI article §2 contract,
+ * PN-Mix Eq. 2 clipping and constant-group branch (step stored 0).
+ * KVQ_K_MIXED: importance is I_d, fp32 [B][Hkv][D] (device), and the group's
+ * tiers come from A_d = I_d * S_d with S_d at 2 bits, ranked by the cache's
+ * n_bf16/n_uint4 (KeyQuant = OutlierReserve + GroupQuant); uniform caches
+ * take importance = NULL.
+ * Errors: ARG, MODE, RESIDUAL_NOT_FULL, CAPACITY, CUDA.  Flags: NONFINITE,
+ * RANGE.
+ */
+int kvq_flush_group(kvq_cache* cache, const float* importance, cudaStream_t s);
+
+/*
+ * MixKVQ Algorithm 1, Prefill: k, v bf16 [B][Hkv][L][D]; the first
+ * L - (L mod 128) tokens are quantized into floor(L/128) groups exactly as
+ * kvq_flush_group does, the last L mod 128 tokens go to the residual.
+ * importance: as for kvq_flush_group.  L = 0 is allowed (no-op).
+ * Errors: ARG, MODE, NOT_EMPTY, CAPACITY, CUDA.  Flags: NONFINITE, RANGE.
+ */
+int kvq_quantize_prefill(kvq_cache* cache, const kvq_bf16* k,
+                         const kvq_bf16* v, int L, const float* importance,
+                         cudaStream_t s);
+
+/*
+ * Workspace bytes kvq_decode_attention needs for Hq query heads at the
+ * cache's capacity (split-K partials: per query head and split, the running
+ * max, the normalizer and D accumulators, fp32).  0 on bad arguments.
+ */
+size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int Hq);
+
+/*
+ * Fused decode attention (KIVI article §1 and §6; MixKVQ Algorithm 1 last
+ * three lines): for each (b, h), s_t = q·k^_t / sqrt(D) over the
+ * dequantized history followed by the residual tokens, p = softmax over all
+ * of them together, o = sum_t p_t v^_t.  q: bf16 [B][Hq][D], Hq a multiple
+ * of Hkv (at most 8 query heads per KV head); out: fp32 [B][Hq][D].
+ * ws: device scratch of >= kvq_decode_workspace_bytes(cache, Hq), not
+ * aliased with any argument; its contents are overwritten.
+ * Errors: ARG, SHAPE, EMPTY, WORKSPACE, CUDA.
+ */
+int kvq_decode_attention(const kvq_cache* cache, const kvq_bf16* q, int Hq,
+                         float* out, void* ws, size_t ws_bytes, cudaStream_t s);
+
+/*
+ * Unquantized comparator: the same decode attention over plain bf16
+ * k, v [B][Hkv][T][D] (T >= 1), same q/out/ws conventions.
+ */
+size_t kvq_decode_bf16_workspace_bytes(int B, int Hkv, int T, int Hq);
+int kvq_decode_bf16(const kvq_bf16* k, const kvq_bf16* v, int B, int Hkv,
+                    int T, const kvq_bf16* q, int Hq, float* out, void* ws,
+                    size_t ws_bytes, cudaStream_t s);
+
+/*
+ * MixKVQ salience: q_win bf16 [B][Hq][Lq][D] (query window), k_grp bf16
+ * [B][Hkv][G][D] (key group, G tokens).  Per (b, kv head, d):
+ *   I_d = (sum over tokens i ascending, then heads of the GQA group
+ *          ascending, of |Q|, in fp32) / (n_rep * Lq)
+ *   S_d = (max_t k - min_t k) / (2^sal_bits - 1)       (fp32)
+ *   A_d = I_d * S_d                                     (fp32)
+ * and tiers by spec: RANK orders channels by (A_d descending, d ascending)
+ * and gives the first n_bf16 BF16, the next n_uint4 UINT4, the rest UINT2;
+ * THRESHOLD applies A > tau_bf16 -> BF16, tau_uint4 < A <= tau_bf16 ->
+ * UINT4, else UINT2.  I_out, A_out: fp32 [B][Hkv][D]; tiers_out: uint8
+ * [B][Hkv][D]; any of the three may be NULL.
+ * Errors: ARG, SHAPE, CUDA.  Non-finite inputs leave NaN in A_out and
+ * UINT2 tiers (no cache to flag).
+ */
+int kvq_channel_saliency(const kvq_bf16* q_win, int Hq, int Lq,
+                         const kvq_bf16* k_grp, int B, int Hkv, int G,
+                         int sal_bits, const kvq_tier_spec* spec, float* I_out,
+                         float* A_out, uint8_t* tiers_out, cudaStream_t s);
+
+/* Synchronize s and return the cache's sticky KVQ_FLAG_* word. */
+int kvq_cache_status(kvq_cache* cache, cudaStream_t s, int* status);
+
+/*
+ * Canonical export of the quantized history (device destination buffers),
+ * for checking and debugging.  T = quantized tokens, n = T/128.
+ *  Key (uniform): codes uint8 [B][Hkv][n][D][128*k_bits/8] (each channel's
+ *    128 codes LSB first along tokens), kmin bf16 [B][Hkv][n][D], kscale
+ *    fp32 [B][Hkv][n][D].
+ *  Value: codes uint8 [B][Hkv][T][D*v_bits/8] (LSB first along channels),
+ *    vmin bf16 [B][Hkv][T][D/32], vscale fp32 [B][Hkv][T][D/32].
+ *  Residual: k_r, v_r bf16 [B][Hkv][r][D].
+ *  Key (mixed), per (b, kv head, group) with nb = n_bf16, n4 = n_uint4,
+ *    n2 = D - nb - n4: perm uint8 [..][D] (BF16, UINT4, UINT2 channels, each
+ *    ascending), raw bf16 [..][nb][128], c4 uint8 [..][n4][64], m4 bf16
+ *    [..][n4], s4 fp32 [..][n4], c2 uint8 [..][n2][32], m2 bf16 [..][n2],
+ *    s2 fp32 [..][n2].
+ * Errors: ARG, MODE, CUDA.
+ */
+int kvq_export_k(const kvq_cache* cache, uint8_t* codes, kvq_bf16* kmin,
+                 float* kscale, cudaStream_t s);
+int kvq_export_v(const kvq_cache* cache, uint8_t* codes, kvq_bf16* vmin,
+                 float* vscale, cudaStream_t s);
+int kvq_export_residual(const kvq_cache* cache, kvq_bf16* k_r, kvq_bf16* v_r,
+                        cudaStream_t s);
+int kvq_export_k_mixed(const kvq_cache* cache, uint8_t* perm, kvq_bf16* raw,
+                       uint8_t* c4, kvq_bf16* m4, float* s4, uint8_t* c2,
+                       kvq_bf16* m2, float* s2, cudaStream_t s);
+
+/* Human-readable name of a return code. */
+const char* kvq_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */
