@@ -50,16 +50,25 @@ __device__ __forceinline__ uint64_t load_bits(const uint8_t* p) {
   else return __ldg(reinterpret_cast<const unsigned short*>(p));
 }
 
+// Reductions over one team of TL lanes.  Teams of a warp run different
+// numbers of groups (and only one team takes the residual), so every
+// shuffle names the calling team's lanes only.
+template <int TL>
+__device__ __forceinline__ unsigned team_mask_of() {
+  return (TL == 32 ? 0xffffffffu : ((1u << TL) - 1u)) << ((threadIdx.x & 31) / TL * TL);
+}
 template <int TL>
 __device__ __forceinline__ float team_sum(float x) {
+  const unsigned m = team_mask_of<TL>();
 #pragma unroll
-  for (int o = TL / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  for (int o = TL / 2; o > 0; o >>= 1) x += __shfl_xor_sync(m, x, o);
   return x;
 }
 template <int TL>
 __device__ __forceinline__ float team_max(float x) {
+  const unsigned m = team_mask_of<TL>();
 #pragma unroll
-  for (int o = TL / 2; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  for (int o = TL / 2; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(m, x, o));
   return x;
 }
 
@@ -229,8 +238,7 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
   const int u = blockIdx.y;
   const int b = u / a.Hkv, kvh = u % a.Hkv;
   const int team = threadIdx.x / TL, li = threadIdx.x % TL;
-  const unsigned team_mask = (TL == 32 ? 0xffffffffu : ((1u << TL) - 1u))
-                             << ((threadIdx.x & 31) / TL * TL);
+  const unsigned team_mask = team_mask_of<TL>();
   for (int i = threadIdx.x; i < NREP * kD; i += blockDim.x) {
     const int h = i / kD, d = i % kD;
     s_q[i] = bf2f(a.q[(static_cast<long long>(b) * a.Hq + kvh * NREP + h) * kD + d]) * a.qscale;
@@ -353,8 +361,7 @@ __global__ void __launch_bounds__(128) decode_bf16_kernel(Bf16Args a, DecodeArgs
   const int u = blockIdx.y;
   const int b = u / a.Hkv, kvh = u % a.Hkv;
   const int team = threadIdx.x / TL, li = threadIdx.x % TL;
-  const unsigned team_mask = (TL == 32 ? 0xffffffffu : ((1u << TL) - 1u))
-                             << ((threadIdx.x & 31) / TL * TL);
+  const unsigned team_mask = team_mask_of<TL>();
   for (int i = threadIdx.x; i < NREP * kD; i += blockDim.x) {
     const int h = i / kD, d = i % kD;
     s_q[i] = bf2f(a.q[(static_cast<long long>(b) * a.Hq + kvh * NREP + h) * kD + d]) * a.qscale;
