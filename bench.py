@@ -75,7 +75,7 @@ class ClockSampler(threading.Thread):
         self.samples = []
         self.reasons = 0
         self.max_mhz = None
-        self._stop = threading.Event()
+        self._halt = threading.Event()
         self.ok = False
         try:
             self.nv = ctypes.CDLL("libnvidia-ml.so.1")
@@ -103,7 +103,7 @@ class ClockSampler(threading.Thread):
         rs = ctypes.c_ulonglong()
         getr = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
-        while not self._stop.is_set():
+        while not self._halt.is_set():
             if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:
                 self.samples.append(mhz.value)
             if getr(self.h, ctypes.byref(rs)) == 0:
@@ -111,7 +111,7 @@ class ClockSampler(threading.Thread):
             time.sleep(self.period)
 
     def stop(self):
-        self._stop.set()
+        self._halt.set()
         self.join(timeout=1.0)
 
     def summary(self):

@@ -263,20 +263,25 @@ int kvq_cache_status(kvq_cache* c, cudaStream_t s, int* status) {
 
 int kvq_export_k(const kvq_cache* c, uint8_t* codes, kvq_bf16* kmin, float* kscale,
                  cudaStream_t s) {
-  if (!c || !codes || !kmin || !kscale) return KVQ_ERR_ARG;
+  if (!c) return KVQ_ERR_ARG;
   if (c->cfg.k_mode != KVQ_K_UNIFORM) return KVQ_ERR_MODE;
+  if (c->t_q == 0) return KVQ_OK;   // nothing to copy; empty buffers may be NULL
+  if (!codes || !kmin || !kscale) return KVQ_ERR_ARG;
   return cuda_status(launch_export_k_uniform(c, codes, kmin, kscale, s));
 }
 
 int kvq_export_v(const kvq_cache* c, uint8_t* codes, kvq_bf16* vmin, float* vscale,
                  cudaStream_t s) {
-  if (!c || !codes || !vmin || !vscale) return KVQ_ERR_ARG;
+  if (!c) return KVQ_ERR_ARG;
+  if (c->t_q == 0) return KVQ_OK;
+  if (!codes || !vmin || !vscale) return KVQ_ERR_ARG;
   return cuda_status(launch_export_v(c, codes, vmin, vscale, s));
 }
 
 int kvq_export_residual(const kvq_cache* c, kvq_bf16* k_r, kvq_bf16* v_r, cudaStream_t s) {
-  if (!c || !k_r || !v_r) return KVQ_ERR_ARG;
-  if (c->r == 0) return KVQ_OK;
+  if (!c) return KVQ_ERR_ARG;
+  if (c->r == 0) return KVQ_OK;   // nothing to copy; empty buffers may be NULL
+  if (!k_r || !v_r) return KVQ_ERR_ARG;
   const int units = c->cfg.batch * c->cfg.kv_heads;
   const size_t row = kD * sizeof(kvq_bf16);
   cudaError_t e = cudaMemcpy2DAsync(k_r, c->r * row, c->res_k, kR * row, c->r * row, units,
@@ -290,8 +295,13 @@ int kvq_export_residual(const kvq_cache* c, kvq_bf16* k_r, kvq_bf16* v_r, cudaSt
 int kvq_export_k_mixed(const kvq_cache* c, uint8_t* perm, kvq_bf16* raw, uint8_t* c4,
                        kvq_bf16* m4, float* s4, uint8_t* c2, kvq_bf16* m2, float* s2,
                        cudaStream_t s) {
-  if (!c || !perm || !raw || !c4 || !m4 || !s4 || !c2 || !m2 || !s2) return KVQ_ERR_ARG;
+  if (!c) return KVQ_ERR_ARG;
   if (c->cfg.k_mode != KVQ_K_MIXED) return KVQ_ERR_MODE;
+  if (c->t_q == 0) return KVQ_OK;
+  // a tier with no channels has an empty (possibly NULL) destination
+  const RecLayout& L = c->lay;
+  if (!perm || (L.nb && !raw) || (L.n4 && (!c4 || !m4 || !s4)) || (L.n2 && (!c2 || !m2 || !s2)))
+    return KVQ_ERR_ARG;
   return cuda_status(launch_export_k_mixed(c, perm, raw, c4, m4, s4, c2, m2, s2, s));
 }
 

@@ -230,12 +230,13 @@ int kvq_cache_status(kvq_cache* cache, cudaStream_t s, int* status);
  *    fp32 [B][Hkv][n][D].
  *  Value: codes uint8 [B][Hkv][T][D*v_bits/8] (LSB first along channels),
  *    vmin bf16 [B][Hkv][T][D/32], vscale fp32 [B][Hkv][T][D/32].
- *  Residual: k_r, v_r bf16 [B][Hkv][r][D].
+ *  Residual: k_r, v_r bf16 [B][Hkv][r][D] (may be NULL when r = 0).
  *  Key (mixed), per (b, kv head, group) with nb = n_bf16, n4 = n_uint4,
  *    n2 = D - nb - n4: perm uint8 [..][D] (BF16, UINT4, UINT2 channels, each
  *    ascending), raw bf16 [..][nb][128], c4 uint8 [..][n4][64], m4 bf16
  *    [..][n4], s4 fp32 [..][n4], c2 uint8 [..][n2][32], m2 bf16 [..][n2],
  *    s2 fp32 [..][n2].
+ * With no quantized tokens nothing is copied and the buffers may be NULL.
  * Errors: ARG, MODE, CUDA.
  */
 int kvq_export_k(const kvq_cache* cache, uint8_t* codes, kvq_bf16* kmin,
