@@ -308,6 +308,9 @@ def run_ours(args, rank, world):
         return launches + 2, nb + attention_bytes(w, tq, r), attention_bytes(w, tq, r)
 
     prefill()
+    if args.no_bf16 and args.no_e2e:       # keep device memory small (profiling)
+        del Kall, Vall
+        torch.cuda.empty_cache()
     for i in range(W):
         step(i)
     torch.cuda.synchronize()
