@@ -191,6 +191,31 @@ int kvq_decode_attention(const kvq_cache* cache, const kvq_bf16* q, int Hq,
                          float* out, void* ws, size_t ws_bytes, cudaStream_t s);
 
 /*
+ * Decode attention without any allocation (this entry point has no
+ * counterpart on the pages; it exists for callers that cannot allocate).
+ * Same inputs, output and errors as kvq_decode_attention, but the split-K
+ * workspace is a fixed array of KVQ_STATIC_WORKSPACE_BYTES inside the
+ * library's device memory instead of a caller buffer, and the call makes no
+ * cudaMalloc, cudaFree or other allocating call.  It is meant for callers
+ * that cannot allocate device memory when they decode: servers that reserve
+ * all memory at start-up and forbid allocation on the request path, plain C
+ * hosts without an allocator, replayed launch sequences.
+ *  - Every GPU that loads the library holds the array until process exit.
+ *  - The first call on a device looks the array's device address up once
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array, so calls whose work overlaps on the GPU
+ *    (other streams, other threads) race and corrupt each other's results;
+ *    serialize them.  Each call rewrites every workspace entry it reads.
+ *  - The split count is reduced to fit the array.  B*Hq*(D+2)*4 bytes must
+ *    fit (B*Hq <= 16131 query rows); beyond that it returns
+ *    KVQ_ERR_WORKSPACE.
+ */
+#define KVQ_STATIC_WORKSPACE_BYTES (8u << 20) /* 8 MiB per GPU */
+int kvq_decode_attention_static(const kvq_cache* cache, const kvq_bf16* q,
+                                int Hq, float* out, cudaStream_t s);
+
+/*
  * Unquantized comparator: the same decode attention over plain bf16
  * k, v [B][Hkv][T][D] (T >= 1), same q/out/ws conventions.
  */
