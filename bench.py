@@ -133,7 +133,7 @@ def measured_peak():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("decode.cu", "kvq_internal.h"):
+    for name in ("decode_mma.cu", "frag_layout.h", "kvq_internal.h"):
         with open(os.path.join(ROOT, "bit_kv_cache_kvq_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -191,7 +191,8 @@ int kvq_quantize_prefill(kvq_cache* c, const kvq_bf16* k, const kvq_bf16* v, int
 
 size_t kvq_decode_workspace_bytes(const kvq_cache* c, int Hq) {
   if (!c || Hq < 1 || Hq % c->cfg.kv_heads) return 0;
-  return decode_ws_bytes(static_cast<long long>(c->cfg.batch) * Hq, kMaxSplits);
+  return mma_ws_bytes(c->num_sms, c->cfg.batch, c->cfg.kv_heads, Hq, c->max_groups,
+                      c->lay.bytes);
 }
 
 static bool valid_rep(int Hq, int Hkv) {
@@ -208,9 +209,11 @@ int kvq_decode_attention(const kvq_cache* c, const kvq_bf16* q, int Hq, float* o
   if (c->t_q + c->r == 0) return KVQ_ERR_EMPTY;
   if (!ws || ws_bytes < kvq_decode_workspace_bytes(c, Hq) || !aligned16(ws))
     return KVQ_ERR_WORKSPACE;
-  const int units = c->cfg.batch * c->cfg.kv_heads;
-  const int n_split = choose_splits(c->num_sms, units, c->t_q / kKG);
-  return cuda_status(launch_decode(c, q, Hq, out, static_cast<float*>(ws), n_split, s));
+  MmaPlan plan;
+  if (!mma_plan(c->num_sms, c->cfg.batch * c->cfg.kv_heads, Hq / c->cfg.kv_heads,
+                c->t_q / kKG, c->r, c->lay.bytes, ws_bytes, &plan))
+    return KVQ_ERR_WORKSPACE;
+  return cuda_status(launch_decode_mma(c, q, Hq, out, static_cast<float*>(ws), plan, s));
 }
 
 size_t kvq_decode_bf16_workspace_bytes(int B, int Hkv, int T, int Hq) {

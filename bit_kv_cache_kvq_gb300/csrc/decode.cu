@@ -1,5 +1,5 @@
-// Split-K ("flash-decoding") decode attention over the packed cache and the
-// bf16 residual, plus the combine kernel and the unquantized bf16 comparator.
+// Unquantized bf16 comparator: split-K ("flash-decoding") decode attention
+// over plain bf16 K, V on CUDA cores, plus its combine kernel.
 //
 // Math ("KIVI: KV cache axes" §1 and §6; MixKVQ Algorithm 1): for query
 // head h of KV head kvh, s_t = q·k^_t / sqrt(D) over the dequantized
@@ -7,20 +7,13 @@
 // o = sum_t p_t v^_t.  Scores are kept in log2 units (q pre-scaled by
 // log2(e)/sqrt(D)) so p = exp2(s - max).
 //
-// Key dequantization is folded into the query (per 128-token group g and
-// channel d, k^ = m_gd + step_gd * c):  q·k^_t = sum_d q_d m_gd  +
-// sum_d (q_d step_gd) c_td, so the inner loop is one FMA per code and head.
-// Value dequantization is folded into the probabilities (per token t and
-// 32-channel group j): sum_t p_t v^_td = sum_t p_t m_tj + sum_t (p_t step_tj) c_td.
-//
 // Work split: grid (n_split, B*Hkv).  A CTA streams a contiguous range of
-// group records of one (b, kv head) for all n_rep query heads that share
-// it (GQA: each packed byte is read once).  Inside the CTA, teams of TL
-// lanes each own whole groups and keep their own online-softmax state, so
-// the loop needs no CTA-wide barrier; teams merge once at the end.  The
-// last split also takes the residual tokens.  A second kernel merges the
-// splits with the exact log-sum-exp rule (KIVI §6: blockwise softmax is
-// allowed when the blocks share one global normalization).
+// 128-token blocks of one (b, kv head) for all n_rep query heads that share
+// it (GQA: each byte is read once).  Inside the CTA, teams of TL lanes each
+// own whole blocks and keep their own online-softmax state; teams merge
+// once at the end.  A second kernel merges the splits with the exact
+// log-sum-exp rule (KIVI §6: blockwise softmax is allowed when the blocks
+// share one global normalization).
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -41,13 +34,6 @@ __device__ __forceinline__ void bf2x8(const uint4& w, float* f) {
     f[2 * i] = __uint_as_float(v[i] << 16);
     f[2 * i + 1] = __uint_as_float(v[i] & 0xffff0000u);
   }
-}
-
-template <int BYTES>
-__device__ __forceinline__ uint64_t load_bits(const uint8_t* p) {
-  if constexpr (BYTES == 8) return __ldg(reinterpret_cast<const unsigned long long*>(p));
-  else if constexpr (BYTES == 4) return __ldg(reinterpret_cast<const unsigned int*>(p));
-  else return __ldg(reinterpret_cast<const unsigned short*>(p));
 }
 
 // Reductions over one team of TL lanes.  Teams of a warp run different
@@ -72,20 +58,11 @@ __device__ __forceinline__ float team_max(float x) {
   return x;
 }
 
+// Fields the partial writer needs.
 struct DecodeArgs {
-  const uint8_t* records;
-  long long rec_bytes;
-  int max_groups;
-  RecLayout lay;
-  int n_groups;           // quantized groups (history)
-  int r;                  // residual tokens
-  const uint16_t* res_k;  // [units][128][D]
-  const uint16_t* res_v;
-  const uint16_t* q;      // [B][Hq][D]
   int Hkv, Hq;
-  int n_split, gps;       // splits, groups per split
+  int n_split;
   float* ws;              // o [rows][n_split][D], then (m, l) [rows][n_split][2]
-  float qscale;           // log2(e) / sqrt(D)
 };
 
 template <int NREP>
@@ -178,162 +155,6 @@ __device__ void write_partial(const DecodeArgs& a, State& st, float* s_o,
       ws_ml[(row * a.n_split + split) * 2 + 1] = l;
     }
   }
-}
-
-// Residual tokens (bf16), processed by one team of the last split.
-template <int NREP, int TL, int CPT, typename State>
-__device__ void residual_block(const DecodeArgs& a, State& st, const float* s_q,
-                               float* s_p, int u, int li, unsigned team_mask) {
-  float s[CPT][NREP];
-#pragma unroll
-  for (int i = 0; i < CPT; ++i) {
-    const int t = li * CPT + i;
-#pragma unroll
-    for (int h = 0; h < NREP; ++h) s[i][h] = -INFINITY;
-    if (t < a.r) {
-      const uint4* row = reinterpret_cast<const uint4*>(a.res_k + (static_cast<long long>(u) * kR + t) * kD);
-      float acc[NREP];
-#pragma unroll
-      for (int h = 0; h < NREP; ++h) acc[h] = 0.0f;
-      for (int dc = 0; dc < kD / 8; ++dc) {
-        float f[8];
-        bf2x8(__ldg(row + dc), f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-#pragma unroll
-          for (int h = 0; h < NREP; ++h) acc[h] = fmaf(s_q[h * kD + dc * 8 + e], f[e], acc[h]);
-      }
-#pragma unroll
-      for (int h = 0; h < NREP; ++h) s[i][h] = acc[h];
-    }
-  }
-  st.template absorb<TL>(s, s_p, li);
-  __syncwarp(team_mask);
-  const uint16_t* vbase = a.res_v + static_cast<long long>(u) * kR * kD + li * CPT;
-  for (int t = 0; t < a.r; ++t) {
-    float vf[CPT];
-#pragma unroll
-    for (int c8 = 0; c8 < CPT / 8; ++c8)
-      bf2x8(__ldg(reinterpret_cast<const uint4*>(vbase + t * kD) + c8), vf + 8 * c8);
-#pragma unroll
-    for (int h = 0; h < NREP; ++h) {
-      const float p = s_p[h * 128 + t];
-#pragma unroll
-      for (int i = 0; i < CPT; ++i) st.o[i][h] = fmaf(p, vf[i], st.o[i][h]);
-    }
-  }
-  __syncwarp(team_mask);
-}
-
-template <int KB, int VB, int NREP>
-__global__ void __launch_bounds__(128) decode_partial_kernel(DecodeArgs a) {
-  using Shape = TeamShape<NREP>;
-  constexpr int TL = Shape::TL, CPT = Shape::CPT, TEAMS = Shape::TEAMS;
-  constexpr unsigned KMASK = (1u << KB) - 1u, VMASK = (1u << VB) - 1u;
-  __shared__ float s_q[NREP * kD];
-  __shared__ float s_p[TEAMS * NREP * 128];
-  __shared__ float s_ml[TEAMS * NREP * 2];
-
-  const int split = blockIdx.x;
-  const int u = blockIdx.y;
-  const int b = u / a.Hkv, kvh = u % a.Hkv;
-  const int team = threadIdx.x / TL, li = threadIdx.x % TL;
-  const unsigned team_mask = team_mask_of<TL>();
-  for (int i = threadIdx.x; i < NREP * kD; i += blockDim.x) {
-    const int h = i / kD, d = i % kD;
-    s_q[i] = bf2f(a.q[(static_cast<long long>(b) * a.Hq + kvh * NREP + h) * kD + d]) * a.qscale;
-  }
-  __syncthreads();
-
-  SoftState<NREP, CPT> st;
-  st.init();
-  float* p_buf = s_p + team * NREP * 128;
-  const RecLayout& L = a.lay;
-  const int g_begin = split * a.gps;
-  const int g_end = min(g_begin + a.gps, a.n_groups);
-  const int vj = li * CPT / kVG;  // this lane's value group (PV phase)
-
-  for (int g = g_begin + team; g < g_end; g += TEAMS) {
-    const uint8_t* rec = a.records + (static_cast<long long>(u) * a.max_groups + g) * a.rec_bytes;
-    const float* kscale = reinterpret_cast<const float*>(rec + L.k_scale);
-    const uint16_t* kmin = reinterpret_cast<const uint16_t*>(rec + L.k_min);
-    // bias_h = sum_d q_hd m_gd over this lane's channels, then the team
-    float bias[NREP];
-#pragma unroll
-    for (int h = 0; h < NREP; ++h) bias[h] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < CPT; ++i) {
-      const int d = li * CPT + i;
-      const float m = bf2f(__ldg(kmin + d));
-#pragma unroll
-      for (int h = 0; h < NREP; ++h) bias[h] = fmaf(s_q[h * kD + d], m, bias[h]);
-    }
-#pragma unroll
-    for (int h = 0; h < NREP; ++h) bias[h] = team_sum<TL>(bias[h]);
-
-    // scores of this lane's CPT tokens: bias + sum_d (q_hd step_gd) c_td
-    float s[CPT][NREP];
-#pragma unroll
-    for (int i = 0; i < CPT; ++i)
-#pragma unroll
-      for (int h = 0; h < NREP; ++h) s[i][h] = bias[h];
-    constexpr int KBYTES = CPT * KB / 8;
-    const uint8_t* kc = rec + L.k_codes + li * KBYTES;
-#pragma unroll 4
-    for (int d = 0; d < kD; ++d) {
-      const uint64_t w = load_bits<KBYTES>(kc + d * (kKG * KB / 8));
-      const float sc = __ldg(kscale + d);
-      float qd[NREP];
-#pragma unroll
-      for (int h = 0; h < NREP; ++h) qd[h] = s_q[h * kD + d] * sc;
-#pragma unroll
-      for (int i = 0; i < CPT; ++i) {
-        const float c = static_cast<float>(static_cast<uint32_t>(w >> (KB * i)) & KMASK);
-#pragma unroll
-        for (int h = 0; h < NREP; ++h) s[i][h] = fmaf(qd[h], c, s[i][h]);
-      }
-    }
-    st.template absorb<TL>(s, p_buf, li);
-    __syncwarp(team_mask);
-
-    // o_hd += sum_t p_ht (m_tj + step_tj c_td) for this lane's channels
-    const float* vscale = reinterpret_cast<const float*>(rec + L.v_scale);
-    const uint16_t* vmin = reinterpret_cast<const uint16_t*>(rec + L.v_min);
-    constexpr int VBYTES = CPT * VB / 8;
-    const uint8_t* vc = rec + L.v_codes + li * VBYTES;
-    float vm[NREP];
-#pragma unroll
-    for (int h = 0; h < NREP; ++h) vm[h] = 0.0f;
-#pragma unroll 4
-    for (int t = 0; t < kKG; ++t) {
-      const uint64_t w = load_bits<VBYTES>(vc + t * (kD * VB / 8));
-      const float sc = __ldg(vscale + t * kVGroups + vj);
-      const float mn = bf2f(__ldg(vmin + t * kVGroups + vj));
-      float ps[NREP];
-#pragma unroll
-      for (int h = 0; h < NREP; ++h) {
-        const float p = p_buf[h * 128 + t];
-        ps[h] = p * sc;
-        vm[h] = fmaf(p, mn, vm[h]);
-      }
-#pragma unroll
-      for (int i = 0; i < CPT; ++i) {
-        const float c = static_cast<float>(static_cast<uint32_t>(w >> (VB * i)) & VMASK);
-#pragma unroll
-        for (int h = 0; h < NREP; ++h) st.o[i][h] = fmaf(ps[h], c, st.o[i][h]);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < CPT; ++i)
-#pragma unroll
-      for (int h = 0; h < NREP; ++h) st.o[i][h] += vm[h];
-    __syncwarp(team_mask);
-  }
-
-  if (split == a.n_split - 1 && a.r > 0 && team == 0)
-    residual_block<NREP, TL, CPT>(a, st, s_q, p_buf, u, li, team_mask);
-
-  write_partial<NREP, TL, CPT, TEAMS>(a, st, s_p, s_ml, team, li, b, kvh, split);
 }
 
 // ---------------------------------------------------------------------------
@@ -444,18 +265,6 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int KB, int VB>
-cudaError_t launch_kb_vb(const DecodeArgs& a, int nrep, dim3 grid, cudaStream_t s) {
-  switch (nrep) {
-    case 1: decode_partial_kernel<KB, VB, 1><<<grid, 128, 0, s>>>(a); break;
-    case 2: decode_partial_kernel<KB, VB, 2><<<grid, 128, 0, s>>>(a); break;
-    case 4: decode_partial_kernel<KB, VB, 4><<<grid, 128, 0, s>>>(a); break;
-    case 8: decode_partial_kernel<KB, VB, 8><<<grid, 128, 0, s>>>(a); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 int choose_splits(int num_sms, int units, int n_chunks) {
@@ -470,38 +279,6 @@ cudaError_t launch_combine(const float* ws, int rows, int n_split, float* out,
                            cudaStream_t s) {
   combine_kernel<<<rows, kD, 0, s>>>(ws, rows, n_split, out);
   return cudaGetLastError();
-}
-
-cudaError_t launch_decode(const kvq_cache* c, const kvq_bf16* q, int Hq,
-                          float* out, float* ws, int n_split, cudaStream_t s) {
-  const int units = c->cfg.batch * c->cfg.kv_heads;
-  DecodeArgs a;
-  a.records = c->records;
-  a.rec_bytes = c->lay.bytes;
-  a.max_groups = c->max_groups;
-  a.lay = c->lay;
-  a.n_groups = c->t_q / kKG;
-  a.r = c->r;
-  a.res_k = c->res_k;
-  a.res_v = c->res_v;
-  a.q = q;
-  a.Hkv = c->cfg.kv_heads;
-  a.Hq = Hq;
-  a.n_split = n_split;
-  a.gps = (a.n_groups + n_split - 1) / n_split;
-  a.ws = ws;
-  a.qscale = kLog2e / sqrtf(static_cast<float>(kD));
-  const int nrep = Hq / c->cfg.kv_heads;
-  const dim3 grid(n_split, units);
-  cudaError_t e;
-  if (c->cfg.k_mode == KVQ_K_MIXED) return cudaErrorNotSupported;
-  const int kb = c->cfg.k_bits, vb = c->cfg.v_bits;
-  if (kb == 2 && vb == 2) e = launch_kb_vb<2, 2>(a, nrep, grid, s);
-  else if (kb == 2 && vb == 4) e = launch_kb_vb<2, 4>(a, nrep, grid, s);
-  else if (kb == 4 && vb == 2) e = launch_kb_vb<4, 2>(a, nrep, grid, s);
-  else e = launch_kb_vb<4, 4>(a, nrep, grid, s);
-  if (e != cudaSuccess) return e;
-  return launch_combine(ws, c->cfg.batch * Hq, n_split, out, s);
 }
 
 cudaError_t launch_decode_bf16(const kvq_bf16* k, const kvq_bf16* v, int B,

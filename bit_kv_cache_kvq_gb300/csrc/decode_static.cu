@@ -55,23 +55,20 @@ extern "C" int kvq_decode_attention_static(const kvq_cache* c, const kvq_bf16* q
   if (c->cfg.k_mode != KVQ_K_UNIFORM) return KVQ_ERR_MODE;
   if (c->t_q + c->r == 0) return KVQ_ERR_EMPTY;
 
-  // Fit the split count into the fixed array; reject what cannot fit even
-  // unsplit.
-  const long long rows = static_cast<long long>(c->cfg.batch) * Hq;
-  const size_t per_split = decode_ws_bytes(rows, 1);
-  if (per_split > static_cast<size_t>(KVQ_STATIC_WORKSPACE_BYTES)) return KVQ_ERR_WORKSPACE;
-  const int units = c->cfg.batch * c->cfg.kv_heads;
-  int n_split = choose_splits(c->num_sms, units, c->t_q / kKG);
-  const int fit = static_cast<int>(KVQ_STATIC_WORKSPACE_BYTES / per_split);
-  if (n_split > fit) n_split = fit;
+  // Plan the split so its partials fit the fixed array; reject what cannot
+  // fit with two partial slots per (batch row, KV head).
+  MmaPlan plan;
+  if (!mma_plan(c->num_sms, c->cfg.batch * c->cfg.kv_heads, n_rep, c->t_q / kKG, c->r,
+                c->lay.bytes, KVQ_STATIC_WORKSPACE_BYTES, &plan))
+    return KVQ_ERR_WORKSPACE;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   void* ws = nullptr;
   if (static_ws_address(dev, &ws) != cudaSuccess) return KVQ_ERR_CUDA;
-  // Every split writes all of its partial entries on every call, so nothing
+  // Every partial the combine reads is rewritten by this call, so nothing
   // in the array has to start at zero.
-  return launch_decode(c, q, Hq, out, static_cast<float*>(ws), n_split, s) == cudaSuccess
+  return launch_decode_mma(c, q, Hq, out, static_cast<float*>(ws), plan, s) == cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;
 }

@@ -1,0 +1,136 @@
+// Bit layout of the packed codes inside a group record.
+//
+// The decode kernel multiplies codes on tensor cores with
+// mma.sync.m16n8k16 (f16 operands, fp32 accumulators).  Its A operand comes
+// from registers, so the codes are stored in the order the A fragments need
+// them: one 16-byte load per lane yields the codes of whole fragments, and
+// one shift plus one LOP3 turns a pair of codes into an f16x2 register.
+//
+// Fragment convention (lane = 4g + t):
+//   A (16x16, row): a0 = A[g][2t,2t+1]  a1 = A[g+8][2t,2t+1]
+//                   a2 = A[g][2t+8,+9]  a3 = A[g+8][2t+8,+9]
+//   B (16x8, col):  b0 = B[2t,2t+1][g]  b1 = B[2t+8,2t+9][g]
+//   C (16x8):       c0 = C[g][2t] c1 = C[g][2t+1] c2 = C[g+8][2t] c3 = C[g+8][2t+1]
+//
+// Key codes form A of S = C_K Q' (rows = 16 tokens of M-tile mt, columns =
+// 16 channels of k-step ks); value codes form A of O^T = C_V^T P' (rows =
+// 16 channels of M-tile mc, columns = 16 tokens of k-step kt).  Both use the
+// same in-word layout; they differ in which index is "row".
+//
+// 2-bit: a 32-bit word holds two k-steps (k_local = k & 1) of one (tile,
+// lane): 8 pairs P, pair P's first code at bits 2P, second at 16 + 2P, with
+//   P(k_local, reg) = 2 * (2 * k_local + (reg & 1)) + (reg >> 1).
+// Pairs with even P decode to 1 + c/4 (a0, a1: B rows 2t, 2t+1 scaled by
+// 4), odd P to 1 + c/16 (a2, a3: B rows 2t+8, 2t+9 scaled by 16).
+// 4-bit: a word holds one k-step: pair reg at bits 4*reg and 16 + 4*reg,
+// decoded to 1 + c/16 (all B rows scaled by 16).
+//
+// Word order in the 4096 B (2-bit) / 8192 B (4-bit) code section:
+//   key  2-bit: word(mt, lane, w = ks/2)       = (mt*32 + lane)*4 + w
+//   key  4-bit: word(mt, lane, ks)             = ((mt*2 + ks/4)*32 + lane)*4 + ks%4
+//   value 2-bit: word(mc, lane, w = kt/2)      = ((w*2 + mc/4)*32 + lane)*4 + mc%4
+//   value 4-bit: word(mc, lane, kt)            = ((kt*2 + mc/4)*32 + lane)*4 + mc%4
+// so a warp reads 512 contiguous bytes per 16-byte-per-lane load.
+#pragma once
+
+#include <cstdint>
+
+namespace kvq {
+
+// Position of one code: 32-bit word index in the section and bit offset.
+struct CodePos {
+  int word;
+  int bit;
+};
+
+// (row, col) -> fragment coordinates shared by both layouts.
+__host__ __device__ inline void frag_coords(int row, int col, int& tile, int& k,
+                                            int& lane, int& reg, int& half) {
+  tile = row >> 4;
+  k = col >> 4;
+  const int r = row & 15, c = col & 15;
+  const int g = r & 7, rhi = r >> 3;
+  const int chi = c >> 3, t = (c & 7) >> 1;
+  half = c & 1;
+  lane = 4 * g + t;
+  reg = rhi + 2 * chi;
+}
+
+__host__ __device__ inline int pair_2bit(int k_local, int reg) {
+  return 2 * (2 * k_local + (reg & 1)) + (reg >> 1);
+}
+
+// Key code of token tok, channel ch (rows = tokens, columns = channels).
+__host__ __device__ inline CodePos key_code_pos(int tok, int ch, int bits) {
+  int mt, ks, lane, reg, half;
+  frag_coords(tok, ch, mt, ks, lane, reg, half);
+  if (bits == 2)
+    return {(mt * 32 + lane) * 4 + (ks >> 1), 2 * pair_2bit(ks & 1, reg) + 16 * half};
+  return {((mt * 2 + (ks >> 2)) * 32 + lane) * 4 + (ks & 3), 4 * reg + 16 * half};
+}
+
+// Value code of token tok, channel ch (rows = channels, columns = tokens).
+__host__ __device__ inline CodePos value_code_pos(int tok, int ch, int bits) {
+  int mc, kt, lane, reg, half;
+  frag_coords(ch, tok, mc, kt, lane, reg, half);
+  if (bits == 2)
+    return {(((kt >> 1) * 2 + (mc >> 2)) * 32 + lane) * 4 + (mc & 3),
+            2 * pair_2bit(kt & 1, reg) + 16 * half};
+  return {((kt * 2 + (mc >> 2)) * 32 + lane) * 4 + (mc & 3), 4 * reg + 16 * half};
+}
+
+// Inverse maps: for word w and bit position p of a code, the (row, col) it
+// holds.  Used by the packer, which assembles whole words.
+__host__ __device__ inline void frag_rowcol(int tile, int k, int lane, int reg, int half,
+                                            int& row, int& col) {
+  const int g = lane >> 2, t = lane & 3;
+  row = tile * 16 + g + 8 * (reg & 1);
+  col = k * 16 + 2 * t + 8 * (reg >> 1) + half;
+}
+
+// Key word w, code slot s (0..32/bits-1 in bit order) -> (tok, ch).
+__host__ __device__ inline void key_word_code(int w, int s, int bits, int& tok, int& ch) {
+  int tile, k, lane, reg, half;
+  if (bits == 2) {
+    const int wi = w & 3;
+    lane = (w >> 2) & 31;
+    tile = w >> 7;
+    half = s >> 3;
+    const int P = s & 7;  // bit 2P (+16)
+    const int k_local = P >> 2;
+    reg = ((P >> 1) & 1) | ((P & 1) << 1);
+    k = 2 * wi + k_local;
+  } else {
+    k = (w & 3) + 4 * ((w >> 7) & 1);
+    lane = (w >> 2) & 31;
+    tile = w >> 8;
+    half = s >> 2;
+    reg = s & 3;
+  }
+  frag_rowcol(tile, k, lane, reg, half, tok, ch);
+}
+
+// Value word w, code slot s -> (tok, ch).
+__host__ __device__ inline void value_word_code(int w, int s, int bits, int& tok, int& ch) {
+  int tile, k, lane, reg, half, row, col;
+  const int m4 = w & 3;
+  lane = (w >> 2) & 31;
+  const int hf = (w >> 7) & 1;
+  tile = hf * 4 + m4;
+  if (bits == 2) {
+    const int wi = w >> 8;  // k-step pair
+    half = s >> 3;
+    const int P = s & 7;
+    reg = ((P >> 1) & 1) | ((P & 1) << 1);
+    k = 2 * wi + (P >> 2);
+  } else {
+    k = w >> 8;
+    half = s >> 2;
+    reg = s & 3;
+  }
+  frag_rowcol(tile, k, lane, reg, half, row, col);
+  ch = row;
+  tok = col;
+}
+
+}  // namespace kvq

@@ -16,7 +16,7 @@ constexpr int kKG = KVQ_K_GROUP;   // tokens per key group
 constexpr int kVG = KVQ_V_GROUP;   // channels per value group
 constexpr int kR = KVQ_RESIDUAL;   // residual capacity
 constexpr int kVGroups = kD / kVG; // value groups per token (4)
-constexpr int kMaxSplits = 64;     // split-K partitions per (batch, KV head)
+constexpr int kMaxSplits = 64;     // bf16 comparator: split-K partitions per (b, kv head)
 constexpr int kMaxRep = 8;         // query heads per KV head
 
 // ---------------------------------------------------------------------------
@@ -24,11 +24,11 @@ constexpr int kMaxRep = 8;         // query heads per KV head
 // consecutive tokens of one (batch row, KV head): the Key codes and per-
 // channel (step, origin), then the Value codes and per-token (step, origin).
 // Records of one (b, kv head) are contiguous, so a split of the token axis
-// is one contiguous byte range (streamed with plain 16-byte loads).
+// is one contiguous byte range (streamed with 16-byte cp.async copies).
 //
 // Uniform key (k_bits = kb):
-//   [0]            K codes  uint8 [D][128*kb/8]   channel d's 128 codes,
-//                                                 LSB first along tokens
+//   [0]            K codes  128*128*kb/8 bytes in tensor-core fragment
+//                           order (frag_layout.h)
 //   [kc]           kscale   fp32  [D]
 //   [kc+4D]        kmin     bf16  [D]
 // Mixed key (n_bf16 = nb, n_uint4 = n4, n_uint2 = n2):
@@ -39,8 +39,7 @@ constexpr int kMaxRep = 8;         // query heads per KV head
 //   [..]           s4, s2   fp32  [n4], [n2]
 //   [..]           m4, m2   bf16  [n4], [n2]      (padded to 16 bytes)
 // Value (v_bits = vb), after the key part at offset kpart:
-//   [kpart]        V codes  uint8 [128][D*vb/8]   token t's D codes, LSB
-//                                                 first along channels
+//   [kpart]        V codes  128*128*vb/8 bytes in fragment order
 //   [+vc]          vscale   fp32  [128][D/32]
 //   [+vc+2048]     vmin     bf16  [128][D/32]
 // Every section starts on a 16-byte boundary.
@@ -134,8 +133,21 @@ cudaError_t launch_residual_tail(const kvq_cache* c, const kvq_bf16* k,
 
 int choose_splits(int num_sms, int units, int n_chunks);
 
-cudaError_t launch_decode(const kvq_cache* c, const kvq_bf16* q, int Hq,
-                          float* out, float* ws, int n_split, cudaStream_t s);
+// Tensor-core decode (decode_mma.cu).  The plan cuts the weighted item
+// sequence (per unit: its groups, then its residual) into n_slots warp
+// slices; each unit's partials occupy max_parts slots of the workspace.
+struct MmaPlan {
+  long long unit_len;
+  int n_slots;
+  int max_parts;
+};
+int mma_warps_per_cta(int rec_bytes);
+// false if even two partial slots per unit exceed ws_cap (0 = no cap)
+bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int rec_bytes,
+              size_t ws_cap, MmaPlan* plan);
+size_t mma_ws_bytes(int num_sms, int B, int Hkv, int Hq, int max_groups, int rec_bytes);
+cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, float* out,
+                              float* ws, const MmaPlan& plan, cudaStream_t s);
 cudaError_t launch_decode_bf16(const kvq_bf16* k, const kvq_bf16* v, int B,
                                int Hkv, int T, const kvq_bf16* q, int Hq,
                                float* out, float* ws, int n_split, int num_sms,

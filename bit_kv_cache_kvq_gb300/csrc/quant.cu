@@ -7,9 +7,13 @@
 // with IEEE fp32 subtraction and division (__fsub_rn / __fdiv_rn), codes
 // rounded half-to-even, and a constant group (M == m) stored as step 0,
 // codes 0, origin m.  Groups: Key per channel over the 128 tokens of a tile,
-// Value per token over 32 consecutive channels (KIVI §3).
+// Value per token over 32 consecutive channels (KIVI §3).  Codes are first
+// staged as bytes in shared memory and then packed word by word into the
+// tensor-core fragment order of frag_layout.h; kvq_export_* converts back to
+// the canonical LSB-first layout.
 #include <cuda_runtime.h>
 
+#include "frag_layout.h"
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -101,8 +105,34 @@ __device__ __forceinline__ void channel_range(const uint16_t* sK, int d,
   hi = unkey(kmax);
 }
 
+// Codes of one Key channel into the staging bytes cK[tok][ch].
+__device__ __forceinline__ void stage_channel(const uint16_t* sK, int d, const Params& p,
+                                              int bits, uint8_t* cK) {
+  const int top = (1 << bits) - 1;
+  for (int t = 0; t < kKG; ++t) cK[t * kD + d] = static_cast<uint8_t>(code_of(bf2f(sK[t * kD + d]), p, top));
+}
+
+// Pack staged key (cK) or value (cV) codes into the fragment-order words of
+// a record section (see frag_layout.h); all threads of the block take part.
+template <int BITS, bool KEY>
+__device__ __forceinline__ void pack_words(const uint8_t* codes, uint32_t* dst) {
+  constexpr int per = 32 / BITS;
+  constexpr int words = kKG * kD * BITS / 32;
+  for (int w = threadIdx.x; w < words; w += blockDim.x) {
+    uint32_t acc = 0;
+#pragma unroll
+    for (int s2 = 0; s2 < per; ++s2) {
+      int tok, ch;
+      if (KEY) key_word_code(w, s2, BITS, tok, ch);
+      else value_word_code(w, s2, BITS, tok, ch);
+      acc |= static_cast<uint32_t>(codes[tok * kD + ch]) << (BITS * s2);
+    }
+    dst[w] = acc;
+  }
+}
+
 // Codes of one Key channel, packed LSB first along tokens into dst (16-byte
-// aligned, 128*bits/8 bytes).
+// aligned, 128*bits/8 bytes): the canonical layout the mixed key tiers use.
 __device__ __forceinline__ void pack_channel(const uint16_t* sK, int d,
                                              const Params& p, int bits,
                                              uint8_t* dst) {
@@ -122,14 +152,12 @@ __device__ __forceinline__ void pack_channel(const uint16_t* sK, int d,
 // Value groups: one warp per (token, 32-channel group); lane = channel.
 template <int VB>
 __device__ __forceinline__ unsigned value_groups(const QuantArgs& a,
-                                                 const uint16_t* sV,
+                                                 const uint16_t* sV, uint8_t* cV,
                                                  uint8_t* rec, int warp0,
                                                  int nwarps) {
   constexpr int top = (1 << VB) - 1;
-  constexpr int per = 32 / VB;  // lanes per 32-bit code word
   const int lane = threadIdx.x & 31;
   const int warp = (threadIdx.x >> 5) - warp0;
-  uint8_t* vcodes = rec + a.lay.v_codes;
   float* vscale = reinterpret_cast<float*>(rec + a.lay.v_scale);
   uint16_t* vmin = reinterpret_cast<uint16_t*>(rec + a.lay.v_min);
   unsigned flags = 0;
@@ -142,13 +170,7 @@ __device__ __forceinline__ unsigned value_groups(const QuantArgs& a,
     const float lo = unkey(__reduce_min_sync(kFull, k));
     const float hi = unkey(__reduce_max_sync(kFull, k));
     const Params p = group_params(lo, hi, top, bad);
-    const uint32_t c = code_of(x, p, top) << (VB * (lane % per));
-    uint32_t* dst = reinterpret_cast<uint32_t*>(vcodes + t * (kD * VB / 8) + j * (kVG * VB / 8));
-#pragma unroll
-    for (int wi = 0; wi < 32 / per; ++wi) {
-      const uint32_t word = __reduce_or_sync(kFull, (lane / per == wi) ? c : 0u);
-      if (lane == 0) dst[wi] = word;
-    }
+    cV[t * kD + j * kVG + lane] = static_cast<uint8_t>(code_of(x, p, top));
     if (lane == 0) {
       vscale[t * kVGroups + j] = p.step;
       vmin[t * kVGroups + j] = f2bf_bits(p.m);
@@ -163,6 +185,8 @@ __global__ void __launch_bounds__(256) quantize_uniform_kernel(QuantArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem);
   uint16_t* sV = sK + kKG * kD;
+  uint8_t* cK = reinterpret_cast<uint8_t*>(sV + kKG * kD);
+  uint8_t* cV = cK + kKG * kD;
   load_tiles(a, sK, sV);
   __syncthreads();
 
@@ -177,14 +201,17 @@ __global__ void __launch_bounds__(256) quantize_uniform_kernel(QuantArgs a) {
     bool bad;
     channel_range(sK, d, lo, hi, bad);
     const Params p = group_params(lo, hi, (1 << KB) - 1, bad);
-    pack_channel(sK, d, p, KB, rec + a.lay.k_codes + d * (kKG * KB / 8));
+    stage_channel(sK, d, p, KB, cK);
     reinterpret_cast<float*>(rec + a.lay.k_scale)[d] = p.step;
     reinterpret_cast<uint16_t*>(rec + a.lay.k_min)[d] = f2bf_bits(p.m);
     flags = p.flags;
   } else {
     // warps 4-7: the Value groups
-    flags = value_groups<VB>(a, sV, rec, 4, 4);
+    flags = value_groups<VB>(a, sV, cV, rec, 4, 4);
   }
+  __syncthreads();
+  pack_words<KB, true>(cK, reinterpret_cast<uint32_t*>(rec + a.lay.k_codes));
+  pack_words<VB, false>(cV, reinterpret_cast<uint32_t*>(rec + a.lay.v_codes));
   if (flags) atomicOr(a.status, flags);
 }
 
@@ -197,6 +224,7 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem);
   uint16_t* sV = sK + kKG * kD;
+  uint8_t* cV = reinterpret_cast<uint8_t*>(sV + kKG * kD) + kKG * kD;
   __shared__ uint32_t sKey[kD];
   __shared__ uint8_t sTier[kD];
   load_tiles(a, sK, sV);
@@ -258,8 +286,10 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
       }
     }
   } else {
-    flags = value_groups<VB>(a, sV, rec, 4, 4);
+    flags = value_groups<VB>(a, sV, cV, rec, 4, 4);
   }
+  __syncthreads();
+  pack_words<VB, false>(cV, reinterpret_cast<uint32_t*>(rec + a.lay.v_codes));
   if (flags) atomicOr(a.status, flags);
 }
 
@@ -296,6 +326,42 @@ __global__ void gather_section_kernel(const uint8_t* __restrict__ records,
   }
 }
 
+// Canonical export of the fragment-order codes of records [u][0..n).
+// Keys: dst [u][n][D][128*bits/8], channel d's codes LSB first along tokens.
+// Values: dst [u][n*128][D*bits/8], token t's codes LSB first along channels.
+__global__ void export_codes_kernel(const uint8_t* __restrict__ records, long long rec_bytes,
+                                    int max_groups, int off, int bits, bool key,
+                                    uint8_t* dst, int n) {
+  const int g = blockIdx.x;
+  const int u = blockIdx.y;
+  const uint32_t* words = reinterpret_cast<const uint32_t*>(
+      records + (static_cast<long long>(u) * max_groups + g) * rec_bytes + off);
+  const int x = threadIdx.x;  // channel (keys) or token (values)
+  const int per = 8 / bits, row_bytes = 128 * bits / 8;
+  const uint32_t mask = (1u << bits) - 1u;
+  uint8_t* out = dst + ((static_cast<long long>(u) * n + g) * 128 + x) * row_bytes;
+  for (int i = 0; i < row_bytes; ++i) {
+    uint32_t byte = 0;
+    for (int e = 0; e < per; ++e) {
+      const int y = i * per + e;  // token (keys) or channel (values)
+      const CodePos p = key ? key_code_pos(y, x, bits) : value_code_pos(x, y, bits);
+      byte |= ((words[p.word] >> p.bit) & mask) << (bits * e);
+    }
+    out[i] = static_cast<uint8_t>(byte);
+  }
+}
+
+cudaError_t export_codes(const kvq_cache* c, int off, int bits, bool key, void* dst,
+                         cudaStream_t s) {
+  const int n = c->t_q / kKG;
+  const int units = c->cfg.batch * c->cfg.kv_heads;
+  if (n == 0) return cudaSuccess;
+  export_codes_kernel<<<dim3(n, units), 128, 0, s>>>(c->records, c->lay.bytes, c->max_groups,
+                                                     off, bits, key,
+                                                     static_cast<uint8_t*>(dst), n);
+  return cudaGetLastError();
+}
+
 cudaError_t gather(const kvq_cache* c, int off, int bytes, void* dst,
                    cudaStream_t s) {
   const int n = c->t_q / kKG;
@@ -307,7 +373,7 @@ cudaError_t gather(const kvq_cache* c, int off, int bytes, void* dst,
   return cudaGetLastError();
 }
 
-constexpr int kQuantSmem = 2 * kKG * kD * 2;  // K and V tiles, 64 KB
+constexpr int kQuantSmem = 2 * kKG * kD * 2 + 2 * kKG * kD;  // bf16 tiles + staged codes, 96 KB
 
 template <typename K>
 cudaError_t set_smem(K kernel) {
@@ -384,7 +450,7 @@ cudaError_t launch_export_k_uniform(const kvq_cache* c, uint8_t* codes,
                                     kvq_bf16* kmin, float* kscale,
                                     cudaStream_t s) {
   const RecLayout& L = c->lay;
-  cudaError_t e = gather(c, L.k_codes, kD * kKG * L.kb / 8, codes, s);
+  cudaError_t e = export_codes(c, L.k_codes, L.kb, true, codes, s);
   if (e == cudaSuccess) e = gather(c, L.k_min, kD * 2, kmin, s);
   if (e == cudaSuccess) e = gather(c, L.k_scale, kD * 4, kscale, s);
   return e;
@@ -393,7 +459,7 @@ cudaError_t launch_export_k_uniform(const kvq_cache* c, uint8_t* codes,
 cudaError_t launch_export_v(const kvq_cache* c, uint8_t* codes, kvq_bf16* vmin,
                             float* vscale, cudaStream_t s) {
   const RecLayout& L = c->lay;
-  cudaError_t e = gather(c, L.v_codes, kKG * kD * L.vb / 8, codes, s);
+  cudaError_t e = export_codes(c, L.v_codes, L.vb, false, codes, s);
   if (e == cudaSuccess) e = gather(c, L.v_min, kKG * kVGroups * 2, vmin, s);
   if (e == cudaSuccess) e = gather(c, L.v_scale, kKG * kVGroups * 4, vscale, s);
   return e;

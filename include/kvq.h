@@ -207,9 +207,9 @@ int kvq_decode_attention(const kvq_cache* cache, const kvq_bf16* q, int Hq,
  *  - All calls share the one array, so calls whose work overlaps on the GPU
  *    (other streams, other threads) race and corrupt each other's results;
  *    serialize them.  Each call rewrites every workspace entry it reads.
- *  - The split count is reduced to fit the array.  B*Hq*(D+2)*4 bytes must
- *    fit (B*Hq <= 16131 query rows); beyond that it returns
- *    KVQ_ERR_WORKSPACE.
+ *  - The split of the token axis is reduced to fit the array.  Two partial
+ *    slots per query row, 2*B*Hq*(D+2)*4 bytes, must fit (B*Hq <= 8065
+ *    query rows); beyond that it returns KVQ_ERR_WORKSPACE.
  */
 #define KVQ_STATIC_WORKSPACE_BYTES (8u << 20) /* 8 MiB per GPU */
 int kvq_decode_attention_static(const kvq_cache* cache, const kvq_bf16* q,
