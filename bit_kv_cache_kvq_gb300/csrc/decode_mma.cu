@@ -13,11 +13,11 @@
 // Codes are exact in f16.  A pair of codes becomes an f16x2 register with
 // one shift and one LOP3: the code lands in the mantissa of 1.0, giving
 // 1 + c/4 or 1 + c/16, the B rows carry the matching factor 4 or 16, and
-// the constant part sum_k B[k][h] is removed with one more MMA whose A tile
-// is all ones (exactly the same B values, so it cancels to fp32 rounding).
-// Each group's P·V products accumulate from zero over its 8 k-steps, so the
-// offset never builds up; the offset-free difference joins the running
-// output with one fp32 FMA that also applies the softmax rescale.
+// the constant part sum_k B[k][h] of the scores is removed with one more
+// MMA whose A tile is all ones (exactly the same B values, so it cancels to
+// fp32 rounding).  Value codes are made exact (c, one HFMA2 per pair) so the
+// running output accumulates offset-free in the MMA accumulators across
+// groups.
 // Q' and P' are normalized by powers of two per group (and V channel group)
 // so every f16 operand stays in range for any bf16 input.  Q' is split into
 // an f16 high part and an f16 low part (the rounding error of the high part)
@@ -29,10 +29,12 @@
 // Work split ("stream-K"): the flattened sequence of items (for each unit
 // its groups, then its residual as one item of weight kResidualWeight) is
 // cut into equal contiguous slices, one per warp; a warp keeps one online-
-// softmax state per unit it touches and writes one partial per unit.  Group
-// records stream through a private 2-stage cp.async ring in shared memory
-// per warp, so warps never wait on each other.  The combine kernel merges
-// each query head's partials with the exact log-sum-exp rule.
+// softmax state per unit it touches and writes one partial per unit.  Each
+// warp stages one record at a time in its own shared memory, in two parts:
+// the key part of the next group loads while the current group's softmax and
+// P·V run, the value part of the next group while its QK runs.  Warps never
+// wait on each other.  The combine kernel merges each query head's partials
+// with the exact log-sum-exp rule.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -48,14 +50,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kResidualWeight = 3;       // residual item ~ 3 groups of work
 constexpr float kSentinel = 4.2535295865117308e37f;  // 2^125: "no group yet"
 
-// Per-warp shared memory after the two record stages: the value-step table
-// (256 words), the value-origin table (4 rows of 72 words) and the unit's
-// query, bf16 [8 heads][136] (rows padded so head rows fall in different
-// banks).
+// Per-warp shared memory after the record buffer (key part, then value
+// part): the value-step table (256 words), the value-origin table (4 rows of
+// 72 words) and the unit's query, [8 heads][136] bf16 or, with at most 4
+// heads per KV head, [4 heads][136] fp32 pre-scaled by log2(e)/sqrt(D)
+// (rows padded so head rows fall in different banks).
 constexpr int kVsbBytes = 256 * 4;
 constexpr int kVmbBytes = 4 * 72 * 4;
 constexpr int kQRow = 136;
-constexpr int kQBytes = 8 * kQRow * 2;
+constexpr int kQBytes = 8 * kQRow * 2;   // = 4 * kQRow * 4
 constexpr int kWarpExtra = kVsbBytes + kVmbBytes + kQBytes;
 
 __device__ __forceinline__ float bf2f(uint32_t b16) { return __uint_as_float(b16 << 16); }
@@ -83,6 +86,13 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
+  const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a),
+                            *reinterpret_cast<const __half2*>(&b),
+                            *reinterpret_cast<const __half2*>(&c));
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
@@ -120,31 +130,57 @@ __device__ __forceinline__ int vmb_index(int kt, int j, int t, int slot) {
   return j * 72 + kt * 8 + t * 2 + slot;
 }
 
+// (a & b) | c in one three-input logic instruction (lookup table 0xEA).
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // --- code unpacking: word -> A fragment registers (see frag_layout.h)
 template <int KL>
 __device__ __forceinline__ void unpack2(uint32_t x, uint32_t (&a)[4]) {
   constexpr uint32_t M4 = 0x03000300u, M16 = 0x00C000C0u;
   if (KL == 0) {
     const uint32_t l8 = x << 8, l4 = x << 4;
-    a[0] = (l8 & M4) | kOne2;
-    a[1] = (l4 & M4) | kOne2;
-    a[2] = (l4 & M16) | kOne2;
-    a[3] = (x & M16) | kOne2;
+    a[0] = and_or(l8, M4, kOne2);
+    a[1] = and_or(l4, M4, kOne2);
+    a[2] = and_or(l4, M16, kOne2);
+    a[3] = and_or(x, M16, kOne2);
   } else {
     const uint32_t r4 = x >> 4, r8 = x >> 8;
-    a[0] = (x & M4) | kOne2;
-    a[1] = (r4 & M4) | kOne2;
-    a[2] = (r4 & M16) | kOne2;
-    a[3] = (r8 & M16) | kOne2;
+    a[0] = and_or(x, M4, kOne2);
+    a[1] = and_or(r4, M4, kOne2);
+    a[2] = and_or(r4, M16, kOne2);
+    a[3] = and_or(r8, M16, kOne2);
   }
+}
+
+// Value codes exact: (1 + c/s)*s - s = c for the s = 4 and s = 16 pairs.
+template <int KL>
+__device__ __forceinline__ void unpack2_exact(uint32_t x, uint32_t (&a)[4]) {
+  constexpr uint32_t s4 = 0x44004400u, n4 = 0xC400C400u;     // (4, 4), (-4, -4)
+  constexpr uint32_t s16 = 0x4C004C00u, n16 = 0xCC00CC00u;   // (16, 16), (-16, -16)
+  unpack2<KL>(x, a);
+  a[0] = hfma2_u(a[0], s4, n4);
+  a[1] = hfma2_u(a[1], s4, n4);
+  a[2] = hfma2_u(a[2], s16, n16);
+  a[3] = hfma2_u(a[3], s16, n16);
 }
 
 __device__ __forceinline__ void unpack4(uint32_t x, uint32_t (&a)[4]) {
   constexpr uint32_t M = 0x03C003C0u;
-  a[0] = ((x << 6) & M) | kOne2;
-  a[1] = ((x << 2) & M) | kOne2;
-  a[2] = ((x >> 2) & M) | kOne2;
-  a[3] = ((x >> 6) & M) | kOne2;
+  a[0] = and_or(x << 6, M, kOne2);
+  a[1] = and_or(x << 2, M, kOne2);
+  a[2] = and_or(x >> 2, M, kOne2);
+  a[3] = and_or(x >> 6, M, kOne2);
+}
+
+__device__ __forceinline__ void unpack4_exact(uint32_t x, uint32_t (&a)[4]) {
+  constexpr uint32_t s16 = 0x4C004C00u, n16 = 0xCC00CC00u;
+  unpack4(x, a);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a[i] = hfma2_u(a[i], s16, n16);
 }
 
 struct MmaArgs {
@@ -176,29 +212,32 @@ template <int KB, int VB, int NREP>
 struct Warp {
   static constexpr int KSCALE_B = KB == 2 ? 4 : 16;   // B-row factor for a0/a1
   static constexpr int KSCALE_T = 16;                  // B-row factor for a2/a3
-  static constexpr int VSCALE_B = VB == 2 ? 4 : 16;
-  static constexpr int VSCALE_T = 16;
   static constexpr bool SPARE = NREP <= 4;             // Q' low part in columns 4-7
+  static constexpr int NL = SPARE ? 1 : 8;             // low-part fragments kept
 
   const MmaArgs& a;
   const int lane, g, t;
-  uint8_t* stage0;  // two record stages of rec_bytes each, back to back
-  int rb;
-  uint32_t* vsb;   // [kt 8][t 4][j 4][2]  f16x2: normalized value steps, B order
-  uint32_t* vmb;   // [kt 8][j 4][t 4][2]  f16x2: normalized value origins, A order
+  uint8_t* kbuf;   // key part of the staged record
+  uint8_t* vbuf;   // value part of the staged record
+  uint32_t* vsb;   // value-step table, B order (vsb_index)
+  uint32_t* vmb;   // value-origin table, A order (vmb_index)
+  void* qs;        // the unit's query (see kQBytes)
 
   // online-softmax state (heads 2t, 2t+1 of this lane)
   float O[8][4];   // running O^T in units of sv[j] (channel tiles mc = 0..7)
   float vm[2];     // origin term (lanes g < 4: channel group j = g)
   float mrun[2], lrun[2];
   float sv[4], inv_sv[4];  // current units of O per j
-  uint16_t* qs;    // the unit's query (bf16), [head][kQRow]
 
-  __device__ __forceinline__ Warp(const MmaArgs& args, uint8_t* st0, int rec_bytes, uint32_t* vs,
-                                  uint32_t* vmn, uint16_t* q)
-      : a(args), lane(threadIdx.x & 31), g((threadIdx.x & 31) >> 2), t(threadIdx.x & 3),
-        stage0(st0), rb(rec_bytes), vsb(vs), vmb(vmn), qs(q) {}
-  __device__ __forceinline__ uint8_t* stage(int s) const { return stage0 + s * rb; }
+  __device__ __forceinline__ Warp(const MmaArgs& args, uint8_t* base)
+      : a(args), lane(threadIdx.x & 31), g((threadIdx.x & 31) >> 2), t(threadIdx.x & 3) {
+    const int rb = static_cast<int>(a.rec_bytes);
+    kbuf = base;
+    vbuf = base + a.lay.kpart;
+    vsb = reinterpret_cast<uint32_t*>(base + rb);
+    vmb = reinterpret_cast<uint32_t*>(base + rb + kVsbBytes);
+    qs = base + rb + kVsbBytes + kVmbBytes;
+  }
 
   // x rounded to 11 significant bits (an f16 value for the normalized
   // range used here); x - result is exact in fp32
@@ -206,7 +245,6 @@ struct Warp {
     return __uint_as_float((__float_as_uint(x) + 0x00001000u) & 0xFFFFE000u);
   }
 
-  template <int NL>
   __device__ __forceinline__ static void qk_mma(float (&s)[4], const uint32_t (&A)[4],
                                                 const uint32_t (&bq)[8][2],
                                                 const uint32_t (&bl)[NL][2], int ks) {
@@ -214,19 +252,23 @@ struct Warp {
     if (!SPARE) mma_f16(s, A[0], A[1], A[2], A[3], bl[ks % NL][0], bl[ks % NL][1]);
   }
 
-  // channel of B-row slot i (0..31) of this lane: ks = i/4, then 2t, 2t+1, 2t+8, 2t+9
-  __device__ __forceinline__ static int bch(int i, int t) { return 16 * (i >> 2) + 2 * t + ((i & 2) << 2) + (i & 1); }
-
   __device__ __forceinline__ void begin_unit(int u) {
     const int b = u / a.Hkv, kvh = u % a.Hkv;
+    const uint16_t* qg = a.q + (static_cast<long long>(b) * a.Hq + kvh * NREP) * kD;
+    const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
     __syncwarp();
-    for (int i = lane; i < 8 * (kD / 2); i += 32) {   // bf16 pairs
-      const int h = i / (kD / 2), c2 = i % (kD / 2);
-      uint32_t v = 0;
-      if (h < NREP)
-        v = reinterpret_cast<const uint32_t*>(
-            a.q + (static_cast<long long>(b) * a.Hq + kvh * NREP + h) * kD)[c2];
-      reinterpret_cast<uint32_t*>(qs + h * kQRow)[c2] = v;
+    if (SPARE) {   // fp32 [4][kQRow], pre-scaled
+      float* q = static_cast<float*>(qs);
+      for (int i = lane; i < 4 * kD; i += 32) {
+        const int h = i / kD, c = i % kD;
+        q[h * kQRow + c] = h < NREP ? bf2f(qg[h * kD + c]) * c0 : 0.0f;
+      }
+    } else {       // bf16 [8][kQRow]
+      uint32_t* q = static_cast<uint32_t*>(qs);
+      for (int i = lane; i < 8 * (kD / 2); i += 32) {
+        const int h = i / (kD / 2), c2 = i % (kD / 2);
+        q[h * (kQRow / 2) + c2] = reinterpret_cast<const uint32_t*>(qg + h * kD)[c2];
+      }
     }
     __syncwarp();
 #pragma unroll
@@ -243,82 +285,47 @@ struct Warp {
     lrun[0] = lrun[1] = 0.0f;
   }
 
-  __device__ __forceinline__ void issue(int u, int grp, int s) {
-    const uint8_t* src = a.records + (static_cast<long long>(u) * a.max_groups + grp) * a.rec_bytes;
-    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(stage(s)));
-    const int chunks = static_cast<int>(a.rec_bytes >> 4);
+  // cp.async of bytes [lo, hi) of group record grp of unit u into dst.
+  __device__ __forceinline__ void issue(int u, int grp, uint8_t* dst, int lo, int hi) {
+    const uint8_t* src = a.records + (static_cast<long long>(u) * a.max_groups + grp) * a.rec_bytes + lo;
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    const int chunks = (hi - lo) >> 4;
     for (int c = lane; c < chunks; c += 32)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + 16 * c),
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d + 16 * c),
                    "l"(src + 16 * c));
   }
-
-  // Value-side tables of one group: lane l handles tokens 4l..4l+3.
-  __device__ __forceinline__ void value_tables(const uint8_t* rec, float (&svn)[4], float (&inv_svm)[4]) {
-    const RecLayout& L = a.lay;
-    const float* vscale = reinterpret_cast<const float*>(rec + L.v_scale);
-    const uint2* vmin2 = reinterpret_cast<const uint2*>(rec + L.v_min);
-    float vs[4][4], vmn[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 f = reinterpret_cast<const float4*>(vscale)[4 * lane + i];
-      vs[i][0] = f.x; vs[i][1] = f.y; vs[i][2] = f.z; vs[i][3] = f.w;
-      const uint2 m = vmin2[4 * lane + i];
-      vmn[i][0] = bf2f(m.x & 0xffffu); vmn[i][1] = bf2f(m.x >> 16);
-      vmn[i][2] = bf2f(m.y & 0xffffu); vmn[i][3] = bf2f(m.y >> 16);
-    }
-    float svm[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float mx = fmaxf(fmaxf(vs[0][j], vs[1][j]), fmaxf(vs[2][j], vs[3][j]));
-      float mm = fmaxf(fmaxf(fabsf(vmn[0][j]), fabsf(vmn[1][j])),
-                       fmaxf(fabsf(vmn[2][j]), fabsf(vmn[3][j])));
-      mx = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(mx)));
-      mm = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(mm)));
-      float s_new, inv_new;
-      pow2_norm(mx, s_new, inv_new);
-      svn[j] = s_new;
-      pow2_norm(mm, svm[j], inv_svm[j]);
-      (void)inv_new;
-    }
-    // the units this group's P' uses: never larger than the running ones
-#pragma unroll
-    for (int j = 0; j < 4; ++j) svn[j] = fminf(svn[j], sv[j]);
-    const int kt = lane >> 2, q4 = lane & 3;
-    const int t0 = 2 * (q4 & 1), chi = q4 >> 1;
-    const float fac = chi ? static_cast<float>(VSCALE_T) : static_cast<float>(VSCALE_B);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float sc = svn[j] * fac;
-      vsb[vsb_index(kt, t0, j, chi)] = pack_h2(vs[0][j] * sc, vs[1][j] * sc);
-      vsb[vsb_index(kt, t0 + 1, j, chi)] = pack_h2(vs[2][j] * sc, vs[3][j] * sc);
-      const float sm = svm[j];
-      vmb[vmb_index(kt, j, t0, chi)] = pack_h2(vmn[0][j] * sm, vmn[1][j] * sm);
-      vmb[vmb_index(kt, j, t0 + 1, chi)] = pack_h2(vmn[2][j] * sm, vmn[3][j] * sm);
-    }
+  __device__ __forceinline__ void issue_k(int u, int grp) { issue(u, grp, kbuf, 0, a.lay.kpart); }
+  __device__ __forceinline__ void issue_v(int u, int grp) {
+    issue(u, grp, vbuf, a.lay.kpart, static_cast<int>(a.rec_bytes));
   }
 
-  __device__ __forceinline__ void group(const uint8_t* rec) {
+  // Scores of one group (keys in kbuf), softmax folded into the running
+  // state; returns p in S (C-fragment layout) and the rescale factors.
+  __device__ __forceinline__ void qk_softmax(float (&S)[8][4], float (&alpha)[2]) {
     const RecLayout& L = a.lay;
-    float svn[4], inv_svm[4];
-    value_tables(rec, svn, inv_svm);
-
-    // ---- Q' B fragments: Q'' = q * kscale * sq * {factor}
-    const float* kscale = reinterpret_cast<const float*>(rec + L.k_scale);
-    const uint32_t* kmin2 = reinterpret_cast<const uint32_t*>(rec + L.k_min);
+    const float* kscale = reinterpret_cast<const float*>(kbuf + L.k_scale);
+    const uint32_t* kmin2 = reinterpret_cast<const uint32_t*>(kbuf + L.k_min);
     float qk[32];
     float mx = 0.0f, bias = 0.0f;
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qs + (SPARE ? (g & 3) : g) * kQRow);
-    const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const float2 s01 = *reinterpret_cast<const float2*>(kscale + 16 * ks + 2 * t);
       const float2 s89 = *reinterpret_cast<const float2*>(kscale + 16 * ks + 2 * t + 8);
       const uint32_t m01 = kmin2[8 * ks + t];
       const uint32_t m89 = kmin2[8 * ks + t + 4];
-      const uint32_t q01 = qrow[8 * ks + t];
-      const uint32_t q89 = qrow[8 * ks + t + 4];
-      const float qa = bf2f(q01 & 0xffffu) * c0, qb = bf2f(q01 >> 16) * c0;
-      const float qc = bf2f(q89 & 0xffffu) * c0, qd = bf2f(q89 >> 16) * c0;
+      float qa, qb, qc, qd;
+      if (SPARE) {
+        const float* qrow = static_cast<const float*>(qs) + (g & 3) * kQRow;
+        const float2 q01 = *reinterpret_cast<const float2*>(qrow + 16 * ks + 2 * t);
+        const float2 q89 = *reinterpret_cast<const float2*>(qrow + 16 * ks + 2 * t + 8);
+        qa = q01.x; qb = q01.y; qc = q89.x; qd = q89.y;
+      } else {
+        const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
+        const uint32_t* qrow = static_cast<const uint32_t*>(qs) + g * (kQRow / 2);
+        const uint32_t q01 = qrow[8 * ks + t], q89 = qrow[8 * ks + t + 4];
+        qa = bf2f(q01 & 0xffffu) * c0; qb = bf2f(q01 >> 16) * c0;
+        qc = bf2f(q89 & 0xffffu) * c0; qd = bf2f(q89 >> 16) * c0;
+      }
       qk[4 * ks + 0] = qa * s01.x;
       qk[4 * ks + 1] = qb * s01.y;
       qk[4 * ks + 2] = qc * s89.x;
@@ -337,7 +344,7 @@ struct Warp {
     float sq, inv_sq;
     pow2_norm(mx, sq, inv_sq);
     // high part: the value rounded to f16 precision; low part: the rest
-    uint32_t bq[8][2], bl[NREP > 4 ? 8 : 1][2];
+    uint32_t bq[8][2], bl[NL][2];
     {
       const float fb = sq * KSCALE_B, ft = sq * KSCALE_T;
       const bool low_lane = SPARE && g >= 4;
@@ -359,8 +366,8 @@ struct Warp {
         } else {
           bq[ks][0] = pack_h2(hi[0], hi[1]);
           bq[ks][1] = pack_h2(hi[2], hi[3]);
-          bl[ks % (NREP > 4 ? 8 : 1)][0] = pack_h2(lo[0], lo[1]);
-          bl[ks % (NREP > 4 ? 8 : 1)][1] = pack_h2(lo[2], lo[3]);
+          bl[ks % NL][0] = pack_h2(lo[0], lo[1]);
+          bl[ks % NL][1] = pack_h2(lo[2], lo[3]);
         }
       }
     }
@@ -373,42 +380,51 @@ struct Warp {
       hbias[h] = __shfl_sync(kFull, bias, src);
     }
 
-    // ---- QK on tensor cores
+    // ---- QK on tensor cores, k-step outer: eight independent accumulator chains
     float Ck[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       mma_f16(Ck, kOne2, kOne2, kOne2, kOne2, bq[ks][0], bq[ks][1]);
-      if (!SPARE) mma_f16(Ck, kOne2, kOne2, kOne2, kOne2, bl[ks % (NREP > 4 ? 8 : 1)][0],
-                          bl[ks % (NREP > 4 ? 8 : 1)][1]);
+      if (!SPARE) mma_f16(Ck, kOne2, kOne2, kOne2, kOne2, bl[ks % NL][0], bl[ks % NL][1]);
     }
-    float S[8][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
       for (int c = 0; c < 4; ++c) S[mt][c] = 0.0f;
-    // k-step outer, M-tile inner: eight independent accumulator chains
+    const uint8_t* kc = kbuf + L.k_codes;
+    if (KB == 2) {
 #pragma unroll
-    for (int hf = 0; hf < (KB == 2 ? 1 : 2); ++hf) {
-      uint32_t kw[8][4];
+      for (int w = 0; w < 4; ++w) {
+        uint32_t kw[8];
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int off = KB == 2 ? (mt * 32 + lane) * 16 : ((mt * 2 + hf) * 32 + lane) * 16;
-        const uint4 w = *reinterpret_cast<const uint4*>(rec + L.k_codes + off);
-        kw[mt][0] = w.x; kw[mt][1] = w.y; kw[mt][2] = w.z; kw[mt][3] = w.w;
-      }
+        for (int mt = 0; mt < 8; ++mt)
+          kw[mt] = reinterpret_cast<const uint32_t*>(kc)[(mt * 4 + w) * 32 + lane];
 #pragma unroll
-      for (int kk = 0; kk < (KB == 2 ? 8 : 4); ++kk) {
-        const int ks = KB == 2 ? kk : 4 * hf + kk;
+        for (int kl = 0; kl < 2; ++kl) {
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          uint32_t A[4];
-          if (KB == 2) {
-            if (kk & 1) unpack2<1>(kw[mt][kk >> 1], A);
-            else unpack2<0>(kw[mt][kk >> 1], A);
-          } else {
-            unpack4(kw[mt][kk], A);
+          for (int mt = 0; mt < 8; ++mt) {
+            uint32_t A[4];
+            if (kl) unpack2<1>(kw[mt], A);
+            else unpack2<0>(kw[mt], A);
+            qk_mma(S[mt], A, bq, bl, 2 * w + kl);
           }
-          qk_mma(S[mt], A, bq, bl, ks);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int kp = 0; kp < 4; ++kp) {
+        uint2 kw[8];
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+          kw[mt] = reinterpret_cast<const uint2*>(kc)[(mt * 4 + kp) * 32 + lane];
+#pragma unroll
+        for (int kl = 0; kl < 2; ++kl) {
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            uint32_t A[4];
+            unpack4(kl ? kw[mt].y : kw[mt].x, A);
+            qk_mma(S[mt], A, bq, bl, 2 * kp + kl);
+          }
         }
       }
     }
@@ -422,85 +438,114 @@ struct Warp {
       Ck[0] += __shfl_xor_sync(kFull, Ck[0], 2);
       Ck[1] += __shfl_xor_sync(kFull, Ck[1], 2);
     }
-    float alpha[2];
+    // score = acc * hinv + off with hinv > 0, so the max is taken on the raw
+    // accumulators and p = 2^(acc * hinv + off - m) is one FMA and one ex2
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const float off = hbias[h] - Ck[h] * hinv[h];
       float m = -INFINITY;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        S[mt][h] = fmaf(S[mt][h], hinv[h], off);
-        S[mt][h + 2] = fmaf(S[mt][h + 2], hinv[h], off);
-        m = fmaxf(m, fmaxf(S[mt][h], S[mt][h + 2]));
-      }
+      for (int mt = 0; mt < 8; ++mt) m = fmaxf(m, fmaxf(S[mt][h], S[mt][h + 2]));
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 16));
-      const float m_new = fmaxf(mrun[h], m);
+      const float m_new = fmaxf(mrun[h], fmaf(m, hinv[h], off));
       alpha[h] = ex2(mrun[h] - m_new);
       mrun[h] = m_new;
+      const float shift = off - m_new;
       float ls = 0.0f;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        S[mt][h] = ex2(S[mt][h] - m_new);
-        S[mt][h + 2] = ex2(S[mt][h + 2] - m_new);
+        S[mt][h] = ex2(fmaf(S[mt][h], hinv[h], shift));
+        S[mt][h + 2] = ex2(fmaf(S[mt][h + 2], hinv[h], shift));
         ls += S[mt][h] + S[mt][h + 2];
       }
       lrun[h] = fmaf(lrun[h], alpha[h], ls);
     }
+  }
 
-    // ---- factors taking the running output to this group's units
-    float fo[4][2];
+  // Value-side tables of one group (values in vbuf): lane l handles tokens
+  // 4l..4l+3.  Returns this group's units per j and the origin scale.
+  __device__ __forceinline__ void value_tables(float (&svn)[4], float (&inv_svm)[4]) {
+    const RecLayout& L = a.lay;
+    const float* vscale = reinterpret_cast<const float*>(vbuf + (L.v_scale - L.kpart));
+    const uint2* vmin2 = reinterpret_cast<const uint2*>(vbuf + (L.v_min - L.kpart));
+    float vs[4][4], vmn[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 f = reinterpret_cast<const float4*>(vscale)[4 * lane + i];
+      vs[i][0] = f.x; vs[i][1] = f.y; vs[i][2] = f.z; vs[i][3] = f.w;
+      const uint2 m = vmin2[4 * lane + i];
+      vmn[i][0] = bf2f(m.x & 0xffffu); vmn[i][1] = bf2f(m.x >> 16);
+      vmn[i][2] = bf2f(m.y & 0xffffu); vmn[i][3] = bf2f(m.y >> 16);
+    }
+    float svm[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float mx = fmaxf(fmaxf(vs[0][j], vs[1][j]), fmaxf(vs[2][j], vs[3][j]));
+      float mm = fmaxf(fmaxf(fabsf(vmn[0][j]), fabsf(vmn[1][j])),
+                       fmaxf(fabsf(vmn[2][j]), fabsf(vmn[3][j])));
+      mx = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(mx)));
+      mm = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(mm)));
+      float s_new, inv_new;
+      pow2_norm(mx, s_new, inv_new);
+      (void)inv_new;
+      // the units of this group's P' never exceed the running ones
+      svn[j] = fminf(s_new, sv[j]);
+      pow2_norm(mm, svm[j], inv_svm[j]);
+    }
+    const int kt = lane >> 2, q4 = lane & 3;
+    const int t0 = 2 * (q4 & 1), chi = q4 >> 1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float sc = svn[j];
+      vsb[vsb_index(kt, t0, j, chi)] = pack_h2(vs[0][j] * sc, vs[1][j] * sc);
+      vsb[vsb_index(kt, t0 + 1, j, chi)] = pack_h2(vs[2][j] * sc, vs[3][j] * sc);
+      const float sm = svm[j];
+      vmb[vmb_index(kt, j, t0, chi)] = pack_h2(vmn[0][j] * sm, vmn[1][j] * sm);
+      vmb[vmb_index(kt, j, t0 + 1, chi)] = pack_h2(vmn[2][j] * sm, vmn[3][j] * sm);
+    }
+  }
+
+  // P·V of one group (values in vbuf) into the running output.
+  __device__ __forceinline__ void pv(float (&S)[8][4], const float (&alpha)[2]) {
+    const RecLayout& L = a.lay;
+    float svn[4], inv_svm[4];
+    value_tables(svn, inv_svm);
+    // running output to this group's units
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float ratio = svn[j] * inv_sv[j];
-      fo[j][0] = alpha[0] * ratio;
-      fo[j][1] = alpha[1] * ratio;
+      const float f0 = alpha[0] * ratio, f1 = alpha[1] * ratio;
+#pragma unroll
+      for (int mm = 0; mm < 2; ++mm) {
+        O[2 * j + mm][0] *= f0; O[2 * j + mm][2] *= f0;
+        O[2 * j + mm][1] *= f1; O[2 * j + mm][3] *= f1;
+      }
       sv[j] = svn[j];
       inv_sv[j] = pow2_rcp(svn[j]);
     }
     __syncwarp();   // value tables written by all lanes
 
-    // ---- PV on tensor cores: this group's contributions accumulate from
-    // zero (eight k-steps) and join the running output once, in fp32
     float Dvm[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    float D[8][4], Cv[4][4];
-#pragma unroll
-    for (int m = 0; m < 8; ++m)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) D[m][c] = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) Cv[j][c] = 0.0f;
+    const uint8_t* vc = vbuf + (L.v_codes - L.kpart);
     uint32_t vw[8];
 #pragma unroll
     for (int kt = 0; kt < 8; ++kt) {
       const uint32_t b0 = movmatrix_t(pack_h2(S[kt][0], S[kt][1]));
       const uint32_t b1 = movmatrix_t(pack_h2(S[kt][2], S[kt][3]));
       {
-        uint32_t a0 = 0, a2 = 0;
-        if (g < 4) {
-          const uint2 av = *reinterpret_cast<const uint2*>(vmb + vmb_index(kt, g, t, 0));
-          a0 = av.x;
-          a2 = av.y;
-        }
+        const uint2 av = *reinterpret_cast<const uint2*>(vmb + vmb_index(kt, g & 3, t, 0));
+        const uint32_t a0 = g < 4 ? av.x : 0u, a2 = g < 4 ? av.y : 0u;
         mma_f16(Dvm, a0, 0u, a2, 0u, b0, b1);
       }
       const uint4 vsA = *reinterpret_cast<const uint4*>(vsb + vsb_index(kt, t, 0, 0));
       const uint4 vsB = *reinterpret_cast<const uint4*>(vsb + vsb_index(kt, t, 2, 0));
       const uint32_t vsr[4][2] = {{vsA.x, vsA.y}, {vsA.z, vsA.w}, {vsB.x, vsB.y}, {vsB.z, vsB.w}};
-      if (VB == 2) {
-        if ((kt & 1) == 0) {
-          const int w = kt >> 1;
-          const uint4 lo = *reinterpret_cast<const uint4*>(rec + L.v_codes + ((w * 2 + 0) * 32 + lane) * 16);
-          const uint4 hi = *reinterpret_cast<const uint4*>(rec + L.v_codes + ((w * 2 + 1) * 32 + lane) * 16);
-          vw[0] = lo.x; vw[1] = lo.y; vw[2] = lo.z; vw[3] = lo.w;
-          vw[4] = hi.x; vw[5] = hi.y; vw[6] = hi.z; vw[7] = hi.w;
-        }
-      } else {
-        const uint4 lo = *reinterpret_cast<const uint4*>(rec + L.v_codes + ((kt * 2 + 0) * 32 + lane) * 16);
-        const uint4 hi = *reinterpret_cast<const uint4*>(rec + L.v_codes + ((kt * 2 + 1) * 32 + lane) * 16);
+      if (VB == 4 || (kt & 1) == 0) {
+        const int row = VB == 2 ? (kt >> 1) : kt;
+        const uint4 lo = *reinterpret_cast<const uint4*>(vc + ((row * 2 + 0) * 32 + lane) * 16);
+        const uint4 hi = *reinterpret_cast<const uint4*>(vc + ((row * 2 + 1) * 32 + lane) * 16);
         vw[0] = lo.x; vw[1] = lo.y; vw[2] = lo.z; vw[3] = lo.w;
         vw[4] = hi.x; vw[5] = hi.y; vw[6] = hi.z; vw[7] = hi.w;
       }
@@ -508,27 +553,19 @@ struct Warp {
       for (int j = 0; j < 4; ++j) {
         const uint32_t bj0 = hmul2_u(b0, vsr[j][0]);
         const uint32_t bj1 = hmul2_u(b1, vsr[j][1]);
-        mma_f16(Cv[j], kOne2, kOne2, kOne2, kOne2, bj0, bj1);
 #pragma unroll
         for (int mm = 0; mm < 2; ++mm) {
           const int mc = 2 * j + mm;
           uint32_t A[4];
           if (VB == 2) {
-            if (kt & 1) unpack2<1>(vw[mc], A);
-            else unpack2<0>(vw[mc], A);
+            if (kt & 1) unpack2_exact<1>(vw[mc], A);
+            else unpack2_exact<0>(vw[mc], A);
           } else {
-            unpack4(vw[mc], A);
+            unpack4_exact(vw[mc], A);
           }
-          mma_f16(D[mc], A[0], A[1], A[2], A[3], bj0, bj1);
+          mma_f16(O[mc], A[0], A[1], A[2], A[3], bj0, bj1);
         }
       }
-    }
-#pragma unroll
-    for (int mc = 0; mc < 8; ++mc) {
-      const int j = mc >> 1;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        O[mc][c] = fmaf(O[mc][c], fo[j][c & 1], D[mc][c] - Cv[j][c & 1]);
     }
     // origin term in true units (lanes g < 4 hold channel group j = g)
     {
@@ -539,16 +576,18 @@ struct Warp {
     }
   }
 
-  // The bf16 residual window (r tokens) on CUDA cores, with the stage
-  // buffers as scratch.  Added into the same online-softmax state.
+  // The bf16 residual window (r tokens) on CUDA cores, with the record
+  // buffer as scratch.  Added into the same online-softmax state.
   __device__ __forceinline__ void residual(int u) {
-    float* qf = reinterpret_cast<float*>(stage0);           // [NREP][128]
+    float* qf = reinterpret_cast<float*>(kbuf);             // [NREP][128], later o_r
     float* pb = qf + NREP * kD;                             // [NREP][128]
-    float* ob = pb + NREP * kD;                             // [NREP][128]
     const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
     __syncwarp();
-    for (int i = lane; i < NREP * kD; i += 32)
-      qf[i] = bf2f(qs[(i / kD) * kQRow + (i % kD)]) * c0;
+    for (int i = lane; i < NREP * kD; i += 32) {
+      const int h = i / kD, c = i % kD;
+      qf[i] = SPARE ? static_cast<const float*>(qs)[h * kQRow + c]
+                    : bf2f(static_cast<const uint16_t*>(qs)[h * kQRow + c]) * c0;
+    }
     __syncwarp();
     const uint16_t* kr = a.res_k + static_cast<long long>(u) * kR * kD;
     const uint16_t* vr = a.res_v + static_cast<long long>(u) * kR * kD;
@@ -642,6 +681,7 @@ struct Warp {
         o[h][3] = fmaf(p, v3, o[h][3]);
       }
     }
+    float* ob = qf;   // q no longer needed
 #pragma unroll
     for (int h = 0; h < NREP; ++h)
       *reinterpret_cast<float4*>(ob + h * kD + 4 * lane) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
@@ -706,11 +746,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_mma_kernel(MmaArgs a) {
   const int warp = threadIdx.x >> 5;
   const int slot = blockIdx.x * WARPS + warp;
   if (slot >= a.n_slots) return;            // warp-uniform
-  const int rb = static_cast<int>(a.rec_bytes);
-  uint8_t* mine = smem + static_cast<size_t>(warp) * (2 * rb + kWarpExtra);
-  Warp<KB, VB, NREP> W(a, mine, rb, reinterpret_cast<uint32_t*>(mine + 2 * rb),
-                       reinterpret_cast<uint32_t*>(mine + 2 * rb + kVsbBytes),
-                       reinterpret_cast<uint16_t*>(mine + 2 * rb + kVsbBytes + kVmbBytes));
+  uint8_t* mine = smem + static_cast<size_t>(warp) * (a.rec_bytes + kWarpExtra);
+  Warp<KB, VB, NREP> W(a, mine);
   const long long p0 = slot_start(a, slot), p1 = slot_start(a, slot + 1);
   for (int u = static_cast<int>(p0 / a.unit_len); u <= static_cast<int>((p1 - 1) / a.unit_len); ++u) {
     const long long ub = static_cast<long long>(u) * a.unit_len;
@@ -720,16 +757,27 @@ __global__ void __launch_bounds__(WARPS * 32, 1) decode_mma_kernel(MmaArgs a) {
     const bool res = a.r > 0 && lo <= a.n_groups && a.n_groups < hi;
     W.begin_unit(u);
     if (g0 < g1) {
-      W.issue(u, g0, 0);
+      // keys of group i+1 load during the softmax and P·V of group i; values
+      // of group i+1 during its QK.  One commit group per part, in order.
+      W.issue_k(u, g0);
+      asm volatile("cp.async.commit_group;\n" ::);
+      W.issue_v(u, g0);
       asm volatile("cp.async.commit_group;\n" ::);
       for (int gi = g0; gi < g1; ++gi) {
-        const int s = (gi - g0) & 1;
-        if (gi + 1 < g1) W.issue(u, gi + 1, s ^ 1);
+        const bool more = gi + 1 < g1;
+        asm volatile("cp.async.wait_group 1;\n" ::);   // keys of gi
+        __syncwarp();
+        float S[8][4], alpha[2];
+        W.qk_softmax(S, alpha);
+        __syncwarp();                                  // key part consumed
+        if (more) W.issue_k(u, gi + 1);
         asm volatile("cp.async.commit_group;\n" ::);
-        asm volatile("cp.async.wait_group 1;\n" ::);
+        asm volatile("cp.async.wait_group 1;\n" ::);   // values of gi
         __syncwarp();
-        W.group(W.stage(s));
-        __syncwarp();
+        W.pv(S, alpha);
+        __syncwarp();                                  // value part consumed
+        if (more) W.issue_v(u, gi + 1);
+        asm volatile("cp.async.commit_group;\n" ::);
       }
       asm volatile("cp.async.wait_group 0;\n" ::);
       __syncwarp();
@@ -768,7 +816,7 @@ __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restr
 
 template <int KB, int VB, int NREP, int WARPS>
 cudaError_t launch_cfg(const MmaArgs& a, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(WARPS) * (2 * a.rec_bytes + kWarpExtra);
+  const size_t smem = static_cast<size_t>(WARPS) * (a.rec_bytes + kWarpExtra);
   auto kern = decode_mma_kernel<KB, VB, NREP, WARPS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -792,10 +840,11 @@ cudaError_t launch_rep(const MmaArgs& a, int nrep, cudaStream_t s) {
 }  // namespace
 
 int mma_warps_per_cta(int rec_bytes) {
-  // two record stages plus the tables and the query per warp, within the
-  // 227 KB of shared memory a block may use
-  const int per = 2 * rec_bytes + kWarpExtra;
-  return max(1, min(8, (227 * 1024) / per));
+  // one record buffer plus the tables and the query per warp, within the
+  // 227 KB of shared memory a block may use; at most 12 warps so a thread
+  // keeps up to 168 registers
+  const int per = rec_bytes + kWarpExtra;
+  return max(1, min(12, (227 * 1024) / per));
 }
 
 bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int rec_bytes,
@@ -850,13 +899,13 @@ cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, flo
   a.ws = ws;
   const int nrep = Hq / c->cfg.kv_heads;
   const int kb = c->cfg.k_bits, vb = c->cfg.v_bits;
-  if (mma_warps_per_cta(c->lay.bytes) != (kb == 2 && vb == 2 ? 8 : kb == 4 && vb == 4 ? 5 : 6))
+  if (mma_warps_per_cta(c->lay.bytes) != (kb == 2 && vb == 2 ? 12 : kb == 4 && vb == 4 ? 9 : 11))
     return cudaErrorInvalidConfiguration;
   cudaError_t e;
-  if (kb == 2 && vb == 2) e = launch_rep<2, 2, 8>(a, nrep, s);
-  else if (kb == 2 && vb == 4) e = launch_rep<2, 4, 6>(a, nrep, s);
-  else if (kb == 4 && vb == 2) e = launch_rep<4, 2, 6>(a, nrep, s);
-  else e = launch_rep<4, 4, 5>(a, nrep, s);
+  if (kb == 2 && vb == 2) e = launch_rep<2, 2, 12>(a, nrep, s);
+  else if (kb == 2 && vb == 4) e = launch_rep<2, 4, 11>(a, nrep, s);
+  else if (kb == 4 && vb == 2) e = launch_rep<4, 2, 11>(a, nrep, s);
+  else e = launch_rep<4, 4, 9>(a, nrep, s);
   if (e != cudaSuccess) return e;
   combine_parts_kernel<<<c->cfg.batch * Hq, kD, 0, s>>>(ws, a.Hkv, Hq, a.max_parts, a.unit_len,
                                                         a.total, a.n_slots, out);

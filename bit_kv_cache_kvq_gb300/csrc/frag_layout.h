@@ -26,11 +26,14 @@
 // decoded to 1 + c/16 (all B rows scaled by 16).
 //
 // Word order in the 4096 B (2-bit) / 8192 B (4-bit) code section:
-//   key  2-bit: word(mt, lane, w = ks/2)       = (mt*32 + lane)*4 + w
-//   key  4-bit: word(mt, lane, ks)             = ((mt*2 + ks/4)*32 + lane)*4 + ks%4
+//   key  2-bit: word(mt, lane, w = ks/2)       = (mt*4 + w)*32 + lane
+//   key  4-bit: word(mt, lane, ks)             = ((mt*4 + ks/2)*32 + lane)*2 + ks%2
 //   value 2-bit: word(mc, lane, w = kt/2)      = ((w*2 + mc/4)*32 + lane)*4 + mc%4
 //   value 4-bit: word(mc, lane, kt)            = ((kt*2 + mc/4)*32 + lane)*4 + mc%4
-// so a warp reads 512 contiguous bytes per 16-byte-per-lane load.
+// Keys: a warp reads one word (2-bit) or two (4-bit) per lane per load, the
+// k-step order of the QK loop; values: 16 bytes per lane per load, all
+// eight channel tiles of one k-step (pair).  Every load is contiguous
+// across the warp, so it is free of shared-memory bank conflicts.
 #pragma once
 
 #include <cstdint>
@@ -65,8 +68,8 @@ __host__ __device__ inline CodePos key_code_pos(int tok, int ch, int bits) {
   int mt, ks, lane, reg, half;
   frag_coords(tok, ch, mt, ks, lane, reg, half);
   if (bits == 2)
-    return {(mt * 32 + lane) * 4 + (ks >> 1), 2 * pair_2bit(ks & 1, reg) + 16 * half};
-  return {((mt * 2 + (ks >> 2)) * 32 + lane) * 4 + (ks & 3), 4 * reg + 16 * half};
+    return {(mt * 4 + (ks >> 1)) * 32 + lane, 2 * pair_2bit(ks & 1, reg) + 16 * half};
+  return {((mt * 4 + (ks >> 1)) * 32 + lane) * 2 + (ks & 1), 4 * reg + 16 * half};
 }
 
 // Value code of token tok, channel ch (rows = channels, columns = tokens).
@@ -92,8 +95,8 @@ __host__ __device__ inline void frag_rowcol(int tile, int k, int lane, int reg, 
 __host__ __device__ inline void key_word_code(int w, int s, int bits, int& tok, int& ch) {
   int tile, k, lane, reg, half;
   if (bits == 2) {
-    const int wi = w & 3;
-    lane = (w >> 2) & 31;
+    lane = w & 31;
+    const int wi = (w >> 5) & 3;
     tile = w >> 7;
     half = s >> 3;
     const int P = s & 7;  // bit 2P (+16)
@@ -101,8 +104,8 @@ __host__ __device__ inline void key_word_code(int w, int s, int bits, int& tok, 
     reg = ((P >> 1) & 1) | ((P & 1) << 1);
     k = 2 * wi + k_local;
   } else {
-    k = (w & 3) + 4 * ((w >> 7) & 1);
-    lane = (w >> 2) & 31;
+    lane = (w >> 1) & 31;
+    k = 2 * ((w >> 6) & 3) + (w & 1);
     tile = w >> 8;
     half = s >> 2;
     reg = s & 3;
