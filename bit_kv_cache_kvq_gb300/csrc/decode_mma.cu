@@ -10,21 +10,19 @@
 //
 // with the origins added on the side: bias_h = sum_ch q m_K (CUDA cores) and
 // sum_tok p m_V (a fifth small MMA whose A rows are the value origins).
-// Codes are exact in f16.  A pair of codes becomes an f16x2 register with
-// one shift and one LOP3: the code lands in the mantissa of 1.0, giving
-// 1 + c/4 or 1 + c/16, the B rows carry the matching factor 4 or 16, and
-// the constant part sum_k B[k][h] of the scores is removed with one more
-// MMA whose A tile is all ones (exactly the same B values, so it cancels to
-// fp32 rounding).  Value codes are made exact (c, one HFMA2 per pair) so the
-// running output accumulates offset-free in the MMA accumulators across
-// groups.
+// A pair of codes becomes an f16x2 register with one AND (frag_layout.h):
+// the masked half is the subnormal c * 2^(pos - 24), exact, and the B rows
+// that meet it carry 2^(15 - pos), so every product is c * B' * 2^-9 with
+// B' the normalized Q' or P' entry.  No offset enters the sums, so the
+// running output accumulates across groups in the MMA accumulators.
 // Q' and P' are normalized by powers of two per group (and V channel group)
-// so every f16 operand stays in range for any bf16 input.  Q' is split into
-// an f16 high part and an f16 low part (the rounding error of the high part)
-// so the scores carry ~22 bits of Q': with at most 4 query heads per KV head
-// the low part rides in the 4 otherwise unused B columns (lanes of columns
-// 4-7 hold head (column - 4)) and one shuffle adds it back; with 8 heads a
-// second MMA per k-step accumulates it.
+// so every f16 operand stays in range (at most 2^15) for any bf16 input.
+// Scores need more than f16's 11 bits of Q' (a large score's error is its
+// size times the operand rounding), so Q' is split into an f16 high part
+// and an f16 low part (the rounding error of the high part), ~22 bits in
+// all: with at most 4 query heads per KV head the low part rides in the 4
+// otherwise unused B columns (lanes of columns 4-7 hold head column - 4) and
+// one shuffle adds it back; with 8 heads a second MMA per k-step adds it.
 //
 // Work split ("stream-K"): the flattened sequence of items (for each unit
 // its groups, then its residual as one item of weight kResidualWeight) is
@@ -44,11 +42,12 @@
 namespace kvq {
 namespace {
 
-constexpr uint32_t kOne2 = 0x3C003C00u;  // f16x2 (1.0, 1.0)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kResidualWeight = 3;       // residual item ~ 3 groups of work
 constexpr float kSentinel = 4.2535295865117308e37f;  // 2^125: "no group yet"
+constexpr float kCodeUnit = 512.0f;      // 2^9: products carry c * B' / 2^9
+constexpr float kInvCodeUnit = 1.0f / 512.0f;
 
 // Per-warp shared memory after the record buffer (key part, then value
 // part): the value-step table (256 words), the value-origin table (4 rows of
@@ -130,57 +129,30 @@ __device__ __forceinline__ int vmb_index(int kt, int j, int t, int slot) {
   return j * 72 + kt * 8 + t * 2 + slot;
 }
 
-// (a & b) | c in one three-input logic instruction (lookup table 0xEA).
-__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-// --- code unpacking: word -> A fragment registers (see frag_layout.h)
+// --- code unpacking: word x and y = x >> 8 -> A fragment registers
+// (frag_layout.h).  Each register is one AND; its halves are f16 subnormals.
+// B-row factor of register pair (a0, a1) / (a2, a3) is 2^(15 - pos).
 template <int KL>
-__device__ __forceinline__ void unpack2(uint32_t x, uint32_t (&a)[4]) {
-  constexpr uint32_t M4 = 0x03000300u, M16 = 0x00C000C0u;
-  if (KL == 0) {
-    const uint32_t l8 = x << 8, l4 = x << 4;
-    a[0] = and_or(l8, M4, kOne2);
-    a[1] = and_or(l4, M4, kOne2);
-    a[2] = and_or(l4, M16, kOne2);
-    a[3] = and_or(x, M16, kOne2);
-  } else {
-    const uint32_t r4 = x >> 4, r8 = x >> 8;
-    a[0] = and_or(x, M4, kOne2);
-    a[1] = and_or(r4, M4, kOne2);
-    a[2] = and_or(r4, M16, kOne2);
-    a[3] = and_or(r8, M16, kOne2);
-  }
+__device__ __forceinline__ void unpack2(uint32_t x, uint32_t y, uint32_t (&a)[4]) {
+  constexpr uint32_t Mb = 0x00030003u << (4 * KL), Mt = 0x000C000Cu << (4 * KL);
+  a[0] = x & Mb;
+  a[1] = y & Mb;
+  a[2] = x & Mt;
+  a[3] = y & Mt;
 }
-
-// Value codes exact: (1 + c/s)*s - s = c for the s = 4 and s = 16 pairs.
-template <int KL>
-__device__ __forceinline__ void unpack2_exact(uint32_t x, uint32_t (&a)[4]) {
-  constexpr uint32_t s4 = 0x44004400u, n4 = 0xC400C400u;     // (4, 4), (-4, -4)
-  constexpr uint32_t s16 = 0x4C004C00u, n16 = 0xCC00CC00u;   // (16, 16), (-16, -16)
-  unpack2<KL>(x, a);
-  a[0] = hfma2_u(a[0], s4, n4);
-  a[1] = hfma2_u(a[1], s4, n4);
-  a[2] = hfma2_u(a[2], s16, n16);
-  a[3] = hfma2_u(a[3], s16, n16);
+__device__ __forceinline__ void unpack4(uint32_t x, uint32_t y, uint32_t (&a)[4]) {
+  constexpr uint32_t Mb = 0x000F000Fu, Mt = 0x00F000F0u;
+  a[0] = x & Mb;
+  a[1] = y & Mb;
+  a[2] = x & Mt;
+  a[3] = y & Mt;
 }
-
-__device__ __forceinline__ void unpack4(uint32_t x, uint32_t (&a)[4]) {
-  constexpr uint32_t M = 0x03C003C0u;
-  a[0] = and_or(x << 6, M, kOne2);
-  a[1] = and_or(x << 2, M, kOne2);
-  a[2] = and_or(x >> 2, M, kOne2);
-  a[3] = and_or(x >> 6, M, kOne2);
-}
-
-__device__ __forceinline__ void unpack4_exact(uint32_t x, uint32_t (&a)[4]) {
-  constexpr uint32_t s16 = 0x4C004C00u, n16 = 0xCC00CC00u;
-  unpack4(x, a);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) a[i] = hfma2_u(a[i], s16, n16);
+// 2^(15 - pos) for B rows b0 (slot 0: rows 2t, 2t+1) and b1 (slot 1: rows
+// 2t+8, 2t+9) of k-step k.
+template <int BITS>
+__host__ __device__ constexpr float row_factor(int k, int slot) {
+  return BITS == 2 ? static_cast<float>(1 << (15 - 4 * (k & 1) - 2 * slot))
+                   : static_cast<float>(1 << (15 - 4 * slot));
 }
 
 struct MmaArgs {
@@ -210,10 +182,9 @@ __device__ __forceinline__ int slot_of(const MmaArgs& a, long long p) {
 
 template <int KB, int VB, int NREP>
 struct Warp {
-  static constexpr int KSCALE_B = KB == 2 ? 4 : 16;   // B-row factor for a0/a1
-  static constexpr int KSCALE_T = 16;                  // B-row factor for a2/a3
-  static constexpr bool SPARE = NREP <= 4;             // Q' low part in columns 4-7
-  static constexpr int NL = SPARE ? 1 : 8;             // low-part fragments kept
+  static constexpr bool SPARE = NREP <= 4;  // Q' low part in columns 4-7;
+                                            // query kept as pre-scaled fp32
+  static constexpr int NL = SPARE ? 1 : 8;  // low-part fragments kept
 
   const MmaArgs& a;
   const int lane, g, t;
@@ -224,7 +195,7 @@ struct Warp {
   void* qs;        // the unit's query (see kQBytes)
 
   // online-softmax state (heads 2t, 2t+1 of this lane)
-  float O[8][4];   // running O^T in units of sv[j] (channel tiles mc = 0..7)
+  float O[8][4];   // running O^T in units of sv[j] / 2^9 (channel tiles mc = 0..7)
   float vm[2];     // origin term (lanes g < 4: channel group j = g)
   float mrun[2], lrun[2];
   float sv[4], inv_sv[4];  // current units of O per j
@@ -314,7 +285,7 @@ struct Warp {
       const uint32_t m01 = kmin2[8 * ks + t];
       const uint32_t m89 = kmin2[8 * ks + t + 4];
       float qa, qb, qc, qd;
-      if (SPARE) {
+      if (SPARE) {   // rows h >= NREP of the stored query are zero
         const float* qrow = static_cast<const float*>(qs) + (g & 3) * kQRow;
         const float2 q01 = *reinterpret_cast<const float2*>(qrow + 16 * ks + 2 * t);
         const float2 q89 = *reinterpret_cast<const float2*>(qrow + 16 * ks + 2 * t + 8);
@@ -343,15 +314,16 @@ struct Warp {
     bias += __shfl_xor_sync(kFull, bias, 2);
     float sq, inv_sq;
     pow2_norm(mx, sq, inv_sq);
-    // high part: the value rounded to f16 precision; low part: the rest
+    // B' = Q' * sq in [0, 1), times the row factor of its code position;
+    // high part: B' rounded to f16 precision, low part: the rest
     uint32_t bq[8][2], bl[NL][2];
     {
-      const float fb = sq * KSCALE_B, ft = sq * KSCALE_T;
       const bool low_lane = SPARE && g >= 4;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        float x[4] = {qk[4 * ks + 0] * fb, qk[4 * ks + 1] * fb, qk[4 * ks + 2] * ft,
-                      qk[4 * ks + 3] * ft};
+        const float f0 = sq * row_factor<KB>(ks, 0), f1 = sq * row_factor<KB>(ks, 1);
+        float x[4] = {qk[4 * ks + 0] * f0, qk[4 * ks + 1] * f0, qk[4 * ks + 2] * f1,
+                      qk[4 * ks + 3] * f1};
         float hi[4], lo[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -371,22 +343,17 @@ struct Warp {
         }
       }
     }
-    // per head of this lane's C columns: 1/sq and bias from that head's lanes
+    // per head of this lane's C columns: the score unit and bias from that
+    // head's lanes
     float hinv[2], hbias[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int src = 4 * (SPARE ? ((2 * t + h) & 3) : (2 * t + h));
-      hinv[h] = __shfl_sync(kFull, inv_sq, src);
+      hinv[h] = __shfl_sync(kFull, inv_sq, src) * kCodeUnit;
       hbias[h] = __shfl_sync(kFull, bias, src);
     }
 
     // ---- QK on tensor cores, k-step outer: eight independent accumulator chains
-    float Ck[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      mma_f16(Ck, kOne2, kOne2, kOne2, kOne2, bq[ks][0], bq[ks][1]);
-      if (!SPARE) mma_f16(Ck, kOne2, kOne2, kOne2, kOne2, bl[ks % NL][0], bl[ks % NL][1]);
-    }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -395,18 +362,21 @@ struct Warp {
     if (KB == 2) {
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
-        uint32_t kw[8];
+        uint32_t kx[8], ky[8];
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-          kw[mt] = reinterpret_cast<const uint32_t*>(kc)[(mt * 4 + w) * 32 + lane];
+        for (int mt = 0; mt < 8; ++mt) {
+          kx[mt] = reinterpret_cast<const uint32_t*>(kc)[(mt * 4 + w) * 32 + lane];
+          ky[mt] = kx[mt] >> 8;
+        }
 #pragma unroll
         for (int kl = 0; kl < 2; ++kl) {
+          const int ks = 2 * w + kl;
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
             uint32_t A[4];
-            if (kl) unpack2<1>(kw[mt], A);
-            else unpack2<0>(kw[mt], A);
-            qk_mma(S[mt], A, bq, bl, 2 * w + kl);
+            if (kl) unpack2<1>(kx[mt], ky[mt], A);
+            else unpack2<0>(kx[mt], ky[mt], A);
+            qk_mma(S[mt], A, bq, bl, ks);
           }
         }
       }
@@ -419,11 +389,13 @@ struct Warp {
           kw[mt] = reinterpret_cast<const uint2*>(kc)[(mt * 4 + kp) * 32 + lane];
 #pragma unroll
         for (int kl = 0; kl < 2; ++kl) {
+          const int ks = 2 * kp + kl;
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
+            const uint32_t x = kl ? kw[mt].y : kw[mt].x;
             uint32_t A[4];
-            unpack4(kl ? kw[mt].y : kw[mt].x, A);
-            qk_mma(S[mt], A, bq, bl, 2 * kp + kl);
+            unpack4(x, x >> 8, A);
+            qk_mma(S[mt], A, bq, bl, ks);
           }
         }
       }
@@ -435,14 +407,12 @@ struct Warp {
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
         for (int c = 0; c < 4; ++c) S[mt][c] += __shfl_xor_sync(kFull, S[mt][c], 2);
-      Ck[0] += __shfl_xor_sync(kFull, Ck[0], 2);
-      Ck[1] += __shfl_xor_sync(kFull, Ck[1], 2);
     }
     // score = acc * hinv + off with hinv > 0, so the max is taken on the raw
     // accumulators and p = 2^(acc * hinv + off - m) is one FMA and one ex2
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const float off = hbias[h] - Ck[h] * hinv[h];
+      const float off = hbias[h];
       float m = -INFINITY;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) m = fmaxf(m, fmaxf(S[mt][h], S[mt][h + 2]));
@@ -496,9 +466,12 @@ struct Warp {
     }
     const int kt = lane >> 2, q4 = lane & 3;
     const int t0 = 2 * (q4 & 1), chi = q4 >> 1;
+    // the row factor of the code position these tokens meet (frag_layout.h)
+    const float rf = VB == 2 ? __uint_as_float((142u - 4u * (kt & 1) - 2u * chi) << 23)
+                             : __uint_as_float((142u - 4u * chi) << 23);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float sc = svn[j];
+      const float sc = svn[j] * rf;
       vsb[vsb_index(kt, t0, j, chi)] = pack_h2(vs[0][j] * sc, vs[1][j] * sc);
       vsb[vsb_index(kt, t0 + 1, j, chi)] = pack_h2(vs[2][j] * sc, vs[3][j] * sc);
       const float sm = svm[j];
@@ -507,64 +480,82 @@ struct Warp {
     }
   }
 
-  // P·V of one group (values in vbuf) into the running output.
+  // P·V of one group (values in vbuf) into the running output.  Each
+  // channel tile sums the group in a fresh accumulator and one FFMA folds it
+  // into the rescaled running output: the running sum of the (always
+  // non-negative) code terms never passes through the tensor cores'
+  // accumulation, whose truncation would otherwise grow with the context.
   __device__ __forceinline__ void pv(float (&S)[8][4], const float (&alpha)[2]) {
     const RecLayout& L = a.lay;
     float svn[4], inv_svm[4];
     value_tables(svn, inv_svm);
-    // running output to this group's units
+    // rescale of the running output to this group's units, per j and head
+    float f0[4], f1[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float ratio = svn[j] * inv_sv[j];
-      const float f0 = alpha[0] * ratio, f1 = alpha[1] * ratio;
-#pragma unroll
-      for (int mm = 0; mm < 2; ++mm) {
-        O[2 * j + mm][0] *= f0; O[2 * j + mm][2] *= f0;
-        O[2 * j + mm][1] *= f1; O[2 * j + mm][3] *= f1;
-      }
+      f0[j] = alpha[0] * ratio;
+      f1[j] = alpha[1] * ratio;
       sv[j] = svn[j];
       inv_sv[j] = pow2_rcp(svn[j]);
     }
     __syncwarp();   // value tables written by all lanes
 
+    // B fragments of p for the 8 token k-steps; origin term on the side
+    uint32_t pb[8][2];
     float Dvm[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    const uint8_t* vc = vbuf + (L.v_codes - L.kpart);
-    uint32_t vw[8];
 #pragma unroll
     for (int kt = 0; kt < 8; ++kt) {
-      const uint32_t b0 = movmatrix_t(pack_h2(S[kt][0], S[kt][1]));
-      const uint32_t b1 = movmatrix_t(pack_h2(S[kt][2], S[kt][3]));
-      {
-        const uint2 av = *reinterpret_cast<const uint2*>(vmb + vmb_index(kt, g & 3, t, 0));
-        const uint32_t a0 = g < 4 ? av.x : 0u, a2 = g < 4 ? av.y : 0u;
-        mma_f16(Dvm, a0, 0u, a2, 0u, b0, b1);
-      }
-      const uint4 vsA = *reinterpret_cast<const uint4*>(vsb + vsb_index(kt, t, 0, 0));
-      const uint4 vsB = *reinterpret_cast<const uint4*>(vsb + vsb_index(kt, t, 2, 0));
-      const uint32_t vsr[4][2] = {{vsA.x, vsA.y}, {vsA.z, vsA.w}, {vsB.x, vsB.y}, {vsB.z, vsB.w}};
-      if (VB == 4 || (kt & 1) == 0) {
-        const int row = VB == 2 ? (kt >> 1) : kt;
-        const uint4 lo = *reinterpret_cast<const uint4*>(vc + ((row * 2 + 0) * 32 + lane) * 16);
-        const uint4 hi = *reinterpret_cast<const uint4*>(vc + ((row * 2 + 1) * 32 + lane) * 16);
-        vw[0] = lo.x; vw[1] = lo.y; vw[2] = lo.z; vw[3] = lo.w;
-        vw[4] = hi.x; vw[5] = hi.y; vw[6] = hi.z; vw[7] = hi.w;
+      pb[kt][0] = movmatrix_t(pack_h2(S[kt][0], S[kt][1]));
+      pb[kt][1] = movmatrix_t(pack_h2(S[kt][2], S[kt][3]));
+      const uint2 av = *reinterpret_cast<const uint2*>(vmb + vmb_index(kt, g & 3, t, 0));
+      const uint32_t a0 = g < 4 ? av.x : 0u, a2 = g < 4 ? av.y : 0u;
+      mma_f16(Dvm, a0, 0u, a2, 0u, pb[kt][0], pb[kt][1]);
+    }
+    const uint8_t* vc = vbuf + (L.v_codes - L.kpart);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // P' = p * step of this channel group (with the row factors)
+      uint32_t bj[8][2];
+#pragma unroll
+      for (int kt = 0; kt < 8; ++kt) {
+        const uint2 vs = *reinterpret_cast<const uint2*>(vsb + vsb_index(kt, t, j, 0));
+        bj[kt][0] = hmul2_u(pb[kt][0], vs.x);
+        bj[kt][1] = hmul2_u(pb[kt][1], vs.y);
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t bj0 = hmul2_u(b0, vsr[j][0]);
-        const uint32_t bj1 = hmul2_u(b1, vsr[j][1]);
+      for (int mm = 0; mm < 2; ++mm) {
+        const int mc = 2 * j + mm;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (VB == 2) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(vc + (mc * 32 + lane) * 16);
+          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-        for (int mm = 0; mm < 2; ++mm) {
-          const int mc = 2 * j + mm;
-          uint32_t A[4];
-          if (VB == 2) {
-            if (kt & 1) unpack2_exact<1>(vw[mc], A);
-            else unpack2_exact<0>(vw[mc], A);
-          } else {
-            unpack4_exact(vw[mc], A);
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t x = wv[w], y = x >> 8;
+            uint32_t A[4];
+            unpack2<0>(x, y, A);
+            mma_f16(acc, A[0], A[1], A[2], A[3], bj[2 * w][0], bj[2 * w][1]);
+            unpack2<1>(x, y, A);
+            mma_f16(acc, A[0], A[1], A[2], A[3], bj[2 * w + 1][0], bj[2 * w + 1][1]);
           }
-          mma_f16(O[mc], A[0], A[1], A[2], A[3], bj0, bj1);
+        } else {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint4 w4 = *reinterpret_cast<const uint4*>(vc + ((mc * 2 + hh) * 32 + lane) * 16);
+            const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint32_t A[4];
+              unpack4(wv[i], wv[i] >> 8, A);
+              mma_f16(acc, A[0], A[1], A[2], A[3], bj[4 * hh + i][0], bj[4 * hh + i][1]);
+            }
+          }
         }
+        O[mc][0] = fmaf(O[mc][0], f0[j], acc[0]);
+        O[mc][2] = fmaf(O[mc][2], f0[j], acc[2]);
+        O[mc][1] = fmaf(O[mc][1], f1[j], acc[1]);
+        O[mc][3] = fmaf(O[mc][3], f1[j], acc[3]);
       }
     }
     // origin term in true units (lanes g < 4 hold channel group j = g)
@@ -693,7 +684,7 @@ struct Warp {
       for (int c = 0; c < 4; ++c) {
         const int h = 2 * t + (c & 1);
         const int ch = 16 * mc + g + 8 * (c >> 1);
-        if (h < NREP) O[mc][c] = fmaf(ob[h * kD + ch], sv[j], O[mc][c]);
+        if (h < NREP) O[mc][c] = fmaf(ob[h * kD + ch], sv[j] * kInvCodeUnit, O[mc][c]);
       }
     }
     __syncwarp();
@@ -722,7 +713,7 @@ struct Warp {
         for (int c = 0; c < 4; ++c) {
           const int h = 2 * t + (c & 1);
           const int ch = 16 * mc + g + 8 * (c >> 1);
-          const float val = O[mc][c] * inv_sv[j] + ((c & 1) ? vm1 : vm0);
+          const float val = O[mc][c] * (inv_sv[j] * kCodeUnit) + ((c & 1) ? vm1 : vm0);
           if (h < NREP) base[h * (kD + 2) + ch] = val;
         }
       }
