@@ -44,7 +44,7 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kResidualWeight = 3;       // residual item ~ 3 groups of work
+constexpr int kResidualWeight = 1;       // residual item ~ half a group of work
 constexpr float kSentinel = 4.2535295865117308e37f;  // 2^125: "no group yet"
 constexpr float kCodeUnit = 512.0f;      // 2^9: products carry c * B' / 2^9
 constexpr float kInvCodeUnit = 1.0f / 512.0f;
@@ -68,6 +68,36 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 b16 matrices from shared memory (row addresses from lanes 8i..8i+7
+// for matrix i), plain or transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// fp32 pair -> bf16x2 (low half = lo), round to nearest even
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
@@ -408,11 +438,19 @@ struct Warp {
 #pragma unroll
         for (int c = 0; c < 4; ++c) S[mt][c] += __shfl_xor_sync(kFull, S[mt][c], 2);
     }
-    // score = acc * hinv + off with hinv > 0, so the max is taken on the raw
-    // accumulators and p = 2^(acc * hinv + off - m) is one FMA and one ex2
+    softmax_update(S, hinv, hbias, alpha);
+  }
+
+  // One online-softmax step over 128 scores in C layout (rows = tokens,
+  // columns 2t, 2t+1 = this lane's heads): score = acc * hinv + off in log2
+  // units with hinv > 0, so the max is taken on the raw accumulators and
+  // p = 2^(acc * hinv + off - m) is one FMA and one ex2.  Returns p in S and
+  // the factors that rescale the earlier state.
+  __device__ __forceinline__ void softmax_update(float (&S)[8][4], const float (&hinv)[2],
+                                                 const float (&hoff)[2], float (&alpha)[2]) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const float off = hbias[h];
+      const float off = hoff[h];
       float m = -INFINITY;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) m = fmaxf(m, fmaxf(S[mt][h], S[mt][h + 2]));
@@ -567,126 +605,137 @@ struct Warp {
     }
   }
 
-  // The bf16 residual window (r tokens) on CUDA cores, with the record
-  // buffer as scratch.  Added into the same online-softmax state.
+  // 16-token chunk c (16 rows x 256 B) of a residual tensor into chunk slot
+  // `slot` of the record buffer, 16-byte pieces placed at column piece
+  // (col ^ (row & 7)) so the ldmatrix row reads are free of bank conflicts.
+  __device__ __forceinline__ void stage_chunk(const uint8_t* src, int c, int slot) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(kbuf)) + slot * 4096;
+    const uint8_t* s0 = src + c * 4096;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = lane + 32 * k, row = i >> 4, col = i & 15;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
+                       d + row * 256 + ((col ^ (row & 7)) << 4)),
+                   "l"(s0 + 16 * i));
+    }
+  }
+  __device__ __forceinline__ uint32_t chunk_addr(int slot, int row, int col16) const {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(kbuf)) + slot * 4096 + row * 256 +
+           ((col16 ^ (row & 7)) << 4);
+  }
+
+  // The bf16 residual window (r tokens) on tensor cores, folded into the
+  // same online-softmax state.  Scores: bf16 MMA of the exact bf16 keys and
+  // query (exact products, fp32 sums).  P·V: the values transposed by
+  // ldmatrix, p split into bf16 high and low parts (16 bits in all), one
+  // fresh accumulator per chunk and channel tile.  Keys and values stream
+  // through two 4 KB chunk slots of the record buffer.
   __device__ __forceinline__ void residual(int u) {
-    float* qf = reinterpret_cast<float*>(kbuf);             // [NREP][128], later o_r
-    float* pb = qf + NREP * kD;                             // [NREP][128]
-    const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
-    __syncwarp();
-    for (int i = lane; i < NREP * kD; i += 32) {
-      const int h = i / kD, c = i % kD;
-      qf[i] = SPARE ? static_cast<const float*>(qs)[h * kQRow + c]
-                    : bf2f(static_cast<const uint16_t*>(qs)[h * kQRow + c]) * c0;
+    const int r = a.r, nc = (r + 15) >> 4;
+    const uint8_t* kr = reinterpret_cast<const uint8_t*>(a.res_k + static_cast<long long>(u) * kR * kD);
+    const uint8_t* vr = reinterpret_cast<const uint8_t*>(a.res_v + static_cast<long long>(u) * kR * kD);
+    // query B fragments: column g = head g (zero for g >= NREP)
+    uint32_t bqr[8][2];
+    {
+      const int b = u / a.Hkv, kvh = u % a.Hkv;
+      const uint32_t* qg = reinterpret_cast<const uint32_t*>(
+          a.q + (static_cast<long long>(b) * a.Hq + kvh * NREP + min(g, NREP - 1)) * kD);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        bqr[ks][0] = g < NREP ? __ldg(qg + 8 * ks + t) : 0u;
+        bqr[ks][1] = g < NREP ? __ldg(qg + 8 * ks + t + 4) : 0u;
+      }
     }
     __syncwarp();
-    const uint16_t* kr = a.res_k + static_cast<long long>(u) * kR * kD;
-    const uint16_t* vr = a.res_v + static_cast<long long>(u) * kR * kD;
-    float s[4][NREP];
+    float S[8][4];
+    stage_chunk(kr, 0, 0);
+    asm volatile("cp.async.commit_group;\n" ::);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int tk = lane + 32 * i;
+    for (int c = 0; c < 8; ++c) {
+      if (c < nc) {
+        if (c + 1 < nc) stage_chunk(kr, c + 1, (c + 1) & 1);
+        asm volatile("cp.async.commit_group;\n" ::);
+        asm volatile("cp.async.wait_group 1;\n" ::);
+        __syncwarp();
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const int row = (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
-      for (int h = 0; h < NREP; ++h) s[i][h] = 0.0f;
-      if (tk < a.r) {
-        const uint4* row = reinterpret_cast<const uint4*>(kr + tk * kD);
-        for (int c8 = 0; c8 < kD / 8; ++c8) {
-          const uint4 w = __ldg(row + c8);
-          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float k0 = bf2f(wv[e] & 0xffffu), k1 = bf2f(wv[e] >> 16);
-#pragma unroll
-            for (int h = 0; h < NREP; ++h)
-              s[i][h] = fmaf(qf[h * kD + c8 * 8 + 2 * e], k0,
-                             fmaf(qf[h * kD + c8 * 8 + 2 * e + 1], k1, s[i][h]));
-          }
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t A[4];
+          ldsm_x4(A, chunk_addr(c & 1, row, 2 * ks + (lane >> 4)));
+          mma_bf16(acc, A, bqr[ks][0], bqr[ks][1]);
         }
+        __syncwarp();   // slot read before it is staged again
+#pragma unroll
+        for (int i = 0; i < 4; ++i) S[c][i] = 16 * c + g + 8 * (i >> 1) < r ? acc[i] : -INFINITY;
       } else {
 #pragma unroll
-        for (int h = 0; h < NREP; ++h) s[i][h] = -INFINITY;
+        for (int i = 0; i < 4; ++i) S[c][i] = -INFINITY;
       }
     }
-    float alpha_all[NREP], lsum_all[NREP];
+    // the first value chunk loads during the softmax
+    stage_chunk(vr, 0, 0);
+    asm volatile("cp.async.commit_group;\n" ::);
+    {
+      const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
+      const float hinv[2] = {c0, c0}, hoff[2] = {0.0f, 0.0f};
+      float alpha[2];
+      softmax_update(S, hinv, hoff, alpha);
 #pragma unroll
-    for (int h = 0; h < NREP; ++h) {
-      float m = fmaxf(fmaxf(s[0][h], s[1][h]), fmaxf(s[2][h], s[3][h]));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-      const float m_old = __shfl_sync(kFull, mrun[h & 1], h >> 1);  // lane (0, h/2)
-      const float m_new = fmaxf(m_old, m);
-      alpha_all[h] = ex2(m_old - m_new);
-      float ls = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float p = ex2(s[i][h] - m_new);
-        ls += p;
-        pb[h * kD + lane + 32 * i] = p;
+      for (int j = 0; j < 4; ++j) {
+        if (sv[j] == kSentinel) {   // no group in this segment: O is still zero
+          sv[j] = 1.0f;
+          inv_sv[j] = 1.0f;
+        }
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(kFull, ls, o);
-      lsum_all[h] = ls;
-      if ((h >> 1) == t) mrun[h & 1] = m_new;
-    }
-    float al[2] = {1.0f, 1.0f}, lsn[2] = {0.0f, 0.0f};
-#pragma unroll
-    for (int h = 0; h < NREP; ++h) {
-      if ((h >> 1) == t) {
-        al[h & 1] = alpha_all[h];
-        lsn[h & 1] = lsum_all[h];
+      for (int mc = 0; mc < 8; ++mc) {
+        O[mc][0] *= alpha[0]; O[mc][2] *= alpha[0];
+        O[mc][1] *= alpha[1]; O[mc][3] *= alpha[1];
       }
+      vm[0] *= alpha[0];
+      vm[1] *= alpha[1];
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) lrun[h] = lrun[h] * al[h] + (g == 0 ? lsn[h] : 0.0f);
+    for (int c = 0; c < 8; ++c) {
+      if (c < nc) {
+        if (c + 1 < nc) stage_chunk(vr, c + 1, (c + 1) & 1);
+        asm volatile("cp.async.commit_group;\n" ::);
+        // p of this chunk as bf16 B fragments: high part, then the rest
+        uint32_t ph[2], pl[2];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (sv[j] == kSentinel) {   // no group in this segment: O is still zero
-        sv[j] = 1.0f;
-        inv_sv[j] = 1.0f;
-      }
+        for (int i = 0; i < 2; ++i) {
+          const float p0 = S[c][2 * i], p1 = S[c][2 * i + 1];
+          const uint32_t hi = pack_bf2(p0, p1);
+          const float l0 = p0 - __uint_as_float(hi << 16);
+          const float l1 = p1 - __uint_as_float(hi & 0xffff0000u);
+          ph[i] = movmatrix_t(hi);
+          pl[i] = movmatrix_t(pack_bf2(l0, l1));
+        }
+        // tokens past r (last chunk): zero their value columns, whatever
+        // the buffer holds there
+        const int t0 = 16 * c + 2 * t;
+        const uint32_t m01 = (t0 < r ? 0xffffu : 0u) | (t0 + 1 < r ? 0xffff0000u : 0u);
+        const uint32_t m89 = (t0 + 8 < r ? 0xffffu : 0u) | (t0 + 9 < r ? 0xffff0000u : 0u);
+        asm volatile("cp.async.wait_group 1;\n" ::);
+        __syncwarp();
+        const int row = (lane & 7) + 8 * (lane >> 4);
 #pragma unroll
-      for (int mm = 0; mm < 2; ++mm) {
-        O[2 * j + mm][0] *= al[0]; O[2 * j + mm][2] *= al[0];
-        O[2 * j + mm][1] *= al[1]; O[2 * j + mm][3] *= al[1];
-      }
-    }
-    vm[0] *= al[0];
-    vm[1] *= al[1];
-    __syncwarp();
-    // o_r[h][ch] for channels 4*lane .. 4*lane+3
-    float o[NREP][4];
+        for (int mc = 0; mc < 8; ++mc) {
+          uint32_t A[4];
+          ldsm_x4_t(A, chunk_addr(c & 1, row, 2 * mc + ((lane >> 3) & 1)));
+          A[0] &= m01; A[1] &= m01; A[2] &= m89; A[3] &= m89;
+          float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          mma_bf16(acc, A, ph[0], ph[1]);
+          mma_bf16(acc, A, pl[0], pl[1]);
+          const float sc = sv[mc >> 1] * kInvCodeUnit;
 #pragma unroll
-    for (int h = 0; h < NREP; ++h)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[h][e] = 0.0f;
-    for (int tk = 0; tk < a.r; ++tk) {
-      const uint2 w = __ldg(reinterpret_cast<const uint2*>(vr + tk * kD + 4 * lane));
-      const float v0 = bf2f(w.x & 0xffffu), v1 = bf2f(w.x >> 16);
-      const float v2 = bf2f(w.y & 0xffffu), v3 = bf2f(w.y >> 16);
-#pragma unroll
-      for (int h = 0; h < NREP; ++h) {
-        const float p = pb[h * kD + tk];
-        o[h][0] = fmaf(p, v0, o[h][0]);
-        o[h][1] = fmaf(p, v1, o[h][1]);
-        o[h][2] = fmaf(p, v2, o[h][2]);
-        o[h][3] = fmaf(p, v3, o[h][3]);
-      }
-    }
-    float* ob = qf;   // q no longer needed
-#pragma unroll
-    for (int h = 0; h < NREP; ++h)
-      *reinterpret_cast<float4*>(ob + h * kD + 4 * lane) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-    __syncwarp();
-#pragma unroll
-    for (int mc = 0; mc < 8; ++mc) {
-      const int j = mc >> 1;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int h = 2 * t + (c & 1);
-        const int ch = 16 * mc + g + 8 * (c >> 1);
-        if (h < NREP) O[mc][c] = fmaf(ob[h * kD + ch], sv[j] * kInvCodeUnit, O[mc][c]);
+          for (int i = 0; i < 4; ++i) O[mc][i] = fmaf(acc[i], sc, O[mc][i]);
+        }
+        __syncwarp();   // slot read before it is staged again
       }
     }
+    asm volatile("cp.async.wait_group 0;\n" ::);
     __syncwarp();
   }
 
