@@ -205,7 +205,6 @@ int kvq_decode_attention(const kvq_cache* c, const kvq_bf16* q, int Hq, float* o
                          void* ws, size_t ws_bytes, cudaStream_t s) {
   if (!c || !q || !out) return KVQ_ERR_ARG;
   if (!valid_rep(Hq, c->cfg.kv_heads)) return KVQ_ERR_SHAPE;
-  if (c->cfg.k_mode != KVQ_K_UNIFORM) return KVQ_ERR_MODE;
   if (c->t_q + c->r == 0) return KVQ_ERR_EMPTY;
   if (!ws || ws_bytes < kvq_decode_workspace_bytes(c, Hq) || !aligned16(ws))
     return KVQ_ERR_WORKSPACE;

@@ -58,7 +58,9 @@ constexpr int kVsbBytes = 256 * 4;
 constexpr int kVmbBytes = 4 * 72 * 4;
 constexpr int kQRow = 136;
 constexpr int kQBytes = 8 * kQRow * 2;   // = 4 * kQRow * 4
-constexpr int kWarpExtra = kVsbBytes + kVmbBytes + kQBytes;
+constexpr int kZeroBytes = 16;           // a zero row for ldmatrix padding
+constexpr int kWarpExtra = kVsbBytes + kVmbBytes + kQBytes + kZeroBytes;
+constexpr int kMaxWarps = 12;           // warps per block: up to 168 registers a thread
 
 __device__ __forceinline__ float bf2f(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
@@ -115,13 +117,6 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
-  const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a),
-                            *reinterpret_cast<const __half2*>(&b),
-                            *reinterpret_cast<const __half2*>(&c));
-  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
@@ -210,7 +205,7 @@ __device__ __forceinline__ int slot_of(const MmaArgs& a, long long p) {
   return static_cast<int>(((p + 1) * a.n_slots - 1) / a.total);
 }
 
-template <int KB, int VB, int NREP>
+template <int KB, int VB, int NREP, bool MIX>
 struct Warp {
   static constexpr bool SPARE = NREP <= 4;  // Q' low part in columns 4-7;
                                             // query kept as pre-scaled fp32
@@ -223,6 +218,9 @@ struct Warp {
   uint32_t* vsb;   // value-step table, B order (vsb_index)
   uint32_t* vmb;   // value-origin table, A order (vmb_index)
   void* qs;        // the unit's query (see kQBytes)
+  uint8_t* zero16; // 16 zero bytes
+  const uint16_t* qg_row;  // this lane's query head (g, capped at NREP - 1) in global memory
+  float qmax;      // max |query| of the head row this lane builds B columns for
 
   // online-softmax state (heads 2t, 2t+1 of this lane)
   float O[8][4];   // running O^T in units of sv[j] / 2^9 (channel tiles mc = 0..7)
@@ -238,6 +236,9 @@ struct Warp {
     vsb = reinterpret_cast<uint32_t*>(base + rb);
     vmb = reinterpret_cast<uint32_t*>(base + rb + kVsbBytes);
     qs = base + rb + kVsbBytes + kVmbBytes;
+    zero16 = base + rb + kVsbBytes + kVmbBytes + kQBytes;
+    if (lane < 4) reinterpret_cast<uint32_t*>(zero16)[lane] = 0u;
+    __syncwarp();
   }
 
   // x rounded to 11 significant bits (an f16 value for the normalized
@@ -256,6 +257,7 @@ struct Warp {
   __device__ __forceinline__ void begin_unit(int u) {
     const int b = u / a.Hkv, kvh = u % a.Hkv;
     const uint16_t* qg = a.q + (static_cast<long long>(b) * a.Hq + kvh * NREP) * kD;
+    qg_row = qg + min(g, NREP - 1) * kD;
     const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
     __syncwarp();
     if (SPARE) {   // fp32 [4][kQRow], pre-scaled
@@ -272,6 +274,14 @@ struct Warp {
       }
     }
     __syncwarp();
+    if (MIX) {   // max |q| of the row: fp32 pre-scaled row g & 3, or bf16 row g
+      float mx = 0.0f;
+      for (int c = t; c < kD; c += 4)
+        mx = fmaxf(mx, SPARE ? fabsf(static_cast<const float*>(qs)[(g & 3) * kQRow + c])
+                             : fabsf(bf2f(static_cast<const uint16_t*>(qs)[g * kQRow + c])));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+      qmax = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    }
 #pragma unroll
     for (int m = 0; m < 8; ++m)
 #pragma unroll
@@ -303,6 +313,22 @@ struct Warp {
   // Scores of one group (keys in kbuf), softmax folded into the running
   // state; returns p in S (C-fragment layout) and the rescale factors.
   __device__ __forceinline__ void qk_softmax(float (&S)[8][4], float (&alpha)[2]) {
+    float hinv[2], hbias[2];
+    if constexpr (MIX) scores_mixed(S, hinv, hbias);
+    else scores_uniform(S, hinv, hbias);
+    if (SPARE) {   // columns c and c + 4 hold the high and low parts of one head
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) S[mt][c] += __shfl_xor_sync(kFull, S[mt][c], 2);
+    }
+    softmax_update(S, hinv, hbias, alpha);
+  }
+
+  // Uniform keys: score accumulators S (code units), their unit hinv and the
+  // origin term hbias per head of this lane's C columns, in log2 units.
+  __device__ __forceinline__ void scores_uniform(float (&S)[8][4], float (&hinv)[2],
+                                                 float (&hbias)[2]) {
     const RecLayout& L = a.lay;
     const float* kscale = reinterpret_cast<const float*>(kbuf + L.k_scale);
     const uint32_t* kmin2 = reinterpret_cast<const uint32_t*>(kbuf + L.k_min);
@@ -375,7 +401,6 @@ struct Warp {
     }
     // per head of this lane's C columns: the score unit and bias from that
     // head's lanes
-    float hinv[2], hbias[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int src = 4 * (SPARE ? ((2 * t + h) & 3) : (2 * t + h));
@@ -430,15 +455,147 @@ struct Warp {
         }
       }
     }
+  }
 
-    // ---- scores in log2 units and the online softmax
-    if (SPARE) {   // columns c and c + 4 hold the high and low parts of one head
+  // Mixed keys (MixKVQ): the BF16 tier on bf16 MMAs of the raw keys and the
+  // exact query (ldmatrix transposes the channel-major raw rows), rescaled
+  // into the code path's units; the UINT4 and UINT2 tiers as 2-bit virtual
+  // channels on the code path.  A per-group table, built in the value-table
+  // area (free until this group's P·V), gives each virtual channel its key
+  // channel, step (times 4 for the high half of a UINT4 code, times the row
+  // factor) and origin (zero for a high half).  Q' is normalized by the bound
+  // max|q| * max step, so the table needs no pass over the products.
+  __device__ __forceinline__ void scores_mixed(float (&S)[8][4], float (&hinv)[2],
+                                               float (&hbias)[2]) {
+    const RecLayout& L = a.lay;
+    const int nb = L.nb, n4 = L.n4, nv = L.nv, kw2 = L.kw2;
+    const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
+    uint2* tab = reinterpret_cast<uint2*>(vsb);
+    const float* sc = reinterpret_cast<const float*>(kbuf + L.s4);
+    const uint16_t* mn = reinterpret_cast<const uint16_t*>(kbuf + L.m4);
+    const uint8_t* perm = kbuf + L.perm;
+    uint32_t smax = 0u;
+    for (int v = lane; v < 32 * kw2; v += 32) {
+      float sm = 0.0f;
+      uint32_t mc = 0u;
+      if (v < nv) {
+        const bool hi = v >= n4 && v < 2 * n4;
+        const int idx = v < n4 ? v : v - n4;
+        const float st = sc[idx] * (hi ? 4.0f : 1.0f);
+        smax = max(smax, __float_as_uint(st));   // steps are >= 0
+        const float rf = __uint_as_float((142u - 4u * ((v >> 4) & 1) - 2u * ((v >> 3) & 1)) << 23);
+        sm = st * rf * (SPARE ? 1.0f : c0);
+        mc = (hi ? 0u : static_cast<uint32_t>(mn[idx])) | (static_cast<uint32_t>(perm[nb + idx]) << 16);
+      }
+      tab[v] = make_uint2(__float_as_uint(sm), mc);
+    }
+    smax = __reduce_max_sync(kFull, smax);
+    float sq, inv_sq;
+    pow2_norm(qmax * __uint_as_float(smax) * (SPARE ? 1.0f : c0), sq, inv_sq);
+    if (sq > 1.099511627776e12f) {   // cap at 2^40: raw scores stay finite in code units
+      sq = 1.099511627776e12f;
+      inv_sq = 1.0f / 1.099511627776e12f;
+    }
+    __syncwarp();   // table written by all lanes
+
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) S[mt][c] = 0.0f;
+    // ---- BF16 tier: raw keys (A, via ldmatrix.trans) times the exact query
+    if (nb > 0) {
+      const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(kbuf + L.raw));
+      const uint32_t zaddr = static_cast<uint32_t>(__cvta_generic_to_shared(zero16));
+      for (int k16 = 0; k16 < (nb + 15) >> 4; ++k16) {
+        uint32_t qb[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 16 * k16 + 2 * t + (e & 1) + 8 * (e >> 1);
+          qb[e] = (i < nb && g < NREP) ? static_cast<uint32_t>(__ldg(qg_row + perm[i])) : 0u;
+        }
+        const uint32_t b0 = qb[0] | (qb[1] << 16), b1 = qb[2] | (qb[3] << 16);
+        const int i = 16 * k16 + (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const int pc = 2 * mt + ((lane >> 3) & 1);
+          uint32_t A[4];
+          ldsm_x4_t(A, i < nb ? raw + i * 256 + ((pc ^ (i & 7)) << 4) : zaddr);
+          mma_bf16(S[mt], A, b0, b1);
+        }
+      }
+      // raw dot products -> code units: * c0 * sq / 2^9 per head
+      float rr[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int src = 4 * (SPARE ? ((2 * t + h) & 3) : (2 * t + h));
+        rr[h] = c0 * __shfl_sync(kFull, sq, src) * kInvCodeUnit;
+      }
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) S[mt][c] += __shfl_xor_sync(kFull, S[mt][c], 2);
+        for (int c = 0; c < 4; ++c) S[mt][c] *= rr[c & 1];
     }
-    softmax_update(S, hinv, hbias, alpha);
+
+    // ---- UINT4 and UINT2 tiers: virtual 2-bit channels
+    const uint32_t* kcw = reinterpret_cast<const uint32_t*>(kbuf + L.kc);
+    const bool low_lane = SPARE && g >= 4;
+    float bias = 0.0f;
+    for (int w = 0; w < kw2; ++w) {
+      uint32_t kx[8], ky[8];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        kx[mt] = kcw[(mt * kw2 + w) * 32 + lane];
+        ky[mt] = kx[mt] >> 8;
+      }
+#pragma unroll
+      for (int kl = 0; kl < 2; ++kl) {
+        const int v0 = 32 * w + 16 * kl + 2 * t;
+        const uint4 e01 = *reinterpret_cast<const uint4*>(tab + v0);
+        const uint4 e89 = *reinterpret_cast<const uint4*>(tab + v0 + 8);
+        const uint32_t es[4] = {e01.x, e01.z, e89.x, e89.z};
+        const uint32_t em[4] = {e01.y, e01.w, e89.y, e89.w};
+        float x[4], hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int ch = static_cast<int>(em[i] >> 16);
+          const float qv = SPARE ? static_cast<const float*>(qs)[(g & 3) * kQRow + ch]
+                                 : bf2f(static_cast<const uint16_t*>(qs)[g * kQRow + ch]);
+          bias = fmaf(qv, bf2f(em[i] & 0xffffu), bias);
+          x[i] = qv * __uint_as_float(es[i]) * sq;
+          hi[i] = round_f16_precision(x[i]);
+          lo[i] = x[i] - hi[i];
+        }
+        uint32_t bq0, bq1, bl0 = 0u, bl1 = 0u;
+        if (SPARE) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) x[i] = low_lane ? lo[i] : hi[i];
+          bq0 = pack_h2(x[0], x[1]);
+          bq1 = pack_h2(x[2], x[3]);
+        } else {
+          bq0 = pack_h2(hi[0], hi[1]);
+          bq1 = pack_h2(hi[2], hi[3]);
+          bl0 = pack_h2(lo[0], lo[1]);
+          bl1 = pack_h2(lo[2], lo[3]);
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t A[4];
+          if (kl) unpack2<1>(kx[mt], ky[mt], A);
+          else unpack2<0>(kx[mt], ky[mt], A);
+          mma_f16(S[mt], A[0], A[1], A[2], A[3], bq0, bq1);
+          if (!SPARE) mma_f16(S[mt], A[0], A[1], A[2], A[3], bl0, bl1);
+        }
+      }
+    }
+    bias += __shfl_xor_sync(kFull, bias, 1);
+    bias += __shfl_xor_sync(kFull, bias, 2);
+    if (!SPARE) bias *= c0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int src = 4 * (SPARE ? ((2 * t + h) & 3) : (2 * t + h));
+      hinv[h] = __shfl_sync(kFull, inv_sq, src) * kCodeUnit;
+      hbias[h] = __shfl_sync(kFull, bias, src);
+    }
   }
 
   // One online-softmax step over 128 scores in C layout (rows = tokens,
@@ -780,14 +937,14 @@ struct Warp {
   }
 };
 
-template <int KB, int VB, int NREP, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32, 1) decode_mma_kernel(MmaArgs a) {
+template <int KB, int VB, int NREP, bool MIX>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) decode_mma_kernel(MmaArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
-  const int slot = blockIdx.x * WARPS + warp;
+  const int slot = blockIdx.x * (blockDim.x >> 5) + warp;
   if (slot >= a.n_slots) return;            // warp-uniform
   uint8_t* mine = smem + static_cast<size_t>(warp) * (a.rec_bytes + kWarpExtra);
-  Warp<KB, VB, NREP> W(a, mine);
+  Warp<KB, VB, NREP, MIX> W(a, mine);
   const long long p0 = slot_start(a, slot), p1 = slot_start(a, slot + 1);
   for (int u = static_cast<int>(p0 / a.unit_len); u <= static_cast<int>((p1 - 1) / a.unit_len); ++u) {
     const long long ub = static_cast<long long>(u) * a.unit_len;
@@ -854,25 +1011,25 @@ __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restr
   out[static_cast<long long>(row) * kD + threadIdx.x] = o / l;
 }
 
-template <int KB, int VB, int NREP, int WARPS>
-cudaError_t launch_cfg(const MmaArgs& a, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(WARPS) * (a.rec_bytes + kWarpExtra);
-  auto kern = decode_mma_kernel<KB, VB, NREP, WARPS>;
+template <int KB, int VB, int NREP, bool MIX>
+cudaError_t launch_cfg(const MmaArgs& a, int warps, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(warps) * (a.rec_bytes + kWarpExtra);
+  auto kern = decode_mma_kernel<KB, VB, NREP, MIX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int grid = (a.n_slots + WARPS - 1) / WARPS;
-  kern<<<grid, WARPS * 32, smem, s>>>(a);
+  const int grid = (a.n_slots + warps - 1) / warps;
+  kern<<<grid, warps * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
-template <int KB, int VB, int WARPS>
-cudaError_t launch_rep(const MmaArgs& a, int nrep, cudaStream_t s) {
+template <int KB, int VB, bool MIX>
+cudaError_t launch_rep(const MmaArgs& a, int nrep, int warps, cudaStream_t s) {
   switch (nrep) {
-    case 1: return launch_cfg<KB, VB, 1, WARPS>(a, s);
-    case 2: return launch_cfg<KB, VB, 2, WARPS>(a, s);
-    case 4: return launch_cfg<KB, VB, 4, WARPS>(a, s);
-    case 8: return launch_cfg<KB, VB, 8, WARPS>(a, s);
+    case 1: return launch_cfg<KB, VB, 1, MIX>(a, warps, s);
+    case 2: return launch_cfg<KB, VB, 2, MIX>(a, warps, s);
+    case 4: return launch_cfg<KB, VB, 4, MIX>(a, warps, s);
+    case 8: return launch_cfg<KB, VB, 8, MIX>(a, warps, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -884,7 +1041,7 @@ int mma_warps_per_cta(int rec_bytes) {
   // 227 KB of shared memory a block may use; at most 12 warps so a thread
   // keeps up to 168 registers
   const int per = rec_bytes + kWarpExtra;
-  return max(1, min(12, (227 * 1024) / per));
+  return max(1, min(kMaxWarps, (227 * 1024) / per));
 }
 
 bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int rec_bytes,
@@ -939,13 +1096,20 @@ cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, flo
   a.ws = ws;
   const int nrep = Hq / c->cfg.kv_heads;
   const int kb = c->cfg.k_bits, vb = c->cfg.v_bits;
-  if (mma_warps_per_cta(c->lay.bytes) != (kb == 2 && vb == 2 ? 12 : kb == 4 && vb == 4 ? 9 : 11))
-    return cudaErrorInvalidConfiguration;
+  const int warps = mma_warps_per_cta(c->lay.bytes);
   cudaError_t e;
-  if (kb == 2 && vb == 2) e = launch_rep<2, 2, 12>(a, nrep, s);
-  else if (kb == 2 && vb == 4) e = launch_rep<2, 4, 11>(a, nrep, s);
-  else if (kb == 4 && vb == 2) e = launch_rep<4, 2, 11>(a, nrep, s);
-  else e = launch_rep<4, 4, 9>(a, nrep, s);
+  if (c->cfg.k_mode == KVQ_K_MIXED) {
+    if (vb == 2) e = launch_rep<2, 2, true>(a, nrep, warps, s);
+    else e = launch_rep<2, 4, true>(a, nrep, warps, s);
+  } else if (kb == 2 && vb == 2) {
+    e = launch_rep<2, 2, false>(a, nrep, warps, s);
+  } else if (kb == 2 && vb == 4) {
+    e = launch_rep<2, 4, false>(a, nrep, warps, s);
+  } else if (kb == 4 && vb == 2) {
+    e = launch_rep<4, 2, false>(a, nrep, warps, s);
+  } else {
+    e = launch_rep<4, 4, false>(a, nrep, warps, s);
+  }
   if (e != cudaSuccess) return e;
   combine_parts_kernel<<<c->cfg.batch * Hq, kD, 0, s>>>(ws, a.Hkv, Hq, a.max_parts, a.unit_len,
                                                         a.total, a.n_slots, out);

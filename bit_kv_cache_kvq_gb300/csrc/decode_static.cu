@@ -52,7 +52,6 @@ extern "C" int kvq_decode_attention_static(const kvq_cache* c, const kvq_bf16* q
   if (Hq < 1 || Hq % c->cfg.kv_heads) return KVQ_ERR_SHAPE;
   const int n_rep = Hq / c->cfg.kv_heads;
   if (n_rep != 1 && n_rep != 2 && n_rep != 4 && n_rep != 8) return KVQ_ERR_SHAPE;
-  if (c->cfg.k_mode != KVQ_K_UNIFORM) return KVQ_ERR_MODE;
   if (c->t_q + c->r == 0) return KVQ_ERR_EMPTY;
 
   // Plan the split so its partials fit the fixed array; reject what cannot

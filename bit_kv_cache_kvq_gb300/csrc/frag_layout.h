@@ -84,6 +84,14 @@ __host__ __device__ inline CodePos key_code_pos(int tok, int ch, int bits) {
   return {((mt * 4 + (ks >> 1)) * 32 + lane) * 2 + (ks & 1), 4 * nibble_4bit(reg) + 16 * half};
 }
 
+// Mixed keys: 2-bit virtual channel v of token tok, kw2 words per (tile,
+// lane) instead of 4 (the uniform 2-bit key layout is the case kw2 = 4).
+__host__ __device__ inline CodePos mixed_code_pos(int tok, int v, int kw2) {
+  int mt, ks, lane, reg, half;
+  frag_coords(tok, v, mt, ks, lane, reg, half);
+  return {(mt * kw2 + (ks >> 1)) * 32 + lane, 2 * pair_2bit(ks & 1, reg) + 16 * half};
+}
+
 // Value code of token tok, channel ch (rows = channels, columns = tokens).
 __host__ __device__ inline CodePos value_code_pos(int tok, int ch, int bits) {
   int mc, kt, lane, reg, half;
@@ -121,6 +129,14 @@ __host__ __device__ inline void key_word_code(int w, int s, int bits, int& tok, 
     reg = reg_of_nibble(s & 3);
   }
   frag_rowcol(tile, k, lane, reg, half, tok, ch);
+}
+
+// Mixed key word w, code slot s -> (tok, virtual channel v).
+__host__ __device__ inline void mixed_word_code(int w, int s, int kw2, int& tok, int& v) {
+  const int lane = w & 31, q = w >> 5;
+  const int tile = q / kw2, wi = q % kw2;
+  const int P = s & 7;
+  frag_rowcol(tile, 2 * wi + k_local_of_pair(P), lane, reg_of_pair(P), s >> 3, tok, v);
 }
 
 // Value word w, code slot s -> (tok, ch).

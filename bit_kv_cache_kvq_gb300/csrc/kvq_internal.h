@@ -33,11 +33,15 @@ constexpr int kMaxRep = 8;         // query heads per KV head
 //   [kc+4D]        kmin     bf16  [D]
 // Mixed key (n_bf16 = nb, n_uint4 = n4, n_uint2 = n2):
 //   [0]            perm     uint8 [D]   BF16, UINT4, UINT2 channels, ascending
-//   [D]            raw      bf16  [nb][128]
-//   [..]           c4       uint8 [n4][64]
-//   [..]           c2       uint8 [n2][32]
-//   [..]           s4, s2   fp32  [n4], [n2]
-//   [..]           m4, m2   bf16  [n4], [n2]      (padded to 16 bytes)
+//   [D]            raw      bf16  [nb][128] channel-major; the 16-byte piece
+//                           p of tier channel i sits at piece p ^ (i & 7)
+//   [kc]           codes    2-bit "virtual channels" in the key fragment
+//                           order (frag_layout.h) with kw2 words per (tile,
+//                           lane): v < n4 the low two bits of UINT4 channel
+//                           v, n4 <= v < 2 n4 its high two bits, then the
+//                           n2 UINT2 channels, zero up to 32 kw2 channels
+//   [..]           s4, s2   fp32  [n4], [n2]  (contiguous)
+//   [..]           m4, m2   bf16  [n4], [n2]  (contiguous; padded to 16 bytes)
 // Value (v_bits = vb), after the key part at offset kpart:
 //   [kpart]        V codes  128*128*vb/8 bytes in fragment order
 //   [+vc]          vscale   fp32  [128][D/32]
@@ -51,7 +55,8 @@ struct RecLayout {
   // key (uniform)
   int k_codes, k_scale, k_min;
   // key (mixed)
-  int perm, raw, c4, c2, s4, s2, m4, m2;
+  int perm, raw, kc, s4, s2, m4, m2;
+  int nv, kw2;  // virtual 2-bit channels (2 n4 + n2) and words per (tile, lane)
   int kpart;  // bytes of the key part
   // value
   int v_codes, v_scale, v_min;
@@ -77,9 +82,10 @@ __host__ __device__ inline RecLayout make_layout(int mixed, int kb, int vb,
     L.n2 = kD - nb - n4;
     L.perm = 0;
     L.raw = kD;
-    L.c4 = L.raw + nb * kKG * 2;
-    L.c2 = L.c4 + L.n4 * (kKG / 2);
-    L.s4 = L.c2 + L.n2 * (kKG / 4);
+    L.nv = 2 * n4 + L.n2;
+    L.kw2 = (L.nv + 31) / 32;
+    L.kc = align16(L.raw + nb * kKG * 2);
+    L.s4 = L.kc + L.kw2 * 8 * 32 * 4;
     L.s2 = L.s4 + 4 * L.n4;
     L.m4 = L.s2 + 4 * L.n2;
     L.m2 = L.m4 + 2 * L.n4;

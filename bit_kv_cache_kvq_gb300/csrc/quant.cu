@@ -131,24 +131,6 @@ __device__ __forceinline__ void pack_words(const uint8_t* codes, uint32_t* dst) 
   }
 }
 
-// Codes of one Key channel, packed LSB first along tokens into dst (16-byte
-// aligned, 128*bits/8 bytes): the canonical layout the mixed key tiers use.
-__device__ __forceinline__ void pack_channel(const uint16_t* sK, int d,
-                                             const Params& p, int bits,
-                                             uint8_t* dst) {
-  const int top = (1 << bits) - 1;
-  const int per = 32 / bits;
-  uint32_t* w = reinterpret_cast<uint32_t*>(dst);
-  for (int wi = 0; wi < kKG / per; ++wi) {
-    uint32_t acc = 0;
-    for (int i = 0; i < per; ++i) {
-      const int t = wi * per + i;
-      acc |= code_of(bf2f(sK[t * kD + d]), p, top) << (bits * i);
-    }
-    w[wi] = acc;
-  }
-}
-
 // Value groups: one warp per (token, 32-channel group); lane = channel.
 template <int VB>
 __device__ __forceinline__ unsigned value_groups(const QuantArgs& a,
@@ -218,22 +200,31 @@ __global__ void __launch_bounds__(256) quantize_uniform_kernel(QuantArgs a) {
 // Mixed keys (MixKVQ KeyQuant): per channel S_d = fl32(fl32(M - m)/3) over
 // the tile, A_d = fl32(I_d * S_d); tiers by rank (A descending, channel
 // ascending on ties): n_bf16 BF16, n_uint4 UINT4, rest UINT2.  Storage
-// order BF16, UINT4, UINT2 channels, each ascending.
+// order BF16, UINT4, UINT2 channels, each ascending (the permutation).  The
+// BF16 tier is stored raw, channel-major and piece-swizzled; the UINT4 and
+// UINT2 codes become 2-bit virtual channels (kvq_internal.h), staged as
+// bytes cKv[tok][v] and packed in the key fragment order.
 template <int VB>
 __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
+  const RecLayout& L = a.lay;
+  const int kvs = 32 * L.kw2;   // staged virtual channels per token
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem);
   uint16_t* sV = sK + kKG * kD;
-  uint8_t* cV = reinterpret_cast<uint8_t*>(sV + kKG * kD) + kKG * kD;
+  uint8_t* cV = reinterpret_cast<uint8_t*>(sV + kKG * kD);
+  uint8_t* cKv = cV + kKG * kD;
   __shared__ uint32_t sKey[kD];
   __shared__ uint8_t sTier[kD];
   load_tiles(a, sK, sV);
+  // zero the padding virtual channels
+  const int pad = kvs - L.nv;
+  for (int i = threadIdx.x; i < kKG * pad; i += blockDim.x)
+    cKv[(i / pad) * kvs + L.nv + i % pad] = 0;
   __syncthreads();
 
   const int u = blockIdx.y;
   uint8_t* rec = a.records + (static_cast<long long>(u) * a.max_groups +
                               a.first_group + blockIdx.x) * a.rec_bytes;
-  const RecLayout& L = a.lay;
   unsigned flags = 0;
   if (threadIdx.x < kD) {
     const int d = threadIdx.x;
@@ -268,27 +259,44 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
     rec[L.perm + slot] = static_cast<uint8_t>(d);
     if (tier == KVQ_TIER_BF16) {
       uint16_t* raw = reinterpret_cast<uint16_t*>(rec + L.raw) + slot * kKG;
-      for (int t = 0; t < kKG; ++t) raw[t] = sK[t * kD + d];
+      for (int t = 0; t < kKG; ++t) raw[(((t >> 3) ^ (slot & 7)) << 3) | (t & 7)] = sK[t * kD + d];
     } else {
       const int bits = tier == KVQ_TIER_UINT4 ? 4 : 2;
-      const Params p = group_params(lo, hi, (1 << bits) - 1, bad);
+      const int top = (1 << bits) - 1;
+      const Params p = group_params(lo, hi, top, bad);
       flags |= p.flags;
+      const int j = slot - L.nb;   // index among the quantized channels
+      reinterpret_cast<float*>(rec + L.s4)[j] = p.step;
+      reinterpret_cast<uint16_t*>(rec + L.m4)[j] = f2bf_bits(p.m);
       if (bits == 4) {
-        const int j = slot - L.nb;
-        pack_channel(sK, d, p, 4, rec + L.c4 + j * (kKG / 2));
-        reinterpret_cast<float*>(rec + L.s4)[j] = p.step;
-        reinterpret_cast<uint16_t*>(rec + L.m4)[j] = f2bf_bits(p.m);
+        for (int t = 0; t < kKG; ++t) {
+          const uint32_t c = code_of(bf2f(sK[t * kD + d]), p, top);
+          cKv[t * kvs + j] = static_cast<uint8_t>(c & 3u);
+          cKv[t * kvs + L.n4 + j] = static_cast<uint8_t>(c >> 2);
+        }
       } else {
-        const int j = slot - L.nb - L.n4;
-        pack_channel(sK, d, p, 2, rec + L.c2 + j * (kKG / 4));
-        reinterpret_cast<float*>(rec + L.s2)[j] = p.step;
-        reinterpret_cast<uint16_t*>(rec + L.m2)[j] = f2bf_bits(p.m);
+        for (int t = 0; t < kKG; ++t)
+          cKv[t * kvs + L.n4 + j] = static_cast<uint8_t>(code_of(bf2f(sK[t * kD + d]), p, top));
       }
     }
   } else {
     flags = value_groups<VB>(a, sV, cV, rec, 4, 4);
   }
   __syncthreads();
+  {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(rec + L.kc);
+    const int words = 8 * L.kw2 * 32;
+    for (int w = threadIdx.x; w < words; w += blockDim.x) {
+      uint32_t acc = 0;
+#pragma unroll
+      for (int s2 = 0; s2 < 16; ++s2) {
+        int tok, v;
+        mixed_word_code(w, s2, L.kw2, tok, v);
+        acc |= static_cast<uint32_t>(cKv[tok * kvs + v]) << (2 * s2);
+      }
+      dst[w] = acc;
+    }
+  }
   pack_words<VB, false>(cV, reinterpret_cast<uint32_t*>(rec + a.lay.v_codes));
   if (flags) atomicOr(a.status, flags);
 }
@@ -351,6 +359,48 @@ __global__ void export_codes_kernel(const uint8_t* __restrict__ records, long lo
   }
 }
 
+// Canonical export of mixed key groups [u][0..n): raw [u][n][nb][128] in
+// token order, UINT4 codes [u][n][n4][64] and UINT2 codes [u][n][n2][32],
+// LSB first along tokens, rebuilt from the virtual 2-bit channels.
+__global__ void export_mixed_kernel(const uint8_t* __restrict__ records, long long rec_bytes,
+                                    int max_groups, RecLayout L, uint16_t* raw, uint8_t* c4,
+                                    uint8_t* c2, int n) {
+  const int g = blockIdx.x;
+  const int u = blockIdx.y;
+  const uint8_t* rec = records + (static_cast<long long>(u) * max_groups + g) * rec_bytes;
+  const long long ug = static_cast<long long>(u) * n + g;
+  const uint16_t* rraw = reinterpret_cast<const uint16_t*>(rec + L.raw);
+  for (int e = threadIdx.x; e < L.nb * kKG; e += blockDim.x) {
+    const int i = e >> 7, t = e & 127;
+    raw[ug * L.nb * kKG + e] = rraw[i * kKG + ((((t >> 3) ^ (i & 7)) << 3) | (t & 7))];
+  }
+  const uint32_t* words = reinterpret_cast<const uint32_t*>(rec + L.kc);
+  auto code2 = [&](int tok, int v) {
+    const CodePos p = mixed_code_pos(tok, v, L.kw2);
+    return (words[p.word] >> p.bit) & 3u;
+  };
+  const int j = threadIdx.x;
+  if (j < L.n4) {
+    uint8_t* out = c4 + (ug * L.n4 + j) * (kKG / 2);
+    for (int i = 0; i < kKG / 2; ++i) {
+      uint32_t byte = 0;
+      for (int e = 0; e < 2; ++e) {
+        const int t = 2 * i + e;
+        byte |= (code2(t, j) | (code2(t, L.n4 + j) << 2)) << (4 * e);
+      }
+      out[i] = static_cast<uint8_t>(byte);
+    }
+  } else if (j < L.n4 + L.n2) {
+    const int jj = j - L.n4;
+    uint8_t* out = c2 + (ug * L.n2 + jj) * (kKG / 4);
+    for (int i = 0; i < kKG / 4; ++i) {
+      uint32_t byte = 0;
+      for (int e = 0; e < 4; ++e) byte |= code2(4 * i + e, 2 * L.n4 + jj) << (2 * e);
+      out[i] = static_cast<uint8_t>(byte);
+    }
+  }
+}
+
 cudaError_t export_codes(const kvq_cache* c, int off, int bits, bool key, void* dst,
                          cudaStream_t s) {
   const int n = c->t_q / kKG;
@@ -376,9 +426,8 @@ cudaError_t gather(const kvq_cache* c, int off, int bytes, void* dst,
 constexpr int kQuantSmem = 2 * kKG * kD * 2 + 2 * kKG * kD;  // bf16 tiles + staged codes, 96 KB
 
 template <typename K>
-cudaError_t set_smem(K kernel) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kQuantSmem);
+cudaError_t set_smem(K kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 }  // namespace
@@ -409,23 +458,24 @@ cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
   const dim3 grid(n_groups, c->cfg.batch * c->cfg.kv_heads);
   const int kb = c->cfg.k_bits, vb = c->cfg.v_bits;
   cudaError_t e = cudaSuccess;
-#define KVQ_LAUNCH(KERNEL)                                   \
+#define KVQ_LAUNCH(KERNEL, SMEM)                             \
   do {                                                       \
-    e = set_smem(KERNEL);                                    \
+    e = set_smem(KERNEL, SMEM);                              \
     if (e != cudaSuccess) return e;                          \
-    KERNEL<<<grid, 256, kQuantSmem, s>>>(a);                 \
+    KERNEL<<<grid, 256, SMEM, s>>>(a);                       \
   } while (0)
   if (c->cfg.k_mode == KVQ_K_MIXED) {
-    if (vb == 2) KVQ_LAUNCH(quantize_mixed_kernel<2>);
-    else KVQ_LAUNCH(quantize_mixed_kernel<4>);
+    const int smem = 2 * kKG * kD * 2 + kKG * kD + kKG * 32 * c->lay.kw2;
+    if (vb == 2) KVQ_LAUNCH(quantize_mixed_kernel<2>, smem);
+    else KVQ_LAUNCH(quantize_mixed_kernel<4>, smem);
   } else if (kb == 2 && vb == 2) {
-    KVQ_LAUNCH((quantize_uniform_kernel<2, 2>));
+    KVQ_LAUNCH((quantize_uniform_kernel<2, 2>), kQuantSmem);
   } else if (kb == 2 && vb == 4) {
-    KVQ_LAUNCH((quantize_uniform_kernel<2, 4>));
+    KVQ_LAUNCH((quantize_uniform_kernel<2, 4>), kQuantSmem);
   } else if (kb == 4 && vb == 2) {
-    KVQ_LAUNCH((quantize_uniform_kernel<4, 2>));
+    KVQ_LAUNCH((quantize_uniform_kernel<4, 2>), kQuantSmem);
   } else {
-    KVQ_LAUNCH((quantize_uniform_kernel<4, 4>));
+    KVQ_LAUNCH((quantize_uniform_kernel<4, 4>), kQuantSmem);
   }
 #undef KVQ_LAUNCH
   return cudaGetLastError();
@@ -471,11 +521,15 @@ cudaError_t launch_export_k_mixed(const kvq_cache* c, uint8_t* perm,
                                   float* s2, cudaStream_t s) {
   const RecLayout& L = c->lay;
   cudaError_t e = gather(c, L.perm, kD, perm, s);
-  if (e == cudaSuccess) e = gather(c, L.raw, L.nb * kKG * 2, raw, s);
-  if (e == cudaSuccess) e = gather(c, L.c4, L.n4 * kKG / 2, c4, s);
+  const int n = c->t_q / kKG;
+  const int units = c->cfg.batch * c->cfg.kv_heads;
+  if (e == cudaSuccess && n > 0) {
+    export_mixed_kernel<<<dim3(n, units), 128, 0, s>>>(
+        c->records, c->lay.bytes, c->max_groups, L, reinterpret_cast<uint16_t*>(raw), c4, c2, n);
+    e = cudaGetLastError();
+  }
   if (e == cudaSuccess) e = gather(c, L.m4, L.n4 * 2, m4, s);
   if (e == cudaSuccess) e = gather(c, L.s4, L.n4 * 4, s4, s);
-  if (e == cudaSuccess) e = gather(c, L.c2, L.n2 * kKG / 4, c2, s);
   if (e == cudaSuccess) e = gather(c, L.m2, L.n2 * 2, m2, s);
   if (e == cudaSuccess) e = gather(c, L.s2, L.n2 * 4, s2, s);
   return e;

@@ -183,6 +183,8 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int Hq);
  * dequantized history followed by the residual tokens, p = softmax over all
  * of them together, o = sum_t p_t v^_t.  q: bf16 [B][Hq][D], Hq a multiple
  * of Hkv (at most 8 query heads per KV head); out: fp32 [B][Hq][D].
+ * Uniform and mixed (MixKVQ) key caches alike: in a mixed group k^ is the
+ * raw bf16 key on the BF16 tier and the dequantized code on the others.
  * ws: device scratch of >= kvq_decode_workspace_bytes(cache, Hq), not
  * aliased with any argument; its contents are overwritten.
  * Errors: ARG, SHAPE, EMPTY, WORKSPACE, CUDA.

@@ -110,3 +110,40 @@ def assert_uniform_exports_equal(cache: kvq.KVCache, ref: UnitOracles):
         r = oc.r
         assert np.array_equal(krb[b, h], oc.res_k[0, :r]), f"K residual differs (unit {u})"
         assert np.array_equal(vrb[b, h], oc.res_v[0, :r]), f"V residual differs (unit {u})"
+
+
+def assert_mixed_exports_equal(cache: kvq.KVCache, ref: UnitOracles):
+    """Mixed keys: permutation, raw BF16 tier, UINT4/UINT2 codes, origins and
+    steps per group; values and residual as in the uniform case."""
+    t = cache.export_k_mixed()
+    vc, vm, vs = cache.export_v()
+    kr, vr = cache.export_residual()
+    torch.cuda.synchronize()
+    perm, c4, c2 = t["perm"].cpu().numpy(), t["c4"].cpu().numpy(), t["c2"].cpu().numpy()
+    raw, m4, m2 = bf16_bits(t["raw"]), bf16_bits(t["m4"]), bf16_bits(t["m2"])
+    s4, s2 = f32_bits(t["s4"]), f32_bits(t["s2"])
+    vc, vm, vs = vc.cpu().numpy(), bf16_bits(vm), f32_bits(vs)
+    krb, vrb = bf16_bits(kr), bf16_bits(vr)
+    for u, oc in zip(ref.units, ref.caches):
+        b, h = divmod(u, ref.Hkv)
+        groups = oc.k_groups[0]
+        assert perm.shape[2] == len(groups)
+        for gi, grp in enumerate(groups):
+            where = f"(unit {u}, group {gi})"
+            assert np.array_equal(perm[b, h, gi], grp.perm), f"permutation differs {where}"
+            assert np.array_equal(raw[b, h, gi], grp.raw), f"BF16 tier differs {where}"
+            assert np.array_equal(c4[b, h, gi], grp.c4), f"UINT4 codes differ {where}"
+            assert np.array_equal(m4[b, h, gi], grp.m4), f"UINT4 origins differ {where}"
+            assert np.array_equal(s4[b, h, gi], grp.s4.view(np.uint32)), f"UINT4 steps differ {where}"
+            assert np.array_equal(c2[b, h, gi], grp.c2), f"UINT2 codes differ {where}"
+            assert np.array_equal(m2[b, h, gi], grp.m2), f"UINT2 origins differ {where}"
+            assert np.array_equal(s2[b, h, gi], grp.s2.view(np.uint32)), f"UINT2 steps differ {where}"
+        parts = oc.v_parts[0]
+        if parts:
+            ovc, ovm, ovs = (np.concatenate([p[i] for p in parts]) for i in range(3))
+            assert np.array_equal(vc[b, h], ovc), f"V codes differ (unit {u})"
+            assert np.array_equal(vm[b, h], ovm), f"V origins differ (unit {u})"
+            assert np.array_equal(vs[b, h], ovs.view(np.uint32)), f"V steps differ (unit {u})"
+        r = oc.r
+        assert np.array_equal(krb[b, h], oc.res_k[0, :r]), f"K residual differs (unit {u})"
+        assert np.array_equal(vrb[b, h], oc.res_v[0, :r]), f"V residual differs (unit {u})"
