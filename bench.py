@@ -140,18 +140,26 @@ def kernel_source_hash():
 
 
 # ------------------------------------------------------ algorithmic bytes
-def bytes_per_token(bits):  # packed K + V, per quantized token per KV head
-    D = 128
-    return (D * bits // 8 + D * 6 // 128) + (D * bits // 8 + (D // 32) * 6)
+def mixed_k_group_bytes(w):
+    """Mixed key group: permutation, raw BF16 tier, UINT4 and UINT2 codes and
+    an (fp32 step, bf16 origin) per quantized channel (7100 B at 6/25/97)."""
+    n2 = 128 - w.n_bf16 - w.n_uint4
+    return 128 + w.n_bf16 * 256 + w.n_uint4 * 64 + n2 * 32 + (w.n_uint4 + n2) * 6
+
+
+def token_bytes(w):
+    """Algorithmic bytes of one quantized token of one (b, kv head)."""
+    v = 128 * w.v_bits // 8 + 24
+    if w.mode == "mixed":
+        return mixed_k_group_bytes(w) / 128 + v
+    return 128 * w.k_bits // 8 + 6 + v
 
 
 def attention_bytes(w, T_q, r):
     """Packed cache + bf16 residual + q (bf16) + o (fp32) of one decode
     attention call."""
     U = w.B * w.Hkv
-    per_tok = bytes_per_token(w.k_bits) if w.k_bits == w.v_bits else \
-        (128 * w.k_bits // 8 + 6) + (128 * w.v_bits // 8 + 24)
-    return U * (T_q * per_tok + r * 512) + w.B * w.Hq * (256 + 512)
+    return U * (T_q * token_bytes(w) + r * 512) + w.B * w.Hq * (256 + 512)
 
 
 def append_bytes(w):
@@ -159,10 +167,7 @@ def append_bytes(w):
 
 
 def flush_bytes(w):
-    U = w.B * w.Hkv
-    per_tok = bytes_per_token(w.k_bits) if w.k_bits == w.v_bits else \
-        (128 * w.k_bits // 8 + 6) + (128 * w.v_bits // 8 + 24)
-    return U * (128 * 512 + 128 * per_tok)
+    return w.B * w.Hkv * 128 * (512 + token_bytes(w))
 
 
 # ---------------------------------------------------------------- arms
@@ -183,6 +188,9 @@ def config_of(w, extra=None):
     c = {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": 128,
          "quantized_tokens": w.T_q, "residual_tokens": w.r, "k_bits": w.k_bits,
          "v_bits": w.v_bits, "k_group_tokens": 128, "v_group_channels": 32}
+    if w.mode == "mixed":
+        c.update({"k_mode": "mixed", "n_bf16": w.n_bf16, "n_uint4": w.n_uint4,
+                  "n_uint2": 128 - w.n_bf16 - w.n_uint4, "query_window": w.Lq})
     if extra:
         c.update(extra)
     return c
@@ -195,15 +203,20 @@ class OracleSample:
 
     def __init__(self, w, n_units):
         import oracle as orc
-        from bit_kv_cache_kvq_gb300.workloads import bf16_bits, make_kv, make_q, scaled
+        from bit_kv_cache_kvq_gb300.workloads import (bf16_bits, make_kv, make_q,
+                                                      make_query_window, scaled)
         oracle_mod = orc
         self.one = scaled(w, B=1, Hkv=1, Hq=w.n_rep, k_outliers=min(w.k_outliers, 4))
         self.units = []
         for j in range(n_units):
             u = scaled(self.one, seed=self.one.seed + 17 * j)
             K, V = make_kv(u)
-            c = oracle_mod.OracleCache(1, 1, 128, u.k_bits, u.v_bits)
-            c.prefill(bf16_bits(K), bf16_bits(V))
+            c = oracle_mod.OracleCache(1, 1, 128, u.k_bits, u.v_bits, mode=u.mode,
+                                       n_bf16=u.n_bf16, n_uint4=u.n_uint4)
+            imp = None
+            if u.mode == "mixed":
+                imp = orc.importance(bf16_bits(make_query_window(u)[0]))[None, None]
+            c.prefill(bf16_bits(K), bf16_bits(V), imp)
             self.units.append((u, c, [bf16_bits(make_q(u, step=s)) for s in range(4)]))
         self.calls = 0
 
@@ -262,7 +275,8 @@ def run_ours(args, rank, world):
     import torch
     import bit_kv_cache_kvq_gb300 as kvq
     from bit_kv_cache_kvq_gb300 import _build
-    from bit_kv_cache_kvq_gb300.workloads import make_kv, make_q, make_token, scaled
+    from bit_kv_cache_kvq_gb300.workloads import (make_kv, make_q, make_query_window,
+                                                  make_token, scaled)
 
     _build.build()
     kvq.lib()
@@ -270,25 +284,47 @@ def run_ours(args, rank, world):
     w0 = workload_from(args)
     w = scaled(w0, seed=w0.seed + 100 * rank)     # weak scaling: each rank its own batch
     K, W = args.steps, args.warmup
-    if W > w.r:
-        raise SystemExit("--warmup must not exceed the residual tokens of the workload")
     n_flush = (w.r + K) // 128                     # flushes inside the timed steps
     T0 = max(0, w.T_q - 128 * (n_flush // 2))     # mean context over the timed steps ~ workload's
-    r0 = w.r - W
+    L0 = T0 + w.r - W                              # prefill; the warm-up appends reach T0 + r
+    if L0 < 0:
+        raise SystemExit("--warmup exceeds the workload's tokens")
     cap = T0 + 128 * (n_flush + 2)
 
     Kall, Vall = make_kv(w, L=w.T_q + w.r, device=dev)
     toks = [make_token(w, i, device=dev) for i in range(W + K)]
     n_q = min(W + K, 64)
     qs = [make_q(w, step=i, device=dev) for i in range(n_q)]
-    cache = kvq.KVCache(w.B, w.Hkv, cap, w.k_bits, w.v_bits, device=dev)
+    importance = None
+    if w.mode == "mixed":   # MixKVQ: I_d from the query window, on the GPU
+        importance, _, _ = kvq.channel_saliency(make_query_window(w, device=dev),
+                                                Kall[:, :, :128].contiguous(), 2,
+                                                n_bf16=w.n_bf16, n_uint4=w.n_uint4)
+    cache = kvq.KVCache(w.B, w.Hkv, cap, w.k_bits, w.v_bits, mode=w.mode, n_bf16=w.n_bf16,
+                        n_uint4=w.n_uint4, device=dev)
     out = torch.empty(w.B, w.Hq, 128, dtype=torch.float32, device=dev)
     ws = cache.workspace(w.Hq)
     stream = torch.cuda.current_stream()
+    K0, V0 = Kall[:, :, :L0].contiguous(), Vall[:, :, :L0].contiguous()
 
     def prefill():
         cache.reset()
-        cache.prefill(Kall[:, :, :T0 + r0].contiguous(), Vall[:, :, :T0 + r0].contiguous())
+        cache.prefill(K0, V0, importance=importance)
+
+    # prefill quantize (kvq_quantize_prefill) on its own: bf16 K, V read once,
+    # packed groups written, the L mod 128 tail copied to the residual
+    for _ in range(2):
+        prefill()
+    pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p_reps = 5
+    pa.record(stream)
+    for _ in range(p_reps):
+        prefill()
+    pb.record(stream)
+    torch.cuda.synchronize()
+    prefill_us = 1e3 * pa.elapsed_time(pb) / p_reps
+    n_grp = L0 // 128
+    prefill_nb = w.B * w.Hkv * (L0 * 512 + n_grp * 128 * token_bytes(w) + (L0 % 128) * 512)
 
     def step(i, ev=None):
         """One decode step; returns (launches, algorithmic bytes)."""
@@ -296,7 +332,7 @@ def run_ours(args, rank, world):
         cache.append(kn, vn)
         launches, nb = 1, append_bytes(w)
         if cache.lengths()[1] == 128:
-            cache.flush()
+            cache.flush(importance=importance)
             launches += 1
             nb += flush_bytes(w)
         tq, r = cache.lengths()
@@ -308,6 +344,8 @@ def run_ours(args, rank, world):
         return launches + 2, nb + attention_bytes(w, tq, r), attention_bytes(w, tq, r)
 
     prefill()
+    if args.no_e2e:
+        del K0, V0
     if args.no_bf16 and args.no_e2e:       # keep device memory small (profiling)
         del Kall, Vall
         torch.cuda.empty_cache()
@@ -367,6 +405,10 @@ def run_ours(args, rank, world):
                      "kernel_source": src_hash},
         "gpu_launches": launches,
         "clocks": clk.summary(),
+        "prefill": {"tokens": L0, "us": prefill_us,
+                    "gbs": prefill_nb / (prefill_us * 1e-6) / 1e9,
+                    "algorithmic_bytes": prefill_nb,
+                    "note": "kvq_quantize_prefill alone, outside the timed decode steps"},
     }
 
     # bf16 unquantized comparator at the same batch and context
@@ -407,7 +449,7 @@ def run_ours(args, rank, world):
             cache.append(d_k, d_v)
             nb = append_bytes(w)
             if cache.lengths()[1] == 128:
-                cache.flush()
+                cache.flush(importance=importance)
                 nb += flush_bytes(w)
             tq, r = cache.lengths()
             cache.attention(d_q, out=out, workspace=ws)

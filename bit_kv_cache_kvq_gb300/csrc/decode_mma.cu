@@ -53,13 +53,18 @@ constexpr float kInvCodeUnit = 1.0f / 512.0f;
 // part): the value-step table (256 words), the value-origin table (4 rows of
 // 72 words) and the unit's query, [8 heads][136] bf16 or, with at most 4
 // heads per KV head, [4 heads][136] fp32 pre-scaled by log2(e)/sqrt(D)
-// (rows padded so head rows fall in different banks).
+// (rows padded so head rows fall in different banks).  The padding of the
+// first row, never read as query, holds the 16 zero bytes ldmatrix reads
+// for absent rows.
 constexpr int kVsbBytes = 256 * 4;
 constexpr int kVmbBytes = 4 * 72 * 4;
 constexpr int kQRow = 136;
 constexpr int kQBytes = 8 * kQRow * 2;   // = 4 * kQRow * 4
-constexpr int kZeroBytes = 16;           // a zero row for ldmatrix padding
-constexpr int kWarpExtra = kVsbBytes + kVmbBytes + kQBytes + kZeroBytes;
+// Per-warp regions stay multiples of 128 bytes: cp.async copies of 128-byte
+// aligned record lines into misaligned shared memory cost ~10% of the
+// decode time.
+constexpr int kWarpExtra = kVsbBytes + kVmbBytes + kQBytes;
+static_assert(kWarpExtra % 128 == 0, "per-warp extra must keep 128-byte alignment");
 constexpr int kMaxWarps = 12;           // warps per block: up to 168 registers a thread
 
 __device__ __forceinline__ float bf2f(uint32_t b16) { return __uint_as_float(b16 << 16); }
@@ -218,7 +223,7 @@ struct Warp {
   uint32_t* vsb;   // value-step table, B order (vsb_index)
   uint32_t* vmb;   // value-origin table, A order (vmb_index)
   void* qs;        // the unit's query (see kQBytes)
-  uint8_t* zero16; // 16 zero bytes
+  // mixed keys only:
   const uint16_t* qg_row;  // this lane's query head (g, capped at NREP - 1) in global memory
   float qmax;      // max |query| of the head row this lane builds B columns for
 
@@ -236,9 +241,16 @@ struct Warp {
     vsb = reinterpret_cast<uint32_t*>(base + rb);
     vmb = reinterpret_cast<uint32_t*>(base + rb + kVsbBytes);
     qs = base + rb + kVsbBytes + kVmbBytes;
-    zero16 = base + rb + kVsbBytes + kVmbBytes + kQBytes;
-    if (lane < 4) reinterpret_cast<uint32_t*>(zero16)[lane] = 0u;
-    __syncwarp();
+    if (MIX) {
+      if (lane < 4) reinterpret_cast<uint32_t*>(zero_row())[lane] = 0u;
+      __syncwarp();
+    }
+  }
+
+  // 16 zero bytes in the padding of query row 0 (fp32 rows: 128 floats used
+  // of 136; bf16 rows: 128 of 136)
+  __device__ __forceinline__ uint8_t* zero_row() const {
+    return static_cast<uint8_t*>(qs) + (SPARE ? kD * 4 : kD * 2);
   }
 
   // x rounded to 11 significant bits (an f16 value for the normalized
@@ -257,7 +269,7 @@ struct Warp {
   __device__ __forceinline__ void begin_unit(int u) {
     const int b = u / a.Hkv, kvh = u % a.Hkv;
     const uint16_t* qg = a.q + (static_cast<long long>(b) * a.Hq + kvh * NREP) * kD;
-    qg_row = qg + min(g, NREP - 1) * kD;
+    if (MIX) qg_row = qg + min(g, NREP - 1) * kD;
     const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
     __syncwarp();
     if (SPARE) {   // fp32 [4][kQRow], pre-scaled
@@ -505,7 +517,7 @@ struct Warp {
     // ---- BF16 tier: raw keys (A, via ldmatrix.trans) times the exact query
     if (nb > 0) {
       const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(kbuf + L.raw));
-      const uint32_t zaddr = static_cast<uint32_t>(__cvta_generic_to_shared(zero16));
+      const uint32_t zaddr = static_cast<uint32_t>(__cvta_generic_to_shared(zero_row()));
       for (int k16 = 0; k16 < (nb + 15) >> 4; ++k16) {
         uint32_t qb[4];
 #pragma unroll
@@ -942,6 +954,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) decode_mma_kernel(MmaArgs a
   extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int slot = blockIdx.x * (blockDim.x >> 5) + warp;
+  // the combine kernel may be scheduled now; it waits for this grid's results
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   if (slot >= a.n_slots) return;            // warp-uniform
   uint8_t* mine = smem + static_cast<size_t>(warp) * (a.rec_bytes + kWarpExtra);
   Warp<KB, VB, NREP, MIX> W(a, mine);
@@ -984,10 +998,37 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) decode_mma_kernel(MmaArgs a
   }
 }
 
+// Block-wide reductions of the combine kernel (128 threads).
+__device__ __forceinline__ float block_max128(float x, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+  __syncthreads();
+  x = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  return x;
+}
+__device__ __forceinline__ float block_sum128(float x, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+  __syncthreads();
+  x = (red[0] + red[1]) + (red[2] + red[3]);
+  __syncthreads();
+  return x;
+}
+
+// Merge the partials (o, m, l) of one query head (block = (b, hq), thread =
+// channel) with the log-sum-exp rule: M = max m_k, w_k = 2^(m_k - M),
+// o = sum w_k o_k / sum w_k l_k.  Launched as a programmatic dependent of
+// the decode kernel: it may start while that kernel drains and waits for
+// its results with griddepcontrol.wait.
 __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restrict__ ws,
                                                            int Hkv, int Hq, int max_parts,
                                                            long long unit_len, long long total,
                                                            int n_slots, float* __restrict__ out) {
+  extern __shared__ float wk[];   // [parts] weights
+  __shared__ float red[4];
   const int row = blockIdx.x;                 // b * Hq + hq
   const int n_rep = Hq / Hkv;
   const int b = row / Hq, hq = row % Hq;
@@ -998,17 +1039,26 @@ __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restr
   const int n = last - first + 1;
   const float* base = ws + static_cast<long long>(u) * max_parts * n_rep * (kD + 2) + h * (kD + 2);
   const long long stride = static_cast<long long>(n_rep) * (kD + 2);
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   float M = -INFINITY;
-  for (int k = 0; k < n; ++k) M = fmaxf(M, base[k * stride + kD]);
-  float o = 0.0f, l = 0.0f;
-  for (int k = 0; k < n; ++k) {
+  for (int k = threadIdx.x; k < n; k += 128) M = fmaxf(M, base[k * stride + kD]);
+  M = block_max128(M, red);
+  float ls = 0.0f;
+  for (int k = threadIdx.x; k < n; k += 128) {
     const float mk = base[k * stride + kD];
-    if (mk == -INFINITY) continue;
-    const float w = exp2f(mk - M);
-    o = fmaf(w, base[k * stride + threadIdx.x], o);
-    l = fmaf(w, base[k * stride + kD + 1], l);
+    const float w = mk == -INFINITY ? 0.0f : exp2f(mk - M);
+    wk[k] = w;
+    ls = fmaf(w, base[k * stride + kD + 1], ls);
   }
-  out[static_cast<long long>(row) * kD + threadIdx.x] = o / l;
+  const float l = block_sum128(ls, red);   // its barriers also publish wk
+  float o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  int k = 0;
+  for (; k + 4 <= n; k += 4) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = fmaf(wk[k + i], base[(k + i) * stride + threadIdx.x], o[i]);
+  }
+  for (; k < n; ++k) o[0] = fmaf(wk[k], base[k * stride + threadIdx.x], o[0]);
+  out[static_cast<long long>(row) * kD + threadIdx.x] = ((o[0] + o[1]) + (o[2] + o[3])) / l;
 }
 
 template <int KB, int VB, int NREP, bool MIX>
@@ -1111,9 +1161,18 @@ cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, flo
     e = launch_rep<4, 4, false>(a, nrep, warps, s);
   }
   if (e != cudaSuccess) return e;
-  combine_parts_kernel<<<c->cfg.batch * Hq, kD, 0, s>>>(ws, a.Hkv, Hq, a.max_parts, a.unit_len,
-                                                        a.total, a.n_slots, out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(c->cfg.batch * Hq);
+  lc.blockDim = dim3(kD);
+  lc.dynamicSmemBytes = static_cast<size_t>(a.max_parts) * sizeof(float);
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, combine_parts_kernel, static_cast<const float*>(ws), a.Hkv, Hq,
+                            a.max_parts, a.unit_len, a.total, a.n_slots, out);
 }
 
 }  // namespace kvq

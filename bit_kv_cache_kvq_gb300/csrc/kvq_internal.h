@@ -46,7 +46,10 @@ constexpr int kMaxRep = 8;         // query heads per KV head
 //   [kpart]        V codes  128*128*vb/8 bytes in fragment order
 //   [+vc]          vscale   fp32  [128][D/32]
 //   [+vc+2048]     vmin     bf16  [128][D/32]
-// Every section starts on a 16-byte boundary.
+// Every section starts on a 16-byte boundary; the value part and the
+// record size are multiples of 128 bytes (uniform layouts are by
+// construction, mixed key parts are padded), so records and their parts
+// start on 128-byte lines.
 // ---------------------------------------------------------------------------
 struct RecLayout {
   int mixed;
@@ -89,7 +92,7 @@ __host__ __device__ inline RecLayout make_layout(int mixed, int kb, int vb,
     L.s2 = L.s4 + 4 * L.n4;
     L.m4 = L.s2 + 4 * L.n2;
     L.m2 = L.m4 + 2 * L.n4;
-    L.kpart = align16(L.m2 + 2 * L.n2);
+    L.kpart = (L.m2 + 2 * L.n2 + 127) & ~127;   // value part on a 128-byte line
   }
   L.v_codes = L.kpart;
   L.v_scale = L.v_codes + kKG * kD * vb / 8;

@@ -59,15 +59,15 @@ def test_mixed_record_bytes(lib):
     """Mixed keys, 6 BF16 / 25 UINT4 / 97 UINT2 channels: channel permutation
     (128 B) + raw bf16 + 4-bit and 2-bit codes + (fp32 step, bf16 origin) per
     quantized channel = 7100 B.  Stored as 2-bit virtual channels (two per
-    UINT4 channel): 147, zero-padded to 160 (13 x 32 B), then to 16 bytes;
-    values as uniform 2-bit."""
+    UINT4 channel): 147, zero-padded to 160 (13 x 32 B), then to a 128-byte
+    line; values as uniform 2-bit."""
     per_group = (_bytes(1, 1, 128 * 9, 2, 2, 1, 6, 25) - _bytes(1, 1, 128, 2, 2, 1, 6, 25)) / 8
     kpart = 128 + 6 * 128 * 2 + 25 * 64 + 97 * 32 + (25 + 97) * 6
     assert kpart == 7100
     padding = (160 - (2 * 25 + 97)) * 32
     v = orc.cache_bytes(T=128, rK=128, rV=0, D=128, k_bits=2, v_bits=2, Gk=128, Gv=32,
                         origin_bytes=2, step_bytes=4, float_bytes=0)
-    assert per_group == (kpart + padding + 15) // 16 * 16 + v
+    assert per_group == (kpart + padding + 127) // 128 * 128 + v
 
 
 def test_invalid_configs_report_zero_bytes(lib):
