@@ -19,7 +19,6 @@
 namespace kvq {
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ float bf2f(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
@@ -51,13 +50,6 @@ __device__ __forceinline__ Params group_params(float lo, float hi, int top,
   return p;
 }
 
-__device__ __forceinline__ uint32_t code_of(float x, const Params& p, int top) {
-  if (p.step == 0.0f) return 0u;
-  const float y = __fdiv_rn(__fsub_rn(x, p.m), p.step);
-  float r = rintf(y);  // round half to even
-  r = fminf(fmaxf(r, 0.0f), static_cast<float>(top));
-  return static_cast<uint32_t>(r);
-}
 
 __device__ __forceinline__ uint16_t f2bf_bits(float exact_bf16_value) {
   return static_cast<uint16_t>(__float_as_uint(exact_bf16_value) >> 16);
@@ -74,50 +66,135 @@ struct QuantArgs {
   unsigned* status;
 };
 
-// Stage one 128-token tile of K and V (bf16 [128][128] each) in shared memory.
-__device__ __forceinline__ void load_tiles(const QuantArgs& a, uint16_t* sK,
-                                           uint16_t* sV) {
-  const long long off = static_cast<long long>(blockIdx.y) * a.src.unit_stride +
-                        static_cast<long long>(blockIdx.x) * a.src.group_stride;
-  const uint4* gk = reinterpret_cast<const uint4*>(a.src.k + off);
-  const uint4* gv = reinterpret_cast<const uint4*>(a.src.v + off);
-  uint4* tk = reinterpret_cast<uint4*>(sK);
-  uint4* tv = reinterpret_cast<uint4*>(sV);
-  for (int i = threadIdx.x; i < kKG * kD * 2 / 16; i += blockDim.x) {
-    tk[i] = __ldg(gk + i);
-    tv[i] = __ldg(gv + i);
-  }
+// Staged tiles: bf16 [128 tokens][128 channels], the 16-byte piece ch/8 of
+// row t at piece (ch/8) ^ (t & 7), so column reads (a channel over tokens)
+// and row reads (a token's channels) are both free of bank conflicts.
+__device__ __forceinline__ int swz(int t, int ch) {
+  return t * kD + ((((ch >> 3) ^ (t & 7)) << 3) | (ch & 7));
 }
 
-// One Key channel over the tile's 128 tokens: min/max and finiteness.
-__device__ __forceinline__ void channel_range(const uint16_t* sK, int d,
-                                              float& lo, float& hi, bool& bad) {
+// Stage one 128-token tile of K and V in shared memory (cp.async, 16 bytes).
+__device__ __forceinline__ void load_tiles(const QuantArgs& a, uint16_t* sK, uint16_t* sV) {
+  const long long off = static_cast<long long>(blockIdx.y) * a.src.unit_stride +
+                        static_cast<long long>(blockIdx.x) * a.src.group_stride;
+  const uint8_t* gk = reinterpret_cast<const uint8_t*>(a.src.k + off);
+  const uint8_t* gv = reinterpret_cast<const uint8_t*>(a.src.v + off);
+  const uint32_t dk = static_cast<uint32_t>(__cvta_generic_to_shared(sK));
+  const uint32_t dv = static_cast<uint32_t>(__cvta_generic_to_shared(sV));
+  for (int i = threadIdx.x; i < kKG * kD * 2 / 16; i += blockDim.x) {
+    const int t = i >> 4, pc = i & 15;
+    const uint32_t o = static_cast<uint32_t>((t * 16 + (pc ^ (t & 7))) * 16);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dk + o), "l"(gk + 16 * i));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dv + o), "l"(gv + 16 * i));
+  }
+  asm volatile("cp.async.commit_group;\n" ::);
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+}
+
+// Per-group quantizer parameters kept for the code pass: origin m, step,
+// and rcp = RN(1 / step) (0 for a constant group).
+struct GroupQ {
+  float m, step, rcp;
+};
+
+__device__ __forceinline__ GroupQ make_q(const Params& p) {
+  return {p.m, p.step, p.step > 0.0f ? __frcp_rn(p.step) : 0.0f};
+}
+
+// c = clip(RNE(fl32(fl32(x - m) / step)), 0, top), bit-identical to the IEEE
+// quotient.  q' = RN(d * RN(1/step)) is within 2^-22 q of RN(d / step); the
+// code can differ only if a half-integer lies that close to q', and then
+// (or for a non-finite q') the exact quotient is taken.
+__device__ __forceinline__ uint32_t code_fast(float x, const GroupQ& g, int top) {
+  if (g.step == 0.0f) return 0u;
+  const float d = __fsub_rn(x, g.m);
+  float q = __fmul_rn(d, g.rcp);
+  const float n = rintf(q);
+  if (!(fabsf(fabsf(q - n) - 0.5f) > q * 4.76837158203125e-7f)) q = __fdiv_rn(d, g.step);
+  return static_cast<uint32_t>(fminf(fmaxf(rintf(q), 0.0f), static_cast<float>(top)));
+}
+
+// Key channel ranges: two threads per channel over 64 tokens each, merged
+// through shared memory.  Returns (for threads 0..127, channel = thread) the
+// range and finiteness of the channel over the tile.
+__device__ __forceinline__ void key_ranges(const uint16_t* sK, uint32_t* sRed, float& lo,
+                                           float& hi, bool& bad) {
+  const int ch = threadIdx.x & 127, hf = threadIdx.x >> 7;
   uint32_t kmin = 0xffffffffu, kmax = 0u;
-  bad = false;
-  for (int t = 0; t < kKG; ++t) {
-    const float x = bf2f(sK[t * kD + d]);
-    bad |= !isfinite(x);
+  bool b = false;
+  for (int t = 64 * hf; t < 64 * hf + 64; ++t) {
+    const float x = bf2f(sK[swz(t, ch)]);
+    b |= !isfinite(x);
     const uint32_t k = fkey(x);
     kmin = min(kmin, k);
     kmax = max(kmax, k);
   }
+  if (hf) {
+    sRed[ch] = kmin;
+    sRed[128 + ch] = kmax;
+    sRed[256 + ch] = b;
+  }
+  __syncthreads();
+  if (!hf) {
+    kmin = min(kmin, sRed[ch]);
+    kmax = max(kmax, sRed[128 + ch]);
+    b = b || sRed[256 + ch];
+  }
   lo = unkey(kmin);
   hi = unkey(kmax);
+  bad = b;
 }
 
-// Codes of one Key channel into the staging bytes cK[tok][ch].
-__device__ __forceinline__ void stage_channel(const uint16_t* sK, int d, const Params& p,
-                                              int bits, uint8_t* cK) {
-  const int top = (1 << bits) - 1;
-  for (int t = 0; t < kKG; ++t) cK[t * kD + d] = static_cast<uint8_t>(code_of(bf2f(sK[t * kD + d]), p, top));
+// Value groups: thread (token t = tid / 2, h = tid & 1) takes two of the
+// token's four 32-channel groups (h = 0: 0, 1; h = 1: 3, 2 -- the order keeps
+// a quarter warp's 16-byte reads on distinct banks).  Writes the steps and
+// origins to the record and the parameters to vq[t * 4 + j].
+template <int VB>
+__device__ __forceinline__ unsigned value_groups(const QuantArgs& a, const uint16_t* sV,
+                                                 GroupQ* vq, uint8_t* rec) {
+  constexpr int top = (1 << VB) - 1;
+  const int t = threadIdx.x >> 1, h = threadIdx.x & 1;
+  float* vscale = reinterpret_cast<float*>(rec + a.lay.v_scale);
+  uint16_t* vmin = reinterpret_cast<uint16_t*>(rec + a.lay.v_min);
+  const uint4* row = reinterpret_cast<const uint4*>(sV + t * kD);
+  unsigned flags = 0;
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    const int j = h ? 3 - jj : jj;
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 w = row[(4 * j + k) ^ (t & 7)];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x = __uint_as_float(e & 1 ? (ws[e >> 1] & 0xffff0000u) : (ws[e >> 1] << 16));
+        bad |= !isfinite(x);
+        const uint32_t key = fkey(x);
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
+      }
+    }
+    const Params p = group_params(unkey(kmin), unkey(kmax), top, bad);
+    vq[t * kVGroups + j] = make_q(p);
+    vscale[t * kVGroups + j] = p.step;
+    vmin[t * kVGroups + j] = f2bf_bits(p.m);
+    flags |= p.flags;
+  }
+  return flags;
 }
 
-// Pack staged key (cK) or value (cV) codes into the fragment-order words of
-// a record section (see frag_layout.h); all threads of the block take part.
+// Codes of a staged tile packed straight into the fragment-order words of
+// a record section (frag_layout.h): each thread builds whole words.
+// Keys: parameters per channel (kq[ch]); values: per token and 32-channel
+// group (vq[tok * 4 + ch / 32]).
 template <int BITS, bool KEY>
-__device__ __forceinline__ void pack_words(const uint8_t* codes, uint32_t* dst) {
+__device__ __forceinline__ void pack_codes(const uint16_t* tile, const GroupQ* gq,
+                                           uint32_t* dst) {
   constexpr int per = 32 / BITS;
   constexpr int words = kKG * kD * BITS / 32;
+  constexpr int top = (1 << BITS) - 1;
   for (int w = threadIdx.x; w < words; w += blockDim.x) {
     uint32_t acc = 0;
 #pragma unroll
@@ -125,41 +202,11 @@ __device__ __forceinline__ void pack_words(const uint8_t* codes, uint32_t* dst) 
       int tok, ch;
       if (KEY) key_word_code(w, s2, BITS, tok, ch);
       else value_word_code(w, s2, BITS, tok, ch);
-      acc |= static_cast<uint32_t>(codes[tok * kD + ch]) << (BITS * s2);
+      const GroupQ g = KEY ? gq[ch] : gq[tok * kVGroups + (ch >> 5)];
+      acc |= code_fast(bf2f(tile[swz(tok, ch)]), g, top) << (BITS * s2);
     }
     dst[w] = acc;
   }
-}
-
-// Value groups: one warp per (token, 32-channel group); lane = channel.
-template <int VB>
-__device__ __forceinline__ unsigned value_groups(const QuantArgs& a,
-                                                 const uint16_t* sV, uint8_t* cV,
-                                                 uint8_t* rec, int warp0,
-                                                 int nwarps) {
-  constexpr int top = (1 << VB) - 1;
-  const int lane = threadIdx.x & 31;
-  const int warp = (threadIdx.x >> 5) - warp0;
-  float* vscale = reinterpret_cast<float*>(rec + a.lay.v_scale);
-  uint16_t* vmin = reinterpret_cast<uint16_t*>(rec + a.lay.v_min);
-  unsigned flags = 0;
-  for (int task = warp; task < kKG * kVGroups; task += nwarps) {
-    const int t = task / kVGroups;
-    const int j = task % kVGroups;
-    const float x = bf2f(sV[t * kD + j * kVG + lane]);
-    const bool bad = __any_sync(kFull, !isfinite(x));
-    const uint32_t k = fkey(x);
-    const float lo = unkey(__reduce_min_sync(kFull, k));
-    const float hi = unkey(__reduce_max_sync(kFull, k));
-    const Params p = group_params(lo, hi, top, bad);
-    cV[t * kD + j * kVG + lane] = static_cast<uint8_t>(code_of(x, p, top));
-    if (lane == 0) {
-      vscale[t * kVGroups + j] = p.step;
-      vmin[t * kVGroups + j] = f2bf_bits(p.m);
-    }
-    flags |= p.flags;
-  }
-  return flags;
 }
 
 template <int KB, int VB>
@@ -167,33 +214,30 @@ __global__ void __launch_bounds__(256) quantize_uniform_kernel(QuantArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem);
   uint16_t* sV = sK + kKG * kD;
-  uint8_t* cK = reinterpret_cast<uint8_t*>(sV + kKG * kD);
-  uint8_t* cV = cK + kKG * kD;
+  __shared__ GroupQ kq[kD];
+  __shared__ GroupQ vq[kKG * kVGroups];
+  __shared__ uint32_t sRed[3 * kD];
   load_tiles(a, sK, sV);
   __syncthreads();
 
   const int u = blockIdx.y;
   uint8_t* rec = a.records + (static_cast<long long>(u) * a.max_groups +
                               a.first_group + blockIdx.x) * a.rec_bytes;
-  unsigned flags = 0;
+  unsigned flags = value_groups<VB>(a, sV, vq, rec);
+  float lo, hi;
+  bool bad;
+  key_ranges(sK, sRed, lo, hi, bad);
   if (threadIdx.x < kD) {
-    // warps 0-3: one Key channel per thread
     const int d = threadIdx.x;
-    float lo, hi;
-    bool bad;
-    channel_range(sK, d, lo, hi, bad);
     const Params p = group_params(lo, hi, (1 << KB) - 1, bad);
-    stage_channel(sK, d, p, KB, cK);
+    kq[d] = make_q(p);
     reinterpret_cast<float*>(rec + a.lay.k_scale)[d] = p.step;
     reinterpret_cast<uint16_t*>(rec + a.lay.k_min)[d] = f2bf_bits(p.m);
-    flags = p.flags;
-  } else {
-    // warps 4-7: the Value groups
-    flags = value_groups<VB>(a, sV, cV, rec, 4, 4);
+    flags |= p.flags;
   }
   __syncthreads();
-  pack_words<KB, true>(cK, reinterpret_cast<uint32_t*>(rec + a.lay.k_codes));
-  pack_words<VB, false>(cV, reinterpret_cast<uint32_t*>(rec + a.lay.v_codes));
+  pack_codes<KB, true>(sK, kq, reinterpret_cast<uint32_t*>(rec + a.lay.k_codes));
+  pack_codes<VB, false>(sV, vq, reinterpret_cast<uint32_t*>(rec + a.lay.v_codes));
   if (flags) atomicOr(a.status, flags);
 }
 
@@ -211,10 +255,11 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
   const int kvs = 32 * L.kw2;   // staged virtual channels per token
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem);
   uint16_t* sV = sK + kKG * kD;
-  uint8_t* cV = reinterpret_cast<uint8_t*>(sV + kKG * kD);
-  uint8_t* cKv = cV + kKG * kD;
+  uint8_t* cKv = reinterpret_cast<uint8_t*>(sV + kKG * kD);
   __shared__ uint32_t sKey[kD];
   __shared__ uint8_t sTier[kD];
+  __shared__ GroupQ vq[kKG * kVGroups];
+  __shared__ uint32_t sRed[3 * kD];
   load_tiles(a, sK, sV);
   // zero the padding virtual channels
   const int pad = kvs - L.nv;
@@ -225,12 +270,12 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
   const int u = blockIdx.y;
   uint8_t* rec = a.records + (static_cast<long long>(u) * a.max_groups +
                               a.first_group + blockIdx.x) * a.rec_bytes;
-  unsigned flags = 0;
+  unsigned flags = value_groups<VB>(a, sV, vq, rec);
+  float lo, hi;
+  bool bad;
+  key_ranges(sK, sRed, lo, hi, bad);
   if (threadIdx.x < kD) {
     const int d = threadIdx.x;
-    float lo, hi;
-    bool bad;
-    channel_range(sK, d, lo, hi, bad);
     float S = 0.0f;
     if (!bad) S = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
     const float I = a.importance[static_cast<long long>(u) * kD + d];
@@ -259,28 +304,27 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
     rec[L.perm + slot] = static_cast<uint8_t>(d);
     if (tier == KVQ_TIER_BF16) {
       uint16_t* raw = reinterpret_cast<uint16_t*>(rec + L.raw) + slot * kKG;
-      for (int t = 0; t < kKG; ++t) raw[(((t >> 3) ^ (slot & 7)) << 3) | (t & 7)] = sK[t * kD + d];
+      for (int t = 0; t < kKG; ++t) raw[(((t >> 3) ^ (slot & 7)) << 3) | (t & 7)] = sK[swz(t, d)];
     } else {
       const int bits = tier == KVQ_TIER_UINT4 ? 4 : 2;
       const int top = (1 << bits) - 1;
       const Params p = group_params(lo, hi, top, bad);
+      const GroupQ gq = make_q(p);
       flags |= p.flags;
       const int j = slot - L.nb;   // index among the quantized channels
       reinterpret_cast<float*>(rec + L.s4)[j] = p.step;
       reinterpret_cast<uint16_t*>(rec + L.m4)[j] = f2bf_bits(p.m);
       if (bits == 4) {
         for (int t = 0; t < kKG; ++t) {
-          const uint32_t c = code_of(bf2f(sK[t * kD + d]), p, top);
+          const uint32_t c = code_fast(bf2f(sK[swz(t, d)]), gq, top);
           cKv[t * kvs + j] = static_cast<uint8_t>(c & 3u);
           cKv[t * kvs + L.n4 + j] = static_cast<uint8_t>(c >> 2);
         }
       } else {
         for (int t = 0; t < kKG; ++t)
-          cKv[t * kvs + L.n4 + j] = static_cast<uint8_t>(code_of(bf2f(sK[t * kD + d]), p, top));
+          cKv[t * kvs + L.n4 + j] = static_cast<uint8_t>(code_fast(bf2f(sK[swz(t, d)]), gq, top));
       }
     }
-  } else {
-    flags = value_groups<VB>(a, sV, cV, rec, 4, 4);
   }
   __syncthreads();
   {
@@ -297,7 +341,7 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
       dst[w] = acc;
     }
   }
-  pack_words<VB, false>(cV, reinterpret_cast<uint32_t*>(rec + a.lay.v_codes));
+  pack_codes<VB, false>(sV, vq, reinterpret_cast<uint32_t*>(rec + a.lay.v_codes));
   if (flags) atomicOr(a.status, flags);
 }
 
@@ -423,7 +467,7 @@ cudaError_t gather(const kvq_cache* c, int off, int bytes, void* dst,
   return cudaGetLastError();
 }
 
-constexpr int kQuantSmem = 2 * kKG * kD * 2 + 2 * kKG * kD;  // bf16 tiles + staged codes, 96 KB
+constexpr int kQuantSmem = 2 * kKG * kD * 2;  // the two bf16 tiles, 64 KB
 
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
@@ -465,7 +509,7 @@ cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
     KERNEL<<<grid, 256, SMEM, s>>>(a);                       \
   } while (0)
   if (c->cfg.k_mode == KVQ_K_MIXED) {
-    const int smem = 2 * kKG * kD * 2 + kKG * kD + kKG * 32 * c->lay.kw2;
+    const int smem = 2 * kKG * kD * 2 + kKG * 32 * c->lay.kw2;
     if (vb == 2) KVQ_LAUNCH(quantize_mixed_kernel<2>, smem);
     else KVQ_LAUNCH(quantize_mixed_kernel<4>, smem);
   } else if (kb == 2 && vb == 2) {
