@@ -29,9 +29,6 @@ __device__ __forceinline__ uint32_t fkey(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-__device__ __forceinline__ float unkey(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
 
 struct Params {
   float m;
@@ -73,85 +70,110 @@ __device__ __forceinline__ int swz(int t, int ch) {
   return t * kD + ((((ch >> 3) ^ (t & 7)) << 3) | (ch & 7));
 }
 
-// Stage one 128-token tile of K and V in shared memory (cp.async, 16 bytes).
-__device__ __forceinline__ void load_tiles(const QuantArgs& a, uint16_t* sK, uint16_t* sV) {
+// Stage one 128-token bf16 tile (K or V) in shared memory (cp.async, 16 bytes).
+__device__ __forceinline__ void load_tile(const QuantArgs& a, const kvq_bf16* src, uint16_t* sT) {
   const long long off = static_cast<long long>(blockIdx.y) * a.src.unit_stride +
                         static_cast<long long>(blockIdx.x) * a.src.group_stride;
-  const uint8_t* gk = reinterpret_cast<const uint8_t*>(a.src.k + off);
-  const uint8_t* gv = reinterpret_cast<const uint8_t*>(a.src.v + off);
-  const uint32_t dk = static_cast<uint32_t>(__cvta_generic_to_shared(sK));
-  const uint32_t dv = static_cast<uint32_t>(__cvta_generic_to_shared(sV));
+  const uint8_t* gs = reinterpret_cast<const uint8_t*>(src + off);
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(sT));
   for (int i = threadIdx.x; i < kKG * kD * 2 / 16; i += blockDim.x) {
     const int t = i >> 4, pc = i & 15;
     const uint32_t o = static_cast<uint32_t>((t * 16 + (pc ^ (t & 7))) * 16);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dk + o), "l"(gk + 16 * i));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dv + o), "l"(gv + 16 * i));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d + o), "l"(gs + 16 * i));
   }
   asm volatile("cp.async.commit_group;\n" ::);
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
 }
 
-// Per-group quantizer parameters kept for the code pass: origin m, step,
-// and rcp = RN(1 / step) (0 for a constant group).
+// Per-group quantizer parameters kept for the code pass: origin m and
+// rcp = RN(1 / step) (0 for a constant group), plus the step itself for the
+// exact fallback.
 struct GroupQ {
-  float m, step, rcp;
+  float m, rcp;
 };
 
 __device__ __forceinline__ GroupQ make_q(const Params& p) {
-  return {p.m, p.step, p.step > 0.0f ? __frcp_rn(p.step) : 0.0f};
+  return {p.m, p.step > 0.0f ? __frcp_rn(p.step) : 0.0f};
 }
 
-// c = clip(RNE(fl32(fl32(x - m) / step)), 0, top), bit-identical to the IEEE
-// quotient.  q' = RN(d * RN(1/step)) is within 2^-22 q of RN(d / step); the
-// code can differ only if a half-integer lies that close to q', and then
-// (or for a non-finite q') the exact quotient is taken.
-__device__ __forceinline__ uint32_t code_fast(float x, const GroupQ& g, int top) {
-  if (g.step == 0.0f) return 0u;
+// c = clip(RNE(fl32(fl32(x - m) / step)), 0, top), fast form.  With
+// q' = RN(d * RN(1/step)), |q' - RN(d / step)| <= 2^-22 q <= 2^-18 (q <= 15
+// plus a rounding, as x <= the group max), so the two round to the same
+// integer unless q' lies within 2^-17 of a half-integer; such codes (and
+// non-finite q') set `exact` and the caller recomputes with the IEEE
+// quotient (code_exact).  Rounding: adding 1.5 * 2^23 rounds q in [0, 2^22)
+// to the nearest integer, ties to even, into the low mantissa bits; no
+// clamp is needed since 0 <= q < top + 1/2.
+constexpr float kTieMargin = 0.4999923706054688f;   // 0.5 - 2^-17
+__device__ __forceinline__ uint32_t code_fast(float x, GroupQ g, float& rmax) {
+  constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
   const float d = __fsub_rn(x, g.m);
-  float q = __fmul_rn(d, g.rcp);
-  const float n = rintf(q);
-  if (!(fabsf(fabsf(q - n) - 0.5f) > q * 4.76837158203125e-7f)) q = __fdiv_rn(d, g.step);
+  const float q = __fmul_rn(d, g.rcp);
+  const float tq = __fadd_rn(q, kMagic);
+  const float n = __fsub_rn(tq, kMagic);
+  // NaN (a non-finite group) must reach the exact path: fmaxf would drop it
+  const float r = fabsf(__fsub_rn(q, n));
+  rmax = r == r ? fmaxf(rmax, r) : 1.0f;
+  return __float_as_uint(tq) & 0xFFu;
+}
+__device__ __forceinline__ uint32_t code_exact(float x, float m, float step, int top) {
+  if (step == 0.0f) return 0u;
+  const float q = __fdiv_rn(__fsub_rn(x, m), step);
   return static_cast<uint32_t>(fminf(fmaxf(rintf(q), 0.0f), static_cast<float>(top)));
 }
 
-// Key channel ranges: two threads per channel over 64 tokens each, merged
-// through shared memory.  Returns (for threads 0..127, channel = thread) the
-// range and finiteness of the channel over the tile.
+// Two bf16 values in a 32-bit word -> two 16-bit order keys (key order =
+// value order, -0.0 below +0.0, NaN beyond the infinities).
+__device__ __forceinline__ uint32_t key2(uint32_t x) {
+  return x ^ (((x >> 15) & 0x00010001u) * 0x7FFFu) ^ 0x80008000u;
+}
+__device__ __forceinline__ float unkey16(uint32_t k) {
+  const uint32_t u = (k & 0x8000u) ? (k ^ 0x8000u) : (~k & 0xFFFFu);
+  return __uint_as_float(u << 16);
+}
+// a 16-bit key range holds a non-finite value iff an extreme is beyond +-inf
+__device__ __forceinline__ bool bad_range(uint32_t kmin, uint32_t kmax) {
+  return kmax >= 0xFF80u || kmin <= 0x007Fu;
+}
+
+// Key channel ranges: thread (pair p = tid & 63 of channels 2p, 2p+1,
+// quarter tid >> 6 of 32 tokens), packed keys, merged through shared memory.
+// Threads 0..127 return the range of channel tid.
 __device__ __forceinline__ void key_ranges(const uint16_t* sK, uint32_t* sRed, float& lo,
                                            float& hi, bool& bad) {
-  const int ch = threadIdx.x & 127, hf = threadIdx.x >> 7;
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-  bool b = false;
-  for (int t = 64 * hf; t < 64 * hf + 64; ++t) {
-    const float x = bf2f(sK[swz(t, ch)]);
-    b |= !isfinite(x);
-    const uint32_t k = fkey(x);
-    kmin = min(kmin, k);
-    kmax = max(kmax, k);
+  const int p = threadIdx.x & 63, qq = threadIdx.x >> 6;
+  const uint32_t* t32 = reinterpret_cast<const uint32_t*>(sK);
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll 8
+  for (int t = 32 * qq; t < 32 * qq + 32; ++t) {
+    const uint32_t k = key2(t32[t * 64 + ((((p >> 2) ^ (t & 7)) << 2) | (p & 3))]);
+    kmin = __vminu2(kmin, k);
+    kmax = __vmaxu2(kmax, k);
   }
-  if (hf) {
-    sRed[ch] = kmin;
-    sRed[128 + ch] = kmax;
-    sRed[256 + ch] = b;
-  }
+  sRed[qq * 64 + p] = kmin;
+  sRed[256 + qq * 64 + p] = kmax;
   __syncthreads();
-  if (!hf) {
-    kmin = min(kmin, sRed[ch]);
-    kmax = max(kmax, sRed[128 + ch]);
-    b = b || sRed[256 + ch];
+  if (threadIdx.x < kD) {
+    const int c = threadIdx.x, pp = c >> 1, sh = 16 * (c & 1);
+    uint32_t mn = 0xFFFFu, mx = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      mn = min(mn, (sRed[i * 64 + pp] >> sh) & 0xFFFFu);
+      mx = max(mx, (sRed[256 + i * 64 + pp] >> sh) & 0xFFFFu);
+    }
+    lo = unkey16(mn);
+    hi = unkey16(mx);
+    bad = bad_range(mn, mx);
   }
-  lo = unkey(kmin);
-  hi = unkey(kmax);
-  bad = b;
 }
 
 // Value groups: thread (token t = tid / 2, h = tid & 1) takes two of the
 // token's four 32-channel groups (h = 0: 0, 1; h = 1: 3, 2 -- the order keeps
 // a quarter warp's 16-byte reads on distinct banks).  Writes the steps and
-// origins to the record and the parameters to vq[t * 4 + j].
+// origins to the record and the parameters to vq / vstep [t * 4 + j].
 template <int VB>
 __device__ __forceinline__ unsigned value_groups(const QuantArgs& a, const uint16_t* sV,
-                                                 GroupQ* vq, uint8_t* rec) {
+                                                 GroupQ* vq, float* vstep, uint8_t* rec) {
   constexpr int top = (1 << VB) - 1;
   const int t = threadIdx.x >> 1, h = threadIdx.x & 1;
   float* vscale = reinterpret_cast<float*>(rec + a.lay.v_scale);
@@ -161,23 +183,22 @@ __device__ __forceinline__ unsigned value_groups(const QuantArgs& a, const uint1
 #pragma unroll
   for (int jj = 0; jj < 2; ++jj) {
     const int j = h ? 3 - jj : jj;
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
-    bool bad = false;
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint4 w = row[(4 * j + k) ^ (t & 7)];
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float x = __uint_as_float(e & 1 ? (ws[e >> 1] & 0xffff0000u) : (ws[e >> 1] << 16));
-        bad |= !isfinite(x);
-        const uint32_t key = fkey(x);
-        kmin = min(kmin, key);
-        kmax = max(kmax, key);
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t kk = key2(ws[e]);
+        kmin = __vminu2(kmin, kk);
+        kmax = __vmaxu2(kmax, kk);
       }
     }
-    const Params p = group_params(unkey(kmin), unkey(kmax), top, bad);
+    const uint32_t mn = min(kmin & 0xFFFFu, kmin >> 16), mx = max(kmax & 0xFFFFu, kmax >> 16);
+    const Params p = group_params(unkey16(mn), unkey16(mx), top, bad_range(mn, mx));
     vq[t * kVGroups + j] = make_q(p);
+    vstep[t * kVGroups + j] = p.step;
     vscale[t * kVGroups + j] = p.step;
     vmin[t * kVGroups + j] = f2bf_bits(p.m);
     flags |= p.flags;
@@ -185,59 +206,223 @@ __device__ __forceinline__ unsigned value_groups(const QuantArgs& a, const uint1
   return flags;
 }
 
-// Codes of a staged tile packed straight into the fragment-order words of
-// a record section (frag_layout.h): each thread builds whole words.
-// Keys: parameters per channel (kq[ch]); values: per token and 32-channel
-// group (vq[tok * 4 + ch / 32]).
-template <int BITS, bool KEY>
-__device__ __forceinline__ void pack_codes(const uint16_t* tile, const GroupQ* gq,
-                                           uint32_t* dst) {
-  constexpr int per = 32 / BITS;
-  constexpr int words = kKG * kD * BITS / 32;
-  constexpr int top = (1 << BITS) - 1;
-  for (int w = threadIdx.x; w < words; w += blockDim.x) {
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Rare exact recomputation of one key word (kept out of line so the fast
+// loop stays small in the instruction cache).
+template <int KB>
+__device__ __noinline__ uint32_t key_word_exact(const uint32_t* t32, const GroupQ* kq,
+                                                const float* kstep, int mt, int ks0, int g,
+                                                int t) {
+  constexpr int top = (1 << KB) - 1;
+  constexpr int KSW = KB == 2 ? 2 : 1;
+  uint32_t acc = 0;
+  for (int kl = 0; kl < KSW; ++kl)
+    for (int r = 0; r < 4; ++r) {
+      const int tok = 16 * mt + g + 8 * (r & 1);
+      const int ch0 = 16 * (ks0 + kl) + 2 * t + 8 * (r >> 1);
+      const uint32_t xw = t32[tok * 64 + ((((ch0 >> 3) ^ (tok & 7)) << 2) | ((ch0 & 7) >> 1))];
+      for (int hh = 0; hh < 2; ++hh) {
+        const float x = hh ? __uint_as_float(xw & 0xFFFF0000u) : __uint_as_float(xw << 16);
+        const int ch = ch0 + hh;
+        const int pos = KB == 2 ? 2 * pair_2bit(kl, r) + 16 * hh : 4 * nibble_4bit(r) + 16 * hh;
+        acc |= code_exact(x, kq[ch].m, kstep[ch], top) << pos;
+      }
+    }
+  return acc;
+}
+
+// Rare exact recomputation of one value word.
+template <int VB>
+__device__ __noinline__ uint32_t value_word_exact(const uint16_t* sV, const GroupQ* vq,
+                                                  const float* vstep, int mc, int kt0, int g,
+                                                  int t) {
+  constexpr int top = (1 << VB) - 1;
+  constexpr int KSW = VB == 2 ? 2 : 1;
+  const int j = mc >> 1;
+  uint32_t acc = 0;
+  for (int kl = 0; kl < KSW; ++kl)
+    for (int r = 0; r < 4; ++r)
+      for (int hh = 0; hh < 2; ++hh) {
+        const int ch = 16 * mc + g + 8 * (r & 1);
+        const int tok = 16 * (kt0 + kl) + 2 * t + 8 * (r >> 1) + hh;
+        const int pos = VB == 2 ? 2 * pair_2bit(kl, r) + 16 * hh : 4 * nibble_4bit(r) + 16 * hh;
+        acc |= code_exact(bf2f(sV[swz(tok, ch)]), vq[tok * kVGroups + j].m,
+                          vstep[tok * kVGroups + j], top) << pos;
+      }
+  return acc;
+}
+
+// Key codes straight into fragment-order words (frag_layout.h).  A word of
+// (tile mt, k-step pair or k-step, lane g,t) holds tokens g, g+8 of the tile
+// and channels 2t, 2t+1, 2t+8, 2t+9 of its k-step(s); each register's pair of
+// adjacent channels is one 32-bit read of the staged tile.  A thread's words
+// share their lane and k-steps (only the tile differs), so the channel
+// parameters and the swizzled column offsets are set up once.
+template <int KB>
+__device__ __forceinline__ void pack_key_words(const uint16_t* sK, const GroupQ* kq,
+                                               const float* kstep, uint32_t* dst) {
+  constexpr int KSW = KB == 2 ? 2 : 1;   // k-steps per word
+  constexpr int NWT = KB == 2 ? 4 : 8;   // words per thread (256 threads)
+  const uint32_t* t32 = reinterpret_cast<const uint32_t*>(sK);
+  const int tid = threadIdx.x;
+  int lane, ks0, mt0, mstep;
+  if (KB == 2) {   // word (mt*4 + ks/2)*32 + lane = tid + 256 k
+    lane = tid & 31;
+    ks0 = 2 * ((tid >> 5) & 3);
+    mt0 = tid >> 7;
+    mstep = 2;
+  } else {         // word ((mt*4 + ks/2)*32 + lane)*2 + ks%2 = tid + 256 k
+    lane = (tid >> 1) & 31;
+    ks0 = 2 * ((tid >> 6) & 3) + (tid & 1);
+    mt0 = 0;
+    mstep = 1;
+  }
+  const int g = lane >> 2, t = lane & 3;
+  GroupQ gq[KSW][4];
+  int col[KSW][2];   // 32-bit column offset of channels 2t (+8) in rows with t & 7 = g
+#pragma unroll
+  for (int kl = 0; kl < KSW; ++kl) {
+#pragma unroll
+    for (int r2 = 0; r2 < 4; ++r2)   // channels 2t, 2t+1, 2t+8, 2t+9
+      gq[kl][r2] = kq[16 * (ks0 + kl) + 2 * t + (r2 & 1) + 8 * (r2 >> 1)];
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      const int ch = 16 * (ks0 + kl) + 2 * t + 8 * hb;
+      col[kl][hb] = (((ch >> 3) ^ g) << 2) | ((ch & 7) >> 1);
+    }
+  }
+#pragma unroll 1
+  for (int k = 0; k < NWT; ++k) {
+    const int mt = mt0 + mstep * k;
+    const uint32_t* row0 = t32 + (16 * mt + g) * 64;   // token g of the tile (row + 8: token g+8)
+    float rmax = 0.0f;
     uint32_t acc = 0;
 #pragma unroll
-    for (int s2 = 0; s2 < per; ++s2) {
-      int tok, ch;
-      if (KEY) key_word_code(w, s2, BITS, tok, ch);
-      else value_word_code(w, s2, BITS, tok, ch);
-      const GroupQ g = KEY ? gq[ch] : gq[tok * kVGroups + (ch >> 5)];
-      acc |= code_fast(bf2f(tile[swz(tok, ch)]), g, top) << (BITS * s2);
-    }
-    dst[w] = acc;
+    for (int kl = 0; kl < KSW; ++kl)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t xw = row0[8 * 64 * (r & 1) + col[kl][r >> 1]];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const float x = hh ? bf_hi(xw) : bf_lo(xw);
+          const int pos = KB == 2 ? 2 * pair_2bit(kl, r) + 16 * hh : 4 * nibble_4bit(r) + 16 * hh;
+          acc |= code_fast(x, gq[kl][2 * (r >> 1) + hh], rmax) << pos;
+        }
+      }
+    if (!(rmax < kTieMargin)) acc = key_word_exact<KB>(t32, kq, kstep, mt, ks0, g, t);   // rare
+    dst[tid + 256 * k] = acc;
   }
 }
 
+// Value codes straight into fragment-order words: thread (channel tile mc,
+// lane g,t) builds the words of all the group's token k-steps (2-bit: 4
+// words, k-step pairs; 4-bit: 8) and stores them as 16-byte vectors.  A word
+// holds channels g, g+8 of the tile and tokens 2t, 2t+1, 2t+8, 2t+9 of its
+// k-step(s); parameters per (token, 32-channel group).
+template <int VB>
+__device__ __forceinline__ void pack_value_words(const uint16_t* sV, const GroupQ* vq,
+                                                 const float* vstep, uint32_t* dst) {
+  constexpr int KSW = VB == 2 ? 2 : 1;
+  constexpr int NW = VB == 2 ? 4 : 8;   // words per (mc, lane)
+  const int mc = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3, j = mc >> 1;
+  uint32_t* out4 = dst + (mc * (NW / 4)) * 128 + lane * 4;   // word (mc, lane, wi)
+#pragma unroll 1
+  for (int wi = 0; wi < NW; ++wi) {
+    float rmax = 0.0f;
+    uint32_t acc = 0;
+    float xs[KSW][4][2];
+#pragma unroll
+    for (int kl = 0; kl < KSW; ++kl)
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int kt = KSW * wi + kl;
+          const int ch = 16 * mc + g + 8 * (r & 1);
+          const int tok = 16 * kt + 2 * t + 8 * (r >> 1) + hh;
+          xs[kl][r][hh] = bf2f(sV[swz(tok, ch)]);
+        }
+#pragma unroll
+    for (int kl = 0; kl < KSW; ++kl)
+#pragma unroll
+      for (int r2 = 0; r2 < 4; ++r2) {   // tokens 2t, 2t+1, 2t+8, 2t+9
+        const int tok = 16 * (KSW * wi + kl) + 2 * t + (r2 & 1) + 8 * (r2 >> 1);
+        const GroupQ gq = vq[tok * kVGroups + j];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {   // the two registers holding this token
+          const int r = 2 * (r2 >> 1) + rr, hh = r2 & 1;
+          const int pos = VB == 2 ? 2 * pair_2bit(kl, r) + 16 * hh : 4 * nibble_4bit(r) + 16 * hh;
+          acc |= code_fast(xs[kl][r][hh], gq, rmax) << pos;
+        }
+      }
+    if (!(rmax < kTieMargin)) acc = value_word_exact<VB>(sV, vq, vstep, mc, KSW * wi, g, t);   // rare
+    // word index of (mc, lane, wi): 2-bit (mc*32 + lane)*4 + wi; 4-bit
+    // ((mc*2 + wi/4)*32 + lane)*4 + wi%4
+    out4[(wi >> 2) * 128 + (wi & 3)] = acc;
+  }
+}
+
+__device__ __forceinline__ uint8_t* group_record(const QuantArgs& a) {
+  return a.records + (static_cast<long long>(blockIdx.y) * a.max_groups + a.first_group +
+                      blockIdx.x) * a.rec_bytes;
+}
+
+// Dynamic shared memory of a quantize block: the staged tile (32 KB), then
+// the parameter area (kParamBytes): values use vq [512] and vstep [512];
+// keys use kq [128], kstep [128], a 2 KB reduction buffer and (mixed keys)
+// the rank keys and tiers; mixed key blocks add their virtual codes after.
+constexpr int kTileBytes = kKG * kD * 2;
+constexpr int kParamBytes = kKG * kVGroups * (8 + 4);   // 6 KB, the larger of the two uses
+
+// Value half of a group (block z = 1 of every quantize launch).
+template <int VB>
+__device__ __forceinline__ void value_part(const QuantArgs& a, uint8_t* smem) {
+  uint16_t* sV = reinterpret_cast<uint16_t*>(smem);
+  GroupQ* vq = reinterpret_cast<GroupQ*>(smem + kTileBytes);
+  float* vstep = reinterpret_cast<float*>(smem + kTileBytes + kKG * kVGroups * 8);
+  load_tile(a, a.src.v, sV);
+  __syncthreads();
+  uint8_t* rec = group_record(a);
+  const unsigned flags = value_groups<VB>(a, sV, vq, vstep, rec);
+  __syncthreads();
+  pack_value_words<VB>(sV, vq, vstep, reinterpret_cast<uint32_t*>(rec + a.lay.v_codes));
+  if (flags) atomicOr(a.status, flags);
+}
+
+// Uniform keys and values of one 128-token group: block (group, unit, z),
+// z = 0 the keys, z = 1 the values, each from its own 32 KB staged tile.
 template <int KB, int VB>
 __global__ void __launch_bounds__(256) quantize_uniform_kernel(QuantArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* sK = reinterpret_cast<uint16_t*>(smem);
-  uint16_t* sV = sK + kKG * kD;
-  __shared__ GroupQ kq[kD];
-  __shared__ GroupQ vq[kKG * kVGroups];
-  __shared__ uint32_t sRed[3 * kD];
-  load_tiles(a, sK, sV);
+  if (blockIdx.z) {
+    value_part<VB>(a, smem);
+    return;
+  }
+  uint16_t* sT = reinterpret_cast<uint16_t*>(smem);
+  GroupQ* kq = reinterpret_cast<GroupQ*>(smem + kTileBytes);
+  float* kstep = reinterpret_cast<float*>(smem + kTileBytes + kD * 8);
+  uint32_t* sRed = reinterpret_cast<uint32_t*>(smem + kTileBytes + kD * 12);
+  load_tile(a, a.src.k, sT);
   __syncthreads();
-
-  const int u = blockIdx.y;
-  uint8_t* rec = a.records + (static_cast<long long>(u) * a.max_groups +
-                              a.first_group + blockIdx.x) * a.rec_bytes;
-  unsigned flags = value_groups<VB>(a, sV, vq, rec);
+  uint8_t* rec = group_record(a);
+  unsigned flags = 0;
   float lo, hi;
   bool bad;
-  key_ranges(sK, sRed, lo, hi, bad);
+  key_ranges(sT, sRed, lo, hi, bad);
   if (threadIdx.x < kD) {
     const int d = threadIdx.x;
     const Params p = group_params(lo, hi, (1 << KB) - 1, bad);
     kq[d] = make_q(p);
+    kstep[d] = p.step;
     reinterpret_cast<float*>(rec + a.lay.k_scale)[d] = p.step;
     reinterpret_cast<uint16_t*>(rec + a.lay.k_min)[d] = f2bf_bits(p.m);
-    flags |= p.flags;
+    flags = p.flags;
   }
   __syncthreads();
-  pack_codes<KB, true>(sK, kq, reinterpret_cast<uint32_t*>(rec + a.lay.k_codes));
-  pack_codes<VB, false>(sV, vq, reinterpret_cast<uint32_t*>(rec + a.lay.v_codes));
+  pack_key_words<KB>(sT, kq, kstep, reinterpret_cast<uint32_t*>(rec + a.lay.k_codes));
   if (flags) atomicOr(a.status, flags);
 }
 
@@ -253,14 +438,16 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const RecLayout& L = a.lay;
   const int kvs = 32 * L.kw2;   // staged virtual channels per token
+  if (blockIdx.z) {
+    value_part<VB>(a, smem);
+    return;
+  }
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem);
-  uint16_t* sV = sK + kKG * kD;
-  uint8_t* cKv = reinterpret_cast<uint8_t*>(sV + kKG * kD);
-  __shared__ uint32_t sKey[kD];
-  __shared__ uint8_t sTier[kD];
-  __shared__ GroupQ vq[kKG * kVGroups];
-  __shared__ uint32_t sRed[3 * kD];
-  load_tiles(a, sK, sV);
+  uint32_t* sRed = reinterpret_cast<uint32_t*>(smem + kTileBytes);             // 2 KB
+  uint32_t* sKey = reinterpret_cast<uint32_t*>(smem + kTileBytes + 2048);     // 512 B
+  uint8_t* sTier = smem + kTileBytes + 2048 + 512;                            // 128 B
+  uint8_t* cKv = smem + kTileBytes + kParamBytes;
+  load_tile(a, a.src.k, sK);
   // zero the padding virtual channels
   const int pad = kvs - L.nv;
   for (int i = threadIdx.x; i < kKG * pad; i += blockDim.x)
@@ -268,9 +455,8 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
   __syncthreads();
 
   const int u = blockIdx.y;
-  uint8_t* rec = a.records + (static_cast<long long>(u) * a.max_groups +
-                              a.first_group + blockIdx.x) * a.rec_bytes;
-  unsigned flags = value_groups<VB>(a, sV, vq, rec);
+  uint8_t* rec = group_record(a);
+  unsigned flags = 0;
   float lo, hi;
   bool bad;
   key_ranges(sK, sRed, lo, hi, bad);
@@ -309,20 +495,19 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
       const int bits = tier == KVQ_TIER_UINT4 ? 4 : 2;
       const int top = (1 << bits) - 1;
       const Params p = group_params(lo, hi, top, bad);
-      const GroupQ gq = make_q(p);
       flags |= p.flags;
       const int j = slot - L.nb;   // index among the quantized channels
       reinterpret_cast<float*>(rec + L.s4)[j] = p.step;
       reinterpret_cast<uint16_t*>(rec + L.m4)[j] = f2bf_bits(p.m);
       if (bits == 4) {
         for (int t = 0; t < kKG; ++t) {
-          const uint32_t c = code_fast(bf2f(sK[swz(t, d)]), gq, top);
+          const uint32_t c = code_exact(bf2f(sK[swz(t, d)]), p.m, p.step, top);
           cKv[t * kvs + j] = static_cast<uint8_t>(c & 3u);
           cKv[t * kvs + L.n4 + j] = static_cast<uint8_t>(c >> 2);
         }
       } else {
         for (int t = 0; t < kKG; ++t)
-          cKv[t * kvs + L.n4 + j] = static_cast<uint8_t>(code_fast(bf2f(sK[swz(t, d)]), gq, top));
+          cKv[t * kvs + L.n4 + j] = static_cast<uint8_t>(code_exact(bf2f(sK[swz(t, d)]), p.m, p.step, top));
       }
     }
   }
@@ -341,7 +526,6 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
       dst[w] = acc;
     }
   }
-  pack_codes<VB, false>(sV, vq, reinterpret_cast<uint32_t*>(rec + a.lay.v_codes));
   if (flags) atomicOr(a.status, flags);
 }
 
@@ -467,7 +651,7 @@ cudaError_t gather(const kvq_cache* c, int off, int bytes, void* dst,
   return cudaGetLastError();
 }
 
-constexpr int kQuantSmem = 2 * kKG * kD * 2;  // the two bf16 tiles, 64 KB
+constexpr int kQuantSmem = kTileBytes + kParamBytes;  // 38 KB
 
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
@@ -499,7 +683,7 @@ cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
   a.lay = c->lay;
   a.importance = importance;
   a.status = c->status;
-  const dim3 grid(n_groups, c->cfg.batch * c->cfg.kv_heads);
+  const dim3 grid(n_groups, c->cfg.batch * c->cfg.kv_heads, 2);   // z: keys, values
   const int kb = c->cfg.k_bits, vb = c->cfg.v_bits;
   cudaError_t e = cudaSuccess;
 #define KVQ_LAUNCH(KERNEL, SMEM)                             \
@@ -509,7 +693,7 @@ cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
     KERNEL<<<grid, 256, SMEM, s>>>(a);                       \
   } while (0)
   if (c->cfg.k_mode == KVQ_K_MIXED) {
-    const int smem = 2 * kKG * kD * 2 + kKG * 32 * c->lay.kw2;
+    const int smem = kTileBytes + kParamBytes + kKG * 32 * c->lay.kw2;   // + virtual codes
     if (vb == 2) KVQ_LAUNCH(quantize_mixed_kernel<2>, smem);
     else KVQ_LAUNCH(quantize_mixed_kernel<4>, smem);
   } else if (kb == 2 && vb == 2) {
