@@ -215,26 +215,32 @@ int kvq_decode_attention(const kvq_cache* c, const kvq_bf16* q, int Hq, float* o
   return cuda_status(launch_decode_mma(c, q, Hq, out, static_cast<float*>(ws), plan, s));
 }
 
+static int current_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return sms;
+}
+
 size_t kvq_decode_bf16_workspace_bytes(int B, int Hkv, int T, int Hq) {
   if (B < 1 || Hkv < 1 || T < 1 || !valid_rep(Hq, Hkv)) return 0;
-  return decode_ws_bytes(static_cast<long long>(B) * Hq, kMaxSplits);
+  const int sms = current_sms();
+  return sms ? bf16_ws_bytes(sms, B, Hkv, Hq, T) : 0;
 }
 
 int kvq_decode_bf16(const kvq_bf16* k, const kvq_bf16* v, int B, int Hkv, int T,
                     const kvq_bf16* q, int Hq, float* out, void* ws, size_t ws_bytes,
                     cudaStream_t s) {
   if (!k || !v || !q || !out || B < 1 || Hkv < 1 || T < 1) return KVQ_ERR_ARG;
-  if (!aligned16(k) || !aligned16(v)) return KVQ_ERR_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(q)) return KVQ_ERR_ARG;
   if (!valid_rep(Hq, Hkv)) return KVQ_ERR_SHAPE;
-  if (!ws || ws_bytes < kvq_decode_bf16_workspace_bytes(B, Hkv, T, Hq) || !aligned16(ws))
+  const int sms = current_sms();
+  if (!sms) return KVQ_ERR_CUDA;
+  if (!ws || ws_bytes < bf16_ws_bytes(sms, B, Hkv, Hq, T) || !aligned16(ws))
     return KVQ_ERR_WORKSPACE;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return KVQ_ERR_CUDA;
-  const int n_split = choose_splits(sms, B * Hkv, (T + kKG - 1) / kKG);
-  return cuda_status(launch_decode_bf16(k, v, B, Hkv, T, q, Hq, out,
-                                        static_cast<float*>(ws), n_split, sms, s));
+  return cuda_status(launch_decode_bf16(k, v, B, Hkv, T, q, Hq, out, static_cast<float*>(ws),
+                                        ws_bytes, sms, s));
 }
 
 int kvq_channel_saliency(const kvq_bf16* q_win, int Hq, int Lq, const kvq_bf16* k_grp,

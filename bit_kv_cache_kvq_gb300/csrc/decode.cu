@@ -1,319 +1,280 @@
-// Unquantized bf16 comparator: split-K ("flash-decoding") decode attention
-// over plain bf16 K, V on CUDA cores, plus its combine kernel.
+// Unquantized comparator: decode attention over plain bf16 K, V (the 16-bit
+// baseline the pages measure against: MixKVQ "BF16" rows, PN-Mix FP16).
 //
-// Math ("KIVI: KV cache axes" §1 and §6; MixKVQ Algorithm 1): for query
-// head h of KV head kvh, s_t = q·k^_t / sqrt(D) over the dequantized
-// history and the residual tokens, p = softmax over all of them together,
-// o = sum_t p_t v^_t.  Scores are kept in log2 units (q pre-scaled by
-// log2(e)/sqrt(D)) so p = exp2(s - max).
+// Same math as the quantized path (KIVI: KV cache axes §1, §6): s = q·k /
+// sqrt(D) in log2 units, one softmax over all tokens, o = sum p v, split-K
+// with an exact log-sum-exp combine.  Tensor cores do both contractions of
+// every 16-token chunk: scores from bf16 MMAs of the exact keys and query
+// (exact products, fp32 sums), P·V from the values transposed by ldmatrix
+// and p split into bf16 high and low parts (16 bits), each chunk summed in a
+// fresh accumulator and folded into the running output in fp32.
 //
-// Work split: grid (n_split, B*Hkv).  A CTA streams a contiguous range of
-// 128-token blocks of one (b, kv head) for all n_rep query heads that share
-// it (GQA: each byte is read once).  Inside the CTA, teams of TL lanes each
-// own whole blocks and keep their own online-softmax state; teams merge
-// once at the end.  A second kernel merges the splits with the exact
-// log-sum-exp rule (KIVI §6: blockwise softmax is allowed when the blocks
-// share one global normalization).
+// Work split ("stream-K"): the (unit, chunk) items, units = (b, kv head),
+// are cut into equal contiguous slices, one per warp of a persistent grid
+// (12 warps per SM); each warp streams its chunks through two 8 KB slots
+// (K and V of one chunk) of its own shared memory with 16-byte cp.async,
+// the next chunk loading while the current one computes, and writes one
+// partial per unit it touches.  combine_parts_kernel merges them.
 #include <cuda_runtime.h>
 
-#include <cfloat>
-
 #include "kvq_internal.h"
+#include "mma_util.h"
 
 namespace kvq {
 namespace {
 
-__device__ __forceinline__ float bf2f(uint16_t b) {
-  return __uint_as_float(static_cast<uint32_t>(b) << 16);
-}
+constexpr int kChunk = 16;                       // tokens per item
+constexpr int kChunkBytes = kChunk * kD * 2;     // 4 KB of K (or V)
+constexpr int kSlotBytes = 2 * kChunkBytes;      // K then V
+constexpr int kWarps = 12;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ void bf2x8(const uint4& w, float* f) {
-  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(v[i] << 16);
-    f[2 * i + 1] = __uint_as_float(v[i] & 0xffff0000u);
-  }
-}
-
-// Reductions over one team of TL lanes.  Teams of a warp run different
-// numbers of groups (and only one team takes the residual), so every
-// shuffle names the calling team's lanes only.
-template <int TL>
-__device__ __forceinline__ unsigned team_mask_of() {
-  return (TL == 32 ? 0xffffffffu : ((1u << TL) - 1u)) << ((threadIdx.x & 31) / TL * TL);
-}
-template <int TL>
-__device__ __forceinline__ float team_sum(float x) {
-  const unsigned m = team_mask_of<TL>();
-#pragma unroll
-  for (int o = TL / 2; o > 0; o >>= 1) x += __shfl_xor_sync(m, x, o);
-  return x;
-}
-template <int TL>
-__device__ __forceinline__ float team_max(float x) {
-  const unsigned m = team_mask_of<TL>();
-#pragma unroll
-  for (int o = TL / 2; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(m, x, o));
-  return x;
-}
-
-// Fields the partial writer needs.
-struct DecodeArgs {
-  int Hkv, Hq;
-  int n_split;
-  float* ws;              // o [rows][n_split][D], then (m, l) [rows][n_split][2]
-};
-
-template <int NREP>
-struct TeamShape {
-  static constexpr int TL = NREP <= 4 ? 8 : 16;  // lanes per team
-  static constexpr int CPT = 128 / TL;           // tokens (QK) / channels (PV) per lane
-  static constexpr int TEAMS = 128 / TL;         // teams per 128-thread CTA
-};
-
-// Online-softmax state of one lane: its running max (team-uniform), its
-// share of the normalizer, and the output accumulators of its CPT channels.
-template <int NREP, int CPT>
-struct SoftState {
-  float m[NREP];
-  float l[NREP];
-  float o[CPT][NREP];
-  __device__ void init() {
-#pragma unroll
-    for (int h = 0; h < NREP; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.0f;
-#pragma unroll
-      for (int i = 0; i < CPT; ++i) o[i][h] = 0.0f;
-    }
-  }
-  // Fold a block of scores s[CPT][NREP] (masked entries -inf) into the
-  // state and write exp2(s - m_new) to p_out[h][lane*CPT + i].
-  template <int TL>
-  __device__ void absorb(float (&s)[CPT][NREP], float* p_out, int li) {
-#pragma unroll
-    for (int h = 0; h < NREP; ++h) {
-      float bm = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < CPT; ++i) bm = fmaxf(bm, s[i][h]);
-      bm = team_max<TL>(bm);
-      const float m_new = fmaxf(m[h], bm);
-      const float alpha = (m[h] == -INFINITY) ? 0.0f : exp2f(m[h] - m_new);
-      l[h] *= alpha;
-#pragma unroll
-      for (int i = 0; i < CPT; ++i) o[i][h] *= alpha;
-      m[h] = m_new;
-#pragma unroll
-      for (int i = 0; i < CPT; ++i) {
-        const float p = (s[i][h] == -INFINITY) ? 0.0f : exp2f(s[i][h] - m_new);
-        l[h] += p;
-        p_out[h * 128 + li * CPT + i] = p;
-      }
-    }
-  }
-};
-
-// Merge the teams of a CTA and write its partial (o, m, l) per query head.
-template <int NREP, int TL, int CPT, int TEAMS, typename State>
-__device__ void write_partial(const DecodeArgs& a, State& st, float* s_o,
-                              float* s_ml, int team, int li, int b, int kvh,
-                              int split) {
-  __syncthreads();  // all teams done with their probability buffers
-#pragma unroll
-  for (int h = 0; h < NREP; ++h) {
-    const float l = team_sum<TL>(st.l[h]);
-#pragma unroll
-    for (int i = 0; i < CPT; ++i) s_o[(team * NREP + h) * 128 + li * CPT + i] = st.o[i][h];
-    if (li == 0) {
-      s_ml[(team * NREP + h) * 2 + 0] = st.m[h];
-      s_ml[(team * NREP + h) * 2 + 1] = l;
-    }
-  }
-  __syncthreads();
-  const int ch = threadIdx.x;  // 128 threads = 128 channels
-  const long long rows = static_cast<long long>(gridDim.y / a.Hkv) * a.Hq;
-  float* ws_o = a.ws;
-  float* ws_ml = a.ws + rows * a.n_split * kD;
-#pragma unroll
-  for (int h = 0; h < NREP; ++h) {
-    float M = -INFINITY;
-    for (int t = 0; t < TEAMS; ++t) M = fmaxf(M, s_ml[(t * NREP + h) * 2]);
-    float o = 0.0f, l = 0.0f;
-    if (M != -INFINITY) {
-      for (int t = 0; t < TEAMS; ++t) {
-        const float mt = s_ml[(t * NREP + h) * 2];
-        const float w = (mt == -INFINITY) ? 0.0f : exp2f(mt - M);
-        o += w * s_o[(t * NREP + h) * 128 + ch];
-        l += w * s_ml[(t * NREP + h) * 2 + 1];
-      }
-    }
-    const long long row = static_cast<long long>(b) * a.Hq + kvh * NREP + h;
-    ws_o[(row * a.n_split + split) * kD + ch] = o;
-    if (ch == 0) {
-      ws_ml[(row * a.n_split + split) * 2 + 0] = M;
-      ws_ml[(row * a.n_split + split) * 2 + 1] = l;
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Unquantized comparator: identical split-K skeleton over bf16 K, V
-// [units][T][D].  A "group" is 128 consecutive tokens; the last is ragged.
 struct Bf16Args {
-  const uint16_t* k;
-  const uint16_t* v;
-  const uint16_t* q;
-  int T, Hkv, Hq;
-  int n_groups, n_split, gps;
-  float* ws;
-  float qscale;
-  // fields read by write_partial
+  const uint8_t* k;   // [units][T][D] bf16
+  const uint8_t* v;
+  const uint16_t* q;  // [B][Hq][D]
+  int Hkv, Hq, T, n_chunks;
+  long long total;    // units * n_chunks
+  int n_slots, max_parts;
+  float* ws;          // [units][max_parts][n_rep][D + 2]
 };
 
-template <int NREP>
-__global__ void __launch_bounds__(128) decode_bf16_kernel(Bf16Args a, DecodeArgs shape) {
-  using Shape = TeamShape<NREP>;
-  constexpr int TL = Shape::TL, CPT = Shape::CPT, TEAMS = Shape::TEAMS;
-  __shared__ float s_q[NREP * kD];
-  __shared__ float s_p[TEAMS * NREP * 128];
-  __shared__ float s_ml[TEAMS * NREP * 2];
-  const int split = blockIdx.x;
-  const int u = blockIdx.y;
-  const int b = u / a.Hkv, kvh = u % a.Hkv;
-  const int team = threadIdx.x / TL, li = threadIdx.x % TL;
-  const unsigned team_mask = team_mask_of<TL>();
-  for (int i = threadIdx.x; i < NREP * kD; i += blockDim.x) {
-    const int h = i / kD, d = i % kD;
-    s_q[i] = bf2f(a.q[(static_cast<long long>(b) * a.Hq + kvh * NREP + h) * kD + d]) * a.qscale;
+__device__ __forceinline__ long long slice_start(const Bf16Args& a, int w) {
+  return (static_cast<long long>(w) * a.total) / a.n_slots;
+}
+__device__ __forceinline__ int slice_of(const Bf16Args& a, long long p) {
+  return static_cast<int>(((p + 1) * a.n_slots - 1) / a.total);
+}
+
+// Chunk c of unit u (K and V, 16 rows of 256 B) into slot `slot`: 16-byte
+// piece p of row t at piece p ^ (t & 7), so ldmatrix row reads are free of
+// bank conflicts.  Rows past T repeat row T - 1 (never read past the
+// tensor); their scores are masked.
+__device__ __forceinline__ void stage(const Bf16Args& a, int u, int c, uint32_t slot_addr,
+                                      int lane) {
+  const long long ubase = static_cast<long long>(u) * a.T;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i, row = e >> 4, pc = e & 15;
+    const int tok = min(c * kChunk + row, a.T - 1);
+    const long long off = ((ubase + tok) * kD) * 2 + pc * 16;
+    const uint32_t d = slot_addr + row * 256 + ((pc ^ (row & 7)) << 4);
+    cp_async16(d, a.k + off);
+    cp_async16(d + kChunkBytes, a.v + off);
   }
-  __syncthreads();
-  SoftState<NREP, CPT> st;
-  st.init();
-  float* p_buf = s_p + team * NREP * 128;
-  const uint16_t* kbase = a.k + static_cast<long long>(u) * a.T * kD;
-  const uint16_t* vbase = a.v + static_cast<long long>(u) * a.T * kD;
-  const int g_begin = split * a.gps;
-  const int g_end = min(g_begin + a.gps, a.n_groups);
-  for (int g = g_begin + team; g < g_end; g += TEAMS) {
-    const int t0 = g * 128;
-    const int nt = min(128, a.T - t0);
-    float s[CPT][NREP];
+}
+
+template <int NREP>
+__global__ void __launch_bounds__(kWarps * 32, 1) decode_bf16_kernel(Bf16Args a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  // the combine kernel may be scheduled now; it waits for this grid's results
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  const int slot = blockIdx.x * kWarps + warp;
+  if (slot >= a.n_slots) return;   // warp-uniform
+  const uint32_t buf = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) +
+                       warp * 2 * kSlotBytes;
+  const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
+  const long long p0 = slice_start(a, slot), p1 = slice_start(a, slot + 1);
+  for (int u = static_cast<int>(p0 / a.n_chunks); u <= static_cast<int>((p1 - 1) / a.n_chunks);
+       ++u) {
+    const long long ub = static_cast<long long>(u) * a.n_chunks;
+    const int c_lo = static_cast<int>(max(p0, ub) - ub);
+    const int c_hi = static_cast<int>(min(p1, ub + a.n_chunks) - ub);
+    // query B fragments: column g = head g (zero for g >= NREP), exact bf16
+    uint32_t bq[8][2];
+    {
+      const int b = u / a.Hkv, kvh = u % a.Hkv;
+      const uint32_t* qg = reinterpret_cast<const uint32_t*>(
+          a.q + (static_cast<long long>(b) * a.Hq + kvh * NREP + min(g, NREP - 1)) * kD);
 #pragma unroll
-    for (int i = 0; i < CPT; ++i) {
-      const int t = li * CPT + i;
-      float acc[NREP];
+      for (int ks = 0; ks < 8; ++ks) {
+        bq[ks][0] = g < NREP ? __ldg(qg + 8 * ks + t) : 0u;
+        bq[ks][1] = g < NREP ? __ldg(qg + 8 * ks + t + 4) : 0u;
+      }
+    }
+    float O[8][4];
 #pragma unroll
-      for (int h = 0; h < NREP; ++h) acc[h] = 0.0f;
-      if (t < nt) {
-        const uint4* row = reinterpret_cast<const uint4*>(kbase + static_cast<long long>(t0 + t) * kD);
-#pragma unroll 4
-        for (int dc = 0; dc < kD / 8; ++dc) {
-          float f[8];
-          bf2x8(__ldg(row + dc), f);
+    for (int mc = 0; mc < 8; ++mc)
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
+      for (int i = 0; i < 4; ++i) O[mc][i] = 0.0f;
+    float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.0f, 0.0f};
+
+    __syncwarp();
+    stage(a, u, c_lo, buf, lane);
+    cp_async_commit();
+    for (int c = c_lo; c < c_hi; ++c) {
+      const uint32_t cur = buf + ((c - c_lo) & 1) * kSlotBytes;
+      if (c + 1 < c_hi) stage(a, u, c + 1, buf + ((c + 1 - c_lo) & 1) * kSlotBytes, lane);
+      cp_async_commit();
+      cp_async_wait<1>();
+      __syncwarp();
+      // ---- scores of the chunk's 16 tokens
+      float S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      {
+        const int row = (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
-            for (int h = 0; h < NREP; ++h) acc[h] = fmaf(s_q[h * kD + dc * 8 + e], f[e], acc[h]);
+        for (int ks = 0; ks < 8; ++ks) {
+          const int pc = 2 * ks + (lane >> 4);
+          uint32_t A[4];
+          ldsm_x4(A, cur + row * 256 + ((pc ^ (row & 7)) << 4));
+          mma_bf16(S, A, bq[ks][0], bq[ks][1]);
         }
       }
 #pragma unroll
-      for (int h = 0; h < NREP; ++h) s[i][h] = (t < nt) ? acc[h] : -INFINITY;
+      for (int i = 0; i < 4; ++i)
+        if (c * kChunk + g + 8 * (i >> 1) >= a.T) S[i] = -INFINITY;
+      // ---- online softmax (log2 units), per head column 2t + h
+      float alpha[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float m = fmaxf(S[h], S[h + 2]);
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 16));
+        const float m_new = fmaxf(mrun[h], m * c0);
+        alpha[h] = ex2(mrun[h] - m_new);
+        mrun[h] = m_new;
+        S[h] = ex2(fmaf(S[h], c0, -m_new));
+        S[h + 2] = ex2(fmaf(S[h + 2], c0, -m_new));
+        lrun[h] = fmaf(lrun[h], alpha[h], S[h] + S[h + 2]);
+      }
+      if (__any_sync(kFull, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+#pragma unroll
+        for (int mc = 0; mc < 8; ++mc) {
+          O[mc][0] *= alpha[0]; O[mc][2] *= alpha[0];
+          O[mc][1] *= alpha[1]; O[mc][3] *= alpha[1];
+        }
+      }
+      // ---- P·V: p as bf16 high + low B fragments, values transposed
+      uint32_t ph[2], pl[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float x0 = S[2 * i], x1 = S[2 * i + 1];
+        const uint32_t hi = pack_bf2(x0, x1);
+        const float l0 = x0 - __uint_as_float(hi << 16);
+        const float l1 = x1 - __uint_as_float(hi & 0xffff0000u);
+        ph[i] = movmatrix_t(hi);
+        pl[i] = movmatrix_t(pack_bf2(l0, l1));
+      }
+      {
+        const uint32_t vb = cur + kChunkBytes;
+        const int row = (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+        for (int mc = 0; mc < 8; ++mc) {
+          const int pc = 2 * mc + ((lane >> 3) & 1);
+          uint32_t A[4];
+          ldsm_x4_t(A, vb + row * 256 + ((pc ^ (row & 7)) << 4));
+          float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          mma_bf16(acc, A, ph[0], ph[1]);
+          mma_bf16(acc, A, pl[0], pl[1]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) O[mc][i] += acc[i];
+        }
+      }
+      __syncwarp();   // slot read before it is staged again
     }
-    st.template absorb<TL>(s, p_buf, li);
-    __syncwarp(team_mask);
-    const uint16_t* vrow0 = vbase + static_cast<long long>(t0) * kD + li * CPT;
-#pragma unroll 2
-    for (int t = 0; t < nt; ++t) {
-      float vf[CPT];
+    cp_async_wait<0>();
+    __syncwarp();
+    // ---- partial (o, m, l) of this unit's slice
+    float l[2];
 #pragma unroll
-      for (int c8 = 0; c8 < CPT / 8; ++c8)
-        bf2x8(__ldg(reinterpret_cast<const uint4*>(vrow0 + static_cast<long long>(t) * kD) + c8), vf + 8 * c8);
+    for (int h = 0; h < 2; ++h) {
+      float x = lrun[h];
+      x += __shfl_xor_sync(kFull, x, 4);
+      x += __shfl_xor_sync(kFull, x, 8);
+      x += __shfl_xor_sync(kFull, x, 16);
+      l[h] = x;
+    }
+    const int part = slot - slice_of(a, ub);
+    float* base = a.ws + (static_cast<long long>(u) * a.max_parts + part) * NREP * (kD + 2);
 #pragma unroll
-      for (int h = 0; h < NREP; ++h) {
-        const float p = p_buf[h * 128 + t];
+    for (int mc = 0; mc < 8; ++mc)
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) st.o[i][h] = fmaf(p, vf[i], st.o[i][h]);
+      for (int i = 0; i < 4; ++i) {
+        const int h = 2 * t + (i & 1);
+        if (h < NREP) base[h * (kD + 2) + 16 * mc + g + 8 * (i >> 1)] = O[mc][i];
+      }
+    if (g == 0) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int hh = 2 * t + h;
+        if (hh < NREP) {
+          base[hh * (kD + 2) + kD] = mrun[h];
+          base[hh * (kD + 2) + kD + 1] = l[h];
+        }
       }
     }
-    __syncwarp(team_mask);
   }
-  write_partial<NREP, TL, CPT, TEAMS>(shape, st, s_p, s_ml, team, li, b, kvh, split);
 }
 
-// Exact merge of the split partials: M = max m_i, o = sum 2^(m_i-M) o_i /
-// sum 2^(m_i-M) l_i.
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ ws,
-                                                     int rows, int n_split,
-                                                     float* __restrict__ out) {
-  const long long row = blockIdx.x;
-  const int ch = threadIdx.x;
-  const float* ws_o = ws;
-  const float* ws_ml = ws + static_cast<long long>(rows) * n_split * kD;
-  float M = -INFINITY;
-  for (int i = 0; i < n_split; ++i) M = fmaxf(M, ws_ml[(row * n_split + i) * 2]);
-  float o = 0.0f, l = 0.0f;
-  for (int i = 0; i < n_split; ++i) {
-    const float mi = ws_ml[(row * n_split + i) * 2];
-    if (mi == -INFINITY) continue;
-    const float w = exp2f(mi - M);
-    o = fmaf(w, ws_o[(row * n_split + i) * kD + ch], o);
-    l = fmaf(w, ws_ml[(row * n_split + i) * 2 + 1], l);
-  }
-  out[row * kD + ch] = o / l;
+struct Bf16Plan {
+  int n_chunks;
+  long long total;
+  int n_slots, max_parts;
+};
+
+Bf16Plan plan_bf16(int num_sms, int units, int T) {
+  Bf16Plan p;
+  p.n_chunks = (T + kChunk - 1) / kChunk;
+  p.total = static_cast<long long>(units) * p.n_chunks;
+  const long long resident = static_cast<long long>(num_sms) * kWarps;
+  p.n_slots = static_cast<int>(p.total < resident ? p.total : resident);
+  // each unit's chunks meet at most ceil(slots / units) + 1 slots
+  p.max_parts = (p.n_slots + units - 1) / units + 1;
+  return p;
 }
 
-constexpr float kLog2e = 1.4426950408889634f;
-
-}  // namespace
-
-int choose_splits(int num_sms, int units, int n_chunks) {
-  const int target = 4 * num_sms;  // CTAs wanted in flight
-  int n = (target + units - 1) / units;
-  n = min(n, max(n_chunks, 1));
-  n = min(n, kMaxSplits);
-  return max(n, 1);
-}
-
-cudaError_t launch_combine(const float* ws, int rows, int n_split, float* out,
-                           cudaStream_t s) {
-  combine_kernel<<<rows, kD, 0, s>>>(ws, rows, n_split, out);
+template <int NREP>
+cudaError_t launch_nrep(const Bf16Args& a, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(kWarps) * 2 * kSlotBytes;
+  auto kern = decode_bf16_kernel<NREP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<(a.n_slots + kWarps - 1) / kWarps, kWarps * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_bf16(const kvq_bf16* k, const kvq_bf16* v, int B,
-                               int Hkv, int T, const kvq_bf16* q, int Hq,
-                               float* out, float* ws, int n_split, int num_sms,
-                               cudaStream_t s) {
-  (void)num_sms;
+}  // namespace
+
+size_t bf16_ws_bytes(int num_sms, int B, int Hkv, int Hq, int T) {
+  const int units = B * Hkv;
+  const Bf16Plan p = plan_bf16(num_sms, units, T);
+  return static_cast<size_t>(units) * p.max_parts * (Hq / Hkv) * (kD + 2) * sizeof(float);
+}
+
+cudaError_t launch_decode_bf16(const kvq_bf16* k, const kvq_bf16* v, int B, int Hkv, int T,
+                               const kvq_bf16* q, int Hq, float* out, float* ws,
+                               size_t ws_bytes, int num_sms, cudaStream_t s) {
+  const int units = B * Hkv, nrep = Hq / Hkv;
+  const Bf16Plan p = plan_bf16(num_sms, units, T);
+  if (ws_bytes < bf16_ws_bytes(num_sms, B, Hkv, Hq, T)) return cudaErrorInvalidValue;
   Bf16Args a;
-  a.k = k;
-  a.v = v;
+  a.k = reinterpret_cast<const uint8_t*>(k);
+  a.v = reinterpret_cast<const uint8_t*>(v);
   a.q = q;
-  a.T = T;
   a.Hkv = Hkv;
   a.Hq = Hq;
-  a.n_groups = (T + 127) / 128;
-  a.n_split = n_split;
-  a.gps = (a.n_groups + n_split - 1) / n_split;
+  a.T = T;
+  a.n_chunks = p.n_chunks;
+  a.total = p.total;
+  a.n_slots = p.n_slots;
+  a.max_parts = p.max_parts;
   a.ws = ws;
-  a.qscale = kLog2e / sqrtf(static_cast<float>(kD));
-  DecodeArgs shape{};
-  shape.Hkv = Hkv;
-  shape.Hq = Hq;
-  shape.n_split = n_split;
-  shape.ws = ws;
-  const dim3 grid(n_split, B * Hkv);
-  switch (Hq / Hkv) {
-    case 1: decode_bf16_kernel<1><<<grid, 128, 0, s>>>(a, shape); break;
-    case 2: decode_bf16_kernel<2><<<grid, 128, 0, s>>>(a, shape); break;
-    case 4: decode_bf16_kernel<4><<<grid, 128, 0, s>>>(a, shape); break;
-    case 8: decode_bf16_kernel<8><<<grid, 128, 0, s>>>(a, shape); break;
+  cudaError_t e;
+  switch (nrep) {
+    case 1: e = launch_nrep<1>(a, s); break;
+    case 2: e = launch_nrep<2>(a, s); break;
+    case 4: e = launch_nrep<4>(a, s); break;
+    case 8: e = launch_nrep<8>(a, s); break;
     default: return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_combine(ws, B * Hq, n_split, out, s);
+  return launch_combine_parts(ws, B, Hkv, Hq, p.max_parts, p.n_chunks, p.total, p.n_slots, out,
+                              s);
 }
 
 }  // namespace kvq

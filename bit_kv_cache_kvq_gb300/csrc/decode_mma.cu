@@ -38,6 +38,7 @@
 
 #include "frag_layout.h"
 #include "kvq_internal.h"
+#include "mma_util.h"
 
 namespace kvq {
 namespace {
@@ -66,83 +67,6 @@ constexpr int kQBytes = 8 * kQRow * 2;   // = 4 * kQRow * 4
 constexpr int kWarpExtra = kVsbBytes + kVmbBytes + kQBytes;
 static_assert(kWarpExtra % 128 == 0, "per-warp extra must keep 128-byte alignment");
 constexpr int kMaxWarps = 12;           // warps per block: up to 168 registers a thread
-
-__device__ __forceinline__ float bf2f(uint32_t b16) { return __uint_as_float(b16 << 16); }
-
-__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Four 8x8 b16 matrices from shared memory (row addresses from lanes 8i..8i+7
-// for matrix i), plain or transposed.
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
-
-// fp32 pair -> bf16x2 (low half = lo), round to nearest even
-__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
-  uint32_t d;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(d) : "f"(hi), "f"(lo));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-  uint32_t y;
-  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
-  return y;
-}
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
-  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
-                            *reinterpret_cast<const __half2*>(&b));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-// Power-of-two normalizer for a non-negative magnitude x: returns s with
-// x*s in [0.5, 1) for ordinary x (clamped at the extremes), and 1/s.
-__device__ __forceinline__ void pow2_norm(float x, float& s, float& inv) {
-  int e = (__float_as_uint(x) >> 23) & 0xff;
-  e = min(max(e, 1), 252);
-  s = __uint_as_float(static_cast<uint32_t>(253 - e) << 23);
-  inv = __uint_as_float(static_cast<uint32_t>(e + 1) << 23);
-}
-
-// 1/x for x an exact power of two in the normal range (exponent arithmetic).
-__device__ __forceinline__ float pow2_rcp(float x) {
-  return __uint_as_float((254u << 23) - __float_as_uint(x));
-}
 
 // Swizzled positions in the per-warp value tables (u32 index), chosen so
 // both the writers (lane = 4 tokens) and the readers (lane = fragment
@@ -1124,6 +1048,23 @@ size_t mma_ws_bytes(int num_sms, int B, int Hkv, int Hq, int max_groups, int rec
   return static_cast<size_t>(units) * parts * (Hq / Hkv) * (kD + 2) * sizeof(float);
 }
 
+cudaError_t launch_combine_parts(const float* ws, int B, int Hkv, int Hq, int max_parts,
+                                 long long unit_len, long long total, int n_slots, float* out,
+                                 cudaStream_t s) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(B * Hq);
+  lc.blockDim = dim3(kD);
+  lc.dynamicSmemBytes = static_cast<size_t>(max_parts) * sizeof(float);
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, combine_parts_kernel, ws, Hkv, Hq, max_parts, unit_len, total,
+                            n_slots, out);
+}
+
 cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, float* out,
                               float* ws, const MmaPlan& plan, cudaStream_t s) {
   MmaArgs a;
@@ -1161,18 +1102,8 @@ cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, flo
     e = launch_rep<4, 4, false>(a, nrep, warps, s);
   }
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(c->cfg.batch * Hq);
-  lc.blockDim = dim3(kD);
-  lc.dynamicSmemBytes = static_cast<size_t>(a.max_parts) * sizeof(float);
-  lc.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, combine_parts_kernel, static_cast<const float*>(ws), a.Hkv, Hq,
-                            a.max_parts, a.unit_len, a.total, a.n_slots, out);
+  return launch_combine_parts(ws, c->cfg.batch, a.Hkv, Hq, a.max_parts, a.unit_len, a.total,
+                              a.n_slots, out, s);
 }
 
 }  // namespace kvq

@@ -16,7 +16,6 @@ constexpr int kKG = KVQ_K_GROUP;   // tokens per key group
 constexpr int kVG = KVQ_V_GROUP;   // channels per value group
 constexpr int kR = KVQ_RESIDUAL;   // residual capacity
 constexpr int kVGroups = kD / kVG; // value groups per token (4)
-constexpr int kMaxSplits = 64;     // bf16 comparator: split-K partitions per (b, kv head)
 constexpr int kMaxRep = 8;         // query heads per KV head
 
 // ---------------------------------------------------------------------------
@@ -140,7 +139,6 @@ cudaError_t launch_residual_tail(const kvq_cache* c, const kvq_bf16* k,
                                  const kvq_bf16* v, int L, int first,
                                  int count, cudaStream_t s);
 
-int choose_splits(int num_sms, int units, int n_chunks);
 
 // Tensor-core decode (decode_mma.cu).  The plan cuts the weighted item
 // sequence (per unit: its groups, then its residual) into n_slots warp
@@ -157,12 +155,19 @@ bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int rec_by
 size_t mma_ws_bytes(int num_sms, int B, int Hkv, int Hq, int max_groups, int rec_bytes);
 cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, float* out,
                               float* ws, const MmaPlan& plan, cudaStream_t s);
-cudaError_t launch_decode_bf16(const kvq_bf16* k, const kvq_bf16* v, int B,
-                               int Hkv, int T, const kvq_bf16* q, int Hq,
-                               float* out, float* ws, int n_split, int num_sms,
-                               cudaStream_t s);
-cudaError_t launch_combine(const float* ws, int rows, int n_split, float* out,
-                           cudaStream_t s);
+// Merge split-K partials [units][max_parts][n_rep][D + 2] (o, m, l) of the
+// slots of a plan into out [B][Hq][D]; launched as a programmatic dependent
+// of the kernel that wrote them.
+cudaError_t launch_combine_parts(const float* ws, int B, int Hkv, int Hq, int max_parts,
+                                 long long unit_len, long long total, int n_slots, float* out,
+                                 cudaStream_t s);
+
+// bf16 comparator (decode.cu): stream-K over 16-token chunks of plain bf16
+// K, V; workspace as the quantized decode's.
+size_t bf16_ws_bytes(int num_sms, int B, int Hkv, int Hq, int T);
+cudaError_t launch_decode_bf16(const kvq_bf16* k, const kvq_bf16* v, int B, int Hkv, int T,
+                               const kvq_bf16* q, int Hq, float* out, float* ws,
+                               size_t ws_bytes, int num_sms, cudaStream_t s);
 
 cudaError_t launch_saliency(const kvq_bf16* q_win, int Hq, int Lq,
                             const kvq_bf16* k_grp, int B, int Hkv, int G,
@@ -180,10 +185,5 @@ cudaError_t launch_export_k_mixed(const kvq_cache* c, uint8_t* perm,
                                   float* s4, uint8_t* c2, kvq_bf16* m2,
                                   float* s2, cudaStream_t s);
 
-// Workspace layout of the split-K decode: o partials [rows][n_split][D]
-// followed by (m, l) pairs [rows][n_split][2], fp32.
-inline size_t decode_ws_bytes(long long rows, int n_split) {
-  return (size_t)rows * (size_t)n_split * (size_t)(kD + 2) * sizeof(float);
-}
 
 }  // namespace kvq

@@ -1,0 +1,104 @@
+// Inline PTX helpers shared by the decode kernels: warp-level tensor-core
+// MMAs with register operands, ldmatrix and movmatrix fragment moves, and
+// small float utilities.  Fragment convention (lane = 4g + t):
+//   A (16x16, row): a0 = A[g][2t,2t+1]  a1 = A[g+8][2t,2t+1]
+//                   a2 = A[g][2t+8,+9]  a3 = A[g+8][2t+8,+9]
+//   B (16x8, col):  b0 = B[2t,2t+1][g]  b1 = B[2t+8,2t+9][g]
+//   C (16x8):       c0 = C[g][2t] c1 = C[g][2t+1] c2 = C[g+8][2t] c3 = C[g+8][2t+1]
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cstdint>
+
+namespace kvq {
+namespace {
+
+__device__ __forceinline__ float bf2f(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 b16 matrices from shared memory (row addresses from lanes 8i..8i+7
+// for matrix i), plain or transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// fp32 pair -> bf16x2 (low half = lo), round to nearest even
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
+                            *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Power-of-two normalizer for a non-negative magnitude x: returns s with
+// x*s in [0.5, 1) for ordinary x (clamped at the extremes), and 1/s.
+__device__ __forceinline__ void pow2_norm(float x, float& s, float& inv) {
+  int e = (__float_as_uint(x) >> 23) & 0xff;
+  e = min(max(e, 1), 252);
+  s = __uint_as_float(static_cast<uint32_t>(253 - e) << 23);
+  inv = __uint_as_float(static_cast<uint32_t>(e + 1) << 23);
+}
+
+// 1/x for x an exact power of two in the normal range (exponent arithmetic).
+__device__ __forceinline__ float pow2_rcp(float x) {
+  return __uint_as_float((254u << 23) - __float_as_uint(x));
+}
+
+// 16-byte global -> shared copy (cp.async.cg: bypasses L1).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+}  // namespace
+}  // namespace kvq

@@ -218,8 +218,12 @@ int kvq_decode_attention_static(const kvq_cache* cache, const kvq_bf16* q,
                                 int Hq, float* out, cudaStream_t s);
 
 /*
- * Unquantized comparator: the same decode attention over plain bf16
- * k, v [B][Hkv][T][D] (T >= 1), same q/out/ws conventions.
+ * Unquantized comparator (the 16-bit baseline of MixKVQ's and PN-Mix's
+ * comparisons): the same decode attention over plain bf16 k, v
+ * [B][Hkv][T][D] (T >= 1; k, v, q 16-byte aligned), same q/out
+ * conventions.  ws: >= kvq_decode_bf16_workspace_bytes(B, Hkv, T, Hq) for
+ * the current device (the split depends on its SM count; 0 on bad
+ * arguments).  Errors: ARG, SHAPE, WORKSPACE, CUDA.
  */
 size_t kvq_decode_bf16_workspace_bytes(int B, int Hkv, int T, int Hq);
 int kvq_decode_bf16(const kvq_bf16* k, const kvq_bf16* v, int B, int Hkv,
