@@ -177,6 +177,26 @@ def flush_bytes(w):
     return w.B * w.Hkv * 128 * (512 + token_bytes(w))
 
 
+# ------------------------------------------------------------- multi-rank
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (the slowest rank's time); x itself
+    for one rank.  Ranks shard whole (batch row, KV head) units, so this
+    and a barrier are the only cross-rank traffic."""
+    if world == 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_workload(w, rank: int):
+    """Weak scaling: every rank decodes its own batch of the workload (its
+    own (batch row, KV head) units), drawn from seeds offset by the rank."""
+    from bit_kv_cache_kvq_gb300.workloads import scaled
+    return scaled(w, seed=w.seed + 100 * rank)
+
+
 # ---------------------------------------------------------------- arms
 def workload_from(args):
     from bit_kv_cache_kvq_gb300.workloads import WORKLOADS, scaled
@@ -289,7 +309,7 @@ def run_ours(args, rank, world):
     kvq.lib()
     dev = torch.device("cuda", torch.cuda.current_device())
     w0 = workload_from(args)
-    w = scaled(w0, seed=w0.seed + 100 * rank)     # weak scaling: each rank its own batch
+    w = rank_workload(w0, rank)                    # weak scaling: each rank its own batch
     K, W = args.steps, args.warmup
     n_flush = (w.r + K) // 128                     # flushes inside the timed steps
     T0 = max(0, w.T_q - 128 * (n_flush // 2))     # mean context over the timed steps ~ workload's
@@ -379,11 +399,8 @@ def run_ours(args, rank, world):
     t_end.record(stream)
     torch.cuda.synchronize()
     clk.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
         torch.distributed.barrier()
     attn_ms = [a.elapsed_time(b) for a, b in evs]
     attn_avg_ms = sum(attn_ms) / K
@@ -472,11 +489,7 @@ def run_ours(args, rank, world):
         for i in range(KE):
             e2e_bytes += e2e_step(W + i)
         t1 = time.perf_counter()
-        e2e_s = t1 - t0
-        if world > 1:
-            t = torch.tensor([e2e_s], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks(t1 - t0, world, dev)
         h2d = d_k.numel() * 2 + d_v.numel() * 2 + d_q.numel() * 2
         line["e2e"] = {"value": e2e_bytes * world / e2e_s / 1e9, "unit": "GB/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * 4,
