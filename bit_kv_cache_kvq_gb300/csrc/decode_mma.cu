@@ -152,10 +152,10 @@ struct Warp {
   float qmax;      // max |query| of the head row this lane builds B columns for
 
   // online-softmax state (heads 2t, 2t+1 of this lane)
-  float O[8][4];   // running O^T in units of sv[j] / 2^9 (channel tiles mc = 0..7)
+  float O[8][4];   // running O^T in units of sv / 2^9 (channel tiles mc = 0..7)
   float vm[2];     // origin term (lanes g < 4: channel group j = g)
   float mrun[2], lrun[2];
-  float sv[4], inv_sv[4];  // current units of O per j
+  float sv, inv_sv;  // current units of O
 
   __device__ __forceinline__ Warp(const MmaArgs& args, uint8_t* base)
       : a(args), lane(threadIdx.x & 31), g((threadIdx.x & 31) >> 2), t(threadIdx.x & 3) {
@@ -222,11 +222,8 @@ struct Warp {
     for (int m = 0; m < 8; ++m)
 #pragma unroll
       for (int c = 0; c < 4; ++c) O[m][c] = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      sv[j] = kSentinel;
-      inv_sv[j] = 1.0f / kSentinel;
-    }
+    sv = kSentinel;
+    inv_sv = 1.0f / kSentinel;
     vm[0] = vm[1] = 0.0f;
     mrun[0] = mrun[1] = -INFINITY;
     lrun[0] = lrun[1] = 0.0f;
@@ -567,11 +564,12 @@ struct Warp {
 
   // Value-side tables of one group (values in vbuf): lane l handles tokens
   // 4l..4l+3.  Returns this group's units per j and the origin scale.
-  __device__ __forceinline__ void value_tables(float (&svn)[4], float (&inv_svm)[4]) {
+  __device__ __forceinline__ void value_tables(float& svn, float& inv_svm) {
     const RecLayout& L = a.lay;
     const float* vscale = reinterpret_cast<const float*>(vbuf + (L.v_scale - L.kpart));
     const uint2* vmin2 = reinterpret_cast<const uint2*>(vbuf + (L.v_min - L.kpart));
     float vs[4][4], vmn[4][4];
+    float mx = 0.0f, mm = 0.0f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float4 f = reinterpret_cast<const float4*>(vscale)[4 * lane + i];
@@ -579,35 +577,34 @@ struct Warp {
       const uint2 m = vmin2[4 * lane + i];
       vmn[i][0] = bf2f(m.x & 0xffffu); vmn[i][1] = bf2f(m.x >> 16);
       vmn[i][2] = bf2f(m.y & 0xffffu); vmn[i][3] = bf2f(m.y >> 16);
-    }
-    float svm[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float mx = fmaxf(fmaxf(vs[0][j], vs[1][j]), fmaxf(vs[2][j], vs[3][j]));
-      float mm = fmaxf(fmaxf(fabsf(vmn[0][j]), fabsf(vmn[1][j])),
-                       fmaxf(fabsf(vmn[2][j]), fabsf(vmn[3][j])));
-      mx = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(mx)));
-      mm = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(mm)));
-      float s_new, inv_new;
-      pow2_norm(mx, s_new, inv_new);
-      (void)inv_new;
-      // the units of this group's P' never exceed the running ones
-      svn[j] = fminf(s_new, sv[j]);
-      pow2_norm(mm, svm[j], inv_svm[j]);
+      for (int j = 0; j < 4; ++j) {
+        mx = fmaxf(mx, vs[i][j]);
+        mm = fmaxf(mm, fabsf(vmn[i][j]));
+      }
     }
+    // one power-of-two unit for the group's steps and one for its origins
+    // (steps are >= 0, so their bit patterns order like their values)
+    mx = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(mx)));
+    mm = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(mm)));
+    float s_new, inv_new, svm;
+    pow2_norm(mx, s_new, inv_new);
+    (void)inv_new;
+    // the units of this group's P' never exceed the running ones
+    svn = fminf(s_new, sv);
+    pow2_norm(mm, svm, inv_svm);
     const int kt = lane >> 2, q4 = lane & 3;
     const int t0 = 2 * (q4 & 1), chi = q4 >> 1;
     // the row factor of the code position these tokens meet (frag_layout.h)
     const float rf = VB == 2 ? __uint_as_float((142u - 4u * (kt & 1) - 2u * chi) << 23)
                              : __uint_as_float((142u - 4u * chi) << 23);
+    const float sc = svn * rf;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float sc = svn[j] * rf;
       vsb[vsb_index(kt, t0, j, chi)] = pack_h2(vs[0][j] * sc, vs[1][j] * sc);
       vsb[vsb_index(kt, t0 + 1, j, chi)] = pack_h2(vs[2][j] * sc, vs[3][j] * sc);
-      const float sm = svm[j];
-      vmb[vmb_index(kt, j, t0, chi)] = pack_h2(vmn[0][j] * sm, vmn[1][j] * sm);
-      vmb[vmb_index(kt, j, t0 + 1, chi)] = pack_h2(vmn[2][j] * sm, vmn[3][j] * sm);
+      vmb[vmb_index(kt, j, t0, chi)] = pack_h2(vmn[0][j] * svm, vmn[1][j] * svm);
+      vmb[vmb_index(kt, j, t0 + 1, chi)] = pack_h2(vmn[2][j] * svm, vmn[3][j] * svm);
     }
   }
 
@@ -618,17 +615,16 @@ struct Warp {
   // accumulation, whose truncation would otherwise grow with the context.
   __device__ __forceinline__ void pv(float (&S)[8][4], const float (&alpha)[2]) {
     const RecLayout& L = a.lay;
-    float svn[4], inv_svm[4];
+    float svn, inv_svm;
     value_tables(svn, inv_svm);
-    // rescale of the running output to this group's units, per j and head
-    float f0[4], f1[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float ratio = svn[j] * inv_sv[j];
-      f0[j] = alpha[0] * ratio;
-      f1[j] = alpha[1] * ratio;
-      sv[j] = svn[j];
-      inv_sv[j] = pow2_rcp(svn[j]);
+    // rescale of the running output to this group's units, per head
+    float f0, f1;
+    {
+      const float ratio = svn * inv_sv;
+      f0 = alpha[0] * ratio;
+      f1 = alpha[1] * ratio;
+      sv = svn;
+      inv_sv = pow2_rcp(svn);
     }
     __syncwarp();   // value tables written by all lanes
 
@@ -683,16 +679,15 @@ struct Warp {
             }
           }
         }
-        O[mc][0] = fmaf(O[mc][0], f0[j], acc[0]);
-        O[mc][2] = fmaf(O[mc][2], f0[j], acc[2]);
-        O[mc][1] = fmaf(O[mc][1], f1[j], acc[1]);
-        O[mc][3] = fmaf(O[mc][3], f1[j], acc[3]);
+        O[mc][0] = fmaf(O[mc][0], f0, acc[0]);
+        O[mc][2] = fmaf(O[mc][2], f0, acc[2]);
+        O[mc][1] = fmaf(O[mc][1], f1, acc[1]);
+        O[mc][3] = fmaf(O[mc][3], f1, acc[3]);
       }
     }
     // origin term in true units (lanes g < 4 hold channel group j = g)
     {
-      const float im = g == 0 ? inv_svm[0] : g == 1 ? inv_svm[1] : g == 2 ? inv_svm[2]
-                       : g == 3 ? inv_svm[3] : 0.0f;
+      const float im = g < 4 ? inv_svm : 0.0f;
       vm[0] = fmaf(vm[0], alpha[0], Dvm[0] * im);
       vm[1] = fmaf(vm[1], alpha[1], Dvm[1] * im);
     }
@@ -774,12 +769,9 @@ struct Warp {
       const float hinv[2] = {c0, c0}, hoff[2] = {0.0f, 0.0f};
       float alpha[2];
       softmax_update(S, hinv, hoff, alpha);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (sv[j] == kSentinel) {   // no group in this segment: O is still zero
-          sv[j] = 1.0f;
-          inv_sv[j] = 1.0f;
-        }
+      if (sv == kSentinel) {   // no group in this segment: O is still zero
+        sv = 1.0f;
+        inv_sv = 1.0f;
       }
 #pragma unroll
       for (int mc = 0; mc < 8; ++mc) {
@@ -821,7 +813,7 @@ struct Warp {
           float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
           mma_bf16(acc, A, ph[0], ph[1]);
           mma_bf16(acc, A, pl[0], pl[1]);
-          const float sc = sv[mc >> 1] * kInvCodeUnit;
+          const float sc = sv * kInvCodeUnit;
 #pragma unroll
           for (int i = 0; i < 4; ++i) O[mc][i] = fmaf(acc[i], sc, O[mc][i]);
         }
@@ -855,7 +847,7 @@ struct Warp {
         for (int c = 0; c < 4; ++c) {
           const int h = 2 * t + (c & 1);
           const int ch = 16 * mc + g + 8 * (c >> 1);
-          const float val = O[mc][c] * (inv_sv[j] * kCodeUnit) + ((c & 1) ? vm1 : vm0);
+          const float val = O[mc][c] * (inv_sv * kCodeUnit) + ((c & 1) ? vm1 : vm0);
           if (h < NREP) base[h * (kD + 2) + ch] = val;
         }
       }
