@@ -444,7 +444,12 @@ struct Warp {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = 16 * k16 + 2 * t + (e & 1) + 8 * (e >> 1);
-          qb[e] = (i < nb && g < NREP) ? static_cast<uint32_t>(__ldg(qg_row + perm[i])) : 0u;
+          // exact bf16 query: the staged copy (8 heads) or global memory
+          // (with at most 4 heads the staged copy is pre-scaled fp32)
+          qb[e] = (i < nb && g < NREP)
+                      ? static_cast<uint32_t>(SPARE ? __ldg(qg_row + perm[i])
+                                                    : static_cast<const uint16_t*>(qs)[g * kQRow + perm[i]])
+                      : 0u;
         }
         const uint32_t b0 = qb[0] | (qb[1] << 16), b1 = qb[2] | (qb[3] << 16);
         const int i = 16 * k16 + (lane & 7) + 8 * (lane >> 4);
