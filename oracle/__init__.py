@@ -295,10 +295,16 @@ class OracleCache:
     mode "uniform": K k_bits per channel over Gk tokens; V v_bits per token
     over Gv channels.  mode "mixed": K tiers per flushed group from
     A = I * S (S at sal_bits) by rank (n_bf16, n_uint4), V as in uniform.
+
+    n_sink > 0: the first n_sink tokens of the sequence are attention sinks
+    kept in bf16 and never quantized (PN-Mix "sink 原精度保护", N_s = 32;
+    InnerQ's high-precision window for attention-sink tokens).  The
+    quantized groups and the residual start after them; while the sink is
+    not full, appended tokens go to it.
     """
 
     def __init__(self, B, Hkv, D, k_bits=2, v_bits=2, Gk=128, Gv=32, R=128,
-                 mode="uniform", n_bf16=0, n_uint4=0, sal_bits=2):
+                 mode="uniform", n_bf16=0, n_uint4=0, sal_bits=2, n_sink=0):
         if R % Gk:
             raise ValueError("R must be a multiple of the key group")
         self.B, self.Hkv, self.D = B, Hkv, D
@@ -309,13 +315,25 @@ class OracleCache:
         self.v_parts = [[] for _ in range(U)]    # (codes, vmin, vscale) per token block
         self.res_k = np.zeros((U, R, D), np.uint16)
         self.res_v = np.zeros((U, R, D), np.uint16)
+        self.n_sink = n_sink
+        self.sink_k = np.zeros((U, n_sink, D), np.uint16)
+        self.sink_v = np.zeros((U, n_sink, D), np.uint16)
+        self.s = 0
         self.T_q = 0
         self.r = 0
 
     # -- Algorithm 1, Prefill: r = l_prompt mod R (F read as 0)
     def prefill(self, K: np.ndarray, V: np.ndarray, importance: np.ndarray | None = None):
-        if self.T_q or self.r:
+        if self.T_q or self.r or self.s:
             raise ValueError("prefill into a non-empty cache")
+        s = min(K.shape[2], self.n_sink)
+        if s:   # the sink takes the first tokens; the rest follows Algorithm 1
+            for u in range(self.B * self.Hkv):
+                b, h = divmod(u, self.Hkv)
+                self.sink_k[u, :s] = K[b, h, :s]
+                self.sink_v[u, :s] = V[b, h, :s]
+            self.s = s
+            K, V = K[:, :, s:], V[:, :, s:]
         B, Hkv, L, D = K.shape
         r = L % self.R
         n_q = L - r
@@ -330,6 +348,11 @@ class OracleCache:
 
     # -- Algorithm 1, Decoding: append to the residual
     def append(self, k_new: np.ndarray, v_new: np.ndarray):
+        if self.s < self.n_sink:   # the sequence's first tokens fill the sink
+            self.sink_k[:, self.s] = k_new.reshape(-1, self.D)
+            self.sink_v[:, self.s] = v_new.reshape(-1, self.D)
+            self.s += 1
+            return
         if self.r == self.R:
             raise ValueError("residual full: flush first")
         self.res_k[:, self.r] = k_new.reshape(-1, self.D)
@@ -361,7 +384,7 @@ class OracleCache:
 
     # ------------------------------------------------------------- readers
     def dequant_unit(self, u: int):
-        """fp64 K^, V^ of the quantized history followed by the residual."""
+        """fp64 K^, V^: the sink (exact), the quantized history, the residual."""
         D = self.D
         ks = []
         for grp in self.k_groups[u]:
@@ -374,14 +397,16 @@ class OracleCache:
         vq = np.concatenate(vs) if vs else np.zeros((0, D))
         kr = bf16_to_f32(self.res_k[u, :self.r]).astype(np.float64)
         vr = bf16_to_f32(self.res_v[u, :self.r]).astype(np.float64)
-        return np.concatenate([kq, kr]), np.concatenate([vq, vr])
+        ks = bf16_to_f32(self.sink_k[u, :self.s]).astype(np.float64)
+        vs = bf16_to_f32(self.sink_v[u, :self.s]).astype(np.float64)
+        return np.concatenate([ks, kq, kr]), np.concatenate([vs, vq, vr])
 
     def attention(self, q: np.ndarray, units=None) -> np.ndarray:
         """q bf16 bits [B, Hq, D] -> fp64 [B, Hq, D] (rows of units not in
         ``units`` are left NaN).  Query head h reads KV head h // n_rep."""
         B, Hq, D = q.shape
         n_rep = Hq // self.Hkv
-        if self.T_q + self.r == 0:
+        if self.s + self.T_q + self.r == 0:
             raise ValueError("attention over an empty cache")
         out = np.full((B, Hq, D), np.nan)
         qf = bf16_to_f32(q).astype(np.float64)

@@ -422,3 +422,75 @@ def test_byte_formula_example():
     one = orc.cache_bytes(T=g["G"], rK=0, rV=0, D=1, k_bits=g["b"], v_bits=g["b"], Gk=g["G"],
                           Gv=g["G"], origin_bytes=g["e"], step_bytes=g["e"], float_bytes=g["f"])
     assert one * 8 / (2 * g["G"]) == g["bits_per_element"]
+
+
+# ------------------------------------------------ attention-sink window (f3)
+# PN-Mix keeps the first N_s = 32 tokens at original precision ahead of the
+# residual buffer; InnerQ keeps a high-precision window for attention-sink
+# tokens.  Reading: tokens [0, n_sink) of the sequence stay bf16 and are
+# never quantized; groups and the residual follow them.
+
+def _bf16(x):
+    """bf16 bits of x truncated toward zero (any bf16 values will do)."""
+    x = np.ascontiguousarray(x, np.float32)
+    return (x.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _seq(L, seed, D=32):
+    rng = np.random.default_rng(seed)
+    return _bf16(rng.standard_normal((1, 1, L, D))), _bf16(rng.standard_normal((1, 1, L, D)))
+
+
+def test_sink_only_cache_is_plain_bf16_attention():
+    K, V = _seq(20, 1)
+    q = _bf16(np.random.default_rng(2).standard_normal((1, 1, 32)))
+    c = orc.OracleCache(1, 1, 32, Gk=4, R=4, n_sink=32)
+    c.prefill(K, V)
+    assert (c.s, c.T_q, c.r) == (20, 0, 0)
+    ref = orc.attention(orc.bf16_to_f32(q[0, 0]).astype(np.float64),
+                        orc.bf16_to_f32(K[0, 0]).astype(np.float64),
+                        orc.bf16_to_f32(V[0, 0]).astype(np.float64))
+    assert np.allclose(c.attention(q)[0, 0], ref, rtol=0, atol=1e-12)
+
+
+def test_sink_shifts_quantization_by_its_length():
+    K, V = _seq(3 + 9 * 4 + 2, 3)
+    a = orc.OracleCache(1, 1, 32, Gk=4, R=4, n_sink=3)
+    a.prefill(K, V)
+    b = orc.OracleCache(1, 1, 32, Gk=4, R=4)
+    b.prefill(K[:, :, 3:], V[:, :, 3:])
+    assert (a.s, a.T_q, a.r) == (3, b.T_q, b.r) == (3, 36, 2)
+    for (ca, ma, sa), (cb, mb, sb) in zip(a.k_groups[0], b.k_groups[0]):
+        assert np.array_equal(ca, cb) and np.array_equal(ma, mb) and np.array_equal(sa, sb)
+    assert np.array_equal(a.sink_k[0], K[0, 0, :3]) and np.array_equal(a.sink_v[0], V[0, 0, :3])
+
+
+def test_sink_fills_before_the_residual_on_append():
+    K, V = _seq(2, 4)
+    c = orc.OracleCache(1, 1, 32, Gk=4, R=4, n_sink=3)
+    c.prefill(K, V)
+    k2, v2 = _seq(9, 5)
+    lengths = []
+    for i in range(9):
+        c.append(k2[0, 0, i], v2[0, 0, i])
+        if c.r == c.R:
+            c.flush()
+        lengths.append((c.s, c.T_q, c.r))
+    assert lengths == [(3, 0, 0), (3, 0, 1), (3, 0, 2), (3, 0, 3), (3, 4, 0), (3, 4, 1),
+                       (3, 4, 2), (3, 4, 3), (3, 8, 0)]
+    assert np.array_equal(c.sink_k[0, 2], k2[0, 0, 0])
+
+
+def test_sink_attention_is_attention_over_sink_then_history():
+    K, V = _seq(5 + 2 * 4 + 1, 6)
+    q = _bf16(np.random.default_rng(7).standard_normal((1, 1, 32)))
+    a = orc.OracleCache(1, 1, 32, Gk=4, R=4, n_sink=5)
+    a.prefill(K, V)
+    b = orc.OracleCache(1, 1, 32, Gk=4, R=4)
+    b.prefill(K[:, :, 5:], V[:, :, 5:])
+    kb, vb = b.dequant_unit(0)
+    ks = orc.bf16_to_f32(K[0, 0, :5]).astype(np.float64)
+    vs = orc.bf16_to_f32(V[0, 0, :5]).astype(np.float64)
+    ref = orc.attention(orc.bf16_to_f32(q[0, 0]).astype(np.float64),
+                        np.concatenate([ks, kb]), np.concatenate([vs, vb]))
+    assert np.allclose(a.attention(q)[0, 0], ref, rtol=0, atol=1e-12)
