@@ -44,7 +44,7 @@ class KVQError(RuntimeError):
 class _Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "batch", "kv_heads", "head_dim", "max_tokens", "k_bits", "v_bits", "k_mode",
-        "n_bf16", "n_uint4")]
+        "n_bf16", "n_uint4", "n_sink")]
 
 
 class _TierSpec(ctypes.Structure):
@@ -61,6 +61,7 @@ _SIGS = {
     "kvq_cache_alloc": (_I, [_P, _P, _Z, _P, _P]),
     "kvq_cache_free": (_I, [_P, _P]),
     "kvq_cache_lengths": (_I, [_P, _P, _P]),
+    "kvq_cache_sink_tokens": (_I, [_P, _P]),
     "kvq_cache_reset": (_I, [_P, _P]),
     "kvq_append_residual": (_I, [_P, _P, _P, _P]),
     "kvq_flush_group": (_I, [_P, _P, _P]),
@@ -74,6 +75,7 @@ _SIGS = {
     "kvq_export_k": (_I, [_P, _P, _P, _P, _P]),
     "kvq_export_v": (_I, [_P, _P, _P, _P, _P]),
     "kvq_export_residual": (_I, [_P, _P, _P, _P]),
+    "kvq_export_sink": (_I, [_P, _P, _P, _P]),
     "kvq_export_k_mixed": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvq_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -125,14 +127,17 @@ class KVCache:
     mode "uniform": keys at k_bits per channel over 128-token groups;
     mode "mixed": keys tiered per group into n_bf16 BF16, n_uint4 UINT4 and
     the rest UINT2 channels.  Values always v_bits per token over 32 channels.
+    n_sink > 0 keeps the sequence's first n_sink tokens bf16 (attention
+    sinks, never quantized).
     The device buffer is a torch uint8 tensor owned by this object.
     """
 
     def __init__(self, batch: int, kv_heads: int, max_tokens: int, k_bits: int = 2,
                  v_bits: int = 2, mode: str = "uniform", n_bf16: int = 0, n_uint4: int = 0,
-                 head_dim: int = HEAD_DIM, device=None, stream=None):
+                 head_dim: int = HEAD_DIM, device=None, stream=None, n_sink: int = 0):
         self.cfg = _Config(batch, kv_heads, head_dim, max_tokens, k_bits, v_bits,
-                           KVQ_K_MIXED if mode == "mixed" else KVQ_K_UNIFORM, n_bf16, n_uint4)
+                           KVQ_K_MIXED if mode == "mixed" else KVQ_K_UNIFORM, n_bf16, n_uint4,
+                           n_sink)
         self.mode = mode
         nbytes = lib().kvq_cache_bytes(ctypes.byref(self.cfg))
         if nbytes == 0:
@@ -147,6 +152,7 @@ class KVCache:
         self._h = h
         self.batch, self.kv_heads, self.max_tokens = batch, kv_heads, max_tokens
         self.k_bits, self.v_bits, self.n_bf16, self.n_uint4 = k_bits, v_bits, n_bf16, n_uint4
+        self.n_sink = n_sink
         self.device = dev
 
     def __del__(self):
@@ -164,6 +170,11 @@ class KVCache:
         tq, r = ctypes.c_int(), ctypes.c_int()
         _check(lib().kvq_cache_lengths(self._h, ctypes.byref(tq), ctypes.byref(r)), "lengths")
         return tq.value, r.value
+
+    def sink_tokens(self) -> int:
+        s = ctypes.c_int()
+        _check(lib().kvq_cache_sink_tokens(self._h, ctypes.byref(s)), "sink_tokens")
+        return s.value
 
     def status(self, stream=None) -> int:
         st = ctypes.c_int()
@@ -244,6 +255,15 @@ class KVCache:
         _check(lib().kvq_export_residual(self._h, kr.data_ptr(), vr.data_ptr(), _stream(stream)),
                "kvq_export_residual")
         return kr, vr
+
+    def export_sink(self, stream=None):
+        s = self.sink_tokens()
+        B, H, dev = self.batch, self.kv_heads, self.device
+        ks = torch.empty(B, H, s, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        vs = torch.empty(B, H, s, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        _check(lib().kvq_export_sink(self._h, ks.data_ptr(), vs.data_ptr(), _stream(stream)),
+               "kvq_export_sink")
+        return ks, vs
 
     def export_k_mixed(self, stream=None):
         tq, _ = self.lengths()

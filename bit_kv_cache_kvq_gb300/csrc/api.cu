@@ -22,6 +22,7 @@ bool valid_config(const kvq_config* c) {
   if (c->head_dim != kD) return false;
   if (c->max_tokens % kKG) return false;
   if (c->v_bits != 2 && c->v_bits != 4) return false;
+  if (c->n_sink < 0 || c->n_sink > kR) return false;
   if (c->k_mode == KVQ_K_UNIFORM) {
     if (c->k_bits != 2 && c->k_bits != 4) return false;
   } else if (c->k_mode == KVQ_K_MIXED) {
@@ -38,7 +39,7 @@ RecLayout layout_of(const kvq_config* c) {
 }
 
 struct Sizes {
-  size_t records, residual, status, total;
+  size_t records, residual, sink, status, total;
 };
 
 Sizes sizes_of(const kvq_config* c) {
@@ -47,8 +48,9 @@ Sizes sizes_of(const kvq_config* c) {
   Sizes s;
   s.records = round_up(units * (c->max_tokens / kKG) * static_cast<size_t>(L.bytes));
   s.residual = round_up(units * kR * kD * sizeof(kvq_bf16));
+  s.sink = round_up(units * static_cast<size_t>(c->n_sink) * kD * sizeof(kvq_bf16));
   s.status = kAlign;
-  s.total = s.records + 2 * s.residual + s.status;
+  s.total = s.records + 2 * s.residual + 2 * s.sink + s.status;
   return s;
 }
 
@@ -103,9 +105,12 @@ int kvq_cache_alloc(const kvq_config* cfg, void* dev_buf, size_t buf_bytes,
   c->max_groups = cfg->max_tokens / kKG;
   c->res_k = reinterpret_cast<kvq_bf16*>(c->base + sz.records);
   c->res_v = reinterpret_cast<kvq_bf16*>(c->base + sz.records + sz.residual);
-  c->status = reinterpret_cast<unsigned*>(c->base + sz.records + 2 * sz.residual);
+  c->sink_k = reinterpret_cast<kvq_bf16*>(c->base + sz.records + 2 * sz.residual);
+  c->sink_v = reinterpret_cast<kvq_bf16*>(c->base + sz.records + 2 * sz.residual + sz.sink);
+  c->status = reinterpret_cast<unsigned*>(c->base + sz.records + 2 * sz.residual + 2 * sz.sink);
   c->t_q = 0;
   c->r = 0;
+  c->s = 0;
   if (cudaMemsetAsync(c->status, 0, sizeof(unsigned), s) != cudaSuccess) {
     if (c->owned) cudaFreeAsync(c->base, s);
     delete c;
@@ -130,11 +135,18 @@ int kvq_cache_lengths(const kvq_cache* c, int* quantized_tokens, int* residual_t
   return KVQ_OK;
 }
 
+int kvq_cache_sink_tokens(const kvq_cache* c, int* sink_tokens) {
+  if (!c || !sink_tokens) return KVQ_ERR_ARG;
+  *sink_tokens = c->s;
+  return KVQ_OK;
+}
+
 int kvq_cache_reset(kvq_cache* c, cudaStream_t s) {
   if (!c) return KVQ_ERR_ARG;
   if (cudaMemsetAsync(c->status, 0, sizeof(unsigned), s) != cudaSuccess) return KVQ_ERR_CUDA;
   c->t_q = 0;
   c->r = 0;
+  c->s = 0;
   return KVQ_OK;
 }
 
@@ -142,8 +154,15 @@ int kvq_append_residual(kvq_cache* c, const kvq_bf16* k_new, const kvq_bf16* v_n
                         cudaStream_t s) {
   if (!c || !k_new || !v_new) return KVQ_ERR_ARG;
   if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
+  if (c->s < c->cfg.n_sink) {   // the sequence's first tokens are the sinks
+    const cudaError_t e = launch_append(c, k_new, v_new, c->sink_k, c->sink_v, c->cfg.n_sink,
+                                        c->s, s);
+    if (e != cudaSuccess) return KVQ_ERR_CUDA;
+    c->s += 1;
+    return KVQ_OK;
+  }
   if (c->r >= kR) return KVQ_ERR_RESIDUAL_FULL;
-  const cudaError_t e = launch_append(c, k_new, v_new, s);
+  const cudaError_t e = launch_append(c, k_new, v_new, c->res_k, c->res_v, kR, c->r, s);
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
   c->r += 1;
   return KVQ_OK;
@@ -175,15 +194,21 @@ int kvq_quantize_prefill(kvq_cache* c, const kvq_bf16* k, const kvq_bf16* v, int
   if (L > 0 && (!aligned16(k) || !aligned16(v))) return KVQ_ERR_ARG;
   const int m = check_importance(c, importance);
   if (m != KVQ_OK) return m;
-  if (c->t_q != 0 || c->r != 0) return KVQ_ERR_NOT_EMPTY;
-  const int n_q = L / kKG;
-  const int r = L % kKG;
+  if (c->t_q != 0 || c->r != 0 || c->s != 0) return KVQ_ERR_NOT_EMPTY;
+  const int sk = L < c->cfg.n_sink ? L : c->cfg.n_sink;   // sink tokens
+  const int n_q = (L - sk) / kKG;
+  const int r = (L - sk) % kKG;
   if (n_q * kKG > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
   if (L == 0) return KVQ_OK;
-  QuantSrc src{k, v, static_cast<long long>(L) * kD, static_cast<long long>(kKG) * kD};
-  cudaError_t e = launch_quantize(c, src, n_q, 0, importance, s);
-  if (e == cudaSuccess) e = launch_residual_tail(c, k, v, L, n_q * kKG, r, s);
+  const int units = c->cfg.batch * c->cfg.kv_heads;
+  cudaError_t e = launch_copy_tokens(k, v, L, 0, sk, c->sink_k, c->sink_v, c->cfg.n_sink, units, s);
+  QuantSrc src{k + static_cast<size_t>(sk) * kD, v + static_cast<size_t>(sk) * kD,
+               static_cast<long long>(L) * kD, static_cast<long long>(kKG) * kD};
+  if (e == cudaSuccess) e = launch_quantize(c, src, n_q, 0, importance, s);
+  if (e == cudaSuccess)
+    e = launch_copy_tokens(k, v, L, sk + n_q * kKG, r, c->res_k, c->res_v, kR, units, s);
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  c->s = sk;
   c->t_q = n_q * kKG;
   c->r = r;
   return KVQ_OK;
@@ -205,12 +230,12 @@ int kvq_decode_attention(const kvq_cache* c, const kvq_bf16* q, int Hq, float* o
                          void* ws, size_t ws_bytes, cudaStream_t s) {
   if (!c || !q || !out) return KVQ_ERR_ARG;
   if (!valid_rep(Hq, c->cfg.kv_heads)) return KVQ_ERR_SHAPE;
-  if (c->t_q + c->r == 0) return KVQ_ERR_EMPTY;
+  if (c->s + c->t_q + c->r == 0) return KVQ_ERR_EMPTY;
   if (!ws || ws_bytes < kvq_decode_workspace_bytes(c, Hq) || !aligned16(ws))
     return KVQ_ERR_WORKSPACE;
   MmaPlan plan;
   if (!mma_plan(c->num_sms, c->cfg.batch * c->cfg.kv_heads, Hq / c->cfg.kv_heads,
-                c->t_q / kKG, c->r, c->lay.bytes, ws_bytes, &plan))
+                c->t_q / kKG, c->r, c->s, c->lay.bytes, ws_bytes, &plan))
     return KVQ_ERR_WORKSPACE;
   return cuda_status(launch_decode_mma(c, q, Hq, out, static_cast<float*>(ws), plan, s));
 }
@@ -296,6 +321,21 @@ int kvq_export_residual(const kvq_cache* c, kvq_bf16* k_r, kvq_bf16* v_r, cudaSt
                                     cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess)
     e = cudaMemcpy2DAsync(v_r, c->r * row, c->res_v, kR * row, c->r * row, units,
+                          cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+int kvq_export_sink(const kvq_cache* c, kvq_bf16* k, kvq_bf16* v, cudaStream_t s) {
+  if (!c) return KVQ_ERR_ARG;
+  if (c->s == 0) return KVQ_OK;   // nothing to copy; empty buffers may be NULL
+  if (!k || !v) return KVQ_ERR_ARG;
+  const int units = c->cfg.batch * c->cfg.kv_heads;
+  const size_t row = kD * sizeof(kvq_bf16);
+  const size_t cap = static_cast<size_t>(c->cfg.n_sink) * row;
+  cudaError_t e = cudaMemcpy2DAsync(k, c->s * row, c->sink_k, cap, c->s * row, units,
+                                    cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpy2DAsync(v, c->s * row, c->sink_v, cap, c->s * row, units,
                           cudaMemcpyDeviceToDevice, s);
   return cuda_status(e);
 }

@@ -25,7 +25,8 @@
 // one shuffle adds it back; with 8 heads a second MMA per k-step adds it.
 //
 // Work split ("stream-K"): the flattened sequence of items (for each unit
-// its groups, then its residual as one item of weight kResidualWeight) is
+// its groups, then its residual window and its attention-sink window, one
+// item each) is
 // cut into equal contiguous slices, one per warp; a warp keeps one online-
 // softmax state per unit it touches and writes one partial per unit.  Each
 // warp stages one record at a time in its own shared memory, in two parts:
@@ -118,6 +119,9 @@ struct MmaArgs {
   int r;                  // residual tokens
   const uint16_t* res_k;  // [units][128][D]
   const uint16_t* res_v;
+  int s, n_sink;          // sink tokens, sink window capacity
+  const uint16_t* sink_k; // [units][n_sink][D]
+  const uint16_t* sink_v;
   const uint16_t* q;      // [B][Hq][D]
   int Hkv, Hq, units;
   long long unit_len;     // weighted positions per unit
@@ -717,16 +721,18 @@ struct Warp {
            ((col16 ^ (row & 7)) << 4);
   }
 
-  // The bf16 residual window (r tokens) on tensor cores, folded into the
-  // same online-softmax state.  Scores: bf16 MMA of the exact bf16 keys and
+  // A bf16 window (the residual, or the attention sinks: count tokens of a
+  // [units][cap][D] pair) on tensor cores, folded into the same
+  // online-softmax state.  Scores: bf16 MMA of the exact bf16 keys and
   // query (exact products, fp32 sums).  P·V: the values transposed by
   // ldmatrix, p split into bf16 high and low parts (16 bits in all), one
   // fresh accumulator per chunk and channel tile.  Keys and values stream
   // through two 4 KB chunk slots of the record buffer.
-  __device__ __forceinline__ void residual(int u) {
-    const int r = a.r, nc = (r + 15) >> 4;
-    const uint8_t* kr = reinterpret_cast<const uint8_t*>(a.res_k + static_cast<long long>(u) * kR * kD);
-    const uint8_t* vr = reinterpret_cast<const uint8_t*>(a.res_v + static_cast<long long>(u) * kR * kD);
+  __device__ __forceinline__ void window(int u, const uint16_t* kbase, const uint16_t* vbase,
+                                        int count, int cap) {
+    const int r = count, nc = (r + 15) >> 4;
+    const uint8_t* kr = reinterpret_cast<const uint8_t*>(kbase + static_cast<long long>(u) * cap * kD);
+    const uint8_t* vr = reinterpret_cast<const uint8_t*>(vbase + static_cast<long long>(u) * cap * kD);
     // query B fragments: column g = head g (zero for g >= NREP)
     uint32_t bqr[8][2];
     {
@@ -887,6 +893,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) decode_mma_kernel(MmaArgs a
     const int g0 = static_cast<int>(lo);
     const int g1 = static_cast<int>(min(hi, static_cast<long long>(a.n_groups)));
     const bool res = a.r > 0 && lo <= a.n_groups && a.n_groups < hi;
+    const int ps = a.n_groups + (a.r > 0 ? 1 : 0);   // position of the sink item
+    const bool snk = a.s > 0 && lo <= ps && ps < hi;
     W.begin_unit(u);
     if (g0 < g1) {
       // keys of group i+1 load during the softmax and P·V of group i; values
@@ -914,7 +922,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) decode_mma_kernel(MmaArgs a
       asm volatile("cp.async.wait_group 0;\n" ::);
       __syncwarp();
     }
-    if (res) W.residual(u);
+    if (res) W.window(u, a.res_k, a.res_v, a.r, kR);
+    if (snk) W.window(u, a.sink_k, a.sink_v, a.s, a.n_sink);
     W.finish(u, slot - slot_of(a, ub));
   }
 }
@@ -1015,9 +1024,9 @@ int mma_warps_per_cta(int rec_bytes) {
   return max(1, min(kMaxWarps, (227 * 1024) / per));
 }
 
-bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int rec_bytes,
+bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int sink, int rec_bytes,
               size_t ws_cap, MmaPlan* plan) {
-  plan->unit_len = n_groups + (r > 0 ? kResidualWeight : 0);
+  plan->unit_len = n_groups + (r > 0 ? kResidualWeight : 0) + (sink > 0 ? kResidualWeight : 0);
   const long long total = static_cast<long long>(units) * plan->unit_len;
   const long long resident = static_cast<long long>(num_sms) * mma_warps_per_cta(rec_bytes);
   long long slots = total < resident ? total : resident;
@@ -1040,7 +1049,7 @@ size_t mma_ws_bytes(int num_sms, int B, int Hkv, int Hq, int max_groups, int rec
   const int units = B * Hkv;
   const long long resident = static_cast<long long>(num_sms) * mma_warps_per_cta(rec_bytes);
   const long long per_unit = (resident + units - 1) / units + 2;
-  const long long cap = static_cast<long long>(max_groups) + kResidualWeight + 1;
+  const long long cap = static_cast<long long>(max_groups) + 2 * kResidualWeight + 1;
   const long long parts = per_unit < cap ? per_unit : cap;
   return static_cast<size_t>(units) * parts * (Hq / Hkv) * (kD + 2) * sizeof(float);
 }
@@ -1073,6 +1082,10 @@ cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, flo
   a.r = c->r;
   a.res_k = c->res_k;
   a.res_v = c->res_v;
+  a.s = c->s;
+  a.n_sink = c->cfg.n_sink;
+  a.sink_k = c->sink_k;
+  a.sink_v = c->sink_v;
   a.q = q;
   a.Hkv = c->cfg.kv_heads;
   a.Hq = Hq;

@@ -52,12 +52,12 @@ extern "C" int kvq_decode_attention_static(const kvq_cache* c, const kvq_bf16* q
   if (Hq < 1 || Hq % c->cfg.kv_heads) return KVQ_ERR_SHAPE;
   const int n_rep = Hq / c->cfg.kv_heads;
   if (n_rep != 1 && n_rep != 2 && n_rep != 4 && n_rep != 8) return KVQ_ERR_SHAPE;
-  if (c->t_q + c->r == 0) return KVQ_ERR_EMPTY;
+  if (c->s + c->t_q + c->r == 0) return KVQ_ERR_EMPTY;
 
   // Plan the split so its partials fit the fixed array; reject what cannot
   // fit with two partial slots per (batch row, KV head).
   MmaPlan plan;
-  if (!mma_plan(c->num_sms, c->cfg.batch * c->cfg.kv_heads, n_rep, c->t_q / kKG, c->r,
+  if (!mma_plan(c->num_sms, c->cfg.batch * c->cfg.kv_heads, n_rep, c->t_q / kKG, c->r, c->s,
                 c->lay.bytes, KVQ_STATIC_WORKSPACE_BYTES, &plan))
     return KVQ_ERR_WORKSPACE;
 

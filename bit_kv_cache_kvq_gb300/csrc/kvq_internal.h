@@ -115,9 +115,12 @@ struct kvq_cache {
   int max_groups;
   kvq_bf16* res_k;     // [B*Hkv][128][D]
   kvq_bf16* res_v;
+  kvq_bf16* sink_k;    // [B*Hkv][n_sink][D] (attention-sink window)
+  kvq_bf16* sink_v;
   unsigned* status;    // sticky KVQ_FLAG_* word
   int t_q;             // quantized tokens (multiple of 128)
   int r;               // residual tokens (0..128)
+  int s;               // sink tokens (0..n_sink)
 };
 
 namespace kvq {
@@ -130,14 +133,18 @@ struct QuantSrc {
   long long group_stride;  // elements between consecutive 128-token tiles
 };
 
-cudaError_t launch_append(const kvq_cache* c, const kvq_bf16* k_new,
-                          const kvq_bf16* v_new, cudaStream_t s);
+// One token into slot `slot` of a [units][cap][D] bf16 window pair (the
+// residual or the sink).
+cudaError_t launch_append(const kvq_cache* c, const kvq_bf16* k_new, const kvq_bf16* v_new,
+                          kvq_bf16* dst_k, kvq_bf16* dst_v, int cap, int slot, cudaStream_t s);
+// Tokens [first, first + count) of k, v [units][L][D] into rows 0..count-1
+// of a [units][cap][D] window pair.
+cudaError_t launch_copy_tokens(const kvq_bf16* k, const kvq_bf16* v, int L, int first, int count,
+                               kvq_bf16* dst_k, kvq_bf16* dst_v, int cap, int units,
+                               cudaStream_t s);
 cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
                             int first_group, const float* importance,
                             cudaStream_t s);
-cudaError_t launch_residual_tail(const kvq_cache* c, const kvq_bf16* k,
-                                 const kvq_bf16* v, int L, int first,
-                                 int count, cudaStream_t s);
 
 
 // Tensor-core decode (decode_mma.cu).  The plan cuts the weighted item
@@ -150,7 +157,7 @@ struct MmaPlan {
 };
 int mma_warps_per_cta(int rec_bytes);
 // false if even two partial slots per unit exceed ws_cap (0 = no cap)
-bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int rec_bytes,
+bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int sink, int rec_bytes,
               size_t ws_cap, MmaPlan* plan);
 size_t mma_ws_bytes(int num_sms, int B, int Hkv, int Hq, int max_groups, int rec_bytes);
 cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, float* out,

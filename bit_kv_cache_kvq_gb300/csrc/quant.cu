@@ -530,17 +530,17 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
 }
 
 __global__ void append_kernel(const uint4* __restrict__ k_new,
-                              const uint4* __restrict__ v_new, uint4* res_k,
-                              uint4* res_v, int r) {
+                              const uint4* __restrict__ v_new, uint4* dst_k,
+                              uint4* dst_v, int cap, int slot) {
   // one (b, kv head) per block; 16 x 16 bytes per row of D bf16
   constexpr int kRow = kD * 2 / 16;
   const int u = blockIdx.x;
   const int i = threadIdx.x;
-  const long long dst = (static_cast<long long>(u) * kR + r) * kRow;
+  const long long dst = (static_cast<long long>(u) * cap + slot) * kRow;
   if (i < kRow)
-    res_k[dst + i] = __ldg(k_new + static_cast<long long>(u) * kRow + i);
+    dst_k[dst + i] = __ldg(k_new + static_cast<long long>(u) * kRow + i);
   else if (i < 2 * kRow)
-    res_v[dst + i - kRow] = __ldg(v_new + static_cast<long long>(u) * kRow + i - kRow);
+    dst_v[dst + i - kRow] = __ldg(v_new + static_cast<long long>(u) * kRow + i - kRow);
 }
 
 // Copy one section (bytes at offset off of every group record) of records
@@ -660,13 +660,13 @@ cudaError_t set_smem(K kernel, int bytes) {
 
 }  // namespace
 
-cudaError_t launch_append(const kvq_cache* c, const kvq_bf16* k_new,
-                          const kvq_bf16* v_new, cudaStream_t s) {
+cudaError_t launch_append(const kvq_cache* c, const kvq_bf16* k_new, const kvq_bf16* v_new,
+                          kvq_bf16* dst_k, kvq_bf16* dst_v, int cap, int slot, cudaStream_t s) {
   const int units = c->cfg.batch * c->cfg.kv_heads;
   append_kernel<<<units, 32, 0, s>>>(reinterpret_cast<const uint4*>(k_new),
                                      reinterpret_cast<const uint4*>(v_new),
-                                     reinterpret_cast<uint4*>(c->res_k),
-                                     reinterpret_cast<uint4*>(c->res_v), c->r);
+                                     reinterpret_cast<uint4*>(dst_k),
+                                     reinterpret_cast<uint4*>(dst_v), cap, slot);
   return cudaGetLastError();
 }
 
@@ -709,17 +709,16 @@ cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
   return cudaGetLastError();
 }
 
-cudaError_t launch_residual_tail(const kvq_cache* c, const kvq_bf16* k,
-                                 const kvq_bf16* v, int L, int first,
-                                 int count, cudaStream_t s) {
+cudaError_t launch_copy_tokens(const kvq_bf16* k, const kvq_bf16* v, int L, int first, int count,
+                               kvq_bf16* dst_k, kvq_bf16* dst_v, int cap, int units,
+                               cudaStream_t s) {
   if (count == 0) return cudaSuccess;
-  const int units = c->cfg.batch * c->cfg.kv_heads;
   const size_t row = static_cast<size_t>(kD) * sizeof(kvq_bf16);
-  cudaError_t e = cudaMemcpy2DAsync(c->res_k, kR * row, k + static_cast<size_t>(first) * kD,
+  cudaError_t e = cudaMemcpy2DAsync(dst_k, cap * row, k + static_cast<size_t>(first) * kD,
                                     static_cast<size_t>(L) * row, count * row, units,
                                     cudaMemcpyDeviceToDevice, s);
   if (e != cudaSuccess) return e;
-  return cudaMemcpy2DAsync(c->res_v, kR * row, v + static_cast<size_t>(first) * kD,
+  return cudaMemcpy2DAsync(dst_v, cap * row, v + static_cast<size_t>(first) * kD,
                            static_cast<size_t>(L) * row, count * row, units,
                            cudaMemcpyDeviceToDevice, s);
 }

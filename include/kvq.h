@@ -96,6 +96,10 @@ typedef struct kvq_config {
   int n_bf16;      /* KVQ_K_MIXED: BF16-tier channels per key group         */
   int n_uint4;     /* KVQ_K_MIXED: UINT4-tier channels per key group; the
                       remaining D - n_bf16 - n_uint4 channels are UINT2     */
+  int n_sink;      /* attention-sink window, 0..128: the sequence's first
+                      n_sink tokens stay bf16 and are never quantized
+                      (PN-Mix sink protection, N_s = 32; InnerQ's
+                      high-precision window); 0 = none                      */
 } kvq_config;
 
 typedef struct kvq_tier_spec {
@@ -112,7 +116,8 @@ typedef struct kvq_cache kvq_cache; /* opaque */
  * Device bytes one cache needs: the packed history (per (batch row, KV
  * head), max_tokens/128 group records of codes plus per-group origins
  * (bf16) and steps (fp32)), the bf16 residual windows [B][Hkv][128][D] for
- * K and V, and the status word.  KIVI article §7 gives the accounting.
+ * K and V, the bf16 sink windows [B][Hkv][n_sink][D], and the status word.
+ * KIVI article §7 gives the accounting.
  * Returns 0 for an invalid config.
  */
 size_t kvq_cache_bytes(const kvq_config* cfg);
@@ -133,12 +138,17 @@ int kvq_cache_free(kvq_cache* cache, cudaStream_t s);
 int kvq_cache_lengths(const kvq_cache* cache, int* quantized_tokens,
                       int* residual_tokens);
 
+/* Host-side length of the attention-sink window (0..n_sink). */
+int kvq_cache_sink_tokens(const kvq_cache* cache, int* sink_tokens);
+
 /* Empty the cache (lengths to 0, status word cleared on s). */
 int kvq_cache_reset(kvq_cache* cache, cudaStream_t s);
 
 /*
  * MixKVQ Algorithm 1, Decoding, first step: append one token's key and
- * value (k_new, v_new: bf16 [B][Hkv][D]) to residual slot r; r += 1.
+ * value (k_new, v_new: bf16 [B][Hkv][D]) to residual slot r; r += 1.  While
+ * the attention-sink window holds fewer than n_sink tokens the token goes
+ * there instead (the sequence's first tokens are the sinks).
  * Errors: ARG, RESIDUAL_FULL (r == 128: call kvq_flush_group first), CUDA.
  */
 int kvq_append_residual(kvq_cache* cache, const kvq_bf16* k_new,
@@ -161,9 +171,10 @@ int kvq_flush_group(kvq_cache* cache, const float* importance, cudaStream_t s);
 
 /*
  * MixKVQ Algorithm 1, Prefill: k, v bf16 [B][Hkv][L][D]; the first
- * L - (L mod 128) tokens are quantized into floor(L/128) groups exactly as
- * kvq_flush_group does, the last L mod 128 tokens go to the residual.
- * importance: as for kvq_flush_group.  L = 0 is allowed (no-op).
+ * s = min(L, n_sink) tokens go to the attention-sink window; of the other
+ * L' = L - s, the first L' - (L' mod 128) are quantized into floor(L'/128)
+ * groups exactly as kvq_flush_group does and the last L' mod 128 go to the
+ * residual.  importance: as for kvq_flush_group.  L = 0 is allowed (no-op).
  * Errors: ARG, MODE, NOT_EMPTY, CAPACITY, CUDA.  Flags: NONFINITE, RANGE.
  */
 int kvq_quantize_prefill(kvq_cache* cache, const kvq_bf16* k,
@@ -180,8 +191,8 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int Hq);
 /*
  * Fused decode attention (KIVI article §1 and §6; MixKVQ Algorithm 1 last
  * three lines): for each (b, h), s_t = q·k^_t / sqrt(D) over the
- * dequantized history followed by the residual tokens, p = softmax over all
- * of them together, o = sum_t p_t v^_t.  q: bf16 [B][Hq][D], Hq a multiple
+ * attention-sink tokens (bf16), the dequantized history and the residual
+ * tokens, p = softmax over all of them together, o = sum_t p_t v^_t.  q: bf16 [B][Hq][D], Hq a multiple
  * of Hkv (at most 8 query heads per KV head); out: fp32 [B][Hq][D].
  * Uniform and mixed (MixKVQ) key caches alike: in a mixed group k^ is the
  * raw bf16 key on the BF16 tier and the dequantized code on the others.
@@ -279,6 +290,12 @@ int kvq_export_residual(const kvq_cache* cache, kvq_bf16* k_r, kvq_bf16* v_r,
 int kvq_export_k_mixed(const kvq_cache* cache, uint8_t* perm, kvq_bf16* raw,
                        uint8_t* c4, kvq_bf16* m4, float* s4, uint8_t* c2,
                        kvq_bf16* m2, float* s2, cudaStream_t s);
+
+/*
+ * The attention-sink window: k, v bf16 [B][Hkv][s][D] (s =
+ * kvq_cache_sink_tokens; NULL allowed when s = 0).  Errors: ARG, CUDA.
+ */
+int kvq_export_sink(const kvq_cache* cache, kvq_bf16* k, kvq_bf16* v, cudaStream_t s);
 
 /* Human-readable name of a return code. */
 const char* kvq_status_string(int code);

@@ -49,11 +49,12 @@ class UnitOracles:
     """One oracle cache per sampled (b, kv head) unit, fed the same bf16
     inputs as the GPU cache."""
 
-    def __init__(self, units, Hkv, k_bits=2, v_bits=2, mode="uniform", n_bf16=0, n_uint4=0):
+    def __init__(self, units, Hkv, k_bits=2, v_bits=2, mode="uniform", n_bf16=0, n_uint4=0,
+                 n_sink=0):
         self.units = list(units)
         self.Hkv = Hkv
         self.caches = [orc.OracleCache(1, 1, 128, k_bits, v_bits, mode=mode, n_bf16=n_bf16,
-                                       n_uint4=n_uint4) for _ in self.units]
+                                       n_uint4=n_uint4, n_sink=n_sink) for _ in self.units]
 
     def _sel(self, t: torch.Tensor, u: int):
         b, h = divmod(u, self.Hkv)
@@ -147,3 +148,15 @@ def assert_mixed_exports_equal(cache: kvq.KVCache, ref: UnitOracles):
         r = oc.r
         assert np.array_equal(krb[b, h], oc.res_k[0, :r]), f"K residual differs (unit {u})"
         assert np.array_equal(vrb[b, h], oc.res_v[0, :r]), f"V residual differs (unit {u})"
+
+
+def assert_sink_equal(cache: kvq.KVCache, ref: UnitOracles):
+    """The attention-sink window, bit-exact, and its length."""
+    ks, vs = cache.export_sink()
+    torch.cuda.synchronize()
+    ksb, vsb = bf16_bits(ks), bf16_bits(vs)
+    for u, oc in zip(ref.units, ref.caches):
+        b, h = divmod(u, ref.Hkv)
+        assert cache.sink_tokens() == oc.s
+        assert np.array_equal(ksb[b, h], oc.sink_k[0, :oc.s]), f"K sink differs (unit {u})"
+        assert np.array_equal(vsb[b, h], oc.sink_v[0, :oc.s]), f"V sink differs (unit {u})"

@@ -70,12 +70,24 @@ def test_mixed_record_bytes(lib):
     assert per_group == (kpart + padding + 127) // 128 * 128 + v
 
 
+def test_sink_windows_add_their_bytes(lib):
+    """An attention-sink window of n_sink tokens adds two bf16 windows
+    [B][Hkv][n_sink][D] (rounded to 256 bytes)."""
+    base = _bytes(2, 3, 256)
+    cfg = kvq._Config(2, 3, 128, 256, 2, 2, 0, 0, 0, 32)
+    with_sink = kvq.lib().kvq_cache_bytes(ctypes.byref(cfg))
+    assert with_sink - base == 2 * ((2 * 3 * 32 * 128 * 2 + 255) // 256 * 256)
+
+
 def test_invalid_configs_report_zero_bytes(lib):
     assert _bytes(1, 1, 128, D=64) == 0          # head_dim other than 128
     assert _bytes(1, 1, 100) == 0                # capacity not a multiple of 128
     assert _bytes(1, 1, 128, k_bits=3) == 0
     assert _bytes(0, 1, 128) == 0
     assert _bytes(1, 1, 128, mode=1, nb=100, n4=40) == 0
+    for n_sink in (-1, 129):                     # sink window 0..128
+        cfg = kvq._Config(1, 1, 128, 128, 2, 2, 0, 0, 0, n_sink)
+        assert kvq.lib().kvq_cache_bytes(ctypes.byref(cfg)) == 0
 
 
 def test_status_strings(lib):
