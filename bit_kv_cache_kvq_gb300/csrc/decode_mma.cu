@@ -129,7 +129,28 @@ struct MmaArgs {
   int n_slots;            // warps with work
   int max_parts;          // partial slots per unit in ws
   float* ws;              // [units][max_parts][NREP][D + 2]
+  unsigned* status;       // sticky KVQ_FLAG_* word of the cache
 };
+
+// mbarrier helpers for the bulk staging of records.
+__device__ __forceinline__ void mbar_init(uint32_t mb) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(mb) : "memory");
+}
+// Wait for phase `parity` of mbarrier mb; false if it did not complete
+// within the iteration limit (each try_wait also suspends for a while).
+__device__ __forceinline__ bool mbar_wait(uint32_t mb, uint32_t parity) {
+  for (int i = 0; i < (1 << 20); ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(mb), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
 
 __device__ __forceinline__ long long slot_start(const MmaArgs& a, int w) {
   return (static_cast<long long>(w) * a.total) / a.n_slots;
@@ -151,6 +172,8 @@ struct Warp {
   uint32_t* vsb;   // value-step table, B order (vsb_index)
   uint32_t* vmb;   // value-origin table, A order (vmb_index)
   void* qs;        // the unit's query (see kQBytes)
+  uint32_t mb_k, mb_v;        // mbarriers of the staged key / value parts
+  uint32_t ph_k = 0, ph_v = 0;  // their current phase parities
   // mixed keys only:
   const uint16_t* qg_row;  // this lane's query head (g, capped at NREP - 1) in global memory
   float qmax;      // max |query| of the head row this lane builds B columns for
@@ -169,6 +192,15 @@ struct Warp {
     vsb = reinterpret_cast<uint32_t*>(base + rb);
     vmb = reinterpret_cast<uint32_t*>(base + rb + kVsbBytes);
     qs = base + rb + kVsbBytes + kVmbBytes;
+    // the two mbarriers sit in the padding of query row 1
+    mb_k = static_cast<uint32_t>(__cvta_generic_to_shared(qs)) + (SPARE ? (kQRow + kD) * 4 : (kQRow + kD) * 2);
+    mb_v = mb_k + 8;
+    if (lane == 0) {
+      mbar_init(mb_k);
+      mbar_init(mb_v);
+      asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncwarp();
     if (MIX) {
       if (lane < 4) reinterpret_cast<uint32_t*>(zero_row())[lane] = 0u;
       __syncwarp();
@@ -233,18 +265,37 @@ struct Warp {
     lrun[0] = lrun[1] = 0.0f;
   }
 
-  // cp.async of bytes [lo, hi) of group record grp of unit u into dst.
-  __device__ __forceinline__ void issue(int u, int grp, uint8_t* dst, int lo, int hi) {
-    const uint8_t* src = a.records + (static_cast<long long>(u) * a.max_groups + grp) * a.rec_bytes + lo;
-    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-    const int chunks = (hi - lo) >> 4;
-    for (int c = lane; c < chunks; c += 32)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d + 16 * c),
-                   "l"(src + 16 * c));
+  // Bytes [lo, hi) of group record grp of unit u into dst with one bulk
+  // copy issued by lane 0, completing on mbarrier mb (the warp has read
+  // dst's previous contents: __syncwarp before, then the proxy fence).
+  __device__ __forceinline__ void issue(int u, int grp, uint8_t* dst, int lo, int hi, uint32_t mb) {
+    if (lane == 0) {
+      const uint8_t* src = a.records + (static_cast<long long>(u) * a.max_groups + grp) * a.rec_bytes + lo;
+      const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+      const uint32_t bytes = static_cast<uint32_t>(hi - lo);
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mb), "r"(bytes)
+                   : "memory");
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+          ::"r"(d), "l"(src), "r"(bytes), "r"(mb)
+          : "memory");
+    }
   }
-  __device__ __forceinline__ void issue_k(int u, int grp) { issue(u, grp, kbuf, 0, a.lay.kpart); }
+  __device__ __forceinline__ void issue_k(int u, int grp) { issue(u, grp, kbuf, 0, a.lay.kpart, mb_k); }
   __device__ __forceinline__ void issue_v(int u, int grp) {
-    issue(u, grp, vbuf, a.lay.kpart, static_cast<int>(a.rec_bytes));
+    issue(u, grp, vbuf, a.lay.kpart, static_cast<int>(a.rec_bytes), mb_v);
+  }
+  // Wait for the staged key (value) part; on a timeout record the flag and
+  // return false (the caller stops; the copy is waited for once more).
+  __device__ __forceinline__ bool wait_part(uint32_t mb, uint32_t& phase) {
+    const bool ok = mbar_wait(mb, phase);
+    phase ^= 1u;
+    if (!ok) {
+      if (lane == 0) atomicOr(a.status, static_cast<unsigned>(KVQ_FLAG_TIMEOUT));
+      mbar_wait(mb, phase ^ 1u);
+    }
+    return ok;
   }
 
   // Scores of one group (keys in kbuf), softmax folded into the running
@@ -897,30 +948,28 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) decode_mma_kernel(MmaArgs a
     const bool snk = a.s > 0 && lo <= ps && ps < hi;
     W.begin_unit(u);
     if (g0 < g1) {
-      // keys of group i+1 load during the softmax and P·V of group i; values
-      // of group i+1 during its QK.  One commit group per part, in order.
+      // keys of group i+1 load during the P·V of group i, values of group
+      // i+1 during its QK: one bulk copy and one mbarrier per part.
       W.issue_k(u, g0);
-      asm volatile("cp.async.commit_group;\n" ::);
       W.issue_v(u, g0);
-      asm volatile("cp.async.commit_group;\n" ::);
       for (int gi = g0; gi < g1; ++gi) {
         const bool more = gi + 1 < g1;
-        asm volatile("cp.async.wait_group 1;\n" ::);   // keys of gi
-        __syncwarp();
+        if (!W.wait_part(W.mb_k, W.ph_k)) {   // keys of gi (bounded wait)
+          W.wait_part(W.mb_v, W.ph_v);        // the value copy in flight
+          return;
+        }
         float S[8][4], alpha[2];
         W.qk_softmax(S, alpha);
-        __syncwarp();                                  // key part consumed
+        __syncwarp();                          // key part consumed
         if (more) W.issue_k(u, gi + 1);
-        asm volatile("cp.async.commit_group;\n" ::);
-        asm volatile("cp.async.wait_group 1;\n" ::);   // values of gi
-        __syncwarp();
+        if (!W.wait_part(W.mb_v, W.ph_v)) {   // values of gi
+          if (more) W.wait_part(W.mb_k, W.ph_k);
+          return;
+        }
         W.pv(S, alpha);
-        __syncwarp();                                  // value part consumed
+        __syncwarp();                          // value part consumed
         if (more) W.issue_v(u, gi + 1);
-        asm volatile("cp.async.commit_group;\n" ::);
       }
-      asm volatile("cp.async.wait_group 0;\n" ::);
-      __syncwarp();
     }
     if (res) W.window(u, a.res_k, a.res_v, a.r, kR);
     if (snk) W.window(u, a.sink_k, a.sink_v, a.s, a.n_sink);
@@ -1095,6 +1144,7 @@ cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, flo
   a.max_parts = plan.max_parts;
   a.total = static_cast<long long>(a.units) * a.unit_len;
   a.ws = ws;
+  a.status = c->status;
   const int nrep = Hq / c->cfg.kv_heads;
   const int kb = c->cfg.k_bits, vb = c->cfg.v_bits;
   const int warps = mma_warps_per_cta(c->lay.bytes);

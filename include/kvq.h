@@ -73,7 +73,9 @@ enum {
 /* Sticky device status flags (OR-ed), read by kvq_cache_status. */
 enum {
   KVQ_FLAG_NONFINITE = 1,     /* a group held a NaN or infinity             */
-  KVQ_FLAG_RANGE = 2          /* (max - min)/(2^b - 1) not positive finite  */
+  KVQ_FLAG_RANGE = 2,         /* (max - min)/(2^b - 1) not positive finite  */
+  KVQ_FLAG_TIMEOUT = 4        /* a decode wait for staged data gave up; that
+                                 call's output is invalid                   */
 };
 
 /* Key storage mode. */
