@@ -977,37 +977,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) decode_mma_kernel(MmaArgs a
   }
 }
 
-// Block-wide reductions of the combine kernel (128 threads).
-__device__ __forceinline__ float block_max128(float x, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
-  __syncthreads();
-  x = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  __syncthreads();
-  return x;
-}
-__device__ __forceinline__ float block_sum128(float x, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
-  __syncthreads();
-  x = (red[0] + red[1]) + (red[2] + red[3]);
-  __syncthreads();
-  return x;
-}
-
 // Merge the partials (o, m, l) of one query head (block = (b, hq), thread =
 // channel) with the log-sum-exp rule: M = max m_k, w_k = 2^(m_k - M),
-// o = sum w_k o_k / sum w_k l_k.  Launched as a programmatic dependent of
-// the decode kernel: it may start while that kernel drains and waits for
+// o = sum w_k o_k / sum w_k l_k.  Every warp takes the weights itself (lane
+// k % 32 holds part k's), so no block barrier is needed, and the values of
+// the first 16 parts load together with the maxima: for up to 16 parts the
+// merge is one round trip to memory.  Launched as a programmatic dependent
+// of the decode kernel: it may start while that kernel drains and waits for
 // its results with griddepcontrol.wait.
 __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restrict__ ws,
                                                            int Hkv, int Hq, int max_parts,
                                                            long long unit_len, long long total,
                                                            int n_slots, float* __restrict__ out) {
-  extern __shared__ float wk[];   // [parts] weights
-  __shared__ float red[4];
+  constexpr int kEarly = 16;
   const int row = blockIdx.x;                 // b * Hq + hq
   const int n_rep = Hq / Hkv;
   const int b = row / Hq, hq = row % Hq;
@@ -1016,28 +998,41 @@ __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restr
   const int first = static_cast<int>(((ub + 1) * n_slots - 1) / total);
   const int last = static_cast<int>(((ub + unit_len) * n_slots - 1) / total);
   const int n = last - first + 1;
+  const int c = threadIdx.x, lane = c & 31;
   const float* base = ws + static_cast<long long>(u) * max_parts * n_rep * (kD + 2) + h * (kD + 2);
   const long long stride = static_cast<long long>(n_rep) * (kD + 2);
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  float M = -INFINITY;
-  for (int k = threadIdx.x; k < n; k += 128) M = fmaxf(M, base[k * stride + kD]);
-  M = block_max128(M, red);
-  float ls = 0.0f;
-  for (int k = threadIdx.x; k < n; k += 128) {
-    const float mk = base[k * stride + kD];
-    const float w = mk == -INFINITY ? 0.0f : exp2f(mk - M);
-    wk[k] = w;
-    ls = fmaf(w, base[k * stride + kD + 1], ls);
-  }
-  const float l = block_sum128(ls, red);   // its barriers also publish wk
-  float o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  int k = 0;
-  for (; k + 4 <= n; k += 4) {
+  float o[kEarly];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = fmaf(wk[k + i], base[(k + i) * stride + threadIdx.x], o[i]);
+  for (int j = 0; j < kEarly; ++j) o[j] = j < n ? base[j * stride + c] : 0.0f;
+  const float m0 = lane < n ? base[lane * stride + kD] : -INFINITY;
+  const float l0 = lane < n ? base[lane * stride + kD + 1] : 0.0f;
+  float M = m0;
+  for (int k = lane + 32; k < n; k += 32) M = fmaxf(M, base[k * stride + kD]);
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
+  // parts 0..31: weights from lane k; a part that saw no token weighs 0
+  float w = m0 == -INFINITY ? 0.0f : exp2f(m0 - M);
+  float L = w * l0, O = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kEarly; ++j) O = fmaf(__shfl_sync(kFull, w, j), o[j], O);
+  const int n32 = min(n, 32);
+#pragma unroll 4
+  for (int j = kEarly; j < n32; ++j) O = fmaf(__shfl_sync(kFull, w, j), base[j * stride + c], O);
+  // parts 32 and up, 32 at a time
+  for (int k0 = 32; k0 < n; k0 += 32) {
+    const int k = k0 + lane;
+    const float mk = k < n ? base[k * stride + kD] : -INFINITY;
+    w = mk == -INFINITY ? 0.0f : exp2f(mk - M);
+    L = fmaf(w, k < n ? base[k * stride + kD + 1] : 0.0f, L);
+    const int cnt = min(32, n - k0);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j)
+      O = fmaf(__shfl_sync(kFull, w, j), base[(k0 + j) * stride + c], O);
   }
-  for (; k < n; ++k) o[0] = fmaf(wk[k], base[k * stride + threadIdx.x], o[0]);
-  out[static_cast<long long>(row) * kD + threadIdx.x] = ((o[0] + o[1]) + (o[2] + o[3])) / l;
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) L += __shfl_xor_sync(kFull, L, x);
+  out[static_cast<long long>(row) * kD + c] = O / L;
 }
 
 template <int KB, int VB, int NREP, bool MIX>
@@ -1109,7 +1104,7 @@ cudaError_t launch_combine_parts(const float* ws, int B, int Hkv, int Hq, int ma
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(B * Hq);
   lc.blockDim = dim3(kD);
-  lc.dynamicSmemBytes = static_cast<size_t>(max_parts) * sizeof(float);
+  lc.dynamicSmemBytes = 0;
   lc.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

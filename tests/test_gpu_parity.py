@@ -139,6 +139,55 @@ def test_decode_repeatable_and_workspace_reuse():
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("B,Hkv,n_rep,T_q,r", [
+    (4, 8, 4, 1024, 50),    # 32 units of 9 items: a few partials a unit
+    (1, 1, 4, 8192, 3),     # one unit of 65 items: 65 partials to merge
+])
+def test_decode_merge_of_partials(B, Hkv, n_rep, T_q, r):
+    w = small(B, Hkv, n_rep, T_q, r, seed=41)
+    units = None if B * Hkv <= 4 else [0, 13, 31]
+    cache, ref, q = run_case(w, units=units)
+    assert_attention_close(cache.attention(q.cuda()), ref.attention(q), f"merge {w}")
+
+
+def test_decode_workspace_needs_no_initial_contents():
+    """Any prior workspace contents (here all bytes 0xff, then 0x00) give
+    the same result: every partial the merge reads is written by the call."""
+    w = small(4, 8, 4, 1024, 50, seed=42)
+    cache, ref, q = run_case(w, units=[0, 31])
+    want = ref.attention(q)
+    for fill in (0xFF, 0x00, 0xFF):
+        ws = cache.workspace(w.Hq)
+        ws.fill_(fill)
+        assert_attention_close(cache.attention(q.cuda(), workspace=ws), want, f"fill {fill:#x}")
+
+
+def test_decode_replayed_as_a_cuda_graph():
+    """A captured decode (decode kernel and its programmatic-dependent
+    combine) replays correctly with new queries in the captured buffer."""
+    w = small(4, 8, 4, 1024, 50, seed=43)
+    cache, ref, _ = run_case(w, units=[0, 5, 31])
+    qs = [make_q(w, step=i) for i in range(3)]
+    q_dev = qs[0].cuda()
+    out = torch.empty(w.B, w.Hq, 128, dtype=torch.float32, device="cuda")
+    ws = cache.workspace(w.Hq)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        cache.attention(q_dev, out=out, workspace=ws)   # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cache.attention(q_dev, out=out, workspace=ws)
+    for i in (1, 2, 0, 1):
+        q_dev.copy_(qs[i].cuda())
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_attention_close(out, ref.attention(qs[i]), f"replay q{i}")
+
+
 # ----------------------------------------------------- the named workloads
 def test_tiny_single_head_workload():
     w = WORKLOADS["tiny_1head_1k"]
