@@ -20,9 +20,11 @@
 // Scores need more than f16's 11 bits of Q' (a large score's error is its
 // size times the operand rounding), so Q' is split into an f16 high part
 // and an f16 low part (the rounding error of the high part), ~22 bits in
-// all: with at most 4 query heads per KV head the low part rides in the 4
-// otherwise unused B columns (lanes of columns 4-7 hold head column - 4) and
-// one shuffle adds it back; with 8 heads a second MMA per k-step adds it.
+// all: with at most 4 query heads per KV head, B column 2h holds head h's
+// high part and column 2h + 1 its low part, so a lane's two accumulator
+// columns are one head and one add merges them (the softmax then runs once
+// per score, on lane (g, t) for head t); with 8 heads a second MMA per
+// k-step adds the low part.
 //
 // Work split ("stream-K"): the flattened sequence of items (for each unit
 // its groups, then its residual window and its attention-sink window, one
@@ -161,7 +163,7 @@ __device__ __forceinline__ int slot_of(const MmaArgs& a, long long p) {
 
 template <int KB, int VB, int NREP, bool MIX>
 struct Warp {
-  static constexpr bool SPARE = NREP <= 4;  // Q' low part in columns 4-7;
+  static constexpr bool SPARE = NREP <= 4;  // Q' low part in odd columns;
                                             // query kept as pre-scaled fp32
   static constexpr int NL = SPARE ? 1 : 8;  // low-part fragments kept
 
@@ -213,6 +215,15 @@ struct Warp {
     return static_cast<uint8_t*>(qs) + (SPARE ? kD * 4 : kD * 2);
   }
 
+  // Query head of the B column this lane builds (column g): with at most 4
+  // heads, column 2h holds head h's high part and column 2h + 1 its low
+  // part; with 8 heads column g is head g.
+  __device__ __forceinline__ int hrow() const { return SPARE ? (g >> 1) : g; }
+  __device__ __forceinline__ bool low_col() const { return SPARE && (g & 1); }
+  // Lane of this lane's quad holding head hh's scores (one head per lane,
+  // at most 4 heads): lane (g, hh & 3).
+  __device__ __forceinline__ int head_lane(int hh) const { return (lane & ~3) | (hh & 3); }
+
   // x rounded to 11 significant bits (an f16 value for the normalized
   // range used here); x - result is exact in fp32
   __device__ __forceinline__ static float round_f16_precision(float x) {
@@ -229,7 +240,7 @@ struct Warp {
   __device__ __forceinline__ void begin_unit(int u) {
     const int b = u / a.Hkv, kvh = u % a.Hkv;
     const uint16_t* qg = a.q + (static_cast<long long>(b) * a.Hq + kvh * NREP) * kD;
-    if (MIX) qg_row = qg + min(g, NREP - 1) * kD;
+    if (MIX) qg_row = qg + min(hrow(), NREP - 1) * kD;
     const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
     __syncwarp();
     if (SPARE) {   // fp32 [4][kQRow], pre-scaled
@@ -246,10 +257,10 @@ struct Warp {
       }
     }
     __syncwarp();
-    if (MIX) {   // max |q| of the row: fp32 pre-scaled row g & 3, or bf16 row g
+    if (MIX) {   // max |q| of this lane's head row (fp32 pre-scaled, or bf16)
       float mx = 0.0f;
       for (int c = t; c < kD; c += 4)
-        mx = fmaxf(mx, SPARE ? fabsf(static_cast<const float*>(qs)[(g & 3) * kQRow + c])
+        mx = fmaxf(mx, SPARE ? fabsf(static_cast<const float*>(qs)[hrow() * kQRow + c])
                              : fabsf(bf2f(static_cast<const uint16_t*>(qs)[g * kQRow + c])));
       mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
       qmax = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
@@ -304,11 +315,12 @@ struct Warp {
     float hinv[2], hbias[2];
     if constexpr (MIX) scores_mixed(S, hinv, hbias);
     else scores_uniform(S, hinv, hbias);
-    if (SPARE) {   // columns c and c + 4 hold the high and low parts of one head
+    if (SPARE) {   // columns 2t and 2t + 1: the high and low parts of head t
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) S[mt][c] += __shfl_xor_sync(kFull, S[mt][c], 2);
+      for (int mt = 0; mt < 8; ++mt) {
+        S[mt][0] += S[mt][1];
+        S[mt][2] += S[mt][3];
+      }
     }
     softmax_update(S, hinv, hbias, alpha);
   }
@@ -330,7 +342,7 @@ struct Warp {
       const uint32_t m89 = kmin2[8 * ks + t + 4];
       float qa, qb, qc, qd;
       if (SPARE) {   // rows h >= NREP of the stored query are zero
-        const float* qrow = static_cast<const float*>(qs) + (g & 3) * kQRow;
+        const float* qrow = static_cast<const float*>(qs) + hrow() * kQRow;
         const float2 q01 = *reinterpret_cast<const float2*>(qrow + 16 * ks + 2 * t);
         const float2 q89 = *reinterpret_cast<const float2*>(qrow + 16 * ks + 2 * t + 8);
         qa = q01.x; qb = q01.y; qc = q89.x; qd = q89.y;
@@ -362,7 +374,7 @@ struct Warp {
     // high part: B' rounded to f16 precision, low part: the rest
     uint32_t bq[8][2], bl[NL][2];
     {
-      const bool low_lane = SPARE && g >= 4;
+      const bool low_lane = low_col();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const float f0 = sq * row_factor<KB>(ks, 0), f1 = sq * row_factor<KB>(ks, 1);
@@ -387,11 +399,11 @@ struct Warp {
         }
       }
     }
-    // per head of this lane's C columns: the score unit and bias from that
-    // head's lanes
+    // per head of this lane's C columns: the score unit and bias from the
+    // lane that built that head's (high) B column
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int src = 4 * (SPARE ? ((2 * t + h) & 3) : (2 * t + h));
+      const int src = SPARE ? 8 * t : 4 * (2 * t + h);
       hinv[h] = __shfl_sync(kFull, inv_sq, src) * kCodeUnit;
       hbias[h] = __shfl_sync(kFull, bias, src);
     }
@@ -501,7 +513,7 @@ struct Warp {
           const int i = 16 * k16 + 2 * t + (e & 1) + 8 * (e >> 1);
           // exact bf16 query: the staged copy (8 heads) or global memory
           // (with at most 4 heads the staged copy is pre-scaled fp32)
-          qb[e] = (i < nb && g < NREP)
+          qb[e] = (i < nb && !low_col() && hrow() < NREP)
                       ? static_cast<uint32_t>(SPARE ? __ldg(qg_row + perm[i])
                                                     : static_cast<const uint16_t*>(qs)[g * kQRow + perm[i]])
                       : 0u;
@@ -520,7 +532,7 @@ struct Warp {
       float rr[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int src = 4 * (SPARE ? ((2 * t + h) & 3) : (2 * t + h));
+        const int src = SPARE ? 8 * t : 4 * (2 * t + h);
         rr[h] = c0 * __shfl_sync(kFull, sq, src) * kInvCodeUnit;
       }
 #pragma unroll
@@ -531,7 +543,7 @@ struct Warp {
 
     // ---- UINT4 and UINT2 tiers: virtual 2-bit channels
     const uint32_t* kcw = reinterpret_cast<const uint32_t*>(kbuf + L.kc);
-    const bool low_lane = SPARE && g >= 4;
+    const bool low_lane = low_col();
     float bias = 0.0f;
     for (int w = 0; w < kw2; ++w) {
       uint32_t kx[8], ky[8];
@@ -551,7 +563,7 @@ struct Warp {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int ch = static_cast<int>(em[i] >> 16);
-          const float qv = SPARE ? static_cast<const float*>(qs)[(g & 3) * kQRow + ch]
+          const float qv = SPARE ? static_cast<const float*>(qs)[hrow() * kQRow + ch]
                                  : bf2f(static_cast<const uint16_t*>(qs)[g * kQRow + ch]);
           bias = fmaf(qv, bf2f(em[i] & 0xffffu), bias);
           x[i] = qv * __uint_as_float(es[i]) * sq;
@@ -585,40 +597,65 @@ struct Warp {
     if (!SPARE) bias *= c0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int src = 4 * (SPARE ? ((2 * t + h) & 3) : (2 * t + h));
+      const int src = SPARE ? 8 * t : 4 * (2 * t + h);
       hinv[h] = __shfl_sync(kFull, inv_sq, src) * kCodeUnit;
       hbias[h] = __shfl_sync(kFull, bias, src);
     }
   }
 
-  // One online-softmax step over 128 scores in C layout (rows = tokens,
-  // columns 2t, 2t+1 = this lane's heads): score = acc * hinv + off in log2
-  // units with hinv > 0, so the max is taken on the raw accumulators and
-  // p = 2^(acc * hinv + off - m) is one FMA and one ex2.  Returns p in S and
-  // the factors that rescale the earlier state.
+  // One online-softmax step over 128 scores in C layout (rows = tokens):
+  // score = acc * hinv + off in log2 units with hinv > 0, so the max is taken
+  // on the raw accumulators and p = 2^(acc * hinv + off - m) is one FMA and
+  // one ex2.  With at most 4 heads lane (g, t) holds head t in columns 0 and
+  // 2 (rows g, g + 8; the state is in mrun[0], lrun[0]), else heads 2t,
+  // 2t + 1 in columns (0, 2) and (1, 3).  Returns p in S and the factors
+  // that rescale the earlier state of heads 2t, 2t + 1 (the output's columns).
   __device__ __forceinline__ void softmax_update(float (&S)[8][4], const float (&hinv)[2],
                                                  const float (&hoff)[2], float (&alpha)[2]) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float off = hoff[h];
+    if constexpr (SPARE) {
       float m = -INFINITY;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) m = fmaxf(m, fmaxf(S[mt][h], S[mt][h + 2]));
+      for (int mt = 0; mt < 8; ++mt) m = fmaxf(m, fmaxf(S[mt][0], S[mt][2]));
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 16));
-      const float m_new = fmaxf(mrun[h], fmaf(m, hinv[h], off));
-      alpha[h] = ex2(mrun[h] - m_new);
-      mrun[h] = m_new;
-      const float shift = off - m_new;
+      const float m_new = fmaxf(mrun[0], fmaf(m, hinv[0], hoff[0]));
+      const float al = ex2(mrun[0] - m_new);
+      mrun[0] = m_new;
+      const float shift = hoff[0] - m_new;
       float ls = 0.0f;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        S[mt][h] = ex2(fmaf(S[mt][h], hinv[h], shift));
-        S[mt][h + 2] = ex2(fmaf(S[mt][h + 2], hinv[h], shift));
-        ls += S[mt][h] + S[mt][h + 2];
+        S[mt][0] = ex2(fmaf(S[mt][0], hinv[0], shift));
+        S[mt][2] = ex2(fmaf(S[mt][2], hinv[0], shift));
+        ls += S[mt][0] + S[mt][2];
       }
-      lrun[h] = fmaf(lrun[h], alpha[h], ls);
+      lrun[0] = fmaf(lrun[0], al, ls);
+      alpha[0] = __shfl_sync(kFull, al, head_lane(2 * t));
+      alpha[1] = __shfl_sync(kFull, al, head_lane(2 * t + 1));
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float off = hoff[h];
+        float m = -INFINITY;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) m = fmaxf(m, fmaxf(S[mt][h], S[mt][h + 2]));
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 16));
+        const float m_new = fmaxf(mrun[h], fmaf(m, hinv[h], off));
+        alpha[h] = ex2(mrun[h] - m_new);
+        mrun[h] = m_new;
+        const float shift = off - m_new;
+        float ls = 0.0f;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          S[mt][h] = ex2(fmaf(S[mt][h], hinv[h], shift));
+          S[mt][h + 2] = ex2(fmaf(S[mt][h + 2], hinv[h], shift));
+          ls += S[mt][h] + S[mt][h + 2];
+        }
+        lrun[h] = fmaf(lrun[h], alpha[h], ls);
+      }
     }
   }
 
@@ -693,8 +730,16 @@ struct Warp {
     float Dvm[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int kt = 0; kt < 8; ++kt) {
-      pb[kt][0] = movmatrix_t(pack_h2(S[kt][0], S[kt][1]));
-      pb[kt][1] = movmatrix_t(pack_h2(S[kt][2], S[kt][3]));
+      if constexpr (SPARE) {   // rows g, g + 8 of heads 2t, 2t + 1 from their lanes
+        const uint32_t pk = pack_h2(S[kt][0], S[kt][2]);
+        const uint32_t x0 = __shfl_sync(kFull, pk, head_lane(2 * t));
+        const uint32_t x1 = __shfl_sync(kFull, pk, head_lane(2 * t + 1));
+        pb[kt][0] = movmatrix_t(__byte_perm(x0, x1, 0x5410));
+        pb[kt][1] = movmatrix_t(__byte_perm(x0, x1, 0x7632));
+      } else {
+        pb[kt][0] = movmatrix_t(pack_h2(S[kt][0], S[kt][1]));
+        pb[kt][1] = movmatrix_t(pack_h2(S[kt][2], S[kt][3]));
+      }
       const uint2 av = *reinterpret_cast<const uint2*>(vmb + vmb_index(kt, g & 3, t, 0));
       const uint32_t a0 = g < 4 ? av.x : 0u, a2 = g < 4 ? av.y : 0u;
       mma_f16(Dvm, a0, 0u, a2, 0u, pb[kt][0], pb[kt][1]);
@@ -784,16 +829,18 @@ struct Warp {
     const int r = count, nc = (r + 15) >> 4;
     const uint8_t* kr = reinterpret_cast<const uint8_t*>(kbase + static_cast<long long>(u) * cap * kD);
     const uint8_t* vr = reinterpret_cast<const uint8_t*>(vbase + static_cast<long long>(u) * cap * kD);
-    // query B fragments: column g = head g (zero for g >= NREP)
+    // query B fragments: the high-part columns of the code path hold the
+    // exact query (column 2h with at most 4 heads, else g), the others zero
     uint32_t bqr[8][2];
     {
       const int b = u / a.Hkv, kvh = u % a.Hkv;
+      const bool on = !low_col() && hrow() < NREP;
       const uint32_t* qg = reinterpret_cast<const uint32_t*>(
-          a.q + (static_cast<long long>(b) * a.Hq + kvh * NREP + min(g, NREP - 1)) * kD);
+          a.q + (static_cast<long long>(b) * a.Hq + kvh * NREP + min(hrow(), NREP - 1)) * kD);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        bqr[ks][0] = g < NREP ? __ldg(qg + 8 * ks + t) : 0u;
-        bqr[ks][1] = g < NREP ? __ldg(qg + 8 * ks + t + 4) : 0u;
+        bqr[ks][0] = on ? __ldg(qg + 8 * ks + t) : 0u;
+        bqr[ks][1] = on ? __ldg(qg + 8 * ks + t + 4) : 0u;
       }
     }
     __syncwarp();
@@ -852,7 +899,10 @@ struct Warp {
         uint32_t ph[2], pl[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          const float p0 = S[c][2 * i], p1 = S[c][2 * i + 1];
+          // row g (i = 0) or g + 8 (i = 1) of heads 2t, 2t + 1
+          const float p0 = SPARE ? __shfl_sync(kFull, S[c][2 * i], head_lane(2 * t)) : S[c][2 * i];
+          const float p1 = SPARE ? __shfl_sync(kFull, S[c][2 * i], head_lane(2 * t + 1))
+                                 : S[c][2 * i + 1];
           const uint32_t hi = pack_bf2(p0, p1);
           const float l0 = p0 - __uint_as_float(hi << 16);
           const float l1 = p1 - __uint_as_float(hi & 0xffff0000u);
@@ -890,7 +940,7 @@ struct Warp {
   __device__ __forceinline__ void finish(int u, int part) {
     float l[2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < (SPARE ? 1 : 2); ++h) {
       float x = lrun[h];
       x += __shfl_xor_sync(kFull, x, 4);
       x += __shfl_xor_sync(kFull, x, 8);
@@ -914,14 +964,17 @@ struct Warp {
         }
       }
     }
-    if (g == 0) {
+    if (SPARE) {   // lane (0, t): head t
+      if (g == 0 && t < NREP) {
+        base[t * (kD + 2) + kD] = mrun[0];
+        base[t * (kD + 2) + kD + 1] = l[0];
+      }
+    } else if (g == 0) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int hh = 2 * t + h;
-        if (hh < NREP) {
-          base[hh * (kD + 2) + kD] = mrun[h];
-          base[hh * (kD + 2) + kD + 1] = l[h];
-        }
+        base[hh * (kD + 2) + kD] = mrun[h];
+        base[hh * (kD + 2) + kD + 1] = l[h];
       }
     }
   }
