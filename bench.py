@@ -43,13 +43,13 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_mma_kernel
 # launch, from the ncu capture of this workload at batch 8 kept under
 # profiles/, keyed by the sha256 of the decode kernel source it was taken on
-# (a stale entry reports null).  The capture
-# ran at batch 8 (64 units, 32768 + 100 tokens): 200.96 MB read + 3.67 MB
-# written; traffic per unit is independent of the batch, so the batch-16
-# launch is twice that, scaled to the timed steps' mean context (399.3 MB of
-# algorithmic bytes per launch against 401.2 MB at the captured context).
+# (a stale entry reports null).  The capture ran at batch 8 (64 units,
+# 32768 + 100 tokens): 200.963 MB read + 3.282 MB written against 200.884 MB
+# of algorithmic bytes (ratio 1.0167: mostly the split-K partials written).
+# Traffic per unit is independent of the batch, so the batch-16 launch is
+# that ratio times its algorithmic bytes at the timed steps' mean context.
 NCU_TRAFFIC = {
-    "95190e9d4fa5e176": {("llama8b_gqa_32k_b16", 16, 32768, 2): 2 * 204.633344e6 * 399.3 / 401.2},
+    "cfff8f26d15dd5ea": {("llama8b_gqa_32k_b16", 16, 32768, 2): 204.244992 / 200.884224 * 399.264512e6},
 }
 
 
