@@ -75,6 +75,9 @@ def lib() -> ctypes.CDLL:
             "orc_salience": (None, [P, P, i, P]),
             "orc_tiers_rank": (i, [P, i, i, i, P]),
             "orc_tiers_threshold": (i, [P, i, f, f, P]),
+            "orc_tiers_capped": (i, [P, i, f, f, i, i, P]),
+            "orc_observe_query": (i, [P, P, i, i]),
+            "orc_importance_from_sum": (i, [P, i, i, i, P]),
             "orc_quantize_k_mixed_group": (i, [P, i, i, P, P, P, P, P, P, P, P, P]),
             "orc_dequant_k_mixed_group": (None, [i, i, P, i, i, P, P, P, P, P, P, P, P]),
             "orc_cache_bytes": (d, [l, l, l, i, i, i, i, i, i, i, i]),
@@ -195,6 +198,34 @@ def tiers_threshold(A: np.ndarray, tau_bf16: float, tau_uint4: float) -> np.ndar
     return out
 
 
+def tiers_capped(A: np.ndarray, tau_bf16: float, tau_uint4: float, cap_bf16: int,
+                 cap_uint4: int) -> np.ndarray:
+    """Threshold tiers with at most cap_bf16 BF16 and cap_uint4 UINT4
+    channels, taken from the largest A down (kvq_oracle.c orc_tiers_capped)."""
+    A = np.ascontiguousarray(A, np.float32)
+    out = np.zeros(A.size, np.uint8)
+    _check(lib().orc_tiers_capped(_p(A), A.size, tau_bf16, tau_uint4, cap_bf16, cap_uint4,
+                                  _p(out)), "tiers_capped")
+    return out
+
+
+def observe_query(acc: np.ndarray, q_step: np.ndarray) -> None:
+    """acc fp32 [D] += |q| of each head row of q_step (bf16 bits [n_rep, D]),
+    heads in order (MixKVQ online saliency accumulator)."""
+    q_step = np.ascontiguousarray(q_step, np.uint16)
+    assert acc.dtype == np.float32 and acc.flags["C_CONTIGUOUS"]
+    n_rep, D = q_step.shape
+    _check(lib().orc_observe_query(_p(acc), _p(q_step), n_rep, D), "observe_query")
+
+
+def importance_from_sum(acc: np.ndarray, n_rep: int, steps: int) -> np.ndarray:
+    acc = np.ascontiguousarray(acc, np.float32)
+    out = np.zeros(acc.size, np.float32)
+    _check(lib().orc_importance_from_sum(_p(acc), n_rep, steps, acc.size, _p(out)),
+           "importance_from_sum")
+    return out
+
+
 def cache_bytes(T, rK, rV, D, k_bits, v_bits, Gk, Gv, origin_bytes, step_bytes,
                 float_bytes) -> float:
     return lib().orc_cache_bytes(T, rK, rV, D, k_bits, v_bits, Gk, Gv,
@@ -294,7 +325,15 @@ class OracleCache:
 
     mode "uniform": K k_bits per channel over Gk tokens; V v_bits per token
     over Gv channels.  mode "mixed": K tiers per flushed group from
-    A = I * S (S at sal_bits) by rank (n_bf16, n_uint4), V as in uniform.
+    A = I * S (S at sal_bits), V as in uniform; tier_mode "rank" takes the
+    n_bf16 largest A as BF16 and the next n_uint4 as UINT4, tier_mode
+    "threshold" applies tau_bf16 / tau_uint4 with n_bf16 / n_uint4 as the
+    group's capacities (tiers_capped).
+
+    Online saliency (MixKVQ "efficient online salience estimation"): observe
+    adds each decode step's |q| to a running sum per (unit, channel); a mixed
+    flush given no importance takes I_d = sum / (n_rep * steps) over the
+    steps observed since the previous flush, then starts a new window.
 
     n_sink > 0: the first n_sink tokens of the sequence are attention sinks
     kept in bf16 and never quantized (PN-Mix "sink 原精度保护", N_s = 32;
@@ -304,13 +343,20 @@ class OracleCache:
     """
 
     def __init__(self, B, Hkv, D, k_bits=2, v_bits=2, Gk=128, Gv=32, R=128,
-                 mode="uniform", n_bf16=0, n_uint4=0, sal_bits=2, n_sink=0):
+                 mode="uniform", n_bf16=0, n_uint4=0, sal_bits=2, n_sink=0,
+                 tier_mode="rank", tau_bf16=0.0, tau_uint4=0.0):
         if R % Gk:
             raise ValueError("R must be a multiple of the key group")
         self.B, self.Hkv, self.D = B, Hkv, D
         self.k_bits, self.v_bits, self.Gk, self.Gv, self.R = k_bits, v_bits, Gk, Gv, R
         self.mode, self.n_bf16, self.n_uint4, self.sal_bits = mode, n_bf16, n_uint4, sal_bits
+        if tier_mode not in ("rank", "threshold"):
+            raise ValueError("tier_mode is 'rank' or 'threshold'")
+        self.tier_mode, self.tau_bf16, self.tau_uint4 = tier_mode, tau_bf16, tau_uint4
         U = B * Hkv
+        self.qacc = np.zeros((U, D), np.float32)   # online |q| sums of the window
+        self.q_steps = 0
+        self.q_rep = 0
         self.k_groups = [[] for _ in range(U)]   # uniform: (codes, kmin, kscale) per group
         self.v_parts = [[] for _ in range(U)]    # (codes, vmin, vscale) per token block
         self.res_k = np.zeros((U, R, D), np.uint16)
@@ -359,10 +405,36 @@ class OracleCache:
         self.res_v[:, self.r] = v_new.reshape(-1, self.D)
         self.r += 1
 
+    # -- online saliency: one decode step's query (bf16 bits [B, Hq, D])
+    def observe(self, q: np.ndarray):
+        B, Hq, D = q.shape
+        if B != self.B or D != self.D or Hq % self.Hkv:
+            raise ValueError("query shape does not match the cache")
+        n_rep = Hq // self.Hkv
+        if self.q_steps and n_rep != self.q_rep:
+            raise ValueError("query heads changed within a window")
+        for u in range(self.B * self.Hkv):
+            b, h = divmod(u, self.Hkv)
+            observe_query(self.qacc[u], q[b, h * n_rep:(h + 1) * n_rep])
+        self.q_rep = n_rep
+        self.q_steps += 1
+
+    def window_importance(self) -> np.ndarray:
+        """I [B, Hkv, D] of the queries observed since the last flush."""
+        if self.q_steps == 0:
+            raise ValueError("no query observed in this window")
+        I = np.stack([importance_from_sum(self.qacc[u], self.q_rep, self.q_steps)
+                      for u in range(self.B * self.Hkv)])
+        return I.reshape(self.B, self.Hkv, self.D)
+
     # -- Algorithm 1, Decoding: when len == R, quantize K and V, empty residual
     def flush(self, importance: np.ndarray | None = None):
         if self.r != self.R:
             raise ValueError("flush needs a full residual")
+        if self.mode == "mixed" and importance is None:   # the online window
+            importance = self.window_importance()
+            self.qacc[:] = 0.0
+            self.q_steps = 0
         for u in range(self.B * self.Hkv):
             b, h = divmod(u, self.Hkv)
             self._flush_block(u, self.res_k[u], self.res_v[u],
@@ -378,7 +450,11 @@ class OracleCache:
             else:
                 S = sensitivity(kg, self.sal_bits)
                 A = salience(np.asarray(imp, np.float32), S)
-                tiers = tiers_rank(A, self.n_bf16, self.n_uint4)
+                if self.tier_mode == "rank":
+                    tiers = tiers_rank(A, self.n_bf16, self.n_uint4)
+                else:
+                    tiers = tiers_capped(A, self.tau_bf16, self.tau_uint4, self.n_bf16,
+                                         self.n_uint4)
                 self.k_groups[u].append(quantize_k_mixed_group(kg, tiers))
         self.v_parts[u].append(quantize_v_unit(vb, self.Gv, self.v_bits))
 

@@ -351,6 +351,73 @@ int orc_tiers_threshold(const float* A, int D, float tau_bf16, float tau_uint4,
 }
 
 /*
+ * [MixKVQ] threshold tiers in a key record of fixed capacity (at most
+ * cap_bf16 BF16 and cap_uint4 UINT4 channels a group).  Channels are taken
+ * from the largest A_d down (ties: lower index first); each one is BF16 if
+ * A_d > tau_bf16 and fewer than cap_bf16 channels are BF16 so far, else
+ * UINT4 if A_d > tau_uint4 and fewer than cap_uint4 are UINT4, else UINT2.
+ * With both caps = D this is the plain threshold rule; with both thresholds
+ * at -infinity it is the rank rule with counts cap_bf16, cap_uint4.
+ */
+int orc_tiers_capped(const float* A, int D, float tau_bf16, float tau_uint4,
+                     int cap_bf16, int cap_uint4, uint8_t* tiers) {
+  if (D <= 0 || cap_bf16 < 0 || cap_uint4 < 0) return ORC_ERR_ARG;
+  for (int d = 0; d < D; ++d)
+    if (!isfinite(A[d])) return ORC_ERR_NONFINITE;
+  uint8_t* taken = (uint8_t*)calloc((size_t)D, 1);
+  int nb = 0, n4 = 0;
+  for (int k = 0; k < D; ++k) {
+    int best = -1;
+    for (int d = 0; d < D; ++d) {
+      if (taken[d]) continue;
+      if (best < 0 || A[d] > A[best]) best = d;  /* strict: lower d wins ties */
+    }
+    taken[best] = 1;
+    if (A[best] > tau_bf16 && nb < cap_bf16) {
+      tiers[best] = ORC_TIER_BF16;
+      ++nb;
+    } else if (A[best] > tau_uint4 && n4 < cap_uint4) {
+      tiers[best] = ORC_TIER_UINT4;
+      ++n4;
+    } else {
+      tiers[best] = ORC_TIER_UINT2;
+    }
+  }
+  free(taken);
+  return ORC_OK;
+}
+
+/*
+ * [MixKVQ] online saliency estimation: the cache keeps a running fp32 sum
+ * of query magnitudes per key channel, and every decode step adds the
+ * current query token's |q| of each head of the KV group, heads in order
+ * (q_step: n_rep rows of D bf16).  Summed over the steps of a window this is
+ * the importance sum of orc_importance in the same order (token, then head).
+ */
+int orc_observe_query(float* acc, const uint16_t* q_step, int n_rep, int D) {
+  if (n_rep <= 0 || D <= 0) return ORC_ERR_ARG;
+  for (int h = 0; h < n_rep; ++h)
+    for (int d = 0; d < D; ++d)
+      if (!isfinite(orc_bf16_to_f32(q_step[(long)h * D + d]))) return ORC_ERR_NONFINITE;
+  for (int d = 0; d < D; ++d) {
+    volatile float a = acc[d];
+    for (int h = 0; h < n_rep; ++h) a = a + fabsf(orc_bf16_to_f32(q_step[(long)h * D + d]));
+    acc[d] = a;
+  }
+  return ORC_OK;
+}
+
+/* I_d of the window the accumulator covers: acc_d / (n_rep * steps). */
+int orc_importance_from_sum(const float* acc, int n_rep, int steps, int D, float* I) {
+  if (n_rep <= 0 || steps <= 0 || D <= 0) return ORC_ERR_ARG;
+  for (int d = 0; d < D; ++d) {
+    volatile float count = (float)(n_rep * steps);
+    I[d] = acc[d] / count;
+  }
+  return ORC_OK;
+}
+
+/*
  * [MixKVQ] Algorithm 1 KeyQuant: OutlierReserve splits the key channels by
  * tier; BF16 channels are kept as they are ("sparse outlier store"), UINT4
  * and UINT2 channels are group-quantized along tokens at 4 and 2 bits.

@@ -82,6 +82,10 @@ int orc_tiers_rank(const float* A, int D, int n_bf16, int n_uint4,
                    uint8_t* tiers);
 int orc_tiers_threshold(const float* A, int D, float tau_bf16, float tau_uint4,
                         uint8_t* tiers);
+int orc_tiers_capped(const float* A, int D, float tau_bf16, float tau_uint4,
+                     int cap_bf16, int cap_uint4, uint8_t* tiers);
+int orc_observe_query(float* acc, const uint16_t* q_step, int n_rep, int D);
+int orc_importance_from_sum(const float* acc, int n_rep, int steps, int D, float* I);
 
 /* One mixed-precision key group: k bf16 [G][D], tiers[D] given.
  *   perm     [D]                   channels: BF16 tier, then UINT4, then

@@ -29,6 +29,11 @@ def frac(s):
     return Fraction(s)
 
 
+def bf16_trunc(x):
+    """bf16 bit patterns of x (float32 truncated to its top 16 bits)."""
+    return (np.asarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
 def qdq_rows(mat, bits):
     """Per-row groups (Value per-token axis) via the unit-level V quantizer."""
     m = np.asarray(mat, np.float32)
@@ -377,6 +382,79 @@ def test_tier_rank_ties_lower_channel_first():
     A = np.array([1.0, 3.0, 3.0, 1.0, 3.0], np.float32)
     assert list(orc.tiers_rank(A, 2, 2)) == [orc.TIER_UINT4, orc.TIER_BF16, orc.TIER_BF16,
                                              orc.TIER_UINT2, orc.TIER_UINT4]
+
+
+def test_capped_tiers_hand_example():
+    """Threshold tiers with record capacities: the overflow of a full tier
+    drops one tier, smallest salience first (MixKVQ thresholds; the record
+    holds at most cap_bf16 BF16 and cap_uint4 UINT4 channels)."""
+    A = np.array([3.0, 1.0, 2.0, 5.0, 0.5, 2.0], np.float32)
+    B, U4, U2 = orc.TIER_BF16, orc.TIER_UINT4, orc.TIER_UINT2
+    # uncapped: A > 1.5 -> BF16 (d0, d2, d3, d5); 0.75 < A <= 1.5 -> UINT4 (d1)
+    assert list(orc.tiers_capped(A, 1.5, 0.75, 6, 6)) == [B, U4, B, B, U2, B]
+    # two BF16 slots: d3 (5.0) and d0 (3.0); d2 and d5 tie at 2.0 and drop
+    # to UINT4; d1 also qualifies for UINT4
+    assert list(orc.tiers_capped(A, 1.5, 0.75, 2, 6)) == [B, U4, U4, B, U2, U4]
+    # two UINT4 slots as well: d2 (lower index of the tie) and d5 take them,
+    # d1 (1.0) is over the UINT4 capacity -> UINT2
+    assert list(orc.tiers_capped(A, 1.5, 0.75, 2, 2)) == [B, U2, U4, B, U2, U4]
+    # a threshold above every A: nothing is BF16 whatever the capacity
+    assert list(orc.tiers_capped(A, 9.0, 2.5, 6, 6)) == [U4, U2, U2, U4, U2, U2]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_capped_tiers_reduce_to_rank_and_threshold(seed):
+    """The two special cases: thresholds at -inf give the rank rule, and
+    capacities of D give the plain threshold rule."""
+    rng = np.random.default_rng(seed)
+    A = np.round(rng.exponential(1.0, 128), 2).astype(np.float32)   # ties included
+    for nb, n4 in [(6, 25), (0, 0), (128, 0), (3, 125)]:
+        assert np.array_equal(orc.tiers_capped(A, -np.inf, -np.inf, nb, n4),
+                              orc.tiers_rank(A, nb, n4))
+    for tb, t4 in [(1.5, 0.5), (0.2, 0.2), (9.0, 0.1), (0.5, 1.0)]:
+        assert np.array_equal(orc.tiers_capped(A, tb, t4, 128, 128),
+                              orc.tiers_threshold(A, tb, t4))
+
+
+def test_online_accumulator_equals_window_importance():
+    """MixKVQ online saliency: per-step |q| sums, divided by (n_rep * steps)
+    at the window's end, give bit for bit the importance of the same window
+    of queries computed in one pass."""
+    rng = np.random.default_rng(4)
+    n_rep, L, D = 4, 37, 128
+    q = bf16_trunc(rng.standard_normal((n_rep, L, D)) * 3)
+    acc = np.zeros(D, np.float32)
+    for i in range(L):
+        orc.observe_query(acc, q[:, i])
+    I_online = orc.importance_from_sum(acc, n_rep, L)
+    assert np.array_equal(I_online.view(np.uint32), orc.importance(q).view(np.uint32))
+
+
+def test_mixed_cache_online_window_and_threshold_tiers():
+    """A mixed cache flushed without importance takes it from the queries
+    observed since the previous flush, then starts a new window; threshold
+    tiers then follow tiers_capped on that importance."""
+    rng = np.random.default_rng(6)
+    B, Hkv, n_rep, D, R = 1, 2, 2, 128, 128
+    c = orc.OracleCache(B, Hkv, D, mode="mixed", n_bf16=8, n_uint4=16,
+                        tier_mode="threshold", tau_bf16=0.9, tau_uint4=0.3)
+    with pytest.raises(ValueError):
+        c.observe(np.zeros((B, Hkv * n_rep, 3), np.uint16))   # wrong head dim
+    K = bf16_trunc(rng.standard_normal((B, Hkv, R, D)))
+    V = bf16_trunc(rng.standard_normal((B, Hkv, R, D)))
+    qs = [bf16_trunc(rng.standard_normal((B, Hkv * n_rep, D))) for _ in range(5)]
+    for i in range(R):
+        c.append(K[:, :, i], V[:, :, i])
+    with pytest.raises(ValueError):
+        c.flush()                                   # mixed, no importance, no window
+    for q in qs:
+        c.observe(q)
+    want_I = orc.importance(np.stack(qs, axis=2)[0, 0:n_rep])     # unit 0's window
+    c.flush()
+    assert c.q_steps == 0 and not c.qacc.any()       # a new window starts
+    S = orc.sensitivity(K[0, 0], 2)
+    want = orc.tiers_capped(orc.salience(want_I, S), 0.9, 0.3, 8, 16)
+    assert np.array_equal(c.k_groups[0][0].tiers, want)
 
 
 def test_mixed_group_storage_and_reconstruction():
