@@ -44,7 +44,8 @@ class KVQError(RuntimeError):
 class _Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "batch", "kv_heads", "head_dim", "max_tokens", "k_bits", "v_bits", "k_mode",
-        "n_bf16", "n_uint4", "n_sink")]
+        "n_bf16", "n_uint4", "n_sink", "tier_mode")] + [
+        ("tau_bf16", ctypes.c_float), ("tau_uint4", ctypes.c_float)]
 
 
 class _TierSpec(ctypes.Structure):
@@ -65,6 +66,7 @@ _SIGS = {
     "kvq_cache_reset": (_I, [_P, _P]),
     "kvq_append_residual": (_I, [_P, _P, _P, _P]),
     "kvq_flush_group": (_I, [_P, _P, _P]),
+    "kvq_observe_query": (_I, [_P, _P, _I, _P]),
     "kvq_quantize_prefill": (_I, [_P, _P, _P, _I, _P, _P]),
     "kvq_decode_workspace_bytes": (_Z, [_P, _I]),
     "kvq_decode_attention": (_I, [_P, _P, _I, _P, _P, _Z, _P]),
@@ -76,7 +78,7 @@ _SIGS = {
     "kvq_export_v": (_I, [_P, _P, _P, _P, _P]),
     "kvq_export_residual": (_I, [_P, _P, _P, _P]),
     "kvq_export_sink": (_I, [_P, _P, _P, _P]),
-    "kvq_export_k_mixed": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "kvq_export_k_mixed": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvq_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -125,8 +127,10 @@ class KVCache:
     state: packed history + bf16 residual of up to 128 tokens).
 
     mode "uniform": keys at k_bits per channel over 128-token groups;
-    mode "mixed": keys tiered per group into n_bf16 BF16, n_uint4 UINT4 and
-    the rest UINT2 channels.  Values always v_bits per token over 32 channels.
+    mode "mixed": keys tiered per group into BF16, UINT4 and UINT2 channels,
+    tier_mode "rank" exactly n_bf16 / n_uint4 of the first two, "threshold"
+    A > tau_bf16 / A > tau_uint4 with at most n_bf16 / n_uint4 of them.
+    Values always v_bits per token over 32 channels.
     n_sink > 0 keeps the sequence's first n_sink tokens bf16 (attention
     sinks, never quantized).
     The device buffer is a torch uint8 tensor owned by this object.
@@ -134,10 +138,15 @@ class KVCache:
 
     def __init__(self, batch: int, kv_heads: int, max_tokens: int, k_bits: int = 2,
                  v_bits: int = 2, mode: str = "uniform", n_bf16: int = 0, n_uint4: int = 0,
-                 head_dim: int = HEAD_DIM, device=None, stream=None, n_sink: int = 0):
+                 head_dim: int = HEAD_DIM, device=None, stream=None, n_sink: int = 0,
+                 tier_mode: str = "rank", tau_bf16: float = 0.0, tau_uint4: float = 0.0):
+        if tier_mode not in ("rank", "threshold"):
+            raise ValueError("tier_mode is 'rank' or 'threshold'")
         self.cfg = _Config(batch, kv_heads, head_dim, max_tokens, k_bits, v_bits,
                            KVQ_K_MIXED if mode == "mixed" else KVQ_K_UNIFORM, n_bf16, n_uint4,
-                           n_sink)
+                           n_sink, TIERS_THRESHOLD if tier_mode == "threshold"
+                           else TIERS_RANK, tau_bf16, tau_uint4)
+        self.tier_mode = tier_mode
         self.mode = mode
         nbytes = lib().kvq_cache_bytes(ctypes.byref(self.cfg))
         if nbytes == 0:
@@ -199,6 +208,14 @@ class KVCache:
         _check(lib().kvq_append_residual(self._h, _ptr(k_new, torch.bfloat16, shp, "k_new"),
                                          _ptr(v_new, torch.bfloat16, shp, "v_new"),
                                          _stream(stream)), "kvq_append_residual")
+
+    def observe(self, q: torch.Tensor, stream=None):
+        """Add one decode step's query (bf16 [B, Hq, D]) to the mixed cache's
+        online |q| window (the importance a flush without one uses)."""
+        B, Hq, D = q.shape
+        _check(lib().kvq_observe_query(self._h, _ptr(q, torch.bfloat16, (self.batch, Hq, HEAD_DIM),
+                                                     "q"), Hq, _stream(stream)),
+               "kvq_observe_query")
 
     def flush(self, importance: torch.Tensor | None = None, stream=None):
         _check(lib().kvq_flush_group(
@@ -270,8 +287,9 @@ class KVCache:
         n = tq // K_GROUP
         B, H, dev = self.batch, self.kv_heads, self.device
         nb, n4 = self.n_bf16, self.n_uint4
-        n2 = HEAD_DIM - nb - n4
+        n2 = HEAD_DIM if self.tier_mode == "threshold" else HEAD_DIM - nb - n4
         t = dict(
+            counts=torch.empty(B, H, n, 2, dtype=torch.uint8, device=dev),
             perm=torch.empty(B, H, n, HEAD_DIM, dtype=torch.uint8, device=dev),
             raw=torch.empty(B, H, n, nb, K_GROUP, dtype=torch.bfloat16, device=dev),
             c4=torch.empty(B, H, n, n4, K_GROUP // 2, dtype=torch.uint8, device=dev),

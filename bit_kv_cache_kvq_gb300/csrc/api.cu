@@ -27,6 +27,11 @@ bool valid_config(const kvq_config* c) {
     if (c->k_bits != 2 && c->k_bits != 4) return false;
   } else if (c->k_mode == KVQ_K_MIXED) {
     if (c->n_bf16 < 0 || c->n_uint4 < 0 || c->n_bf16 + c->n_uint4 > kD) return false;
+    if (c->tier_mode == KVQ_TIERS_THRESHOLD) {
+      if (c->tau_bf16 != c->tau_bf16 || c->tau_uint4 != c->tau_uint4) return false;  // NaN
+    } else if (c->tier_mode != KVQ_TIERS_RANK) {
+      return false;
+    }
   } else {
     return false;
   }
@@ -35,11 +40,12 @@ bool valid_config(const kvq_config* c) {
 
 RecLayout layout_of(const kvq_config* c) {
   return make_layout(c->k_mode == KVQ_K_MIXED, c->k_mode == KVQ_K_MIXED ? 2 : c->k_bits,
-                     c->v_bits, c->n_bf16, c->n_uint4);
+                     c->v_bits, c->n_bf16, c->n_uint4,
+                     c->k_mode == KVQ_K_MIXED && c->tier_mode == KVQ_TIERS_THRESHOLD);
 }
 
 struct Sizes {
-  size_t records, residual, sink, status, total;
+  size_t records, residual, sink, qacc, status, total;
 };
 
 Sizes sizes_of(const kvq_config* c) {
@@ -49,8 +55,9 @@ Sizes sizes_of(const kvq_config* c) {
   s.records = round_up(units * (c->max_tokens / kKG) * static_cast<size_t>(L.bytes));
   s.residual = round_up(units * kR * kD * sizeof(kvq_bf16));
   s.sink = round_up(units * static_cast<size_t>(c->n_sink) * kD * sizeof(kvq_bf16));
+  s.qacc = c->k_mode == KVQ_K_MIXED ? round_up(units * kD * sizeof(float)) : 0;
   s.status = kAlign;
-  s.total = s.records + 2 * s.residual + 2 * s.sink + s.status;
+  s.total = s.records + 2 * s.residual + 2 * s.sink + s.qacc + s.status;
   return s;
 }
 
@@ -107,11 +114,16 @@ int kvq_cache_alloc(const kvq_config* cfg, void* dev_buf, size_t buf_bytes,
   c->res_v = reinterpret_cast<kvq_bf16*>(c->base + sz.records + sz.residual);
   c->sink_k = reinterpret_cast<kvq_bf16*>(c->base + sz.records + 2 * sz.residual);
   c->sink_v = reinterpret_cast<kvq_bf16*>(c->base + sz.records + 2 * sz.residual + sz.sink);
-  c->status = reinterpret_cast<unsigned*>(c->base + sz.records + 2 * sz.residual + 2 * sz.sink);
+  uint8_t* tail = c->base + sz.records + 2 * sz.residual + 2 * sz.sink;
+  c->qacc = sz.qacc ? reinterpret_cast<float*>(tail) : nullptr;
+  c->status = reinterpret_cast<unsigned*>(tail + sz.qacc);
   c->t_q = 0;
   c->r = 0;
   c->s = 0;
-  if (cudaMemsetAsync(c->status, 0, sizeof(unsigned), s) != cudaSuccess) {
+  c->q_steps = 0;
+  c->q_rep = 0;
+  // the online |q| sums and the status word are adjacent: one memset
+  if (cudaMemsetAsync(tail, 0, sz.qacc + sizeof(unsigned), s) != cudaSuccess) {
     if (c->owned) cudaFreeAsync(c->base, s);
     delete c;
     return KVQ_ERR_CUDA;
@@ -144,9 +156,14 @@ int kvq_cache_sink_tokens(const kvq_cache* c, int* sink_tokens) {
 int kvq_cache_reset(kvq_cache* c, cudaStream_t s) {
   if (!c) return KVQ_ERR_ARG;
   if (cudaMemsetAsync(c->status, 0, sizeof(unsigned), s) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (c->qacc && cudaMemsetAsync(c->qacc, 0, sizeof(float) * kD * c->cfg.batch * c->cfg.kv_heads,
+                                 s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
   c->t_q = 0;
   c->r = 0;
   c->s = 0;
+  c->q_steps = 0;
+  c->q_rep = 0;
   return KVQ_OK;
 }
 
@@ -175,15 +192,35 @@ static int check_importance(const kvq_cache* c, const float* importance) {
 
 int kvq_flush_group(kvq_cache* c, const float* importance, cudaStream_t s) {
   if (!c) return KVQ_ERR_ARG;
-  const int m = check_importance(c, importance);
-  if (m != KVQ_OK) return m;
+  const bool mixed = c->cfg.k_mode == KVQ_K_MIXED;
+  if (!mixed && importance) return KVQ_ERR_MODE;
+  const bool window = mixed && !importance;   // I_d from the online window
+  if (window && c->q_steps == 0) return KVQ_ERR_EMPTY;
   if (c->r != kR) return KVQ_ERR_RESIDUAL_NOT_FULL;
   if (c->t_q + kKG > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
   QuantSrc src{c->res_k, c->res_v, static_cast<long long>(kR) * kD, 0};
-  const cudaError_t e = launch_quantize(c, src, 1, c->t_q / kKG, importance, s);
+  cudaError_t e = launch_quantize(c, src, 1, c->t_q / kKG, importance, s);
+  if (e == cudaSuccess && window)   // the next window starts from zero
+    e = cudaMemsetAsync(c->qacc, 0, sizeof(float) * kD * c->cfg.batch * c->cfg.kv_heads, s);
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
   c->t_q += kKG;
   c->r = 0;
+  if (window) {
+    c->q_steps = 0;
+    c->q_rep = 0;
+  }
+  return KVQ_OK;
+}
+
+int kvq_observe_query(kvq_cache* c, const kvq_bf16* q, int Hq, cudaStream_t s) {
+  if (!c || !q) return KVQ_ERR_ARG;
+  if (c->cfg.k_mode != KVQ_K_MIXED) return KVQ_ERR_MODE;
+  const int Hkv = c->cfg.kv_heads;
+  if (Hq < Hkv || Hq % Hkv) return KVQ_ERR_SHAPE;
+  if (c->q_steps && Hq / Hkv != c->q_rep) return KVQ_ERR_SHAPE;
+  if (launch_observe_query(c, q, Hq, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  c->q_rep = Hq / Hkv;
+  c->q_steps += 1;
   return KVQ_OK;
 }
 
@@ -340,17 +377,18 @@ int kvq_export_sink(const kvq_cache* c, kvq_bf16* k, kvq_bf16* v, cudaStream_t s
   return cuda_status(e);
 }
 
-int kvq_export_k_mixed(const kvq_cache* c, uint8_t* perm, kvq_bf16* raw, uint8_t* c4,
-                       kvq_bf16* m4, float* s4, uint8_t* c2, kvq_bf16* m2, float* s2,
-                       cudaStream_t s) {
+int kvq_export_k_mixed(const kvq_cache* c, uint8_t* counts, uint8_t* perm, kvq_bf16* raw,
+                       uint8_t* c4, kvq_bf16* m4, float* s4, uint8_t* c2, kvq_bf16* m2,
+                       float* s2, cudaStream_t s) {
   if (!c) return KVQ_ERR_ARG;
   if (c->cfg.k_mode != KVQ_K_MIXED) return KVQ_ERR_MODE;
   if (c->t_q == 0) return KVQ_OK;
-  // a tier with no channels has an empty (possibly NULL) destination
+  // a tier with no room has an empty (possibly NULL) destination
   const RecLayout& L = c->lay;
-  if (!perm || (L.nb && !raw) || (L.n4 && (!c4 || !m4 || !s4)) || (L.n2 && (!c2 || !m2 || !s2)))
+  if (!perm || (L.nb && !raw) || (L.n4 && (!c4 || !m4 || !s4)) ||
+      (L.n2cap && (!c2 || !m2 || !s2)))
     return KVQ_ERR_ARG;
-  return cuda_status(launch_export_k_mixed(c, perm, raw, c4, m4, s4, c2, m2, s2, s));
+  return cuda_status(launch_export_k_mixed(c, counts, perm, raw, c4, m4, s4, c2, m2, s2, s));
 }
 
 const char* kvq_status_string(int code) {

@@ -468,7 +468,9 @@ struct Warp {
   __device__ __forceinline__ void scores_mixed(float (&S)[8][4], float (&hinv)[2],
                                                float (&hbias)[2]) {
     const RecLayout& L = a.lay;
-    const int nb = L.nb, n4 = L.n4, nv = L.nv, kw2 = L.kw2;
+    // this group's tier counts (its header); kw2 is the record's room
+    const int nb = kbuf[L.hdr], n4 = kbuf[L.hdr + 1], nv = kD + n4 - nb, kw2 = L.kw2;
+    const int kw_used = (nv + 31) >> 5;   // words of the group's virtual channels
     const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
     uint2* tab = reinterpret_cast<uint2*>(vsb);
     const float* sc = reinterpret_cast<const float*>(kbuf + L.s4);
@@ -545,7 +547,7 @@ struct Warp {
     const uint32_t* kcw = reinterpret_cast<const uint32_t*>(kbuf + L.kc);
     const bool low_lane = low_col();
     float bias = 0.0f;
-    for (int w = 0; w < kw2; ++w) {
+    for (int w = 0; w < kw_used; ++w) {
       uint32_t kx[8], ky[8];
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {

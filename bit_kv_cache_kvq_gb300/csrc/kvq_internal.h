@@ -30,17 +30,21 @@ constexpr int kMaxRep = 8;         // query heads per KV head
 //                           order (frag_layout.h)
 //   [kc]           kscale   fp32  [D]
 //   [kc+4D]        kmin     bf16  [D]
-// Mixed key (n_bf16 = nb, n_uint4 = n4, n_uint2 = n2):
+// Mixed key: the group's own counts nb (BF16), n4 (UINT4), n2 = D - nb - n4
+// (UINT2) are in its header; rank tiers fix them to the config's n_bf16,
+// n_uint4, threshold tiers bound them by those (the sections are sized for
+// the largest case):
 //   [0]            perm     uint8 [D]   BF16, UINT4, UINT2 channels, ascending
-//   [D]            raw      bf16  [nb][128] channel-major; the 16-byte piece
-//                           p of tier channel i sits at piece p ^ (i & 7)
+//   [D]            raw      bf16  [n_bf16][128] channel-major; the 16-byte
+//                           piece p of tier channel i sits at piece p ^ (i & 7)
 //   [kc]           codes    2-bit "virtual channels" in the key fragment
 //                           order (frag_layout.h) with kw2 words per (tile,
 //                           lane): v < n4 the low two bits of UINT4 channel
 //                           v, n4 <= v < 2 n4 its high two bits, then the
 //                           n2 UINT2 channels, zero up to 32 kw2 channels
-//   [..]           s4, s2   fp32  [n4], [n2]  (contiguous)
-//   [..]           m4, m2   bf16  [n4], [n2]  (contiguous; padded to 16 bytes)
+//   [s4]           steps    fp32  [nq]  UINT4 channels, then UINT2 (perm order)
+//   [m4]           origins  bf16  [nq]  same order
+//   [hdr]          counts   uint8 nb, n4 (16 bytes reserved)
 // Value (v_bits = vb), after the key part at offset kpart:
 //   [kpart]        V codes  128*128*vb/8 bytes in fragment order
 //   [+vc]          vscale   fp32  [128][D/32]
@@ -53,12 +57,18 @@ constexpr int kMaxRep = 8;         // query heads per KV head
 struct RecLayout {
   int mixed;
   int kb, vb;
-  int nb, n4, n2;
+  int thresh;    // mixed: threshold tiers (per-group counts up to nb, n4)
+  int nb, n4;    // mixed: BF16 / UINT4 channels a group (rank tiers) or at most
   // key (uniform)
   int k_codes, k_scale, k_min;
-  // key (mixed)
-  int perm, raw, kc, s4, s2, m4, m2;
-  int nv, kw2;  // virtual 2-bit channels (2 n4 + n2) and words per (tile, lane)
+  // key (mixed): perm [D], raw [nb][128], virtual 2-bit channel words, the
+  // quantized channels' steps [nq] (fp32) and origins [nq] (bf16) in perm
+  // order (UINT4 first), then the header: the group's BF16 and UINT4
+  // channel counts (one byte each)
+  int perm, raw, kc, s4, m4, hdr;
+  int nq;       // capacity of the step / origin tables
+  int n2cap;    // UINT2 channels a group at most (D - nb - n4, or D)
+  int nv, kw2;  // virtual 2-bit channels (2 n4 + n2) at most, words per (tile, lane)
   int kpart;  // bytes of the key part
   // value
   int v_codes, v_scale, v_min;
@@ -68,7 +78,7 @@ struct RecLayout {
 __host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
 
 __host__ __device__ inline RecLayout make_layout(int mixed, int kb, int vb,
-                                                 int nb, int n4) {
+                                                 int nb, int n4, int thresh) {
   RecLayout L{};
   L.mixed = mixed;
   L.kb = kb;
@@ -79,19 +89,23 @@ __host__ __device__ inline RecLayout make_layout(int mixed, int kb, int vb,
     L.k_min = L.k_scale + 4 * kD;
     L.kpart = align16(L.k_min + 2 * kD);
   } else {
+    // rank tiers: exactly nb BF16 and n4 UINT4 channels a group; threshold
+    // tiers: any counts up to those, so the tables take the largest case
+    // (no BF16 channel, n4 UINT4 channels: D + n4 virtual channels)
+    L.thresh = thresh;
     L.nb = nb;
     L.n4 = n4;
-    L.n2 = kD - nb - n4;
     L.perm = 0;
     L.raw = kD;
-    L.nv = 2 * n4 + L.n2;
+    L.nq = thresh ? kD : kD - nb;
+    L.n2cap = thresh ? kD : kD - nb - n4;
+    L.nv = kD + n4 - (thresh ? 0 : nb);
     L.kw2 = (L.nv + 31) / 32;
     L.kc = align16(L.raw + nb * kKG * 2);
     L.s4 = L.kc + L.kw2 * 8 * 32 * 4;
-    L.s2 = L.s4 + 4 * L.n4;
-    L.m4 = L.s2 + 4 * L.n2;
-    L.m2 = L.m4 + 2 * L.n4;
-    L.kpart = (L.m2 + 2 * L.n2 + 127) & ~127;   // value part on a 128-byte line
+    L.m4 = L.s4 + 4 * L.nq;
+    L.hdr = align16(L.m4 + 2 * L.nq);
+    L.kpart = (L.hdr + 16 + 127) & ~127;   // value part on a 128-byte line
   }
   L.v_codes = L.kpart;
   L.v_scale = L.v_codes + kKG * kD * vb / 8;
@@ -118,6 +132,9 @@ struct kvq_cache {
   kvq_bf16* sink_k;    // [B*Hkv][n_sink][D] (attention-sink window)
   kvq_bf16* sink_v;
   unsigned* status;    // sticky KVQ_FLAG_* word
+  float* qacc;         // mixed: running sum of |q| [B*Hkv][D] (online saliency)
+  int q_steps;         // decode steps summed in qacc since the last flush
+  int q_rep;           // query heads per KV head of those steps
   int t_q;             // quantized tokens (multiple of 128)
   int r;               // residual tokens (0..128)
   int s;               // sink tokens (0..n_sink)
@@ -142,6 +159,8 @@ cudaError_t launch_append(const kvq_cache* c, const kvq_bf16* k_new, const kvq_b
 cudaError_t launch_copy_tokens(const kvq_bf16* k, const kvq_bf16* v, int L, int first, int count,
                                kvq_bf16* dst_k, kvq_bf16* dst_v, int cap, int units,
                                cudaStream_t s);
+// importance: mixed keys' I_d [units][D]; NULL takes it from the cache's
+// online window (qacc / (q_rep * q_steps)).
 cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
                             int first_group, const float* importance,
                             cudaStream_t s);
@@ -181,13 +200,17 @@ cudaError_t launch_saliency(const kvq_bf16* q_win, int Hq, int Lq,
                             int sal_bits, const kvq_tier_spec* spec,
                             float* I_out, float* A_out, uint8_t* tiers_out,
                             cudaStream_t s);
+// Online saliency (saliency.cu): qacc[u][d] += |q| of the unit's query
+// heads, in head order; I[u][d] = qacc[u][d] / count.
+cudaError_t launch_observe_query(const kvq_cache* c, const kvq_bf16* q, int Hq, cudaStream_t s);
+cudaError_t launch_window_importance(const kvq_cache* c, float* I, cudaStream_t s);
 
 cudaError_t launch_export_k_uniform(const kvq_cache* c, uint8_t* codes,
                                     kvq_bf16* kmin, float* kscale,
                                     cudaStream_t s);
 cudaError_t launch_export_v(const kvq_cache* c, uint8_t* codes, kvq_bf16* vmin,
                             float* vscale, cudaStream_t s);
-cudaError_t launch_export_k_mixed(const kvq_cache* c, uint8_t* perm,
+cudaError_t launch_export_k_mixed(const kvq_cache* c, uint8_t* counts, uint8_t* perm,
                                   kvq_bf16* raw, uint8_t* c4, kvq_bf16* m4,
                                   float* s4, uint8_t* c2, kvq_bf16* m2,
                                   float* s2, cudaStream_t s);

@@ -59,7 +59,10 @@ struct QuantArgs {
   int max_groups;
   int first_group;
   RecLayout lay;
-  const float* importance;  // mixed: [units][D]
+  const float* importance;  // mixed: [units][D], or NULL: qacc / q_count
+  const float* qacc;        // mixed: the online window's |q| sums [units][D]
+  float q_count;            // (query heads per KV head) * (steps observed)
+  float tau_bf16, tau_uint4;  // threshold tiers (lay.thresh)
   unsigned* status;
 };
 
@@ -427,8 +430,14 @@ __global__ void __launch_bounds__(256) quantize_uniform_kernel(QuantArgs a) {
 }
 
 // Mixed keys (MixKVQ KeyQuant): per channel S_d = fl32(fl32(M - m)/3) over
-// the tile, A_d = fl32(I_d * S_d); tiers by rank (A descending, channel
-// ascending on ties): n_bf16 BF16, n_uint4 UINT4, rest UINT2.  Storage
+// the tile, A_d = fl32(I_d * S_d), with I_d given or taken from the online
+// window (fl32(sum |q| / count)).  Channels are ranked by A (descending,
+// channel ascending on ties).  Rank tiers: the first n_bf16 BF16, the next
+// n_uint4 UINT4, the rest UINT2.  Threshold tiers: the channels with
+// A > tau_bf16 lead the ranking, so the first min(#{A > tau_bf16}, n_bf16)
+// are BF16; of the rest, those with A > tau_uint4 (again a prefix) are
+// UINT4 up to n_uint4; the others UINT2 (channels over a capacity drop one
+// tier, smallest A first).  The counts go to the record's header.  Storage
 // order BF16, UINT4, UINT2 channels, each ascending (the permutation).  The
 // BF16 tier is stored raw, channel-major and piece-swizzled; the UINT4 and
 // UINT2 codes become 2-bit virtual channels (kvq_internal.h), staged as
@@ -446,12 +455,12 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
   uint32_t* sRed = reinterpret_cast<uint32_t*>(smem + kTileBytes);             // 2 KB
   uint32_t* sKey = reinterpret_cast<uint32_t*>(smem + kTileBytes + 2048);     // 512 B
   uint8_t* sTier = smem + kTileBytes + 2048 + 512;                            // 128 B
+  float* sA = reinterpret_cast<float*>(smem + kTileBytes + 2048 + 512 + 128);  // 512 B
   uint8_t* cKv = smem + kTileBytes + kParamBytes;
   load_tile(a, a.src.k, sK);
-  // zero the padding virtual channels
-  const int pad = kvs - L.nv;
-  for (int i = threadIdx.x; i < kKG * pad; i += blockDim.x)
-    cKv[(i / pad) * kvs + L.nv + i % pad] = 0;
+  // virtual channels past this group's count stay zero
+  for (int i = threadIdx.x; i < kKG * kvs / 4; i += blockDim.x)
+    reinterpret_cast<uint32_t*>(cKv)[i] = 0u;
   __syncthreads();
 
   const int u = blockIdx.y;
@@ -464,7 +473,8 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
     const int d = threadIdx.x;
     float S = 0.0f;
     if (!bad) S = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
-    const float I = a.importance[static_cast<long long>(u) * kD + d];
+    const long long ud = static_cast<long long>(u) * kD + d;
+    const float I = a.importance ? a.importance[ud] : __fdiv_rn(a.qacc[ud], a.q_count);
     if (!isfinite(I)) flags |= KVQ_FLAG_NONFINITE;
     if (bad) flags |= KVQ_FLAG_NONFINITE;
     else if (!isfinite(S)) flags |= KVQ_FLAG_RANGE;
@@ -474,18 +484,34 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
     // inside its tier's region.
     const uint32_t key = isnan(A) ? 0u : fkey(A);
     sKey[d] = key;
+    sA[d] = A;
     asm volatile("bar.sync 1, 128;");
-    int rank = 0;
+    // rank, and how many channels pass each threshold (NaN passes none)
+    int rank = 0, above_b = 0, above_4 = 0;
     for (int e = 0; e < kD; ++e) {
       const uint32_t ke = sKey[e];
       rank += (ke > key || (ke == key && e < d)) ? 1 : 0;
+      if (L.thresh) {
+        const float Ae = sA[e];
+        above_b += Ae > a.tau_bf16 ? 1 : 0;
+        above_4 += Ae > a.tau_uint4 ? 1 : 0;
+      }
     }
-    const int tier = rank < L.nb ? KVQ_TIER_BF16
-                     : rank < L.nb + L.n4 ? KVQ_TIER_UINT4
-                                          : KVQ_TIER_UINT2;
+    int nb = L.nb, n4 = L.n4;
+    if (L.thresh) {
+      nb = min(above_b, L.nb);
+      n4 = max(0, min(above_4 - nb, L.n4));
+    }
+    const int tier = rank < nb ? KVQ_TIER_BF16
+                     : rank < nb + n4 ? KVQ_TIER_UINT4
+                                      : KVQ_TIER_UINT2;
     sTier[d] = static_cast<uint8_t>(tier);
+    if (d == 0) {
+      rec[L.hdr] = static_cast<uint8_t>(nb);
+      rec[L.hdr + 1] = static_cast<uint8_t>(n4);
+    }
     asm volatile("bar.sync 1, 128;");
-    int slot = tier == KVQ_TIER_BF16 ? 0 : tier == KVQ_TIER_UINT4 ? L.nb : L.nb + L.n4;
+    int slot = tier == KVQ_TIER_BF16 ? 0 : tier == KVQ_TIER_UINT4 ? nb : nb + n4;
     for (int e = 0; e < d; ++e) slot += (sTier[e] == tier) ? 1 : 0;
     rec[L.perm + slot] = static_cast<uint8_t>(d);
     if (tier == KVQ_TIER_BF16) {
@@ -496,18 +522,18 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
       const int top = (1 << bits) - 1;
       const Params p = group_params(lo, hi, top, bad);
       flags |= p.flags;
-      const int j = slot - L.nb;   // index among the quantized channels
+      const int j = slot - nb;   // index among the quantized channels
       reinterpret_cast<float*>(rec + L.s4)[j] = p.step;
       reinterpret_cast<uint16_t*>(rec + L.m4)[j] = f2bf_bits(p.m);
       if (bits == 4) {
         for (int t = 0; t < kKG; ++t) {
           const uint32_t c = code_exact(bf2f(sK[swz(t, d)]), p.m, p.step, top);
           cKv[t * kvs + j] = static_cast<uint8_t>(c & 3u);
-          cKv[t * kvs + L.n4 + j] = static_cast<uint8_t>(c >> 2);
+          cKv[t * kvs + n4 + j] = static_cast<uint8_t>(c >> 2);
         }
       } else {
         for (int t = 0; t < kKG; ++t)
-          cKv[t * kvs + L.n4 + j] = static_cast<uint8_t>(code_exact(bf2f(sK[swz(t, d)]), p.m, p.step, top));
+          cKv[t * kvs + n4 + j] = static_cast<uint8_t>(code_exact(bf2f(sK[swz(t, d)]), p.m, p.step, top));
       }
     }
   }
@@ -587,45 +613,63 @@ __global__ void export_codes_kernel(const uint8_t* __restrict__ records, long lo
   }
 }
 
-// Canonical export of mixed key groups [u][0..n): raw [u][n][nb][128] in
-// token order, UINT4 codes [u][n][n4][64] and UINT2 codes [u][n][n2][32],
-// LSB first along tokens, rebuilt from the virtual 2-bit channels.
+// Canonical export of mixed key groups [u][0..n) at the record capacities
+// (cb = n_bf16, c4 = n_uint4 of the config, c2 = n2cap; the group's own
+// counts nb, n4 go to counts[..][0..1] if counts is not NULL, n2 = D - nb -
+// n4): perm [..][D], raw [..][cb][128] in token order, UINT4 codes
+// [..][c4][64] with origins and steps [..][c4], UINT2 codes [..][c2][32]
+// with origins and steps [..][c2], codes LSB first along tokens, rebuilt
+// from the virtual 2-bit channels; entries past a group's count are zero.
 __global__ void export_mixed_kernel(const uint8_t* __restrict__ records, long long rec_bytes,
-                                    int max_groups, RecLayout L, uint16_t* raw, uint8_t* c4,
-                                    uint8_t* c2, int n) {
+                                    int max_groups, RecLayout L, uint8_t* counts,
+                                    uint8_t* perm, uint16_t* raw, uint8_t* c4, uint16_t* m4,
+                                    float* s4, uint8_t* c2, uint16_t* m2, float* s2, int n) {
   const int g = blockIdx.x;
   const int u = blockIdx.y;
   const uint8_t* rec = records + (static_cast<long long>(u) * max_groups + g) * rec_bytes;
   const long long ug = static_cast<long long>(u) * n + g;
+  const int nb = rec[L.hdr], n4 = rec[L.hdr + 1], n2 = kD - nb - n4;
+  if (counts && threadIdx.x == 0) {
+    counts[ug * 2] = static_cast<uint8_t>(nb);
+    counts[ug * 2 + 1] = static_cast<uint8_t>(n4);
+  }
+  if (threadIdx.x < kD) perm[ug * kD + threadIdx.x] = rec[L.perm + threadIdx.x];
   const uint16_t* rraw = reinterpret_cast<const uint16_t*>(rec + L.raw);
   for (int e = threadIdx.x; e < L.nb * kKG; e += blockDim.x) {
     const int i = e >> 7, t = e & 127;
-    raw[ug * L.nb * kKG + e] = rraw[i * kKG + ((((t >> 3) ^ (i & 7)) << 3) | (t & 7))];
+    raw[ug * L.nb * kKG + e] =
+        i < nb ? rraw[i * kKG + ((((t >> 3) ^ (i & 7)) << 3) | (t & 7))] : 0;
   }
   const uint32_t* words = reinterpret_cast<const uint32_t*>(rec + L.kc);
+  const float* steps = reinterpret_cast<const float*>(rec + L.s4);
+  const uint16_t* mins = reinterpret_cast<const uint16_t*>(rec + L.m4);
   auto code2 = [&](int tok, int v) {
     const CodePos p = mixed_code_pos(tok, v, L.kw2);
     return (words[p.word] >> p.bit) & 3u;
   };
   const int j = threadIdx.x;
-  if (j < L.n4) {
+  if (j < L.n4) {   // UINT4 slot j: lo plane v = j, hi plane v = n4 + j
     uint8_t* out = c4 + (ug * L.n4 + j) * (kKG / 2);
     for (int i = 0; i < kKG / 2; ++i) {
       uint32_t byte = 0;
-      for (int e = 0; e < 2; ++e) {
+      for (int e = 0; e < 2 && j < n4; ++e) {
         const int t = 2 * i + e;
-        byte |= (code2(t, j) | (code2(t, L.n4 + j) << 2)) << (4 * e);
+        byte |= (code2(t, j) | (code2(t, n4 + j) << 2)) << (4 * e);
       }
       out[i] = static_cast<uint8_t>(byte);
     }
-  } else if (j < L.n4 + L.n2) {
-    const int jj = j - L.n4;
-    uint8_t* out = c2 + (ug * L.n2 + jj) * (kKG / 4);
+    m4[ug * L.n4 + j] = j < n4 ? mins[j] : 0;
+    s4[ug * L.n4 + j] = j < n4 ? steps[j] : 0.0f;
+  }
+  if (j < L.n2cap) {   // UINT2 slot j: virtual channel 2 n4 + j
+    uint8_t* out = c2 + (ug * L.n2cap + j) * (kKG / 4);
     for (int i = 0; i < kKG / 4; ++i) {
       uint32_t byte = 0;
-      for (int e = 0; e < 4; ++e) byte |= code2(4 * i + e, 2 * L.n4 + jj) << (2 * e);
+      for (int e = 0; e < 4 && j < n2; ++e) byte |= code2(4 * i + e, 2 * n4 + j) << (2 * e);
       out[i] = static_cast<uint8_t>(byte);
     }
+    m2[ug * L.n2cap + j] = j < n2 ? mins[n4 + j] : 0;
+    s2[ug * L.n2cap + j] = j < n2 ? steps[n4 + j] : 0.0f;
   }
 }
 
@@ -682,6 +726,11 @@ cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
   a.first_group = first_group;
   a.lay = c->lay;
   a.importance = importance;
+  a.qacc = c->qacc;
+  a.q_count = static_cast<float>(c->q_rep * c->q_steps);
+  // +0.0f turns a threshold of -0 into +0, so A = +0 is not above it
+  a.tau_bf16 = c->cfg.tau_bf16 + 0.0f;
+  a.tau_uint4 = c->cfg.tau_uint4 + 0.0f;
   a.status = c->status;
   const dim3 grid(n_groups, c->cfg.batch * c->cfg.kv_heads, 2);   // z: keys, values
   const int kb = c->cfg.k_bits, vb = c->cfg.v_bits;
@@ -742,24 +791,18 @@ cudaError_t launch_export_v(const kvq_cache* c, uint8_t* codes, kvq_bf16* vmin,
   return e;
 }
 
-cudaError_t launch_export_k_mixed(const kvq_cache* c, uint8_t* perm,
+cudaError_t launch_export_k_mixed(const kvq_cache* c, uint8_t* counts, uint8_t* perm,
                                   kvq_bf16* raw, uint8_t* c4, kvq_bf16* m4,
                                   float* s4, uint8_t* c2, kvq_bf16* m2,
                                   float* s2, cudaStream_t s) {
-  const RecLayout& L = c->lay;
-  cudaError_t e = gather(c, L.perm, kD, perm, s);
   const int n = c->t_q / kKG;
   const int units = c->cfg.batch * c->cfg.kv_heads;
-  if (e == cudaSuccess && n > 0) {
-    export_mixed_kernel<<<dim3(n, units), 128, 0, s>>>(
-        c->records, c->lay.bytes, c->max_groups, L, reinterpret_cast<uint16_t*>(raw), c4, c2, n);
-    e = cudaGetLastError();
-  }
-  if (e == cudaSuccess) e = gather(c, L.m4, L.n4 * 2, m4, s);
-  if (e == cudaSuccess) e = gather(c, L.s4, L.n4 * 4, s4, s);
-  if (e == cudaSuccess) e = gather(c, L.m2, L.n2 * 2, m2, s);
-  if (e == cudaSuccess) e = gather(c, L.s2, L.n2 * 4, s2, s);
-  return e;
+  if (n == 0) return cudaSuccess;
+  export_mixed_kernel<<<dim3(n, units), 128, 0, s>>>(
+      c->records, c->lay.bytes, c->max_groups, c->lay, counts, perm,
+      reinterpret_cast<uint16_t*>(raw), c4, reinterpret_cast<uint16_t*>(m4), s4, c2,
+      reinterpret_cast<uint16_t*>(m2), s2, n);
+  return cudaGetLastError();
 }
 
 }  // namespace kvq

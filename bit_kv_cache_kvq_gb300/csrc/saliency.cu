@@ -9,6 +9,11 @@
 //   S_d = fl32(fl32(max_t k - min_t k) / (2^B - 1))
 //   A_d = fl32(I_d * S_d)
 // The summation order is fixed so the result is bit-reproducible.
+//
+// Online form (MixKVQ "efficient online salience estimation"): the cache
+// keeps the running |q| sum per (batch row, KV head, channel); each decode
+// step adds its query heads' magnitudes in head order, so a window of steps
+// sums in exactly the order above and its I_d is the same number.
 #include <cuda_runtime.h>
 
 #include "kvq_internal.h"
@@ -72,7 +77,44 @@ __global__ void __launch_bounds__(kD) saliency_kernel(
   if (tiers_out) tiers_out[o] = static_cast<uint8_t>(tier);
 }
 
+// One decode step into the running sums: block = unit, thread = channel.
+__global__ void __launch_bounds__(kD) observe_query_kernel(const uint16_t* __restrict__ q,
+                                                           int Hq, int Hkv, float* acc,
+                                                           unsigned* status) {
+  const int u = blockIdx.x, d = threadIdx.x;
+  const int b = u / Hkv, kvh = u % Hkv, n_rep = Hq / Hkv;
+  const uint16_t* qb = q + (static_cast<long long>(b) * Hq + kvh * n_rep) * kD + d;
+  const long long o = static_cast<long long>(u) * kD + d;
+  float a = acc[o];
+  bool bad = false;
+  for (int h = 0; h < n_rep; ++h) {
+    const float x = bf2f(qb[h * kD]);
+    bad |= !isfinite(x);
+    a = __fadd_rn(a, fabsf(x));
+  }
+  acc[o] = a;
+  if (bad) atomicOr(status, static_cast<unsigned>(KVQ_FLAG_NONFINITE));
+}
+
+__global__ void __launch_bounds__(kD) window_importance_kernel(const float* __restrict__ acc,
+                                                               float count, float* I) {
+  const long long o = static_cast<long long>(blockIdx.x) * kD + threadIdx.x;
+  I[o] = __fdiv_rn(acc[o], count);
+}
+
 }  // namespace
+
+cudaError_t launch_observe_query(const kvq_cache* c, const kvq_bf16* q, int Hq, cudaStream_t s) {
+  observe_query_kernel<<<c->cfg.batch * c->cfg.kv_heads, kD, 0, s>>>(
+      q, Hq, c->cfg.kv_heads, c->qacc, c->status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_window_importance(const kvq_cache* c, float* I, cudaStream_t s) {
+  window_importance_kernel<<<c->cfg.batch * c->cfg.kv_heads, kD, 0, s>>>(
+      c->qacc, static_cast<float>(c->q_rep * c->q_steps), I);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_saliency(const kvq_bf16* q_win, int Hq, int Lq,
                             const kvq_bf16* k_grp, int B, int Hkv, int G,

@@ -84,7 +84,12 @@ enum { KVQ_K_UNIFORM = 0, KVQ_K_MIXED = 1 };
 /* Channel tier ids (MixKVQ three-tier strategy). */
 enum { KVQ_TIER_BF16 = 0, KVQ_TIER_UINT4 = 1, KVQ_TIER_UINT2 = 2 };
 
-/* Tier selection rule for kvq_channel_saliency. */
+/*
+ * Tier selection rule (kvq_channel_saliency, and a mixed cache's flushes).
+ * In a mixed cache the record of a group has room for n_bf16 BF16 and
+ * n_uint4 UINT4 channels; under THRESHOLD the channels are taken from the
+ * largest A_d down, and a channel over its tier's room drops one tier.
+ */
 enum { KVQ_TIERS_RANK = 0, KVQ_TIERS_THRESHOLD = 1 };
 
 typedef struct kvq_config {
@@ -95,13 +100,18 @@ typedef struct kvq_config {
   int k_bits;      /* 2 or 4 (KVQ_K_UNIFORM); ignored for KVQ_K_MIXED       */
   int v_bits;      /* 2 or 4                                                */
   int k_mode;      /* KVQ_K_UNIFORM or KVQ_K_MIXED                          */
-  int n_bf16;      /* KVQ_K_MIXED: BF16-tier channels per key group         */
-  int n_uint4;     /* KVQ_K_MIXED: UINT4-tier channels per key group; the
-                      remaining D - n_bf16 - n_uint4 channels are UINT2     */
+  int n_bf16;      /* KVQ_K_MIXED: BF16-tier channels per key group (RANK),
+                      or at most that many (THRESHOLD)                      */
+  int n_uint4;     /* KVQ_K_MIXED: UINT4-tier channels per key group (RANK),
+                      or at most that many (THRESHOLD); the remaining
+                      channels are UINT2                                    */
   int n_sink;      /* attention-sink window, 0..128: the sequence's first
                       n_sink tokens stay bf16 and are never quantized
                       (PN-Mix sink protection, N_s = 32; InnerQ's
                       high-precision window); 0 = none                      */
+  int tier_mode;   /* KVQ_K_MIXED: KVQ_TIERS_RANK (0) or KVQ_TIERS_THRESHOLD */
+  float tau_bf16;  /* THRESHOLD: A_d > tau_bf16 -> BF16 (MixKVQ tau_BF16)   */
+  float tau_uint4; /* THRESHOLD: A_d > tau_uint4 -> UINT4 (tau_UINT4)       */
 } kvq_config;
 
 typedef struct kvq_tier_spec {
@@ -163,13 +173,38 @@ int kvq_append_residual(kvq_cache* cache, const kvq_bf16* k_new,
  * the packed history and empty the residual.  KIVI article §2 contract,
  * PN-Mix Eq. 2 clipping and constant-group branch (step stored 0).
  * KVQ_K_MIXED: importance is I_d, fp32 [B][Hkv][D] (device), and the group's
- * tiers come from A_d = I_d * S_d with S_d at 2 bits, ranked by the cache's
- * n_bf16/n_uint4 (KeyQuant = OutlierReserve + GroupQuant); uniform caches
- * take importance = NULL.
- * Errors: ARG, MODE, RESIDUAL_NOT_FULL, CAPACITY, CUDA.  Flags: NONFINITE,
- * RANGE.
+ * tiers come from A_d = I_d * S_d with S_d at 2 bits (KeyQuant =
+ * OutlierReserve + GroupQuant): RANK gives the n_bf16 largest A_d BF16 and
+ * the next n_uint4 UINT4; THRESHOLD gives A_d > tau_bf16 BF16 and A_d >
+ * tau_uint4 UINT4, from the largest A_d down, at most n_bf16 and n_uint4
+ * (the channel ranking breaks ties by the lower index).  importance = NULL
+ * in a mixed cache takes I_d from the online window (kvq_observe_query):
+ * the running |q| sum / (query heads per KV head * steps observed since the
+ * previous flush); the window then starts again.  Uniform caches take
+ * importance = NULL.
+ * Errors: ARG, MODE (importance given to a uniform cache), EMPTY (mixed
+ * cache, importance NULL and no query observed), RESIDUAL_NOT_FULL,
+ * CAPACITY, CUDA.  Flags: NONFINITE, RANGE.
  */
 int kvq_flush_group(kvq_cache* cache, const float* importance, cudaStream_t s);
+
+/*
+ * MixKVQ online salience estimation (the running accumulator of query
+ * magnitudes kept in the cache), with the workflow's window: I_d is the
+ * mean |Q| of the queries of the current window, renewed every R tokens.
+ * Add one decode step's query (q: bf16
+ * [B][Hq][D], device, Hq a multiple of Hkv) to the mixed cache's running
+ * sums, acc[b][kvh][d] += |q[b][h][d]| for the query heads h of the KV
+ * group in ascending order (fp32, round to nearest).  Over a window of
+ * steps this is the same sum, in the same order (token, then head), that
+ * kvq_channel_saliency forms for I_d.  The window ends at the next
+ * kvq_flush_group that takes its importance from it, and at
+ * kvq_cache_reset.
+ * Errors: ARG, MODE (uniform cache), SHAPE (Hq not a multiple of Hkv, or a
+ * query head count other than the window's earlier steps), CUDA.  Flags:
+ * NONFINITE (a non-finite query element).
+ */
+int kvq_observe_query(kvq_cache* cache, const kvq_bf16* q, int Hq, cudaStream_t s);
 
 /*
  * MixKVQ Algorithm 1, Prefill: k, v bf16 [B][Hkv][L][D]; the first
@@ -275,11 +310,14 @@ int kvq_cache_status(kvq_cache* cache, cudaStream_t s, int* status);
  *  Value: codes uint8 [B][Hkv][T][D*v_bits/8] (LSB first along channels),
  *    vmin bf16 [B][Hkv][T][D/32], vscale fp32 [B][Hkv][T][D/32].
  *  Residual: k_r, v_r bf16 [B][Hkv][r][D] (may be NULL when r = 0).
- *  Key (mixed), per (b, kv head, group) with nb = n_bf16, n4 = n_uint4,
- *    n2 = D - nb - n4: perm uint8 [..][D] (BF16, UINT4, UINT2 channels, each
- *    ascending), raw bf16 [..][nb][128], c4 uint8 [..][n4][64], m4 bf16
- *    [..][n4], s4 fp32 [..][n4], c2 uint8 [..][n2][32], m2 bf16 [..][n2],
- *    s2 fp32 [..][n2].
+ *  Key (mixed), per (b, kv head, group), at the record's room cb = n_bf16,
+ *    c4 = n_uint4, c2 = D - cb - c4 (RANK) or D (THRESHOLD): counts uint8
+ *    [..][2] (the group's own BF16 and UINT4 channel counts nb, n4; n2 =
+ *    D - nb - n4; may be NULL), perm uint8 [..][D] (BF16, UINT4, UINT2
+ *    channels, each ascending), raw bf16 [..][cb][128], c4 uint8
+ *    [..][c4][64], m4 bf16 [..][c4], s4 fp32 [..][c4], c2 uint8
+ *    [..][c2][32], m2 bf16 [..][c2], s2 fp32 [..][c2]; entries past the
+ *    group's own count are zero.
  * With no quantized tokens nothing is copied and the buffers may be NULL.
  * Errors: ARG, MODE, CUDA.
  */
@@ -289,7 +327,7 @@ int kvq_export_v(const kvq_cache* cache, uint8_t* codes, kvq_bf16* vmin,
                  float* vscale, cudaStream_t s);
 int kvq_export_residual(const kvq_cache* cache, kvq_bf16* k_r, kvq_bf16* v_r,
                         cudaStream_t s);
-int kvq_export_k_mixed(const kvq_cache* cache, uint8_t* perm, kvq_bf16* raw,
+int kvq_export_k_mixed(const kvq_cache* cache, uint8_t* counts, uint8_t* perm, kvq_bf16* raw,
                        uint8_t* c4, kvq_bf16* m4, float* s4, uint8_t* c2,
                        kvq_bf16* m2, float* s2, cudaStream_t s);
 

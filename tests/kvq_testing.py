@@ -50,11 +50,13 @@ class UnitOracles:
     inputs as the GPU cache."""
 
     def __init__(self, units, Hkv, k_bits=2, v_bits=2, mode="uniform", n_bf16=0, n_uint4=0,
-                 n_sink=0):
+                 n_sink=0, tier_mode="rank", tau_bf16=0.0, tau_uint4=0.0):
         self.units = list(units)
         self.Hkv = Hkv
         self.caches = [orc.OracleCache(1, 1, 128, k_bits, v_bits, mode=mode, n_bf16=n_bf16,
-                                       n_uint4=n_uint4, n_sink=n_sink) for _ in self.units]
+                                       n_uint4=n_uint4, n_sink=n_sink, tier_mode=tier_mode,
+                                       tau_bf16=tau_bf16, tau_uint4=tau_uint4)
+                       for _ in self.units]
 
     def _sel(self, t: torch.Tensor, u: int):
         b, h = divmod(u, self.Hkv)
@@ -70,6 +72,12 @@ class UnitOracles:
         for u, c in zip(self.units, self.caches):
             b, h = divmod(u, self.Hkv)
             c.append(bf16_bits(k_new[b:b + 1, h:h + 1]), bf16_bits(v_new[b:b + 1, h:h + 1]))
+
+    def observe(self, q: torch.Tensor):
+        n_rep = q.shape[1] // self.Hkv
+        for u, c in zip(self.units, self.caches):
+            b, h = divmod(u, self.Hkv)
+            c.observe(bf16_bits(q[b:b + 1, h * n_rep:(h + 1) * n_rep]))
 
     def flush(self, importance=None):
         for u, c in zip(self.units, self.caches):
@@ -117,6 +125,7 @@ def assert_mixed_exports_equal(cache: kvq.KVCache, ref: UnitOracles):
     """Mixed keys: permutation, raw BF16 tier, UINT4/UINT2 codes, origins and
     steps per group; values and residual as in the uniform case."""
     t = cache.export_k_mixed()
+    counts = t["counts"].cpu().numpy()
     vc, vm, vs = cache.export_v()
     kr, vr = cache.export_residual()
     torch.cuda.synchronize()
@@ -131,14 +140,20 @@ def assert_mixed_exports_equal(cache: kvq.KVCache, ref: UnitOracles):
         assert perm.shape[2] == len(groups)
         for gi, grp in enumerate(groups):
             where = f"(unit {u}, group {gi})"
+            nb, n4, n2 = grp.raw.shape[0], grp.c4.shape[0], grp.c2.shape[0]
+            assert tuple(counts[b, h, gi]) == (nb, n4), f"tier counts differ {where}"
             assert np.array_equal(perm[b, h, gi], grp.perm), f"permutation differs {where}"
-            assert np.array_equal(raw[b, h, gi], grp.raw), f"BF16 tier differs {where}"
-            assert np.array_equal(c4[b, h, gi], grp.c4), f"UINT4 codes differ {where}"
-            assert np.array_equal(m4[b, h, gi], grp.m4), f"UINT4 origins differ {where}"
-            assert np.array_equal(s4[b, h, gi], grp.s4.view(np.uint32)), f"UINT4 steps differ {where}"
-            assert np.array_equal(c2[b, h, gi], grp.c2), f"UINT2 codes differ {where}"
-            assert np.array_equal(m2[b, h, gi], grp.m2), f"UINT2 origins differ {where}"
-            assert np.array_equal(s2[b, h, gi], grp.s2.view(np.uint32)), f"UINT2 steps differ {where}"
+            # the export has the record's room per tier; rows past the group's
+            # own count are zero
+            for name, got, want in (("BF16 tier", raw, grp.raw), ("UINT4 codes", c4, grp.c4),
+                                    ("UINT4 origins", m4, grp.m4),
+                                    ("UINT4 steps", s4, grp.s4.view(np.uint32)),
+                                    ("UINT2 codes", c2, grp.c2), ("UINT2 origins", m2, grp.m2),
+                                    ("UINT2 steps", s2, grp.s2.view(np.uint32))):
+                g = got[b, h, gi]
+                n = want.shape[0]
+                assert np.array_equal(g[:n], want), f"{name} differ {where}"
+                assert not g[n:].any(), f"{name} padding not zero {where}"
         parts = oc.v_parts[0]
         if parts:
             ovc, ovm, ovs = (np.concatenate([p[i] for p in parts]) for i in range(3))
