@@ -309,10 +309,9 @@ struct Warp {
     return ok;
   }
 
-  // Scores of one group (keys in kbuf), softmax folded into the running
-  // state; returns p in S (C-fragment layout) and the rescale factors.
-  __device__ __forceinline__ void qk_softmax(float (&S)[8][4], float (&alpha)[2]) {
-    float hinv[2], hbias[2];
+  // Scores of one group (keys in kbuf) in C-fragment layout, with their
+  // unit hinv and origin term hbias per head (the softmax comes later).
+  __device__ __forceinline__ void scores(float (&S)[8][4], float (&hinv)[2], float (&hbias)[2]) {
     if constexpr (MIX) scores_mixed(S, hinv, hbias);
     else scores_uniform(S, hinv, hbias);
     if (SPARE) {   // columns 2t and 2t + 1: the high and low parts of head t
@@ -322,7 +321,6 @@ struct Warp {
         S[mt][2] += S[mt][3];
       }
     }
-    softmax_update(S, hinv, hbias, alpha);
   }
 
   // Uniform keys: score accumulators S (code units), their unit hinv and the
@@ -332,49 +330,80 @@ struct Warp {
     const RecLayout& L = a.lay;
     const float* kscale = reinterpret_cast<const float*>(kbuf + L.k_scale);
     const uint32_t* kmin2 = reinterpret_cast<const uint32_t*>(kbuf + L.k_min);
-    float qk[32];
-    float mx = 0.0f, bias = 0.0f;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const float2 s01 = *reinterpret_cast<const float2*>(kscale + 16 * ks + 2 * t);
-      const float2 s89 = *reinterpret_cast<const float2*>(kscale + 16 * ks + 2 * t + 8);
-      const uint32_t m01 = kmin2[8 * ks + t];
-      const uint32_t m89 = kmin2[8 * ks + t + 4];
-      float qa, qb, qc, qd;
-      if (SPARE) {   // rows h >= NREP of the stored query are zero
-        const float* qrow = static_cast<const float*>(qs) + hrow() * kQRow;
-        const float2 q01 = *reinterpret_cast<const float2*>(qrow + 16 * ks + 2 * t);
-        const float2 q89 = *reinterpret_cast<const float2*>(qrow + 16 * ks + 2 * t + 8);
-        qa = q01.x; qb = q01.y; qc = q89.x; qd = q89.y;
-      } else {
-        const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
-        const uint32_t* qrow = static_cast<const uint32_t*>(qs) + g * (kQRow / 2);
-        const uint32_t q01 = qrow[8 * ks + t], q89 = qrow[8 * ks + t + 4];
-        qa = bf2f(q01 & 0xffffu) * c0; qb = bf2f(q01 >> 16) * c0;
-        qc = bf2f(q89 & 0xffffu) * c0; qd = bf2f(q89 >> 16) * c0;
-      }
-      qk[4 * ks + 0] = qa * s01.x;
-      qk[4 * ks + 1] = qb * s01.y;
-      qk[4 * ks + 2] = qc * s89.x;
-      qk[4 * ks + 3] = qd * s89.y;
-      bias = fmaf(qa, bf2f(m01 & 0xffffu), bias);
-      bias = fmaf(qb, bf2f(m01 >> 16), bias);
-      bias = fmaf(qc, bf2f(m89 & 0xffffu), bias);
-      bias = fmaf(qd, bf2f(m89 >> 16), bias);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fabsf(qk[4 * ks + i]));
-    }
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-    bias += __shfl_xor_sync(kFull, bias, 1);
-    bias += __shfl_xor_sync(kFull, bias, 2);
-    float sq, inv_sq;
-    pow2_norm(mx, sq, inv_sq);
-    // B' = Q' * sq in [0, 1), times the row factor of its code position;
-    // high part: B' rounded to f16 precision, low part: the rest
     uint32_t bq[8][2], bl[NL][2];
-    {
-      const bool low_lane = low_col();
+    float sq, inv_sq, bias = 0.0f;
+    if constexpr (SPARE) {
+      // The two lanes of a head (columns 2h: high part, 2h + 1: low part)
+      // share the work: the even lane takes the rows of b0 (channels 2t,
+      // 2t + 1 of each k-step), the odd lane those of b1 (2t + 8, 2t + 9);
+      // each rounds its Q' into high and low parts and hands the part it
+      // does not keep to its partner (lane ^ 4) in one shuffle per k-step.
+      const int par = g & 1;
+      const int c_off = 2 * t + 8 * par;
+      const float* qrow = static_cast<const float*>(qs) + hrow() * kQRow;
+      float qk[16];
+      float mx = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const float2 sc = *reinterpret_cast<const float2*>(kscale + 16 * ks + c_off);
+        const float2 qv = *reinterpret_cast<const float2*>(qrow + 16 * ks + c_off);
+        const uint32_t m2 = kmin2[8 * ks + t + 4 * par];
+        qk[2 * ks + 0] = qv.x * sc.x;
+        qk[2 * ks + 1] = qv.y * sc.y;
+        bias = fmaf(qv.x, bf2f(m2 & 0xffffu), bias);
+        bias = fmaf(qv.y, bf2f(m2 >> 16), bias);
+        mx = fmaxf(mx, fmaxf(fabsf(qk[2 * ks]), fabsf(qk[2 * ks + 1])));
+      }
+#pragma unroll
+      for (int x = 1; x <= 4; x <<= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, x));
+        bias += __shfl_xor_sync(kFull, bias, x);
+      }
+      pow2_norm(mx, sq, inv_sq);
+      // the row factor of this lane's slot (b0 or b1), times the norm
+      const float sp = sq * (par ? row_factor<KB>(0, 1) : row_factor<KB>(0, 0));
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const float f = sp * (row_factor<KB>(ks, 0) / row_factor<KB>(0, 0));
+        const float x0 = qk[2 * ks] * f, x1 = qk[2 * ks + 1] * f;
+        const float h0 = round_f16_precision(x0), h1 = round_f16_precision(x1);
+        const uint32_t H = pack_h2(h0, h1), Lo = pack_h2(x0 - h0, x1 - h1);
+        const uint32_t recv = __shfl_xor_sync(kFull, par ? H : Lo, 4);
+        bq[ks][0] = par ? recv : H;
+        bq[ks][1] = par ? Lo : recv;
+      }
+    } else {
+      float qk[32];
+      float mx = 0.0f;
+      const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
+      const uint32_t* qrow = static_cast<const uint32_t*>(qs) + g * (kQRow / 2);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const float2 s01 = *reinterpret_cast<const float2*>(kscale + 16 * ks + 2 * t);
+        const float2 s89 = *reinterpret_cast<const float2*>(kscale + 16 * ks + 2 * t + 8);
+        const uint32_t m01 = kmin2[8 * ks + t];
+        const uint32_t m89 = kmin2[8 * ks + t + 4];
+        const uint32_t q01 = qrow[8 * ks + t], q89 = qrow[8 * ks + t + 4];
+        const float qa = bf2f(q01 & 0xffffu) * c0, qb = bf2f(q01 >> 16) * c0;
+        const float qc = bf2f(q89 & 0xffffu) * c0, qd = bf2f(q89 >> 16) * c0;
+        qk[4 * ks + 0] = qa * s01.x;
+        qk[4 * ks + 1] = qb * s01.y;
+        qk[4 * ks + 2] = qc * s89.x;
+        qk[4 * ks + 3] = qd * s89.y;
+        bias = fmaf(qa, bf2f(m01 & 0xffffu), bias);
+        bias = fmaf(qb, bf2f(m01 >> 16), bias);
+        bias = fmaf(qc, bf2f(m89 & 0xffffu), bias);
+        bias = fmaf(qd, bf2f(m89 >> 16), bias);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fabsf(qk[4 * ks + i]));
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+      bias += __shfl_xor_sync(kFull, bias, 1);
+      bias += __shfl_xor_sync(kFull, bias, 2);
+      pow2_norm(mx, sq, inv_sq);
+      // B' = Q' * sq in [0, 1), times the row factor of its code position;
+      // high part: B' rounded to f16 precision, low part: the rest
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const float f0 = sq * row_factor<KB>(ks, 0), f1 = sq * row_factor<KB>(ks, 1);
@@ -386,17 +415,10 @@ struct Warp {
           hi[i] = round_f16_precision(x[i]);
           lo[i] = x[i] - hi[i];
         }
-        if (SPARE) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) x[i] = low_lane ? lo[i] : hi[i];
-          bq[ks][0] = pack_h2(x[0], x[1]);
-          bq[ks][1] = pack_h2(x[2], x[3]);
-        } else {
-          bq[ks][0] = pack_h2(hi[0], hi[1]);
-          bq[ks][1] = pack_h2(hi[2], hi[3]);
-          bl[ks % NL][0] = pack_h2(lo[0], lo[1]);
-          bl[ks % NL][1] = pack_h2(lo[2], lo[3]);
-        }
+        bq[ks][0] = pack_h2(hi[0], hi[1]);
+        bq[ks][1] = pack_h2(hi[2], hi[3]);
+        bl[ks % NL][0] = pack_h2(lo[0], lo[1]);
+        bl[ks % NL][1] = pack_h2(lo[2], lo[3]);
       }
     }
     // per head of this lane's C columns: the score unit and bias from the
@@ -712,10 +734,9 @@ struct Warp {
   // into the rescaled running output: the running sum of the (always
   // non-negative) code terms never passes through the tensor cores'
   // accumulation, whose truncation would otherwise grow with the context.
-  __device__ __forceinline__ void pv(float (&S)[8][4], const float (&alpha)[2]) {
+  __device__ __forceinline__ void pv(float (&S)[8][4], const float (&alpha)[2], float svn,
+                                     float inv_svm) {
     const RecLayout& L = a.lay;
-    float svn, inv_svm;
-    value_tables(svn, inv_svm);
     // rescale of the running output to this group's units, per head
     float f0, f1;
     {
@@ -1013,15 +1034,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) decode_mma_kernel(MmaArgs a
           W.wait_part(W.mb_v, W.ph_v);        // the value copy in flight
           return;
         }
-        float S[8][4], alpha[2];
-        W.qk_softmax(S, alpha);
-        __syncwarp();                          // key part consumed
+        float S[8][4], hinv[2], hbias[2], alpha[2], svn, inv_svm;
+        W.scores(S, hinv, hbias);
+        __syncwarp();                          // key part (and mixed table) consumed
         if (more) W.issue_k(u, gi + 1);
         if (!W.wait_part(W.mb_v, W.ph_v)) {   // values of gi
           if (more) W.wait_part(W.mb_k, W.ph_k);
           return;
         }
-        W.pv(S, alpha);
+        // the value tables' shared-memory round trip overlaps the softmax
+        W.value_tables(svn, inv_svm);
+        W.softmax_update(S, hinv, hbias, alpha);
+        W.pv(S, alpha, svn, inv_svm);
         __syncwarp();                          // value part consumed
         if (more) W.issue_v(u, gi + 1);
       }
