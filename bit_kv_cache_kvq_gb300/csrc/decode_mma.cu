@@ -243,12 +243,32 @@ struct Warp {
     if (MIX) qg_row = qg + min(hrow(), NREP - 1) * kD;
     const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
     __syncwarp();
-    if (SPARE) {   // fp32 [4][kQRow], pre-scaled
+    if (SPARE) {   // fp32 [4][kQRow], pre-scaled; lane = 16 channels of one head
       float* q = static_cast<float*>(qs);
-      for (int i = lane; i < 4 * kD; i += 32) {
-        const int h = i / kD, c = i % kD;
-        q[h * kQRow + c] = h < NREP ? bf2f(qg[h * kD + c]) * c0 : 0.0f;
+      const int h = lane >> 3, c = (lane & 7) * 16;
+      float v[16];
+      if (h >= NREP) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+      } else if ((reinterpret_cast<uintptr_t>(a.q) & 15) == 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(qg + h * kD + c);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint4 w = __ldg(src + k);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[8 * k + 2 * i] = bf2f(ww[i] & 0xffffu) * c0;
+            v[8 * k + 2 * i + 1] = bf2f(ww[i] >> 16) * c0;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = bf2f(qg[h * kD + c + i]) * c0;
       }
+#pragma unroll
+      for (int i = 0; i < 16; i += 4)
+        *reinterpret_cast<float4*>(q + h * kQRow + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
     } else {       // bf16 [8][kQRow]
       uint32_t* q = static_cast<uint32_t*>(qs);
       for (int i = lane; i < 8 * (kD / 2); i += 32) {
@@ -729,6 +749,42 @@ struct Warp {
     }
   }
 
+  // Channel tile mc (16 channels) of one group's P·V with B fragments bj,
+  // summed in a fresh accumulator and folded into the running output.
+  __device__ __forceinline__ void pv_tile(const uint8_t* vc, int mc, const uint32_t (&bj)[8][2],
+                                          float f0, float f1) {
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (VB == 2) {
+      const uint4 w4 = *reinterpret_cast<const uint4*>(vc + (mc * 32 + lane) * 16);
+      const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t x = wv[w], y = x >> 8;
+        uint32_t A[4];
+        unpack2<0>(x, y, A);
+        mma_f16(acc, A[0], A[1], A[2], A[3], bj[2 * w][0], bj[2 * w][1]);
+        unpack2<1>(x, y, A);
+        mma_f16(acc, A[0], A[1], A[2], A[3], bj[2 * w + 1][0], bj[2 * w + 1][1]);
+      }
+    } else {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint4 w4 = *reinterpret_cast<const uint4*>(vc + ((mc * 2 + hh) * 32 + lane) * 16);
+        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t A[4];
+          unpack4(wv[i], wv[i] >> 8, A);
+          mma_f16(acc, A[0], A[1], A[2], A[3], bj[4 * hh + i][0], bj[4 * hh + i][1]);
+        }
+      }
+    }
+    O[mc][0] = fmaf(O[mc][0], f0, acc[0]);
+    O[mc][2] = fmaf(O[mc][2], f0, acc[2]);
+    O[mc][1] = fmaf(O[mc][1], f1, acc[1]);
+    O[mc][3] = fmaf(O[mc][3], f1, acc[3]);
+  }
+
   // P·V of one group (values in vbuf) into the running output.  Each
   // channel tile sums the group in a fresh accumulator and one FFMA folds it
   // into the rescaled running output: the running sum of the (always
@@ -768,49 +824,36 @@ struct Warp {
       mma_f16(Dvm, a0, 0u, a2, 0u, pb[kt][0], pb[kt][1]);
     }
     const uint8_t* vc = vbuf + (L.v_codes - L.kpart);
+    if constexpr (SPARE) {
+      // B columns 4..7 repeat heads 0..3, so they carry the next channel
+      // group's P': one set of B fragments serves groups 2jp and 2jp + 1
+      // (their channel tiles keep the results of columns 0..3 and 4..7).
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      // P' = p * step of this channel group (with the row factors)
-      uint32_t bj[8][2];
+      for (int jp = 0; jp < 2; ++jp) {
+        const int jl = 2 * jp + (g >> 2);
+        uint32_t bj[8][2];
 #pragma unroll
-      for (int kt = 0; kt < 8; ++kt) {
-        const uint2 vs = *reinterpret_cast<const uint2*>(vsb + vsb_index(kt, t, j, 0));
-        bj[kt][0] = hmul2_u(pb[kt][0], vs.x);
-        bj[kt][1] = hmul2_u(pb[kt][1], vs.y);
-      }
-#pragma unroll
-      for (int mm = 0; mm < 2; ++mm) {
-        const int mc = 2 * j + mm;
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (VB == 2) {
-          const uint4 w4 = *reinterpret_cast<const uint4*>(vc + (mc * 32 + lane) * 16);
-          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const uint32_t x = wv[w], y = x >> 8;
-            uint32_t A[4];
-            unpack2<0>(x, y, A);
-            mma_f16(acc, A[0], A[1], A[2], A[3], bj[2 * w][0], bj[2 * w][1]);
-            unpack2<1>(x, y, A);
-            mma_f16(acc, A[0], A[1], A[2], A[3], bj[2 * w + 1][0], bj[2 * w + 1][1]);
-          }
-        } else {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint4 w4 = *reinterpret_cast<const uint4*>(vc + ((mc * 2 + hh) * 32 + lane) * 16);
-            const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint32_t A[4];
-              unpack4(wv[i], wv[i] >> 8, A);
-              mma_f16(acc, A[0], A[1], A[2], A[3], bj[4 * hh + i][0], bj[4 * hh + i][1]);
-            }
-          }
+        for (int kt = 0; kt < 8; ++kt) {
+          const uint2 vs = *reinterpret_cast<const uint2*>(vsb + vsb_index(kt, t, jl, 0));
+          bj[kt][0] = hmul2_u(pb[kt][0], vs.x);
+          bj[kt][1] = hmul2_u(pb[kt][1], vs.y);
         }
-        O[mc][0] = fmaf(O[mc][0], f0, acc[0]);
-        O[mc][2] = fmaf(O[mc][2], f0, acc[2]);
-        O[mc][1] = fmaf(O[mc][1], f1, acc[1]);
-        O[mc][3] = fmaf(O[mc][3], f1, acc[3]);
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) pv_tile(vc, 4 * jp + mm, bj, f0, f1);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        // P' = p * step of this channel group (with the row factors)
+        uint32_t bj[8][2];
+#pragma unroll
+        for (int kt = 0; kt < 8; ++kt) {
+          const uint2 vs = *reinterpret_cast<const uint2*>(vsb + vsb_index(kt, t, j, 0));
+          bj[kt][0] = hmul2_u(pb[kt][0], vs.x);
+          bj[kt][1] = hmul2_u(pb[kt][1], vs.y);
+        }
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm) pv_tile(vc, 2 * j + mm, bj, f0, f1);
       }
     }
     // origin term in true units (lanes g < 4 hold channel group j = g)
@@ -980,10 +1023,13 @@ struct Warp {
         const int mc = 2 * j + mm;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int h = 2 * t + (c & 1);
+          // with at most 4 heads, channel groups of odd j keep columns 4..7
+          // (lanes t >= 2), which hold heads 2t - 4 and 2t - 3
+          const int h = SPARE ? ((2 * t + (c & 1)) & 3) : 2 * t + (c & 1);
+          const bool mine = !SPARE || ((j & 1) ? t >= 2 : t < 2);
           const int ch = 16 * mc + g + 8 * (c >> 1);
           const float val = O[mc][c] * (inv_sv * kCodeUnit) + ((c & 1) ? vm1 : vm0);
-          if (h < NREP) base[h * (kD + 2) + ch] = val;
+          if (mine && h < NREP) base[h * (kD + 2) + ch] = val;
         }
       }
     }
@@ -1022,12 +1068,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) decode_mma_kernel(MmaArgs a
     const bool res = a.r > 0 && lo <= a.n_groups && a.n_groups < hi;
     const int ps = a.n_groups + (a.r > 0 ? 1 : 0);   // position of the sink item
     const bool snk = a.s > 0 && lo <= ps && ps < hi;
-    W.begin_unit(u);
+    // keys of group i+1 load during the P·V of group i, values of group
+    // i+1 during its QK: one bulk copy and one mbarrier per part.  The
+    // unit's first group is requested before its query is read.
     if (g0 < g1) {
-      // keys of group i+1 load during the P·V of group i, values of group
-      // i+1 during its QK: one bulk copy and one mbarrier per part.
       W.issue_k(u, g0);
       W.issue_v(u, g0);
+    }
+    W.begin_unit(u);
+    if (g0 < g1) {
       for (int gi = g0; gi < g1; ++gi) {
         const bool more = gi + 1 < g1;
         if (!W.wait_part(W.mb_k, W.ph_k)) {   // keys of gi (bounded wait)
