@@ -253,8 +253,7 @@ int kvq_quantize_prefill(kvq_cache* c, const kvq_bf16* k, const kvq_bf16* v, int
 
 size_t kvq_decode_workspace_bytes(const kvq_cache* c, int Hq) {
   if (!c || Hq < 1 || Hq % c->cfg.kv_heads) return 0;
-  return mma_ws_bytes(c->num_sms, c->cfg.batch, c->cfg.kv_heads, Hq, c->max_groups,
-                      c->lay.bytes);
+  return mma_ws_bytes(c->num_sms, c->cfg.batch, c->cfg.kv_heads, Hq, c->max_groups, c->lay);
 }
 
 static bool valid_rep(int Hq, int Hkv) {
@@ -272,7 +271,7 @@ int kvq_decode_attention(const kvq_cache* c, const kvq_bf16* q, int Hq, float* o
     return KVQ_ERR_WORKSPACE;
   MmaPlan plan;
   if (!mma_plan(c->num_sms, c->cfg.batch * c->cfg.kv_heads, Hq / c->cfg.kv_heads,
-                c->t_q / kKG, c->r, c->s, c->lay.bytes, ws_bytes, &plan))
+                c->t_q / kKG, c->r, c->s, c->lay, ws_bytes, &plan))
     return KVQ_ERR_WORKSPACE;
   return cuda_status(launch_decode_mma(c, q, Hq, out, static_cast<float*>(ws), plan, s));
 }

@@ -54,22 +54,37 @@ constexpr float kCodeUnit = 512.0f;      // 2^9: products carry c * B' / 2^9
 constexpr float kInvCodeUnit = 1.0f / 512.0f;
 
 // Per-warp shared memory after the record buffer (key part, then value
-// part): the value-step table (256 words), the value-origin table (4 rows of
-// 72 words) and the unit's query, [8 heads][136] bf16 or, with at most 4
-// heads per KV head, [4 heads][136] fp32 pre-scaled by log2(e)/sqrt(D)
-// (rows padded so head rows fall in different banks).  The padding of the
-// first row, never read as query, holds the 16 zero bytes ldmatrix reads
-// for absent rows.
+// part): with mixed keys the value-step table (256 words) and the
+// value-origin table (4 rows of 72 words), then the unit's query, [8
+// heads][136] bf16 or, with at most 4 heads per KV head, [4 heads][136] fp32
+// pre-scaled by log2(e)/sqrt(D) (rows padded so head rows fall in different
+// banks).  The padding of the first row, never read as query, holds the 16
+// zero bytes ldmatrix reads for absent rows.  With uniform keys the two
+// value tables are built in place over the staged value steps and origins
+// they are computed from (3072 bytes, read into registers first).
 constexpr int kVsbBytes = 256 * 4;
 constexpr int kVmbBytes = 4 * 72 * 4;
 constexpr int kQRow = 136;
 constexpr int kQBytes = 8 * kQRow * 2;   // = 4 * kQRow * 4
+static_assert(kVsbBytes + kVmbBytes <= 4 * kKG * kVGroups + 2 * kKG * kVGroups,
+              "value tables must fit over the staged value metadata");
 // Per-warp regions stay multiples of 128 bytes: cp.async copies of 128-byte
 // aligned record lines into misaligned shared memory cost ~10% of the
 // decode time.
-constexpr int kWarpExtra = kVsbBytes + kVmbBytes + kQBytes;
-static_assert(kWarpExtra % 128 == 0, "per-warp extra must keep 128-byte alignment");
-constexpr int kMaxWarps = 12;           // warps per block: up to 168 registers a thread
+__host__ __device__ constexpr int warp_extra(bool mix) {
+  return (mix ? kVsbBytes + kVmbBytes : 0) + kQBytes;
+}
+static_assert(warp_extra(false) % 128 == 0 && warp_extra(true) % 128 == 0,
+              "per-warp extra must keep 128-byte alignment");
+// Warps per block.  Two-bit uniform records with at most 4 query heads per
+// KV head fit 16 warps (4 per scheduler, up to 128 registers a thread) in
+// shared memory; the other variants run 12 (up to 168 registers).
+#ifndef KVQ_UNIFORM_WARPS
+#define KVQ_UNIFORM_WARPS 16
+#endif
+__host__ __device__ constexpr int max_warps(int kb, int vb, int nrep, bool mix) {
+  return (!mix && kb == 2 && vb == 2 && nrep <= 4) ? KVQ_UNIFORM_WARPS : 12;
+}
 
 // Swizzled positions in the per-warp value tables (u32 index), chosen so
 // both the writers (lane = 4 tokens) and the readers (lane = fragment
@@ -181,7 +196,11 @@ struct Warp {
   float qmax;      // max |query| of the head row this lane builds B columns for
 
   // online-softmax state (heads 2t, 2t+1 of this lane)
-  float O[8][4];   // running O^T in units of sv / 2^9 (channel tiles mc = 0..7)
+  // Running O^T in units of sv / 2^9: channel tiles mc = 0..7, or with at
+  // most 4 heads only the 4 tiles whose accumulator columns this lane keeps
+  // (tile_of: channel groups of odd j keep columns 4..7, lanes t >= 2).
+  static constexpr int NO = SPARE ? 4 : 8;
+  float O[NO][4];
   float vm[2];     // origin term (lanes g < 4: channel group j = g)
   float mrun[2], lrun[2];
   float sv, inv_sv;  // current units of O
@@ -191,9 +210,10 @@ struct Warp {
     const int rb = static_cast<int>(a.rec_bytes);
     kbuf = base;
     vbuf = base + a.lay.kpart;
-    vsb = reinterpret_cast<uint32_t*>(base + rb);
-    vmb = reinterpret_cast<uint32_t*>(base + rb + kVsbBytes);
-    qs = base + rb + kVsbBytes + kVmbBytes;
+    uint8_t* tables = MIX ? base + rb : vbuf + (a.lay.v_scale - a.lay.kpart);
+    vsb = reinterpret_cast<uint32_t*>(tables);
+    vmb = reinterpret_cast<uint32_t*>(tables + kVsbBytes);
+    qs = base + rb + (MIX ? kVsbBytes + kVmbBytes : 0);
     // the two mbarriers sit in the padding of query row 1
     mb_k = static_cast<uint32_t>(__cvta_generic_to_shared(qs)) + (SPARE ? (kQRow + kD) * 4 : (kQRow + kD) * 2);
     mb_v = mb_k + 8;
@@ -213,6 +233,11 @@ struct Warp {
   // of 136; bf16 rows: 128 of 136)
   __device__ __forceinline__ uint8_t* zero_row() const {
     return static_cast<uint8_t*>(qs) + (SPARE ? kD * 4 : kD * 2);
+  }
+
+  // Channel tile of output slot i (see O).
+  __device__ __forceinline__ int tile_of(int i) const {
+    return SPARE ? 4 * (i >> 1) + (i & 1) + 2 * (t >> 1) : i;
   }
 
   // Query head of the B column this lane builds (column g): with at most 4
@@ -286,7 +311,7 @@ struct Warp {
       qmax = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
     }
 #pragma unroll
-    for (int m = 0; m < 8; ++m)
+    for (int m = 0; m < NO; ++m)
 #pragma unroll
       for (int c = 0; c < 4; ++c) O[m][c] = 0.0f;
     sv = kSentinel;
@@ -300,11 +325,14 @@ struct Warp {
   // copy issued by lane 0, completing on mbarrier mb (the warp has read
   // dst's previous contents: __syncwarp before, then the proxy fence).
   __device__ __forceinline__ void issue(int u, int grp, uint8_t* dst, int lo, int hi, uint32_t mb) {
+    // every lane orders its earlier shared-memory accesses (reads of the
+    // buffer, the in-place tables) before the copy that overwrites them
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    __syncwarp();
     if (lane == 0) {
       const uint8_t* src = a.records + (static_cast<long long>(u) * a.max_groups + grp) * a.rec_bytes + lo;
       const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
       const uint32_t bytes = static_cast<uint32_t>(hi - lo);
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mb), "r"(bytes)
                    : "memory");
       asm volatile(
@@ -728,6 +756,8 @@ struct Warp {
     // (steps are >= 0, so their bit patterns order like their values)
     mx = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(mx)));
     mm = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(mm)));
+    // uniform keys: the tables overwrite the metadata every lane has read
+    if (!MIX) __syncwarp();
     float s_new, inv_new, svm;
     pow2_norm(mx, s_new, inv_new);
     (void)inv_new;
@@ -750,10 +780,11 @@ struct Warp {
   }
 
   // Channel tile mc (16 channels) of one group's P·V with B fragments bj,
-  // summed in a fresh accumulator and folded into the running output.
+  // summed in a fresh accumulator acc.
   __device__ __forceinline__ void pv_tile(const uint8_t* vc, int mc, const uint32_t (&bj)[8][2],
-                                          float f0, float f1) {
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                                          float (&acc)[4]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[c] = 0.0f;
     if (VB == 2) {
       const uint4 w4 = *reinterpret_cast<const uint4*>(vc + (mc * 32 + lane) * 16);
       const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
@@ -779,10 +810,13 @@ struct Warp {
         }
       }
     }
-    O[mc][0] = fmaf(O[mc][0], f0, acc[0]);
-    O[mc][2] = fmaf(O[mc][2], f0, acc[2]);
-    O[mc][1] = fmaf(O[mc][1], f1, acc[1]);
-    O[mc][3] = fmaf(O[mc][3], f1, acc[3]);
+  }
+  // One FFMA per accumulator folds a group's tile into the rescaled output.
+  __device__ __forceinline__ void fold(int i, const float (&acc)[4], float f0, float f1) {
+    O[i][0] = fmaf(O[i][0], f0, acc[0]);
+    O[i][2] = fmaf(O[i][2], f0, acc[2]);
+    O[i][1] = fmaf(O[i][1], f1, acc[1]);
+    O[i][3] = fmaf(O[i][3], f1, acc[3]);
   }
 
   // P·V of one group (values in vbuf) into the running output.  Each
@@ -838,8 +872,18 @@ struct Warp {
           bj[kt][0] = hmul2_u(pb[kt][0], vs.x);
           bj[kt][1] = hmul2_u(pb[kt][1], vs.y);
         }
+        // tiles 4jp + k (group 2jp, columns 0..3) and 4jp + k + 2 (group
+        // 2jp + 1, columns 4..7): each lane keeps the one of its columns
+        const bool hi = t >= 2;
 #pragma unroll
-        for (int mm = 0; mm < 4; ++mm) pv_tile(vc, 4 * jp + mm, bj, f0, f1);
+        for (int k = 0; k < 2; ++k) {
+          float acc_e[4], acc_o[4], acc[4];
+          pv_tile(vc, 4 * jp + k, bj, acc_e);
+          pv_tile(vc, 4 * jp + k + 2, bj, acc_o);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[c] = hi ? acc_o[c] : acc_e[c];
+          fold(2 * jp + k, acc, f0, f1);
+        }
       }
     } else {
 #pragma unroll
@@ -853,7 +897,11 @@ struct Warp {
           bj[kt][1] = hmul2_u(pb[kt][1], vs.y);
         }
 #pragma unroll
-        for (int mm = 0; mm < 2; ++mm) pv_tile(vc, 2 * j + mm, bj, f0, f1);
+        for (int mm = 0; mm < 2; ++mm) {
+          float acc[4];
+          pv_tile(vc, 2 * j + mm, bj, acc);
+          fold(2 * j + mm, acc, f0, f1);
+        }
       }
     }
     // origin term in true units (lanes g < 4 hold channel group j = g)
@@ -949,7 +997,7 @@ struct Warp {
         inv_sv = 1.0f;
       }
 #pragma unroll
-      for (int mc = 0; mc < 8; ++mc) {
+      for (int mc = 0; mc < NO; ++mc) {
         O[mc][0] *= alpha[0]; O[mc][2] *= alpha[0];
         O[mc][1] *= alpha[1]; O[mc][3] *= alpha[1];
       }
@@ -983,17 +1031,27 @@ struct Warp {
         asm volatile("cp.async.wait_group 1;\n" ::);
         __syncwarp();
         const int row = (lane & 7) + 8 * (lane >> 4);
+        const float sc = sv * kInvCodeUnit;
+        float acc8[8][4];
 #pragma unroll
         for (int mc = 0; mc < 8; ++mc) {
           uint32_t A[4];
           ldsm_x4_t(A, chunk_addr(c & 1, row, 2 * mc + ((lane >> 3) & 1)));
           A[0] &= m01; A[1] &= m01; A[2] &= m89; A[3] &= m89;
-          float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          mma_bf16(acc, A, ph[0], ph[1]);
-          mma_bf16(acc, A, pl[0], pl[1]);
-          const float sc = sv * kInvCodeUnit;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) O[mc][i] = fmaf(acc[i], sc, O[mc][i]);
+          for (int i = 0; i < 4; ++i) acc8[mc][i] = 0.0f;
+          mma_bf16(acc8[mc], A, ph[0], ph[1]);
+          mma_bf16(acc8[mc], A, pl[0], pl[1]);
+        }
+#pragma unroll
+        for (int k = 0; k < NO; ++k) {
+          // with at most 4 heads: the tile of this lane's kept columns
+          const int me = SPARE ? 4 * (k >> 1) + (k & 1) : k;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float v = SPARE ? (t >= 2 ? acc8[me + 2][i] : acc8[me][i]) : acc8[me][i];
+            O[k][i] = fmaf(v, sc, O[k][i]);
+          }
         }
         __syncwarp();   // slot read before it is staged again
       }
@@ -1015,22 +1073,18 @@ struct Warp {
     }
     float* base = a.ws + (static_cast<long long>(u) * a.max_parts + part) * NREP * (kD + 2);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int i = 0; i < NO; ++i) {
+      // with at most 4 heads, the tiles of odd channel groups keep columns
+      // 4..7 (lanes t >= 2), which hold heads 2t - 4 and 2t - 3
+      const int mc = tile_of(i), j = mc >> 1;
       const float vm0 = __shfl_sync(kFull, vm[0], 4 * j + t);
       const float vm1 = __shfl_sync(kFull, vm[1], 4 * j + t);
 #pragma unroll
-      for (int mm = 0; mm < 2; ++mm) {
-        const int mc = 2 * j + mm;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          // with at most 4 heads, channel groups of odd j keep columns 4..7
-          // (lanes t >= 2), which hold heads 2t - 4 and 2t - 3
-          const int h = SPARE ? ((2 * t + (c & 1)) & 3) : 2 * t + (c & 1);
-          const bool mine = !SPARE || ((j & 1) ? t >= 2 : t < 2);
-          const int ch = 16 * mc + g + 8 * (c >> 1);
-          const float val = O[mc][c] * (inv_sv * kCodeUnit) + ((c & 1) ? vm1 : vm0);
-          if (mine && h < NREP) base[h * (kD + 2) + ch] = val;
-        }
+      for (int c = 0; c < 4; ++c) {
+        const int h = SPARE ? ((2 * t + (c & 1)) & 3) : 2 * t + (c & 1);
+        const int ch = 16 * mc + g + 8 * (c >> 1);
+        const float val = O[i][c] * (inv_sv * kCodeUnit) + ((c & 1) ? vm1 : vm0);
+        if (h < NREP) base[h * (kD + 2) + ch] = val;
       }
     }
     if (SPARE) {   // lane (0, t): head t
@@ -1050,14 +1104,14 @@ struct Warp {
 };
 
 template <int KB, int VB, int NREP, bool MIX>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) decode_mma_kernel(MmaArgs a) {
+__global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX) * 32, 1) decode_mma_kernel(MmaArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int slot = blockIdx.x * (blockDim.x >> 5) + warp;
   // the combine kernel may be scheduled now; it waits for this grid's results
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   if (slot >= a.n_slots) return;            // warp-uniform
-  uint8_t* mine = smem + static_cast<size_t>(warp) * (a.rec_bytes + kWarpExtra);
+  uint8_t* mine = smem + static_cast<size_t>(warp) * (a.rec_bytes + warp_extra(MIX));
   Warp<KB, VB, NREP, MIX> W(a, mine);
   const long long p0 = slot_start(a, slot), p1 = slot_start(a, slot + 1);
   for (int u = static_cast<int>(p0 / a.unit_len); u <= static_cast<int>((p1 - 1) / a.unit_len); ++u) {
@@ -1165,7 +1219,7 @@ __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restr
 
 template <int KB, int VB, int NREP, bool MIX>
 cudaError_t launch_cfg(const MmaArgs& a, int warps, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(warps) * (a.rec_bytes + kWarpExtra);
+  const size_t smem = static_cast<size_t>(warps) * (a.rec_bytes + warp_extra(MIX));
   auto kern = decode_mma_kernel<KB, VB, NREP, MIX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -1188,19 +1242,20 @@ cudaError_t launch_rep(const MmaArgs& a, int nrep, int warps, cudaStream_t s) {
 
 }  // namespace
 
-int mma_warps_per_cta(int rec_bytes) {
-  // one record buffer plus the tables and the query per warp, within the
-  // 227 KB of shared memory a block may use; at most 12 warps so a thread
-  // keeps up to 168 registers
-  const int per = rec_bytes + kWarpExtra;
-  return max(1, min(kMaxWarps, (227 * 1024) / per));
+int mma_warps_per_cta(const RecLayout& lay, int n_rep) {
+  // one record buffer plus the query (and, with mixed keys, the tables) per
+  // warp, within the 227 KB of shared memory a block may use, and at most
+  // the variant's register-bound warp count
+  const bool mix = lay.mixed != 0;
+  const int per = lay.bytes + warp_extra(mix);
+  return max(1, min(max_warps(lay.kb, lay.vb, n_rep, mix), (227 * 1024) / per));
 }
 
-bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int sink, int rec_bytes,
-              size_t ws_cap, MmaPlan* plan) {
+bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int sink,
+              const RecLayout& lay, size_t ws_cap, MmaPlan* plan) {
   plan->unit_len = n_groups + (r > 0 ? kResidualWeight : 0) + (sink > 0 ? kResidualWeight : 0);
   const long long total = static_cast<long long>(units) * plan->unit_len;
-  const long long resident = static_cast<long long>(num_sms) * mma_warps_per_cta(rec_bytes);
+  const long long resident = static_cast<long long>(num_sms) * mma_warps_per_cta(lay, n_rep);
   long long slots = total < resident ? total : resident;
   if (ws_cap) {
     // each unit's positions meet at most ceil(slots / units) + 1 slots
@@ -1215,11 +1270,11 @@ bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int sink, 
   return true;
 }
 
-size_t mma_ws_bytes(int num_sms, int B, int Hkv, int Hq, int max_groups, int rec_bytes) {
+size_t mma_ws_bytes(int num_sms, int B, int Hkv, int Hq, int max_groups, const RecLayout& lay) {
   // worst case over the lengths this cache can hold: one warp slot per
   // weighted position or all resident warps, whichever is fewer
   const int units = B * Hkv;
-  const long long resident = static_cast<long long>(num_sms) * mma_warps_per_cta(rec_bytes);
+  const long long resident = static_cast<long long>(num_sms) * mma_warps_per_cta(lay, Hq / Hkv);
   const long long per_unit = (resident + units - 1) / units + 2;
   const long long cap = static_cast<long long>(max_groups) + 2 * kResidualWeight + 1;
   const long long parts = per_unit < cap ? per_unit : cap;
@@ -1270,7 +1325,7 @@ cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, flo
   a.status = c->status;
   const int nrep = Hq / c->cfg.kv_heads;
   const int kb = c->cfg.k_bits, vb = c->cfg.v_bits;
-  const int warps = mma_warps_per_cta(c->lay.bytes);
+  const int warps = mma_warps_per_cta(c->lay, nrep);
   cudaError_t e;
   if (c->cfg.k_mode == KVQ_K_MIXED) {
     if (vb == 2) e = launch_rep<2, 2, true>(a, nrep, warps, s);

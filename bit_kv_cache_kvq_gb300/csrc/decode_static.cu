@@ -58,7 +58,7 @@ extern "C" int kvq_decode_attention_static(const kvq_cache* c, const kvq_bf16* q
   // fit with two partial slots per (batch row, KV head).
   MmaPlan plan;
   if (!mma_plan(c->num_sms, c->cfg.batch * c->cfg.kv_heads, n_rep, c->t_q / kKG, c->r, c->s,
-                c->lay.bytes, KVQ_STATIC_WORKSPACE_BYTES, &plan))
+                c->lay, KVQ_STATIC_WORKSPACE_BYTES, &plan))
     return KVQ_ERR_WORKSPACE;
 
   int dev = 0;

@@ -174,11 +174,11 @@ struct MmaPlan {
   int n_slots;
   int max_parts;
 };
-int mma_warps_per_cta(int rec_bytes);
+int mma_warps_per_cta(const RecLayout& lay, int n_rep);
 // false if even two partial slots per unit exceed ws_cap (0 = no cap)
-bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int sink, int rec_bytes,
-              size_t ws_cap, MmaPlan* plan);
-size_t mma_ws_bytes(int num_sms, int B, int Hkv, int Hq, int max_groups, int rec_bytes);
+bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int sink,
+              const RecLayout& lay, size_t ws_cap, MmaPlan* plan);
+size_t mma_ws_bytes(int num_sms, int B, int Hkv, int Hq, int max_groups, const RecLayout& lay);
 cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, float* out,
                               float* ws, const MmaPlan& plan, cudaStream_t s);
 // Merge split-K partials [units][max_parts][n_rep][D + 2] (o, m, l) of the
