@@ -1163,7 +1163,7 @@ __global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX) * 32, 1) decode_m
 // channel) with the log-sum-exp rule: M = max m_k, w_k = 2^(m_k - M),
 // o = sum w_k o_k / sum w_k l_k.  Every warp takes the weights itself (lane
 // k % 32 holds part k's), so no block barrier is needed, and the values of
-// the first 16 parts load together with the maxima: for up to 16 parts the
+// the first 32 parts load together with the maxima: for up to 32 parts the
 // merge is one round trip to memory.  Launched as a programmatic dependent
 // of the decode kernel: it may start while that kernel drains and waits for
 // its results with griddepcontrol.wait.
@@ -1171,7 +1171,7 @@ __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restr
                                                            int Hkv, int Hq, int max_parts,
                                                            long long unit_len, long long total,
                                                            int n_slots, float* __restrict__ out) {
-  constexpr int kEarly = 16;
+  constexpr int kEarly = 32;
   const int row = blockIdx.x;                 // b * Hq + hq
   const int n_rep = Hq / Hkv;
   const int b = row / Hq, hq = row % Hq;
@@ -1198,9 +1198,6 @@ __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restr
   float L = w * l0, O = 0.0f;
 #pragma unroll
   for (int j = 0; j < kEarly; ++j) O = fmaf(__shfl_sync(kFull, w, j), o[j], O);
-  const int n32 = min(n, 32);
-#pragma unroll 4
-  for (int j = kEarly; j < n32; ++j) O = fmaf(__shfl_sync(kFull, w, j), base[j * stride + c], O);
   // parts 32 and up, 32 at a time
   for (int k0 = 32; k0 < n; k0 += 32) {
     const int k = k0 + lane;
@@ -1284,6 +1281,12 @@ size_t mma_ws_bytes(int num_sms, int B, int Hkv, int Hq, int max_groups, const R
 cudaError_t launch_combine_parts(const float* ws, int B, int Hkv, int Hq, int max_parts,
                                  long long unit_len, long long total, int n_slots, float* out,
                                  cudaStream_t s) {
+  // the combine's blocks land on SMs configured for the decode grid's
+  // shared memory: ask for the same split so none has to reconfigure
+  static const cudaError_t carve = cudaFuncSetAttribute(
+      combine_parts_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+      cudaSharedmemCarveoutMaxShared);
+  if (carve != cudaSuccess) return carve;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(B * Hq);
   lc.blockDim = dim3(kD);

@@ -707,6 +707,11 @@ cudaError_t set_smem(K kernel, int bytes) {
 cudaError_t launch_append(const kvq_cache* c, const kvq_bf16* k_new, const kvq_bf16* v_new,
                           kvq_bf16* dst_k, kvq_bf16* dst_v, int cap, int slot, cudaStream_t s) {
   const int units = c->cfg.batch * c->cfg.kv_heads;
+  // same shared-memory split as the decode grid that usually follows
+  static const cudaError_t carve = cudaFuncSetAttribute(
+      append_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+      cudaSharedmemCarveoutMaxShared);
+  if (carve != cudaSuccess) return carve;
   append_kernel<<<units, 32, 0, s>>>(reinterpret_cast<const uint4*>(k_new),
                                      reinterpret_cast<const uint4*>(v_new),
                                      reinterpret_cast<uint4*>(dst_k),
