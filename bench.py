@@ -44,12 +44,12 @@ FALLBACK_HBM_GBS = 6800.0
 # launch, from the ncu capture of this workload at batch 8 kept under
 # profiles/, keyed by the sha256 of the decode kernel source it was taken on
 # (a stale entry reports null).  The capture ran at batch 8 (64 units,
-# 32768 + 100 tokens): 200.963 MB read + 3.282 MB written against 200.884 MB
-# of algorithmic bytes (ratio 1.0167: mostly the split-K partials written).
+# 32768 + 100 tokens): 201.241 MB read + 5.844 MB written against 200.884 MB
+# of algorithmic bytes (ratio 1.0309: mostly the split-K partials written).
 # Traffic per unit is independent of the batch, so the batch-16 launch is
 # that ratio times its algorithmic bytes at the timed steps' mean context.
 NCU_TRAFFIC = {
-    "cfff8f26d15dd5ea": {("llama8b_gqa_32k_b16", 16, 32768, 2): 204.244992 / 200.884224 * 399.264512e6},
+    "3c86e86ed8c5ab05": {("llama8b_gqa_32k_b16", 16, 32768, 2): 207.084800 / 200.884224 * 399.264512e6},
 }
 
 
@@ -67,6 +67,9 @@ def parse_args():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-bf16", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--sweep", action="store_true",
+                   help="long-context sweep: one JSON line per context x batch x bits point "
+                        "(decode steps and the bf16 comparator; no e2e or CPU legs)")
     return p.parse_args()
 
 
@@ -199,8 +202,12 @@ def rank_workload(w, rank: int):
 
 # ---------------------------------------------------------------- arms
 def workload_from(args):
-    from bit_kv_cache_kvq_gb300.workloads import WORKLOADS, scaled
-    w = WORKLOADS[args.workload]
+    from bit_kv_cache_kvq_gb300.workloads import WORKLOADS, scaled, sweep_workload
+    if args.workload.startswith("sweep_c"):      # sweep_c<context>_b<batch>_k<bits>
+        c, b, k = (int(x[1:]) for x in args.workload[len("sweep_"):].split("_"))
+        w = sweep_workload(c, b, k)
+    else:
+        w = WORKLOADS[args.workload]
     ch = {}
     if args.batch:
         ch["B"] = args.batch
@@ -520,6 +527,27 @@ def _cpu_model():
     return platform.machine()
 
 
+def run_sweep(args, rank, world):
+    """The long-context sweep (Llama-8B GQA shape, 32 q / 8 kv heads): every
+    context x batch point at 2 and 4 bits that fits, each its own line."""
+    import copy
+    import torch
+    from bit_kv_cache_kvq_gb300.workloads import SWEEP_BATCHES, SWEEP_CONTEXTS
+    for bits in (2, 4):
+        for c in SWEEP_CONTEXTS:
+            for b in SWEEP_BATCHES:
+                a = copy.copy(args)
+                a.workload = f"sweep_c{c}_b{b}_k{bits}"
+                a.batch = a.context = a.bits = 0
+                a.no_e2e = a.no_cpu = True
+                a.no_bf16 = args.no_bf16 or bits != 2     # bf16 comparator once per point
+                line = run_ours(a, rank, world)
+                if rank == 0 and line is not None:
+                    print(json.dumps(line), flush=True)
+                del line
+                torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -532,9 +560,12 @@ def main():
             dist.init_process_group("nccl")
         else:
             dist.init_process_group("gloo")
-    line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
-    if rank == 0 and line is not None:
-        print(json.dumps(line), flush=True)
+    if args.sweep and args.impl == "ours":
+        run_sweep(args, rank, world)
+    else:
+        line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
