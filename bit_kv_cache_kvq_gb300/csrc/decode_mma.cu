@@ -1214,6 +1214,87 @@ __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restr
   out[static_cast<long long>(row) * kD + c] = O / L;
 }
 
+// The same merge for rows with many partials (small batches split over
+// the whole GPU): 8 warps per query head, warp w merging parts w, w + 8, ...
+// with eight parts' values in flight per lane (lane = channels 2l, 2l + 1,
+// 64 + 2l, 65 + 2l), then the warps' (M, L, O) merge through shared memory
+// by the same rule.
+constexpr int kManyWarps = 8;
+__global__ void __launch_bounds__(kManyWarps * 32) combine_many_kernel(
+    const float* __restrict__ ws, int Hkv, int Hq, int max_parts, long long unit_len,
+    long long total, int n_slots, float* __restrict__ out) {
+  __shared__ float sO[kManyWarps][kD];
+  __shared__ float sM[kManyWarps], sL[kManyWarps];
+  const int row = blockIdx.x;                 // b * Hq + hq
+  const int n_rep = Hq / Hkv;
+  const int b = row / Hq, hq = row % Hq;
+  const int u = b * Hkv + hq / n_rep, h = hq % n_rep;
+  const long long ub = static_cast<long long>(u) * unit_len;
+  const int first = static_cast<int>(((ub + 1) * n_slots - 1) / total);
+  const int last = static_cast<int>(((ub + unit_len) * n_slots - 1) / total);
+  const int n = last - first + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* base = ws + static_cast<long long>(u) * max_parts * n_rep * (kD + 2) + h * (kD + 2);
+  const long long stride = static_cast<long long>(n_rep) * (kD + 2);
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  // this warp's parts: k = warp + kManyWarps * i
+  float M = -INFINITY;
+  for (int k = warp + kManyWarps * lane; k < n; k += kManyWarps * 32)
+    M = fmaxf(M, base[k * stride + kD]);
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
+  float L = 0.0f;
+  float2 o0 = make_float2(0.0f, 0.0f), o1 = make_float2(0.0f, 0.0f);
+  for (int i0 = 0; warp + kManyWarps * i0 < n; i0 += 32) {
+    const int k = warp + kManyWarps * (i0 + lane);
+    const float mk = k < n ? base[k * stride + kD] : -INFINITY;
+    const float wk = mk == -INFINITY ? 0.0f : exp2f(mk - M);
+    L = fmaf(wk, k < n ? base[k * stride + kD + 1] : 0.0f, L);
+    const int cnt = min(32, (n - warp + kManyWarps - 1) / kManyWarps - i0);
+    for (int j0 = 0; j0 < cnt; j0 += 8) {
+      float2 a[8], c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float* pj = base + static_cast<long long>(warp + kManyWarps * (i0 + j0 + j)) * stride;
+        const bool ok = j0 + j < cnt;
+        a[j] = ok ? *reinterpret_cast<const float2*>(pj + 2 * lane) : make_float2(0.0f, 0.0f);
+        c[j] = ok ? *reinterpret_cast<const float2*>(pj + 64 + 2 * lane) : make_float2(0.0f, 0.0f);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float wj = __shfl_sync(kFull, wk, (j0 + j) & 31);
+        o0.x = fmaf(wj, a[j].x, o0.x); o0.y = fmaf(wj, a[j].y, o0.y);
+        o1.x = fmaf(wj, c[j].x, o1.x); o1.y = fmaf(wj, c[j].y, o1.y);
+      }
+    }
+  }
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) L += __shfl_xor_sync(kFull, L, x);
+  sO[warp][2 * lane] = o0.x;
+  sO[warp][2 * lane + 1] = o0.y;
+  sO[warp][64 + 2 * lane] = o1.x;
+  sO[warp][65 + 2 * lane] = o1.y;
+  if (lane == 0) {
+    sM[warp] = M;
+    sL[warp] = L;
+  }
+  __syncthreads();
+  if (threadIdx.x < kD) {
+    const int ch = threadIdx.x;
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kManyWarps; ++w) Mx = fmaxf(Mx, sM[w]);
+    float O = 0.0f, Lt = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kManyWarps; ++w) {
+      const float f = sM[w] == -INFINITY ? 0.0f : exp2f(sM[w] - Mx);
+      O = fmaf(f, sO[w][ch], O);
+      Lt = fmaf(f, sL[w], Lt);
+    }
+    out[static_cast<long long>(row) * kD + ch] = O / Lt;
+  }
+}
+
 template <int KB, int VB, int NREP, bool MIX>
 cudaError_t launch_cfg(const MmaArgs& a, int warps, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(warps) * (a.rec_bytes + warp_extra(MIX));
@@ -1287,9 +1368,11 @@ cudaError_t launch_combine_parts(const float* ws, int B, int Hkv, int Hq, int ma
       combine_parts_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
       cudaSharedmemCarveoutMaxShared);
   if (carve != cudaSuccess) return carve;
+  // rows of up to 32 partials: one round trip per row; more: 8 warps a row
+  const bool many = max_parts > 32;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(B * Hq);
-  lc.blockDim = dim3(kD);
+  lc.blockDim = dim3(many ? kManyWarps * 32 : kD);
   lc.dynamicSmemBytes = 0;
   lc.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1297,6 +1380,9 @@ cudaError_t launch_combine_parts(const float* ws, int B, int Hkv, int Hq, int ma
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
+  if (many)
+    return cudaLaunchKernelEx(&lc, combine_many_kernel, ws, Hkv, Hq, max_parts, unit_len, total,
+                              n_slots, out);
   return cudaLaunchKernelEx(&lc, combine_parts_kernel, ws, Hkv, Hq, max_parts, unit_len, total,
                             n_slots, out);
 }
