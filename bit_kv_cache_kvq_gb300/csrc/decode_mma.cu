@@ -335,9 +335,14 @@ struct Warp {
       const uint32_t bytes = static_cast<uint32_t>(hi - lo);
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mb), "r"(bytes)
                    : "memory");
+      // records are read once per call: first out of L2, which keeps the
+      // split-K partials there for the combine
+      uint64_t pol;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
       asm volatile(
-          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
-          ::"r"(d), "l"(src), "r"(bytes), "r"(mb)
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+          " [%0], [%1], %2, [%3], %4;\n"
+          ::"r"(d), "l"(src), "r"(bytes), "r"(mb), "l"(pol)
           : "memory");
     }
   }
