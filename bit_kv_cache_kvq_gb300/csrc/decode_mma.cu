@@ -620,7 +620,6 @@ struct Warp {
 
     // ---- UINT4 and UINT2 tiers: virtual 2-bit channels
     const uint32_t* kcw = reinterpret_cast<const uint32_t*>(kbuf + L.kc);
-    const bool low_lane = low_col();
     float bias = 0.0f;
     for (int w = 0; w < kw_used; ++w) {
       uint32_t kx[8], ky[8];
@@ -632,28 +631,43 @@ struct Warp {
 #pragma unroll
       for (int kl = 0; kl < 2; ++kl) {
         const int v0 = 32 * w + 16 * kl + 2 * t;
-        const uint4 e01 = *reinterpret_cast<const uint4*>(tab + v0);
-        const uint4 e89 = *reinterpret_cast<const uint4*>(tab + v0 + 8);
-        const uint32_t es[4] = {e01.x, e01.z, e89.x, e89.z};
-        const uint32_t em[4] = {e01.y, e01.w, e89.y, e89.w};
-        float x[4], hi[4], lo[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int ch = static_cast<int>(em[i] >> 16);
-          const float qv = SPARE ? static_cast<const float*>(qs)[hrow() * kQRow + ch]
-                                 : bf2f(static_cast<const uint16_t*>(qs)[g * kQRow + ch]);
-          bias = fmaf(qv, bf2f(em[i] & 0xffffu), bias);
-          x[i] = qv * __uint_as_float(es[i]) * sq;
-          hi[i] = round_f16_precision(x[i]);
-          lo[i] = x[i] - hi[i];
-        }
         uint32_t bq0, bq1, bl0 = 0u, bl1 = 0u;
-        if (SPARE) {
+        if constexpr (SPARE) {
+          // a head's two lanes share the build (as for uniform keys): the
+          // even lane takes the b0 rows (v0, v0 + 1), the odd lane the b1
+          // rows (v0 + 8, v0 + 9), and they swap the part they do not keep
+          const int par = g & 1;
+          const uint4 e = *reinterpret_cast<const uint4*>(tab + v0 + 8 * par);
+          const uint32_t es[2] = {e.x, e.z}, em[2] = {e.y, e.w};
+          float hi[2], lo[2];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) x[i] = low_lane ? lo[i] : hi[i];
-          bq0 = pack_h2(x[0], x[1]);
-          bq1 = pack_h2(x[2], x[3]);
+          for (int i = 0; i < 2; ++i) {
+            const int ch = static_cast<int>(em[i] >> 16);
+            const float qv = static_cast<const float*>(qs)[hrow() * kQRow + ch];
+            bias = fmaf(qv, bf2f(em[i] & 0xffffu), bias);
+            const float x = qv * __uint_as_float(es[i]) * sq;
+            hi[i] = round_f16_precision(x);
+            lo[i] = x - hi[i];
+          }
+          const uint32_t H = pack_h2(hi[0], hi[1]), Lo = pack_h2(lo[0], lo[1]);
+          const uint32_t recv = __shfl_xor_sync(kFull, par ? H : Lo, 4);
+          bq0 = par ? recv : H;
+          bq1 = par ? Lo : recv;
         } else {
+          const uint4 e01 = *reinterpret_cast<const uint4*>(tab + v0);
+          const uint4 e89 = *reinterpret_cast<const uint4*>(tab + v0 + 8);
+          const uint32_t es[4] = {e01.x, e01.z, e89.x, e89.z};
+          const uint32_t em[4] = {e01.y, e01.w, e89.y, e89.w};
+          float hi[4], lo[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int ch = static_cast<int>(em[i] >> 16);
+            const float qv = bf2f(static_cast<const uint16_t*>(qs)[g * kQRow + ch]);
+            bias = fmaf(qv, bf2f(em[i] & 0xffffu), bias);
+            const float x = qv * __uint_as_float(es[i]) * sq;
+            hi[i] = round_f16_precision(x);
+            lo[i] = x - hi[i];
+          }
           bq0 = pack_h2(hi[0], hi[1]);
           bq1 = pack_h2(hi[2], hi[3]);
           bl0 = pack_h2(lo[0], lo[1]);
@@ -671,7 +685,8 @@ struct Warp {
     }
     bias += __shfl_xor_sync(kFull, bias, 1);
     bias += __shfl_xor_sync(kFull, bias, 2);
-    if (!SPARE) bias *= c0;
+    if (SPARE) bias += __shfl_xor_sync(kFull, bias, 4);   // the pair's halves
+    else bias *= c0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int src = SPARE ? 8 * t : 4 * (2 * t + h);
