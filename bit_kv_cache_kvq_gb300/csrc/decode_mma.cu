@@ -48,7 +48,7 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kResidualWeight = 1;       // residual item ~ half a group of work
+constexpr int kResidualWeight = 1;       // split positions of a window item (a group: 1)
 constexpr float kSentinel = 4.2535295865117308e37f;  // 2^125: "no group yet"
 constexpr float kCodeUnit = 512.0f;      // 2^9: products carry c * B' / 2^9
 constexpr float kInvCodeUnit = 1.0f / 512.0f;
@@ -1140,7 +1140,7 @@ __global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX) * 32, 1) decode_m
     const int g0 = static_cast<int>(lo);
     const int g1 = static_cast<int>(min(hi, static_cast<long long>(a.n_groups)));
     const bool res = a.r > 0 && lo <= a.n_groups && a.n_groups < hi;
-    const int ps = a.n_groups + (a.r > 0 ? 1 : 0);   // position of the sink item
+    const int ps = a.n_groups + (a.r > 0 ? kResidualWeight : 0);   // position of the sink item
     const bool snk = a.s > 0 && lo <= ps && ps < hi;
     // keys of group i+1 load during the P·V of group i, values of group
     // i+1 during its QK: one bulk copy and one mbarrier per part.  The
