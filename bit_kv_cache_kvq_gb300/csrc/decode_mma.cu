@@ -1127,7 +1127,9 @@ template <int KB, int VB, int NREP, bool MIX>
 __global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX) * 32, 1) decode_mma_kernel(MmaArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
-  const int slot = blockIdx.x * (blockDim.x >> 5) + warp;
+  // consecutive slices (records of one unit, contiguous in memory) run on
+  // different SMs, so each SM's warps read from several places at once
+  const int slot = warp * gridDim.x + blockIdx.x;
   // the combine kernel may be scheduled now; it waits for this grid's results
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   if (slot >= a.n_slots) return;            // warp-uniform
