@@ -44,12 +44,12 @@ FALLBACK_HBM_GBS = 6800.0
 # launch, from the ncu capture of this workload at batch 8 kept under
 # profiles/, keyed by the sha256 of the decode kernel source it was taken on
 # (a stale entry reports null).  The capture ran at batch 8 (64 units,
-# 32768 + 100 tokens): 201.241 MB read + 5.844 MB written against 200.884 MB
-# of algorithmic bytes (ratio 1.0309: mostly the split-K partials written).
+# 32768 + 100 tokens): 200.957 MB read + 4.372 MB written against 200.884 MB
+# of algorithmic bytes (ratio 1.0221: mostly the split-K partials written).
 # Traffic per unit is independent of the batch, so the batch-16 launch is
 # that ratio times its algorithmic bytes at the timed steps' mean context.
 NCU_TRAFFIC = {
-    "3c86e86ed8c5ab05": {("llama8b_gqa_32k_b16", 16, 32768, 2): 207.084800 / 200.884224 * 399.264512e6},
+    "4a66d7d68a26410f": {("llama8b_gqa_32k_b16", 16, 32768, 2): 205.329152 / 200.884224 * 399.264512e6},
 }
 
 
