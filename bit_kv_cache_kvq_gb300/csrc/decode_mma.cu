@@ -28,13 +28,13 @@
 //
 // Work split ("stream-K"): the flattened sequence of items (for each unit
 // its groups, then its residual window and its attention-sink window, one
-// item each) is
-// cut into equal contiguous slices, one per warp; a warp keeps one online-
-// softmax state per unit it touches and writes one partial per unit.  Each
-// warp stages one record at a time in its own shared memory, in two parts:
-// the key part of the next group loads while the current group's softmax and
+// item each) is cut into equal contiguous slices, one per warp, and
+// consecutive slices run on different SMs; a warp keeps one online-softmax
+// state per unit it touches and writes one partial per unit.  Each warp
+// stages one record at a time in its own shared memory, in two parts: the
+// key part of the next group loads while the current group's softmax and
 // P·V run, the value part of the next group while its QK runs.  Warps never
-// wait on each other.  The combine kernel merges each query head's partials
+// wait on each other.  The combine kernels merge each query head's partials
 // with the exact log-sum-exp rule.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
