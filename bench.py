@@ -7,10 +7,11 @@ V at 2 bits (K per channel over 128-token groups, V per token over 32
 channels), synthetic seeded bf16 inputs with 4 outlier key channels per KV
 head.
 
-A step is one MixKVQ Algorithm 1 decode step through the C ABI: append the
-new token's key/value to the residual, flush (quantize 128 tokens) when the
-residual is full, then the fused split-K decode attention (partial +
-combine).  The quantized history starts below the workload's length by half
+A step is one MixKVQ Algorithm 1 decode step through the C ABI
+(kvq_decode_step): append the new token's key/value to the residual, flush
+(quantize 128 tokens) when the residual is full, then the fused split-K
+decode attention (partial + combine); without a flush the decode kernel
+writes the token itself, so a step is the decode launch and its combine.  The quantized history starts below the workload's length by half
 the groups the timed steps will flush, so the mean context over the timed
 region is the workload's.
 
@@ -369,21 +370,19 @@ def run_ours(args, rank, world):
     prefill_nb = w.B * w.Hkv * (L0 * 512 + n_grp * 128 * token_bytes(w) + (L0 % 128) * 512)
 
     def step(i, ev=None):
-        """One decode step; returns (launches, algorithmic bytes)."""
+        """One decode step (kvq_decode_step: append, flush when the residual
+        fills, attention); returns (launches, algorithmic bytes, bytes of the
+        call).  Without a flush the decode kernel does the append itself."""
         kn, vn = toks[i]
-        cache.append(kn, vn)
-        launches, nb = 1, append_bytes(w)
-        if cache.lengths()[1] == 128:
-            cache.flush(importance=importance)
-            launches += 1
-            nb += flush_bytes(w)
-        tq, r = cache.lengths()
+        flushes = cache.lengths()[1] + 1 == 128
         if ev is not None:
             ev[0].record(stream)
-        cache.attention(qs[i % n_q], out=out, workspace=ws)
+        cache.decode_step(kn, vn, qs[i % n_q], out=out, workspace=ws, importance=importance)
         if ev is not None:
             ev[1].record(stream)
-        return launches + 2, nb + attention_bytes(w, tq, r), attention_bytes(w, tq, r)
+        tq, r = cache.lengths()
+        nb = append_bytes(w) + attention_bytes(w, tq, r) + (flush_bytes(w) if flushes else 0)
+        return (4 if flushes else 2), nb, nb
 
     def warm():
         prefill()
@@ -511,13 +510,10 @@ def run_ours(args, rank, world):
         def compute(j):
             d_k, d_v, d_q = views[j % 2]
             stream.wait_event(ev["in"][j % 2])
-            cache.append(d_k, d_v)
-            nb = append_bytes(w)
-            if cache.lengths()[1] == 128:
-                cache.flush(importance=importance)
-                nb += flush_bytes(w)
+            flushes = cache.lengths()[1] + 1 == 128
+            cache.decode_step(d_k, d_v, d_q, out=outs[j % 2], workspace=ws, importance=importance)
             tq, r = cache.lengths()
-            cache.attention(d_q, out=outs[j % 2], workspace=ws)
+            nb = append_bytes(w) + (flush_bytes(w) if flushes else 0)
             ev["used"][j % 2].record(stream)
             with torch.cuda.stream(copy_s):
                 copy_s.wait_event(ev["used"][j % 2])

@@ -69,6 +69,7 @@ _SIGS = {
     "kvq_observe_query": (_I, [_P, _P, _I, _P]),
     "kvq_quantize_prefill": (_I, [_P, _P, _P, _I, _P, _P]),
     "kvq_decode_workspace_bytes": (_Z, [_P, _I]),
+    "kvq_decode_step": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _Z, _P]),
     "kvq_decode_attention": (_I, [_P, _P, _I, _P, _P, _Z, _P]),
     "kvq_decode_bf16_workspace_bytes": (_Z, [_I, _I, _I, _I]),
     "kvq_decode_bf16": (_I, [_P, _P, _I, _I, _I, _P, _I, _P, _P, _Z, _P]),
@@ -240,6 +241,27 @@ class KVCache:
             _ptr(out, torch.float32, (self.batch, Hq, HEAD_DIM), "out"),
             _ptr(workspace, torch.uint8, None, "workspace"), workspace.numel(),
             _stream(stream)), "kvq_decode_attention")
+        return out
+
+    def decode_step(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                    out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                    importance: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Append the token, flush if the residual is full, attend (one call,
+        kvq_decode_step)."""
+        B, Hq, D = q.shape
+        if out is None:
+            out = torch.empty(B, Hq, HEAD_DIM, dtype=torch.float32, device=q.device)
+        if workspace is None:
+            workspace = self.workspace(Hq)
+        shp = (self.batch, self.kv_heads, HEAD_DIM)
+        _check(lib().kvq_decode_step(
+            self._h, _ptr(k_new, torch.bfloat16, shp, "k_new"),
+            _ptr(v_new, torch.bfloat16, shp, "v_new"),
+            _ptr(importance, torch.float32, shp, "importance"),
+            _ptr(q, torch.bfloat16, (self.batch, Hq, HEAD_DIM), "q"), Hq,
+            _ptr(out, torch.float32, (self.batch, Hq, HEAD_DIM), "out"),
+            _ptr(workspace, torch.uint8, None, "workspace"), workspace.numel(),
+            _stream(stream)), "kvq_decode_step")
         return out
 
     # -- canonical export (device tensors)

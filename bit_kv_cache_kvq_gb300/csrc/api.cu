@@ -273,7 +273,39 @@ int kvq_decode_attention(const kvq_cache* c, const kvq_bf16* q, int Hq, float* o
   if (!mma_plan(c->num_sms, c->cfg.batch * c->cfg.kv_heads, Hq / c->cfg.kv_heads,
                 c->t_q / kKG, c->r, c->s, c->lay, ws_bytes, &plan))
     return KVQ_ERR_WORKSPACE;
-  return cuda_status(launch_decode_mma(c, q, Hq, out, static_cast<float*>(ws), plan, s));
+  return cuda_status(
+      launch_decode_mma(c, q, Hq, out, static_cast<float*>(ws), plan, nullptr, nullptr, s));
+}
+
+int kvq_decode_step(kvq_cache* c, const kvq_bf16* k_new, const kvq_bf16* v_new,
+                    const float* importance, const kvq_bf16* q, int Hq, float* out, void* ws,
+                    size_t ws_bytes, cudaStream_t s) {
+  if (!c || !k_new || !v_new || !q || !out) return KVQ_ERR_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
+  if (!valid_rep(Hq, c->cfg.kv_heads)) return KVQ_ERR_SHAPE;
+  if (!ws || ws_bytes < kvq_decode_workspace_bytes(c, Hq) || !aligned16(ws))
+    return KVQ_ERR_WORKSPACE;
+  if (c->s < c->cfg.n_sink || c->r + 1 >= kR) {
+    // the token goes to the sink window, or fills the residual (a flush
+    // comes before the attention): the three calls in sequence
+    int e = kvq_append_residual(c, k_new, v_new, s);
+    if (e != KVQ_OK) return e;
+    if (c->r == kR && (e = kvq_flush_group(c, importance, s)) != KVQ_OK) return e;
+    return kvq_decode_attention(c, q, Hq, out, ws, ws_bytes, s);
+  }
+  // the decode kernel writes the token into residual slot r itself
+  MmaPlan plan;
+  if (!mma_plan(c->num_sms, c->cfg.batch * c->cfg.kv_heads, Hq / c->cfg.kv_heads,
+                c->t_q / kKG, c->r + 1, c->s, c->lay, ws_bytes, &plan))
+    return KVQ_ERR_WORKSPACE;
+  c->r += 1;
+  const cudaError_t e =
+      launch_decode_mma(c, q, Hq, out, static_cast<float*>(ws), plan, k_new, v_new, s);
+  if (e != cudaSuccess) {
+    c->r -= 1;
+    return KVQ_ERR_CUDA;
+  }
+  return KVQ_OK;
 }
 
 static int current_sms() {

@@ -140,6 +140,8 @@ struct MmaArgs {
   const uint16_t* sink_k; // [units][n_sink][D]
   const uint16_t* sink_v;
   const uint16_t* q;      // [B][Hq][D]
+  const uint4* new_k;     // fused append: token [units][D] for residual slot r - 1 (or NULL)
+  const uint4* new_v;
   int Hkv, Hq, units;
   long long unit_len;     // weighted positions per unit
   long long total;        // units * unit_len
@@ -932,6 +934,19 @@ struct Warp {
     }
   }
 
+  // Fused append: the unit's new token into residual slot `slot` (lanes
+  // 0..15 the key row, 16..31 the value row), visible to the chunk copies
+  // that read the window next.
+  __device__ __forceinline__ void put_token(int u, int slot) {
+    const int piece = lane & 15;
+    const uint4* src = (lane < 16 ? a.new_k : a.new_v) + static_cast<long long>(u) * (kD / 8) + piece;
+    uint4* dst = reinterpret_cast<uint4*>(const_cast<uint16_t*>(lane < 16 ? a.res_k : a.res_v)) +
+                 (static_cast<long long>(u) * kR + slot) * (kD / 8) + piece;
+    *dst = __ldg(src);
+    __threadfence();
+    __syncwarp();
+  }
+
   // 16-token chunk c (16 rows x 256 B) of a residual tensor into chunk slot
   // `slot` of the record buffer, 16-byte pieces placed at column piece
   // (col ^ (row & 7)) so the ldmatrix row reads are free of bank conflicts.
@@ -1175,7 +1190,10 @@ __global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX) * 32, 1) decode_m
         if (more) W.issue_v(u, gi + 1);
       }
     }
-    if (res) W.window(u, a.res_k, a.res_v, a.r, kR);
+    if (res) {
+      if (a.new_k != nullptr) W.put_token(u, a.r - 1);
+      W.window(u, a.res_k, a.res_v, a.r, kR);
+    }
     if (snk) W.window(u, a.sink_k, a.sink_v, a.s, a.n_sink);
     W.finish(u, slot - slot_of(a, ub));
   }
@@ -1410,7 +1428,8 @@ cudaError_t launch_combine_parts(const float* ws, int B, int Hkv, int Hq, int ma
 }
 
 cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, float* out,
-                              float* ws, const MmaPlan& plan, cudaStream_t s) {
+                              float* ws, const MmaPlan& plan, const kvq_bf16* new_k,
+                              const kvq_bf16* new_v, cudaStream_t s) {
   MmaArgs a;
   a.records = c->records;
   a.rec_bytes = c->lay.bytes;
@@ -1425,6 +1444,8 @@ cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, flo
   a.sink_k = c->sink_k;
   a.sink_v = c->sink_v;
   a.q = q;
+  a.new_k = reinterpret_cast<const uint4*>(new_k);
+  a.new_v = reinterpret_cast<const uint4*>(new_v);
   a.Hkv = c->cfg.kv_heads;
   a.Hq = Hq;
   a.units = c->cfg.batch * c->cfg.kv_heads;

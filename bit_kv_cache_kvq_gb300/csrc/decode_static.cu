@@ -67,7 +67,8 @@ extern "C" int kvq_decode_attention_static(const kvq_cache* c, const kvq_bf16* q
   if (static_ws_address(dev, &ws) != cudaSuccess) return KVQ_ERR_CUDA;
   // Every partial the combine reads is rewritten by this call, so nothing
   // in the array has to start at zero.
-  return launch_decode_mma(c, q, Hq, out, static_cast<float*>(ws), plan, s) == cudaSuccess
+  return launch_decode_mma(c, q, Hq, out, static_cast<float*>(ws), plan, nullptr, nullptr, s) ==
+                 cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;
 }

@@ -179,8 +179,11 @@ int mma_warps_per_cta(const RecLayout& lay, int n_rep);
 bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int sink,
               const RecLayout& lay, size_t ws_cap, MmaPlan* plan);
 size_t mma_ws_bytes(int num_sms, int B, int Hkv, int Hq, int max_groups, const RecLayout& lay);
+// new_k, new_v (or NULL): a token [B][Hkv][D] the kernel writes into
+// residual slot c->r - 1 before reading the residual (a fused append).
 cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, float* out,
-                              float* ws, const MmaPlan& plan, cudaStream_t s);
+                              float* ws, const MmaPlan& plan, const kvq_bf16* new_k,
+                              const kvq_bf16* new_v, cudaStream_t s);
 // Merge split-K partials [units][max_parts][n_rep][D + 2] (o, m, l) of the
 // slots of a plan into out [B][Hq][D]; launched as a programmatic dependent
 // of the kernel that wrote them.

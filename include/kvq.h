@@ -241,6 +241,26 @@ int kvq_decode_attention(const kvq_cache* cache, const kvq_bf16* q, int Hq,
                          float* out, void* ws, size_t ws_bytes, cudaStream_t s);
 
 /*
+ * One decode step of MixKVQ Algorithm 1 (Decoding: append the new token's
+ * key and value, flush when the residual holds R = 128 tokens, then the
+ * attention) in one call: the result equals kvq_append_residual, then
+ * kvq_flush_group(importance) if the residual became full, then
+ * kvq_decode_attention.  When neither a flush nor an append to the
+ * attention-sink window is due, the decode kernel itself writes the token
+ * into the residual, so the step is one decode launch and its combine.
+ * k_new, v_new: bf16 [B][Hkv][D], 16-byte aligned; importance: as for
+ * kvq_flush_group (NULL for uniform caches; NULL takes a mixed cache's
+ * online window), used only when a flush happens; q, out, ws, ws_bytes: as
+ * for kvq_decode_attention (ws sized by kvq_decode_workspace_bytes).
+ * Errors: those of the three calls (RESIDUAL_FULL when the residual was
+ * already full), checked before anything is enqueued where the call is
+ * fused; the cache's lengths advance only on success.
+ */
+int kvq_decode_step(kvq_cache* cache, const kvq_bf16* k_new, const kvq_bf16* v_new,
+                    const float* importance, const kvq_bf16* q, int Hq, float* out,
+                    void* ws, size_t ws_bytes, cudaStream_t s);
+
+/*
  * Decode attention without any allocation (this entry point has no
  * counterpart on the pages; it exists for callers that cannot allocate).
  * Same inputs, output and errors as kvq_decode_attention, but the split-K
