@@ -45,14 +45,15 @@ FALLBACK_HBM_GBS = 6800.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_mma_kernel
 # launch, from the ncu capture of this workload at batch 8 kept under
-# profiles/, keyed by the sha256 of the decode kernel source it was taken on
+# profiles/, keyed by the hash of the decode kernel's code it was taken on
 # (a stale entry reports null).  The capture ran at batch 8 (64 units,
-# 32768 + 100 tokens): 200.957 MB read + 4.372 MB written against 200.884 MB
-# of algorithmic bytes (ratio 1.0221: mostly the split-K partials written).
-# Traffic per unit is independent of the batch, so the batch-16 launch is
-# that ratio times its algorithmic bytes at the timed steps' mean context.
+# 32768 + 100 tokens, the token append fused): 200.958 MB read + 4.277 MB
+# written against 200.884 MB of algorithmic attention bytes (ratio 1.0217:
+# mostly the split-K partials written).  Traffic per unit is independent of
+# the batch, so the batch-16 launch is that ratio times its algorithmic
+# bytes at the timed steps' mean context.
 NCU_TRAFFIC = {
-    "0b23f15b7ee8905d": {("llama8b_gqa_32k_b16", 16, 32768, 2): 205.329152 / 200.884224 * 399.264512e6},
+    "4e86b4276ef94d1d": {("llama8b_gqa_32k_b16", 16, 32768, 2): 205.235456 / 200.884224 * 399.264512e6},
 }
 
 
