@@ -254,7 +254,10 @@ int kvq_decode_attention(const kvq_cache* cache, const kvq_bf16* q, int Hq,
  * for kvq_decode_attention (ws sized by kvq_decode_workspace_bytes).
  * Errors: those of the three calls (RESIDUAL_FULL when the residual was
  * already full), checked before anything is enqueued where the call is
- * fused; the cache's lengths advance only on success.
+ * fused; the cache's lengths advance only on success.  As with the
+ * separate calls, the lengths are host state that advances when the call
+ * is enqueued: a captured stream graph replays the step for the lengths it
+ * was captured at.
  */
 int kvq_decode_step(kvq_cache* cache, const kvq_bf16* k_new, const kvq_bf16* v_new,
                     const float* importance, const kvq_bf16* q, int Hq, float* out,
