@@ -242,11 +242,12 @@ def test_prefill_flush_workload_sampled_units():
 
 
 @pytest.mark.parametrize("context,batch,bits", [(4096, 1, 2), (4096, 8, 4), (131072, 8, 2),
-                                                (65536, 1, 2)])
+                                                (65536, 1, 2), (131072, 64, 4)])
 def test_sweep_points_sampled_units(context, batch, bits):
     """Long-context sweep points.  Small batches split over the whole GPU
     give each query row many partials (33 at 4K x 1; about 300 at 64K x 1,
-    more than one pass of the 8-warp combine's 256-part stride)."""
+    more than one pass of the 8-warp combine's 256-part stride); 128K x 64
+    at 4 bits is the largest point (a 10.6 GB cache)."""
     w = sweep_workload(context, batch, bits)
     units = [0, w.B * w.Hkv - 1]
     K, V = make_kv(w, device="cuda")
