@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
         i, l, f, d = ctypes.c_int, ctypes.c_long, ctypes.c_float, ctypes.c_double
         sig = {
             "orc_quantize_group": (i, [P, l, l, i, P, P, P]),
+            "orc_quantize_group_bf16": (i, [P, l, l, i, P, P, P]),
+            "orc_f32_to_bf16_rn": (ctypes.c_uint16, [f]),
             "orc_pack_lsb": (None, [P, l, i, P]),
             "orc_unpack_lsb": (None, [P, l, i, P]),
             "orc_quantize_k_unit": (i, [P, l, i, i, i, P, P, P]),
@@ -122,6 +124,22 @@ def quantize_group(x, bits: int):
     _check(lib().orc_quantize_group(_p(x), x.size, 1, bits, _p(codes),
                                     ctypes.byref(m), ctypes.byref(s)), "quantize_group")
     return codes, np.float32(m.value), np.float32(s.value)
+
+
+def quantize_group_bf16(x, bits: int):
+    """One group with bf16 metadata and bf16 arithmetic (KIVI §7): returns
+    (codes uint8, origin bf16 bits, step bf16 bits)."""
+    x = np.ascontiguousarray(x, np.float32).reshape(-1)
+    codes = np.zeros(x.size, np.uint8)
+    o, st = ctypes.c_uint16(), ctypes.c_uint16()
+    _check(lib().orc_quantize_group_bf16(_p(x), x.size, 1, bits, _p(codes), ctypes.byref(o),
+                                         ctypes.byref(st)), "quantize_group_bf16")
+    return codes, o.value, st.value
+
+
+def f32_to_bf16_rn(x: float) -> int:
+    """Nearest-even bf16 bits of a finite fp32 value."""
+    return int(lib().orc_f32_to_bf16_rn(float(np.float32(x))))
 
 
 def dequantize_group(codes, origin, step) -> np.ndarray:
@@ -503,3 +521,127 @@ class OracleCache:
         vm = np.concatenate([p[1] for p in self.v_parts[u]]) if self.v_parts[u] else None
         vs = np.concatenate([p[2] for p in self.v_parts[u]]) if self.v_parts[u] else None
         return kc, km, ks, vc, vm, vs
+
+
+class KiviOracleCache:
+    """KIVI's streaming cache ("KIVI: KV cache axes" §4–§6), in its
+    Algorithm 1 order (append, then adjust both caches, then attend), for
+    B x Hkv units of head dimension D:
+
+    - Key: a new token joins the key residual; when it holds R tokens they
+      are quantized per channel in groups of G tokens and the residual
+      empties, so 0 <= r_K < R after every step.
+    - Value: a FIFO; a new token joins the value residual, and when it holds
+      more than R tokens the oldest leaves it, quantized per token in groups
+      of G channels, so r_V = min(tokens, R).
+    - Origins and steps in bf16, computed in bf16 (§7; quantize_group_bf16).
+    - Attention: one softmax over all visible tokens in order; the value
+      rows follow the value boundary, not the key boundary (§6).
+
+    Prefill of L tokens leaves the state L appends would (the persisted
+    invariants of §5): L - L mod R keys quantized, the last min(L, R)
+    values in the FIFO.
+    """
+
+    def __init__(self, B, Hkv, D, k_bits=2, v_bits=2, G=32, R=128):
+        if R % G or D % G:
+            raise ValueError("R and D must be multiples of G")
+        self.B, self.Hkv, self.D = B, Hkv, D
+        self.k_bits, self.v_bits, self.G, self.R = k_bits, v_bits, G, R
+        U = B * Hkv
+        self.kq = [[] for _ in range(U)]   # per G-token group: codes [G][D], origin [D], step [D]
+        self.vq = [[] for _ in range(U)]   # per token: codes [D], origin [D/G], step [D/G]
+        self.kr = [[] for _ in range(U)]   # bf16 bit rows [D]
+        self.vr = [[] for _ in range(U)]
+
+    def _seal_keys(self, u):
+        rows = np.stack(self.kr[u]).astype(np.uint16)          # [R][D]
+        x = bf16_to_f32(rows)
+        for g0 in range(0, self.R, self.G):
+            codes = np.zeros((self.G, self.D), np.uint8)
+            origin = np.zeros(self.D, np.uint16)
+            step = np.zeros(self.D, np.uint16)
+            for d in range(self.D):
+                codes[:, d], origin[d], step[d] = quantize_group_bf16(x[g0:g0 + self.G, d],
+                                                                      self.k_bits)
+            self.kq[u].append((codes, origin, step))
+        self.kr[u] = []
+
+    def _seal_value(self, u):
+        row = bf16_to_f32(np.asarray(self.vr[u].pop(0), np.uint16))
+        nj = self.D // self.G
+        codes = np.zeros(self.D, np.uint8)
+        origin = np.zeros(nj, np.uint16)
+        step = np.zeros(nj, np.uint16)
+        for j in range(nj):
+            sl = slice(j * self.G, (j + 1) * self.G)
+            codes[sl], origin[j], step[j] = quantize_group_bf16(row[sl], self.v_bits)
+        self.vq[u].append((codes, origin, step))
+
+    def append(self, k_new: np.ndarray, v_new: np.ndarray):
+        """One token, bf16 bits [B, Hkv, D] each."""
+        k_new = np.asarray(k_new, np.uint16).reshape(-1, self.D)
+        v_new = np.asarray(v_new, np.uint16).reshape(-1, self.D)
+        for u in range(self.B * self.Hkv):
+            self.kr[u].append(k_new[u].copy())
+            if len(self.kr[u]) == self.R:
+                self._seal_keys(u)
+            self.vr[u].append(v_new[u].copy())
+            if len(self.vr[u]) > self.R:
+                self._seal_value(u)
+
+    def prefill(self, K: np.ndarray, V: np.ndarray):
+        """K, V bf16 bits [B, Hkv, L, D] into an empty cache."""
+        if any(self.kq[u] or self.kr[u] or self.vq[u] or self.vr[u]
+               for u in range(self.B * self.Hkv)):
+            raise ValueError("prefill into a non-empty cache")
+        B, Hkv, L, D = K.shape
+        n_k = L - L % self.R
+        n_v = L - min(L, self.R)
+        for u in range(B * Hkv):
+            b, h = divmod(u, Hkv)
+            for t0 in range(0, n_k, self.R):
+                self.kr[u] = [K[b, h, t] for t in range(t0, t0 + self.R)]
+                self._seal_keys(u)
+            self.kr[u] = [K[b, h, t] for t in range(n_k, L)]
+            self.vr[u] = [V[b, h, t] for t in range(L)]
+            for _ in range(n_v):
+                self._seal_value(u)
+
+    def lengths(self, u: int = 0):
+        """(quantized keys, key residual, quantized values, value residual)."""
+        return (self.G * len(self.kq[u]), len(self.kr[u]), len(self.vq[u]), len(self.vr[u]))
+
+    def dequant_unit(self, u: int):
+        """fp64 K^, V^ of one unit, one row per visible token in order."""
+        D, G = self.D, self.G
+        ks = [bf16_to_f32(o).astype(np.float64)[None, :] +
+              bf16_to_f32(s).astype(np.float64)[None, :] * c.astype(np.float64)
+              for c, o, s in self.kq[u]]
+        vs = []
+        for c, o, s in self.vq[u]:
+            vs.append(np.repeat(bf16_to_f32(o).astype(np.float64), G) +
+                      np.repeat(bf16_to_f32(s).astype(np.float64), G) * c.astype(np.float64))
+        kq = np.concatenate(ks) if ks else np.zeros((0, D))
+        vq = np.stack(vs) if vs else np.zeros((0, D))
+        kr = (bf16_to_f32(np.stack(self.kr[u]).astype(np.uint16)).astype(np.float64)
+              if self.kr[u] else np.zeros((0, D)))
+        vr = (bf16_to_f32(np.stack(self.vr[u]).astype(np.uint16)).astype(np.float64)
+              if self.vr[u] else np.zeros((0, D)))
+        return np.concatenate([kq, kr]), np.concatenate([vq, vr])
+
+    def attention(self, q: np.ndarray) -> np.ndarray:
+        """q bf16 bits [B, Hq, D] -> fp64 [B, Hq, D]; query head h reads KV
+        head h // n_rep."""
+        B, Hq, D = q.shape
+        n_rep = Hq // self.Hkv
+        out = np.zeros((B, Hq, D))
+        qf = bf16_to_f32(q).astype(np.float64)
+        for u in range(B * self.Hkv):
+            b, h = divmod(u, self.Hkv)
+            K, V = self.dequant_unit(u)
+            if K.shape[0] == 0:
+                raise ValueError("attention over an empty cache")
+            for i in range(n_rep):
+                out[b, h * n_rep + i] = attention(qf[b, h * n_rep + i], K, V)
+        return out

@@ -104,6 +104,56 @@ int orc_quantize_group(const float* x, long n, long stride, int bits,
   return ORC_OK;
 }
 
+uint16_t orc_f32_to_bf16_rn(float value) {
+  uint32_t u;
+  memcpy(&u, &value, sizeof u);
+  u += 0x7FFFu + ((u >> 16) & 1u);   /* ties to the even bf16 pattern */
+  return (uint16_t)(u >> 16);
+}
+
+static float orc_bf16_round(float x) { return orc_bf16_to_f32(orc_f32_to_bf16_rn(x)); }
+
+/* [KIVI] §7: the fixed pack path keeps the minimum in a tensor of the
+ * input's dtype and computes the step from it in that dtype; here every
+ * operation is an fp32 operation whose result is rounded to bf16. */
+int orc_quantize_group_bf16(const float* x, long n, long stride, int bits,
+                            uint8_t* codes, uint16_t* origin, uint16_t* step) {
+  if (n <= 0 || stride <= 0 || bits < 1 || bits > 8) return ORC_ERR_ARG;
+  for (long i = 0; i < n; ++i)
+    if (!isfinite(x[i * stride])) return ORC_ERR_NONFINITE;
+
+  float lo = x[0];
+  float hi = x[0];
+  for (long i = 1; i < n; ++i) {
+    float v = x[i * stride];
+    if (orc_less(v, lo)) lo = v;
+    if (orc_less(hi, v)) hi = v;
+  }
+
+  *origin = orc_f32_to_bf16_exact(lo);
+  if (hi == lo) {
+    *step = 0;
+    for (long i = 0; i < n; ++i) codes[i] = 0;
+    return ORC_OK;
+  }
+
+  const int top = (1 << bits) - 1;
+  volatile float range = orc_bf16_round(hi - lo);
+  volatile float delta = orc_bf16_round(range / (float)top);
+  if (!(delta > 0.0f) || !isfinite(delta)) return ORC_ERR_RANGE;
+  *step = orc_f32_to_bf16_exact(delta);
+
+  for (long i = 0; i < n; ++i) {
+    volatile float diff = orc_bf16_round(x[i * stride] - lo);
+    volatile float y = orc_bf16_round(diff / delta);
+    float r = nearbyintf(y);                   /* ties to even */
+    if (r < 0.0f) r = 0.0f;
+    if (r > (float)top) r = (float)top;
+    codes[i] = (uint8_t)r;
+  }
+  return ORC_OK;
+}
+
 /* [KIVI] §3 teaching packer: code i goes to byte i/(8/b) at bit offset
  * b*(i mod 8/b), low bits first; the logical length is carried separately. */
 void orc_pack_lsb(const uint8_t* codes, long n, int bits, uint8_t* out) {

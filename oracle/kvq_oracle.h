@@ -40,6 +40,20 @@ uint16_t orc_f32_to_bf16_exact(float value);
 int orc_quantize_group(const float* x, long n, long stride, int bits,
                        uint8_t* codes, float* origin, float* step);
 
+/* Nearest-even rounding of a finite fp32 value to bf16 (the bf16
+ * arithmetic below computes each operation in fp32 and rounds the result to
+ * bf16, as arithmetic on a bf16 tensor dtype does). */
+uint16_t orc_f32_to_bf16_rn(float value);
+
+/* [KIVI] §7 metadata in the input dtype: one group of n bf16-valued x with
+ * its origin (the minimum) and step kept as bf16 and computed in bf16:
+ *   R = bf16(M - m), step = bf16(R / (2^b - 1)),
+ *   c = clip(RNE(bf16(bf16(x - m) / step)), 0, 2^b - 1);
+ * a constant group (M == m) has step 0 and codes 0.  Errors as for
+ * orc_quantize_group (RANGE when the bf16 step is 0 or not finite). */
+int orc_quantize_group_bf16(const float* x, long n, long stride, int bits,
+                            uint8_t* codes, uint16_t* origin, uint16_t* step);
+
 /* LSB-first packing of b-bit codes (b in {1,2,4,8}). */
 void orc_pack_lsb(const uint8_t* codes, long n, int bits, uint8_t* out);
 void orc_unpack_lsb(const uint8_t* packed, long n, int bits, uint8_t* codes);

@@ -572,3 +572,166 @@ def test_sink_attention_is_attention_over_sink_then_history():
     ref = orc.attention(orc.bf16_to_f32(q[0, 0]).astype(np.float64),
                         np.concatenate([ks, kb]), np.concatenate([vs, vb]))
     assert np.allclose(a.attention(q)[0, 0], ref, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------- KIVI variant (V FIFO, G < R)
+def _bf(bits):
+    """The fp32 value of one bf16 bit pattern."""
+    return float(orc.bf16_to_f32(np.array([bits], np.uint16))[0])
+
+
+def _bf16_vec(x):
+    """Nearest-even bf16 bits of an fp32 vector."""
+    return np.array([orc.f32_to_bf16_rn(v) for v in np.asarray(x, np.float32)], np.uint16)
+
+
+def _kivi_token(t, D):
+    """Token t's key and value rows (bf16 bits), chosen so that 1-bit groups
+    of two tokens (keys) or two channels (values) reconstruct exactly."""
+    k = np.full(D, float(t), np.float32)
+    v = np.array([t + 0.5 * (c % 2) for c in range(D)], np.float32)
+    return orc.f32_to_bf16_exact(k), orc.f32_to_bf16_exact(v)
+
+
+def test_kivi_trace_persisted_lengths_and_order():
+    """KIVI §5's trace (R = 4, G = 2, nine tokens): key residual lengths
+    1,2,3,0,1,2,3,0,1 and value residual lengths min(t, R) after every step;
+    the quantized part and the residual together hold every token in order;
+    at step 9 keys split 8 + 1 and values 5 + 4 (Algorithm 1 order)."""
+    g = golden("kivi_residual_trace.json")
+    R, G, D = g["R"], g["G"], 4
+    cache = orc.KiviOracleCache(1, 1, D, k_bits=1, v_bits=1, G=G, R=R)
+    kl, vl = [], []
+    for t in range(1, g["steps"] + 1):
+        k, v = _kivi_token(t, D)
+        cache.append(k[None, None], v[None, None])
+        nk, rk, nv, rv = cache.lengths()
+        kl.append(rk)
+        vl.append(rv)
+        K, V = cache.dequant_unit(0)
+        want_k = np.stack([orc.bf16_to_f32(_kivi_token(i, D)[0]) for i in range(1, t + 1)])
+        want_v = np.stack([orc.bf16_to_f32(_kivi_token(i, D)[1]) for i in range(1, t + 1)])
+        assert np.array_equal(K, want_k) and np.array_equal(V, want_v)
+    assert kl == g["persisted_key_residual_lengths"]
+    assert vl == g["persisted_value_residual_lengths"]
+    nk, rk, nv, rv = cache.lengths()
+    assert [nk, rk] == g["step9_key_split"] and [nv, rv] == g["step9_value_split"]
+
+
+def test_kivi_prefill_leaves_the_state_of_appends():
+    """A prefill of L tokens leaves what L appends leave (§5's persisted
+    invariants), for every L up to three windows."""
+    R, G, D = 4, 2, 4
+    rng = np.random.default_rng(3)
+    toks = [(_bf16_vec(rng.standard_normal(D)), _bf16_vec(rng.standard_normal(D)))
+            for _ in range(13)]
+    for L in range(0, 13):
+        a = orc.KiviOracleCache(1, 1, D, G=G, R=R)
+        for k, v in toks[:L]:
+            a.append(k[None, None], v[None, None])
+        b = orc.KiviOracleCache(1, 1, D, G=G, R=R)
+        K = np.stack([k for k, _ in toks[:L]]).reshape(1, 1, L, D) if L else np.zeros((1, 1, 0, D), np.uint16)
+        V = np.stack([v for _, v in toks[:L]]).reshape(1, 1, L, D) if L else np.zeros((1, 1, 0, D), np.uint16)
+        b.prefill(K, V)
+        assert a.lengths() == b.lengths()
+        Ka, Va = a.dequant_unit(0)
+        Kb, Vb = b.dequant_unit(0)
+        assert np.array_equal(Ka, Kb) and np.array_equal(Va, Vb)
+
+
+def test_kivi_value_rows_follow_the_value_boundary():
+    """§6: one softmax over all visible tokens, then the probabilities meet
+    the values at the values' own boundary.  At step 9 (keys 8 + 1, values
+    5 + 4) the cache's attention equals textbook attention over the tokens'
+    keys and values rebuilt one by one: the first 8 keys and 5 values from
+    their quantized groups, the rest exact."""
+    R, G, D = 4, 2, 4
+    rng = np.random.default_rng(11)
+    cache = orc.KiviOracleCache(1, 1, D, k_bits=2, v_bits=2, G=G, R=R)
+    raw_k, raw_v = [], []
+    for _ in range(9):
+        k = _bf16_vec(rng.standard_normal(D))
+        v = _bf16_vec(rng.standard_normal(D))
+        raw_k.append(orc.bf16_to_f32(k))
+        raw_v.append(orc.bf16_to_f32(v))
+        cache.append(k[None, None], v[None, None])
+    Kx = np.stack(raw_k).astype(np.float64)
+    Vx = np.stack(raw_v).astype(np.float64)
+    Kh, Vh = Kx.copy(), Vx.copy()
+    for t0 in range(0, 8, G):          # keys: groups of G tokens per channel
+        for d in range(D):
+            c, o, s = orc.quantize_group_bf16(Kx[t0:t0 + G, d], 2)
+            Kh[t0:t0 + G, d] = orc.dequantize_group(c, _bf(o),
+                                                    _bf(s))
+    for t in range(5):                 # values: groups of G channels per token
+        for j in range(0, D, G):
+            c, o, s = orc.quantize_group_bf16(Vx[t, j:j + G], 2)
+            Vh[t, j:j + G] = orc.dequantize_group(c, _bf(o),
+                                                  _bf(s))
+    q = _bf16_vec(rng.standard_normal(D))
+    got = cache.attention(q[None, None])[0, 0]
+    qf = orc.bf16_to_f32(q).astype(np.float64)
+    s = Kh @ qf / np.sqrt(D)
+    p = np.exp(s - s.max())
+    want = (p / p.sum()) @ Vh
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    # taking the first 8 value rows from quantized groups (the key boundary)
+    # would give another output
+    Vw = Vx.copy()
+    for t in range(8):
+        for j in range(0, D, G):
+            c, o, s2 = orc.quantize_group_bf16(Vx[t, j:j + G], 2)
+            Vw[t, j:j + G] = orc.dequantize_group(c, _bf(o),
+                                                  _bf(s2))
+    assert np.max(np.abs((p / p.sum()) @ Vw - want)) > 1e-6
+
+
+def test_kivi_bf16_metadata_key_example():
+    """§3's 4x4 Key example with §7's metadata in the input dtype (bf16):
+    the per-token row 0 keeps the page's codes [3, 0, 0, 0] with the bf16
+    step bf16(101/3) = 33.75, so its top value rebuilds as -1 + 3 * 33.75 =
+    100.25 instead of the page's 100; per channel the steps 1 and 1/2 are
+    exact in bf16 and the columns rebuild exactly."""
+    g = golden("kivi_key_4x4.json")
+    codes, o, s = orc.quantize_group_bf16(g["key"][0], g["bits"])
+    assert list(codes) == [3, 0, 0, 0]
+    assert _bf(o) == -1.0
+    assert _bf(s) == 33.75
+    assert abs(Fraction(33.75) - frac(g["per_token_row0_step"])) <= Fraction(1, 2**8) * 101 / 3
+    rec = orc.dequantize_group(codes, -1.0, 33.75)
+    assert rec[0] == 100.25 and list(rec[1:]) == [-1.0, -1.0, -1.0]
+    for col in range(4):
+        column = [r[col] for r in g["key"]]
+        c, o, s = orc.quantize_group_bf16(column, 2)
+        rec = orc.dequantize_group(c, _bf(o), _bf(s))
+        assert np.array_equal(rec, np.asarray(column, np.float64))
+
+
+def test_kivi_bf16_quantizer_special_cases_and_bound():
+    """Constant group: step 0, codes 0, exact.  RNE ties where bf16 is exact
+    ([0, 0.5, 2.5, 3] -> [0, 0, 2, 3]).  A hand-worked group where the bf16
+    rounding of x - m decides a code.  On random bf16 groups the error
+    stays within 0.52 steps: the bf16 roundings of x - m and of the quotient
+    move a 2-bit quotient by at most 3 * 2^-8 (< 0.012), and 3 bf16 steps
+    stay within 2^-8 of the range."""
+    c, o, s = orc.quantize_group_bf16([2.5] * 7, 2)
+    assert list(c) == [0] * 7 and s == 0 and _bf(o) == 2.5
+    c, o, s = orc.quantize_group_bf16([0.0, 0.5, 2.5, 3.0], 2)
+    assert list(c) == [0, 0, 2, 3]
+    # x - m is rounded to bf16 before the division: m = -2^-7, M = 2.5 give
+    # R = bf16(2.5078125) = 2.5 (a tie, to even) and step = bf16(2.5 / 3) =
+    # 0.83203125; for x = 2.078125, x - m = 2.0859375 rounds (a tie) to
+    # 2.09375 and bf16(2.09375 / 0.83203125) = 2.515625 gives code 3, where
+    # the unrounded difference would give the quotient 2.5 and code 2.
+    c, o, s = orc.quantize_group_bf16([-2.0 ** -7, 2.078125, 2.5], 2)
+    assert _bf(s) == 0.83203125 and list(c) == [0, 3, 3]
+    rng = np.random.default_rng(5)
+    worst = 0.0
+    for _ in range(300):
+        x = rng.standard_normal(32).astype(np.float32) * rng.choice([1e-3, 1.0, 50.0])
+        x = orc.bf16_to_f32(_bf16_vec(x))
+        c, o, s = orc.quantize_group_bf16(x, 2)
+        step = _bf(s)
+        rec = orc.dequantize_group(c, _bf(o), step)
+        worst = max(worst, float(np.max(np.abs(rec - x.astype(np.float64)))) / step)
+    assert worst <= 0.52
