@@ -537,8 +537,8 @@ struct Warp {
   // Mixed keys (MixKVQ): the BF16 tier on bf16 MMAs of the raw keys and the
   // exact query (ldmatrix transposes the channel-major raw rows), rescaled
   // into the code path's units; the UINT4 and UINT2 tiers as 2-bit virtual
-  // channels on the code path.  A per-group table, built in the value-table
-  // area (free until this group's P·V), gives each virtual channel its key
+  // channels on the code path.  A per-group table, built in the mixed warps'
+  // own table area (free until this group's value tables), gives each virtual channel its key
   // channel, step (times 4 for the high half of a UINT4 code, times the row
   // factor) and origin (zero for a high half).  Q' is normalized by the bound
   // max|q| * max step, so the table needs no pass over the products.
