@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
             "orc_quantize_group": (i, [P, l, l, i, P, P, P]),
             "orc_quantize_group_bf16": (i, [P, l, l, i, P, P, P]),
             "orc_f32_to_bf16_rn": (ctypes.c_uint16, [f]),
+            "orc_quantize_group_1bit_mid": (i, [P, l, l, P, P, P]),
+            "orc_pair_scores": (i, [P, i, i, P, i, i, i, P]),
             "orc_pack_lsb": (None, [P, l, i, P]),
             "orc_unpack_lsb": (None, [P, l, i, P]),
             "orc_quantize_k_unit": (i, [P, l, i, i, i, P, P, P]),
@@ -140,6 +142,91 @@ def quantize_group_bf16(x, bits: int):
 def f32_to_bf16_rn(x: float) -> int:
     """Nearest-even bf16 bits of a finite fp32 value."""
     return int(lib().orc_f32_to_bf16_rn(float(np.float32(x))))
+
+
+def quantize_group_1bit_mid(x):
+    """PN-Mix Eq. 7 one-bit group: (codes, offset z, scale s), fp32."""
+    x = np.ascontiguousarray(x, np.float32).reshape(-1)
+    codes = np.zeros(x.size, np.uint8)
+    z, sc = ctypes.c_float(), ctypes.c_float()
+    _check(lib().orc_quantize_group_1bit_mid(_p(x), x.size, 1, _p(codes), ctypes.byref(z),
+                                             ctypes.byref(sc)), "quantize_group_1bit_mid")
+    return codes, np.float32(z.value), np.float32(sc.value)
+
+
+PAIR_ADJACENT, PAIR_SPLIT = 0, 1
+
+
+def pair_channels(D: int, layout: int):
+    """The two channels of each RoPE pair: (2i, 2i+1) adjacent (the paper's
+    formula) or (i, i + D/2) split halves (Hugging Face Llama layout)."""
+    P = D // 2
+    i = np.arange(P)
+    return (2 * i, 2 * i + 1) if layout == PAIR_ADJACENT else (i, i + P)
+
+
+def pair_scores(q_group: np.ndarray, k: np.ndarray, layout: int = PAIR_ADJACENT) -> np.ndarray:
+    """PN-Mix Eq. 6: sigma [D/2] fp32 of one KV head from its GQA group's
+    prefill queries (bf16 bits [Hg, Lq, D]) and keys (bf16 bits [Lk, D])."""
+    q = np.ascontiguousarray(q_group, np.uint16)
+    kk = np.ascontiguousarray(k, np.uint16)
+    Hg, Lq, D = q.shape
+    sigma = np.zeros(D // 2, np.float32)
+    _check(lib().orc_pair_scores(_p(q), Hg, Lq, _p(kk), kk.shape[0], D, layout, _p(sigma)),
+           "pair_scores")
+    return sigma
+
+
+def select_pairs(sigma: np.ndarray, n_high: int) -> np.ndarray:
+    """The n_high pairs of largest sigma (ties: lower pair index) as a
+    boolean pair mask."""
+    order = sorted(range(sigma.size), key=lambda i: (-float(sigma[i]), i))
+    mask = np.zeros(sigma.size, bool)
+    mask[order[:n_high]] = True
+    return mask
+
+
+def channel_mask(pair_mask: np.ndarray, layout: int = PAIR_ADJACENT) -> np.ndarray:
+    """Per-channel high-precision flags: both channels of a selected pair."""
+    D = 2 * pair_mask.size
+    a, b = pair_channels(D, layout)
+    m = np.zeros(D, bool)
+    m[a[pair_mask]] = True
+    m[b[pair_mask]] = True
+    return m
+
+
+def quantize_k_h3l1_group(k_group: np.ndarray, high: np.ndarray, b_high: int = 3):
+    """PN-Mix H3/L1 key group (bf16 bits [G, D]): channels with high set at
+    b_high bits by Eq. 2 (min-max, origin the minimum), the others at one
+    bit by Eq. 7.  Returns (codes [G, D], offset [D] fp32, scale [D] fp32)."""
+    x = bf16_to_f32(np.asarray(k_group, np.uint16))
+    G, D = x.shape
+    codes = np.zeros((G, D), np.uint8)
+    off = np.zeros(D, np.float32)
+    sc = np.zeros(D, np.float32)
+    for d in range(D):
+        if high[d]:
+            codes[:, d], off[d], sc[d] = quantize_group(x[:, d], b_high)
+        else:
+            codes[:, d], off[d], sc[d] = quantize_group_1bit_mid(x[:, d])
+    return codes, off, sc
+
+
+def h3l1_planes(codes: np.ndarray, high: np.ndarray):
+    """App. G packing planes: the LSB of every code (all channels) and the
+    upper two bits of the high channels' 3-bit codes."""
+    return codes & 1, (codes >> 1)[:, high]
+
+
+def pnmix_k_bits(T: int, D: int, G: int, n_high_pairs: int, n_sink: int,
+                 meta_bits: int = 16) -> float:
+    """Persistent key bits per quantized element: an LSB plane over all
+    channels, two upper bits for the high channels, an offset and a scale
+    per channel and group, the pair mask once, the sink tokens raw."""
+    bits = T * D + T * 2 * (2 * n_high_pairs) + (T // G) * D * 2 * meta_bits
+    bits += D // 2 + n_sink * D * 16
+    return bits / (T * D)
 
 
 def dequantize_group(codes, origin, step) -> np.ndarray:
@@ -362,7 +449,7 @@ class OracleCache:
 
     def __init__(self, B, Hkv, D, k_bits=2, v_bits=2, Gk=128, Gv=32, R=128,
                  mode="uniform", n_bf16=0, n_uint4=0, sal_bits=2, n_sink=0,
-                 tier_mode="rank", tau_bf16=0.0, tau_uint4=0.0):
+                 tier_mode="rank", tau_bf16=0.0, tau_uint4=0.0, high_channels=None):
         if R % Gk:
             raise ValueError("R must be a multiple of the key group")
         self.B, self.Hkv, self.D = B, Hkv, D
@@ -371,6 +458,11 @@ class OracleCache:
         if tier_mode not in ("rank", "threshold"):
             raise ValueError("tier_mode is 'rank' or 'threshold'")
         self.tier_mode, self.tau_bf16, self.tau_uint4 = tier_mode, tau_bf16, tau_uint4
+        # mode "pnmix": high_channels [B, Hkv, D] bool, the PN-Mix pair mask
+        # chosen once at prefill (channel_mask of select_pairs of pair_scores)
+        self.high = None if high_channels is None else np.asarray(high_channels, bool)
+        if mode == "pnmix" and self.high is None:
+            raise ValueError("pnmix mode needs the high-precision channels")
         U = B * Hkv
         self.qacc = np.zeros((U, D), np.float32)   # online |q| sums of the window
         self.q_steps = 0
@@ -465,6 +557,9 @@ class OracleCache:
             kg = kb[g0:g0 + self.Gk]
             if self.mode == "uniform":
                 self.k_groups[u].append(quantize_k_unit(kg, self.Gk, self.k_bits))
+            elif self.mode == "pnmix":
+                b, h = divmod(u, self.Hkv)
+                self.k_groups[u].append(quantize_k_h3l1_group(kg, self.high[b, h]))
             else:
                 S = sensitivity(kg, self.sal_bits)
                 A = salience(np.asarray(imp, np.float32), S)
@@ -484,6 +579,10 @@ class OracleCache:
         for grp in self.k_groups[u]:
             if self.mode == "uniform":
                 ks.append(dequant_k_unit(*grp, self.Gk, self.k_bits))
+            elif self.mode == "pnmix":
+                codes, off, sc = grp
+                ks.append(off.astype(np.float64)[None, :] +
+                          sc.astype(np.float64)[None, :] * codes.astype(np.float64))
             else:
                 ks.append(dequant_k_mixed_group(grp, self.Gk))
         vs = [dequant_v_unit(*part, self.Gv, self.v_bits) for part in self.v_parts[u]]

@@ -154,6 +154,83 @@ int orc_quantize_group_bf16(const float* x, long n, long stride, int bits,
   return ORC_OK;
 }
 
+/* [PN-Mix] Eq. 7 (quarter-point 1-bit groups). */
+int orc_quantize_group_1bit_mid(const float* x, long n, long stride, uint8_t* codes,
+                                float* offset, float* scale) {
+  if (n <= 0 || stride <= 0) return ORC_ERR_ARG;
+  for (long i = 0; i < n; ++i)
+    if (!isfinite(x[i * stride])) return ORC_ERR_NONFINITE;
+  float lo = x[0], hi = x[0];
+  for (long i = 1; i < n; ++i) {
+    float v = x[i * stride];
+    if (orc_less(v, lo)) lo = v;
+    if (orc_less(hi, v)) hi = v;
+  }
+  if (hi == lo) {
+    *offset = lo;
+    *scale = 0.0f;
+    for (long i = 0; i < n; ++i) codes[i] = 0;
+    return ORC_OK;
+  }
+  volatile float range = hi - lo;
+  volatile float s = range / 2.0f;
+  volatile float three_lo = 3.0f * lo;
+  volatile float num = three_lo + hi;
+  volatile float z = num / 4.0f;
+  if (!(s > 0.0f) || !isfinite(s) || !isfinite(z)) return ORC_ERR_RANGE;
+  *offset = z;
+  *scale = s;
+  for (long i = 0; i < n; ++i) {
+    volatile float diff = x[i * stride] - z;
+    volatile float y = diff / s;
+    float r = nearbyintf(y);
+    if (r < 0.0f) r = 0.0f;
+    if (r > 1.0f) r = 1.0f;
+    codes[i] = (uint8_t)r;
+  }
+  return ORC_OK;
+}
+
+/* [PN-Mix] Eq. 6 (pair-norm scores, fp32 in a fixed order). */
+int orc_pair_scores(const uint16_t* q, int Hg, int Lq, const uint16_t* k, int Lk, int D,
+                    int layout, float* sigma) {
+  if (!q || !k || !sigma || Hg <= 0 || Lq <= 0 || Lk <= 0 || D <= 0 || D % 2 ||
+      (layout != 0 && layout != 1))
+    return ORC_ERR_ARG;
+  const int P = D / 2;
+  for (int i = 0; i < P; ++i) {
+    const int ca = layout == 0 ? 2 * i : i;
+    const int cb = layout == 0 ? 2 * i + 1 : i + P;
+    volatile float qsum = 0.0f;
+    for (int h = 0; h < Hg; ++h) {
+      volatile float acc = 0.0f;
+      for (int t = 0; t < Lq; ++t) {
+        const float a = orc_bf16_to_f32(q[((long)h * Lq + t) * D + ca]);
+        const float b = orc_bf16_to_f32(q[((long)h * Lq + t) * D + cb]);
+        if (!isfinite(a) || !isfinite(b)) return ORC_ERR_NONFINITE;
+        volatile float aa = a * a, bb = b * b;
+        volatile float ss = aa + bb;
+        acc = acc + sqrtf(ss);
+      }
+      volatile float mean = acc / (float)Lq;
+      qsum = qsum + mean;
+    }
+    volatile float qbar = qsum / (float)Hg;
+    volatile float kacc = 0.0f;
+    for (int t = 0; t < Lk; ++t) {
+      const float a = orc_bf16_to_f32(k[(long)t * D + ca]);
+      const float b = orc_bf16_to_f32(k[(long)t * D + cb]);
+      if (!isfinite(a) || !isfinite(b)) return ORC_ERR_NONFINITE;
+      volatile float aa = a * a, bb = b * b;
+      volatile float ss = aa + bb;
+      kacc = kacc + sqrtf(ss);
+    }
+    volatile float kbar = kacc / (float)Lk;
+    sigma[i] = qbar * kbar;
+  }
+  return ORC_OK;
+}
+
 /* [KIVI] §3 teaching packer: code i goes to byte i/(8/b) at bit offset
  * b*(i mod 8/b), low bits first; the logical length is carried separately. */
 void orc_pack_lsb(const uint8_t* codes, long n, int bits, uint8_t* out) {

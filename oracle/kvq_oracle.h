@@ -54,6 +54,23 @@ uint16_t orc_f32_to_bf16_rn(float value);
 int orc_quantize_group_bf16(const float* x, long n, long stride, int bits,
                             uint8_t* codes, uint16_t* origin, uint16_t* step);
 
+/* [PN-Mix] Eq. 7: a 1-bit group whose two reconstructions sit at the
+ * quarter points: s = fl32(fl32(M - m) / 2), z = fl32(fl32(fl32(3 m) + M) / 4),
+ * c = clip(RNE(fl32(fl32(x - z) / s)), 0, 1), x^ = z + s c; a constant
+ * group (M == m) has s = 0 and z = m (zero scale, original offset). */
+int orc_quantize_group_1bit_mid(const float* x, long n, long stride, uint8_t* codes,
+                                float* offset, float* scale);
+
+/* [PN-Mix] Eq. 6 pair scores of one KV head: q bf16 [Hg][Lq][D] (the query
+ * heads of its GQA group, in order), k bf16 [Lk][D]; pair i is channels
+ * (2i, 2i+1) for layout 0 (adjacent) or (i, i + D/2) for layout 1 (split
+ * halves).  In fp32: a token's pair norm is the correctly rounded
+ * sqrt(a*a + b*b); per head the norms are summed in token order and divided
+ * by Lq, the head means summed in head order and divided by Hg, the key
+ * norms summed in token order and divided by Lk; sigma = the product. */
+int orc_pair_scores(const uint16_t* q, int Hg, int Lq, const uint16_t* k, int Lk, int D,
+                    int layout, float* sigma);
+
 /* LSB-first packing of b-bit codes (b in {1,2,4,8}). */
 void orc_pack_lsb(const uint8_t* codes, long n, int bits, uint8_t* out);
 void orc_unpack_lsb(const uint8_t* packed, long n, int bits, uint8_t* codes);

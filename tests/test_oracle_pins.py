@@ -735,3 +735,113 @@ def test_kivi_bf16_quantizer_special_cases_and_bound():
         rec = orc.dequantize_group(c, _bf(o), step)
         worst = max(worst, float(np.max(np.abs(rec - x.astype(np.float64)))) / step)
     assert worst <= 0.52
+
+
+# ------------------------------------------------------ PN-Mix H3/L1 (f4)
+def _bf16_of(x):
+    """Nearest-even bf16 bits of an fp32 array (any shape)."""
+    x = np.asarray(x, np.float32)
+    return np.array([orc.f32_to_bf16_rn(v) for v in x.reshape(-1)], np.uint16).reshape(x.shape)
+
+def test_pnmix_eq7_one_bit_groups_rebuild_at_quarter_points():
+    """PN-Mix Eq. 7: s = (max - min)/2, z = (3 min + max)/4, so the two
+    reconstructions are the quarter points (3m + M)/4 and (m + 3M)/4; codes
+    split at the midpoint (a tie at the midpoint rounds to even, code 0);
+    a constant group has zero scale and the original offset; the error is
+    at most a quarter of the range."""
+    c, z, s = orc.quantize_group_1bit_mid([0.0, 1.0, 3.0, 4.0])
+    assert list(c) == [0, 0, 1, 1] and z == 1.0 and s == 2.0
+    assert sorted({float(z), float(z + s)}) == [(3 * 0 + 4) / 4, (0 + 3 * 4) / 4]
+    c, z, s = orc.quantize_group_1bit_mid([0.0, 2.0, 4.0])
+    assert list(c) == [0, 0, 1]
+    c, z, s = orc.quantize_group_1bit_mid([-1.5] * 5)
+    assert list(c) == [0] * 5 and z == -1.5 and s == 0.0
+    rng = np.random.default_rng(8)
+    for _ in range(200):
+        x = (rng.standard_normal(128) * rng.choice([1e-2, 1.0, 30.0])).astype(np.float32)
+        c, z, s = orc.quantize_group_1bit_mid(x)
+        rec = np.float64(z) + np.float64(s) * c
+        quarter = (float(x.max()) - float(x.min())) / 4
+        assert np.max(np.abs(rec - x)) <= quarter * (1 + 2 ** -20)
+
+
+def test_pnmix_eq6_pair_scores_by_hand():
+    """PN-Mix Eq. 6 on integer pair norms: two query heads of one GQA group,
+    two tokens each, two keys, D = 4 (adjacent pairs (0,1), (2,3)).  Query
+    pair norms: head 0 pair 0 -> 5, 10 (mean 7.5), pair 1 -> 0, 1 (0.5);
+    head 1 pair 0 -> 0, 0, pair 1 -> 5, 0 (2.5); head averages 3.75, 1.5.
+    Key pair norms 1, 1 and 2, 0: means 1 and 1.  sigma = [3.75, 1.5].  The
+    split layout pairs (i, i + D/2): the same scores as the adjacent layout
+    on channels reordered [0, 2, 1, 3]."""
+    bf = lambda a: orc.f32_to_bf16_exact(np.asarray(a, np.float32))
+    q = bf([[[3, 4, 0, 0], [6, 8, 1, 0]], [[0, 0, 3, 4], [0, 0, 0, 0]]])
+    k = bf([[1, 0, 0, 2], [0, 1, 0, 0]])
+    sig = orc.pair_scores(q, k, orc.PAIR_ADJACENT)
+    assert list(sig) == [3.75, 1.5]
+    perm = [0, 2, 1, 3]
+    assert np.array_equal(orc.pair_scores(q, k, orc.PAIR_SPLIT),
+                          orc.pair_scores(q[..., perm], k[..., perm], orc.PAIR_ADJACENT))
+
+
+def test_pnmix_selection_takes_whole_pairs():
+    """floor(r d / 2) pairs at r = 0.5, d = 128: 32 pairs, both channels of
+    each high; ties go to the lower pair index."""
+    sig = np.ones(64, np.float32)
+    sig[[5, 40]] = 2.0
+    mask = orc.select_pairs(sig, int(0.5 * 128 // 2))
+    assert mask.sum() == 32 and mask[5] and mask[40] and mask[:30].sum() == 30
+    for layout in (orc.PAIR_ADJACENT, orc.PAIR_SPLIT):
+        ch = orc.channel_mask(mask, layout)
+        a, b = orc.pair_channels(128, layout)
+        assert ch.sum() == 64 and np.array_equal(ch[a], ch[b]) and np.array_equal(ch[a], mask)
+
+
+def test_pnmix_h3l1_planes_and_storage():
+    """App. G: every channel keeps its code's LSB; high channels add the two
+    upper bits of their 3-bit code (Eq. 2).  The main configuration (b_H = 3,
+    b_L = 1, r = 0.5, G = N = 128, N_s = 32) costs about 2.26 key bits per
+    element at 32K quantized tokens (PN-Mix App. G figure), here 2 (planes)
+    + 0.25 (an fp16 offset and scale per channel and group) + the sink and
+    the pair mask = 2.2656; without the sink it would be 2.25."""
+    rng = np.random.default_rng(9)
+    kg = _bf16_of(rng.standard_normal((128, 16)))
+    high = np.zeros(16, bool)
+    high[[0, 1, 6, 7]] = True
+    codes, off, sc = orc.quantize_k_h3l1_group(kg, high)
+    lsb, upper = orc.h3l1_planes(codes, high)
+    assert upper.shape == (128, 4) and lsb.shape == (128, 16)
+    assert np.array_equal((upper << 1) | lsb[:, high], codes[:, high])
+    assert codes[:, ~high].max() <= 1 and codes[:, high].max() <= 7
+    x = orc.bf16_to_f32(kg)
+    for d in np.flatnonzero(high):   # Eq. 2 at 3 bits: |x - x^| <= s/2
+        rec = np.float64(off[d]) + np.float64(sc[d]) * codes[:, d]
+        assert np.max(np.abs(rec - x[:, d])) <= float(sc[d]) / 2 * (1 + 2 ** -20)
+    bits = orc.pnmix_k_bits(32768, 128, 128, 32, 32)
+    assert abs(bits - 2.26) < 0.006
+    assert abs(orc.pnmix_k_bits(32768, 128, 128, 32, 0) - 2.26) >= 0.006
+
+
+def test_pnmix_cache_attention_over_rebuilt_keys():
+    """A PN-Mix cache (the pair mask fixed before prefill; keys by H3/L1 per
+    128-token group, values as the main path) attends like textbook
+    attention over keys rebuilt group by group."""
+    rng = np.random.default_rng(12)
+    D, L = 8, 2 * 128 + 20
+    K = _bf16_of(rng.standard_normal((1, 1, L, D)))
+    V = _bf16_of(rng.standard_normal((1, 1, L, D)))
+    high = np.zeros((1, 1, D), bool)
+    high[0, 0, [2, 3]] = True
+    cache = orc.OracleCache(1, 1, D, k_bits=2, v_bits=2, Gk=128, Gv=4, R=128, mode="pnmix",
+                            high_channels=high)
+    cache.prefill(K, V)
+    Kh = orc.bf16_to_f32(K[0, 0]).astype(np.float64)
+    for g0 in (0, 128):
+        codes, off, sc = orc.quantize_k_h3l1_group(K[0, 0, g0:g0 + 128], high[0, 0])
+        Kh[g0:g0 + 128] = off[None, :].astype(np.float64) + sc[None, :].astype(np.float64) * codes
+    _, Vh = cache.dequant_unit(0)
+    q = _bf16_of(rng.standard_normal((1, 1, D)))
+    got = cache.attention(q)[0, 0]
+    qf = orc.bf16_to_f32(q[0, 0]).astype(np.float64)
+    s = Kh @ qf / np.sqrt(D)
+    p = np.exp(s - s.max())
+    np.testing.assert_allclose(got, (p / p.sum()) @ Vh, rtol=1e-12, atol=1e-12)
