@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "KVCache", "decode_bf16", "channel_saliency", "KVQError", "lib",
     "KVQ_K_UNIFORM", "KVQ_K_MIXED", "TIER_BF16", "TIER_UINT4", "TIER_UINT2",
-    "FLAG_NONFINITE", "FLAG_RANGE", "HEAD_DIM", "K_GROUP", "V_GROUP", "RESIDUAL",
+    "FLAG_NONFINITE", "FLAG_RANGE", "FLAG_TIMEOUT", "set_wait_limit", "HEAD_DIM", "K_GROUP", "V_GROUP", "RESIDUAL",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -27,7 +27,7 @@ HEAD_DIM, K_GROUP, V_GROUP, RESIDUAL = 128, 128, 32, 128
 KVQ_K_UNIFORM, KVQ_K_MIXED = 0, 1
 TIER_BF16, TIER_UINT4, TIER_UINT2 = 0, 1, 2
 TIERS_RANK, TIERS_THRESHOLD = 0, 1
-FLAG_NONFINITE, FLAG_RANGE = 1, 2
+FLAG_NONFINITE, FLAG_RANGE, FLAG_TIMEOUT = 1, 2, 4
 
 _CODES = {0: "OK", 1: "ARG", 2: "SHAPE", 3: "CAPACITY", 4: "RESIDUAL_FULL",
           5: "RESIDUAL_NOT_FULL", 6: "EMPTY", 7: "NOT_EMPTY", 8: "CUDA", 9: "WORKSPACE",
@@ -80,6 +80,7 @@ _SIGS = {
     "kvq_export_residual": (_I, [_P, _P, _P, _P]),
     "kvq_export_sink": (_I, [_P, _P, _P, _P]),
     "kvq_export_k_mixed": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "kvq_set_wait_limit": (_I, [_I]),
     "kvq_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -372,3 +373,11 @@ def channel_saliency(q_win: torch.Tensor, k_grp: torch.Tensor, sal_bits: int = 2
         ctypes.byref(spec), I.data_ptr(), A.data_ptr(), tiers.data_ptr(), _stream(stream)),
         "kvq_channel_saliency")
     return I, A, tiers
+
+
+def set_wait_limit(polls: int) -> int:
+    """Polls before a decode warp's wait for its staged data gives up
+    (kvq_set_wait_limit; negative restores the default).  A failure-detection
+    hook for tests: 0 makes every wait give up at once, setting
+    FLAG_TIMEOUT.  Returns the previous limit."""
+    return int(lib().kvq_set_wait_limit(int(polls)))

@@ -422,6 +422,12 @@ int kvq_export_k_mixed(const kvq_cache* c, uint8_t* counts, uint8_t* perm, kvq_b
   return cuda_status(launch_export_k_mixed(c, counts, perm, raw, c4, m4, s4, c2, m2, s2, s));
 }
 
+int kvq_set_wait_limit(int polls) {
+  const int previous = decode_wait_polls();
+  set_decode_wait_polls(polls);
+  return previous;
+}
+
 const char* kvq_status_string(int code) {
   switch (code) {
     case KVQ_OK: return "KVQ_OK";

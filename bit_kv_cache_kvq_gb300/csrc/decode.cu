@@ -231,8 +231,8 @@ template <int NREP>
 cudaError_t launch_nrep(const Bf16Args& a, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(kWarps) * 2 * kSlotBytes;
   auto kern = decode_bf16_kernel<NREP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  static SmemOptIn opt_in;
+  cudaError_t e = opt_in.ensure(kern);
   if (e != cudaSuccess) return e;
   kern<<<(a.n_slots + kWarps - 1) / kWarps, kWarps * 32, smem, s>>>(a);
   return cudaGetLastError();

@@ -48,7 +48,10 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kResidualWeight = 1;       // split positions of a window item (a group: 1)
+// Split positions of a bf16 window item (the residual or the sink; a group
+// is 1): a window's 16-token chunks stream through two buffer slots, so it
+// takes about as long as two groups, and slices holding one get fewer.
+constexpr int kResidualWeight = 2;
 constexpr float kSentinel = 4.2535295865117308e37f;  // 2^125: "no group yet"
 constexpr float kCodeUnit = 512.0f;      // 2^9: products carry c * B' / 2^9
 constexpr float kInvCodeUnit = 1.0f / 512.0f;
@@ -63,7 +66,7 @@ constexpr float kInvCodeUnit = 1.0f / 512.0f;
 // value tables are built in place over the staged value steps and origins
 // they are computed from (3072 bytes, read into registers first).
 constexpr int kVsbBytes = 256 * 4;
-constexpr int kVmbBytes = 4 * 72 * 4;
+constexpr int kVmbBytes = 4 * 72 * 4 + 64 * 4;   // 4 origin rows, then a zero row
 constexpr int kQRow = 136;
 constexpr int kQBytes = 8 * kQRow * 2;   // = 4 * kQRow * 4
 static_assert(kVsbBytes + kVmbBytes <= 4 * kKG * kVGroups + 2 * kKG * kVGroups,
@@ -100,6 +103,8 @@ __device__ __forceinline__ int vsb_index(int kt, int t, int j, int slot) {
 __device__ __forceinline__ int vmb_index(int kt, int j, int t, int slot) {
   return j * 72 + kt * 8 + t * 2 + slot;
 }
+// 64 zero words after the four origin rows (index kt * 8 + t * 2 + slot)
+constexpr int kZeroRow = 4 * 72;
 
 // --- code unpacking: word x and y = x >> 8 -> A fragment registers
 // (frag_layout.h).  Each register is one AND; its halves are f16 subnormals.
@@ -149,6 +154,7 @@ struct MmaArgs {
   int max_parts;          // partial slots per unit in ws
   float* ws;              // [units][max_parts][NREP][D + 2]
   unsigned* status;       // sticky KVQ_FLAG_* word of the cache
+  int wait_polls;         // try_wait polls before a wait for a staged part gives up
 };
 
 // mbarrier helpers for the bulk staging of records.
@@ -156,9 +162,10 @@ __device__ __forceinline__ void mbar_init(uint32_t mb) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(mb) : "memory");
 }
 // Wait for phase `parity` of mbarrier mb; false if it did not complete
-// within the iteration limit (each try_wait also suspends for a while).
-__device__ __forceinline__ bool mbar_wait(uint32_t mb, uint32_t parity) {
-  for (int i = 0; i < (1 << 20); ++i) {
+// within `polls` polls (each try_wait also suspends for a while).
+constexpr int kWaitPolls = 1 << 20;
+__device__ __forceinline__ bool mbar_wait(uint32_t mb, uint32_t parity, int polls) {
+  for (int i = 0; i < polls; ++i) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -169,6 +176,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mb, uint32_t parity) {
     if (done) return true;
   }
   return false;
+}
+
+// Bring `bytes` (a multiple of 16) at p into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, int bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ long long slot_start(const MmaArgs& a, int w) {
@@ -353,13 +365,14 @@ struct Warp {
     issue(u, grp, vbuf, a.lay.kpart, static_cast<int>(a.rec_bytes), mb_v);
   }
   // Wait for the staged key (value) part; on a timeout record the flag and
-  // return false (the caller stops; the copy is waited for once more).
+  // return false (the caller stops; the copy in flight is then waited for
+  // with the full limit, so it has landed before the warp leaves).
   __device__ __forceinline__ bool wait_part(uint32_t mb, uint32_t& phase) {
-    const bool ok = mbar_wait(mb, phase);
+    const bool ok = mbar_wait(mb, phase, a.wait_polls);
     phase ^= 1u;
     if (!ok) {
       if (lane == 0) atomicOr(a.status, static_cast<unsigned>(KVQ_FLAG_TIMEOUT));
-      mbar_wait(mb, phase ^ 1u);
+      mbar_wait(mb, phase ^ 1u, kWaitPolls);
     }
     return ok;
   }
@@ -405,10 +418,11 @@ struct Warp {
         const uint32_t m2 = kmin2[8 * ks + t + 4 * par];
         qk[2 * ks + 0] = qv.x * sc.x;
         qk[2 * ks + 1] = qv.y * sc.y;
-        bias = fmaf(qv.x, bf2f(m2 & 0xffffu), bias);
-        bias = fmaf(qv.y, bf2f(m2 >> 16), bias);
-        mx = fmaxf(mx, fmaxf(fabsf(qk[2 * ks]), fabsf(qk[2 * ks + 1])));
+        bias = fmaf(qv.x, bf16_lo(m2), bias);
+        bias = fmaf(qv.y, bf16_hi(m2), bias);
+        mx = max3_abs(mx, qk[2 * ks], qk[2 * ks + 1]);
       }
+      mx = fabsf(mx);
 #pragma unroll
       for (int x = 1; x <= 4; x <<= 1) {
         mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, x));
@@ -421,8 +435,10 @@ struct Warp {
       for (int ks = 0; ks < 8; ++ks) {
         const float f = sp * (row_factor<KB>(ks, 0) / row_factor<KB>(0, 0));
         const float x0 = qk[2 * ks] * f, x1 = qk[2 * ks + 1] * f;
-        const float h0 = round_f16_precision(x0), h1 = round_f16_precision(x1);
-        const uint32_t H = pack_h2(h0, h1), Lo = pack_h2(x0 - h0, x1 - h1);
+        // high part: x rounded to f16; low part: the (exact) rest, rounded
+        const uint32_t H = pack_h2(x0, x1);
+        const float2 hf = h2_to_f2(H);
+        const uint32_t Lo = pack_h2(x0 - hf.x, x1 - hf.y);
         const uint32_t recv = __shfl_xor_sync(kFull, par ? H : Lo, 4);
         bq[ks][0] = par ? recv : H;
         bq[ks][1] = par ? Lo : recv;
@@ -439,19 +455,19 @@ struct Warp {
         const uint32_t m01 = kmin2[8 * ks + t];
         const uint32_t m89 = kmin2[8 * ks + t + 4];
         const uint32_t q01 = qrow[8 * ks + t], q89 = qrow[8 * ks + t + 4];
-        const float qa = bf2f(q01 & 0xffffu) * c0, qb = bf2f(q01 >> 16) * c0;
-        const float qc = bf2f(q89 & 0xffffu) * c0, qd = bf2f(q89 >> 16) * c0;
+        const float qa = bf16_lo(q01) * c0, qb = bf16_hi(q01) * c0;
+        const float qc = bf16_lo(q89) * c0, qd = bf16_hi(q89) * c0;
         qk[4 * ks + 0] = qa * s01.x;
         qk[4 * ks + 1] = qb * s01.y;
         qk[4 * ks + 2] = qc * s89.x;
         qk[4 * ks + 3] = qd * s89.y;
-        bias = fmaf(qa, bf2f(m01 & 0xffffu), bias);
-        bias = fmaf(qb, bf2f(m01 >> 16), bias);
-        bias = fmaf(qc, bf2f(m89 & 0xffffu), bias);
-        bias = fmaf(qd, bf2f(m89 >> 16), bias);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fabsf(qk[4 * ks + i]));
+        bias = fmaf(qa, bf16_lo(m01), bias);
+        bias = fmaf(qb, bf16_hi(m01), bias);
+        bias = fmaf(qc, bf16_lo(m89), bias);
+        bias = fmaf(qd, bf16_hi(m89), bias);
+        mx = max3_abs(mx, max3_abs(qk[4 * ks], qk[4 * ks + 1], qk[4 * ks + 2]), qk[4 * ks + 3]);
       }
+      mx = fabsf(mx);
       mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
       bias += __shfl_xor_sync(kFull, bias, 1);
@@ -464,16 +480,11 @@ struct Warp {
         const float f0 = sq * row_factor<KB>(ks, 0), f1 = sq * row_factor<KB>(ks, 1);
         float x[4] = {qk[4 * ks + 0] * f0, qk[4 * ks + 1] * f0, qk[4 * ks + 2] * f1,
                       qk[4 * ks + 3] * f1};
-        float hi[4], lo[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          hi[i] = round_f16_precision(x[i]);
-          lo[i] = x[i] - hi[i];
-        }
-        bq[ks][0] = pack_h2(hi[0], hi[1]);
-        bq[ks][1] = pack_h2(hi[2], hi[3]);
-        bl[ks % NL][0] = pack_h2(lo[0], lo[1]);
-        bl[ks % NL][1] = pack_h2(lo[2], lo[3]);
+        bq[ks][0] = pack_h2(x[0], x[1]);
+        bq[ks][1] = pack_h2(x[2], x[3]);
+        const float2 h01 = h2_to_f2(bq[ks][0]), h23 = h2_to_f2(bq[ks][1]);
+        bl[ks % NL][0] = pack_h2(x[0] - h01.x, x[1] - h01.y);
+        bl[ks % NL][1] = pack_h2(x[2] - h23.x, x[3] - h23.y);
       }
     }
     // per head of this lane's C columns: the score unit and bias from the
@@ -641,17 +652,17 @@ struct Warp {
           const int par = g & 1;
           const uint4 e = *reinterpret_cast<const uint4*>(tab + v0 + 8 * par);
           const uint32_t es[2] = {e.x, e.z}, em[2] = {e.y, e.w};
-          float hi[2], lo[2];
+          float x[2];
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             const int ch = static_cast<int>(em[i] >> 16);
             const float qv = static_cast<const float*>(qs)[hrow() * kQRow + ch];
-            bias = fmaf(qv, bf2f(em[i] & 0xffffu), bias);
-            const float x = qv * __uint_as_float(es[i]) * sq;
-            hi[i] = round_f16_precision(x);
-            lo[i] = x - hi[i];
+            bias = fmaf(qv, bf16_lo(em[i]), bias);
+            x[i] = qv * __uint_as_float(es[i]) * sq;
           }
-          const uint32_t H = pack_h2(hi[0], hi[1]), Lo = pack_h2(lo[0], lo[1]);
+          const uint32_t H = pack_h2(x[0], x[1]);
+          const float2 hf = h2_to_f2(H);
+          const uint32_t Lo = pack_h2(x[0] - hf.x, x[1] - hf.y);
           const uint32_t recv = __shfl_xor_sync(kFull, par ? H : Lo, 4);
           bq0 = par ? recv : H;
           bq1 = par ? Lo : recv;
@@ -660,20 +671,19 @@ struct Warp {
           const uint4 e89 = *reinterpret_cast<const uint4*>(tab + v0 + 8);
           const uint32_t es[4] = {e01.x, e01.z, e89.x, e89.z};
           const uint32_t em[4] = {e01.y, e01.w, e89.y, e89.w};
-          float hi[4], lo[4];
+          float x[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int ch = static_cast<int>(em[i] >> 16);
             const float qv = bf2f(static_cast<const uint16_t*>(qs)[g * kQRow + ch]);
-            bias = fmaf(qv, bf2f(em[i] & 0xffffu), bias);
-            const float x = qv * __uint_as_float(es[i]) * sq;
-            hi[i] = round_f16_precision(x);
-            lo[i] = x - hi[i];
+            bias = fmaf(qv, bf16_lo(em[i]), bias);
+            x[i] = qv * __uint_as_float(es[i]) * sq;
           }
-          bq0 = pack_h2(hi[0], hi[1]);
-          bq1 = pack_h2(hi[2], hi[3]);
-          bl0 = pack_h2(lo[0], lo[1]);
-          bl1 = pack_h2(lo[2], lo[3]);
+          bq0 = pack_h2(x[0], x[1]);
+          bq1 = pack_h2(x[2], x[3]);
+          const float2 h01 = h2_to_f2(bq0), h23 = h2_to_f2(bq1);
+          bl0 = pack_h2(x[0] - h01.x, x[1] - h01.y);
+          bl1 = pack_h2(x[2] - h23.x, x[3] - h23.y);
         }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
@@ -707,9 +717,10 @@ struct Warp {
   __device__ __forceinline__ void softmax_update(float (&S)[8][4], const float (&hinv)[2],
                                                  const float (&hoff)[2], float (&alpha)[2]) {
     if constexpr (SPARE) {
-      float m = -INFINITY;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) m = fmaxf(m, fmaxf(S[mt][0], S[mt][2]));
+      float m = max3(max3(S[0][0], S[0][2], S[1][0]), max3(S[1][2], S[2][0], S[2][2]),
+                     max3(S[3][0], S[3][2], S[4][0]));
+      m = max3(m, max3(S[4][2], S[5][0], S[5][2]), max3(S[6][0], S[6][2], S[7][0]));
+      m = fmaxf(m, S[7][2]);
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 16));
@@ -731,9 +742,10 @@ struct Warp {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const float off = hoff[h];
-        float m = -INFINITY;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) m = fmaxf(m, fmaxf(S[mt][h], S[mt][h + 2]));
+        float m = max3(max3(S[0][h], S[0][h + 2], S[1][h]), max3(S[1][h + 2], S[2][h], S[2][h + 2]),
+                       max3(S[3][h], S[3][h + 2], S[4][h]));
+        m = max3(m, max3(S[4][h + 2], S[5][h], S[5][h + 2]), max3(S[6][h], S[6][h + 2], S[7][h]));
+        m = fmaxf(m, S[7][h + 2]);
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 16));
@@ -766,14 +778,12 @@ struct Warp {
       const float4 f = reinterpret_cast<const float4*>(vscale)[4 * lane + i];
       vs[i][0] = f.x; vs[i][1] = f.y; vs[i][2] = f.z; vs[i][3] = f.w;
       const uint2 m = vmin2[4 * lane + i];
-      vmn[i][0] = bf2f(m.x & 0xffffu); vmn[i][1] = bf2f(m.x >> 16);
-      vmn[i][2] = bf2f(m.y & 0xffffu); vmn[i][3] = bf2f(m.y >> 16);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        mx = fmaxf(mx, vs[i][j]);
-        mm = fmaxf(mm, fabsf(vmn[i][j]));
-      }
+      vmn[i][0] = bf16_lo(m.x); vmn[i][1] = bf16_hi(m.x);
+      vmn[i][2] = bf16_lo(m.y); vmn[i][3] = bf16_hi(m.y);
+      mx = max3(mx, max3(vs[i][0], vs[i][1], vs[i][2]), vs[i][3]);
+      mm = max3_abs(mm, max3_abs(vmn[i][0], vmn[i][1], vmn[i][2]), vmn[i][3]);
     }
+    mm = fabsf(mm);
     // one power-of-two unit for the group's steps and one for its origins
     // (steps are >= 0, so their bit patterns order like their values)
     mx = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(mx)));
@@ -799,6 +809,8 @@ struct Warp {
       vmb[vmb_index(kt, j, t0, chi)] = pack_h2(vmn[0][j] * svm, vmn[1][j] * svm);
       vmb[vmb_index(kt, j, t0 + 1, chi)] = pack_h2(vmn[2][j] * svm, vmn[3][j] * svm);
     }
+    // the zero row the origin MMA's rows 4..7 read
+    reinterpret_cast<uint2*>(vmb + kZeroRow)[lane] = make_uint2(0u, 0u);
   }
 
   // Channel tile mc (16 channels) of one group's P·V with B fragments bj,
@@ -875,8 +887,9 @@ struct Warp {
         pb[kt][0] = movmatrix_t(pack_h2(S[kt][0], S[kt][1]));
         pb[kt][1] = movmatrix_t(pack_h2(S[kt][2], S[kt][3]));
       }
-      const uint2 av = *reinterpret_cast<const uint2*>(vmb + vmb_index(kt, g & 3, t, 0));
-      const uint32_t a0 = g < 4 ? av.x : 0u, a2 = g < 4 ? av.y : 0u;
+      // lanes g >= 4 (A rows 4..7) read the zero row
+      const uint2 av = *reinterpret_cast<const uint2*>(vmb + (g < 4 ? vmb_index(0, g, t, 0) : kZeroRow + 2 * t) + 8 * kt);
+      const uint32_t a0 = av.x, a2 = av.y;
       mma_f16(Dvm, a0, 0u, a2, 0u, pb[kt][0], pb[kt][1]);
     }
     const uint8_t* vc = vbuf + (L.v_codes - L.kpart);
@@ -1136,22 +1149,62 @@ struct Warp {
       }
     }
   }
+
+  // An empty partial (o = 0, m = -inf, l = 0: it weighs nothing in the
+  // merge) for a unit this warp gave up on, so the combine never reads a
+  // slot left over from an earlier call.
+  __device__ __forceinline__ void empty_part(int u, int part) {
+    float* base = a.ws + (static_cast<long long>(u) * a.max_parts + part) * NREP * (kD + 2);
+    for (int i = lane; i < NREP * (kD + 2); i += 32) {
+      const int c = i % (kD + 2);
+      base[i] = c == kD ? -INFINITY : 0.0f;
+    }
+  }
 };
+
 
 template <int KB, int VB, int NREP, bool MIX>
 __global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX) * 32, 1) decode_mma_kernel(MmaArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
-  // consecutive slices (records of one unit, contiguous in memory) run on
-  // different SMs, so each SM's warps read from several places at once
-  const int slot = warp * gridDim.x + blockIdx.x;
+  // Consecutive slices (records of one unit, contiguous in memory) run on
+  // different SMs, so each SM's warps read from several places at once; row
+  // w of the grid is rotated by w, so a block's warps take slices from
+  // different places of the unit pattern.  (Unrotated, with every unit
+  // spanning a multiple of the grid width in slices, a block's slices all
+  // sat at the same place: blocks carried unequal numbers of groups and the
+  // units' window items all landed on a few SMs.)
+  const int slot = warp * gridDim.x + (blockIdx.x + warp) % gridDim.x;
   // the combine kernel may be scheduled now; it waits for this grid's results
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   if (slot >= a.n_slots) return;            // warp-uniform
   uint8_t* mine = smem + static_cast<size_t>(warp) * (a.rec_bytes + warp_extra(MIX));
   Warp<KB, VB, NREP, MIX> W(a, mine);
   const long long p0 = slot_start(a, slot), p1 = slot_start(a, slot + 1);
-  for (int u = static_cast<int>(p0 / a.unit_len); u <= static_cast<int>((p1 - 1) / a.unit_len); ++u) {
+  const int u_last = static_cast<int>((p1 - 1) / a.unit_len);
+  // after a wait gave up: empty partials for this unit and the rest of the slice
+  auto abandon = [&](int u0) {
+    for (int uu = u0; uu <= u_last; ++uu)
+      W.empty_part(uu, slot - slot_of(a, static_cast<long long>(uu) * a.unit_len));
+  };
+  // The bf16 windows this slice reads last go to L2 now, so their chunk
+  // copies (two in flight) do not wait on HBM at the end of the slice.
+  if (W.lane == 0) {
+    for (int u = static_cast<int>(p0 / a.unit_len); u <= u_last; ++u) {
+      const long long ub = static_cast<long long>(u) * a.unit_len;
+      const long long lo = max(p0, ub) - ub, hi = min(p1, ub + a.unit_len) - ub;
+      if (a.r > 0 && lo <= a.n_groups && a.n_groups < hi) {
+        prefetch_l2(a.res_k + static_cast<long long>(u) * kR * kD, a.r * kD * 2);
+        prefetch_l2(a.res_v + static_cast<long long>(u) * kR * kD, a.r * kD * 2);
+      }
+      const long long ps = a.n_groups + (a.r > 0 ? kResidualWeight : 0);
+      if (a.s > 0 && lo <= ps && ps < hi) {
+        prefetch_l2(a.sink_k + static_cast<long long>(u) * a.n_sink * kD, a.s * kD * 2);
+        prefetch_l2(a.sink_v + static_cast<long long>(u) * a.n_sink * kD, a.s * kD * 2);
+      }
+    }
+  }
+  for (int u = static_cast<int>(p0 / a.unit_len); u <= u_last; ++u) {
     const long long ub = static_cast<long long>(u) * a.unit_len;
     const long long lo = max(p0, ub) - ub, hi = min(p1, ub + a.unit_len) - ub;
     const int g0 = static_cast<int>(lo);
@@ -1172,6 +1225,7 @@ __global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX) * 32, 1) decode_m
         const bool more = gi + 1 < g1;
         if (!W.wait_part(W.mb_k, W.ph_k)) {   // keys of gi (bounded wait)
           W.wait_part(W.mb_v, W.ph_v);        // the value copy in flight
+          abandon(u);
           return;
         }
         float S[8][4], hinv[2], hbias[2], alpha[2], svn, inv_svm;
@@ -1180,6 +1234,7 @@ __global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX) * 32, 1) decode_m
         if (more) W.issue_k(u, gi + 1);
         if (!W.wait_part(W.mb_v, W.ph_v)) {   // values of gi
           if (more) W.wait_part(W.mb_k, W.ph_k);
+          abandon(u);
           return;
         }
         // the value tables' shared-memory round trip overlaps the softmax
@@ -1339,8 +1394,8 @@ template <int KB, int VB, int NREP, bool MIX>
 cudaError_t launch_cfg(const MmaArgs& a, int warps, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(warps) * (a.rec_bytes + warp_extra(MIX));
   auto kern = decode_mma_kernel<KB, VB, NREP, MIX>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  static SmemOptIn opt_in;
+  cudaError_t e = opt_in.ensure(kern);
   if (e != cudaSuccess) return e;
   const int grid = (a.n_slots + warps - 1) / warps;
   kern<<<grid, warps * 32, smem, s>>>(a);
@@ -1358,7 +1413,14 @@ cudaError_t launch_rep(const MmaArgs& a, int nrep, int warps, cudaStream_t s) {
   }
 }
 
+std::atomic<int> g_wait_polls{kWaitPolls};
+
 }  // namespace
+
+int decode_wait_polls() { return g_wait_polls.load(std::memory_order_relaxed); }
+void set_decode_wait_polls(int polls) {
+  g_wait_polls.store(polls < 0 ? kWaitPolls : polls, std::memory_order_relaxed);
+}
 
 int mma_warps_per_cta(const RecLayout& lay, int n_rep) {
   // one record buffer plus the query (and, with mixed keys, the tables) per
@@ -1408,6 +1470,10 @@ cudaError_t launch_combine_parts(const float* ws, int B, int Hkv, int Hq, int ma
       combine_parts_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
       cudaSharedmemCarveoutMaxShared);
   if (carve != cudaSuccess) return carve;
+  static const cudaError_t carve_many = cudaFuncSetAttribute(
+      combine_many_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+      cudaSharedmemCarveoutMaxShared);
+  if (carve_many != cudaSuccess) return carve_many;
   // rows of up to 32 partials: one round trip per row; more: 8 warps a row
   const bool many = max_parts > 32;
   cudaLaunchConfig_t lc = {};
@@ -1455,6 +1521,7 @@ cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, flo
   a.total = static_cast<long long>(a.units) * a.unit_len;
   a.ws = ws;
   a.status = c->status;
+  a.wait_polls = decode_wait_polls();
   const int nrep = Hq / c->cfg.kv_heads;
   const int kb = c->cfg.k_bits, vb = c->cfg.v_bits;
   const int warps = mma_warps_per_cta(c->lay, nrep);

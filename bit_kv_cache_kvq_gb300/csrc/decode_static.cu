@@ -63,9 +63,11 @@ extern "C" int kvq_decode_attention_static(const kvq_cache* c, const kvq_bf16* q
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (dev != c->device) return KVQ_ERR_ARG;   // the array of the cache's own device
   void* ws = nullptr;
   if (static_ws_address(dev, &ws) != cudaSuccess) return KVQ_ERR_CUDA;
-  // Every partial the combine reads is rewritten by this call, so nothing
+  // Every partial the combine reads is rewritten by this call (a warp whose
+  // wait gave up writes empty partials for the units it leaves), so nothing
   // in the array has to start at zero.
   return launch_decode_mma(c, q, Hq, out, static_cast<float*>(ws), plan, nullptr, nullptr, s) ==
                  cudaSuccess

@@ -2,6 +2,7 @@
 // handle and the kernel launchers shared between translation units.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -30,6 +31,13 @@ constexpr int kMaxRep = 8;         // query heads per KV head
 //                           order (frag_layout.h)
 //   [kc]           kscale   fp32  [D]
 //   [kc+4D]        kmin     bf16  [D]
+// KIVI key (KIVI article: keys per channel in groups of 32 tokens, metadata
+// in the input dtype):
+//   [0]            K codes  128*128*kb/8 bytes, fragment order as uniform
+//   [kc]           kstep    bf16  [4][D]   per 32-token sub-group and channel
+//   [kc+8D]        kmin     bf16  [4][D]
+//   value part:    codes as uniform, vstep bf16 [128][D/32], vmin bf16
+//                  [128][D/32]; zero for tokens still in the value FIFO
 // Mixed key: the group's own counts nb (BF16), n4 (UINT4), n2 = D - nb - n4
 // (UINT2) are in its header; rank tiers fix them to the config's n_bf16,
 // n_uint4, threshold tiers bound them by those (the sections are sized for
@@ -56,6 +64,7 @@ constexpr int kMaxRep = 8;         // query heads per KV head
 // ---------------------------------------------------------------------------
 struct RecLayout {
   int mixed;
+  int kivi;      // KIVI variant: bf16 metadata, keys in four 32-token sub-groups
   int kb, vb;
   int thresh;    // mixed: threshold tiers (per-group counts up to nb, n4)
   int nb, n4;    // mixed: BF16 / UINT4 channels a group (rank tiers) or at most
@@ -78,11 +87,24 @@ struct RecLayout {
 __host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
 
 __host__ __device__ inline RecLayout make_layout(int mixed, int kb, int vb,
-                                                 int nb, int n4, int thresh) {
+                                                 int nb, int n4, int thresh, int kivi = 0) {
   RecLayout L{};
   L.mixed = mixed;
+  L.kivi = kivi;
   L.kb = kb;
   L.vb = vb;
+  if (kivi) {
+    // KIVI: steps then origins, bf16 [4 sub-groups of 32 tokens][D]
+    L.k_codes = 0;
+    L.k_scale = kD * kKG * kb / 8;
+    L.k_min = L.k_scale + 2 * 4 * kD;
+    L.kpart = (L.k_min + 2 * 4 * kD + 127) & ~127;
+    L.v_codes = L.kpart;
+    L.v_scale = L.v_codes + kKG * kD * vb / 8;        // bf16 [128][D/32]
+    L.v_min = L.v_scale + 2 * kKG * kVGroups;
+    L.bytes = (L.v_min + 2 * kKG * kVGroups + 127) & ~127;
+    return L;
+  }
   if (!mixed) {
     L.k_codes = 0;
     L.k_scale = kD * kKG * kb / 8;
@@ -142,6 +164,32 @@ struct kvq_cache {
 
 namespace kvq {
 
+// Raises one kernel's dynamic shared-memory limit to the device's opt-in
+// maximum, once per device (a cudaFuncSetAttribute round trip on every
+// launch would add host time to every call).  One instance per kernel.
+struct SmemOptIn {
+  std::atomic<unsigned long long> done{0};   // bit d: device d is set up
+  template <typename K>
+  cudaError_t ensure(K kernel) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    int most = 0;
+    e = cudaDeviceGetAttribute(&most, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+};
+
+// Polls a decode warp makes before its wait for a staged record part gives
+// up (KVQ_FLAG_TIMEOUT); kvq_set_wait_limit changes it for failure tests.
+int decode_wait_polls();
+void set_decode_wait_polls(int polls);
+
 // Where the quantize kernel reads its 128-token tiles from.
 struct QuantSrc {
   const kvq_bf16* k;
@@ -165,6 +213,16 @@ cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
                             int first_group, const float* importance,
                             cudaStream_t s);
 
+
+// KIVI variant (kivi.cu): seal n_records key records from 128-token tiles of
+// src.k (unit u, record k at u * unit_stride + k * group_stride elements),
+// zeroing their value parts; quantize the values of tokens [t0, t1) of
+// records first_record.. from src.v rows (record k's token t at k *
+// group_stride + t * D), limited to the first n_valid tokens of the history.
+cudaError_t launch_kivi_seal(const kvq_cache* c, QuantSrc src, int n_records, int first_record,
+                             cudaStream_t s);
+cudaError_t launch_kivi_values(const kvq_cache* c, QuantSrc src, int n_records, int first_record,
+                               int t0, int t1, int n_valid, cudaStream_t s);
 
 // Tensor-core decode (decode_mma.cu).  The plan cuts the weighted item
 // sequence (per unit: its groups, then its residual) into n_slots warp

@@ -76,6 +76,42 @@ __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// max(a, b, c): one three-input min/max instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// max(|a|, |b|, |c|) in magnitude (the sign of the result is not relied on).
+__device__ __forceinline__ float max3_abs(float a, float b, float c) {
+  float d;
+  asm("max.abs.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// The bf16 in the low (high) half of w as an fp32, computed as x * 1 + (-0)
+// by a mixed-precision FMA (exact, sign of zero kept), which keeps the
+// conversion off the integer/logic pipe.
+__device__ __forceinline__ float bf16_lo(uint32_t w) {
+  float d;
+  asm("{\n .reg .b16 l, h, one;\n mov.b32 {l, h}, %1;\n mov.b16 one, 0x3F80;\n"
+      " fma.rn.f32.bf16 %0, l, one, 0f80000000;\n}\n"
+      : "=f"(d) : "r"(w));
+  return d;
+}
+__device__ __forceinline__ float bf16_hi(uint32_t w) {
+  float d;
+  asm("{\n .reg .b16 l, h, one;\n mov.b32 {l, h}, %1;\n mov.b16 one, 0x3F80;\n"
+      " fma.rn.f32.bf16 %0, h, one, 0f80000000;\n}\n"
+      : "=f"(d) : "r"(w));
+  return d;
+}
+
+// f16x2 (low half = lo) back to two fp32 values.
+__device__ __forceinline__ float2 h2_to_f2(uint32_t h) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
 // Power-of-two normalizer for a non-negative magnitude x: returns s with
 // x*s in [0.5, 1) for ordinary x (clamped at the extremes), and 1/s.
 __device__ __forceinline__ void pow2_norm(float x, float& s, float& inv) {

@@ -697,10 +697,6 @@ cudaError_t gather(const kvq_cache* c, int off, int bytes, void* dst,
 
 constexpr int kQuantSmem = kTileBytes + kParamBytes;  // 38 KB
 
-template <typename K>
-cudaError_t set_smem(K kernel, int bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-}
 
 }  // namespace
 
@@ -742,7 +738,8 @@ cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
   cudaError_t e = cudaSuccess;
 #define KVQ_LAUNCH(KERNEL, SMEM)                             \
   do {                                                       \
-    e = set_smem(KERNEL, SMEM);                              \
+    static SmemOptIn opt_in;                                 \
+    e = opt_in.ensure(KERNEL);                               \
     if (e != cudaSuccess) return e;                          \
     KERNEL<<<grid, 256, SMEM, s>>>(a);                       \
   } while (0)

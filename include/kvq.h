@@ -277,9 +277,16 @@ int kvq_decode_step(kvq_cache* cache, const kvq_bf16* k_new, const kvq_bf16* v_n
  *  - The first call on a device looks the array's device address up once
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture.
+ *  - Call it with the cache's own device current (KVQ_ERR_ARG otherwise).
+ *    The cached address belongs to that device's primary context: after a
+ *    cudaDeviceReset (or anything else that destroys that context) the
+ *    library must be reloaded before this entry point is used again.
  *  - All calls share the one array, so calls whose work overlaps on the GPU
  *    (other streams, other threads) race and corrupt each other's results;
- *    serialize them.  Each call rewrites every workspace entry it reads.
+ *    serialize them.  Each call rewrites every workspace entry it reads: a
+ *    decode warp whose wait gave up (KVQ_FLAG_TIMEOUT) writes empty
+ *    partials for the rows it leaves, so no earlier call's partial enters
+ *    the merge, but that call's output is undefined (rows may be NaN).
  *  - The split of the token axis is reduced to fit the array.  Two partial
  *    slots per query row, 2*B*Hq*(D+2)*4 bytes, must fit (B*Hq <= 8065
  *    query rows); beyond that it returns KVQ_ERR_WORKSPACE.
@@ -359,6 +366,20 @@ int kvq_export_k_mixed(const kvq_cache* cache, uint8_t* counts, uint8_t* perm, k
  * kvq_cache_sink_tokens; NULL allowed when s = 0).  Errors: ARG, CUDA.
  */
 int kvq_export_sink(const kvq_cache* cache, kvq_bf16* k, kvq_bf16* v, cudaStream_t s);
+
+/*
+ * Failure-detection hook (no counterpart on the pages).  Every wait of a
+ * decode warp for a record part it staged is bounded: after `polls` polls
+ * of the barrier (default 2^20, restored by a negative value) the warp sets
+ * KVQ_FLAG_TIMEOUT in the cache's status word, waits for its copy in flight
+ * with the default limit (so no copy outlives the warp), writes empty
+ * partials (weight 0) for the rows it leaves and returns; that call's
+ * output is undefined.  polls = 0 makes every first wait give up at once,
+ * which is how the tests exercise this path without a fault.  The setting
+ * is process-wide and applies to launches enqueued after the call; it is
+ * not meant for production use.  Returns the previous limit.
+ */
+int kvq_set_wait_limit(int polls);
 
 /* Human-readable name of a return code. */
 const char* kvq_status_string(int code);
