@@ -160,7 +160,7 @@ def kernel_source_hash():
     space dropped, so the key follows the code, not its comments."""
     import re
     h = hashlib.sha256()
-    for name in ("decode_mma.cu", "frag_layout.h", "kvq_internal.h"):
+    for name in ("decode_mma.cuh", "decode_mma.cu", "frag_layout.h", "kvq_internal.h"):
         with open(os.path.join(ROOT, "bit_kv_cache_kvq_gb300", "csrc", name)) as f:
             for line in f:
                 code = re.sub(r"//.*", "", line).strip()
@@ -177,8 +177,16 @@ def mixed_k_group_bytes(w):
     return 128 + w.n_bf16 * 256 + w.n_uint4 * 64 + n2 * 32 + (w.n_uint4 + n2) * 6
 
 
+def kivi_half_bytes(w):
+    """KIVI variant, one token's key (or value): codes plus a bf16 origin and
+    step per 32-element group (the KIVI article's 3 bits per element at 2 bits)."""
+    return 128 * w.k_bits // 8 + 16
+
+
 def token_bytes(w):
     """Algorithmic bytes of one quantized token of one (b, kv head)."""
+    if w.mode == "kivi":
+        return 2 * kivi_half_bytes(w)
     v = 128 * w.v_bits // 8 + 24
     if w.mode == "mixed":
         return mixed_k_group_bytes(w) / 128 + v
@@ -187,13 +195,21 @@ def token_bytes(w):
 
 def attention_bytes(w, T_q, r):
     """Packed cache + bf16 residual + q (bf16) + o (fp32) of one decode
-    attention call."""
+    attention call.  KIVI: T_q quantized keys and r bf16 residual keys; of the
+    T_q + r values the last min(T_q + r, 128) are bf16 (the FIFO)."""
     U = w.B * w.Hkv
-    return U * (T_q * token_bytes(w) + r * 512) + w.B * w.Hq * (256 + 512)
+    qo = w.B * w.Hq * (256 + 512)
+    if w.mode == "kivi":
+        fifo = min(T_q + r, 128)
+        return U * ((T_q + T_q + r - fifo) * kivi_half_bytes(w) + (r + fifo) * 256) + qo
+    return U * (T_q * token_bytes(w) + r * 512) + qo
 
 
 def append_bytes(w):
-    return w.B * w.Hkv * 2 * 2 * 256  # read k_new, v_new; write residual slots
+    """Read k_new, v_new; write the residual slots (KIVI: and the value
+    leaving the FIFO, read and written quantized)."""
+    extra = 256 + kivi_half_bytes(w) if w.mode == "kivi" else 0
+    return w.B * w.Hkv * (2 * 2 * 256 + extra)
 
 
 def flush_bytes(w):
@@ -245,6 +261,9 @@ def config_of(w, extra=None):
     if w.mode == "mixed":
         c.update({"k_mode": "mixed", "n_bf16": w.n_bf16, "n_uint4": w.n_uint4,
                   "n_uint2": 128 - w.n_bf16 - w.n_uint4, "query_window": w.Lq})
+    if w.mode == "kivi":
+        c.update({"k_mode": "kivi", "k_group_tokens": 32, "key_seal_tokens": 128,
+                  "value_fifo_tokens": 128, "metadata": "bf16"})
     if extra:
         c.update(extra)
     return c
@@ -265,6 +284,12 @@ class OracleSample:
         for j in range(n_units):
             u = scaled(self.one, seed=self.one.seed + 17 * j)
             K, V = make_kv(u)
+            if u.mode == "kivi":
+                c = oracle_mod.KiviOracleCache(1, 1, 128, u.k_bits, u.v_bits)
+                c.prefill(bf16_bits(K), bf16_bits(V))
+                c.T_q, c.r = c.lengths()[:2]
+                self.units.append((u, c, [bf16_bits(make_q(u, step=s)) for s in range(4)]))
+                continue
             c = oracle_mod.OracleCache(1, 1, 128, u.k_bits, u.v_bits, mode=u.mode,
                                        n_bf16=u.n_bf16, n_uint4=u.n_uint4)
             imp = None

@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "KVCache", "decode_bf16", "channel_saliency", "KVQError", "lib",
-    "KVQ_K_UNIFORM", "KVQ_K_MIXED", "TIER_BF16", "TIER_UINT4", "TIER_UINT2",
+    "KVQ_K_UNIFORM", "KVQ_K_MIXED", "KVQ_K_KIVI", "TIER_BF16", "TIER_UINT4", "TIER_UINT2",
     "FLAG_NONFINITE", "FLAG_RANGE", "FLAG_TIMEOUT", "set_wait_limit", "HEAD_DIM", "K_GROUP", "V_GROUP", "RESIDUAL",
 ]
 
@@ -24,7 +24,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libkvq.so")
 
 HEAD_DIM, K_GROUP, V_GROUP, RESIDUAL = 128, 128, 32, 128
-KVQ_K_UNIFORM, KVQ_K_MIXED = 0, 1
+KVQ_K_UNIFORM, KVQ_K_MIXED, KVQ_K_KIVI = 0, 1, 2
+_MODES = {"uniform": KVQ_K_UNIFORM, "mixed": KVQ_K_MIXED, "kivi": KVQ_K_KIVI}
 TIER_BF16, TIER_UINT4, TIER_UINT2 = 0, 1, 2
 TIERS_RANK, TIERS_THRESHOLD = 0, 1
 FLAG_NONFINITE, FLAG_RANGE, FLAG_TIMEOUT = 1, 2, 4
@@ -45,7 +46,8 @@ class _Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "batch", "kv_heads", "head_dim", "max_tokens", "k_bits", "v_bits", "k_mode",
         "n_bf16", "n_uint4", "n_sink", "tier_mode")] + [
-        ("tau_bf16", ctypes.c_float), ("tau_uint4", ctypes.c_float)]
+        ("tau_bf16", ctypes.c_float), ("tau_uint4", ctypes.c_float),
+        ("n_high_pairs", ctypes.c_int), ("pair_layout", ctypes.c_int)]
 
 
 class _TierSpec(ctypes.Structure):
@@ -81,6 +83,7 @@ _SIGS = {
     "kvq_export_sink": (_I, [_P, _P, _P, _P]),
     "kvq_export_k_mixed": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvq_set_wait_limit": (_I, [_I]),
+    "kvq_export_kivi": (_I, [_P] * 10),
     "kvq_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -144,8 +147,10 @@ class KVCache:
                  tier_mode: str = "rank", tau_bf16: float = 0.0, tau_uint4: float = 0.0):
         if tier_mode not in ("rank", "threshold"):
             raise ValueError("tier_mode is 'rank' or 'threshold'")
+        if mode not in _MODES:
+            raise ValueError("mode is 'uniform', 'mixed' or 'kivi'")
         self.cfg = _Config(batch, kv_heads, head_dim, max_tokens, k_bits, v_bits,
-                           KVQ_K_MIXED if mode == "mixed" else KVQ_K_UNIFORM, n_bf16, n_uint4,
+                           _MODES[mode], n_bf16, n_uint4,
                            n_sink, TIERS_THRESHOLD if tier_mode == "threshold"
                            else TIERS_RANK, tau_bf16, tau_uint4)
         self.tier_mode = tier_mode
@@ -304,6 +309,32 @@ class KVCache:
         _check(lib().kvq_export_sink(self._h, ks.data_ptr(), vs.data_ptr(), _stream(stream)),
                "kvq_export_sink")
         return ks, vs
+
+    def export_kivi(self, stream=None):
+        """KIVI cache state (kvq_export_kivi): dict of device tensors k_codes
+        [B, Hkv, n*4, D, 32*bits/8], k_origin/k_step bf16 [B, Hkv, n*4, D],
+        v_codes [B, Hkv, n*128, D*bits/8], v_origin/v_step bf16 [B, Hkv,
+        n*128, D/32], k_res [B, Hkv, r_K, D], v_res [B, Hkv, r_V, D] (FIFO,
+        oldest first); n = T_k / 128."""
+        tk, rk = self.lengths()
+        n, rv = tk // K_GROUP, min(tk + rk, RESIDUAL)
+        B, H, dev, b = self.batch, self.kv_heads, self.device, self.k_bits
+        out = {
+            "k_codes": torch.zeros(B, H, n * 4, HEAD_DIM, 32 * b // 8, dtype=torch.uint8, device=dev),
+            "k_origin": torch.zeros(B, H, n * 4, HEAD_DIM, dtype=torch.bfloat16, device=dev),
+            "k_step": torch.zeros(B, H, n * 4, HEAD_DIM, dtype=torch.bfloat16, device=dev),
+            "v_codes": torch.zeros(B, H, n * 128, HEAD_DIM * self.v_bits // 8, dtype=torch.uint8,
+                                   device=dev),
+            "v_origin": torch.zeros(B, H, n * 128, HEAD_DIM // V_GROUP, dtype=torch.bfloat16, device=dev),
+            "v_step": torch.zeros(B, H, n * 128, HEAD_DIM // V_GROUP, dtype=torch.bfloat16, device=dev),
+            "k_res": torch.zeros(B, H, rk, HEAD_DIM, dtype=torch.bfloat16, device=dev),
+            "v_res": torch.zeros(B, H, rv, HEAD_DIM, dtype=torch.bfloat16, device=dev),
+        }
+        ptr = lambda t: t.data_ptr() if t.numel() else None
+        _check(lib().kvq_export_kivi(self._h, *(ptr(out[k]) for k in (
+            "k_codes", "k_origin", "k_step", "v_codes", "v_origin", "v_step", "k_res", "v_res")),
+            _stream(stream)), "kvq_export_kivi")
+        return out
 
     def export_k_mixed(self, stream=None):
         tq, _ = self.lengths()

@@ -39,7 +39,8 @@ def _sources():
 
 
 def _deps():
-    return _sources() + glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(INCLUDE, "kvq.h"), __file__]
+    return (_sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
+            + [os.path.join(INCLUDE, "kvq.h"), __file__])
 
 
 def up_to_date() -> bool:

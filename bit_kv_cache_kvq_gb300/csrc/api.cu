@@ -25,6 +25,14 @@ bool valid_config(const kvq_config* c) {
   if (c->n_sink < 0 || c->n_sink > kR) return false;
   if (c->k_mode == KVQ_K_UNIFORM) {
     if (c->k_bits != 2 && c->k_bits != 4) return false;
+  } else if (c->k_mode == KVQ_K_PNMIX) {
+    if (c->n_high_pairs < 0 || c->n_high_pairs > kD / 2 || c->n_high_pairs % 16) return false;
+    if (c->pair_layout != KVQ_PAIRS_ADJACENT && c->pair_layout != KVQ_PAIRS_SPLIT) return false;
+    if (c->n_sink != 0) return false;
+  } else if (c->k_mode == KVQ_K_KIVI) {
+    // KIVI-2 and KIVI-4: keys and values at the same width; no sink window
+    if ((c->k_bits != 2 && c->k_bits != 4) || c->v_bits != c->k_bits) return false;
+    if (c->n_sink != 0) return false;
   } else if (c->k_mode == KVQ_K_MIXED) {
     if (c->n_bf16 < 0 || c->n_uint4 < 0 || c->n_bf16 + c->n_uint4 > kD) return false;
     if (c->tier_mode == KVQ_TIERS_THRESHOLD) {
@@ -41,11 +49,79 @@ bool valid_config(const kvq_config* c) {
 RecLayout layout_of(const kvq_config* c) {
   return make_layout(c->k_mode == KVQ_K_MIXED, c->k_mode == KVQ_K_MIXED ? 2 : c->k_bits,
                      c->v_bits, c->n_bf16, c->n_uint4,
-                     c->k_mode == KVQ_K_MIXED && c->tier_mode == KVQ_TIERS_THRESHOLD);
+                     c->k_mode == KVQ_K_MIXED && c->tier_mode == KVQ_TIERS_THRESHOLD,
+                     c->k_mode == KVQ_K_KIVI,
+                     c->k_mode == KVQ_K_PNMIX ? 2 * c->n_high_pairs : -1);
+}
+
+bool is_pnmix(const kvq_cache* c) { return c->cfg.k_mode == KVQ_K_PNMIX; }
+
+bool is_kivi(const kvq_cache* c) { return c->cfg.k_mode == KVQ_K_KIVI; }
+
+// Rows [first, first + count) of src [units][L][D] into rows [dst_first,
+// dst_first + count) of dst [units][cap][D].
+cudaError_t copy_rows(const kvq_bf16* src, int L, int first, int count, kvq_bf16* dst, int cap,
+                      int dst_first, int units, cudaStream_t s) {
+  if (count <= 0) return cudaSuccess;
+  const size_t row = static_cast<size_t>(kD) * sizeof(kvq_bf16);
+  return cudaMemcpy2DAsync(dst + static_cast<size_t>(dst_first) * kD, cap * row,
+                           src + static_cast<size_t>(first) * kD, static_cast<size_t>(L) * row,
+                           count * row, units, cudaMemcpyDeviceToDevice, s);
+}
+
+// KIVI prefill of L tokens: the persisted state of L appends ("KIVI: KV
+// cache axes" §5).  Keys: L - L mod 128 sealed in records; values: the
+// first L - min(L, 128) quantized token by token into their records; the
+// last min(L, 128) values in the FIFO ring (token t in slot t mod 128); the
+// key residual holds the last L mod 128 keys.
+int kivi_prefill(kvq_cache* c, const kvq_bf16* k, const kvq_bf16* v, int L, cudaStream_t s) {
+  const int n_rec = L / kKG, r = L % kKG;
+  if (n_rec * kKG > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
+  if (L == 0) return KVQ_OK;
+  const int units = c->cfg.batch * c->cfg.kv_heads;
+  const QuantSrc src{k, v, static_cast<long long>(L) * kD, static_cast<long long>(kKG) * kD};
+  cudaError_t e = launch_kivi_seal(c, src, n_rec, 0, s);
+  if (e == cudaSuccess && L > kKG) e = launch_kivi_values(c, src, n_rec, 0, 0, kKG, L - kKG, s);
+  if (e == cudaSuccess) e = copy_rows(k, L, n_rec * kKG, r, c->res_k, kR, 0, units, s);
+  if (e == cudaSuccess && n_rec > 0)   // tokens L - 128 .. 128 n_rec - 1 -> slots r .. 127
+    e = copy_rows(v, L, L - kKG, kKG - r, c->res_v, kR, r, units, s);
+  if (e == cudaSuccess) e = copy_rows(v, L, n_rec * kKG, r, c->res_v, kR, 0, units, s);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  c->t_q = n_rec * kKG;
+  c->r = r;
+  return KVQ_OK;
+}
+
+// KIVI append ("KIVI: KV cache axes" §4, Algorithm 1 order): once the FIFO
+// holds 128 values, the one the new token displaces (slot r, token T_k -
+// 128 + r of the newest record) is quantized into that record; the new key
+// and value take slot r; a key residual reaching 128 tokens is sealed into
+// a new record (four 32-token groups) and empties.
+int kivi_append(kvq_cache* c, const kvq_bf16* k_new, const kvq_bf16* v_new, cudaStream_t s) {
+  const bool seal = c->r + 1 == kR;
+  if (seal && c->t_q + kKG > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
+  cudaError_t e = cudaSuccess;
+  if (c->t_q > 0) {
+    const QuantSrc ring{nullptr, c->res_v, static_cast<long long>(kR) * kD, 0};
+    e = launch_kivi_values(c, ring, 1, c->t_q / kKG - 1, c->r, c->r + 1, 1 << 30, s);
+  }
+  if (e == cudaSuccess) e = launch_append(c, k_new, v_new, c->res_k, c->res_v, kR, c->r, s);
+  if (e == cudaSuccess && seal) {
+    const QuantSrc res{c->res_k, nullptr, static_cast<long long>(kR) * kD, 0};
+    e = launch_kivi_seal(c, res, 1, c->t_q / kKG, s);
+  }
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  if (seal) {
+    c->t_q += kKG;
+    c->r = 0;
+  } else {
+    c->r += 1;
+  }
+  return KVQ_OK;
 }
 
 struct Sizes {
-  size_t records, residual, sink, qacc, status, total;
+  size_t records, residual, sink, qacc, perm, status, total;
 };
 
 Sizes sizes_of(const kvq_config* c) {
@@ -56,8 +132,9 @@ Sizes sizes_of(const kvq_config* c) {
   s.residual = round_up(units * kR * kD * sizeof(kvq_bf16));
   s.sink = round_up(units * static_cast<size_t>(c->n_sink) * kD * sizeof(kvq_bf16));
   s.qacc = c->k_mode == KVQ_K_MIXED ? round_up(units * kD * sizeof(float)) : 0;
+  s.perm = c->k_mode == KVQ_K_PNMIX ? round_up(units * kD) : 0;
   s.status = kAlign;
-  s.total = s.records + 2 * s.residual + 2 * s.sink + s.qacc + s.status;
+  s.total = s.records + 2 * s.residual + 2 * s.sink + s.qacc + s.perm + s.status;
   return s;
 }
 
@@ -116,14 +193,16 @@ int kvq_cache_alloc(const kvq_config* cfg, void* dev_buf, size_t buf_bytes,
   c->sink_v = reinterpret_cast<kvq_bf16*>(c->base + sz.records + 2 * sz.residual + sz.sink);
   uint8_t* tail = c->base + sz.records + 2 * sz.residual + 2 * sz.sink;
   c->qacc = sz.qacc ? reinterpret_cast<float*>(tail) : nullptr;
-  c->status = reinterpret_cast<unsigned*>(tail + sz.qacc);
+  c->pn_perm = sz.perm ? tail + sz.qacc : nullptr;
+  c->pn_ready = false;
+  c->status = reinterpret_cast<unsigned*>(tail + sz.qacc + sz.perm);
   c->t_q = 0;
   c->r = 0;
   c->s = 0;
   c->q_steps = 0;
   c->q_rep = 0;
-  // the online |q| sums and the status word are adjacent: one memset
-  if (cudaMemsetAsync(tail, 0, sz.qacc + sizeof(unsigned), s) != cudaSuccess) {
+  // the online |q| sums, the PN-Mix order and the status word are adjacent
+  if (cudaMemsetAsync(tail, 0, sz.qacc + sz.perm + sizeof(unsigned), s) != cudaSuccess) {
     if (c->owned) cudaFreeAsync(c->base, s);
     delete c;
     return KVQ_ERR_CUDA;
@@ -164,13 +243,34 @@ int kvq_cache_reset(kvq_cache* c, cudaStream_t s) {
   c->s = 0;
   c->q_steps = 0;
   c->q_rep = 0;
+  c->pn_ready = false;   // a new prefill selects its pairs again
   return KVQ_OK;
+}
+
+int kvq_pnmix_pairs(kvq_cache* c, const kvq_bf16* q, int Hq, int Lq, const kvq_bf16* k, int Lk,
+                    float* sigma, cudaStream_t s) {
+  if (!c || !q || !k || Lq < 1 || Lk < 1) return KVQ_ERR_ARG;
+  if (!is_pnmix(c)) return KVQ_ERR_MODE;
+  if (Hq < c->cfg.kv_heads || Hq % c->cfg.kv_heads) return KVQ_ERR_SHAPE;
+  if (c->t_q != 0 || c->r != 0) return KVQ_ERR_NOT_EMPTY;
+  if (launch_pnmix_pairs(c, q, Hq, Lq, k, Lk, sigma, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  c->pn_ready = true;
+  return KVQ_OK;
+}
+
+int kvq_export_pnmix(const kvq_cache* c, uint8_t* codes, float* offset, float* scale,
+                     uint8_t* high, cudaStream_t s) {
+  if (!c) return KVQ_ERR_ARG;
+  if (!is_pnmix(c)) return KVQ_ERR_MODE;
+  if (c->t_q > 0 && (!codes || !offset || !scale)) return KVQ_ERR_ARG;
+  return cuda_status(launch_export_pnmix(c, codes, offset, scale, high, s));
 }
 
 int kvq_append_residual(kvq_cache* c, const kvq_bf16* k_new, const kvq_bf16* v_new,
                         cudaStream_t s) {
   if (!c || !k_new || !v_new) return KVQ_ERR_ARG;
   if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
+  if (is_kivi(c)) return kivi_append(c, k_new, v_new, s);
   if (c->s < c->cfg.n_sink) {   // the sequence's first tokens are the sinks
     const cudaError_t e = launch_append(c, k_new, v_new, c->sink_k, c->sink_v, c->cfg.n_sink,
                                         c->s, s);
@@ -192,12 +292,14 @@ static int check_importance(const kvq_cache* c, const float* importance) {
 
 int kvq_flush_group(kvq_cache* c, const float* importance, cudaStream_t s) {
   if (!c) return KVQ_ERR_ARG;
+  if (is_kivi(c)) return KVQ_ERR_MODE;   // KIVI seals its keys inside the append
   const bool mixed = c->cfg.k_mode == KVQ_K_MIXED;
   if (!mixed && importance) return KVQ_ERR_MODE;
   const bool window = mixed && !importance;   // I_d from the online window
   if (window && c->q_steps == 0) return KVQ_ERR_EMPTY;
   if (c->r != kR) return KVQ_ERR_RESIDUAL_NOT_FULL;
   if (c->t_q + kKG > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
+  if (is_pnmix(c) && !c->pn_ready) return KVQ_ERR_EMPTY;
   QuantSrc src{c->res_k, c->res_v, static_cast<long long>(kR) * kD, 0};
   cudaError_t e = launch_quantize(c, src, 1, c->t_q / kKG, importance, s);
   if (e == cudaSuccess && window)   // the next window starts from zero
@@ -232,6 +334,8 @@ int kvq_quantize_prefill(kvq_cache* c, const kvq_bf16* k, const kvq_bf16* v, int
   const int m = check_importance(c, importance);
   if (m != KVQ_OK) return m;
   if (c->t_q != 0 || c->r != 0 || c->s != 0) return KVQ_ERR_NOT_EMPTY;
+  if (is_kivi(c)) return kivi_prefill(c, k, v, L, s);
+  if (is_pnmix(c) && !c->pn_ready && L >= kKG) return KVQ_ERR_EMPTY;   // pairs not selected
   const int sk = L < c->cfg.n_sink ? L : c->cfg.n_sink;   // sink tokens
   const int n_q = (L - sk) / kKG;
   const int r = (L - sk) % kKG;
@@ -285,7 +389,7 @@ int kvq_decode_step(kvq_cache* c, const kvq_bf16* k_new, const kvq_bf16* v_new,
   if (!valid_rep(Hq, c->cfg.kv_heads)) return KVQ_ERR_SHAPE;
   if (!ws || ws_bytes < kvq_decode_workspace_bytes(c, Hq) || !aligned16(ws))
     return KVQ_ERR_WORKSPACE;
-  if (c->s < c->cfg.n_sink || c->r + 1 >= kR) {
+  if (is_kivi(c) || c->s < c->cfg.n_sink || c->r + 1 >= kR) {
     // the token goes to the sink window, or fills the residual (a flush
     // comes before the attention): the three calls in sequence
     int e = kvq_append_residual(c, k_new, v_new, s);
@@ -426,6 +530,30 @@ int kvq_set_wait_limit(int polls) {
   const int previous = decode_wait_polls();
   set_decode_wait_polls(polls);
   return previous;
+}
+
+int kvq_export_kivi(const kvq_cache* c, uint8_t* k_codes, kvq_bf16* k_origin, kvq_bf16* k_step,
+                    uint8_t* v_codes, kvq_bf16* v_origin, kvq_bf16* v_step, kvq_bf16* k_res,
+                    kvq_bf16* v_res, cudaStream_t s) {
+  if (!c) return KVQ_ERR_ARG;
+  if (!is_kivi(c)) return KVQ_ERR_MODE;
+  const int units = c->cfg.batch * c->cfg.kv_heads;
+  const int total = c->t_q + c->r, rv = total < kR ? total : kR;
+  cudaError_t e = cudaSuccess;
+  if (c->t_q > 0) {
+    if (!k_codes || !k_origin || !k_step || !v_codes || !v_origin || !v_step) return KVQ_ERR_ARG;
+    e = launch_export_kivi(c, k_codes, k_origin, k_step, v_codes, v_origin, v_step, s);
+  }
+  if (e == cudaSuccess && c->r > 0) {
+    if (!k_res) return KVQ_ERR_ARG;
+    e = copy_rows(c->res_k, kR, 0, c->r, k_res, c->r, 0, units, s);
+  }
+  if (e == cudaSuccess && rv > 0) {   // the FIFO oldest first: slots r .. 127, then 0 .. r - 1
+    if (!v_res) return KVQ_ERR_ARG;
+    if (c->t_q > 0) e = copy_rows(c->res_v, kR, c->r, kR - c->r, v_res, rv, 0, units, s);
+    if (e == cudaSuccess) e = copy_rows(c->res_v, kR, 0, c->r, v_res, rv, rv - c->r, units, s);
+  }
+  return cuda_status(e);
 }
 
 const char* kvq_status_string(int code) {

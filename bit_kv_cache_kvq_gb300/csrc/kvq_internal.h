@@ -31,6 +31,15 @@ constexpr int kMaxRep = 8;         // query heads per KV head
 //                           order (frag_layout.h)
 //   [kc]           kscale   fp32  [D]
 //   [kc+4D]        kmin     bf16  [D]
+// PN-Mix key (H3/L1, App. G packing), channels in the unit's stored order
+// (the high channels first, each part ascending; the cache's pn_perm):
+//   [0]            LSB plane 2048 B: bit 0 of every code, 1-bit fragment
+//                  order: word (mt*2 + ks/4)*32 + lane, bit 2*(ks%4) + chi +
+//                  8*rhi + 16*half (frag_layout.h coordinates)
+//   [kc]           upper plane: bits 1-2 of the high channels' codes, nh/32
+//                  words per (tile, lane) in the 2-bit key fragment order
+//   [k_scale]      fp32 [D] steps (high) or Eq. 7 scales (low)
+//   [k_min]        fp32 [D] origins (high) or Eq. 7 offsets (low)
 // KIVI key (KIVI article: keys per channel in groups of 32 tokens, metadata
 // in the input dtype):
 //   [0]            K codes  128*128*kb/8 bytes, fragment order as uniform
@@ -65,6 +74,8 @@ constexpr int kMaxRep = 8;         // query heads per KV head
 struct RecLayout {
   int mixed;
   int kivi;      // KIVI variant: bf16 metadata, keys in four 32-token sub-groups
+  int pnmix;     // PN-Mix H3/L1 keys: LSB plane + upper plane of the high channels
+  int nh;        // PN-Mix: high channels (2 * n_high_pairs), first in the stored order
   int kb, vb;
   int thresh;    // mixed: threshold tiers (per-group counts up to nb, n4)
   int nb, n4;    // mixed: BF16 / UINT4 channels a group (rank tiers) or at most
@@ -87,12 +98,32 @@ struct RecLayout {
 __host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
 
 __host__ __device__ inline RecLayout make_layout(int mixed, int kb, int vb,
-                                                 int nb, int n4, int thresh, int kivi = 0) {
+                                                 int nb, int n4, int thresh, int kivi = 0,
+                                                 int pnmix_high = -1) {
   RecLayout L{};
   L.mixed = mixed;
   L.kivi = kivi;
   L.kb = kb;
   L.vb = vb;
+  if (pnmix_high >= 0) {
+    // PN-Mix: LSB plane (1 bit, all channels), upper plane (2 bits, the
+    // nh high channels), then fp32 scales and offsets, channels in the
+    // unit's stored order (high channels first)
+    L.pnmix = 1;
+    L.kb = 2;
+    L.nh = pnmix_high;
+    L.k_codes = 0;
+    L.kc = kD * kKG / 8;
+    L.kw2 = pnmix_high / 32;
+    L.k_scale = L.kc + pnmix_high * kKG * 2 / 8;
+    L.k_min = L.k_scale + 4 * kD;
+    L.kpart = (L.k_min + 4 * kD + 127) & ~127;
+    L.v_codes = L.kpart;
+    L.v_scale = L.v_codes + kKG * kD * vb / 8;
+    L.v_min = L.v_scale + 4 * kKG * kVGroups;
+    L.bytes = align16(L.v_min + 2 * kKG * kVGroups);
+    return L;
+  }
   if (kivi) {
     // KIVI: steps then origins, bf16 [4 sub-groups of 32 tokens][D]
     L.k_codes = 0;
@@ -155,6 +186,8 @@ struct kvq_cache {
   kvq_bf16* sink_v;
   unsigned* status;    // sticky KVQ_FLAG_* word
   float* qacc;         // mixed: running sum of |q| [B*Hkv][D] (online saliency)
+  uint8_t* pn_perm;    // PN-Mix: [B*Hkv][D] stored position -> channel (high first)
+  bool pn_ready;       // PN-Mix: pairs selected (kvq_pnmix_pairs)
   int q_steps;         // decode steps summed in qacc since the last flush
   int q_rep;           // query heads per KV head of those steps
   int t_q;             // quantized tokens (multiple of 128)
@@ -223,6 +256,19 @@ cudaError_t launch_kivi_seal(const kvq_cache* c, QuantSrc src, int n_records, in
                              cudaStream_t s);
 cudaError_t launch_kivi_values(const kvq_cache* c, QuantSrc src, int n_records, int first_record,
                                int t0, int t1, int n_valid, cudaStream_t s);
+// Canonical KIVI export of records [u][0 .. t_q/128): key codes [u][n*4][D]
+// [32*bits/8] (per 32-token group and channel, LSB first along tokens),
+// origins and steps bf16 [u][n*4][D]; value codes [u][n*128][D*bits/8],
+// origins and steps bf16 [u][n*128][D/32] (zero for tokens in the FIFO).
+// PN-Mix (pnmix.cu): Eq. 6 pair scores and the selection into c->pn_perm;
+// export of the H3/L1 key groups.
+cudaError_t launch_pnmix_pairs(const kvq_cache* c, const kvq_bf16* q, int Hq, int Lq,
+                               const kvq_bf16* k, int Lk, float* sigma, cudaStream_t s);
+cudaError_t launch_export_pnmix(const kvq_cache* c, uint8_t* codes, float* offset, float* scale,
+                                uint8_t* high, cudaStream_t s);
+cudaError_t launch_export_kivi(const kvq_cache* c, uint8_t* k_codes, kvq_bf16* k_origin,
+                               kvq_bf16* k_step, uint8_t* v_codes, kvq_bf16* v_origin,
+                               kvq_bf16* v_step, cudaStream_t s);
 
 // Tensor-core decode (decode_mma.cu).  The plan cuts the weighted item
 // sequence (per unit: its groups, then its residual) into n_slots warp

@@ -63,6 +63,7 @@ struct QuantArgs {
   const float* qacc;        // mixed: the online window's |q| sums [units][D]
   float q_count;            // (query heads per KV head) * (steps observed)
   float tau_bf16, tau_uint4;  // threshold tiers (lay.thresh)
+  const uint8_t* perm;      // PN-Mix: [units][D] stored position -> channel
   unsigned* status;
 };
 
@@ -88,119 +89,303 @@ __device__ __forceinline__ void load_tile(const QuantArgs& a, const kvq_bf16* sr
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
 }
 
-// Per-group quantizer parameters kept for the code pass: origin m and
-// rcp = RN(1 / step) (0 for a constant group), plus the step itself for the
-// exact fallback.
-struct GroupQ {
-  float m, rcp;
-};
-
-__device__ __forceinline__ GroupQ make_q(const Params& p) {
-  return {p.m, p.step > 0.0f ? __frcp_rn(p.step) : 0.0f};
-}
-
-// c = clip(RNE(fl32(fl32(x - m) / step)), 0, top), fast form.  With
-// q' = RN(d * RN(1/step)), |q' - RN(d / step)| <= 2^-22 q <= 2^-18 (q <= 15
-// plus a rounding, as x <= the group max), so the two round to the same
-// integer unless q' lies within 2^-17 of a half-integer; such codes (and
-// non-finite q') set `exact` and the caller recomputes with the IEEE
-// quotient (code_exact).  Rounding: adding 1.5 * 2^23 rounds q in [0, 2^22)
-// to the nearest integer, ties to even, into the low mantissa bits; no
-// clamp is needed since 0 <= q < top + 1/2.
-constexpr float kTieMargin = 0.4999923706054688f;   // 0.5 - 2^-17
-__device__ __forceinline__ uint32_t code_fast(float x, GroupQ g, float& rmax) {
-  constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
-  const float d = __fsub_rn(x, g.m);
-  const float q = __fmul_rn(d, g.rcp);
-  const float tq = __fadd_rn(q, kMagic);
-  const float n = __fsub_rn(tq, kMagic);
-  // NaN (a non-finite group) must reach the exact path: fmaxf would drop it
-  const float r = fabsf(__fsub_rn(q, n));
-  rmax = r == r ? fmaxf(rmax, r) : 1.0f;
-  return __float_as_uint(tq) & 0xFFu;
-}
+// Exact code of one element, IEEE quotient (the definition): the rare path.
 __device__ __forceinline__ uint32_t code_exact(float x, float m, float step, int top) {
   if (step == 0.0f) return 0u;
   const float q = __fdiv_rn(__fsub_rn(x, m), step);
   return static_cast<uint32_t>(fminf(fmaxf(rintf(q), 0.0f), static_cast<float>(top)));
 }
 
-// Two bf16 values in a 32-bit word -> two 16-bit order keys (key order =
-// value order, -0.0 below +0.0, NaN beyond the infinities).
-__device__ __forceinline__ uint32_t key2(uint32_t x) {
-  return x ^ (((x >> 15) & 0x00010001u) * 0x7FFFu) ^ 0x80008000u;
+// ---- bf16x2 helpers
+// Elementwise min / max of two bf16 pairs; a NaN in either operand gives NaN.
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.NaN.bf16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
-__device__ __forceinline__ float unkey16(uint32_t k) {
-  const uint32_t u = (k & 0x8000u) ? (k ^ 0x8000u) : (~k & 0xFFFFu);
-  return __uint_as_float(u << 16);
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
-// a 16-bit key range holds a non-finite value iff an extreme is beyond +-inf
-__device__ __forceinline__ bool bad_range(uint32_t kmin, uint32_t kmax) {
-  return kmax >= 0xFF80u || kmin <= 0x007Fu;
+__device__ __forceinline__ uint32_t swap_halves(uint32_t a) { return __byte_perm(a, 0, 0x1032); }
+
+// d = RN(x - m) for the bf16 x in the low (high) half of w, given nm = -m:
+// one mixed-precision FMA x * 1 + nm (x * 1 is exact, so this is fl32(x - m)).
+#ifndef KVQ_QSUB_FMA
+#define KVQ_QSUB_FMA 1
+#endif
+#if KVQ_QSUB_FMA
+__device__ __forceinline__ float sub_lo(uint32_t w, float nm) {
+  float d;
+  asm("{\n .reg .b16 l, h, one;\n mov.b32 {l, h}, %1;\n mov.b16 one, 0x3F80;\n"
+      " fma.rn.f32.bf16 %0, l, one, %2;\n}\n" : "=f"(d) : "r"(w), "f"(nm));
+  return d;
+}
+__device__ __forceinline__ float sub_hi(uint32_t w, float nm) {
+  float d;
+  asm("{\n .reg .b16 l, h, one;\n mov.b32 {l, h}, %1;\n mov.b16 one, 0x3F80;\n"
+      " fma.rn.f32.bf16 %0, h, one, %2;\n}\n" : "=f"(d) : "r"(w), "f"(nm));
+  return d;
+}
+#else
+__device__ __forceinline__ float sub_lo(uint32_t w, float nm) { return __fadd_rn(__uint_as_float(w << 16), nm); }
+__device__ __forceinline__ float sub_hi(uint32_t w, float nm) { return __fadd_rn(__uint_as_float(w & 0xFFFF0000u), nm); }
+#endif
+
+// The code of d = fl32(x - m) in the fast form.  y = RN(d * r + 48) with r =
+// RN(1/step) lies in [48, 64) (codes <= 15), where the fp32 spacing is
+// 2^-18, so the bits of y hold (d/step) with 18 fraction bits.  |y - 48 -
+// d/step| <= 2^-19 + 16 * 2^-24 and |RN(d/step) - d/step| <= 2^-21, so y -
+// 48 is within 1.2 units of 2^-18 of the IEEE quotient RN(d/step).  Adding
+// 1/2 + 2 units and keeping the integer part gives RNE(RN(d/step)) unless
+// the fraction lies within 2 units of 1/2, below 1/2 or 5 above ("near"):
+// then the element takes the exact path.  Returns the adjusted bits v: the
+// code is (v >> 18) & (2^b - 1).
+constexpr float kCodeMagic = 48.0f;
+constexpr uint32_t kHalfPlus = 0x20002u;    // 1/2 + 2 units of 2^-18
+constexpr uint32_t kNearMask = 0x3FFF8u;    // fraction within [1/2 - 2, 1/2 + 5] units
+__device__ __forceinline__ uint32_t code_bits(float d, float r) {
+  return __float_as_uint(fmaf(d, r, kCodeMagic)) + kHalfPlus;
+}
+__device__ __forceinline__ bool is_near(uint32_t v) { return (v & kNearMask) == 0u; }
+// A near element: its quotient z = d/step lies close to h = n + 1/2, n =
+// floor(y - 48), so its code is n or n + 1, decided by RNE(RN(z)).  With
+// rem = d - h * step, exact in one FMA (the operands nearly cancel: h has at
+// most 5 significant bits and |rem| < 2^-14 d), RN(z) = h exactly when
+// -step * ulp-(h)/2 <= rem <= step * ulp(h)/2 (h has an even significand, so
+// it wins both ties), and then the code is RNE(h) = n + (n & 1); above that
+// band RN(z) > h (code n + 1), below it RN(z) < h (code n).  Needs step >=
+// 2^-100 (no underflow in the bounds); smaller steps take the exact tile
+// path.  Returns the code in code_bits' position.
+__device__ __forceinline__ uint32_t near_bits(uint32_t v, float d, float step, uint32_t top) {
+  const uint32_t n = ((v - kHalfPlus) >> 18) & 15u;
+  const float h = static_cast<float>(n) + 0.5f;
+  const float rem = fmaf(-h, step, d);
+  // step * 2^(e - 24), e = floor(log2 h): the distance from h to its upper
+  // neighbour, halved (and to its lower one, except for h = 1/2)
+  const uint32_t e = __float_as_uint(h) >> 23;   // biased exponent of h
+  const float up = step * __uint_as_float((e - 24u) << 23);
+  const float dn = n == 0u ? 0.5f * up : up;
+  const uint32_t c = rem > up ? n + 1u : rem < -dn ? n : n + (n & 1u);
+  return min(c, top) << 18;
+}
+// The code in v (bits 18..) moved to bit `pos` of a word, masked.
+template <int BITS>
+__device__ __forceinline__ uint32_t place(uint32_t v, int pos) {
+  constexpr uint32_t m = (1u << BITS) - 1u;
+  return (pos >= 18 ? v << (pos - 18) : v >> (18 - pos)) & (m << pos);
 }
 
-// Key channel ranges: thread (pair p = tid & 63 of channels 2p, 2p+1,
-// quarter tid >> 6 of 32 tokens), packed keys, merged through shared memory.
-// Threads 0..127 return the range of channel tid.
+// Range of a group from its bf16 min / max bits (NaN-propagating), with
+// the pages' order of signed zeros (-0 below +0): a zero minimum is -0 iff
+// the group holds a -0 (looked up by the caller only then).
+__device__ __forceinline__ bool nonfinite_bits(uint32_t b) { return (b & 0x7F80u) == 0x7F80u; }
+
+// Per-group parameters of the code pass: -m and RN(1/step) (0 for a constant
+// or non-finite group); the step itself is kept apart for the exact path.
+struct GroupQ {
+  float nm, rcp;
+};
+
+// A tile takes the exact path everywhere when a group is non-finite or has
+// a step in (0, 2^-100) (the near-element bounds would underflow).
+constexpr float kTinyStep = 7.888609052210118e-31f;   // 2^-100
+__device__ __forceinline__ GroupQ make_q(const Params& p, bool& exact_tile) {
+  const float r = p.step > 0.0f ? __frcp_rn(p.step) : 0.0f;
+  if (p.flags) exact_tile = true;
+  if (p.step > 0.0f && p.step < kTinyStep) exact_tile = true;
+  return {-p.m, r};
+}
+
+// ---- Key half: ranges per channel over the tile's 128 tokens.
+// Thread (piece o = tid & 15: channels 8o..8o+7, tokens 8s..8s+7 with s =
+// tid >> 4) reduces its 8 rows with bf16x2 min/max; lanes o and o + 16 merge
+// by a shuffle, the 8 warps through shared memory (sRed: [8][16][8] words).
+// Threads 0..127 return channel tid's range (lo with the signed-zero rule).
 __device__ __forceinline__ void key_ranges(const uint16_t* sK, uint32_t* sRed, float& lo,
                                            float& hi, bool& bad) {
-  const int p = threadIdx.x & 63, qq = threadIdx.x >> 6;
-  const uint32_t* t32 = reinterpret_cast<const uint32_t*>(sK);
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-#pragma unroll 8
-  for (int t = 32 * qq; t < 32 * qq + 32; ++t) {
-    const uint32_t k = key2(t32[t * 64 + ((((p >> 2) ^ (t & 7)) << 2) | (p & 3))]);
-    kmin = __vminu2(kmin, k);
-    kmax = __vmaxu2(kmax, k);
-  }
-  sRed[qq * 64 + p] = kmin;
-  sRed[256 + qq * 64 + p] = kmax;
-  __syncthreads();
-  if (threadIdx.x < kD) {
-    const int c = threadIdx.x, pp = c >> 1, sh = 16 * (c & 1);
-    uint32_t mn = 0xFFFFu, mx = 0u;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int o = lane & 15, s = tid >> 4;
+  const uint4* rows = reinterpret_cast<const uint4*>(sK);
+  uint4 w = rows[(8 * s) * 16 + o];   // token 8s: (8s & 7) = 0
+  uint32_t mn[4] = {w.x, w.y, w.z, w.w}, mx[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      mn = min(mn, (sRed[i * 64 + pp] >> sh) & 0xFFFFu);
-      mx = max(mx, (sRed[256 + i * 64 + pp] >> sh) & 0xFFFFu);
+  for (int i = 1; i < 8; ++i) {
+    w = rows[(8 * s + i) * 16 + (o ^ i)];
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      mn[k] = bmin2(mn[k], ww[k]);
+      mx[k] = bmax2(mx[k], ww[k]);
     }
-    lo = unkey16(mn);
-    hi = unkey16(mx);
-    bad = bad_range(mn, mx);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    mn[k] = bmin2(mn[k], __shfl_xor_sync(0xffffffffu, mn[k], 16));
+    mx[k] = bmax2(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 16));
+  }
+  if (lane < 16) {
+    uint4* dst = reinterpret_cast<uint4*>(sRed + (warp * 16 + o) * 8);
+    dst[0] = make_uint4(mn[0], mn[1], mn[2], mn[3]);
+    dst[1] = make_uint4(mx[0], mx[1], mx[2], mx[3]);
+  }
+  __syncthreads();
+  if (tid < kD) {
+    const int d = tid, oo = d >> 3, k = (d & 7) >> 1, sh = 16 * (d & 1);
+    uint32_t m2 = sRed[oo * 8 + k], x2 = sRed[oo * 8 + 4 + k];
+#pragma unroll
+    for (int wv = 1; wv < 8; ++wv) {
+      m2 = bmin2(m2, sRed[(wv * 16 + oo) * 8 + k]);
+      x2 = bmax2(x2, sRed[(wv * 16 + oo) * 8 + 4 + k]);
+    }
+    uint32_t lb = (m2 >> sh) & 0xFFFFu;
+    const uint32_t hb = (x2 >> sh) & 0xFFFFu;
+    bad = nonfinite_bits(lb) || nonfinite_bits(hb);
+    if (!bad && (lb & 0x7FFFu) == 0u) {   // a zero minimum: -0 iff the channel holds one
+      lb = 0u;
+      for (int t = 0; t < kKG; ++t)
+        if (sK[swz(t, d)] == 0x8000u) lb = 0x8000u;
+    }
+    lo = bf2f(static_cast<uint16_t>(lb));
+    hi = bf2f(static_cast<uint16_t>(hb));
   }
 }
 
-// Value groups: thread (token t = tid / 2, h = tid & 1) takes two of the
-// token's four 32-channel groups (h = 0: 0, 1; h = 1: 3, 2 -- the order keeps
-// a quarter warp's 16-byte reads on distinct banks).  Writes the steps and
-// origins to the record and the parameters to vq / vstep [t * 4 + j].
+// Key codes straight into fragment-order words (frag_layout.h).  Thread
+// (tile mt, row g, word column w) takes tokens 16 mt + g and + 8 and
+// channels 32 w .. 32 w + 31: one 16-byte read gives channels 2t, 2t+1 of
+// lanes t = 0..3 for one (k-step, half of the k-step, token row), and the
+// thread's words are the 4 (2-bit) or 8 (4-bit) consecutive words of lanes
+// (g, 0..3), stored as 16-byte vectors.  Lanes 0..7 of a warp are the eight
+// rows g, so each quarter warp's reads fall on eight different pieces.
+// Exact path of a whole tile (a non-finite group or a step below 2^-100):
+// every code from the IEEE quotient; the same words as key_codes.
+template <int KB>
+__device__ __noinline__ void key_codes_slow(const uint16_t* sK, const GroupQ* kq,
+                                            const float* kstep, uint32_t* dst) {
+  constexpr int NW = KB == 2 ? 4 : 8;
+  constexpr int top = (1 << KB) - 1;
+  const int tid = threadIdx.x;
+  const int g = tid & 7, w = (tid >> 3) & 3, mt = tid >> 5;
+  uint32_t* out = dst + ((mt * 4 + w) * 32 + 4 * g) * (NW / 4);
+#pragma unroll 1
+  for (int i = 0; i < NW; ++i) {
+    const int t = KB == 2 ? i : i >> 1;
+    uint32_t acc = 0;
+#pragma unroll 1
+    for (int e = 0; e < 32 / KB; ++e) {
+      // code slot e of word i: (rhi, kl, chi, half) of this thread's elements
+      int rhi, kl, chi, half;
+      if (KB == 2) {
+        half = e >> 3;
+        const int P = e & 7;
+        rhi = P >> 2;
+        kl = (P >> 1) & 1;
+        chi = P & 1;
+      } else {
+        half = e >> 2;
+        kl = i & 1;
+        rhi = (e >> 1) & 1;
+        chi = e & 1;
+      }
+      const int tok = 16 * mt + g + 8 * rhi;
+      const int ch = 32 * w + 16 * kl + 8 * chi + 2 * t + half;
+      acc |= code_exact(bf2f(sK[swz(tok, ch)]), -kq[ch].nm, kstep[ch], top) << (KB * e);
+    }
+    out[i] = acc;
+  }
+}
+
+template <int KB>
+__device__ __forceinline__ void key_codes(const uint16_t* sK, const GroupQ* kq,
+                                          const float* kstep, bool exact_tile, uint32_t* dst) {
+  constexpr int NW = KB == 2 ? 4 : 8;
+  constexpr int top = (1 << KB) - 1;
+  if (exact_tile) {   // block-uniform, rare
+    key_codes_slow<KB>(sK, kq, kstep, dst);
+    return;
+  }
+  const int tid = threadIdx.x;
+  const int g = tid & 7, w = (tid >> 3) & 3, mt = tid >> 5;
+  const uint4* rows = reinterpret_cast<const uint4*>(sK);
+  const float4* kq4 = reinterpret_cast<const float4*>(kq);
+  uint32_t acc[NW];
+#pragma unroll
+  for (int i = 0; i < NW; ++i) acc[i] = 0u;
+#pragma unroll
+  for (int kl = 0; kl < 2; ++kl)
+#pragma unroll
+    for (int chi = 0; chi < 2; ++chi) {
+      const int p = 4 * w + 2 * kl + chi;   // piece: channels 8p .. 8p + 7
+      // (-m, rcp) of channels 8p + e, e = 2t + half
+      float4 q4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q4[i] = kq4[4 * p + i];
+      const float nm[8] = {q4[0].x, q4[0].z, q4[1].x, q4[1].z, q4[2].x, q4[2].z, q4[3].x, q4[3].z};
+      const float rc[8] = {q4[0].y, q4[0].w, q4[1].y, q4[1].w, q4[2].y, q4[2].w, q4[3].y, q4[3].w};
+#pragma unroll
+      for (int rhi = 0; rhi < 2; ++rhi) {
+        const uint4 x4 = rows[(16 * mt + g + 8 * rhi) * 16 + (p ^ g)];
+        const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int e = 2 * t + half;
+            const float d = half ? sub_hi(xw[t], nm[e]) : sub_lo(xw[t], nm[e]);
+            uint32_t v = code_bits(d, rc[e]);
+            if (is_near(v)) v = near_bits(v, d, kstep[8 * p + e], top);   // rare
+            if (KB == 2) acc[t] |= place<2>(v, 2 * (4 * rhi + 2 * kl + chi) + 16 * half);
+            else acc[2 * t + kl] |= place<4>(v, 4 * (2 * rhi + chi) + 16 * half);
+          }
+      }
+    }
+  // 2-bit: words (mt*4 + w)*32 + 4g + t; 4-bit: ((mt*4 + w)*32 + 4g + t)*2 + kl
+  uint4* out = reinterpret_cast<uint4*>(dst + ((mt * 4 + w) * 32 + 4 * g) * (NW / 4));
+  out[0] = make_uint4(acc[0], acc[1], acc[2], acc[3]);
+  if (NW == 8) out[1] = make_uint4(acc[4 % NW], acc[5 % NW], acc[6 % NW], acc[7 % NW]);
+}
+
+// ---- Value half: ranges per (token, 32-channel group).  Thread (token tid
+// >> 1, h = tid & 1) takes groups j = 2h, 2h + 1 (h = 1 in the order 3, 2 so
+// a quarter warp's 16-byte reads fall on distinct banks).  Writes steps and
+// origins to the record and (-m, rcp) to vq[tok * 4 + j], steps to vstep.
 template <int VB>
-__device__ __forceinline__ unsigned value_groups(const QuantArgs& a, const uint16_t* sV,
-                                                 GroupQ* vq, float* vstep, uint8_t* rec) {
+__device__ __forceinline__ unsigned value_ranges(const uint16_t* sV, GroupQ* vq, float* vstep,
+                                                 uint8_t* rec, const RecLayout& L,
+                                                 bool& exact_tile) {
   constexpr int top = (1 << VB) - 1;
   const int t = threadIdx.x >> 1, h = threadIdx.x & 1;
-  float* vscale = reinterpret_cast<float*>(rec + a.lay.v_scale);
-  uint16_t* vmin = reinterpret_cast<uint16_t*>(rec + a.lay.v_min);
+  float* vscale = reinterpret_cast<float*>(rec + L.v_scale);
+  uint16_t* vmin = reinterpret_cast<uint16_t*>(rec + L.v_min);
   const uint4* row = reinterpret_cast<const uint4*>(sV + t * kD);
   unsigned flags = 0;
 #pragma unroll
   for (int jj = 0; jj < 2; ++jj) {
     const int j = h ? 3 - jj : jj;
-    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+    uint32_t mn = 0u, mx = 0u;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint4 w = row[(4 * j + k) ^ (t & 7)];
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t kk = key2(ws[e]);
-        kmin = __vminu2(kmin, kk);
-        kmax = __vmaxu2(kmax, kk);
-      }
+      const uint32_t a = bmin2(bmin2(w.x, w.y), bmin2(w.z, w.w));
+      const uint32_t b = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+      mn = k ? bmin2(mn, a) : a;
+      mx = k ? bmax2(mx, b) : b;
     }
-    const uint32_t mn = min(kmin & 0xFFFFu, kmin >> 16), mx = max(kmax & 0xFFFFu, kmax >> 16);
-    const Params p = group_params(unkey16(mn), unkey16(mx), top, bad_range(mn, mx));
-    vq[t * kVGroups + j] = make_q(p);
+    mn = bmin2(mn, swap_halves(mn));
+    mx = bmax2(mx, swap_halves(mx));
+    uint32_t lb = mn & 0xFFFFu;
+    const uint32_t hb = mx & 0xFFFFu;
+    const bool bad = nonfinite_bits(lb) || nonfinite_bits(hb);
+    if (!bad && (lb & 0x7FFFu) == 0u) {   // a zero minimum: -0 iff the group holds one
+      lb = 0u;
+      for (int c = 32 * j; c < 32 * j + 32; ++c)
+        if (sV[swz(t, c)] == 0x8000u) lb = 0x8000u;
+    }
+    const Params p = group_params(bf2f(static_cast<uint16_t>(lb)),
+                                  bf2f(static_cast<uint16_t>(hb)), top, bad);
+    vq[t * kVGroups + j] = make_q(p, exact_tile);
     vstep[t * kVGroups + j] = p.step;
     vscale[t * kVGroups + j] = p.step;
     vmin[t * kVGroups + j] = f2bf_bits(p.m);
@@ -209,162 +394,90 @@ __device__ __forceinline__ unsigned value_groups(const QuantArgs& a, const uint1
   return flags;
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Rare exact recomputation of one key word (kept out of line so the fast
-// loop stays small in the instruction cache).
-template <int KB>
-__device__ __noinline__ uint32_t key_word_exact(const uint32_t* t32, const GroupQ* kq,
-                                                const float* kstep, int mt, int ks0, int g,
-                                                int t) {
-  constexpr int top = (1 << KB) - 1;
-  constexpr int KSW = KB == 2 ? 2 : 1;
-  uint32_t acc = 0;
-  for (int kl = 0; kl < KSW; ++kl)
-    for (int r = 0; r < 4; ++r) {
-      const int tok = 16 * mt + g + 8 * (r & 1);
-      const int ch0 = 16 * (ks0 + kl) + 2 * t + 8 * (r >> 1);
-      const uint32_t xw = t32[tok * 64 + ((((ch0 >> 3) ^ (tok & 7)) << 2) | ((ch0 & 7) >> 1))];
-      for (int hh = 0; hh < 2; ++hh) {
-        const float x = hh ? __uint_as_float(xw & 0xFFFF0000u) : __uint_as_float(xw << 16);
-        const int ch = ch0 + hh;
-        const int pos = KB == 2 ? 2 * pair_2bit(kl, r) + 16 * hh : 4 * nibble_4bit(r) + 16 * hh;
-        acc |= code_exact(x, kq[ch].m, kstep[ch], top) << pos;
-      }
-    }
-  return acc;
-}
-
-// Rare exact recomputation of one value word.
+// Value codes straight into fragment-order words.  A word (tile mc, lane
+// (g, t), k-step column) holds channels 16 mc + g and + 8 of tokens 16 kt +
+// 2t + {0, 1, 8, 9}.  Thread (t, token parity half, g-half gh, w-half wh,
+// mc) takes channels 16 mc + 4 gh + {0..3} (and + 8) of its tokens 16 kt +
+// 2t + 8 chi + half, kt in 4 wh .. 4 wh + 3: an 8-byte read per (token,
+// channel half) gives the four channels of lanes g = 4 gh .. 4 gh + 3.  The
+// two lanes of a token pair (half = 0, 1) OR their words together; lanes
+// 0..15 read sixteen different 8-byte places of the swizzled tile.
+// Exact path of a whole value tile: every code from the IEEE quotient, each
+// word built by one thread (words w of lanes (g, t) of tile mc).
 template <int VB>
-__device__ __noinline__ uint32_t value_word_exact(const uint16_t* sV, const GroupQ* vq,
-                                                  const float* vstep, int mc, int kt0, int g,
-                                                  int t) {
+__device__ __noinline__ void value_codes_slow(const uint16_t* sV, const GroupQ* vq,
+                                              const float* vstep, uint32_t* dst) {
   constexpr int top = (1 << VB) - 1;
-  constexpr int KSW = VB == 2 ? 2 : 1;
-  const int j = mc >> 1;
-  uint32_t acc = 0;
-  for (int kl = 0; kl < KSW; ++kl)
-    for (int r = 0; r < 4; ++r)
-      for (int hh = 0; hh < 2; ++hh) {
-        const int ch = 16 * mc + g + 8 * (r & 1);
-        const int tok = 16 * (kt0 + kl) + 2 * t + 8 * (r >> 1) + hh;
-        const int pos = VB == 2 ? 2 * pair_2bit(kl, r) + 16 * hh : 4 * nibble_4bit(r) + 16 * hh;
-        acc |= code_exact(bf2f(sV[swz(tok, ch)]), vq[tok * kVGroups + j].m,
-                          vstep[tok * kVGroups + j], top) << pos;
-      }
-  return acc;
-}
-
-// Key codes straight into fragment-order words (frag_layout.h).  A word of
-// (tile mt, k-step pair or k-step, lane g,t) holds tokens g, g+8 of the tile
-// and channels 2t, 2t+1, 2t+8, 2t+9 of its k-step(s); each register's pair of
-// adjacent channels is one 32-bit read of the staged tile.  A thread's words
-// share their lane and k-steps (only the tile differs), so the channel
-// parameters and the swizzled column offsets are set up once.
-template <int KB>
-__device__ __forceinline__ void pack_key_words(const uint16_t* sK, const GroupQ* kq,
-                                               const float* kstep, uint32_t* dst) {
-  constexpr int KSW = KB == 2 ? 2 : 1;   // k-steps per word
-  constexpr int NWT = KB == 2 ? 4 : 8;   // words per thread (256 threads)
-  const uint32_t* t32 = reinterpret_cast<const uint32_t*>(sK);
-  const int tid = threadIdx.x;
-  int lane, ks0, mt0, mstep;
-  if (KB == 2) {   // word (mt*4 + ks/2)*32 + lane = tid + 256 k
-    lane = tid & 31;
-    ks0 = 2 * ((tid >> 5) & 3);
-    mt0 = tid >> 7;
-    mstep = 2;
-  } else {         // word ((mt*4 + ks/2)*32 + lane)*2 + ks%2 = tid + 256 k
-    lane = (tid >> 1) & 31;
-    ks0 = 2 * ((tid >> 6) & 3) + (tid & 1);
-    mt0 = 0;
-    mstep = 1;
-  }
-  const int g = lane >> 2, t = lane & 3;
-  GroupQ gq[KSW][4];
-  int col[KSW][2];   // 32-bit column offset of channels 2t (+8) in rows with t & 7 = g
-#pragma unroll
-  for (int kl = 0; kl < KSW; ++kl) {
-#pragma unroll
-    for (int r2 = 0; r2 < 4; ++r2)   // channels 2t, 2t+1, 2t+8, 2t+9
-      gq[kl][r2] = kq[16 * (ks0 + kl) + 2 * t + (r2 & 1) + 8 * (r2 >> 1)];
-#pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-      const int ch = 16 * (ks0 + kl) + 2 * t + 8 * hb;
-      col[kl][hb] = (((ch >> 3) ^ g) << 2) | ((ch & 7) >> 1);
+  constexpr int per = 32 / VB;
+#pragma unroll 1
+  for (int wd = threadIdx.x; wd < kKG * kD * VB / 32; wd += blockDim.x) {
+    uint32_t acc = 0;
+#pragma unroll 1
+    for (int sl = 0; sl < per; ++sl) {
+      int tok, ch;
+      value_word_code(wd, sl, VB, tok, ch);
+      const int gi = tok * kVGroups + ch / kVG;
+      acc |= code_exact(bf2f(sV[swz(tok, ch)]), -vq[gi].nm, vstep[gi], top) << (VB * sl);
     }
-  }
-#pragma unroll 1
-  for (int k = 0; k < NWT; ++k) {
-    const int mt = mt0 + mstep * k;
-    const uint32_t* row0 = t32 + (16 * mt + g) * 64;   // token g of the tile (row + 8: token g+8)
-    float rmax = 0.0f;
-    uint32_t acc = 0;
-#pragma unroll
-    for (int kl = 0; kl < KSW; ++kl)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const uint32_t xw = row0[8 * 64 * (r & 1) + col[kl][r >> 1]];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const float x = hh ? bf_hi(xw) : bf_lo(xw);
-          const int pos = KB == 2 ? 2 * pair_2bit(kl, r) + 16 * hh : 4 * nibble_4bit(r) + 16 * hh;
-          acc |= code_fast(x, gq[kl][2 * (r >> 1) + hh], rmax) << pos;
-        }
-      }
-    if (!(rmax < kTieMargin)) acc = key_word_exact<KB>(t32, kq, kstep, mt, ks0, g, t);   // rare
-    dst[tid + 256 * k] = acc;
+    dst[wd] = acc;
   }
 }
 
-// Value codes straight into fragment-order words: thread (channel tile mc,
-// lane g,t) builds the words of all the group's token k-steps (2-bit: 4
-// words, k-step pairs; 4-bit: 8) and stores them as 16-byte vectors.  A word
-// holds channels g, g+8 of the tile and tokens 2t, 2t+1, 2t+8, 2t+9 of its
-// k-step(s); parameters per (token, 32-channel group).
 template <int VB>
-__device__ __forceinline__ void pack_value_words(const uint16_t* sV, const GroupQ* vq,
-                                                 const float* vstep, uint32_t* dst) {
-  constexpr int KSW = VB == 2 ? 2 : 1;
-  constexpr int NW = VB == 2 ? 4 : 8;   // words per (mc, lane)
-  const int mc = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3, j = mc >> 1;
-  uint32_t* out4 = dst + (mc * (NW / 4)) * 128 + lane * 4;   // word (mc, lane, wi)
-#pragma unroll 1
-  for (int wi = 0; wi < NW; ++wi) {
-    float rmax = 0.0f;
-    uint32_t acc = 0;
-    float xs[KSW][4][2];
+__device__ __forceinline__ void value_codes(const uint16_t* sV, const GroupQ* vq,
+                                            const float* vstep, bool exact_tile, uint32_t* dst) {
+  constexpr int top = (1 << VB) - 1;
+  constexpr int NW = VB == 2 ? 8 : 16;   // words before the pair merge: (w, i) or (kt, i)
+  if (exact_tile) {   // block-uniform, rare
+    value_codes_slow<VB>(sV, vq, vstep, dst);
+    return;
+  }
+  const int tid = threadIdx.x;
+  const int t = tid & 3, half = (tid >> 2) & 1, gh = (tid >> 3) & 1, wh = (tid >> 4) & 1,
+            mc = tid >> 5;
+  const int j = mc >> 1;
+  const uint2* rows = reinterpret_cast<const uint2*>(sV);   // [128 tokens][32 half pieces]
+  uint32_t acc[NW];
 #pragma unroll
-    for (int kl = 0; kl < KSW; ++kl)
+  for (int i = 0; i < NW; ++i) acc[i] = 0u;
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+  for (int wl = 0; wl < 2; ++wl)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int kt = KSW * wi + kl;
-          const int ch = 16 * mc + g + 8 * (r & 1);
-          const int tok = 16 * kt + 2 * t + 8 * (r >> 1) + hh;
-          xs[kl][r][hh] = bf2f(sV[swz(tok, ch)]);
-        }
+    for (int kl = 0; kl < 2; ++kl)
 #pragma unroll
-    for (int kl = 0; kl < KSW; ++kl)
+      for (int chi = 0; chi < 2; ++chi) {
+        const int w = 2 * wh + wl;
+        const int tok = 16 * (2 * w + kl) + 2 * t + 8 * chi + half;
+        const GroupQ q = vq[tok * kVGroups + j];
 #pragma unroll
-      for (int r2 = 0; r2 < 4; ++r2) {   // tokens 2t, 2t+1, 2t+8, 2t+9
-        const int tok = 16 * (KSW * wi + kl) + 2 * t + (r2 & 1) + 8 * (r2 >> 1);
-        const GroupQ gq = vq[tok * kVGroups + j];
+        for (int rhi = 0; rhi < 2; ++rhi) {
+          const uint2 x2 = rows[tok * 32 + 2 * ((2 * mc + rhi) ^ (tok & 7)) + gh];
+          const uint32_t xw[2] = {x2.x, x2.y};
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {   // the two registers holding this token
-          const int r = 2 * (r2 >> 1) + rr, hh = r2 & 1;
-          const int pos = VB == 2 ? 2 * pair_2bit(kl, r) + 16 * hh : 4 * nibble_4bit(r) + 16 * hh;
-          acc |= code_fast(xs[kl][r][hh], gq, rmax) << pos;
+          for (int i = 0; i < 4; ++i) {
+            const float d = (i & 1) ? sub_hi(xw[i >> 1], q.nm) : sub_lo(xw[i >> 1], q.nm);
+            uint32_t v = code_bits(d, q.rcp);
+            if (is_near(v)) v = near_bits(v, d, vstep[tok * kVGroups + j], top);   // rare
+            if (VB == 2) acc[4 * wl + i] |= place<2>(v, 2 * (4 * rhi + 2 * kl + chi) + 16 * half);
+            else acc[8 * wl + 4 * kl + i] |= place<4>(v, 4 * (2 * rhi + chi) + 16 * half);
+          }
         }
       }
-    if (!(rmax < kTieMargin)) acc = value_word_exact<VB>(sV, vq, vstep, mc, KSW * wi, g, t);   // rare
-    // word index of (mc, lane, wi): 2-bit (mc*32 + lane)*4 + wi; 4-bit
-    // ((mc*2 + wi/4)*32 + lane)*4 + wi%4
-    out4[(wi >> 2) * 128 + (wi & 3)] = acc;
+  // the other token of each pair (lane ^ 4) holds the other half of every word
+#pragma unroll
+  for (int i = 0; i < NW; ++i) acc[i] |= __shfl_xor_sync(0xffffffffu, acc[i], 4);
+  // lane half = 0 stores the words of w = 2 wh, half = 1 those of 2 wh + 1
+  const int w = 2 * wh + half;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int g = 4 * gh + i;
+    if (VB == 2) {   // word (mc*32 + 4g + t)*4 + w
+      dst[(mc * 32 + 4 * g + t) * 4 + w] = half ? acc[4 + i] : acc[i];
+    } else {         // words ((mc*2 + w/2)*32 + 4g + t)*4 + 2(w%2) + kl
+      const uint32_t a0 = half ? acc[8 + i] : acc[i], a1 = half ? acc[12 + i] : acc[4 + i];
+      *reinterpret_cast<uint2*>(dst + ((mc * 2 + (w >> 1)) * 32 + 4 * g + t) * 4 + 2 * (w & 1)) =
+          make_uint2(a0, a1);
+    }
   }
 }
 
@@ -375,10 +488,14 @@ __device__ __forceinline__ uint8_t* group_record(const QuantArgs& a) {
 
 // Dynamic shared memory of a quantize block: the staged tile (32 KB), then
 // the parameter area (kParamBytes): values use vq [512] and vstep [512];
-// keys use kq [128], kstep [128], a 2 KB reduction buffer and (mixed keys)
-// the rank keys and tiers; mixed key blocks add their virtual codes after.
+// keys use kq [128], kstep [128] and a 4 KB reduction buffer; mixed key
+// blocks keep their rank keys and tiers after the reduction buffer and add
+// their virtual codes after the parameter area.
 constexpr int kTileBytes = kKG * kD * 2;
-constexpr int kParamBytes = kKG * kVGroups * (8 + 4);   // 6 KB, the larger of the two uses
+constexpr int kParamBytes = kKG * kVGroups * (8 + 4);   // 6 KB, the larger of the uses
+constexpr int kRedBytes = 8 * 16 * 8 * 4;               // key range reduction buffer
+static_assert(kD * 12 + kRedBytes <= kParamBytes, "key parameters fit the area");
+static_assert(kRedBytes + 512 + 128 + 512 <= kParamBytes, "mixed ranking area fits");
 
 // Value half of a group (block z = 1 of every quantize launch).
 template <int VB>
@@ -389,9 +506,10 @@ __device__ __forceinline__ void value_part(const QuantArgs& a, uint8_t* smem) {
   load_tile(a, a.src.v, sV);
   __syncthreads();
   uint8_t* rec = group_record(a);
-  const unsigned flags = value_groups<VB>(a, sV, vq, vstep, rec);
-  __syncthreads();
-  pack_value_words<VB>(sV, vq, vstep, reinterpret_cast<uint32_t*>(rec + a.lay.v_codes));
+  bool exact_tile = false;
+  const unsigned flags = value_ranges<VB>(sV, vq, vstep, rec, a.lay, exact_tile);
+  exact_tile = __syncthreads_or(exact_tile);
+  value_codes<VB>(sV, vq, vstep, exact_tile, reinterpret_cast<uint32_t*>(rec + a.lay.v_codes));
   if (flags) atomicOr(a.status, flags);
 }
 
@@ -413,19 +531,106 @@ __global__ void __launch_bounds__(256) quantize_uniform_kernel(QuantArgs a) {
   uint8_t* rec = group_record(a);
   unsigned flags = 0;
   float lo, hi;
-  bool bad;
+  bool bad, exact_tile = false;
   key_ranges(sT, sRed, lo, hi, bad);
   if (threadIdx.x < kD) {
     const int d = threadIdx.x;
     const Params p = group_params(lo, hi, (1 << KB) - 1, bad);
-    kq[d] = make_q(p);
+    kq[d] = make_q(p, exact_tile);
     kstep[d] = p.step;
     reinterpret_cast<float*>(rec + a.lay.k_scale)[d] = p.step;
     reinterpret_cast<uint16_t*>(rec + a.lay.k_min)[d] = f2bf_bits(p.m);
     flags = p.flags;
   }
+  exact_tile = __syncthreads_or(exact_tile);
+  key_codes<KB>(sT, kq, kstep, exact_tile, reinterpret_cast<uint32_t*>(rec + a.lay.k_codes));
+  if (flags) atomicOr(a.status, flags);
+}
+
+// PN-Mix H3/L1 keys and uniform values of one 128-token group (z = 1: the
+// values).  Keys: thread p < 128 takes the unit's stored position p
+// (channel perm[p]; the first nh positions are the selected pairs' channels):
+// high channels by Eq. 2 at 3 bits (origin the minimum, step (M - m)/7),
+// the others by Eq. 7 (s = (M - m)/2, z = (3m + M)/4, code RNE((x - z)/s)
+// clipped to 0..1), every operation fp32 rounded; codes staged as bytes,
+// then the LSB plane and the upper plane packed word by word.
+template <int VB>
+__global__ void __launch_bounds__(256) quantize_pnmix_kernel(QuantArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const RecLayout& L = a.lay;
+  if (blockIdx.z) {
+    value_part<VB>(a, smem);
+    return;
+  }
+  uint16_t* sK = reinterpret_cast<uint16_t*>(smem);
+  uint8_t* cB = smem + kTileBytes;   // codes [128 tokens][128 positions]
+  load_tile(a, a.src.k, sK);
   __syncthreads();
-  pack_key_words<KB>(sT, kq, kstep, reinterpret_cast<uint32_t*>(rec + a.lay.k_codes));
+  uint8_t* rec = group_record(a);
+  unsigned flags = 0;
+  if (threadIdx.x < kD) {
+    const int p = threadIdx.x;
+    const int ch = a.perm[static_cast<long long>(blockIdx.y) * kD + p];
+    float lo = bf2f(sK[swz(0, ch)]), hi = lo;
+    bool bad = false;
+    for (int t = 0; t < kKG; ++t) {
+      const float x = bf2f(sK[swz(t, ch)]);
+      bad |= !isfinite(x);
+      if (x < lo || (x == lo && (__float_as_uint(x) >> 31) && !(__float_as_uint(lo) >> 31))) lo = x;
+      if (x > hi || (x == hi && !(__float_as_uint(x) >> 31) && (__float_as_uint(hi) >> 31))) hi = x;
+    }
+    float off = lo, sc = 0.0f;
+    if (bad) {
+      flags |= KVQ_FLAG_NONFINITE;
+    } else if (hi != lo) {
+      if (p < L.nh) {   // Eq. 2 at 3 bits
+        sc = __fdiv_rn(__fsub_rn(hi, lo), 7.0f);
+        if (!(sc > 0.0f) || !isfinite(sc)) flags |= KVQ_FLAG_RANGE;
+      } else {          // Eq. 7
+        sc = __fdiv_rn(__fsub_rn(hi, lo), 2.0f);
+        off = __fdiv_rn(__fadd_rn(__fmul_rn(3.0f, lo), hi), 4.0f);
+        if (!(sc > 0.0f) || !isfinite(sc) || !isfinite(off)) flags |= KVQ_FLAG_RANGE;
+      }
+    }
+    reinterpret_cast<float*>(rec + L.k_scale)[p] = sc;
+    reinterpret_cast<float*>(rec + L.k_min)[p] = off;
+    const float top = p < L.nh ? 7.0f : 1.0f;
+    for (int t = 0; t < kKG; ++t) {
+      uint32_t c = 0;
+      if (!bad && sc > 0.0f) {
+        const float y = __fdiv_rn(__fsub_rn(bf2f(sK[swz(t, ch)]), off), sc);
+        c = static_cast<uint32_t>(fminf(fmaxf(rintf(y), 0.0f), top));
+      }
+      cB[t * kD + p] = static_cast<uint8_t>(c);
+    }
+  }
+  __syncthreads();
+  // LSB plane: word (mt*2 + ks/4)*32 + lane, bit 2*(ks%4) + chi + 8*rhi + 16*half
+  uint32_t* lsb = reinterpret_cast<uint32_t*>(rec + L.k_codes);
+  for (int w = threadIdx.x; w < kKG * kD / 32; w += blockDim.x) {
+    const int lane = w & 31, kq = (w >> 5) & 1, mt = w >> 6;
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t acc = 0;
+#pragma unroll 4
+    for (int bit = 0; bit < 32; ++bit) {
+      const int half = bit >> 4, rhi = (bit >> 3) & 1, kl4 = (bit >> 1) & 3, chi = bit & 1;
+      const int tok = 16 * mt + g + 8 * rhi;
+      const int p = 16 * (4 * kq + kl4) + 2 * t + 8 * chi + half;
+      acc |= static_cast<uint32_t>(cB[tok * kD + p] & 1u) << bit;
+    }
+    lsb[w] = acc;
+  }
+  // upper plane of the high positions: 2-bit key fragment order, kw2 words a (tile, lane)
+  uint32_t* up = reinterpret_cast<uint32_t*>(rec + L.kc);
+  for (int w = threadIdx.x; w < 8 * L.kw2 * 32; w += blockDim.x) {
+    uint32_t acc = 0;
+    for (int s2 = 0; s2 < 16; ++s2) {
+      int tok, v;
+      mixed_word_code(w, s2, L.kw2, tok, v);
+      acc |= static_cast<uint32_t>(cB[tok * kD + v] >> 1) << (2 * s2);
+    }
+    up[w] = acc;
+  }
   if (flags) atomicOr(a.status, flags);
 }
 
@@ -452,10 +657,10 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
     return;
   }
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem);
-  uint32_t* sRed = reinterpret_cast<uint32_t*>(smem + kTileBytes);             // 2 KB
-  uint32_t* sKey = reinterpret_cast<uint32_t*>(smem + kTileBytes + 2048);     // 512 B
-  uint8_t* sTier = smem + kTileBytes + 2048 + 512;                            // 128 B
-  float* sA = reinterpret_cast<float*>(smem + kTileBytes + 2048 + 512 + 128);  // 512 B
+  uint32_t* sRed = reinterpret_cast<uint32_t*>(smem + kTileBytes);                   // 4 KB
+  uint32_t* sKey = reinterpret_cast<uint32_t*>(smem + kTileBytes + kRedBytes);      // 512 B
+  uint8_t* sTier = smem + kTileBytes + kRedBytes + 512;                             // 128 B
+  float* sA = reinterpret_cast<float*>(smem + kTileBytes + kRedBytes + 512 + 128);  // 512 B
   uint8_t* cKv = smem + kTileBytes + kParamBytes;
   load_tile(a, a.src.k, sK);
   // virtual channels past this group's count stay zero
@@ -732,6 +937,7 @@ cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
   // +0.0f turns a threshold of -0 into +0, so A = +0 is not above it
   a.tau_bf16 = c->cfg.tau_bf16 + 0.0f;
   a.tau_uint4 = c->cfg.tau_uint4 + 0.0f;
+  a.perm = c->pn_perm;
   a.status = c->status;
   const dim3 grid(n_groups, c->cfg.batch * c->cfg.kv_heads, 2);   // z: keys, values
   const int kb = c->cfg.k_bits, vb = c->cfg.v_bits;
@@ -743,7 +949,12 @@ cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
     if (e != cudaSuccess) return e;                          \
     KERNEL<<<grid, 256, SMEM, s>>>(a);                       \
   } while (0)
-  if (c->cfg.k_mode == KVQ_K_MIXED) {
+  if (c->cfg.k_mode == KVQ_K_PNMIX) {
+    const int smem = kTileBytes + kKG * kD;   // the tile, then the code bytes (>= values' need)
+    static_assert(kKG * kD >= kParamBytes, "PN-Mix code bytes cover the value parameters");
+    if (vb == 2) KVQ_LAUNCH(quantize_pnmix_kernel<2>, smem);
+    else KVQ_LAUNCH(quantize_pnmix_kernel<4>, smem);
+  } else if (c->cfg.k_mode == KVQ_K_MIXED) {
     const int smem = kTileBytes + kParamBytes + kKG * 32 * c->lay.kw2;   // + virtual codes
     if (vb == 2) KVQ_LAUNCH(quantize_mixed_kernel<2>, smem);
     else KVQ_LAUNCH(quantize_mixed_kernel<4>, smem);

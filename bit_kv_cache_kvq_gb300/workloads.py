@@ -64,6 +64,10 @@ WORKLOADS = {
     # prefill 32K at batch 8, then 512 decode steps with a flush every 128
     "llama8b_prefill_32k_b8": Workload("llama8b_prefill_32k_b8", 1003, B=8, Hq=32, Hkv=8,
                                        T_q=32768, r=0, steps=512),
+    # KIVI streaming variant (keys in 32-token groups sealed every 128, value
+    # FIFO, bf16 metadata) on the Llama-8B decode layer, KIVI-2
+    "kivi_llama8b_32k_b16": Workload("kivi_llama8b_32k_b16", 1006, B=16, Hq=32, Hkv=8,
+                                     T_q=32768, r=100, mode="kivi"),
     # MixKVQ: Qwen-32B layer, 64 q / 8 kv heads, batch 8, 16K context
     "mixkvq_qwen32b_16k_b8": Workload("mixkvq_qwen32b_16k_b8", 1004, B=8, Hq=64, Hkv=8,
                                       T_q=16384, r=100, k_outliers=6, mode="mixed",

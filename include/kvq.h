@@ -78,8 +78,40 @@ enum {
                                  call's output is invalid                   */
 };
 
-/* Key storage mode. */
-enum { KVQ_K_UNIFORM = 0, KVQ_K_MIXED = 1 };
+/* Key storage mode.  KVQ_K_KIVI is the KIVI article's streaming cache
+ * ("KIVI: KV cache axes" §4–§7; MixKVQ's experimental setting G = 32, R =
+ * 128): keys quantized per channel in groups of 32 tokens, sealed 128
+ * tokens at a time (the key residual holds 0..127 tokens after every
+ * append); values a FIFO residual of 128 tokens whose oldest token, once
+ * the FIFO is full, leaves quantized per token in groups of 32 channels;
+ * origins and steps kept in bf16 and computed in bf16 (every quantizer
+ * operation an fp32 operation rounded to bf16; RNE codes, clipped; a
+ * constant group keeps step 0).  k_bits = v_bits = 2 or 4; no sink window.
+ * Appends seal keys themselves (kvq_flush_group returns MODE);
+ * kvq_cache_lengths gives (quantized keys T_k, key residual r_K); with t =
+ * T_k + r_K tokens, the values of the first max(0, t - 128) are quantized
+ * and the last min(t, 128) sit in the FIFO.  The decode attends over all
+ * t tokens with one softmax; each token's value comes from the side of the
+ * value boundary it is on (§6). */
+enum { KVQ_K_UNIFORM = 0, KVQ_K_MIXED = 1, KVQ_K_KIVI = 2, KVQ_K_PNMIX = 3 };
+
+/* KVQ_K_PNMIX: PN-Mix H3/L1 keys (PN-Mix reproduction notes, Eq. 2, Eq. 6,
+ * Eq. 7, App. G).  Once per prefill, kvq_pnmix_pairs scores every RoPE
+ * channel pair of each (batch row, KV head) by Eq. 6 (mean pair norm of the
+ * GQA group's prefill queries times that of the prefill keys) and keeps the
+ * n_high_pairs highest (ties: the lower pair) at 3 bits; the other channels
+ * take one bit with Eq. 7's midpoint correction.  Every 128-token key group
+ * is quantized per channel: high channels by Eq. 2 (min-max, origin the
+ * minimum, codes 0..7), low channels by Eq. 7 (scale s = (M - m)/2, offset
+ * z = (3m + M)/4, code RNE((x - z)/s) clipped to 0..1), fp32 arithmetic
+ * (each step rounded to fp32), fp32 offsets and scales.  Storage (App. G):
+ * the codes' least significant bits over all channels (one bit each), then
+ * the upper two bits of the high channels' codes.  Values as KVQ_K_UNIFORM
+ * (v_bits per token over 32 channels).  k_bits is ignored; n_high_pairs is
+ * a multiple of 16 in 0..64; no sink window.  The decode stores each
+ * unit's channels with the selected pairs first (a fixed permutation of
+ * the dot product), so the upper plane is dense. */
+enum { KVQ_PAIRS_ADJACENT = 0, KVQ_PAIRS_SPLIT = 1 };
 
 /* Channel tier ids (MixKVQ three-tier strategy). */
 enum { KVQ_TIER_BF16 = 0, KVQ_TIER_UINT4 = 1, KVQ_TIER_UINT2 = 2 };
@@ -97,9 +129,10 @@ typedef struct kvq_config {
   int kv_heads;    /* Hkv >= 1                                              */
   int head_dim;    /* D; must be KVQ_HEAD_DIM                               */
   int max_tokens;  /* capacity of the quantized history; multiple of 128    */
-  int k_bits;      /* 2 or 4 (KVQ_K_UNIFORM); ignored for KVQ_K_MIXED       */
+  int k_bits;      /* 2 or 4 (KVQ_K_UNIFORM, KVQ_K_KIVI); ignored for
+                      KVQ_K_MIXED                                            */
   int v_bits;      /* 2 or 4                                                */
-  int k_mode;      /* KVQ_K_UNIFORM or KVQ_K_MIXED                          */
+  int k_mode;      /* KVQ_K_UNIFORM, KVQ_K_MIXED or KVQ_K_KIVI              */
   int n_bf16;      /* KVQ_K_MIXED: BF16-tier channels per key group (RANK),
                       or at most that many (THRESHOLD)                      */
   int n_uint4;     /* KVQ_K_MIXED: UINT4-tier channels per key group (RANK),
@@ -112,6 +145,11 @@ typedef struct kvq_config {
   int tier_mode;   /* KVQ_K_MIXED: KVQ_TIERS_RANK (0) or KVQ_TIERS_THRESHOLD */
   float tau_bf16;  /* THRESHOLD: A_d > tau_bf16 -> BF16 (MixKVQ tau_BF16)   */
   float tau_uint4; /* THRESHOLD: A_d > tau_uint4 -> UINT4 (tau_UINT4)       */
+  int n_high_pairs;/* KVQ_K_PNMIX: channel pairs kept at 3 bits (multiple of
+                      16, 0..D/2)                                            */
+  int pair_layout; /* KVQ_K_PNMIX: KVQ_PAIRS_ADJACENT (pair i = channels 2i,
+                      2i + 1, the paper's formula) or KVQ_PAIRS_SPLIT
+                      (channels i, i + D/2, the Hugging Face Llama layout)  */
 } kvq_config;
 
 typedef struct kvq_tier_spec {
@@ -360,6 +398,55 @@ int kvq_export_residual(const kvq_cache* cache, kvq_bf16* k_r, kvq_bf16* v_r,
 int kvq_export_k_mixed(const kvq_cache* cache, uint8_t* counts, uint8_t* perm, kvq_bf16* raw,
                        uint8_t* c4, kvq_bf16* m4, float* s4, uint8_t* c2,
                        kvq_bf16* m2, float* s2, cudaStream_t s);
+
+/*
+ * PN-Mix pair selection (PN-Mix reproduction notes, Eq. 6), once per
+ * prefill, before kvq_quantize_prefill of a KVQ_K_PNMIX cache: for every
+ * (b, KV head) and RoPE pair i (channels a, b of the config's layout),
+ *   sigma_i = (1/Hg) sum_h (1/Lq) sum_t sqrt(q_a^2 + q_b^2)
+ *             * (1/Lk) sum_t sqrt(k_a^2 + k_b^2),
+ * over the GQA group's Hg = Hq / Hkv query heads (in order) of q (bf16
+ * [B][Hq][Lq][D]) and the keys k (bf16 [B][Hkv][Lk][D]), every operation
+ * fp32 rounded (sums in token order, then head order).  The n_high_pairs
+ * largest sigma (ties: lower pair) become the 3-bit pairs; the cache keeps
+ * the selection for every later flush.  sigma (fp32 [B][Hkv][D/2], device)
+ * may be NULL.
+ * Errors: ARG, SHAPE, MODE (not a PN-Mix cache), NOT_EMPTY (the cache holds
+ * tokens), CUDA.  Flags: NONFINITE.
+ */
+int kvq_pnmix_pairs(kvq_cache* cache, const kvq_bf16* q, int Hq, int Lq,
+                    const kvq_bf16* k, int Lk, float* sigma, cudaStream_t s);
+
+/*
+ * Canonical export of a KVQ_K_PNMIX cache's keys, n = T/128 groups: codes
+ * uint8 [B][Hkv][n][128][D] (one code per byte, token-major: 0..7 for the
+ * high channels, 0..1 for the others), offset and scale fp32 [B][Hkv][n][D]
+ * (origin m and step for the high channels, Eq. 7's z and s for the
+ * others), high uint8 [B][Hkv][D] (1 for the channels of the selected
+ * pairs; may be NULL).  Values: kvq_export_v.
+ * Errors: ARG, MODE, CUDA.
+ */
+int kvq_export_pnmix(const kvq_cache* cache, uint8_t* codes, float* offset, float* scale,
+                     uint8_t* high, cudaStream_t s);
+
+/*
+ * Canonical export of a KVQ_K_KIVI cache ("KIVI: KV cache axes" §4–§7), n =
+ * T_k / 128 records, r_K key residual tokens, r_V = min(T_k + r_K, 128)
+ * FIFO values (device destination buffers; the quantized ones may be NULL
+ * when T_k = 0, k_res when r_K = 0):
+ *  keys: k_codes uint8 [B][Hkv][n*4][D][32*bits/8] (per 32-token group and
+ *    channel, the 32 codes LSB first along tokens), k_origin, k_step bf16
+ *    [B][Hkv][n*4][D];
+ *  values: v_codes uint8 [B][Hkv][n*128][D*bits/8] (LSB first along
+ *    channels), v_origin, v_step bf16 [B][Hkv][n*128][D/32]; rows of tokens
+ *    whose values are still in the FIFO are zero (the quantized values are
+ *    the first T_k + r_K - r_V rows);
+ *  k_res bf16 [B][Hkv][r_K][D]; v_res bf16 [B][Hkv][r_V][D], oldest first.
+ * Errors: ARG, MODE (not a KIVI cache), CUDA.
+ */
+int kvq_export_kivi(const kvq_cache* cache, uint8_t* k_codes, kvq_bf16* k_origin,
+                    kvq_bf16* k_step, uint8_t* v_codes, kvq_bf16* v_origin,
+                    kvq_bf16* v_step, kvq_bf16* k_res, kvq_bf16* v_res, cudaStream_t s);
 
 /*
  * The attention-sink window: k, v bf16 [B][Hkv][s][D] (s =

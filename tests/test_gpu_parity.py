@@ -79,7 +79,8 @@ def test_append_and_flush_bit_exact(kb, vb):
 
 
 def test_constant_and_special_groups():
-    """Constant channels/tokens (step 0), -0.0 and +0.0 mixes, exact ties."""
+    """Constant channels/tokens (step 0), -0.0 and +0.0 mixes, exact ties, and
+    a record whose value groups are all constant (every value step 0)."""
     w = small(1, 2, 1, 256, 0)
     K, V = make_kv(w)
     K[0, 0, :128, 5] = 3.0                      # constant key channel
@@ -87,6 +88,7 @@ def test_constant_and_special_groups():
     K[0, 1, 130, 7] = -0.0                      # signed zeros only
     V[0, 0, 10, :32] = -2.5                     # constant value group
     V[0, 1, 11, 32:64] = torch.tensor([0.0, 0.5, 2.5, 3.0] * 8)   # RNE ties
+    V[0, 0, 128:, :] = 0.75                     # a whole record of constant value groups
     cache = kvq.KVCache(1, 2, 256, 2, 2)
     cache.prefill(K.cuda(), V.cuda())
     ref = UnitOracles([0, 1], 2)
