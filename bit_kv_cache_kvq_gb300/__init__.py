@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "KVCache", "decode_bf16", "channel_saliency", "KVQError", "lib",
-    "KVQ_K_UNIFORM", "KVQ_K_MIXED", "KVQ_K_KIVI", "TIER_BF16", "TIER_UINT4", "TIER_UINT2",
+    "KVQ_K_UNIFORM", "KVQ_K_MIXED", "KVQ_K_KIVI", "KVQ_K_PNMIX", "TIER_BF16", "TIER_UINT4", "TIER_UINT2",
     "FLAG_NONFINITE", "FLAG_RANGE", "FLAG_TIMEOUT", "set_wait_limit", "HEAD_DIM", "K_GROUP", "V_GROUP", "RESIDUAL",
 ]
 
@@ -24,8 +24,10 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libkvq.so")
 
 HEAD_DIM, K_GROUP, V_GROUP, RESIDUAL = 128, 128, 32, 128
-KVQ_K_UNIFORM, KVQ_K_MIXED, KVQ_K_KIVI = 0, 1, 2
-_MODES = {"uniform": KVQ_K_UNIFORM, "mixed": KVQ_K_MIXED, "kivi": KVQ_K_KIVI}
+KVQ_K_UNIFORM, KVQ_K_MIXED, KVQ_K_KIVI, KVQ_K_PNMIX = 0, 1, 2, 3
+_MODES = {"uniform": KVQ_K_UNIFORM, "mixed": KVQ_K_MIXED, "kivi": KVQ_K_KIVI,
+          "pnmix": KVQ_K_PNMIX}
+PAIRS_ADJACENT, PAIRS_SPLIT = 0, 1
 TIER_BF16, TIER_UINT4, TIER_UINT2 = 0, 1, 2
 TIERS_RANK, TIERS_THRESHOLD = 0, 1
 FLAG_NONFINITE, FLAG_RANGE, FLAG_TIMEOUT = 1, 2, 4
@@ -84,6 +86,8 @@ _SIGS = {
     "kvq_export_k_mixed": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvq_set_wait_limit": (_I, [_I]),
     "kvq_export_kivi": (_I, [_P] * 10),
+    "kvq_pnmix_pairs": (_I, [_P, _P, _I, _I, _P, _I, _P, _P]),
+    "kvq_export_pnmix": (_I, [_P] * 6),
     "kvq_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -144,15 +148,16 @@ class KVCache:
     def __init__(self, batch: int, kv_heads: int, max_tokens: int, k_bits: int = 2,
                  v_bits: int = 2, mode: str = "uniform", n_bf16: int = 0, n_uint4: int = 0,
                  head_dim: int = HEAD_DIM, device=None, stream=None, n_sink: int = 0,
-                 tier_mode: str = "rank", tau_bf16: float = 0.0, tau_uint4: float = 0.0):
+                 tier_mode: str = "rank", tau_bf16: float = 0.0, tau_uint4: float = 0.0,
+                 n_high_pairs: int = 0, pair_layout: int = PAIRS_ADJACENT):
         if tier_mode not in ("rank", "threshold"):
             raise ValueError("tier_mode is 'rank' or 'threshold'")
         if mode not in _MODES:
-            raise ValueError("mode is 'uniform', 'mixed' or 'kivi'")
+            raise ValueError("mode is 'uniform', 'mixed', 'kivi' or 'pnmix'")
         self.cfg = _Config(batch, kv_heads, head_dim, max_tokens, k_bits, v_bits,
                            _MODES[mode], n_bf16, n_uint4,
                            n_sink, TIERS_THRESHOLD if tier_mode == "threshold"
-                           else TIERS_RANK, tau_bf16, tau_uint4)
+                           else TIERS_RANK, tau_bf16, tau_uint4, n_high_pairs, pair_layout)
         self.tier_mode = tier_mode
         self.mode = mode
         nbytes = lib().kvq_cache_bytes(ctypes.byref(self.cfg))
@@ -309,6 +314,35 @@ class KVCache:
         _check(lib().kvq_export_sink(self._h, ks.data_ptr(), vs.data_ptr(), _stream(stream)),
                "kvq_export_sink")
         return ks, vs
+
+    def pnmix_pairs(self, q: torch.Tensor, k: torch.Tensor, stream=None) -> torch.Tensor:
+        """PN-Mix Eq. 6 pair scores from the prefill queries q bf16 [B, Hq, Lq,
+        D] and keys k bf16 [B, Hkv, Lk, D]; the cache keeps the selection of
+        n_high_pairs pairs.  Returns sigma fp32 [B, Hkv, D/2]."""
+        B, Hq, Lq, D = q.shape
+        Lk = k.shape[2]
+        sigma = torch.empty(self.batch, self.kv_heads, HEAD_DIM // 2, dtype=torch.float32,
+                            device=q.device)
+        _check(lib().kvq_pnmix_pairs(
+            self._h, _ptr(q, torch.bfloat16, (self.batch, Hq, Lq, HEAD_DIM), "q"), Hq, Lq,
+            _ptr(k, torch.bfloat16, (self.batch, self.kv_heads, Lk, HEAD_DIM), "k"), Lk,
+            sigma.data_ptr(), _stream(stream)), "kvq_pnmix_pairs")
+        return sigma
+
+    def export_pnmix(self, stream=None):
+        """PN-Mix key groups (kvq_export_pnmix): codes uint8 [B, Hkv, n, 128, D],
+        offset / scale fp32 [B, Hkv, n, D], high uint8 [B, Hkv, D]."""
+        tq, _ = self.lengths()
+        n = tq // K_GROUP
+        B, H, dev = self.batch, self.kv_heads, self.device
+        codes = torch.zeros(B, H, n, K_GROUP, HEAD_DIM, dtype=torch.uint8, device=dev)
+        off = torch.zeros(B, H, n, HEAD_DIM, dtype=torch.float32, device=dev)
+        sc = torch.zeros(B, H, n, HEAD_DIM, dtype=torch.float32, device=dev)
+        high = torch.zeros(B, H, HEAD_DIM, dtype=torch.uint8, device=dev)
+        ptr = lambda t: t.data_ptr() if t.numel() else None
+        _check(lib().kvq_export_pnmix(self._h, ptr(codes), ptr(off), ptr(sc), high.data_ptr(),
+                                      _stream(stream)), "kvq_export_pnmix")
+        return codes, off, sc, high
 
     def export_kivi(self, stream=None):
         """KIVI cache state (kvq_export_kivi): dict of device tensors k_codes

@@ -156,7 +156,7 @@ int mma_warps_per_cta(const RecLayout& lay, int n_rep) {
   // the variant's register-bound warp count
   const bool sep = lay.mixed != 0 || lay.kivi != 0;   // value tables in their own area
   const int per = lay.bytes + warp_extra(sep);
-  return max(1, min(max_warps(lay.kb, lay.vb, n_rep, sep), (227 * 1024) / per));
+  return max(1, min(max_warps(lay.kb, lay.vb, n_rep, sep || lay.pnmix != 0), (227 * 1024) / per));
 }
 
 bool mma_plan(int num_sms, int units, int n_rep, int n_groups, int r, int sink,
@@ -250,12 +250,13 @@ cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, flo
   a.ws = ws;
   a.status = c->status;
   a.wait_polls = decode_wait_polls();
+  a.perm = c->pn_perm;
   const int nrep = Hq / c->cfg.kv_heads;
   const int kb = c->cfg.k_bits, vb = c->cfg.v_bits;
   const int warps = mma_warps_per_cta(c->lay, nrep);
   cudaError_t e;
   if (c->lay.pnmix) {
-    return cudaErrorNotSupported;   // the PN-Mix decode path follows
+    e = launch_decode_pnmix(a, nrep, vb, warps, s);
   } else if (c->lay.kivi) {
     e = launch_decode_kivi(a, nrep, kb, warps, s);
   } else if (c->cfg.k_mode == KVQ_K_MIXED) {

@@ -74,9 +74,11 @@ struct MmaArgs {
   float* ws;              // [units][max_parts][NREP][D + 2]
   unsigned* status;       // sticky KVQ_FLAG_* word of the cache
   int wait_polls;         // try_wait polls before a wait for a staged part gives up
+  const uint8_t* perm;    // PN-Mix: [units][D] stored position -> channel
 };
 
 cudaError_t launch_decode_kivi(const MmaArgs& a, int nrep, int bits, int warps, cudaStream_t s);
+cudaError_t launch_decode_pnmix(const MmaArgs& a, int nrep, int vbits, int warps, cudaStream_t s);
 
 namespace {
 
@@ -158,12 +160,24 @@ __device__ __forceinline__ void unpack4(uint32_t x, uint32_t y, uint32_t (&a)[4]
   a[2] = x & Mt;
   a[3] = y & Mt;
 }
+// PN-Mix LSB plane (1 bit a code): a word holds four k-steps (k_local4 =
+// k & 3); registers a0, a2 from x, a1, a3 from y = x >> 8, each masked to
+// the bits 2 * k_local4 + (reg >> 1) of both halves.
+template <int KL4>
+__device__ __forceinline__ void unpack1(uint32_t x, uint32_t y, uint32_t (&a)[4]) {
+  constexpr uint32_t Mb = 0x00010001u << (2 * KL4), Mt = 0x00020002u << (2 * KL4);
+  a[0] = x & Mb;
+  a[1] = y & Mb;
+  a[2] = x & Mt;
+  a[3] = y & Mt;
+}
 // 2^(15 - pos) for B rows b0 (slot 0: rows 2t, 2t+1) and b1 (slot 1: rows
-// 2t+8, 2t+9) of k-step k.
+// 2t+8, 2t+9) of k-step k (BITS = 1: the PN-Mix LSB plane).
 template <int BITS>
 __host__ __device__ constexpr float row_factor(int k, int slot) {
-  return BITS == 2 ? static_cast<float>(1 << (15 - 4 * (k & 1) - 2 * slot))
-                   : static_cast<float>(1 << (15 - 4 * slot));
+  return BITS == 2   ? static_cast<float>(1 << (15 - 4 * (k & 1) - 2 * slot))
+         : BITS == 1 ? static_cast<float>(1 << (15 - 2 * (k & 3) - slot))
+                     : static_cast<float>(1 << (15 - 4 * slot));
 }
 
 
@@ -200,7 +214,7 @@ __device__ __forceinline__ int slot_of(const MmaArgs& a, long long p) {
   return static_cast<int>(((p + 1) * a.n_slots - 1) / a.total);
 }
 
-template <int KB, int VB, int NREP, bool MIX, bool KIVI = false>
+template <int KB, int VB, int NREP, bool MIX, bool KIVI = false, bool PNMIX = false>
 struct Warp {
   static constexpr bool SEP = MIX || KIVI;  // value tables in their own area
   static constexpr bool SPARE = NREP <= 4;  // Q' low part in odd columns;
@@ -300,6 +314,10 @@ struct Warp {
       if (h >= NREP) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+      } else if (PNMIX) {   // the unit's stored channel order
+        const uint8_t* pm = a.perm + static_cast<long long>(u) * kD + c;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = bf2f(qg[h * kD + pm[i]]) * c0;
       } else if ((reinterpret_cast<uintptr_t>(a.q) & 15) == 0) {
         const uint4* src = reinterpret_cast<const uint4*>(qg + h * kD + c);
 #pragma unroll
@@ -323,7 +341,13 @@ struct Warp {
       uint32_t* q = static_cast<uint32_t*>(qs);
       for (int i = lane; i < 8 * (kD / 2); i += 32) {
         const int h = i / (kD / 2), c2 = i % (kD / 2);
-        q[h * (kQRow / 2) + c2] = reinterpret_cast<const uint32_t*>(qg + h * kD)[c2];
+        if (PNMIX) {   // the unit's stored channel order
+          const uint8_t* pm = a.perm + static_cast<long long>(u) * kD + 2 * c2;
+          q[h * (kQRow / 2) + c2] = static_cast<uint32_t>(qg[h * kD + pm[0]]) |
+                                    (static_cast<uint32_t>(qg[h * kD + pm[1]]) << 16);
+        } else {
+          q[h * (kQRow / 2) + c2] = reinterpret_cast<const uint32_t*>(qg + h * kD)[c2];
+        }
       }
     }
     __syncwarp();
@@ -396,6 +420,7 @@ struct Warp {
       return;
     }
     if constexpr (MIX) scores_mixed(S, hinv, hbias);
+    else if constexpr (PNMIX) scores_pnmix(S, hinv, hbias);
     else scores_uniform(S, hinv, hbias);
     if (SPARE) {   // columns 2t and 2t + 1: the high and low parts of head t
 #pragma unroll
@@ -583,6 +608,142 @@ struct Warp {
             inv_sq, bias);
     head_units(inv_sq, bias, hinv, hbias);
     qk_tiles<0, 8>(S, bq, bl);
+  }
+
+  // PN-Mix H3/L1 keys (PN-Mix reproduction notes, Eq. 2, Eq. 7, App. G), in
+  // the unit's stored channel order (the query in shared memory is in it
+  // too): a code is c = c0 + 2 c12 with c0 its LSB (every channel) and c12
+  // its upper two bits (the nh high channels, stored first), so
+  //   s = sum_p q_p z_p + sum_p (q_p s_p) c0_p + sum_{p < nh} (2 q_p s_p) c12_p
+  // with z the origins / Eq. 7 offsets and s the steps / Eq. 7 scales.  The
+  // LSB plane runs as 1-bit codes over all eight k-steps, the upper plane as
+  // 2-bit codes over the first nh / 16; one power-of-two unit for both.
+  __device__ __forceinline__ void scores_pnmix(float (&S)[8][4], float (&hinv)[2],
+                                               float (&hbias)[2]) {
+    const RecLayout& L = a.lay;
+    const float* ksc = reinterpret_cast<const float*>(kbuf + L.k_scale);
+    const float* kof = reinterpret_cast<const float*>(kbuf + L.k_min);
+    const int nh16 = L.nh >> 4;   // upper-plane k-steps
+    uint32_t b1[8][2], b2[8][2], l1[NL][2], l2[NL][2];
+    float sq, inv_sq, bias = 0.0f;
+    const float c0 = kLog2e * rsqrtf(static_cast<float>(kD));
+    // Q' of this lane's rows (SPARE: 16 channels of one head, the pair's two
+    // lanes splitting b0 / b1 rows; else 32 channels of head g)
+    constexpr int NQ = SPARE ? 16 : 32;
+    float qk[NQ];
+    float mx = 0.0f;
+    const int par = g & 1;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+      for (int j = 0; j < (SPARE ? 2 : 4); ++j) {
+        const int ch = SPARE ? 16 * ks + 2 * t + 8 * par + j : 16 * ks + 2 * t + (j & 1) + 8 * (j >> 1);
+        const float qv = SPARE ? static_cast<const float*>(qs)[hrow() * kQRow + ch]
+                               : bf2f(static_cast<const uint16_t*>(qs)[g * kQRow + ch]) * c0;
+        const float x = qv * ksc[ch];
+        bias = fmaf(qv, kof[ch], bias);
+        qk[(SPARE ? 2 : 4) * ks + j] = x;
+        mx = fmaxf(mx, fabsf(x) * (ch < L.nh ? 2.0f : 1.0f));
+      }
+    }
+    if (SPARE) {
+#pragma unroll
+      for (int x = 1; x <= 4; x <<= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, x));
+        bias += __shfl_xor_sync(kFull, bias, x);
+      }
+    } else {
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+      bias += __shfl_xor_sync(kFull, bias, 1);
+      bias += __shfl_xor_sync(kFull, bias, 2);
+    }
+    pow2_norm(mx, sq, inv_sq);
+    // B fragments of both planes: x * sq * row factor (times 2 for the upper
+    // plane), split into an f16 high part and an f16 low part
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+      for (int plane = 0; plane < 2; ++plane) {
+        if (plane == 1 && ks >= nh16) continue;
+        if constexpr (SPARE) {
+          const float f = sq * (plane ? 2.0f * row_factor<2>(ks, par) : row_factor<1>(ks, par));
+          const float x0 = qk[2 * ks] * f, x1 = qk[2 * ks + 1] * f;
+          const uint32_t H = pack_h2(x0, x1);
+          const float2 hf = h2_to_f2(H);
+          const uint32_t Lo = pack_h2(x0 - hf.x, x1 - hf.y);
+          const uint32_t recv = __shfl_xor_sync(kFull, par ? H : Lo, 4);
+          uint32_t (&bb)[8][2] = plane ? b2 : b1;
+          bb[ks][0] = par ? recv : H;
+          bb[ks][1] = par ? Lo : recv;
+        } else {
+          const float f0 = sq * (plane ? 2.0f * row_factor<2>(ks, 0) : row_factor<1>(ks, 0));
+          const float f1 = sq * (plane ? 2.0f * row_factor<2>(ks, 1) : row_factor<1>(ks, 1));
+          const float x[4] = {qk[4 * ks] * f0, qk[4 * ks + 1] * f0, qk[4 * ks + 2] * f1,
+                              qk[4 * ks + 3] * f1};
+          uint32_t (&bb)[8][2] = plane ? b2 : b1;
+          uint32_t (&ll)[NL][2] = plane ? l2 : l1;
+          bb[ks][0] = pack_h2(x[0], x[1]);
+          bb[ks][1] = pack_h2(x[2], x[3]);
+          const float2 h01 = h2_to_f2(bb[ks][0]), h23 = h2_to_f2(bb[ks][1]);
+          ll[ks % NL][0] = pack_h2(x[0] - h01.x, x[1] - h01.y);
+          ll[ks % NL][1] = pack_h2(x[2] - h23.x, x[3] - h23.y);
+        }
+      }
+    }
+    head_units(inv_sq, bias, hinv, hbias);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) S[mt][c] = 0.0f;
+    // LSB plane: word (mt*2 + ks/4)*32 + lane, four k-steps a word
+    const uint32_t* lsb = reinterpret_cast<const uint32_t*>(kbuf + L.k_codes);
+#pragma unroll
+    for (int kq = 0; kq < 2; ++kq) {
+      uint32_t kx[8], ky[8];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        kx[mt] = lsb[(mt * 2 + kq) * 32 + lane];
+        ky[mt] = kx[mt] >> 8;
+      }
+#pragma unroll
+      for (int kl4 = 0; kl4 < 4; ++kl4) {
+        const int ks = 4 * kq + kl4;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t A[4];
+          if (kl4 == 0) unpack1<0>(kx[mt], ky[mt], A);
+          else if (kl4 == 1) unpack1<1>(kx[mt], ky[mt], A);
+          else if (kl4 == 2) unpack1<2>(kx[mt], ky[mt], A);
+          else unpack1<3>(kx[mt], ky[mt], A);
+          qk_mma(S[mt], A, b1, l1, ks);
+        }
+      }
+    }
+    // upper plane: 2-bit words (mt*kw2 + w)*32 + lane over the first nh channels
+    const uint32_t* up = reinterpret_cast<const uint32_t*>(kbuf + L.kc);
+    const int kw2 = L.kw2;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      if (w >= kw2) break;
+      uint32_t kx[8], ky[8];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        kx[mt] = up[(mt * kw2 + w) * 32 + lane];
+        ky[mt] = kx[mt] >> 8;
+      }
+#pragma unroll
+      for (int kl = 0; kl < 2; ++kl) {
+        const int ks = 2 * w + kl;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t A[4];
+          if (kl) unpack2<1>(kx[mt], ky[mt], A);
+          else unpack2<0>(kx[mt], ky[mt], A);
+          qk_mma(S[mt], A, b2, l2, ks);
+        }
+      }
+    }
   }
 
   // KIVI keys ("KIVI: KV cache axes" §3–§4: keys grouped along tokens): four
@@ -1320,8 +1481,8 @@ struct Warp {
 };
 
 
-template <int KB, int VB, int NREP, bool MIX, bool KIVI = false>
-__global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX || KIVI) * 32, 1) decode_mma_kernel(MmaArgs a) {
+template <int KB, int VB, int NREP, bool MIX, bool KIVI = false, bool PNMIX = false>
+__global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX || KIVI || PNMIX) * 32, 1) decode_mma_kernel(MmaArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   // Consecutive slices (records of one unit, contiguous in memory) run on
@@ -1336,7 +1497,7 @@ __global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX || KIVI) * 32, 1) 
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   if (slot >= a.n_slots) return;            // warp-uniform
   uint8_t* mine = smem + static_cast<size_t>(warp) * (a.rec_bytes + warp_extra(MIX || KIVI));
-  Warp<KB, VB, NREP, MIX, KIVI> W(a, mine);
+  Warp<KB, VB, NREP, MIX, KIVI, PNMIX> W(a, mine);
   const long long p0 = slot_start(a, slot), p1 = slot_start(a, slot + 1);
   const int u_last = static_cast<int>((p1 - 1) / a.unit_len);
   // after a wait gave up: empty partials for this unit and the rest of the slice
@@ -1414,10 +1575,10 @@ __global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX || KIVI) * 32, 1) 
   }
 }
 
-template <int KB, int VB, int NREP, bool MIX, bool KIVI = false>
+template <int KB, int VB, int NREP, bool MIX, bool KIVI = false, bool PNMIX = false>
 cudaError_t launch_cfg(const MmaArgs& a, int warps, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(warps) * (a.rec_bytes + warp_extra(MIX || KIVI));
-  auto kern = decode_mma_kernel<KB, VB, NREP, MIX, KIVI>;
+  auto kern = decode_mma_kernel<KB, VB, NREP, MIX, KIVI, PNMIX>;
   static SmemOptIn opt_in;
   cudaError_t e = opt_in.ensure(kern);
   if (e != cudaSuccess) return e;
@@ -1426,13 +1587,13 @@ cudaError_t launch_cfg(const MmaArgs& a, int warps, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int KB, int VB, bool MIX, bool KIVI = false>
+template <int KB, int VB, bool MIX, bool KIVI = false, bool PNMIX = false>
 cudaError_t launch_rep(const MmaArgs& a, int nrep, int warps, cudaStream_t s) {
   switch (nrep) {
-    case 1: return launch_cfg<KB, VB, 1, MIX, KIVI>(a, warps, s);
-    case 2: return launch_cfg<KB, VB, 2, MIX, KIVI>(a, warps, s);
-    case 4: return launch_cfg<KB, VB, 4, MIX, KIVI>(a, warps, s);
-    case 8: return launch_cfg<KB, VB, 8, MIX, KIVI>(a, warps, s);
+    case 1: return launch_cfg<KB, VB, 1, MIX, KIVI, PNMIX>(a, warps, s);
+    case 2: return launch_cfg<KB, VB, 2, MIX, KIVI, PNMIX>(a, warps, s);
+    case 4: return launch_cfg<KB, VB, 4, MIX, KIVI, PNMIX>(a, warps, s);
+    case 8: return launch_cfg<KB, VB, 8, MIX, KIVI, PNMIX>(a, warps, s);
     default: return cudaErrorInvalidValue;
   }
 }
