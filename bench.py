@@ -51,13 +51,13 @@ ATTN_REPS = 50                     # per-call timed decode attention calls (roof
 # launch, from the ncu capture of this workload at batch 8 kept under
 # profiles/, keyed by the hash of the decode kernel's code it was taken on
 # (a stale entry reports null).  The capture ran at batch 8 (64 units,
-# 32768 + 100 tokens, the token append fused): 200.958 MB read + 4.277 MB
-# written against 200.884 MB of algorithmic attention bytes (ratio 1.0217:
+# 32768 + 100 tokens, the token append fused): 200.988 MB read + 4.122 MB
+# written against 200.638 MB of algorithmic attention bytes (ratio 1.0223:
 # mostly the split-K partials written).  Traffic per unit is independent of
 # the batch, so the batch-16 launch is that ratio times its algorithmic
 # bytes at the timed steps' mean context.
 NCU_TRAFFIC = {
-    "4e86b4276ef94d1d": {("llama8b_gqa_32k_b16", 16, 32768, 2): 205.235456 / 200.884224 * 399.264512e6},
+    "a90e9160ac0c200e": {("llama8b_gqa_32k_b16", 16, 32768, 2): 205.110016 / 200.638464 * 401.375232e6},
 }
 
 
@@ -183,10 +183,20 @@ def kivi_half_bytes(w):
     return 128 * w.k_bits // 8 + 16
 
 
+def pnmix_k_bytes(w):
+    """PN-Mix key bytes per token: the LSB plane (1 bit a channel), the upper
+    two bits of the 2 n_high_pairs high channels, an fp32 offset and scale
+    per channel and 128-token group."""
+    nh = 2 * w.extra.get("n_high_pairs", 32)
+    return 128 / 8 + nh * 2 / 8 + 128 * 8 / 128
+
+
 def token_bytes(w):
     """Algorithmic bytes of one quantized token of one (b, kv head)."""
     if w.mode == "kivi":
         return 2 * kivi_half_bytes(w)
+    if w.mode == "pnmix":
+        return pnmix_k_bytes(w) + 128 * w.v_bits // 8 + 24
     v = 128 * w.v_bits // 8 + 24
     if w.mode == "mixed":
         return mixed_k_group_bytes(w) / 128 + v
@@ -264,6 +274,10 @@ def config_of(w, extra=None):
     if w.mode == "kivi":
         c.update({"k_mode": "kivi", "k_group_tokens": 32, "key_seal_tokens": 128,
                   "value_fifo_tokens": 128, "metadata": "bf16"})
+    if w.mode == "pnmix":
+        c.update({"k_mode": "pnmix", "n_high_pairs": w.extra.get("n_high_pairs", 32),
+                  "high_bits": 3, "low_bits": 1, "pair_layout": "adjacent",
+                  "query_window": w.Lq})
     if extra:
         c.update(extra)
     return c
@@ -284,6 +298,16 @@ class OracleSample:
         for j in range(n_units):
             u = scaled(self.one, seed=self.one.seed + 17 * j)
             K, V = make_kv(u)
+            if u.mode == "pnmix":
+                qw = bf16_bits(make_query_window(u)[0])
+                sig = orc.pair_scores(qw, bf16_bits(K[0, 0]), orc.PAIR_ADJACENT)
+                high = orc.channel_mask(orc.select_pairs(sig, u.extra.get("n_high_pairs", 32)),
+                                        orc.PAIR_ADJACENT)[None, None]
+                c = oracle_mod.OracleCache(1, 1, 128, u.k_bits, u.v_bits, mode="pnmix",
+                                           high_channels=high)
+                c.prefill(bf16_bits(K), bf16_bits(V))
+                self.units.append((u, c, [bf16_bits(make_q(u, step=s)) for s in range(4)]))
+                continue
             if u.mode == "kivi":
                 c = oracle_mod.KiviOracleCache(1, 1, 128, u.k_bits, u.v_bits)
                 c.prefill(bf16_bits(K), bf16_bits(V))
@@ -380,7 +404,9 @@ def run_ours(args, rank, world):
                                                 Kall[:, :, :128].contiguous(), 2,
                                                 n_bf16=w.n_bf16, n_uint4=w.n_uint4)
     cache = kvq.KVCache(w.B, w.Hkv, cap, w.k_bits, w.v_bits, mode=w.mode, n_bf16=w.n_bf16,
-                        n_uint4=w.n_uint4, device=dev)
+                        n_uint4=w.n_uint4, device=dev,
+                        n_high_pairs=w.extra.get("n_high_pairs", 0))
+    qwin = make_query_window(w, device=dev) if w.mode == "pnmix" else None
     out = torch.empty(w.B, w.Hq, 128, dtype=torch.float32, device=dev)
     ws = cache.workspace(w.Hq)
     stream = torch.cuda.current_stream()
@@ -388,6 +414,8 @@ def run_ours(args, rank, world):
 
     def prefill():
         cache.reset()
+        if qwin is not None:     # PN-Mix: Eq. 6 pair selection, once per prefill
+            cache.pnmix_pairs(qwin, K0)
         cache.prefill(K0, V0, importance=importance)
 
     # prefill quantize (kvq_quantize_prefill) on its own: bf16 K, V read once,
@@ -457,6 +485,8 @@ def run_ours(args, rank, world):
     Lp = w.T_q + r0
     Kp, Vp = Kall[:, :, :Lp].contiguous(), Vall[:, :, :Lp].contiguous()
     cache.reset()
+    if qwin is not None:
+        cache.pnmix_pairs(qwin, Kp)
     cache.prefill(Kp, Vp, importance=importance)
     del Kp, Vp
     scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -529,7 +559,8 @@ def run_ours(args, rank, world):
         "prefill": {"tokens": L0, "us": prefill_us,
                     "gbs": prefill_nb / (prefill_us * 1e-6) / 1e9,
                     "algorithmic_bytes": prefill_nb,
-                    "note": "kvq_quantize_prefill alone, outside the timed decode steps"},
+                    "note": "kvq_quantize_prefill alone, outside the timed decode steps"
+                            + ("; includes the Eq. 6 pair selection" if w.mode == "pnmix" else "")},
     }
 
     # bf16 unquantized comparator at the same batch and context

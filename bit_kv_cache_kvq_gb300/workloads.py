@@ -68,6 +68,12 @@ WORKLOADS = {
     # FIFO, bf16 metadata) on the Llama-8B decode layer, KIVI-2
     "kivi_llama8b_32k_b16": Workload("kivi_llama8b_32k_b16", 1006, B=16, Hq=32, Hkv=8,
                                      T_q=32768, r=100, mode="kivi"),
+    # PN-Mix H3/L1 keys (32 of 64 pairs at 3 bits, the rest 1 bit, adjacent
+    # pairs; 2-bit values) on the Llama-8B decode layer; Eq. 6 from a
+    # 128-token query window
+    "pnmix_llama8b_32k_b16": Workload("pnmix_llama8b_32k_b16", 1007, B=16, Hq=32, Hkv=8,
+                                      T_q=32768, r=100, mode="pnmix", Lq=128, q_outliers=8,
+                                      q_scale=6.0, extra={"n_high_pairs": 32}),
     # MixKVQ: Qwen-32B layer, 64 q / 8 kv heads, batch 8, 16K context
     "mixkvq_qwen32b_16k_b8": Workload("mixkvq_qwen32b_16k_b8", 1004, B=8, Hq=64, Hkv=8,
                                       T_q=16384, r=100, k_outliers=6, mode="mixed",
