@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restr
 // 64 + 2l, 65 + 2l), then the warps' (M, L, O) merge through shared memory
 // by the same rule.
 constexpr int kManyWarps = 8;
+constexpr size_t kSpreadSmem = 48 * 1024;
 __global__ void __launch_bounds__(kManyWarps * 32) combine_many_kernel(
     const float* __restrict__ ws, int Hkv, int Hq, int max_parts, long long unit_len,
     long long total, int n_slots, float* __restrict__ out) {
@@ -207,7 +208,11 @@ cudaError_t launch_combine_parts(const float* ws, int B, int Hkv, int Hq, int ma
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(B * Hq);
   lc.blockDim = dim3(many ? kManyWarps * 32 : kD);
-  lc.dynamicSmemBytes = 0;
+  // The decode blocks leave their SMs at different times and the first
+  // SMs to free up would take every combine block (16 a SM), sharing their
+  // L2 bandwidth; 48 KB of (unused) shared memory a block caps it at 4 a
+  // SM, so the rows spread over ~B * Hq / 4 SMs.
+  lc.dynamicSmemBytes = many ? 0 : kSpreadSmem;
   lc.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
