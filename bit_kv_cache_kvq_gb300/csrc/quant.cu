@@ -112,10 +112,6 @@ __device__ __forceinline__ uint32_t swap_halves(uint32_t a) { return __byte_perm
 
 // d = RN(x - m) for the bf16 x in the low (high) half of w, given nm = -m:
 // one mixed-precision FMA x * 1 + nm (x * 1 is exact, so this is fl32(x - m)).
-#ifndef KVQ_QSUB_FMA
-#define KVQ_QSUB_FMA 1
-#endif
-#if KVQ_QSUB_FMA
 __device__ __forceinline__ float sub_lo(uint32_t w, float nm) {
   float d;
   asm("{\n .reg .b16 l, h, one;\n mov.b32 {l, h}, %1;\n mov.b16 one, 0x3F80;\n"
@@ -128,37 +124,38 @@ __device__ __forceinline__ float sub_hi(uint32_t w, float nm) {
       " fma.rn.f32.bf16 %0, h, one, %2;\n}\n" : "=f"(d) : "r"(w), "f"(nm));
   return d;
 }
-#else
-__device__ __forceinline__ float sub_lo(uint32_t w, float nm) { return __fadd_rn(__uint_as_float(w << 16), nm); }
-__device__ __forceinline__ float sub_hi(uint32_t w, float nm) { return __fadd_rn(__uint_as_float(w & 0xFFFF0000u), nm); }
-#endif
 
-// The code of d = fl32(x - m) in the fast form.  y = RN(d * r + 48) with r =
-// RN(1/step) lies in [48, 64) (codes <= 15), where the fp32 spacing is
-// 2^-18, so the bits of y hold (d/step) with 18 fraction bits.  |y - 48 -
+// The code of d = fl32(x - m) in the fast form.  y = RN(d * r + 32) with r =
+// RN(1/step) lies in [32, 64) (codes <= 15), where the fp32 spacing is
+// 2^-18, so the bits of y hold (d/step) with 18 fraction bits.  |y - 32 -
 // d/step| <= 2^-19 + 16 * 2^-24 and |RN(d/step) - d/step| <= 2^-21, so y -
-// 48 is within 1.2 units of 2^-18 of the IEEE quotient RN(d/step).  Adding
+// 32 is within 1.2 units of 2^-18 of the IEEE quotient RN(d/step).  Adding
 // 1/2 + 2 units and keeping the integer part gives RNE(RN(d/step)) unless
 // the fraction lies within 2 units of 1/2, below 1/2 or 5 above ("near"):
-// then the element takes the exact path.  Returns the adjusted bits v: the
-// code is (v >> 18) & (2^b - 1).
-constexpr float kCodeMagic = 48.0f;
+// then the element takes the exact path.  The addition rides in the FMA:
+// 1/2 + 2^-17 is an even multiple of the spacing, so RN(d * r + 32 + 1/2 +
+// 2^-17) is y plus 1/2 + 2 units exactly (ties included) and stays below
+// 64.  Returns those bits v: the code is (v >> 18) & (2^b - 1).
+constexpr float kCodeMagic = 32.500007629394531f;   // 32 + 1/2 + 2^-17
 constexpr uint32_t kHalfPlus = 0x20002u;    // 1/2 + 2 units of 2^-18
 constexpr uint32_t kNearMask = 0x3FFF8u;    // fraction within [1/2 - 2, 1/2 + 5] units
 __device__ __forceinline__ uint32_t code_bits(float d, float r) {
-  return __float_as_uint(fmaf(d, r, kCodeMagic)) + kHalfPlus;
+  return __float_as_uint(fmaf(d, r, kCodeMagic));
 }
 __device__ __forceinline__ bool is_near(uint32_t v) { return (v & kNearMask) == 0u; }
 // A near element: its quotient z = d/step lies close to h = n + 1/2, n =
-// floor(y - 48), so its code is n or n + 1, decided by RNE(RN(z)).  With
+// floor(y - 32), so its code is n or n + 1, decided by RNE(RN(z)).  With
 // rem = d - h * step, exact in one FMA (the operands nearly cancel: h has at
 // most 5 significant bits and |rem| < 2^-14 d), RN(z) = h exactly when
 // -step * ulp-(h)/2 <= rem <= step * ulp(h)/2 (h has an even significand, so
 // it wins both ties), and then the code is RNE(h) = n + (n & 1); above that
 // band RN(z) > h (code n + 1), below it RN(z) < h (code n).  Needs step >=
 // 2^-100 (no underflow in the bounds); smaller steps take the exact tile
-// path.  Returns the code in code_bits' position.
-__device__ __forceinline__ uint32_t near_bits(uint32_t v, float d, float step, uint32_t top) {
+// path.  Returns the code in code_bits' position.  Out of line: elements
+// come here rarely (ties of bf16 data, about one in 2^15 otherwise), and
+// an inline copy at each of a thread's 64 unrolled elements would grow the
+// code passes past the instruction cache.
+__device__ __noinline__ uint32_t near_bits(uint32_t v, float d, float step, uint32_t top) {
   const uint32_t n = ((v - kHalfPlus) >> 18) & 15u;
   const float h = static_cast<float>(n) + 0.5f;
   const float rem = fmaf(-h, step, d);
@@ -515,8 +512,11 @@ __device__ __forceinline__ void value_part(const QuantArgs& a, uint8_t* smem) {
 
 // Uniform keys and values of one 128-token group: block (group, unit, z),
 // z = 0 the keys, z = 1 the values, each from its own 32 KB staged tile.
+// At most 48 registers a thread, so five blocks (40 warps) share an SM:
+// each block waits on its tile load alone, and more blocks keep more loads
+// in flight.
 template <int KB, int VB>
-__global__ void __launch_bounds__(256) quantize_uniform_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(256, 5) quantize_uniform_kernel(QuantArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   if (blockIdx.z) {
     value_part<VB>(a, smem);
