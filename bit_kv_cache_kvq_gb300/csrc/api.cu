@@ -249,7 +249,7 @@ int kvq_cache_reset(kvq_cache* c, cudaStream_t s) {
 
 int kvq_pnmix_pairs(kvq_cache* c, const kvq_bf16* q, int Hq, int Lq, const kvq_bf16* k, int Lk,
                     float* sigma, cudaStream_t s) {
-  if (!c || !q || !k || Lq < 1 || Lk < 1) return KVQ_ERR_ARG;
+  if (!c || !q || !k || Lq < 1 || Lk < 1 || !aligned16(k)) return KVQ_ERR_ARG;
   if (!is_pnmix(c)) return KVQ_ERR_MODE;
   if (Hq < c->cfg.kv_heads || Hq % c->cfg.kv_heads) return KVQ_ERR_SHAPE;
   if (c->t_q != 0 || c->r != 0) return KVQ_ERR_NOT_EMPTY;

@@ -198,7 +198,7 @@ struct kvq_cache {
 namespace kvq {
 
 // Raises one kernel's dynamic shared-memory limit to the device's opt-in
-// maximum, once per device (a cudaFuncSetAttribute round trip on every
+// maximum (less the kernel's static shared memory), once per device (a cudaFuncSetAttribute round trip on every
 // launch would add host time to every call).  One instance per kernel.
 struct SmemOptIn {
   std::atomic<unsigned long long> done{0};   // bit d: device d is set up
@@ -209,10 +209,14 @@ struct SmemOptIn {
     if (e != cudaSuccess) return e;
     const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
     if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    // the opt-in maximum less the kernel's static shared memory
     int most = 0;
+    cudaFuncAttributes fa;
     e = cudaDeviceGetAttribute(&most, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               most - static_cast<int>(fa.sharedSizeBytes));
     if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
     return e;
   }

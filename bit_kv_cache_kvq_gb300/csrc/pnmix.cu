@@ -6,77 +6,194 @@
 
 #include "frag_layout.h"
 #include "kvq_internal.h"
+#include "sqrt_rn.h"
 
 namespace kvq {
 namespace {
 
 __device__ __forceinline__ float bfv(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
-// Mean pair norm of rows [0, L) of x (bf16 [L][D]): (1/L) sum_t
-// sqrt(a^2 + b^2), every operation fp32 rounded, the sum in token order.
-__device__ float mean_pair_norm(const uint16_t* x, int L, int ca, int cb, bool& bad) {
-  float acc = 0.0f;
-  for (int t = 0; t < L; ++t) {
-    const float a = bfv(x[static_cast<long long>(t) * kD + ca]);
-    const float b = bfv(x[static_cast<long long>(t) * kD + cb]);
-    if (!isfinite(a) || !isfinite(b)) bad = true;
-    const float ss = __fadd_rn(__fmul_rn(a, a), __fmul_rn(b, b));
-    acc = __fadd_rn(acc, __fsqrt_rn(ss));
+// Eq. 6 for one (b, KV head): block = unit.  sigma_i = qbar_i * kbar_i
+// (qbar: the mean over the GQA group's heads, in order, of the heads' mean
+// pair norms).  Warps 0-1 (pair i = thread) sum the key pair norms in token
+// order while the unit's key rows stream through a ring of kPairStages
+// shared-memory slots of kPairRows rows (one bulk copy a slot, on an
+// mbarrier); warps 2-3 (pair i = thread - 64) take the query means.  Then
+// the n_high largest sigma (ties: lower pair; a NaN counts as the smallest)
+// are selected, and the unit's stored channel order is written: the
+// selected pairs' channels ascending, then the others ascending.
+constexpr int kPairRows = 64;
+constexpr int kPairStages = 4;
+constexpr int kPairThreads = 128;
+constexpr int kPairWaitPolls = 1 << 20;
+constexpr size_t kPairRing = static_cast<size_t>(kPairStages) * kPairRows * kD * 2;
+constexpr size_t kPairSmem = kPairRing + kPairStages * 8 + 16;
+
+__device__ __forceinline__ bool pair_wait(uint32_t mb, uint32_t parity, int polls) {
+  for (int i = 0; i < polls; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(mb), "r"(parity)
+        : "memory");
+    if (done) return true;
   }
-  return __fdiv_rn(acc, static_cast<float>(L));
+  return false;
 }
 
-// Eq. 6 for one (b, KV head): block = unit, thread = pair i.  sigma_i =
-// qbar_i * kbar_i (qbar: the mean over the GQA group's heads, in order, of
-// the heads' mean pair norms).  Then the n_high largest sigma (ties: lower
-// pair; a NaN counts as the smallest) are selected, and the unit's stored
-// channel order is written: the selected pairs' channels ascending, then
-// the others ascending.
-__global__ void __launch_bounds__(kD / 2) pnmix_pairs_kernel(
+__global__ void __launch_bounds__(kPairThreads) pnmix_pairs_kernel(
     const uint16_t* __restrict__ q, int Hq, int Lq, const uint16_t* __restrict__ k, int Lk,
     int Hkv, int layout, int n_high, float* sigma_out, uint8_t* perm, unsigned* status) {
   constexpr int P = kD / 2;
-  __shared__ float sig[P];
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* ring = reinterpret_cast<uint16_t*>(smem);   // [stage][row][D]
+  const uint32_t bar0 = static_cast<uint32_t>(__cvta_generic_to_shared(smem + kPairRing));
+  __shared__ float qbar_s[P], sig[P];
   __shared__ uint8_t high[kD];
-  const int u = blockIdx.x, i = threadIdx.x;
+  __shared__ int stop;
+  const int u = blockIdx.x, tid = threadIdx.x, i = tid & (P - 1);
   const int b = u / Hkv, kvh = u % Hkv, hg = Hq / Hkv;
   const int ca = layout == KVQ_PAIRS_ADJACENT ? 2 * i : i;
   const int cb = layout == KVQ_PAIRS_ADJACENT ? 2 * i + 1 : i + P;
-  bool bad = false;
-  float qsum = 0.0f;
-  for (int h = 0; h < hg; ++h) {
-    const uint16_t* qh = q + (static_cast<long long>(b) * Hq + kvh * hg + h) * Lq * kD;
-    qsum = __fadd_rn(qsum, mean_pair_norm(qh, Lq, ca, cb, bad));
+  const uint8_t* ku = reinterpret_cast<const uint8_t*>(k + static_cast<long long>(u) * Lk * kD);
+  const int nch = (Lk + kPairRows - 1) / kPairRows;
+  if (tid == 0) {
+    for (int st = 0; st < kPairStages; ++st)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(bar0 + 8 * st) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    stop = 0;
   }
-  const float qbar = __fdiv_rn(qsum, static_cast<float>(hg));
-  const float kbar = mean_pair_norm(k + static_cast<long long>(u) * Lk * kD, Lk, ca, cb, bad);
-  const float s = __fmul_rn(qbar, kbar);
-  sig[i] = s;
-  if (sigma_out) sigma_out[static_cast<long long>(u) * P + i] = s;
+  __syncthreads();
+  // chunk c (rows 64c ..) into stage c % kPairStages (thread 0)
+  auto issue = [&](int c) {
+    const uint32_t bytes = static_cast<uint32_t>(min(kPairRows, Lk - kPairRows * c) * kD * 2);
+    const uint32_t mb = bar0 + 8 * (c % kPairStages);
+    const uint32_t dst = static_cast<uint32_t>(
+        __cvta_generic_to_shared(ring + static_cast<size_t>(c % kPairStages) * kPairRows * kD));
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mb), "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+        ::"r"(dst), "l"(ku + static_cast<long long>(c) * kPairRows * kD * 2), "r"(bytes), "r"(mb)
+        : "memory");
+  };
+  int issued = 0;
+  if (tid == 0)
+    for (; issued < min(kPairStages, nch); ++issued) issue(issued);
+  bool bad = false;
+  if (tid < P) {
+    // key means: warps 0-1 stream the chunks (named barrier 1 between
+    // chunks; thread 0 refills the stage just consumed)
+    float kacc = 0.0f;
+    int c = 0;
+    for (; c < nch; ++c) {
+      const int st = c % kPairStages;
+      if (!pair_wait(bar0 + 8 * st, (c / kPairStages) & 1, kPairWaitPolls)) {
+        atomicOr(&stop, 1);
+      } else {
+        const uint16_t* rows = ring + static_cast<size_t>(st) * kPairRows * kD;
+        const int n = min(kPairRows, Lk - kPairRows * c);
+        // eight tokens' terms at a time (independent, straight-line for
+        // normal squared norms), then added in token order
+        for (int t0 = 0; t0 < n; t0 += 8) {
+          float ss[8], term[8];
+          bool sure = true;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int t = min(t0 + j, n - 1);
+            const float x = bfv(rows[t * kD + ca]);
+            const float y = bfv(rows[t * kD + cb]);
+            if (!isfinite(x) || !isfinite(y)) bad = true;
+            ss[j] = __fadd_rn(__fmul_rn(x, x), __fmul_rn(y, y));
+            bool ok;
+            term[j] = sqrt_rn_fast(ss[j], ok);
+            sure = sure && ok;
+          }
+          if (!sure) {   // a root near a midpoint, or a non-normal square (rare)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) term[j] = sqrt_rn(ss[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (t0 + j < n) kacc = __fadd_rn(kacc, term[j]);
+        }
+      }
+      asm volatile("bar.sync 1, %0;\n" ::"r"(P) : "memory");   // stage st consumed
+      if (stop) break;   // uniform over warps 0-1
+      if (tid == 0 && issued < nch) issue(issued++);
+    }
+    if (stop && tid == 0) {
+      // a wait gave up: every copy still in flight lands before the block
+      // leaves (full limit), and the selection is flagged invalid
+      atomicOr(status, static_cast<unsigned>(KVQ_FLAG_TIMEOUT));
+      for (int cc = c; cc < issued; ++cc)
+        pair_wait(bar0 + 8 * (cc % kPairStages), (cc / kPairStages) & 1, kPairWaitPolls);
+    }
+    sig[i] = __fdiv_rn(kacc, static_cast<float>(Lk));   // kbar, until the product below
+  } else {
+    // query means (short sequences), concurrently: eight tokens' loads at a
+    // time, then their terms in token order
+    float qsum = 0.0f;
+    for (int h = 0; h < hg; ++h) {
+      const uint16_t* qh = q + (static_cast<long long>(b) * Hq + kvh * hg + h) * Lq * kD;
+      float acc = 0.0f;
+      for (int t0 = 0; t0 < Lq; t0 += 8) {
+        float x[8], y[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const long long row = static_cast<long long>(min(t0 + j, Lq - 1)) * kD;
+          x[j] = bfv(qh[row + ca]);
+          y[j] = bfv(qh[row + cb]);
+        }
+        float term[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (t0 + j < Lq && (!isfinite(x[j]) || !isfinite(y[j]))) bad = true;
+          term[j] = sqrt_rn(__fadd_rn(__fmul_rn(x[j], x[j]), __fmul_rn(y[j], y[j])));
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (t0 + j < Lq) acc = __fadd_rn(acc, term[j]);
+      }
+      qsum = __fadd_rn(qsum, __fdiv_rn(acc, static_cast<float>(Lq)));
+    }
+    qbar_s[i] = __fdiv_rn(qsum, static_cast<float>(hg));
+  }
+  __syncthreads();
+  if (tid < P) {
+    const float s = __fmul_rn(qbar_s[i], sig[i]);
+    sig[i] = s;
+    if (sigma_out) sigma_out[static_cast<long long>(u) * P + i] = s;
+  }
   if (bad && status) atomicOr(status, static_cast<unsigned>(KVQ_FLAG_NONFINITE));
   __syncthreads();
-  int rank = 0;
-  for (int j = 0; j < P; ++j) {
-    const float sj = sig[j];
-    const bool before = s != s ? (sj == sj || j < i)                 // NaN: last
-                               : (sj > s || (sj == s && j < i));
-    rank += before ? 1 : 0;
+  if (tid < P) {
+    const float s = sig[i];
+    int rank = 0;
+    for (int j = 0; j < P; ++j) {
+      const float sj = sig[j];
+      const bool before = s != s ? (sj == sj || j < i)                 // NaN: last
+                                 : (sj > s || (sj == s && j < i));
+      rank += before ? 1 : 0;
+    }
+    const bool sel = rank < n_high;
+    high[ca] = sel;
+    high[cb] = sel;
   }
-  const bool sel = rank < n_high;
-  high[ca] = sel;
-  high[cb] = sel;
   __syncthreads();
-  // stored position of channels ca, cb: selected channels first, each part ascending
-  for (int c = i; c < kD; c += P) {
+  // stored position of every channel: selected channels first, each part ascending
+  for (int ch = tid; ch < kD; ch += kPairThreads) {
     int pos = 0;
     const int nh = 2 * n_high;
-    if (high[c]) {
-      for (int e = 0; e < c; ++e) pos += high[e];
+    if (high[ch]) {
+      for (int e = 0; e < ch; ++e) pos += high[e];
     } else {
       pos = nh;
-      for (int e = 0; e < c; ++e) pos += !high[e];
+      for (int e = 0; e < ch; ++e) pos += !high[e];
     }
-    perm[static_cast<long long>(u) * kD + pos] = static_cast<uint8_t>(c);
+    perm[static_cast<long long>(u) * kD + pos] = static_cast<uint8_t>(ch);
   }
 }
 
@@ -119,10 +236,12 @@ __global__ void pnmix_high_kernel(const uint8_t* __restrict__ perm, int nh, uint
 cudaError_t launch_pnmix_pairs(const kvq_cache* c, const kvq_bf16* q, int Hq, int Lq,
                                const kvq_bf16* k, int Lk, float* sigma, cudaStream_t s) {
   const int units = c->cfg.batch * c->cfg.kv_heads;
-  pnmix_pairs_kernel<<<units, kD / 2, 0, s>>>(reinterpret_cast<const uint16_t*>(q), Hq, Lq,
-                                              reinterpret_cast<const uint16_t*>(k), Lk,
-                                              c->cfg.kv_heads, c->cfg.pair_layout,
-                                              c->cfg.n_high_pairs, sigma, c->pn_perm, c->status);
+  static SmemOptIn opt_in;
+  cudaError_t e = opt_in.ensure(pnmix_pairs_kernel);
+  if (e != cudaSuccess) return e;
+  pnmix_pairs_kernel<<<units, kPairThreads, kPairSmem, s>>>(
+      reinterpret_cast<const uint16_t*>(q), Hq, Lq, reinterpret_cast<const uint16_t*>(k), Lk,
+      c->cfg.kv_heads, c->cfg.pair_layout, c->cfg.n_high_pairs, sigma, c->pn_perm, c->status);
   return cudaGetLastError();
 }
 

@@ -410,9 +410,10 @@ int kvq_export_k_mixed(const kvq_cache* cache, uint8_t* counts, uint8_t* perm, k
  * fp32 rounded (sums in token order, then head order).  The n_high_pairs
  * largest sigma (ties: lower pair) become the 3-bit pairs; the cache keeps
  * the selection for every later flush.  sigma (fp32 [B][Hkv][D/2], device)
- * may be NULL.
- * Errors: ARG, SHAPE, MODE (not a PN-Mix cache), NOT_EMPTY (the cache holds
- * tokens), CUDA.  Flags: NONFINITE.
+ * may be NULL.  k must be 16-byte aligned (its rows are copied in bulk).
+ * Errors: ARG (also an unaligned k), SHAPE, MODE (not a PN-Mix cache),
+ * NOT_EMPTY (the cache holds tokens), CUDA.  Flags: NONFINITE, TIMEOUT (a
+ * bounded wait for a staged key chunk gave up: the selection is invalid).
  */
 int kvq_pnmix_pairs(kvq_cache* cache, const kvq_bf16* q, int Hq, int Lq,
                     const kvq_bf16* k, int Lk, float* sigma, cudaStream_t s);
