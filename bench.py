@@ -51,13 +51,13 @@ ATTN_REPS = 50                     # per-call timed decode attention calls (roof
 # launch, from the ncu capture of this workload at batch 8 kept under
 # profiles/, keyed by the hash of the decode kernel's code it was taken on
 # (a stale entry reports null).  The capture ran at batch 8 (64 units,
-# 32768 + 100 tokens, the token append fused): 200.988 MB read + 4.122 MB
-# written against 200.638 MB of algorithmic attention bytes (ratio 1.0223:
+# 32768 + 100 tokens, the token append fused): 200.986 MB read + 4.005 MB
+# written against 200.638 MB of algorithmic attention bytes (ratio 1.0217:
 # mostly the split-K partials written).  Traffic per unit is independent of
 # the batch, so the batch-16 launch is that ratio times its algorithmic
 # bytes at the timed steps' mean context.
 NCU_TRAFFIC = {
-    "a90e9160ac0c200e": {("llama8b_gqa_32k_b16", 16, 32768, 2): 205.110016 / 200.638464 * 401.375232e6},
+    "3d7fbff943adb191": {("llama8b_gqa_32k_b16", 16, 32768, 2): 204.991232 / 200.638464 * 401.375232e6},
 }
 
 
@@ -160,7 +160,7 @@ def kernel_source_hash():
     space dropped, so the key follows the code, not its comments."""
     import re
     h = hashlib.sha256()
-    for name in ("decode_mma.cuh", "decode_mma.cu", "frag_layout.h", "kvq_internal.h"):
+    for name in ("decode_mma.cuh", "decode_mma.cu", "frag_layout.h", "kvq_internal.h", "mma_util.h"):
         with open(os.path.join(ROOT, "bit_kv_cache_kvq_gb300", "csrc", name)) as f:
             for line in f:
                 code = re.sub(r"//.*", "", line).strip()

@@ -102,7 +102,7 @@ constexpr float kInvCodeUnit = 1.0f / 512.0f;
 // value tables are built in place over the staged value steps and origins
 // they are computed from (3072 bytes, read into registers first).
 constexpr int kVsbBytes = 256 * 4;
-constexpr int kVmbBytes = 4 * 72 * 4 + 64 * 4;   // 4 origin rows, then a zero row
+constexpr int kVmbBytes = 4 * 72 * 4;   // 4 origin rows
 constexpr int kQRow = 136;
 constexpr int kQBytes = 8 * kQRow * 2;   // = 4 * kQRow * 4
 static_assert(kVsbBytes + kVmbBytes <= 4 * kKG * kVGroups + 2 * kKG * kVGroups,
@@ -139,8 +139,6 @@ __device__ __forceinline__ int vsb_index(int kt, int t, int j, int slot) {
 __device__ __forceinline__ int vmb_index(int kt, int j, int t, int slot) {
   return j * 72 + kt * 8 + t * 2 + slot;
 }
-// 64 zero words after the four origin rows (index kt * 8 + t * 2 + slot)
-constexpr int kZeroRow = 4 * 72;
 
 // --- code unpacking: word x and y = x >> 8 -> A fragment registers
 // (frag_layout.h).  Each register is one AND; its halves are f16 subnormals.
@@ -1060,8 +1058,6 @@ struct Warp {
       vmb[vmb_index(kt, j, t0, chi)] = pack_h2(vmn[0][j] * svm, vmn[1][j] * svm);
       vmb[vmb_index(kt, j, t0 + 1, chi)] = pack_h2(vmn[2][j] * svm, vmn[3][j] * svm);
     }
-    // the zero row the origin MMA's rows 4..7 read
-    reinterpret_cast<uint2*>(vmb + kZeroRow)[lane] = make_uint2(0u, 0u);
   }
 
   // Channel tile mc (16 channels) of one group's P·V with B fragments bj,
@@ -1138,9 +1134,9 @@ struct Warp {
         pb[kt][0] = movmatrix_t(pack_h2(S[kt][0], S[kt][1]));
         pb[kt][1] = movmatrix_t(pack_h2(S[kt][2], S[kt][3]));
       }
-      // lanes g >= 4 (A rows 4..7) read the zero row
-      const uint2 av = *reinterpret_cast<const uint2*>(vmb + (g < 4 ? vmb_index(0, g, t, 0) : kZeroRow + 2 * t) + 8 * kt);
-      const uint32_t a0 = av.x, a2 = av.y;
+      // lanes g >= 4 (A rows 4..7) take zeros
+      const uint2 av = *reinterpret_cast<const uint2*>(vmb + vmb_index(kt, g & 3, t, 0));
+      const uint32_t a0 = g < 4 ? av.x : 0u, a2 = g < 4 ? av.y : 0u;
       mma_f16(Dvm, a0, 0u, a2, 0u, pb[kt][0], pb[kt][1]);
     }
     const uint8_t* vc = vbuf + (L.v_codes - L.kpart);
@@ -1538,13 +1534,14 @@ __global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX || KIVI || PNMIX) 
       W.issue_v(u, g0);
     }
     W.begin_unit(u);
+    bool gave_up = false;
     if (g0 < g1) {
       for (int gi = g0; gi < g1; ++gi) {
         const bool more = gi + 1 < g1;
         if (!W.wait_part(W.mb_k, W.ph_k)) {   // keys of gi (bounded wait)
           W.wait_part(W.mb_v, W.ph_v);        // the value copy in flight
-          abandon(u);
-          return;
+          gave_up = true;
+          break;
         }
         float S[8][4], hinv[2], hbias[2], alpha[2], svn, inv_svm;
         W.scores(S, hinv, hbias);
@@ -1552,8 +1549,8 @@ __global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX || KIVI || PNMIX) 
         if (more) W.issue_k(u, gi + 1);
         if (!W.wait_part(W.mb_v, W.ph_v)) {   // values of gi
           if (more) W.wait_part(W.mb_k, W.ph_k);
-          abandon(u);
-          return;
+          gave_up = true;
+          break;
         }
         // the value tables' shared-memory round trip overlaps the softmax
         W.value_tables(svn, inv_svm);
@@ -1565,6 +1562,11 @@ __global__ void __launch_bounds__(max_warps(KB, VB, NREP, MIX || KIVI || PNMIX) 
         // value FIFO (ring slots r..127); its codes there are zero
         if (KIVI && gi == a.n_groups - 1) W.ring_values(u, S, a.r);
       }
+    }
+    // out of the group loop, so the loop keeps no state for it
+    if (gave_up) {
+      abandon(u);
+      return;
     }
     if (res) {
       if (a.new_k != nullptr) W.put_token(u, a.r - 1);

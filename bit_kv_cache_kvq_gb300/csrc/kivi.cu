@@ -62,6 +62,29 @@ __device__ __forceinline__ uint32_t kivi_code(float x, const KiviGroup& p, int t
   return static_cast<uint32_t>(fminf(fmaxf(rintf(y), 0.0f), static_cast<float>(top)));
 }
 
+// The same code without a division for most elements.  With rcp =
+// RN(1/step), z = RN(diff * rcp) lies within 2.5 fp32 ulps of the IEEE
+// quotient RN(diff / step), so both round to the same bf16 value unless a
+// bf16 rounding boundary (an fp32 value whose low 16 bits are 0x8000) lies
+// within 3 ulps of z; those elements, and groups whose step is below
+// 2^-100 (rcp could overflow), take the quotient.
+struct KiviFast {
+  float rcp;
+  bool exact;   // every element by the quotient (a constant, flagged or tiny-step group too)
+};
+__device__ __forceinline__ KiviFast kivi_fast(const KiviGroup& p) {
+  return {p.step > 0.0f ? __frcp_rn(p.step) : 0.0f, !(p.step >= 0x1p-100f) || p.flags != 0u};
+}
+__device__ __forceinline__ uint32_t kivi_code_fast(float x, const KiviGroup& p, const KiviFast& f,
+                                                   int top) {
+  if (f.exact) return kivi_code(x, p, top);
+  const float diff = bfr(__fsub_rn(x, p.m));
+  const float z = __fmul_rn(diff, f.rcp);
+  const uint32_t lo = __float_as_uint(z) & 0xFFFFu;
+  const float y = lo - (0x8000u - 3u) <= 6u ? bfr(__fdiv_rn(diff, p.step)) : bfr(z);
+  return static_cast<uint32_t>(fminf(fmaxf(rintf(y), 0.0f), static_cast<float>(top)));
+}
+
 // 128 bf16 rows of D channels into shared memory (row t at t * D), rows
 // [0, n) from src + t * D; 16-byte copies.
 __device__ __forceinline__ void stage_rows(const kvq_bf16* src, int n, uint16_t* s) {
@@ -119,8 +142,9 @@ __global__ void __launch_bounds__(256) kivi_seal_keys_kernel(KiviArgs a) {
     flags |= p.flags;
     kst[sg * kD + d] = bf_bits(p.step);
     kmn[sg * kD + d] = nf ? 0 : bf_bits(p.m);
+    const KiviFast f = kivi_fast(p);
     for (int t = kSub * sg; t < kSub * sg + kSub; ++t)
-      cB[t * kD + d] = static_cast<uint8_t>(kivi_code(bf(sK[t * kD + d]), p, top));
+      cB[t * kD + d] = static_cast<uint8_t>(kivi_code_fast(bf(sK[t * kD + d]), p, f, top));
   }
   // value part of the record: empty until tokens leave the FIFO
   uint4* vz = reinterpret_cast<uint4*>(rec + L.v_codes);
@@ -179,8 +203,9 @@ __global__ void __launch_bounds__(256) kivi_values_kernel(KiviArgs a) {
     flags |= p.flags;
     vst[t * kVGroups + j] = bf_bits(p.step);
     vmn[t * kVGroups + j] = nf ? 0 : bf_bits(p.m);
+    const KiviFast f = kivi_fast(p);
     for (int c = 0; c < kSub; ++c)
-      cB[t * kD + kSub * j + c] = static_cast<uint8_t>(kivi_code(bf(row[c]), p, top));
+      cB[t * kD + kSub * j + c] = static_cast<uint8_t>(kivi_code_fast(bf(row[c]), p, f, top));
   }
   __syncthreads();
   uint32_t* dst = reinterpret_cast<uint32_t*>(rec + L.v_codes);
