@@ -80,8 +80,7 @@ int kivi_prefill(kvq_cache* c, const kvq_bf16* k, const kvq_bf16* v, int L, cuda
   if (L == 0) return KVQ_OK;
   const int units = c->cfg.batch * c->cfg.kv_heads;
   const QuantSrc src{k, v, static_cast<long long>(L) * kD, static_cast<long long>(kKG) * kD};
-  cudaError_t e = launch_kivi_seal(c, src, n_rec, 0, s);
-  if (e == cudaSuccess && L > kKG) e = launch_kivi_values(c, src, n_rec, 0, 0, kKG, L - kKG, s);
+  cudaError_t e = launch_kivi_prefill(c, src, n_rec, L - kKG, s);
   if (e == cudaSuccess) e = copy_rows(k, L, n_rec * kKG, r, c->res_k, kR, 0, units, s);
   if (e == cudaSuccess && n_rec > 0)   // tokens L - 128 .. 128 n_rec - 1 -> slots r .. 127
     e = copy_rows(v, L, L - kKG, kKG - r, c->res_v, kR, r, units, s);

@@ -258,6 +258,10 @@ cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
 // group_stride + t * D), limited to the first n_valid tokens of the history.
 cudaError_t launch_kivi_seal(const kvq_cache* c, QuantSrc src, int n_records, int first_record,
                              cudaStream_t s);
+// KIVI prefill: records 0 .. n_records - 1 sealed and the values of tokens
+// [0, n_valid) quantized, in one launch (quant.cu).
+cudaError_t launch_kivi_prefill(const kvq_cache* c, QuantSrc src, int n_records, int n_valid,
+                                cudaStream_t s);
 cudaError_t launch_kivi_values(const kvq_cache* c, QuantSrc src, int n_records, int first_record,
                                int t0, int t1, int n_valid, cudaStream_t s);
 // Canonical KIVI export of records [u][0 .. t_q/128): key codes [u][n*4][D]

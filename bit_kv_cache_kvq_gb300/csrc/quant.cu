@@ -7,10 +7,12 @@
 // with IEEE fp32 subtraction and division (__fsub_rn / __fdiv_rn), codes
 // rounded half-to-even, and a constant group (M == m) stored as step 0,
 // codes 0, origin m.  Groups: Key per channel over the 128 tokens of a tile,
-// Value per token over 32 consecutive channels (KIVI §3).  Codes are first
-// staged as bytes in shared memory and then packed word by word into the
-// tensor-core fragment order of frag_layout.h; kvq_export_* converts back to
-// the canonical LSB-first layout.
+// Value per token over 32 consecutive channels (KIVI §3).  The uniform and
+// KIVI-prefill passes build whole words of the tensor-core fragment order
+// of frag_layout.h in registers; the mixed and PN-Mix passes stage codes as
+// bytes and pack them word by word; kvq_export_* converts back to the
+// canonical LSB-first layout.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "frag_layout.h"
@@ -64,6 +66,7 @@ struct QuantArgs {
   float q_count;            // (query heads per KV head) * (steps observed)
   float tau_bf16, tau_uint4;  // threshold tiers (lay.thresh)
   const uint8_t* perm;      // PN-Mix: [units][D] stored position -> channel
+  int kivi_valid;           // KIVI prefill: value tokens quantized, from the first record on
   unsigned* status;
 };
 
@@ -185,6 +188,50 @@ struct GroupQ {
   float nm, rcp;
 };
 
+// ---- KIVI streaming variant ("KIVI: KV cache axes" §7): origin and step in
+// bf16, computed in bf16 (every operation an fp32 operation rounded to
+// bf16), code = clip(RNE(bf16(bf16(x - m) / step)), 0, top).
+__device__ __forceinline__ float bfr(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+struct KiviGroupP {
+  float m, step;
+  unsigned flags;
+};
+__device__ __forceinline__ KiviGroupP kivi_group(float lo, float hi, bool nonfinite, int top) {
+  KiviGroupP p{lo, 0.0f, nonfinite ? static_cast<unsigned>(KVQ_FLAG_NONFINITE) : 0u};
+  if (nonfinite || hi == lo) return p;
+  const float step = bfr(__fdiv_rn(bfr(__fsub_rn(hi, lo)), static_cast<float>(top)));
+  if (!(step > 0.0f) || !isfinite(step)) p.flags |= KVQ_FLAG_RANGE;
+  p.step = step;
+  return p;
+}
+// The (-m, rcp) pair the code pass uses: rcp = RN(1/step); 0 for a constant
+// or flagged group (every code 0: with -m = 0 the product is 0, or NaN for a
+// non-finite x, which the clip sends to 0); -1 for a step below 2^-100, which
+// sends every element of the group to the exact quotient.
+__device__ __forceinline__ GroupQ kivi_q(const KiviGroupP& p) {
+  if (p.flags || p.step == 0.0f) return {0.0f, 0.0f};
+  return {-p.m, p.step < 0x1p-100f ? -1.0f : __frcp_rn(p.step)};
+}
+// The code of d32 = fl32(x - m) in code_bits' position.  diff = bf16(d32);
+// z = RN(diff * rcp) lies within 2.5 fp32 ulps of RN(diff / step), so both
+// round to the same bf16 value unless a bf16 rounding boundary (an fp32 value
+// whose low 16 bits are 0x8000) lies within 3 ulps of z; such elements (and
+// tiny-step groups) take the IEEE quotient, with the step read back from the
+// record (bf16).
+template <int BITS>
+__device__ __forceinline__ uint32_t kivi_bits(float d32, float rcp, const uint16_t* step_bf16) {
+  constexpr int top = (1 << BITS) - 1;
+  const float diff = bfr(d32);
+  const float z = __fmul_rn(diff, rcp);
+  float y;
+  if ((__float_as_uint(z) & 0xFFFFu) - 0x7FFDu <= 6u || rcp < 0.0f)   // rare
+    y = bfr(__fdiv_rn(diff, bf2f(*step_bf16)));
+  else
+    y = bfr(z);
+  return static_cast<uint32_t>(fminf(fmaxf(rintf(y), 0.0f), static_cast<float>(top))) << 18;
+}
+
+
 // A tile takes the exact path everywhere when a group is non-finite or has
 // a step in (0, 2^-100) (the near-element bounds would underflow).
 constexpr float kTinyStep = 7.888609052210118e-31f;   // 2^-100
@@ -294,19 +341,23 @@ __device__ __noinline__ void key_codes_slow(const uint16_t* sK, const GroupQ* kq
   }
 }
 
-template <int KB>
+// KIVI (f1): the channel parameters are per 32-token sub-group ([4][128]),
+// the steps bf16 ([4][128]); a thread's tokens all lie in sub-group mt / 2.
+template <int KB, bool KIVI = false>
 __device__ __forceinline__ void key_codes(const uint16_t* sK, const GroupQ* kq,
-                                          const float* kstep, bool exact_tile, uint32_t* dst) {
+                                          const void* steps, bool exact_tile, uint32_t* dst) {
   constexpr int NW = KB == 2 ? 4 : 8;
   constexpr int top = (1 << KB) - 1;
-  if (exact_tile) {   // block-uniform, rare
+  const float* kstep = static_cast<const float*>(steps);
+  if (!KIVI && exact_tile) {   // block-uniform, rare
     key_codes_slow<KB>(sK, kq, kstep, dst);
     return;
   }
   const int tid = threadIdx.x;
   const int g = tid & 7, w = (tid >> 3) & 3, mt = tid >> 5;
   const uint4* rows = reinterpret_cast<const uint4*>(sK);
-  const float4* kq4 = reinterpret_cast<const float4*>(kq);
+  const float4* kq4 = reinterpret_cast<const float4*>(kq) + (KIVI ? (mt >> 1) * (kD / 2) : 0);
+  const uint16_t* kst = static_cast<const uint16_t*>(steps) + (KIVI ? (mt >> 1) * kD : 0);
   uint32_t acc[NW];
 #pragma unroll
   for (int i = 0; i < NW; ++i) acc[i] = 0u;
@@ -331,8 +382,13 @@ __device__ __forceinline__ void key_codes(const uint16_t* sK, const GroupQ* kq,
           for (int half = 0; half < 2; ++half) {
             const int e = 2 * t + half;
             const float d = half ? sub_hi(xw[t], nm[e]) : sub_lo(xw[t], nm[e]);
-            uint32_t v = code_bits(d, rc[e]);
-            if (is_near(v)) v = near_bits(v, d, kstep[8 * p + e], top);   // rare
+            uint32_t v;
+            if constexpr (KIVI) {
+              v = kivi_bits<KB>(d, rc[e], kst + 8 * p + e);
+            } else {
+              v = code_bits(d, rc[e]);
+              if (is_near(v)) v = near_bits(v, d, kstep[8 * p + e], top);   // rare
+            }
             if (KB == 2) acc[t] |= place<2>(v, 2 * (4 * rhi + 2 * kl + chi) + 16 * half);
             else acc[2 * t + kl] |= place<4>(v, 4 * (2 * rhi + chi) + 16 * half);
           }
@@ -420,12 +476,14 @@ __device__ __noinline__ void value_codes_slow(const uint16_t* sV, const GroupQ* 
   }
 }
 
-template <int VB>
+template <int VB, bool KIVI = false>
 __device__ __forceinline__ void value_codes(const uint16_t* sV, const GroupQ* vq,
-                                            const float* vstep, bool exact_tile, uint32_t* dst) {
+                                            const void* steps, bool exact_tile, uint32_t* dst) {
+  const float* vstep = static_cast<const float*>(steps);
+  const uint16_t* vst = static_cast<const uint16_t*>(steps);   // KIVI: bf16 [128][4]
   constexpr int top = (1 << VB) - 1;
   constexpr int NW = VB == 2 ? 8 : 16;   // words before the pair merge: (w, i) or (kt, i)
-  if (exact_tile) {   // block-uniform, rare
+  if (!KIVI && exact_tile) {   // block-uniform, rare
     value_codes_slow<VB>(sV, vq, vstep, dst);
     return;
   }
@@ -453,8 +511,13 @@ __device__ __forceinline__ void value_codes(const uint16_t* sV, const GroupQ* vq
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float d = (i & 1) ? sub_hi(xw[i >> 1], q.nm) : sub_lo(xw[i >> 1], q.nm);
-            uint32_t v = code_bits(d, q.rcp);
-            if (is_near(v)) v = near_bits(v, d, vstep[tok * kVGroups + j], top);   // rare
+            uint32_t v;
+            if constexpr (KIVI) {
+              v = kivi_bits<VB>(d, q.rcp, vst + tok * kVGroups + j);
+            } else {
+              v = code_bits(d, q.rcp);
+              if (is_near(v)) v = near_bits(v, d, vstep[tok * kVGroups + j], top);   // rare
+            }
             if (VB == 2) acc[4 * wl + i] |= place<2>(v, 2 * (4 * rhi + 2 * kl + chi) + 16 * half);
             else acc[8 * wl + 4 * kl + i] |= place<4>(v, 4 * (2 * rhi + chi) + 16 * half);
           }
@@ -544,6 +607,122 @@ __global__ void __launch_bounds__(256, 5) quantize_uniform_kernel(QuantArgs a) {
   }
   exact_tile = __syncthreads_or(exact_tile);
   key_codes<KB>(sT, kq, kstep, exact_tile, reinterpret_cast<uint32_t*>(rec + a.lay.k_codes));
+  if (flags) atomicOr(a.status, flags);
+}
+
+// ---- KIVI streaming variant, prefill (f1; "KIVI: KV cache axes" §4–§7).
+// The records of a prefill in one launch: block (record, unit, z).  z = 0
+// seals the record's 128 keys: per channel four 32-token groups (origin and
+// step bf16, [4][D]), codes in the key fragment order.  z = 1 quantizes the
+// values of the record's tokens that have left the FIFO (kivi_valid counts
+// them from the launch's first record on): per token four 32-channel groups
+// (bf16 [128][4]); the other tokens' codes and metadata are written zero.
+// Ranges are bf16x2 min / max (NaN-propagating) with -0 below +0 (the
+// oracle's order); a non-finite group keeps step 0, origin 0 and zero codes,
+// flagged.
+template <int B>
+__global__ void __launch_bounds__(256, 5) quantize_kivi_kernel(QuantArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  constexpr int top = (1 << B) - 1;
+  constexpr int kSub = 32, kSubs = kKG / kSub;
+  uint8_t* rec = group_record(a);
+  const RecLayout& L = a.lay;
+  uint16_t* sT = reinterpret_cast<uint16_t*>(smem);
+  GroupQ* q = reinterpret_cast<GroupQ*>(smem + kTileBytes);   // 512 groups
+  unsigned flags = 0;
+  if (blockIdx.z == 0) {
+    load_tile(a, a.src.k, sT);
+    __syncthreads();
+    uint16_t* kst = reinterpret_cast<uint16_t*>(rec + L.k_scale);
+    uint16_t* kmn = reinterpret_cast<uint16_t*>(rec + L.k_min);
+    {
+      // thread = (sub-group sg, channel pair 2c, 2c + 1): bf16x2 min / max
+      // (NaN-propagating) over the sub-group's 32 rows, one word a row
+      const int sg = threadIdx.x >> 6, c = threadIdx.x & 63;
+      const uint32_t* rows = reinterpret_cast<const uint32_t*>(sT);
+      uint32_t mn = 0u, mx = 0u;
+      for (int t = kSub * sg; t < kSub * sg + kSub; ++t) {
+        const uint32_t w = rows[swz(t, 2 * c) >> 1];
+        mn = t == kSub * sg ? w : bmin2(mn, w);
+        mx = t == kSub * sg ? w : bmax2(mx, w);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int d = 2 * c + h, gi = sg * kD + d;
+        uint32_t lb = (mn >> (16 * h)) & 0xFFFFu;
+        const uint32_t hb = (mx >> (16 * h)) & 0xFFFFu;
+        const bool nf = nonfinite_bits(lb) || nonfinite_bits(hb);
+        if (!nf && (lb & 0x7FFFu) == 0u) {   // a zero minimum: -0 iff the group holds one
+          lb = 0u;
+          for (int t = kSub * sg; t < kSub * sg + kSub; ++t)
+            if (sT[swz(t, d)] == 0x8000u) lb = 0x8000u;
+        }
+        const KiviGroupP p = kivi_group(bf2f(static_cast<uint16_t>(lb)),
+                                        bf2f(static_cast<uint16_t>(hb)), nf, top);
+        flags |= p.flags;
+        kst[gi] = f2bf_bits(p.step);
+        kmn[gi] = nf ? 0 : f2bf_bits(p.m);
+        q[gi] = kivi_q(p);
+      }
+    }
+    __syncthreads();   // the steps reach the record before the code pass reads them back
+    key_codes<B, true>(sT, q, kst, false, reinterpret_cast<uint32_t*>(rec + L.k_codes));
+  } else {
+    const int nv = min(kKG, a.kivi_valid - kKG * static_cast<int>(blockIdx.x));
+    uint16_t* vst = reinterpret_cast<uint16_t*>(rec + L.v_scale);
+    uint16_t* vmn = reinterpret_cast<uint16_t*>(rec + L.v_min);
+    if (nv <= 0) {   // every value of the record is still in the FIFO: an empty value part
+      uint4* z = reinterpret_cast<uint4*>(rec + L.v_codes);
+      for (int i = threadIdx.x; i < (static_cast<int>(a.rec_bytes) - L.v_codes) / 16; i += blockDim.x)
+        z[i] = make_uint4(0u, 0u, 0u, 0u);
+      return;
+    }
+    load_tile(a, a.src.v, sT);
+    __syncthreads();
+    {
+      // thread = (token t, groups j = 2h, 2h + 1; h = 1 in the order 3, 2):
+      // bf16x2 min / max over the group's four 16-byte pieces
+      const int t = threadIdx.x >> 1, h = threadIdx.x & 1;
+      const uint4* row = reinterpret_cast<const uint4*>(sT + t * kD);
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = h ? 3 - jj : jj, gi = t * kVGroups + j;
+        if (t >= nv) {   // still in the FIFO
+          vst[gi] = 0;
+          vmn[gi] = 0;
+          q[gi] = {0.0f, 0.0f};
+          continue;
+        }
+        uint32_t mn = 0u, mx = 0u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 w = row[(4 * j + k) ^ (t & 7)];
+          const uint32_t lo2 = bmin2(bmin2(w.x, w.y), bmin2(w.z, w.w));
+          const uint32_t hi2 = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+          mn = k ? bmin2(mn, lo2) : lo2;
+          mx = k ? bmax2(mx, hi2) : hi2;
+        }
+        mn = bmin2(mn, swap_halves(mn));
+        mx = bmax2(mx, swap_halves(mx));
+        uint32_t lb = mn & 0xFFFFu;
+        const uint32_t hb = mx & 0xFFFFu;
+        const bool nf = nonfinite_bits(lb) || nonfinite_bits(hb);
+        if (!nf && (lb & 0x7FFFu) == 0u) {   // a zero minimum: -0 iff the group holds one
+          lb = 0u;
+          for (int cc = kSub * j; cc < kSub * j + kSub; ++cc)
+            if (sT[swz(t, cc)] == 0x8000u) lb = 0x8000u;
+        }
+        const KiviGroupP p = kivi_group(bf2f(static_cast<uint16_t>(lb)),
+                                        bf2f(static_cast<uint16_t>(hb)), nf, top);
+        flags |= p.flags;
+        vst[gi] = f2bf_bits(p.step);
+        vmn[gi] = nf ? 0 : f2bf_bits(p.m);
+        q[gi] = kivi_q(p);
+      }
+    }
+    __syncthreads();
+    value_codes<B, true>(sT, q, vst, false, reinterpret_cast<uint32_t*>(rec + L.v_codes));
+  }
   if (flags) atomicOr(a.status, flags);
 }
 
@@ -968,6 +1147,32 @@ cudaError_t launch_quantize(const kvq_cache* c, QuantSrc src, int n_groups,
     KVQ_LAUNCH((quantize_uniform_kernel<4, 4>), kQuantSmem);
   }
 #undef KVQ_LAUNCH
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kivi_prefill(const kvq_cache* c, QuantSrc src, int n_records, int n_valid,
+                                cudaStream_t s) {
+  if (n_records == 0) return cudaSuccess;
+  QuantArgs a = {};
+  a.src = src;
+  a.records = c->records;
+  a.rec_bytes = c->lay.bytes;
+  a.max_groups = c->max_groups;
+  a.first_group = 0;
+  a.lay = c->lay;
+  a.kivi_valid = n_valid;
+  a.status = c->status;
+  const dim3 grid(n_records, c->cfg.batch * c->cfg.kv_heads, 2);   // z: keys, values
+  cudaError_t e;
+  if (c->cfg.k_bits == 2) {
+    static SmemOptIn opt_in;
+    if ((e = opt_in.ensure(quantize_kivi_kernel<2>)) != cudaSuccess) return e;
+    quantize_kivi_kernel<2><<<grid, 256, kQuantSmem, s>>>(a);
+  } else {
+    static SmemOptIn opt_in;
+    if ((e = opt_in.ensure(quantize_kivi_kernel<4>)) != cudaSuccess) return e;
+    quantize_kivi_kernel<4><<<grid, 256, kQuantSmem, s>>>(a);
+  }
   return cudaGetLastError();
 }
 
