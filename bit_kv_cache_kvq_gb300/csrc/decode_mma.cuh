@@ -118,11 +118,8 @@ static_assert(warp_extra(false) % 128 == 0 && warp_extra(true) % 128 == 0,
 // Warps per block.  Two-bit uniform records with at most 4 query heads per
 // KV head fit 16 warps (4 per scheduler, up to 128 registers a thread) in
 // shared memory; the other variants run 12 (up to 168 registers).
-#ifndef KVQ_UNIFORM_WARPS
-#define KVQ_UNIFORM_WARPS 16
-#endif
 __host__ __device__ constexpr int max_warps(int kb, int vb, int nrep, bool mix) {
-  return (!mix && kb == 2 && vb == 2 && nrep <= 4) ? KVQ_UNIFORM_WARPS : 12;
+  return (!mix && kb == 2 && vb == 2 && nrep <= 4) ? 16 : 12;
 }
 
 // Swizzled positions in the per-warp value tables (u32 index), chosen so
