@@ -57,7 +57,7 @@ ATTN_REPS = 50                     # per-call timed decode attention calls (roof
 # the batch, so the batch-16 launch is that ratio times its algorithmic
 # bytes at the timed steps' mean context.
 NCU_TRAFFIC = {
-    "3d7fbff943adb191": {("llama8b_gqa_32k_b16", 16, 32768, 2): 204.991232 / 200.638464 * 401.375232e6},
+    "d3a5bdac2efb0df3": {("llama8b_gqa_32k_b16", 16, 32768, 2): 204.991232 / 200.638464 * 401.375232e6},
 }
 
 
