@@ -743,6 +743,10 @@ __global__ void __launch_bounds__(256) quantize_pnmix_kernel(QuantArgs a) {
   }
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem);
   uint8_t* cB = smem + kTileBytes;   // codes [128 tokens][128 positions]
+  // per stored position: channel, offset, scale, RN(1/scale); mode 0 = all
+  // codes 0, 1 = fast decision, 2 = IEEE quotient for every element
+  __shared__ float s_off[kD], s_sc[kD], s_rcp[kD];
+  __shared__ uint8_t s_ch[kD], s_mode[kD];
   load_tile(a, a.src.k, sK);
   __syncthreads();
   uint8_t* rec = group_record(a);
@@ -773,40 +777,84 @@ __global__ void __launch_bounds__(256) quantize_pnmix_kernel(QuantArgs a) {
     }
     reinterpret_cast<float*>(rec + L.k_scale)[p] = sc;
     reinterpret_cast<float*>(rec + L.k_min)[p] = off;
-    const float top = p < L.nh ? 7.0f : 1.0f;
-    for (int t = 0; t < kKG; ++t) {
+    s_ch[p] = static_cast<uint8_t>(ch);
+    s_off[p] = off;
+    s_sc[p] = sc;
+    s_rcp[p] = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+    s_mode[p] = (bad || !(sc > 0.0f)) ? 0 : (sc < kTinyStep || !isfinite(sc) || !isfinite(off)) ? 2 : 1;
+  }
+  __syncthreads();
+  // Codes, two threads a position (64 tokens each).  High positions (Eq. 2,
+  // 3 bits): the uniform quantizer's decision (code_bits, and near_bits
+  // near a rounding boundary), RNE(RN(d / s)) bit for bit.  Low positions
+  // (Eq. 7): clip(RNE(RN(d / s)), 0, 1) is 1 iff RN(d / s) > 1/2, i.e. iff
+  // d - s/2 > s 2^-25; the remainder by one FMA is exact wherever the
+  // comparison is close (Sterbenz: d within [s/4, s]), and far from it the
+  // rounding cannot change its sign or its side of s 2^-25.
+  {
+    const int p = threadIdx.x & (kD - 1), t0 = (threadIdx.x >> 7) * (kKG / 2);
+    const int ch = s_ch[p], mode = s_mode[p];
+    const float off = s_off[p], sc = s_sc[p], rcp = s_rcp[p];
+    const bool hi3 = p < L.nh;
+    for (int t = t0; t < t0 + kKG / 2; ++t) {
       uint32_t c = 0;
-      if (!bad && sc > 0.0f) {
-        const float y = __fdiv_rn(__fsub_rn(bf2f(sK[swz(t, ch)]), off), sc);
-        c = static_cast<uint32_t>(fminf(fmaxf(rintf(y), 0.0f), top));
+      const float x = bf2f(sK[swz(t, ch)]);
+      if (mode == 1) {
+        const float d = __fsub_rn(x, off);
+        if (hi3) {
+          uint32_t v = code_bits(d, rcp);
+          if (is_near(v)) v = near_bits(v, d, sc, 7u);   // rare
+          c = (v >> 18) & 7u;
+        } else {
+          c = __fmaf_rn(-0.5f, sc, d) > sc * 0x1p-25f ? 1u : 0u;
+        }
+      } else if (mode == 2) {   // rare: the IEEE quotient
+        const float y = __fdiv_rn(__fsub_rn(x, off), sc);
+        c = static_cast<uint32_t>(fminf(fmaxf(rintf(y), 0.0f), hi3 ? 7.0f : 1.0f));
       }
       cB[t * kD + p] = static_cast<uint8_t>(c);
     }
   }
   __syncthreads();
   // LSB plane: word (mt*2 + ks/4)*32 + lane, bit 2*(ks%4) + chi + 8*rhi + 16*half
+  // for token 16 mt + g + 8 rhi and position 16 ks + 2t + 8 chi + half; the
+  // two halves are adjacent positions, read together
+  const uint16_t* cB2 = reinterpret_cast<const uint16_t*>(cB);
   uint32_t* lsb = reinterpret_cast<uint32_t*>(rec + L.k_codes);
   for (int w = threadIdx.x; w < kKG * kD / 32; w += blockDim.x) {
     const int lane = w & 31, kq = (w >> 5) & 1, mt = w >> 6;
     const int g = lane >> 2, t = lane & 3;
     uint32_t acc = 0;
-#pragma unroll 4
-    for (int bit = 0; bit < 32; ++bit) {
-      const int half = bit >> 4, rhi = (bit >> 3) & 1, kl4 = (bit >> 1) & 3, chi = bit & 1;
-      const int tok = 16 * mt + g + 8 * rhi;
-      const int p = 16 * (4 * kq + kl4) + 2 * t + 8 * chi + half;
-      acc |= static_cast<uint32_t>(cB[tok * kD + p] & 1u) << bit;
-    }
+#pragma unroll
+    for (int rhi = 0; rhi < 2; ++rhi)
+#pragma unroll
+      for (int kl4 = 0; kl4 < 4; ++kl4)
+#pragma unroll
+        for (int chi = 0; chi < 2; ++chi) {
+          const int tok = 16 * mt + g + 8 * rhi, p = 16 * (4 * kq + kl4) + 2 * t + 8 * chi;
+          const uint32_t two = cB2[(tok * kD + p) >> 1];   // positions p, p + 1
+          const int bit = 2 * kl4 + chi + 8 * rhi;
+          acc |= (two & 1u) << bit;
+          acc |= ((two >> 8) & 1u) << (bit + 16);
+        }
     lsb[w] = acc;
   }
-  // upper plane of the high positions: 2-bit key fragment order, kw2 words a (tile, lane)
+  // upper plane of the high positions: 2-bit key fragment order, kw2 words a
+  // (tile, lane): word (mt kw2 + wi) 32 + lane, slot P + 8 half for token
+  // 16 mt + g + 8 (P >> 2) and position 32 wi + 16 ((P >> 1) & 1) + 8 (P & 1)
+  // + 2t + half (the fragment pair order of the mixed key records)
   uint32_t* up = reinterpret_cast<uint32_t*>(rec + L.kc);
   for (int w = threadIdx.x; w < 8 * L.kw2 * 32; w += blockDim.x) {
+    const int lane = w & 31, qw = w >> 5, mt = qw / L.kw2, wi = qw - mt * L.kw2;
+    const int g = lane >> 2, t = lane & 3;
     uint32_t acc = 0;
-    for (int s2 = 0; s2 < 16; ++s2) {
-      int tok, v;
-      mixed_word_code(w, s2, L.kw2, tok, v);
-      acc |= static_cast<uint32_t>(cB[tok * kD + v] >> 1) << (2 * s2);
+#pragma unroll
+    for (int P = 0; P < 8; ++P) {
+      const int tok = 16 * mt + g + 8 * (P >> 2);
+      const int v = 32 * wi + 16 * ((P >> 1) & 1) + 8 * (P & 1) + 2 * t;
+      const uint32_t two = cB2[(tok * kD + v) >> 1];   // positions v, v + 1
+      acc |= ((two >> 1) & 3u) << (2 * P);
+      acc |= ((two >> 9) & 3u) << (2 * P + 16);
     }
     up[w] = acc;
   }
