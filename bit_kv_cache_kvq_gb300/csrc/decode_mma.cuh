@@ -332,17 +332,37 @@ struct Warp {
 #pragma unroll
       for (int i = 0; i < 16; i += 4)
         *reinterpret_cast<float4*>(q + h * kQRow + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-    } else {       // bf16 [8][kQRow]
-      uint32_t* q = static_cast<uint32_t*>(qs);
-      for (int i = lane; i < 8 * (kD / 2); i += 32) {
-        const int h = i / (kD / 2), c2 = i % (kD / 2);
+    } else {       // bf16 [8][kQRow]; lane = 8-channel pieces lane + 32 i of the 128
+      // all loads are issued before any store: at the start of a call they
+      // queue behind every warp's first records, so one round trip, not 16
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int piece = lane + 32 * i, h = piece >> 4, c = (piece & 15) * 8;
         if (PNMIX) {   // the unit's stored channel order
-          const uint8_t* pm = a.perm + static_cast<long long>(u) * kD + 2 * c2;
-          q[h * (kQRow / 2) + c2] = static_cast<uint32_t>(qg[h * kD + pm[0]]) |
-                                    (static_cast<uint32_t>(qg[h * kD + pm[1]]) << 16);
+          const uint8_t* pm = a.perm + static_cast<long long>(u) * kD + c;
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            w[k] = static_cast<uint32_t>(qg[h * kD + pm[2 * k]]) |
+                   (static_cast<uint32_t>(qg[h * kD + pm[2 * k + 1]]) << 16);
+          v[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        } else if ((reinterpret_cast<uintptr_t>(a.q) & 15) == 0) {
+          v[i] = __ldg(reinterpret_cast<const uint4*>(qg + h * kD + c));
         } else {
-          q[h * (kQRow / 2) + c2] = reinterpret_cast<const uint32_t*>(qg + h * kD)[c2];
+          const uint16_t* src = qg + h * kD + c;   // any 2-byte aligned q
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            w[k] = static_cast<uint32_t>(src[2 * k]) | (static_cast<uint32_t>(src[2 * k + 1]) << 16);
+          v[i] = make_uint4(w[0], w[1], w[2], w[3]);
         }
+      }
+      uint16_t* q = static_cast<uint16_t*>(qs);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int piece = lane + 32 * i, h = piece >> 4, c = (piece & 15) * 8;
+        *reinterpret_cast<uint4*>(q + h * kQRow + c) = v[i];
       }
     }
     __syncwarp();
