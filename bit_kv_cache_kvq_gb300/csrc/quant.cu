@@ -751,17 +751,28 @@ __global__ void __launch_bounds__(256) quantize_pnmix_kernel(QuantArgs a) {
   __syncthreads();
   uint8_t* rec = group_record(a);
   unsigned flags = 0;
+  // channel ranges (all threads; the code area is free until the codes),
+  // then each stored position takes its channel's
+  {
+    float* s_clo = reinterpret_cast<float*>(cB + kRedBytes);
+    float* s_chi = s_clo + kD;
+    uint8_t* s_cbad = reinterpret_cast<uint8_t*>(s_chi + kD);
+    float lo, hi;
+    bool bad;
+    key_ranges(sK, reinterpret_cast<uint32_t*>(cB), lo, hi, bad);
+    if (threadIdx.x < kD) {
+      s_clo[threadIdx.x] = lo;
+      s_chi[threadIdx.x] = hi;
+      s_cbad[threadIdx.x] = bad;
+    }
+    __syncthreads();
+  }
   if (threadIdx.x < kD) {
     const int p = threadIdx.x;
     const int ch = a.perm[static_cast<long long>(blockIdx.y) * kD + p];
-    float lo = bf2f(sK[swz(0, ch)]), hi = lo;
-    bool bad = false;
-    for (int t = 0; t < kKG; ++t) {
-      const float x = bf2f(sK[swz(t, ch)]);
-      bad |= !isfinite(x);
-      if (x < lo || (x == lo && (__float_as_uint(x) >> 31) && !(__float_as_uint(lo) >> 31))) lo = x;
-      if (x > hi || (x == hi && !(__float_as_uint(x) >> 31) && (__float_as_uint(hi) >> 31))) hi = x;
-    }
+    const float* s_clo = reinterpret_cast<const float*>(cB + kRedBytes);
+    const float lo = s_clo[ch], hi = s_clo[kD + ch];
+    const bool bad = (cB + kRedBytes + 2 * kD * 4)[ch] != 0;
     float off = lo, sc = 0.0f;
     if (bad) {
       flags |= KVQ_FLAG_NONFINITE;
