@@ -17,20 +17,20 @@ __device__ __forceinline__ float bfv(uint16_t b) { return __uint_as_float(static
 // (qbar: the mean over the GQA group's heads, in order, of the heads' mean
 // pair norms).  The unit's key rows stream through a ring of kPairStages
 // shared-memory slots of kPairRows rows (one bulk copy a slot, on an
-// mbarrier).  For each chunk every thread computes pair norms (thread ->
-// pair tid mod 64, rows tid / 64 + 8k) into a term table, then thread i <
-// 64 adds pair i's terms in token order; the query window goes through the
-// same table.  (512 threads and 128-row chunks: 0.84 ms at 32K x 16 units,
-// against 1.29 ms with 256 threads and 64-row chunks.)  Then the n_high largest sigma (ties: lower pair; a NaN counts
-// as the smallest) are selected, and the unit's stored channel order is
-// written: the selected pairs' channels ascending, then the others
-// ascending.
+// mbarrier).  Threads 64 and up compute a chunk's pair norms (thread ->
+// pair tid mod 64, rows tid / 64 - 1 + 7k) into one half of a term table
+// while thread i < 64 adds the previous chunk's terms of pair i in token
+// order from the other half; the query window goes through the table with
+// every thread computing terms.  Then the n_high largest sigma (ties: lower
+// pair; a NaN counts as the smallest) are selected, and the unit's stored
+// channel order is written: the selected pairs' channels ascending, then
+// the others ascending.
 constexpr int kPairRows = 128;
 constexpr int kPairStages = 4;
 constexpr int kPairThreads = 512;
 constexpr int kPairWaitPolls = 1 << 20;
 constexpr size_t kPairRing = static_cast<size_t>(kPairStages) * kPairRows * kD * 2;
-constexpr size_t kPairTerms = static_cast<size_t>(kPairRows) * (kD / 2) * 4;
+constexpr size_t kPairTerms = 2 * static_cast<size_t>(kPairRows) * (kD / 2) * 4;   // two halves
 constexpr size_t kPairSmem = kPairRing + kPairTerms + kPairStages * 8 + 16;
 
 __device__ __forceinline__ bool pair_wait(uint32_t mb, uint32_t parity, int polls) {
@@ -96,34 +96,43 @@ __global__ void __launch_bounds__(kPairThreads) pnmix_pairs_kernel(
   if (tid == 0)
     for (; issued < min(kPairStages, nch); ++issued) issue(issued);
   bool bad = false;
-  // key means: per chunk, every thread's terms into the table, then pair
-  // i's in token order by thread i
+  // Key means, two chunks in flight: in pass c the producer threads (P and
+  // up) write chunk c's pair norms into table half c & 1 while thread i < P
+  // adds chunk c - 1's terms of pair i, in token order, from the other half.
+  constexpr int kProdRows = (kPairThreads - P) / P;   // 7 rows in flight per pass of the producers
   float kacc = 0.0f;
   int c = 0;
-  for (; c < nch; ++c) {
+  for (; c <= nch; ++c) {
+    const bool produce = c < nch;
     const int st = c % kPairStages;
-    if (!pair_wait(bar0 + 8 * st, (c / kPairStages) & 1, kPairWaitPolls)) atomicOr(&stop, 1);
-    __syncthreads();   // every thread has waited (or given up)
+    if (produce && tid >= P && !pair_wait(bar0 + 8 * st, (c / kPairStages) & 1, kPairWaitPolls))
+      atomicOr(&stop, 1);
+    __syncthreads();   // every producer has waited (or given up)
     if (stop) break;   // block-uniform
-    const uint16_t* rows = ring + static_cast<size_t>(st) * kPairRows * kD;
-    const int n = min(kPairRows, Lk - kPairRows * c);
+    if (tid >= P) {
+      if (produce) {
+        const uint16_t* rows = ring + static_cast<size_t>(st) * kPairRows * kD;
+        float* tb = terms + (c & 1) * (kPairRows * P);
+        const int n = min(kPairRows, Lk - kPairRows * c);
 #pragma unroll 4
-    for (int r = r0; r < n; r += kRowStep)
-      terms[r * P + i] = pair_norm(rows[r * kD + ca], rows[r * kD + cb], bad);
-    __syncthreads();   // stage st consumed, the table full
-    if (tid == 0 && issued < nch) issue(issued++);
-    if (tid < P) {
+        for (int r = tid / P - 1; r < n; r += kProdRows)
+          tb[r * P + i] = pair_norm(rows[r * kD + ca], rows[r * kD + cb], bad);
+      }
+    } else if (c > 0) {
+      const float* tb = terms + ((c - 1) & 1) * (kPairRows * P);
+      const int n = min(kPairRows, Lk - kPairRows * (c - 1));
       // sixteen terms' loads ahead of their additions (in token order)
       for (int r0s = 0; r0s < n; r0s += 16) {
         float v[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = terms[min(r0s + j, n - 1) * P + i];
+        for (int j = 0; j < 16; ++j) v[j] = tb[min(r0s + j, n - 1) * P + i];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           if (r0s + j < n) kacc = __fadd_rn(kacc, v[j]);
       }
     }
-    __syncthreads();   // the table read before the next chunk's terms
+    __syncthreads();   // chunk c's stage consumed and its terms written, chunk c - 1's added
+    if (tid == 0 && produce && issued < nch) issue(issued++);
   }
   if (stop && tid == 0) {
     // a wait gave up: every copy still in flight lands before the block
