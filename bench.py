@@ -18,11 +18,14 @@ region is the workload's.
 metric/value: effective HBM GB/s = algorithmic bytes of the steps (packed
 cache 94 B/token/KV head at 2 bits, residual 512 B/token, q and o, append and
 flush traffic) / device time of the K steps between two events.  The
-roofline object covers the decode attention launch pair (partial + combine):
-the median of 50 calls, each between two CUDA events on the launching
-stream, with a scratch write of twice the L2 size (then a read of another
-buffer as large, so no dirty line is written back during the call) before
-every call outside the events (p10/p50/p90 reported).  e2e repeats the steps through the same API with q, k_new
+roofline object covers the dominant kernel, the split-K decode kernel: its
+mean launch duration over 50 calls, each from an event recorded before the
+call to the event the library records between the decode kernel and its
+combine (kvq_set_decode_split_event); 50 more calls, interleaved, between
+two events give the whole call (decode + combine) as p10/p50/p90.  Every
+call runs after a scratch write of twice the L2 size (then a read of another
+buffer as large, so no dirty line is written back during the call) outside
+the events.  e2e repeats the steps through the same API with q, k_new
 and v_new copied from pinned host memory (one packed copy) and the output
 copied back every step, the host reading each output one step later.
 cpu_baseline times the CPU oracle on a bounded sample.
@@ -45,7 +48,7 @@ sys.path.insert(0, ROOT)
 METRIC = "quantized-KV decode attention: effective HBM GB/s (% of peak), µs/step"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024      # GB300 L2
-ATTN_REPS = 50                     # per-call timed decode attention calls (roofline)
+ATTN_REPS = 50                     # timed calls of each kind (kernel alone / whole call)
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_mma_kernel
 # launch, from the ncu capture of this workload at batch 8 kept under
@@ -472,16 +475,21 @@ def run_ours(args, rank, world):
     t_end.record(stream)
     torch.cuda.synchronize()
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-    # pass 2 (roofline): ATTN_REPS decode attention calls (kvq_decode_step: the
-    # decode with the token append fused, and its combine), each between two
-    # events on the launching stream, with a scratch buffer twice the L2 size
-    # written before every call outside the events.  The residual starts
-    # ATTN_REPS / 2 tokens below the workload's, so the calls never flush and
-    # their mean context is the workload's.
+    # pass 2 (roofline): 2 x ATTN_REPS decode attention calls (kvq_decode_step:
+    # the decode with the token append fused, and its combine), with a
+    # scratch buffer twice the L2 size written before every call outside the
+    # events.  Even calls run between two events on the launching stream (the
+    # call's time); odd calls also have the library record an event between
+    # the decode kernel and its combine (kvq_set_decode_split_event), so the
+    # first event and that one bracket the decode kernel alone (the roofline
+    # kernel's launch duration).  The residual starts ATTN_REPS tokens below
+    # the workload's, so the calls never flush and their mean context is the
+    # workload's.
     R, Wp = ATTN_REPS, 3
-    r0 = max(0, w.r - R // 2 - Wp)
-    if r0 + Wp + R >= 128:
-        r0 = 127 - Wp - R
+    R2 = 2 * R
+    r0 = max(0, w.r - R2 // 2 - Wp)
+    if r0 + Wp + R2 >= 128:
+        r0 = 127 - Wp - R2
     Lp = w.T_q + r0
     Kp, Vp = Kall[:, :, :Lp].contiguous(), Vall[:, :, :Lp].contiguous()
     cache.reset()
@@ -502,14 +510,17 @@ def run_ours(args, rank, world):
     for i in range(Wp):                             # untimed warm-up calls
         kn, vn = toks[i % len(toks)]
         cache.decode_step(kn, vn, qs[i % n_q], out=out, workspace=ws, importance=importance)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(R)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(R2)]
+    for ev in evs:
+        ev[2].record(stream)                         # created before the timed calls
     attn_bytes = []
-    for i in range(R):
+    for i in range(R2):
         flush_l2(i)                                  # outside the events
         tq_r = cache.lengths()
         kn, vn = toks[(Wp + i) % len(toks)]
         evs[i][0].record(stream)
+        if i % 2:
+            kvq.set_decode_split_event(evs[i][2])
         cache.decode_step(kn, vn, qs[i % n_q], out=out, workspace=ws, importance=importance)
         evs[i][1].record(stream)
         assert cache.lengths() == (tq_r[0], tq_r[1] + 1), "a timed call flushed"
@@ -524,13 +535,17 @@ def run_ours(args, rank, world):
     if args.no_bf16 and args.no_e2e:       # keep device memory small (profiling)
         del Kall, Vall
         torch.cuda.empty_cache()
-    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    attn_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(0, R2, 2)]
+    kern_ms = [evs[i][0].elapsed_time(evs[i][2]) for i in range(1, R2, 2)]
     p10, p50, p90 = percentiles(attn_ms, (10, 50, 90))
-    attn_avg_bytes = sum(attn_bytes) / R
+    k10, k50, k90 = percentiles(kern_ms, (10, 50, 90))
+    kern_mean = sum(kern_ms) / len(kern_ms)
+    attn_avg_bytes = sum(attn_bytes) / R2
+    kern_avg_bytes = sum(attn_bytes[1::2]) / R
     ms_per_step = elapsed_ms / K
     value = total_bytes * world / (elapsed_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
-    achieved = attn_avg_bytes / (p50 * 1e-3) / 1e9
+    achieved = kern_avg_bytes / (kern_mean * 1e-3) / 1e9
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get(src_hash, {}).get((w.name, w.B, w.T_q, w.k_bits))
     line = {
@@ -545,15 +560,23 @@ def run_ours(args, rank, world):
         "us_per_step": 1e3 * ms_per_step,
         "decode_attention_us": 1e3 * p50,
         "decode_attention_us_p10_p50_p90": [1e3 * p10, 1e3 * p50, 1e3 * p90],
+        "decode_kernel_us_mean": 1e3 * kern_mean,
+        "decode_kernel_us_p10_p50_p90": [1e3 * k10, 1e3 * k50, 1e3 * k90],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": "decode attention (split-K partial + combine)",
-                     "algorithmic_bytes_per_launch": attn_avg_bytes, "traffic": traffic,
+                     "kernel": "decode_mma_kernel (split-K partials; the combine kernel "
+                               "after it is in the call's time)",
+                     "algorithmic_bytes_per_launch": kern_avg_bytes, "traffic": traffic,
                      "kernel_source": src_hash,
-                     "timing": f"median of {R} calls, each between two CUDA events on the "
-                               f"launching stream after a {2 * L2_BYTES / 1e6:.0f} MB scratch "
-                               f"write (2x L2) and a read of another buffer as large, outside "
-                               f"the events; residual {r0 + Wp + 1}..{r0 + Wp + R} tokens"},
+                     "call_frac": attn_avg_bytes / (p50 * 1e-3) / 1e9 / peak,
+                     "timing": f"mean of {R} decode kernel launches, each from an event "
+                               f"recorded before the call to one the library records between "
+                               f"the decode kernel and its combine; call times (p10/p50/p90, "
+                               f"call_frac from the median) from {R} calls between two events, "
+                               f"interleaved; every call after a {2 * L2_BYTES / 1e6:.0f} MB "
+                               f"scratch write (2x L2) and a read of another buffer as large, "
+                               f"outside the events; residual {r0 + Wp + 1}..{r0 + Wp + R2} "
+                               f"tokens"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "prefill": {"tokens": L0, "us": prefill_us,

@@ -85,6 +85,7 @@ _SIGS = {
     "kvq_export_sink": (_I, [_P, _P, _P, _P]),
     "kvq_export_k_mixed": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvq_set_wait_limit": (_I, [_I]),
+    "kvq_set_decode_split_event": (_I, [_P]),
     "kvq_export_kivi": (_I, [_P] * 10),
     "kvq_pnmix_pairs": (_I, [_P, _P, _I, _I, _P, _I, _P, _P]),
     "kvq_export_pnmix": (_I, [_P] * 6),
@@ -446,3 +447,14 @@ def set_wait_limit(polls: int) -> int:
     hook for tests: 0 makes every wait give up at once, setting
     FLAG_TIMEOUT.  Returns the previous limit."""
     return int(lib().kvq_set_wait_limit(int(polls)))
+
+
+def set_decode_split_event(event) -> None:
+    """The next decode attention call records ``event`` (a
+    ``torch.cuda.Event`` with timing, or None to cancel) between its decode
+    kernel and its combine (kvq_set_decode_split_event): an event recorded
+    before the call and this one bracket the decode kernel alone."""
+    if event is not None and not event.cuda_event:
+        event.record()   # torch creates its events on their first record
+    handle = None if event is None else ctypes.c_void_p(int(event.cuda_event))
+    _check(lib().kvq_set_decode_split_event(handle), "kvq_set_decode_split_event")

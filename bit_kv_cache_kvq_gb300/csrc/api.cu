@@ -531,6 +531,11 @@ int kvq_set_wait_limit(int polls) {
   return previous;
 }
 
+int kvq_set_decode_split_event(cudaEvent_t ev) {
+  set_decode_split_event(ev);
+  return KVQ_OK;
+}
+
 int kvq_export_kivi(const kvq_cache* c, uint8_t* k_codes, kvq_bf16* k_origin, kvq_bf16* k_step,
                     uint8_t* v_codes, kvq_bf16* v_origin, kvq_bf16* v_step, kvq_bf16* k_res,
                     kvq_bf16* v_res, cudaStream_t s) {

@@ -159,8 +159,11 @@ __global__ void __launch_bounds__(kManyWarps * 32) combine_many_kernel(
 }
 
 std::atomic<int> g_wait_polls{kWaitPolls};
+std::atomic<cudaEvent_t> g_split_event{nullptr};
 
 }  // namespace
+
+void set_decode_split_event(cudaEvent_t ev) { g_split_event.store(ev, std::memory_order_relaxed); }
 
 int decode_wait_polls() { return g_wait_polls.load(std::memory_order_relaxed); }
 void set_decode_wait_polls(int polls) {
@@ -293,6 +296,11 @@ cudaError_t launch_decode_mma(const kvq_cache* c, const kvq_bf16* q, int Hq, flo
     e = launch_rep<4, 4, false>(a, nrep, warps, s);
   }
   if (e != cudaSuccess) return e;
+  // measurement hook: an event between the decode kernel and its combine
+  if (cudaEvent_t ev = g_split_event.exchange(nullptr, std::memory_order_relaxed)) {
+    e = cudaEventRecord(ev, s);
+    if (e != cudaSuccess) return e;
+  }
   return launch_combine_parts(ws, c->cfg.batch, a.Hkv, Hq, a.max_parts, a.unit_len, a.total,
                               a.n_slots, out, s);
 }

@@ -226,6 +226,7 @@ struct SmemOptIn {
 // up (KVQ_FLAG_TIMEOUT); kvq_set_wait_limit changes it for failure tests.
 int decode_wait_polls();
 void set_decode_wait_polls(int polls);
+void set_decode_split_event(cudaEvent_t ev);
 
 // Where the quantize kernel reads its 128-token tiles from.
 struct QuantSrc {

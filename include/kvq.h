@@ -469,6 +469,20 @@ int kvq_export_sink(const kvq_cache* cache, kvq_bf16* k, kvq_bf16* v, cudaStream
  */
 int kvq_set_wait_limit(int polls);
 
+/*
+ * Measurement hook (no counterpart on the pages).  The next decode
+ * attention call (kvq_decode_attention, kvq_decode_step or
+ * kvq_decode_attention_static) records `ev` on its stream right after it
+ * enqueues the split-K decode kernel and before it enqueues the combine
+ * kernel, then forgets it; so an event recorded before the call and `ev`
+ * bracket the decode kernel alone.  ev: an event of the caller's (created
+ * with timing), owned by the caller; NULL cancels a pending one.  A call
+ * that fails before its decode kernel is enqueued leaves the event pending.
+ * The setting is process-wide, for benchmarks; it is not meant for
+ * concurrent use.  Returns KVQ_OK.
+ */
+int kvq_set_decode_split_event(cudaEvent_t ev);
+
 /* Human-readable name of a return code. */
 const char* kvq_status_string(int code);
 

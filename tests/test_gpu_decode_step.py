@@ -84,3 +84,35 @@ def test_decode_step_rejects_a_full_residual_without_changes():
         cache.decode_step(kn.cuda(), vn.cuda(), make_q(w).cuda())
     assert e.value.name == "RESIDUAL_FULL"
     assert cache.lengths() == (0, 128)
+
+
+def test_decode_split_event_brackets_the_decode_kernel_once():
+    """kvq_set_decode_split_event: the next call records the event between
+    its decode kernel and its combine (inside the call's own events), the
+    output is the same as without it, and the call after forgets it."""
+    w = Workload("split_event", 93, B=2, Hq=8, Hkv=2, T_q=0, r=1000, k_outliers=4)
+    K, V = make_kv(w, 1000)
+    cache = kvq.KVCache(2, 2, 1280)
+    cache.prefill(K.cuda(), V.cuda())
+    q = make_q(w).cuda()
+    ws = cache.workspace(w.Hq)
+    want = cache.attention(q, workspace=ws).clone()
+    e0, mid, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    e0.record()
+    kvq.set_decode_split_event(mid)
+    got = cache.attention(q, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+    t_mid, t_end = e0.elapsed_time(mid), e0.elapsed_time(e1)
+    assert 0.0 < t_mid <= t_end
+    # one-shot: the next call does not record it again
+    cache.attention(q, workspace=ws)
+    torch.cuda.synchronize()
+    assert e0.elapsed_time(mid) == t_mid
+    # a pending event can be cancelled
+    kvq.set_decode_split_event(mid)
+    kvq.set_decode_split_event(None)
+    cache.attention(q, workspace=ws)
+    torch.cuda.synchronize()
+    assert e0.elapsed_time(mid) == t_mid
