@@ -121,6 +121,10 @@ def _stream(stream=None) -> int:
 def _ptr(t: torch.Tensor | None, dtype=None, shape=None, name="tensor"):
     if t is None:
         return None
+    # one combined test on the common path (a decode step checks seven tensors)
+    if (t.is_cuda and (dtype is None or t.dtype == dtype)
+            and (shape is None or t.shape == shape) and t.is_contiguous()):
+        return t.data_ptr()
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if dtype is not None and t.dtype != dtype:
