@@ -51,16 +51,21 @@ L2_BYTES = 129 * 1024 * 1024      # GB300 L2
 ATTN_REPS = 50                     # timed calls of each kind (kernel alone / whole call)
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_mma_kernel
-# launch, from the ncu capture of this workload at batch 8 kept under
-# profiles/, keyed by the hash of the decode kernel's code it was taken on
-# (a stale entry reports null).  The capture ran at batch 8 (64 units,
-# 32768 + 100 tokens, the token append fused): 200.986 MB read + 4.005 MB
-# written against 200.638 MB of algorithmic attention bytes (ratio 1.0217:
-# mostly the split-K partials written).  Traffic per unit is independent of
-# the batch, so the batch-16 launch is that ratio times its algorithmic
-# bytes at the timed steps' mean context.
+# launch, from the ncu captures kept under profiles/, keyed by the hash of
+# the decode kernel's code they were taken on (a stale entry reports null).
+# Llama-8B: captured at batch 8 (64 units, 32768 + 100 tokens, the token
+# append fused): 201.028 MB read + 3.841 MB written against 200.638 MB of
+# algorithmic attention bytes (ratio 1.0211: mostly the split-K partials
+# written).  Traffic per unit is independent of the batch, so the batch-16
+# launch is that ratio times its algorithmic bytes at the timed steps' mean
+# context.  MixKVQ: captured at the bench size (batch 8, 16384 + 100
+# tokens): 124.513 MB read + 3.128 MB written (the stored mixed key records
+# are 7552 B against 7100 B of algorithmic key bytes per group).
 NCU_TRAFFIC = {
-    "d3a5bdac2efb0df3": {("llama8b_gqa_32k_b16", 16, 32768, 2): 204.991232 / 200.638464 * 401.375232e6},
+    "f9e1ae51858e4665": {
+        ("llama8b_gqa_32k_b16", 16, 32768, 2): 204.868608 / 200.638464 * 401.375232e6,
+        ("mixkvq_qwen32b_16k_b8", 8, 16384, 2): 127.641088e6,
+    },
 }
 
 
