@@ -51,20 +51,21 @@ L2_BYTES = 129 * 1024 * 1024      # GB300 L2
 ATTN_REPS = 50                     # timed calls of each kind (kernel alone / whole call)
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_mma_kernel
-# launch, from the ncu captures kept under profiles/, keyed by the hash of
-# the decode kernel's code they were taken on (a stale entry reports null).
-# Llama-8B: captured at batch 8 (64 units, 32768 + 100 tokens, the token
-# append fused): 201.028 MB read + 3.841 MB written against 200.638 MB of
-# algorithmic attention bytes (ratio 1.0211: mostly the split-K partials
-# written).  Traffic per unit is independent of the batch, so the batch-16
-# launch is that ratio times its algorithmic bytes at the timed steps' mean
-# context.  MixKVQ: captured at the bench size (batch 8, 16384 + 100
-# tokens): 124.513 MB read + 3.128 MB written (the stored mixed key records
-# are 7552 B against 7100 B of algorithmic key bytes per group).
+# launch over its algorithmic bytes, from the ncu captures kept under
+# profiles/, keyed by the hash of the decode kernel's code they were taken
+# on (a stale entry reports null); the bench reports that ratio times the
+# timed launches' mean algorithmic bytes (traffic per unit does not depend
+# on the batch, and the captured step's context is the workload's).
+# Llama-8B, captured at batch 8 (64 units, 32768 + 100 tokens, the token
+# append fused): 201.028 MB read + 3.841 MB written against 200.638 MB
+# (mostly the split-K partials written).  MixKVQ, captured at the bench size
+# (batch 8, 16384 + 100 tokens): 124.513 MB read + 3.128 MB written against
+# 120.64 MB (the stored mixed key records are 7552 B against 7100 B of
+# algorithmic key bytes per group).
 NCU_TRAFFIC = {
     "f9e1ae51858e4665": {
-        ("llama8b_gqa_32k_b16", 16, 32768, 2): 204.868608 / 200.638464 * 401.375232e6,
-        ("mixkvq_qwen32b_16k_b8", 8, 16384, 2): 127.641088e6,
+        ("llama8b_gqa_32k_b16", 16, 32768, 2): 204.868608 / 200.638464,
+        ("mixkvq_qwen32b_16k_b8", 8, 16384, 2): 127.641088 / 120.64,
     },
 }
 
@@ -552,7 +553,8 @@ def run_ours(args, rank, world):
     peak, peak_kind = measured_peak()
     achieved = kern_avg_bytes / (kern_mean * 1e-3) / 1e9
     src_hash = kernel_source_hash()
-    traffic = NCU_TRAFFIC.get(src_hash, {}).get((w.name, w.B, w.T_q, w.k_bits))
+    traffic_ratio = NCU_TRAFFIC.get(src_hash, {}).get((w.name, w.B, w.T_q, w.k_bits))
+    traffic = None if traffic_ratio is None else traffic_ratio * kern_avg_bytes
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True,
