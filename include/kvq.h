@@ -173,7 +173,10 @@ typedef struct kvq_cache kvq_cache; /* opaque */
 size_t kvq_cache_bytes(const kvq_config* cfg);
 
 /*
- * Create a cache.  dev_buf: NULL -> the library allocates kvq_cache_bytes
+ * Create a cache: the state MixKVQ Algorithm 1 keeps per layer (the packed
+ * history, the full-precision residual; MixKVQ "system-level implementation
+ * details": quantized store, BF16 outlier store, residual) and KIVI §4's
+ * residual state machine.  dev_buf: NULL -> the library allocates kvq_cache_bytes
  * with cudaMallocAsync on s and frees it in kvq_cache_free; else a caller
  * buffer of buf_bytes >= kvq_cache_bytes (256-byte aligned), which the
  * caller keeps alive and frees after kvq_cache_free.  The cache starts
@@ -182,16 +185,22 @@ size_t kvq_cache_bytes(const kvq_config* cfg);
  */
 int kvq_cache_alloc(const kvq_config* cfg, void* dev_buf, size_t buf_bytes,
                     cudaStream_t s, kvq_cache** out);
+/* Release a cache of kvq_cache_alloc (its own allocation freed on s; a
+ * caller buffer is left to the caller).  Errors: ARG (NULL), CUDA. */
 int kvq_cache_free(kvq_cache* cache, cudaStream_t s);
 
-/* Host-side lengths: quantized history tokens and residual tokens. */
+/* Host-side lengths (MixKVQ Algorithm 1's len(X_K_r) and the quantized
+ * history; KIVI §4's boundaries): quantized history tokens and residual
+ * tokens.  In KIVI mode the first is the sealed key tokens and the second
+ * the key residual; the value FIFO holds min(total, 128) of the newest. */
 int kvq_cache_lengths(const kvq_cache* cache, int* quantized_tokens,
                       int* residual_tokens);
 
 /* Host-side length of the attention-sink window (0..n_sink). */
 int kvq_cache_sink_tokens(const kvq_cache* cache, int* sink_tokens);
 
-/* Empty the cache (lengths to 0, status word cleared on s). */
+/* Empty the cache (lengths to 0, status word cleared on s): the state
+ * before MixKVQ Algorithm 1's Prefill. */
 int kvq_cache_reset(kvq_cache* cache, cudaStream_t s);
 
 /*
@@ -371,7 +380,10 @@ int kvq_cache_status(kvq_cache* cache, cudaStream_t s, int* status);
 
 /*
  * Canonical export of the quantized history (device destination buffers),
- * for checking and debugging.  T = quantized tokens, n = T/128.
+ * for checking and debugging: the (codes, origin, step) of KIVI §2's group
+ * contract on KIVI §3's axes (keys per channel along tokens, values per
+ * token over channel groups), and MixKVQ's per-group tier layout
+ * ("system-level implementation details").  T = quantized tokens, n = T/128.
  *  Key (uniform): codes uint8 [B][Hkv][n][D][128*k_bits/8] (each channel's
  *    128 codes LSB first along tokens), kmin bf16 [B][Hkv][n][D], kscale
  *    fp32 [B][Hkv][n][D].
