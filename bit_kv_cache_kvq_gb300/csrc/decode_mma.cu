@@ -7,17 +7,17 @@ namespace {
 
 // Merge the partials (o, m, l) of one query head (block = (b, hq), thread =
 // channel) with the log-sum-exp rule: M = max m_k, w_k = 2^(m_k - M),
-// o = sum w_k o_k / sum w_k l_k.  Every warp takes the weights itself (lanes
-// k % 32 hold parts k and k + 32), so no block barrier is needed, and the
-// values of the first 64 parts load together with the maxima: for up to 64
-// parts the merge is one round trip to memory.  Launched as a programmatic
-// dependent of the decode kernel: it may start while that kernel drains and
-// waits for its results with griddepcontrol.wait.
+// o = sum w_k o_k / sum w_k l_k.  Every warp takes the weights itself (lane
+// k % 32 holds part k's), so no block barrier is needed, and the values of
+// the first 32 parts load together with the maxima: for up to 32 parts the
+// merge is one round trip to memory.  Launched as a programmatic dependent
+// of the decode kernel: it may start while that kernel drains and waits for
+// its results with griddepcontrol.wait.
 __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restrict__ ws,
                                                            int Hkv, int Hq, int max_parts,
                                                            long long unit_len, long long total,
                                                            int n_slots, float* __restrict__ out) {
-  constexpr int kEarly = 64;
+  constexpr int kEarly = 32;
   const int row = blockIdx.x;                 // b * Hq + hq
   const int n_rep = Hq / Hkv;
   const int b = row / Hq, hq = row % Hq;
@@ -42,27 +42,20 @@ __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restr
     for (int j = 0; j < kEarly; ++j) o[j] = j < np ? base[j * stride + c] : 0.0f;
     const float m0 = lane < np ? base[lane * stride + kD] : -INFINITY;
     const float l0 = lane < np ? base[lane * stride + kD + 1] : 0.0f;
-    const float m1 = lane + 32 < np ? base[(lane + 32) * stride + kD] : -INFINITY;
-    const float l1 = lane + 32 < np ? base[(lane + 32) * stride + kD + 1] : 0.0f;
-    float M = fmaxf(m0, m1);
-    for (int k = lane + kEarly; k < np; k += 32) M = fmaxf(M, base[k * stride + kD]);
+    float M = m0;
+    for (int k = lane + 32; k < np; k += 32) M = fmaxf(M, base[k * stride + kD]);
 #pragma unroll
     for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
-    // parts 0..63: weights from lane k % 32; a part that saw no token weighs 0
-    const float w0 = m0 == -INFINITY ? 0.0f : exp2f(m0 - M);
-    const float w1 = m1 == -INFINITY ? 0.0f : exp2f(m1 - M);
-    float L = fmaf(w1, l1, w0 * l0), O = 0.0f, O1 = 0.0f;
+    // parts 0..31: weights from lane k; a part that saw no token weighs 0
+    float w = m0 == -INFINITY ? 0.0f : exp2f(m0 - M);
+    float L = w * l0, O = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      O = fmaf(__shfl_sync(kFull, w0, j), o[j], O);
-      O1 = fmaf(__shfl_sync(kFull, w1, j), o[32 + j], O1);
-    }
-    O += O1;
-    // parts 64 and up, 32 at a time
-    for (int k0 = kEarly; k0 < np; k0 += 32) {
+    for (int j = 0; j < kEarly; ++j) O = fmaf(__shfl_sync(kFull, w, j), o[j], O);
+    // parts 32 and up, 32 at a time
+    for (int k0 = 32; k0 < np; k0 += 32) {
       const int k = k0 + lane;
       const float mk = k < np ? base[k * stride + kD] : -INFINITY;
-      const float w = mk == -INFINITY ? 0.0f : exp2f(mk - M);
+      w = mk == -INFINITY ? 0.0f : exp2f(mk - M);
       L = fmaf(w, k < np ? base[k * stride + kD + 1] : 0.0f, L);
       const int cnt = min(32, np - k0);
 #pragma unroll 4
@@ -229,8 +222,8 @@ cudaError_t launch_combine_parts(const float* ws, int B, int Hkv, int Hq, int ma
       combine_many_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
       cudaSharedmemCarveoutMaxShared);
   if (carve_many != cudaSuccess) return carve_many;
-  // rows of up to 64 partials: one round trip per row; more: 8 warps a row
-  const bool many = max_parts > 64;
+  // rows of up to 32 partials: one round trip per row; more: 8 warps a row
+  const bool many = max_parts > 32;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(B * Hq);
   lc.blockDim = dim3(many ? kManyWarps * 32 : kD);

@@ -71,8 +71,8 @@ def test_prefill_codes_bit_exact(B, Hkv, L, kb, vb):
 def test_combine_row_sizes(n_groups):
     """Rows of 31, 32, 33, 63 and 64 partials (few units, so one split
     position per warp: a unit's groups, then its residual window weighted as
-    two), on both sides of each combine kernel's limits (one round trip for
-    up to 64 partials a row, 8 warps a row above)."""
+    two), on both sides of the combine kernels' limit (one round trip for up
+    to 32 partials a row, 8 warps a row above)."""
     w = small(1, 2, 4, 128 * n_groups, 50)
     cache, ref, q = run_case(w)
     assert_attention_close(cache.attention(q.cuda()), ref.attention(q), f"{n_groups} groups")
