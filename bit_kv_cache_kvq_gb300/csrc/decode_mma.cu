@@ -69,17 +69,21 @@ __global__ void __launch_bounds__(128) combine_parts_kernel(const float* __restr
 }
 
 // The same merge for rows with many partials (small batches split over
-// the whole GPU): 8 warps per query head, warp w merging parts w, w + 8, ...
-// with eight parts' values in flight per lane (lane = channels 2l, 2l + 1,
-// 64 + 2l, 65 + 2l), then the warps' (M, L, O) merge through shared memory
-// by the same rule.
-constexpr int kManyWarps = 8;
+// the whole GPU): w warps a row, w = ceil(parts / 20) from 4 to 16.  Warp i
+// takes parts 20 i .. 20 i + 19, then 20 (i + w) .., ...: per chunk the
+// twenty parts' values (lane = channels 2l, 2l + 1, 64 + 2l, 65 + 2l), maxima
+// and normalizers load together, and the chunk folds into the warp's
+// running (M, L, O) by the log-sum-exp rule; the warps' states merge
+// through shared memory by the same rule.  For up to 320 parts a row that
+// is one round trip to memory.
+constexpr int kWideParts = 20;   // parts a warp keeps in flight
+constexpr int kWideWarps = 16;
 constexpr size_t kSpreadSmem = 48 * 1024;
-__global__ void __launch_bounds__(kManyWarps * 32) combine_many_kernel(
+__global__ void __launch_bounds__(kWideWarps * 32) combine_wide_kernel(
     const float* __restrict__ ws, int Hkv, int Hq, int max_parts, long long unit_len,
     long long total, int n_slots, float* __restrict__ out) {
-  __shared__ float sO[kManyWarps][kD];
-  __shared__ float sM[kManyWarps], sL[kManyWarps];
+  __shared__ float sO[kWideWarps][kD];
+  __shared__ float sM[kWideWarps], sL[kWideWarps];
   const int row = blockIdx.x;                 // b * Hq + hq
   const int n_rep = Hq / Hkv;
   const int b = row / Hq, hq = row % Hq;
@@ -88,49 +92,52 @@ __global__ void __launch_bounds__(kManyWarps * 32) combine_many_kernel(
   const int first = static_cast<int>(((ub + 1) * n_slots - 1) / total);
   const int last = static_cast<int>(((ub + unit_len) * n_slots - 1) / total);
   const int n = last - first + 1;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const float* base = ws + static_cast<long long>(u) * max_parts * n_rep * (kD + 2) + h * (kD + 2);
   const long long stride = static_cast<long long>(n_rep) * (kD + 2);
   // Two passes over the same code, as in combine_parts_kernel: the first
-  // (before the wait) loads nothing and stores nothing; it only brings the
-  // instructions into the SM's instruction cache.
+  // (before the wait) runs one chunk with every load and the store turned
+  // off; it only brings the instructions into the SM's instruction cache.
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
     if (pass) asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    const bool live = pass != 0;
-    // this warp's parts: k = warp + kManyWarps * i
-    float M = -INFINITY;
-    for (int k = warp + kManyWarps * lane; k < n; k += kManyWarps * 32)
-      M = fmaxf(M, live ? base[k * stride + kD] : -INFINITY);
-#pragma unroll
-    for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
-    float L = 0.0f;
+    const int np = pass ? n : 0;
+    float M = -INFINITY, L = 0.0f;
     float2 o0 = make_float2(0.0f, 0.0f), o1 = make_float2(0.0f, 0.0f);
-    for (int i0 = 0; warp + kManyWarps * i0 < n; i0 += 32) {
-      const int k = warp + kManyWarps * (i0 + lane);
-      const float mk = (live && k < n) ? base[k * stride + kD] : -INFINITY;
-      const float wk = mk == -INFINITY ? 0.0f : exp2f(mk - M);
-      L = fmaf(wk, (live && k < n) ? base[k * stride + kD + 1] : 0.0f, L);
-      const int cnt = min(32, (n - warp + kManyWarps - 1) / kManyWarps - i0);
-      for (int j0 = 0; j0 < cnt; j0 += 8) {
-        float2 a[8], c[8];
+    for (int c0 = warp * kWideParts; c0 < (pass ? np : kWideParts); c0 += nw * kWideParts) {
+      float2 va[kWideParts], vb[kWideParts];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float* pj = base + static_cast<long long>(warp + kManyWarps * (i0 + j0 + j)) * stride;
-          const bool ok = live && j0 + j < cnt;
-          a[j] = ok ? *reinterpret_cast<const float2*>(pj + 2 * lane) : make_float2(0.0f, 0.0f);
-          c[j] = ok ? *reinterpret_cast<const float2*>(pj + 64 + 2 * lane) : make_float2(0.0f, 0.0f);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float wj = __shfl_sync(kFull, wk, (j0 + j) & 31);
-          o0.x = fmaf(wj, a[j].x, o0.x); o0.y = fmaf(wj, a[j].y, o0.y);
-          o1.x = fmaf(wj, c[j].x, o1.x); o1.y = fmaf(wj, c[j].y, o1.y);
-        }
+      for (int j = 0; j < kWideParts; ++j) {
+        const bool ok = c0 + j < np;
+        const float* pj = base + static_cast<long long>(c0 + j) * stride;
+        va[j] = ok ? *reinterpret_cast<const float2*>(pj + 2 * lane) : make_float2(0.0f, 0.0f);
+        vb[j] = ok ? *reinterpret_cast<const float2*>(pj + 64 + 2 * lane) : make_float2(0.0f, 0.0f);
       }
-    }
+      const int kl = c0 + lane;
+      const bool okl = lane < kWideParts && kl < np;
+      const float mk = okl ? base[static_cast<long long>(kl) * stride + kD] : -INFINITY;
+      const float lk = okl ? base[static_cast<long long>(kl) * stride + kD + 1] : 0.0f;
+      float mc = mk;
 #pragma unroll
-    for (int x = 16; x > 0; x >>= 1) L += __shfl_xor_sync(kFull, L, x);
+      for (int x = 16; x > 0; x >>= 1) mc = fmaxf(mc, __shfl_xor_sync(kFull, mc, x));
+      const float mn = fmaxf(M, mc);
+      // running state rescaled to the new maximum; a part (or a state) that
+      // saw no token weighs 0
+      const float f = M == -INFINITY ? 0.0f : exp2f(M - mn);
+      const float wk = mk == -INFINITY ? 0.0f : exp2f(mk - mn);
+      float lw = wk * lk;
+#pragma unroll
+      for (int x = 16; x > 0; x >>= 1) lw += __shfl_xor_sync(kFull, lw, x);
+      L = fmaf(L, f, lw);
+      o0.x *= f; o0.y *= f; o1.x *= f; o1.y *= f;
+#pragma unroll
+      for (int j = 0; j < kWideParts; ++j) {
+        const float wj = __shfl_sync(kFull, wk, j);
+        o0.x = fmaf(wj, va[j].x, o0.x); o0.y = fmaf(wj, va[j].y, o0.y);
+        o1.x = fmaf(wj, vb[j].x, o1.x); o1.y = fmaf(wj, vb[j].y, o1.y);
+      }
+      M = mn;
+    }
     sO[warp][2 * lane] = o0.x;
     sO[warp][2 * lane + 1] = o0.y;
     sO[warp][64 + 2 * lane] = o1.x;
@@ -143,16 +150,14 @@ __global__ void __launch_bounds__(kManyWarps * 32) combine_many_kernel(
     if (threadIdx.x < kD) {
       const int ch = threadIdx.x;
       float Mx = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kManyWarps; ++w) Mx = fmaxf(Mx, sM[w]);
+      for (int w = 0; w < nw; ++w) Mx = fmaxf(Mx, sM[w]);
       float O = 0.0f, Lt = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kManyWarps; ++w) {
+      for (int w = 0; w < nw; ++w) {
         const float f = sM[w] == -INFINITY ? 0.0f : exp2f(sM[w] - Mx);
         O = fmaf(f, sO[w][ch], O);
         Lt = fmaf(f, sL[w], Lt);
       }
-      if (live) out[static_cast<long long>(row) * kD + ch] = O / Lt;
+      if (pass) out[static_cast<long long>(row) * kD + ch] = O / Lt;
     }
     __syncthreads();   // the first pass's reads of the tables before the second's writes
   }
@@ -218,15 +223,19 @@ cudaError_t launch_combine_parts(const float* ws, int B, int Hkv, int Hq, int ma
       combine_parts_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
       cudaSharedmemCarveoutMaxShared);
   if (carve != cudaSuccess) return carve;
-  static const cudaError_t carve_many = cudaFuncSetAttribute(
-      combine_many_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+  static const cudaError_t carve_wide = cudaFuncSetAttribute(
+      combine_wide_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
       cudaSharedmemCarveoutMaxShared);
-  if (carve_many != cudaSuccess) return carve_many;
-  // rows of up to 32 partials: one round trip per row; more: 8 warps a row
+  if (carve_wide != cudaSuccess) return carve_wide;
+  // rows of up to 32 partials: one block of 128 threads a row; more: one
+  // warp per 20 partials a row, at least 4 (the final merge takes a thread
+  // per channel) and at most 16
   const bool many = max_parts > 32;
+  const int wide_warps =
+      max(kD / 32, min(kWideWarps, (max_parts + kWideParts - 1) / kWideParts));
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(B * Hq);
-  lc.blockDim = dim3(many ? kManyWarps * 32 : kD);
+  lc.blockDim = dim3(many ? wide_warps * 32 : kD);
   // The decode blocks leave their SMs at different times and the first
   // SMs to free up would take every combine block (16 a SM), sharing their
   // L2 bandwidth; 48 KB of (unused) shared memory a block caps it at 4 a
@@ -239,7 +248,7 @@ cudaError_t launch_combine_parts(const float* ws, int B, int Hkv, int Hq, int ma
   lc.attrs = attr;
   lc.numAttrs = 1;
   if (many)
-    return cudaLaunchKernelEx(&lc, combine_many_kernel, ws, Hkv, Hq, max_parts, unit_len, total,
+    return cudaLaunchKernelEx(&lc, combine_wide_kernel, ws, Hkv, Hq, max_parts, unit_len, total,
                               n_slots, out);
   return cudaLaunchKernelEx(&lc, combine_parts_kernel, ws, Hkv, Hq, max_parts, unit_len, total,
                             n_slots, out);
