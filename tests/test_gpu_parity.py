@@ -78,6 +78,19 @@ def test_combine_row_sizes(n_groups):
     assert_attention_close(cache.attention(q.cuda()), ref.attention(q), f"{n_groups} groups")
 
 
+@pytest.mark.parametrize("B,Hkv,n_rep,n_groups", [
+    (1, 2, 4, 150),     # 8 rows of ~300 partials: 16 warps a row
+    (3, 8, 4, 200),     # 96 rows of ~100 partials: 6 warps a row
+    (5, 8, 4, 80),      # 160 rows of ~60 partials: 4 warps a row
+])
+def test_combine_many_partials(B, Hkv, n_rep, n_groups):
+    """Rows of more than 32 partials (the many-partials combine) at row
+    counts below, around and above the SM count."""
+    w = small(B, Hkv, n_rep, 128 * n_groups, 77)
+    cache, ref, q = run_case(w)
+    assert_attention_close(cache.attention(q.cuda()), ref.attention(q), f"{B * w.Hq} rows")
+
+
 @pytest.mark.parametrize("kb,vb", [(2, 2), (4, 4)])
 def test_append_and_flush_bit_exact(kb, vb):
     # prefill 2 groups + 120 residual, then 8 appends fill the residual, one
