@@ -57,15 +57,15 @@ ATTN_REPS = 50                     # timed calls of each kind (kernel alone / wh
 # timed launches' mean algorithmic bytes (traffic per unit does not depend
 # on the batch, and the captured step's context is the workload's).
 # Llama-8B, captured at batch 8 (64 units, 32768 + 100 tokens, the token
-# append fused): 201.028 MB read + 3.841 MB written against 200.638 MB
+# append fused): 200.988 MB read + 3.793 MB written against 200.638 MB
 # (mostly the split-K partials written).  MixKVQ, captured at the bench size
-# (batch 8, 16384 + 100 tokens): 124.513 MB read + 3.128 MB written against
+# (batch 8, 16384 + 100 tokens): 124.507 MB read + 2.954 MB written against
 # 120.64 MB (the stored mixed key records are 7552 B against 7100 B of
 # algorithmic key bytes per group).
 NCU_TRAFFIC = {
-    "f9e1ae51858e4665": {
-        ("llama8b_gqa_32k_b16", 16, 32768, 2): 204.868608 / 200.638464,
-        ("mixkvq_qwen32b_16k_b8", 8, 16384, 2): 127.641088 / 120.64,
+    "65b84ef42b3a8a09": {
+        ("llama8b_gqa_32k_b16", 16, 32768, 2): 204.780544 / 200.638464,
+        ("mixkvq_qwen32b_16k_b8", 8, 16384, 2): 127.460864 / 120.64,
     },
 }
 
