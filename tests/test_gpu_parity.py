@@ -82,6 +82,8 @@ def test_combine_row_sizes(n_groups):
     (1, 2, 4, 150),     # 8 rows of ~300 partials: 16 warps a row
     (3, 8, 4, 200),     # 96 rows of ~100 partials: 6 warps a row
     (5, 8, 4, 80),      # 160 rows of ~60 partials: 4 warps a row
+    (1, 1, 4, 700),     # 4 rows of 702 partials: up to three chunks a warp
+    (1, 1, 4, 3000),    # one split position per resident warp: 2432 partials a row
 ])
 def test_combine_many_partials(B, Hkv, n_rep, n_groups):
     """Rows of more than 32 partials (the many-partials combine) at row
