@@ -807,6 +807,9 @@ __global__ void __launch_bounds__(256) quantize_pnmix_kernel(QuantArgs a) {
     const int ch = s_ch[p], mode = s_mode[p];
     const float off = s_off[p], sc = s_sc[p], rcp = s_rcp[p];
     const bool hi3 = p < L.nh;
+    const float half_ulp = sc * 0x1p-25f;
+    // unrolled by the swizzle period, so each element's tile offset is a constant
+#pragma unroll 8
     for (int t = t0; t < t0 + kKG / 2; ++t) {
       uint32_t c = 0;
       const float x = bf2f(sK[swz(t, ch)]);
@@ -817,7 +820,7 @@ __global__ void __launch_bounds__(256) quantize_pnmix_kernel(QuantArgs a) {
           if (is_near(v)) v = near_bits(v, d, sc, 7u);   // rare
           c = (v >> 18) & 7u;
         } else {
-          c = __fmaf_rn(-0.5f, sc, d) > sc * 0x1p-25f ? 1u : 0u;
+          c = __fmaf_rn(-0.5f, sc, d) > half_ulp ? 1u : 0u;
         }
       } else if (mode == 2) {   // rare: the IEEE quotient
         const float y = __fdiv_rn(__fsub_rn(x, off), sc);
