@@ -212,23 +212,34 @@ __device__ __forceinline__ GroupQ kivi_q(const KiviGroupP& p) {
   if (p.flags || p.step == 0.0f) return {0.0f, 0.0f};
   return {-p.m, p.step < 0x1p-100f ? -1.0f : __frcp_rn(p.step)};
 }
+// The rare path of kivi_bits: bf16(RN(diff / step)) with the step read
+// back from the record (bf16).  Out of line, as near_bits: an inline IEEE
+// division at each of a thread's unrolled elements overflows the
+// instruction cache.
+__device__ __noinline__ float kivi_exact(float diff, const uint16_t* step_bf16) {
+  return bfr(__fdiv_rn(diff, bf2f(*step_bf16)));
+}
 // The code of d32 = fl32(x - m) in code_bits' position.  diff = bf16(d32);
 // z = RN(diff * rcp) lies within 2.5 fp32 ulps of RN(diff / step), so both
 // round to the same bf16 value unless a bf16 rounding boundary (an fp32 value
 // whose low 16 bits are 0x8000) lies within 3 ulps of z; such elements (and
-// tiny-step groups) take the IEEE quotient, with the step read back from the
-// record (bf16).
+// tiny-step groups) take the IEEE quotient.  The code is clip(RNE(y), 0,
+// top): the clip first (the same result: RNE is monotonic and the bounds
+// are integers; a NaN y clips to 0 either way), then RNE by adding 1.5 *
+// 2^23, which rounds any value in [0, top] to the nearest integer, ties to
+// even, into the low bits.
 template <int BITS>
 __device__ __forceinline__ uint32_t kivi_bits(float d32, float rcp, const uint16_t* step_bf16) {
-  constexpr int top = (1 << BITS) - 1;
+  constexpr float top = static_cast<float>((1 << BITS) - 1);
   const float diff = bfr(d32);
   const float z = __fmul_rn(diff, rcp);
   float y;
   if ((__float_as_uint(z) & 0xFFFFu) - 0x7FFDu <= 6u || rcp < 0.0f)   // rare
-    y = bfr(__fdiv_rn(diff, bf2f(*step_bf16)));
+    y = kivi_exact(diff, step_bf16);
   else
     y = bfr(z);
-  return static_cast<uint32_t>(fminf(fmaxf(rintf(y), 0.0f), static_cast<float>(top))) << 18;
+  const float c = __fadd_rn(fminf(fmaxf(y, 0.0f), top), 12582912.0f);   // 1.5 * 2^23
+  return (__float_as_uint(c) & 15u) << 18;
 }
 
 
