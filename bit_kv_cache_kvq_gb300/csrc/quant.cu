@@ -744,6 +744,14 @@ __global__ void __launch_bounds__(256, 5) quantize_kivi_kernel(QuantArgs a) {
 // the others by Eq. 7 (s = (M - m)/2, z = (3m + M)/4, code RNE((x - z)/s)
 // clipped to 0..1), every operation fp32 rounded; codes staged as bytes,
 // then the LSB plane and the upper plane packed word by word.
+// The code of a position whose scale is below 2^-100 (or whose offset
+// overflowed): clip(RNE(RN((x - off) / sc)), 0, top) by the IEEE quotient.
+// Out of line, as near_bits: rare, and the code loop is unrolled.
+__device__ __noinline__ uint32_t pnmix_exact_code(float x, float off, float sc, float top) {
+  const float y = __fdiv_rn(__fsub_rn(x, off), sc);
+  return static_cast<uint32_t>(fminf(fmaxf(rintf(y), 0.0f), top));
+}
+
 template <int VB>
 __global__ void __launch_bounds__(256) quantize_pnmix_kernel(QuantArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -834,8 +842,7 @@ __global__ void __launch_bounds__(256) quantize_pnmix_kernel(QuantArgs a) {
           c = __fmaf_rn(-0.5f, sc, d) > half_ulp ? 1u : 0u;
         }
       } else if (mode == 2) {   // rare: the IEEE quotient
-        const float y = __fdiv_rn(__fsub_rn(x, off), sc);
-        c = static_cast<uint32_t>(fminf(fmaxf(rintf(y), 0.0f), hi3 ? 7.0f : 1.0f));
+        c = pnmix_exact_code(x, off, sc, hi3 ? 7.0f : 1.0f);
       }
       cB[t * kD + p] = static_cast<uint8_t>(c);
     }
