@@ -989,15 +989,27 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
       const int j = slot - nb;   // index among the quantized channels
       reinterpret_cast<float*>(rec + L.s4)[j] = p.step;
       reinterpret_cast<uint16_t*>(rec + L.m4)[j] = f2bf_bits(p.m);
-      if (bits == 4) {
-        for (int t = 0; t < kKG; ++t) {
-          const uint32_t c = code_exact(bf2f(sK[swz(t, d)]), p.m, p.step, top);
-          cKv[t * kvs + j] = static_cast<uint8_t>(c & 3u);
-          cKv[t * kvs + n4 + j] = static_cast<uint8_t>(c >> 2);
+      // codes by the uniform quantizer's decision (code_bits, near_bits for
+      // the elements near a rounding boundary): RNE(RN(d / step)) bit for
+      // bit; flagged channels and steps below 2^-100 by the IEEE quotient
+      const bool fast = p.flags == 0u && !(p.step > 0.0f && p.step < kTinyStep);
+      const float r = p.step > 0.0f ? __frcp_rn(p.step) : 0.0f;
+      const int lo_at = bits == 4 ? j : n4 + j, hi_at = n4 + j;
+      // unrolled by the tile's swizzle period, so each element's offset is a constant
+#pragma unroll 8
+      for (int t = 0; t < kKG; ++t) {
+        const float x = bf2f(sK[swz(t, d)]);
+        uint32_t c;
+        if (fast) {
+          const float dd = __fsub_rn(x, p.m);
+          uint32_t v = code_bits(dd, r);
+          if (is_near(v)) v = near_bits(v, dd, p.step, top);   // rare
+          c = (v >> 18) & static_cast<uint32_t>(top);
+        } else {
+          c = code_exact(x, p.m, p.step, top);
         }
-      } else {
-        for (int t = 0; t < kKG; ++t)
-          cKv[t * kvs + n4 + j] = static_cast<uint8_t>(code_exact(bf2f(sK[swz(t, d)]), p.m, p.step, top));
+        cKv[t * kvs + lo_at] = static_cast<uint8_t>(bits == 4 ? (c & 3u) : c);
+        if (bits == 4) cKv[t * kvs + hi_at] = static_cast<uint8_t>(c >> 2);
       }
     }
   }
