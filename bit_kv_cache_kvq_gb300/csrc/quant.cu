@@ -99,6 +99,12 @@ __device__ __forceinline__ uint32_t code_exact(float x, float m, float step, int
   return static_cast<uint32_t>(fminf(fmaxf(rintf(q), 0.0f), static_cast<float>(top)));
 }
 
+// code_exact out of line, for loops whose fast path is inlined many times
+// and whose exact path is rare (flagged or tiny-step groups)
+__device__ __noinline__ uint32_t code_exact_rare(float x, float m, float step, int top) {
+  return code_exact(x, m, step, top);
+}
+
 // ---- bf16x2 helpers
 // Elementwise min / max of two bf16 pairs; a NaN in either operand gives NaN.
 __device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
@@ -921,6 +927,10 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
   uint8_t* sTier = smem + kTileBytes + kRedBytes + 512;                             // 128 B
   float* sA = reinterpret_cast<float*>(smem + kTileBytes + kRedBytes + 512 + 128);  // 512 B
   uint8_t* cKv = smem + kTileBytes + kParamBytes;
+  // per channel, for the code pass: origin, step, RN(1/step), code slots, fast path
+  __shared__ float s_mx[kD], s_st[kD], s_rc[kD];
+  __shared__ int16_t s_at[kD], s_at4[kD];
+  __shared__ bool s_fast[kD];
   load_tile(a, a.src.k, sK);
   // virtual channels past this group's count stay zero
   for (int i = threadIdx.x; i < kKG * kvs / 4; i += blockDim.x)
@@ -989,24 +999,41 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
       const int j = slot - nb;   // index among the quantized channels
       reinterpret_cast<float*>(rec + L.s4)[j] = p.step;
       reinterpret_cast<uint16_t*>(rec + L.m4)[j] = f2bf_bits(p.m);
-      // codes by the uniform quantizer's decision (code_bits, near_bits for
-      // the elements near a rounding boundary): RNE(RN(d / step)) bit for
-      // bit; flagged channels and steps below 2^-100 by the IEEE quotient
-      const bool fast = p.flags == 0u && !(p.step > 0.0f && p.step < kTinyStep);
-      const float r = p.step > 0.0f ? __frcp_rn(p.step) : 0.0f;
-      const int lo_at = bits == 4 ? j : n4 + j, hi_at = n4 + j;
+      // codes below, two threads a channel
+      s_mx[d] = p.m;
+      s_st[d] = p.step;
+      s_rc[d] = p.step > 0.0f ? __frcp_rn(p.step) : 0.0f;
+      s_at[d] = static_cast<int16_t>(bits == 4 ? j : n4 + j);
+      s_at4[d] = static_cast<int16_t>(n4 + j);
+      // flagged channels and steps below 2^-100 take the IEEE quotient
+      s_fast[d] = p.flags == 0u && !(p.step > 0.0f && p.step < kTinyStep);
+    }
+  }
+  __syncthreads();
+  // UINT4 / UINT2 codes, two threads a channel (64 tokens each), by the
+  // uniform quantizer's decision (code_bits, near_bits for the elements near
+  // a rounding boundary): RNE(RN(d / step)) bit for bit
+  {
+    const int d = threadIdx.x & (kD - 1), t0 = (threadIdx.x >> 7) * (kKG / 2);
+    const int tier = sTier[d];
+    if (tier != KVQ_TIER_BF16) {
+      const int bits = tier == KVQ_TIER_UINT4 ? 4 : 2;
+      const int top = (1 << bits) - 1;
+      const float m = s_mx[d], step = s_st[d], r = s_rc[d];
+      const int lo_at = s_at[d], hi_at = s_at4[d];
+      const bool fast = s_fast[d];
       // unrolled by the tile's swizzle period, so each element's offset is a constant
 #pragma unroll 8
-      for (int t = 0; t < kKG; ++t) {
+      for (int t = t0; t < t0 + kKG / 2; ++t) {
         const float x = bf2f(sK[swz(t, d)]);
         uint32_t c;
         if (fast) {
-          const float dd = __fsub_rn(x, p.m);
+          const float dd = __fsub_rn(x, m);
           uint32_t v = code_bits(dd, r);
-          if (is_near(v)) v = near_bits(v, dd, p.step, top);   // rare
+          if (is_near(v)) v = near_bits(v, dd, step, top);   // rare
           c = (v >> 18) & static_cast<uint32_t>(top);
         } else {
-          c = code_exact(x, p.m, p.step, top);
+          c = code_exact_rare(x, m, step, top);
         }
         cKv[t * kvs + lo_at] = static_cast<uint8_t>(bits == 4 ? (c & 3u) : c);
         if (bits == 4) cKv[t * kvs + hi_at] = static_cast<uint8_t>(c >> 2);
