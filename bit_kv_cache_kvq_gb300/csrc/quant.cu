@@ -931,6 +931,10 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
   __shared__ float s_mx[kD], s_st[kD], s_rc[kD];
   __shared__ int16_t s_at[kD], s_at4[kD];
   __shared__ bool s_fast[kD];
+  // ranking: second halves' counts, per-warp tier ballots, BF16 slot -> channel
+  __shared__ int s_rk[kD];
+  __shared__ uint32_t s_tm[3][kD / 32];
+  __shared__ uint8_t s_bf[kD];
   load_tile(a, a.src.k, sK);
   // virtual channels past this group's count stay zero
   for (int i = threadIdx.x; i < kKG * kvs / 4; i += blockDim.x)
@@ -943,8 +947,14 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
   float lo, hi;
   bool bad;
   key_ranges(sK, sRed, lo, hi, bad);
-  if (threadIdx.x < kD) {
-    const int d = threadIdx.x;
+  // per channel (threads below 128): importance, saliency A = I * S, and a
+  // total-order rank key (NaN, only possible on a flagged group, sorts last,
+  // so ranks are always a permutation and every slot stays inside its
+  // tier's region)
+  const int d = threadIdx.x & (kD - 1);
+  const bool chan = threadIdx.x < kD;
+  float A = 0.0f;
+  if (chan) {
     float S = 0.0f;
     if (!bad) S = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
     const long long ud = static_cast<long long>(u) * kD + d;
@@ -952,45 +962,62 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
     if (!isfinite(I)) flags |= KVQ_FLAG_NONFINITE;
     if (bad) flags |= KVQ_FLAG_NONFINITE;
     else if (!isfinite(S)) flags |= KVQ_FLAG_RANGE;
-    const float A = __fmul_rn(I, S);
-    // Rank by a total-order key (NaN, only possible on a flagged group,
-    // sorts last) so ranks are always a permutation and every slot stays
-    // inside its tier's region.
-    const uint32_t key = isnan(A) ? 0u : fkey(A);
-    sKey[d] = key;
-    sA[d] = A;
-    asm volatile("bar.sync 1, 128;");
-    // rank, and how many channels pass each threshold (NaN passes none)
-    int rank = 0, above_b = 0, above_4 = 0;
-    for (int e = 0; e < kD; ++e) {
+    A = __fmul_rn(I, S);
+    sKey[d] = isnan(A) ? 0u : fkey(A);
+  }
+  // how many channels pass each threshold (NaN passes none); each count is
+  // also a barrier, the first one after the keys
+  const int above_b = __syncthreads_count(chan && A > a.tau_bf16);
+  const int above_4 = __syncthreads_count(chan && A > a.tau_uint4);
+  int nb = L.nb, n4 = L.n4;
+  if (L.thresh) {
+    nb = min(above_b, L.nb);
+    n4 = max(0, min(above_4 - nb, L.n4));
+  }
+  // rank: the keys above this channel's, or equal at a lower channel; two
+  // threads a channel, half of the keys each
+  int rank = 0;
+  {
+    const uint32_t key = sKey[d];
+    const int e0 = (threadIdx.x >> 7) * (kD / 2);
+    int part = 0;
+#pragma unroll 8
+    for (int e = e0; e < e0 + kD / 2; ++e) {
       const uint32_t ke = sKey[e];
-      rank += (ke > key || (ke == key && e < d)) ? 1 : 0;
-      if (L.thresh) {
-        const float Ae = sA[e];
-        above_b += Ae > a.tau_bf16 ? 1 : 0;
-        above_4 += Ae > a.tau_uint4 ? 1 : 0;
-      }
+      part += (ke > key || (ke == key && e < d)) ? 1 : 0;
     }
-    int nb = L.nb, n4 = L.n4;
-    if (L.thresh) {
-      nb = min(above_b, L.nb);
-      n4 = max(0, min(above_4 - nb, L.n4));
-    }
-    const int tier = rank < nb ? KVQ_TIER_BF16
-                     : rank < nb + n4 ? KVQ_TIER_UINT4
-                                      : KVQ_TIER_UINT2;
+    if (!chan) s_rk[d] = part;
+    __syncthreads();
+    if (chan) rank = part + s_rk[d];
+  }
+  // tiers; a channel's slot in its tier is the number of lower channels of
+  // that tier (per-warp ballots)
+  int tier = KVQ_TIER_UINT2;
+  if (chan) {
+    tier = rank < nb ? KVQ_TIER_BF16 : rank < nb + n4 ? KVQ_TIER_UINT4 : KVQ_TIER_UINT2;
     sTier[d] = static_cast<uint8_t>(tier);
     if (d == 0) {
       rec[L.hdr] = static_cast<uint8_t>(nb);
       rec[L.hdr + 1] = static_cast<uint8_t>(n4);
     }
-    asm volatile("bar.sync 1, 128;");
-    int slot = tier == KVQ_TIER_BF16 ? 0 : tier == KVQ_TIER_UINT4 ? nb : nb + n4;
-    for (int e = 0; e < d; ++e) slot += (sTier[e] == tier) ? 1 : 0;
+    const unsigned mb = __ballot_sync(0xffffffffu, tier == KVQ_TIER_BF16);
+    const unsigned m4 = __ballot_sync(0xffffffffu, tier == KVQ_TIER_UINT4);
+    const unsigned m2 = __ballot_sync(0xffffffffu, tier == KVQ_TIER_UINT2);
+    if ((d & 31) == 0) {
+      s_tm[0][d >> 5] = mb;
+      s_tm[1][d >> 5] = m4;
+      s_tm[2][d >> 5] = m2;
+    }
+  }
+  __syncthreads();
+  if (chan) {
+    const int ti = tier == KVQ_TIER_BF16 ? 0 : tier == KVQ_TIER_UINT4 ? 1 : 2;
+    int slot = ti == 0 ? 0 : ti == 1 ? nb : nb + n4;
+    for (int w = 0; w < (d >> 5); ++w) slot += __popc(s_tm[ti][w]);
+    slot += __popc(s_tm[ti][d >> 5] & ((1u << (d & 31)) - 1u));
     rec[L.perm + slot] = static_cast<uint8_t>(d);
     if (tier == KVQ_TIER_BF16) {
-      uint16_t* raw = reinterpret_cast<uint16_t*>(rec + L.raw) + slot * kKG;
-      for (int t = 0; t < kKG; ++t) raw[(((t >> 3) ^ (slot & 7)) << 3) | (t & 7)] = sK[swz(t, d)];
+      s_bf[slot] = static_cast<uint8_t>(d);
     } else {
       const int bits = tier == KVQ_TIER_UINT4 ? 4 : 2;
       const int top = (1 << bits) - 1;
@@ -1010,6 +1037,15 @@ __global__ void __launch_bounds__(256) quantize_mixed_kernel(QuantArgs a) {
     }
   }
   __syncthreads();
+  // the BF16 tier's raw keys, all threads: slot s holds channel s_bf[s]'s
+  // 128 tokens, 16-byte pieces rotated by the slot
+  {
+    uint16_t* raw = reinterpret_cast<uint16_t*>(rec + L.raw);
+    for (int i = threadIdx.x; i < nb * kKG; i += blockDim.x) {
+      const int slot = i >> 7, t = i & (kKG - 1);
+      raw[slot * kKG + ((((t >> 3) ^ (slot & 7)) << 3) | (t & 7))] = sK[swz(t, s_bf[slot])];
+    }
+  }
   // UINT4 / UINT2 codes, two threads a channel (64 tokens each), by the
   // uniform quantizer's decision (code_bits, near_bits for the elements near
   // a rounding boundary): RNE(RN(d / step)) bit for bit
