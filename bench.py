@@ -471,6 +471,10 @@ def run_ours(args, rank, world):
     clk = ClockSampler()
     clk.start()
     time.sleep(0.02)
+    # a ~0.5 ms busy kernel before the first event, so the host has queued
+    # the first steps when the timed region starts (the device never waits
+    # on the host's first submissions inside it)
+    torch.cuda._sleep(1_000_000)
     t_start.record(stream)
     launches = 0
     total_bytes = 0
