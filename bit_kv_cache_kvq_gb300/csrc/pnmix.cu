@@ -50,8 +50,11 @@ __device__ __forceinline__ bool pair_wait(uint32_t mb, uint32_t parity, int poll
 // sqrt(a^2 + b^2), every operation fp32 rounded (the root correctly rounded)
 __device__ __forceinline__ float pair_norm(uint16_t xa, uint16_t xb, bool& bad) {
   const float x = bfv(xa), y = bfv(xb);
-  if (!isfinite(x) || !isfinite(y)) bad = true;
-  return sqrt_rn(__fadd_rn(__fmul_rn(x, x), __fmul_rn(y, y)));
+  const float s = __fadd_rn(__fmul_rn(x, x), __fmul_rn(y, y));
+  // a non-finite input leaves s infinite or NaN; only then (or when finite
+  // inputs overflow) are the inputs themselves tested
+  if (!(s <= 3.40282346638528860e38f) && (!isfinite(x) || !isfinite(y))) bad = true;
+  return sqrt_rn(s);
 }
 
 __global__ void __launch_bounds__(kPairThreads) pnmix_pairs_kernel(
