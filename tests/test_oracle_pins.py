@@ -185,10 +185,11 @@ def test_error_bound_half_step(bits):
             assert np.all(np.abs(x.astype(np.float64) - rec) <= float(s) * (g["bound_fraction_of_step"] + slack))
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 def test_codes_brute_force_nearest(bits):
     """Every code is a nearest grid point of the exact (x - m)/step; exact
-    ties (representable without rounding) go to the even code."""
+    ties (representable without rounding) go to the even code.  Three bits
+    are PN-Mix's high channels (Eq. 2)."""
     rng = np.random.default_rng(100 + bits)
     top = 2**bits - 1
     for trial in range(300):
@@ -763,6 +764,31 @@ def test_pnmix_eq7_one_bit_groups_rebuild_at_quarter_points():
         rec = np.float64(z) + np.float64(s) * c
         quarter = (float(x.max()) - float(x.min())) / 4
         assert np.max(np.abs(rec - x)) <= quarter * (1 + 2 ** -20)
+
+
+def test_pnmix_eq7_codes_brute_force_nearest():
+    """Eq. 7 by brute force: each 1-bit code selects the nearer of its
+    group's two reconstruction points z and z + s (exact rationals), the
+    lower one at an exact tie."""
+    rng = np.random.default_rng(77)
+    for trial in range(300):
+        n = int(rng.integers(2, 9))
+        x = (rng.integers(-40, 40, n) / rng.choice([1, 2, 4, 8])).astype(np.float32)
+        if trial % 3 == 0:
+            x = rng.standard_normal(n).astype(np.float32)
+        if x.max() == x.min():
+            continue
+        c, z, s = orc.quantize_group_1bit_mid(x)
+        Z, S = Fraction(float(z)), Fraction(float(s))
+        for xi, ci in zip(x, c):
+            X = Fraction(float(xi))
+            d = [abs(X - Z), abs(X - Z - S)]
+            if d[0] == d[1]:
+                assert ci == 0
+            else:
+                # fp32 (x - z) / s rounds twice: a code may differ only at a
+                # near tie
+                assert d[int(ci)] <= min(d) + S * Fraction(1, 2**20)
 
 
 def test_pnmix_eq6_pair_scores_by_hand():
