@@ -6,7 +6,10 @@
 //   step = fl32(fl32(M - m) / (2^b - 1)),  c = clip(RNE(fl32(fl32(x - m) / step)))
 // with IEEE fp32 subtraction and division (__fsub_rn / __fdiv_rn), codes
 // rounded half-to-even, and a constant group (M == m) stored as step 0,
-// codes 0, origin m.  Groups: Key per channel over the 128 tokens of a tile,
+// codes 0, origin m.  Every pass reaches these codes bit for bit without a
+// division per element (code_bits and near_bits below; KIVI's bf16 rule in
+// kivi_bits); only flagged groups and steps below 2^-100 divide, out of
+// line.  Groups: Key per channel over the 128 tokens of a tile,
 // Value per token over 32 consecutive channels (KIVI §3).  The uniform and
 // KIVI-prefill passes build whole words of the tensor-core fragment order
 // of frag_layout.h in registers; the mixed and PN-Mix passes stage codes as
